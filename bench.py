@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized mul_mat hot path on GB300.
+
+Headline (one JSON line on stdout): decode GB/s of the Q4_K x Q8_K GEMV,
+M = 1, N = K = 4096. One step = the whole decode path for one token batch:
+quantize the fp32 activations to Q8_K (kernel 1) and run the GEMV over the
+packed Q4_K weights (kernel 2). Inputs are resident in HBM; 32 copies of the
+packed weights are used in rotation (302 MB, above the 129 MB L2), so every
+step streams its weights from HBM. Steps are replayed as CUDA graphs of 64
+steps so that the host's launch rate does not set the pace.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Under torchrun each rank runs the same workload on its own GPU (replicas,
+weak scaling; the path has no exchange step, so there is no data-path
+collective); value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "quantized mul_mat GB/s (M=1) and TOPS (M=512) vs GB300 roofline"
+GRAPH_STEPS = 64
+COPIES = 32
+WORKLOAD = ("Q4_K x Q8_K GEMV decode, M=1, N=K=4096 (16 super-blocks of 256 per row, 6-bit "
+            "scale/min in 12 bytes, fp16 d/dmin); W ~ N(0,0.02) + per-row offset N(0,0.005); "
+            "X ~ N(0,1); seed 0")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ environment
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.uuid = None
+        try:
+            u = torch.cuda.get_device_properties(device).uuid
+            self.uuid = str(u)
+        except Exception:
+            pass
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            if self.uuid and self.uuid.replace("GPU-", "") not in f[0]:
+                continue
+            rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+GEMV_SOURCES = ["block_quantized_matmul_q4_gb300/csrc/gemv.cu",
+                "block_quantized_matmul_q4_gb300/csrc/qmm_internal.cuh"]
+
+
+def profiled_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(kernel_key)
+    if not rec or rec.get("source_digest") != source_digest(GEMV_SOURCES):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ GPU arm
+def step_bytes(q, N, K, M):
+    """Algorithmic bytes of one step: weight blocks + Q8_K activations +
+    fp32 outputs + the fp32 activations the quantizer reads."""
+    w = N * (K // 256) * 144
+    xq = M * (K // 256) * 292
+    return w, xq, M * N * 4, M * K * 4
+
+
+def capture(fn, n, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            fn(i)
+    return g
+
+
+def run_graphs(big, small, n_big):
+    for _ in range(n_big):
+        big.replay()
+    if small is not None:
+        small.replay()
+
+
+def timed(stream, fn):
+    """Run fn() between CUDA events on `stream`; returns seconds."""
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    with torch.cuda.stream(stream):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / 1e3
+
+
+def gpu_arm(args, rank, world):
+    import block_quantized_matmul_q4_gb300 as q
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L = wl.GEMV_Q4_K_4096
+    N, K, M = L.N, L.K, 1
+    wt = q.QMM_TYPE_Q4_K
+
+    # inputs resident in HBM
+    w = wl.weights(0, N, K, L.wstd, row_offset_std=L.row_offset_std, device=dev)
+    Wq = q.empty_blocks(wt, N, K)
+    q.qmm_quantize_weights(wt, w, Wq, N, K)
+    del w
+    Wp0 = q.empty_packed(wt, N, K)
+    q.qmm_repack_weights(wt, Wq, Wp0, N, K)
+    copies = [Wp0] + [Wp0.clone() for _ in range(COPIES - 1)]
+    X = wl.activations(0, M, K, device=dev)
+    ws_bytes = q.qmm_workspace_bytes(wt, M, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    Y = torch.empty(M, N, device=dev)
+    stream = torch.cuda.Stream()
+
+    def step(i):
+        q.qmm_mul_mat_ws(wt, copies[i % COPIES], N, K, X, M, Y, ws, ws_bytes, stream)
+
+    def gemv_only(i):
+        q.qmm_mul_mat_prepared(wt, copies[i % COPIES], N, K, ws, ws_bytes, M, Y, stream)
+
+    # warm-up outside capture (module load, function attributes), then graphs
+    for i in range(4):
+        step(i)
+    torch.cuda.synchronize()
+    n0 = q.qmm_kernel_launch_count()
+    g_big = capture(step, GRAPH_STEPS, stream)
+    launches_per_step = (q.qmm_kernel_launch_count() - n0) // GRAPH_STEPS
+    rem = args.steps % GRAPH_STEPS
+    g_small = capture(step, rem, stream) if rem else None
+    wrem = args.warmup % GRAPH_STEPS
+    g_wsmall = capture(step, wrem, stream) if wrem else None
+    g_gemv = capture(gemv_only, GRAPH_STEPS, stream)
+    torch.cuda.synchronize()
+
+    # warm-up steps (untimed)
+    with torch.cuda.stream(stream):
+        run_graphs(g_big, g_wsmall, args.warmup // GRAPH_STEPS)
+    torch.cuda.synchronize()
+
+    # timed region: exactly K steps
+    clocks = ClockSampler(dev.index)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t = timed(stream, lambda: run_graphs(g_big, g_small, args.steps // GRAPH_STEPS))
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    if world > 1:
+        tt = torch.tensor([t], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        t = float(tt.item())
+
+    bw, bxq, by, bx = step_bytes(q, N, K, M)
+    per_step = bw + bxq + by + bx
+    value = per_step * args.steps * world / t / 1e9
+
+    # dominant kernel alone: the GEMV, back to back over the rotating copies
+    reps = max(1, min(2000, args.steps // GRAPH_STEPS))
+    t_gemv = timed(stream, lambda: run_graphs(g_gemv, None, reps)) / (reps * GRAPH_STEPS)
+    gemv_bytes = bw + bxq + by
+    peaks = load_peaks()
+    achieved = gemv_bytes / t_gemv / 1e9
+    traffic = profiled_traffic("gemv_q4_K_4096_m1")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic, "kernel": "gemv_q4_K_kernel<1>",
+                "kernel_us": round(t_gemv * 1e6, 3), "algorithmic_bytes": gemv_bytes,
+                "peak_source": peaks["source"]}
+
+    # end to end through the public API: pinned host X -> device, qmm_mul_mat
+    # (the user call, which quantizes, allocates its workspace stream-ordered
+    # and runs the GEMV), result -> pinned host
+    e2e_steps = max(3, min(args.steps, 3000))
+    Xh = X.cpu().pin_memory()
+    Yh = torch.empty(M, N).pin_memory()
+    Xd = torch.empty_like(X)
+
+    def e2e_loop():
+        for i in range(e2e_steps):
+            Xd.copy_(Xh, non_blocking=True)
+            q.qmm_mul_mat(wt, copies[i % COPIES], N, K, Xd, M, Y, stream)
+            Yh.copy_(Y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            Xd.copy_(Xh, non_blocking=True)
+            q.qmm_mul_mat(wt, copies[i], N, K, Xd, M, Y, stream)
+    t_e2e = timed(stream, e2e_loop)
+    e2e = {"value": round(per_step * e2e_steps * world / t_e2e / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": Xh.numel() * 4, "d2h_bytes_per_step": Yh.numel() * 4,
+           "steps": e2e_steps, "path": "qmm_mul_mat, eager launches"}
+    q.qmm_check_device_error(stream)
+
+    extras = {}
+    if args.extras:
+        extras = gpu_extras(q, dev, stream, args)
+
+    return {
+        "value": round(value, 2), "ms_per_step": t / args.steps * 1e3, "roofline": roofline,
+        "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+        "extras": extras,
+    }
+
+
+def gemv_rate(q, dev, stream, wt, N, K, M, seed, L=None, steps=6400, copies=None, hot=0.0):
+    """GB/s of qmm_mul_mat_ws (quantizer + GEMV) on one projection; weights
+    rotate over enough copies to exceed L2."""
+    if L is None:
+        w = wl.weights(seed, N, K, 0.02, row_offset_std=0.005, device=dev)
+    else:
+        w = wl.weights(seed, N, K, L.wstd, row_offset_std=L.row_offset_std,
+                       outlier_frac=L.outlier_frac, device=dev)
+    Wq = q.empty_blocks(wt, N, K)
+    q.qmm_quantize_weights(wt, w, Wq, N, K)
+    del w
+    Wp = q.empty_packed(wt, N, K)
+    q.qmm_repack_weights(wt, Wq, Wp, N, K)
+    del Wq
+    nbytes = Wp.numel()
+    ncopies = copies or max(1, min(32, -(-300_000_000 // nbytes)))
+    cps = [Wp] + [Wp.clone() for _ in range(ncopies - 1)]
+    X = wl.activations(seed, M, K, hot_frac=hot, device=dev)
+    ws_bytes = q.qmm_workspace_bytes(wt, M, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    Y = torch.empty(M, N, device=dev)
+
+    def step(i):
+        q.qmm_mul_mat_ws(wt, cps[i % ncopies], N, K, X, M, Y, ws, ws_bytes, stream)
+
+    for i in range(3):
+        step(i)
+    g = capture(step, GRAPH_STEPS, stream)
+    reps = max(3, steps // GRAPH_STEPS)
+    with torch.cuda.stream(stream):
+        g.replay()
+    t = timed(stream, lambda: run_graphs(g, None, reps)) / (reps * GRAPH_STEPS)
+    qk = 256 if wt == q.QMM_TYPE_Q4_K else 32
+    bq = 292 if wt == q.QMM_TYPE_Q4_K else 34
+    b = nbytes * N // (-(-N // 8) * 8) + M * (K // qk) * bq + M * N * 4 + M * K * 4
+    del cps, Wp
+    return t, b
+
+
+def gpu_extras(q, dev, stream, args):
+    out = {}
+    # M sweep of the headline GEMV
+    sweep = {}
+    L = wl.GEMV_Q4_K_4096
+    for M in wl.GEMV_Q4_K_M_SWEEP:
+        t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q4_K, L.N, L.K, M, 0, L)
+        sweep[str(M)] = {"us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
+                         "TOPS": round(2 * M * L.N * L.K / t / 1e12, 3)}
+    out["q4_K_4096_M_sweep"] = sweep
+    # Q4_0 x Q8_0 GEMV, 256 x 1024, M = 1 (L2-resident correctness case)
+    Ls = wl.GEMV_Q4_0_SMALL
+    t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q4_0, Ls.N, Ls.K, 1, 0, Ls, copies=1)
+    out["q4_0_256x1024_m1"] = {"us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
+                               "note": "147 KB of weights stay in L2; latency-bound"}
+    # 70B-shaped decode layer: the 7 projections back to back
+    tot_t, tot_b = 0.0, 0
+    per = {}
+    for i, Lp in enumerate(wl.LAYER_70B):
+        t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q4_K, Lp.N, Lp.K, 1, 100 + i, Lp,
+                         steps=640, hot=wl.LAYER_70B_HOT_FRAC)
+        per[Lp.name] = {"us": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1)}
+        tot_t += t
+        tot_b += b
+        torch.cuda.empty_cache()
+    out["layer_70B_q4_K_m1"] = {"us": round(tot_t * 1e6, 2), "GB/s": round(tot_b / tot_t / 1e9, 1),
+                                "bytes": tot_b, "per_projection": per}
+    return out
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+def cpu_arm(target_s: float, steps: int | None = None, warmup: int = 0):
+    """The oracle, as it stands, on the host cores: quantize the activations
+    and run the fp32 vec_dot mul_mat over a sample of the weight rows."""
+    import oracle
+    L = wl.GEMV_Q4_K_4096
+    N, K, M = L.N, L.K, 1
+    nthreads = oracle.default_threads()
+    rows_all = 512
+    w = wl.weights(0, N, K, L.wstd, row_offset_std=L.row_offset_std,
+                   rows=range(rows_all)).numpy()
+    Wc = oracle.quantize(oracle.Q4_K, w, nthreads)
+    x = wl.activations(0, M, K).numpy()
+    row_b = (K // 256) * 144
+
+    def one(nrows):
+        oracle.mul_mat(oracle.Q4_K, Wc[:nrows], nrows, K, x, nthreads=nthreads, want=("y32",))
+
+    one(rows_all)  # warm the thread pool
+    t0 = time.perf_counter()
+    one(rows_all)
+    t_row = max((time.perf_counter() - t0) / rows_all, 1e-9)
+    if steps is None:  # baseline leg: about target_s seconds of work
+        nrows = rows_all
+        reps = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < target_s:
+            one(nrows)
+            reps += 1
+    else:              # reference arm: K steps fit the time budget
+        nrows = int(min(rows_all, max(8, target_s / max(steps, 1) / t_row)))
+        reps = steps
+        for _ in range(warmup):
+            one(nrows)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            one(nrows)
+    t = time.perf_counter() - t0
+    b = nrows * row_b + (K // 256) * 292 + nrows * 4 + K * 4
+    return {"value": round(b * reps / t / 1e9, 4), "unit": "GB/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{nrows} of {N} weight rows per call (M=1, K={K}), {reps} calls, "
+                      f"{t:.1f} s; activation quantization included"}, t / reps
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", dest="extras", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    config = {"workload": WORKLOAD, "M": 1, "N": 4096, "K": 4096,
+              "l2": f"{COPIES} rotating copies of the packed weights (302 MB > 129 MB L2)",
+              "timing": f"CUDA events around CUDA-graph replays of {GRAPH_STEPS} steps"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        budget = 120.0
+        res, per = cpu_arm(budget, steps=args.steps, warmup=args.warmup)
+        line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "int8", "data": "synthetic", "config": config,
+                "cpu_baseline": res,
+                "e2e": {"value": res["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    res = gpu_arm(args, rank, world)
+    if rank == 0:
+        cpu, _ = cpu_arm(args.cpu_seconds)
+        line = {"metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "int8", "data": "synthetic", "config": config,
+                "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
+                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
+                "extras": res["extras"]}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

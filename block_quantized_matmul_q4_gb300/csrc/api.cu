@@ -1,0 +1,356 @@
+// api.cu -- the extern "C" entry points declared in include/qmm.h: argument
+// validation, workspace handling, dispatch to the kernel launchers, status
+// and error reporting.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "qmm_internal.cuh"
+
+namespace qmm {
+
+// Device error word: bit kDevErrTimeout is set by a kernel that gave up a
+// bounded wait. Read and cleared by qmm_check_device_error.
+__device__ unsigned g_device_error = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned *g_err_ptr[kMaxDevices] = {nullptr};
+int g_sms[kMaxDevices] = {0};
+bool g_pool_ready[kMaxDevices] = {false};
+std::set<std::pair<const void *, int>> g_smem_ok;
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_msg[512] = "";
+
+int current_device() {
+    int d = 0;
+    cudaGetDevice(&d);
+    return d < 0 ? 0 : (d >= kMaxDevices ? kMaxDevices - 1 : d);
+}
+}  // namespace
+
+unsigned *device_error_word() {
+    const int d = current_device();
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (!g_err_ptr[d]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) g_err_ptr[d] = (unsigned *)p;
+    }
+    return g_err_ptr[d];
+}
+
+int sm_count() {
+    const int d = current_device();
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (!g_sms[d]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+        g_sms[d] = n > 0 ? n : 1;
+    }
+    return g_sms[d];
+}
+
+cudaError_t ensure_smem_attr(const void *kernel, int bytes) {
+    const int d = current_device();
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (g_smem_ok.count({kernel, d})) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) g_smem_ok.insert({kernel, d});
+    return e;
+}
+
+void count_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+qmm_status set_error(qmm_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+namespace {
+
+bool is_weight(qmm_type t) { return t == QMM_TYPE_Q4_0 || t == QMM_TYPE_Q4_K; }
+bool is_act(qmm_type t) { return t == QMM_TYPE_Q8_0 || t == QMM_TYPE_Q8_K; }
+int elems(qmm_type t) { return (t == QMM_TYPE_Q4_0 || t == QMM_TYPE_Q8_0) ? QK4_0 : QK_K; }
+qmm_type act_of(qmm_type wt) { return wt == QMM_TYPE_Q4_0 ? QMM_TYPE_Q8_0 : QMM_TYPE_Q8_K; }
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+qmm_status ok() {
+    g_msg[0] = 0;
+    return QMM_OK;
+}
+
+qmm_status cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return ok();
+    return set_error(QMM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define QMM_CHECK_ARG(cond, ...)                            \
+    do {                                                    \
+        if (!(cond)) return set_error(QMM_ERR_ARG, __VA_ARGS__); \
+    } while (0)
+
+qmm_status check_weight_args(qmm_type wt, int64_t N, int64_t K) {
+    QMM_CHECK_ARG(is_weight(wt), "weight type must be Q4_0 or Q4_K (got %d)", (int)wt);
+    QMM_CHECK_ARG(N >= 0 && K > 0, "sizes must satisfy N >= 0, K > 0 (N=%lld K=%lld)",
+                  (long long)N, (long long)K);
+    QMM_CHECK_ARG(K % elems(wt) == 0, "K=%lld is not a multiple of the block size %d",
+                  (long long)K, elems(wt));
+    QMM_CHECK_ARG(K <= (int64_t)1 << 30 && N <= (int64_t)1 << 31, "sizes too large");
+    return QMM_OK;
+}
+
+// Default mem pool: keep freed workspace instead of returning it to the
+// driver at every synchronization.
+void prepare_pool() {
+    const int d = current_device();
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (g_pool_ready[d]) return;
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, d) == cudaSuccess) {
+        uint64_t thr = UINT64_MAX;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    }
+    g_pool_ready[d] = true;
+}
+
+qmm_status carve(qmm_type wt, int64_t M, int64_t K, const void *ws, size_t ws_bytes, Planar *p) {
+    const size_t need = planar_bytes(M, K, elems(wt), p, (uint8_t *)ws);
+    if (ws_bytes < need)
+        return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+    return QMM_OK;
+}
+
+qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K, void *ws,
+                              size_t ws_bytes, cudaStream_t s) {
+    Planar p;
+    qmm_status st = carve(wt, M, K, ws, ws_bytes, &p);
+    if (st != QMM_OK) return st;
+    return cuda_status(launch_quantize_q8(act_of(wt), true, X, nullptr, p, M, K, s),
+                       "activation quantizer launch");
+}
+
+qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, const void *ws,
+                         size_t ws_bytes, int64_t M, float *Y, cudaStream_t s) {
+    Planar p;
+    qmm_status st = carve(wt, M, K, ws, ws_bytes, &p);
+    if (st != QMM_OK) return st;
+    return cuda_status(launch_gemv(wt, Wp, N, K, p, M, Y, /*pdl=*/true, s),
+                       "mul_mat kernel launch");
+}
+
+qmm_status mul_mat_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, const float *X,
+                        int64_t M, float *Y, void *ws, size_t ws_bytes, cudaStream_t s) {
+    qmm_status st = quantize_acts_impl(wt, X, M, K, ws, ws_bytes, s);
+    if (st != QMM_OK) return st;
+    return prepared_impl(wt, Wp, N, K, ws, ws_bytes, M, Y, s);
+}
+
+qmm_status check_mul_mat_args(qmm_type wt, const void *Wp, int64_t N, int64_t K, const float *X,
+                              int64_t M, float *Y) {
+    qmm_status st = check_weight_args(wt, N, K);
+    if (st != QMM_OK) return st;
+    QMM_CHECK_ARG(M >= 0, "M must be >= 0 (got %lld)", (long long)M);
+    if (M == 0 || N == 0) return QMM_OK;
+    QMM_CHECK_ARG(Wp && X && Y, "null pointer argument");
+    QMM_CHECK_ARG(aligned(Wp, 16) && aligned(X, 16) && aligned(Y, 4),
+                  "W_packed and X must be 16-byte aligned, Y 4-byte aligned");
+    return QMM_OK;
+}
+
+}  // namespace
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+size_t qmm_block_bytes(qmm_type t) {
+    switch (t) {
+    case QMM_TYPE_Q4_0: return B_Q4_0;
+    case QMM_TYPE_Q4_K: return B_Q4_K;
+    case QMM_TYPE_Q8_0: return B_Q8_0;
+    case QMM_TYPE_Q8_K: return B_Q8_K;
+    default: return 0;
+    }
+}
+
+int qmm_block_elems(qmm_type t) {
+    return (is_weight(t) || is_act(t)) ? elems(t) : 0;
+}
+
+size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K) {
+    if (!is_weight(wt) || N <= 0 || K <= 0 || K % elems(wt)) return 0;
+    return (size_t)tiles_of(N) * kTileRows * (size_t)(K / elems(wt)) * qmm_block_bytes(wt);
+}
+
+size_t qmm_workspace_bytes(qmm_type wt, int64_t M, int64_t K) {
+    if (!is_weight(wt) || M < 0 || K <= 0 || K % elems(wt)) return 0;
+    return planar_bytes(M, K, elems(wt), nullptr, nullptr);
+}
+
+qmm_status qmm_quantize_row_q8(qmm_type vt, const float *X, void *Xq, int64_t M, int64_t K,
+                               qmm_stream_t stream) {
+    QMM_CHECK_ARG(is_act(vt), "activation type must be Q8_0 or Q8_K (got %d)", (int)vt);
+    QMM_CHECK_ARG(M >= 0 && K > 0 && K % elems(vt) == 0,
+                  "need M >= 0, K > 0, K %% %d == 0 (M=%lld K=%lld)", elems(vt), (long long)M,
+                  (long long)K);
+    if (M == 0) return ok();
+    QMM_CHECK_ARG(X && Xq, "null pointer argument");
+    QMM_CHECK_ARG(aligned(X, 16), "X must be 16-byte aligned");
+    QMM_CHECK_ARG(aligned(Xq, vt == QMM_TYPE_Q8_K ? 4 : 2), "Xq misaligned");
+    Planar none{nullptr, nullptr, nullptr};
+    return cuda_status(launch_quantize_q8(vt, false, X, Xq, none, M, K, (cudaStream_t)stream),
+                       "quantizer launch");
+}
+
+qmm_status qmm_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N, int64_t K,
+                                qmm_stream_t stream) {
+    qmm_status st = check_weight_args(wt, N, K);
+    if (st != QMM_OK) return st;
+    if (N == 0) return ok();
+    QMM_CHECK_ARG(W && Wq, "null pointer argument");
+    QMM_CHECK_ARG(aligned(W, 16), "W must be 16-byte aligned");
+    QMM_CHECK_ARG(aligned(Wq, wt == QMM_TYPE_Q4_K ? 16 : 2), "Wq misaligned");
+    return cuda_status(launch_quantize_weights(wt, W, Wq, N, K, (cudaStream_t)stream),
+                       "weight quantizer launch");
+}
+
+static qmm_status repack_common(qmm_type wt, const void *src, void *dst, int64_t N, int64_t K,
+                                bool inverse, qmm_stream_t stream) {
+    qmm_status st = check_weight_args(wt, N, K);
+    if (st != QMM_OK) return st;
+    QMM_CHECK_ARG(N > 0, "N must be > 0");
+    QMM_CHECK_ARG(src && dst, "null pointer argument");
+    const void *canon = inverse ? dst : src;
+    const void *packed = inverse ? src : dst;
+    QMM_CHECK_ARG(aligned(packed, 16), "packed weights must be 16-byte aligned");
+    QMM_CHECK_ARG(aligned(canon, wt == QMM_TYPE_Q4_K ? 16 : 2), "canonical weights misaligned");
+    const uintptr_t a = (uintptr_t)src, b = (uintptr_t)dst;
+    const size_t pb = qmm_packed_bytes(wt, N, K);
+    QMM_CHECK_ARG(a + pb <= b || b + pb <= a, "source and destination overlap");
+    return cuda_status(launch_repack(wt, inverse, src, dst, N, K, (cudaStream_t)stream),
+                       "repack launch");
+}
+
+qmm_status qmm_repack_weights(qmm_type wt, const void *W_canon, void *W_packed, int64_t N,
+                              int64_t K, qmm_stream_t stream) {
+    return repack_common(wt, W_canon, W_packed, N, K, false, stream);
+}
+
+qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon, int64_t N,
+                                int64_t K, qmm_stream_t stream) {
+    return repack_common(wt, W_packed, W_canon, N, K, true, stream);
+}
+
+qmm_status qmm_mul_mat_ws(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X,
+                          int64_t M, float *Y, void *workspace, size_t ws_bytes,
+                          qmm_stream_t stream) {
+    qmm_status st = check_mul_mat_args(wt, W_packed, N, K, X, M, Y);
+    if (st != QMM_OK) return st;
+    if (M == 0 || N == 0) return ok();
+    QMM_CHECK_ARG(workspace && aligned(workspace, 16), "workspace must be non-null, 16-byte aligned");
+    return mul_mat_impl(wt, W_packed, N, K, X, M, Y, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+qmm_status qmm_quantize_activations(qmm_type wt, const float *X, int64_t M, int64_t K,
+                                    void *workspace, size_t ws_bytes, qmm_stream_t stream) {
+    qmm_status st = check_weight_args(wt, 1, K);
+    if (st != QMM_OK) return st;
+    QMM_CHECK_ARG(M >= 0, "M must be >= 0 (got %lld)", (long long)M);
+    if (M == 0) return ok();
+    QMM_CHECK_ARG(X && workspace, "null pointer argument");
+    QMM_CHECK_ARG(aligned(X, 16) && aligned(workspace, 16),
+                  "X and workspace must be 16-byte aligned");
+    return quantize_acts_impl(wt, X, M, K, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
+                                const void *workspace, size_t ws_bytes, int64_t M, float *Y,
+                                qmm_stream_t stream) {
+    qmm_status st = check_weight_args(wt, N, K);
+    if (st != QMM_OK) return st;
+    QMM_CHECK_ARG(M >= 0, "M must be >= 0 (got %lld)", (long long)M);
+    if (M == 0 || N == 0) return ok();
+    QMM_CHECK_ARG(W_packed && workspace && Y, "null pointer argument");
+    QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(workspace, 16) && aligned(Y, 4),
+                  "W_packed and workspace must be 16-byte aligned, Y 4-byte aligned");
+    return prepared_impl(wt, W_packed, N, K, workspace, ws_bytes, M, Y, (cudaStream_t)stream);
+}
+
+qmm_status qmm_mul_mat(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X,
+                       int64_t M, float *Y, qmm_stream_t stream) {
+    qmm_status st = check_mul_mat_args(wt, W_packed, N, K, X, M, Y);
+    if (st != QMM_OK) return st;
+    if (M == 0 || N == 0) return ok();
+    prepare_pool();
+    const size_t need = qmm_workspace_bytes(wt, M, K);
+    cudaStream_t s = (cudaStream_t)stream;
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess || !ws) {
+        cudaGetLastError();
+        return set_error(QMM_ERR_NOMEM, "cudaMallocAsync(%zu): %s", need, cudaGetErrorString(e));
+    }
+    st = mul_mat_impl(wt, W_packed, N, K, X, M, Y, ws, need, s);
+    cudaError_t ef = cudaFreeAsync(ws, s);
+    if (st == QMM_OK && ef != cudaSuccess) return cuda_status(ef, "cudaFreeAsync");
+    return st;
+}
+
+qmm_status qmm_debug_block_sums(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
+                                const void *Xq, int64_t M, int32_t *out, qmm_stream_t stream) {
+    qmm_status st = check_weight_args(wt, N, K);
+    if (st != QMM_OK) return st;
+    QMM_CHECK_ARG(M >= 0, "M must be >= 0");
+    if (M == 0 || N == 0) return ok();
+    QMM_CHECK_ARG(W_packed && Xq && out, "null pointer argument");
+    QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(out, 4), "misaligned pointer");
+    QMM_CHECK_ARG(aligned(Xq, wt == QMM_TYPE_Q4_K ? 4 : 2), "Xq misaligned");
+    return cuda_status(
+        launch_debug_block_sums(wt, W_packed, N, K, Xq, M, out, (cudaStream_t)stream),
+        "debug kernel launch");
+}
+
+const char *qmm_status_string(qmm_status s) {
+    switch (s) {
+    case QMM_OK: return "QMM_OK";
+    case QMM_ERR_ARG: return "QMM_ERR_ARG";
+    case QMM_ERR_UNSUPPORTED: return "QMM_ERR_UNSUPPORTED";
+    case QMM_ERR_CUDA: return "QMM_ERR_CUDA";
+    case QMM_ERR_TIMEOUT: return "QMM_ERR_TIMEOUT";
+    case QMM_ERR_NOMEM: return "QMM_ERR_NOMEM";
+    case QMM_ERR_WORKSPACE: return "QMM_ERR_WORKSPACE";
+    default: return "QMM_ERR_UNKNOWN";
+    }
+}
+
+const char *qmm_last_error(void) { return g_msg; }
+
+qmm_status qmm_check_device_error(qmm_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_status(e, "stream synchronize");
+    unsigned *w = device_error_word();
+    if (!w) return set_error(QMM_ERR_CUDA, "device error word unavailable");
+    unsigned v = 0;
+    e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e, "read device error word");
+    if (v) {
+        const unsigned zero = 0;
+        cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    }
+    if (v & kDevErrTimeout)
+        return set_error(QMM_ERR_TIMEOUT, "a kernel gave up a bounded device-side wait");
+    return ok();
+}
+
+uint64_t qmm_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,197 @@
+// qmm_internal.cuh -- device helpers and private layouts shared by the
+// libqmm translation units (never by the CPU oracle).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qmm.h"
+
+namespace qmm {
+
+// ------------------------------------------------------------------ formats
+constexpr int QK4_0 = 32;   // elements per Q4_0 / Q8_0 block
+constexpr int QK_K = 256;   // elements per Q4_K / Q8_K super-block
+constexpr int B_Q4_0 = 18;  // canonical bytes per block (page 1 block layouts)
+constexpr int B_Q8_0 = 34;
+constexpr int B_Q4_K = 144;
+constexpr int B_Q8_K = 292;
+
+// Packed weight layout: rows grouped in tiles of kTileRows. Within a tile,
+// the blocks of one K position are adjacent, so a (tile, K-range) is one
+// contiguous byte range that a single bulk copy moves:
+//   Q4_K: tile t = [nsb][kTileRows][144 B]   (canonical block bytes)
+//   Q4_0: tile t = [kTileRows][nb][16 B nibbles] then [nb][kTileRows] fp16 d
+//         (a (tile, K-range) is then 8 row segments plus one scale segment)
+constexpr int kTileRows = 8;
+
+__host__ __device__ inline int64_t tiles_of(int64_t N) { return (N + kTileRows - 1) / kTileRows; }
+
+// Private quantized-activation layout ("planar"), written by the quantizer
+// for the mul_mat kernels:
+//   qs   : int8  [M][K]          codes, rows 16-byte aligned (K % 32 == 0)
+//   d    : float [M][K/QK]       block scales (Q8_0: the fp16 scale widened)
+//   sums : int16 [M][K/QK][G]    Q8_K: G = 16 sums of 16 codes (bsums);
+//                                Q8_0: G = 1, the sum of the block's 32 codes
+struct Planar {
+    int8_t *qs;
+    float *d;
+    int16_t *sums;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace carve-up for M rows of K activations with block size qk.
+__host__ __device__ inline size_t planar_bytes(int64_t M, int64_t K, int qk, Planar *p,
+                                               uint8_t *base) {
+    const int64_t nb = K / qk;
+    const int g = qk == QK_K ? 16 : 1;
+    size_t off = 0;
+    size_t o_qs = off;
+    off = align_up(off + (size_t)M * K, 256);
+    size_t o_d = off;
+    off = align_up(off + (size_t)M * nb * sizeof(float), 256);
+    size_t o_s = off;
+    off = align_up(off + (size_t)M * nb * g * sizeof(int16_t), 256);
+    if (p) {
+        p->qs = (int8_t *)(base + o_qs);
+        p->d = (float *)(base + o_d);
+        p->sums = (int16_t *)(base + o_s);
+    }
+    return off;
+}
+
+// ------------------------------------------------------------------ errors
+// Device error word bits (read and cleared by qmm_check_device_error).
+constexpr unsigned kDevErrTimeout = 1u;
+
+// A bounded wait gives up after this many SM clock cycles (about 2 s).
+constexpr long long kWaitTimeoutCycles = 4000000000LL;
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete. Returns
+// false (and records a timeout in *err) if it has not after the bound.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitTimeoutCycles) {
+            atomicOr(err, kDevErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// 1-D bulk async copy global -> shared, completing on an mbarrier.
+// dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue / wait for the previous kernel's memory to be visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc128(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Round half away from zero in fp32 without contraction: sign(v) floor(|v| + 0.5).
+__device__ __forceinline__ float round_half_away(float v) {
+    return v < 0.0f ? -floorf(__fadd_rn(-v, 0.5f)) : floorf(__fadd_rn(v, 0.5f));
+}
+
+__device__ __forceinline__ int clampi(int v, int lo, int hi) { return min(max(v, lo), hi); }
+
+}  // namespace qmm
+
+// ------------------------------------------------------------------ host side
+namespace qmm {
+struct Launch;
+// Defined in api.cu.
+unsigned *device_error_word();           // device pointer for the current device
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device)
+cudaError_t ensure_smem_attr(const void *kernel, int bytes);
+int sm_count();                          // SMs of the current device
+void count_launch(unsigned n = 1);       // bump the launch counter
+qmm_status set_error(qmm_status s, const char *fmt, ...);
+
+// Kernel launchers (each .cu file); all return cudaSuccess or the launch error.
+cudaError_t launch_quantize_q8(qmm_type vt, bool planar, const float *X, void *out, Planar p,
+                               int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N, int64_t K,
+                                    cudaStream_t s);
+cudaError_t launch_repack(qmm_type wt, bool inverse, const void *src, void *dst, int64_t N,
+                          int64_t K, cudaStream_t s);
+cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x, int64_t M,
+                        float *Y, bool pdl, cudaStream_t s);
+cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
+                                    const void *Xq, int64_t M, int32_t *out, cudaStream_t s);
+}  // namespace qmm

@@ -1,0 +1,119 @@
+// repack.cu -- canonical weight blocks <-> the private GPU layout.
+//
+// The layout change is done once at load time (page 3, "Ladder Permutation":
+// a permutation applied offline pays off when R * dT > T_P, and turns
+// run-time address shuffles into contiguous reads; page 4 on GGML_CPU_REPACK).
+// It is a pure byte permutation:
+//   Q4_K: canonical [N][nsb][144 B] -> tiles of 8 rows, [T][nsb][8][144 B].
+//         One (tile, super-block range) is then one contiguous byte range.
+//   Q4_0: canonical [N][nb][18 B]   -> per tile [8][nb][16 B nibbles] followed
+//         by [nb][8] fp16 scales, so the nibbles are 16-byte aligned (the
+//         18-byte block defeats 128-bit loads).
+// Padding rows (N not a multiple of 8) are zero blocks: d = 0 contributes 0.
+#include "qmm_internal.cuh"
+
+namespace qmm {
+namespace {
+
+// Q4_K: one thread per 16-byte chunk of the packed buffer (or of the
+// canonical buffer for the inverse).
+template <bool kInverse>
+__global__ void repack_q4_K_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                   int64_t N, int64_t nsb) {
+    const int64_t Npad = tiles_of(N) * kTileRows;
+    const int64_t total = Npad * nsb * 9;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t pblk = i / 9;  // packed block index
+        const int chunk = (int)(i % 9);
+        const int64_t tile = pblk / (nsb * kTileRows);
+        const int64_t rem = pblk % (nsb * kTileRows);
+        const int64_t sb = rem / kTileRows;
+        const int64_t n = tile * kTileRows + rem % kTileRows;
+        const int64_t cblk = n * nsb + sb;  // canonical block index
+        if (!kInverse) {
+            dst[i] = n < N ? src[cblk * 9 + chunk] : make_uint4(0, 0, 0, 0);
+        } else if (n < N) {
+            dst[cblk * 9 + chunk] = src[i];
+        }
+    }
+}
+
+// Q4_0: one thread per (row, block).
+template <bool kInverse>
+__global__ void repack_q4_0_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
+                                   int64_t N, int64_t nb) {
+    const int64_t Npad = tiles_of(N) * kTileRows;
+    const int64_t total = Npad * nb;
+    const int64_t tile_bytes = nb * kTileRows * B_Q4_0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / nb, b = i % nb;
+        const int64_t tile = n / kTileRows;
+        const int r = (int)(n % kTileRows);
+        uint8_t *packed_base = kInverse ? nullptr : dst + tile * tile_bytes;
+        const uint8_t *packed_src = kInverse ? src + tile * tile_bytes : nullptr;
+        const int64_t qs_off = (r * nb + b) * 16;
+        const int64_t d_off = nb * kTileRows * 16 + (b * kTileRows + r) * 2;
+        if (!kInverse) {
+            uint16_t h[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+            if (n < N) {
+                const uint16_t *c = reinterpret_cast<const uint16_t *>(src + (n * nb + b) * B_Q4_0);
+#pragma unroll
+                for (int k = 0; k < 9; ++k) h[k] = c[k];
+            }
+            uint4 q;
+            q.x = h[1] | ((uint32_t)h[2] << 16);
+            q.y = h[3] | ((uint32_t)h[4] << 16);
+            q.z = h[5] | ((uint32_t)h[6] << 16);
+            q.w = h[7] | ((uint32_t)h[8] << 16);
+            *reinterpret_cast<uint4 *>(packed_base + qs_off) = q;
+            *reinterpret_cast<uint16_t *>(packed_base + d_off) = h[0];
+        } else if (n < N) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(packed_src + qs_off);
+            const uint16_t d = *reinterpret_cast<const uint16_t *>(packed_src + d_off);
+            uint16_t *c = reinterpret_cast<uint16_t *>(dst + (n * nb + b) * B_Q4_0);
+            c[0] = d;
+            c[1] = (uint16_t)q.x;
+            c[2] = (uint16_t)(q.x >> 16);
+            c[3] = (uint16_t)q.y;
+            c[4] = (uint16_t)(q.y >> 16);
+            c[5] = (uint16_t)q.z;
+            c[6] = (uint16_t)(q.z >> 16);
+            c[7] = (uint16_t)q.w;
+            c[8] = (uint16_t)(q.w >> 16);
+        }
+    }
+}
+
+int grid_1d(int64_t n, int threads) {
+    const int64_t ctas = (n + threads - 1) / threads;
+    const int64_t cap = (int64_t)sm_count() * 32;
+    return (int)(ctas < 1 ? 1 : (ctas < cap ? ctas : cap));
+}
+
+}  // namespace
+
+cudaError_t launch_repack(qmm_type wt, bool inverse, const void *src, void *dst, int64_t N,
+                          int64_t K, cudaStream_t s) {
+    const int64_t Npad = tiles_of(N) * kTileRows;
+    if (wt == QMM_TYPE_Q4_K) {
+        const int64_t nsb = K / QK_K;
+        const int grid = grid_1d(Npad * nsb * 9, 256);
+        if (inverse)
+            repack_q4_K_kernel<true><<<grid, 256, 0, s>>>((const uint4 *)src, (uint4 *)dst, N, nsb);
+        else
+            repack_q4_K_kernel<false><<<grid, 256, 0, s>>>((const uint4 *)src, (uint4 *)dst, N, nsb);
+    } else {
+        const int64_t nb = K / QK4_0;
+        const int grid = grid_1d(Npad * nb, 256);
+        if (inverse)
+            repack_q4_0_kernel<true><<<grid, 256, 0, s>>>((const uint8_t *)src, (uint8_t *)dst, N, nb);
+        else
+            repack_q4_0_kernel<false><<<grid, 256, 0, s>>>((const uint8_t *)src, (uint8_t *)dst, N, nb);
+    }
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace qmm

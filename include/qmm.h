@@ -1,0 +1,214 @@
+/*
+ * qmm.h -- C ABI of libqmm, block-quantized matrix multiplication on GB300
+ * (sm_103a).
+ *
+ * The library computes a linear layer y = W x whose weights are stored in
+ * ggml's 4-bit block formats, with the activations quantized on the fly to
+ * 8-bit blocks and the product taken as an integer block dot product with
+ * fp32 accumulation, as described on the page
+ *   "llama.cpp 源码完全拆解(十三): ggml-cpu 的一次 mul_mat"
+ * (sections on the Q4_0/Q8_0 and K-quant block layouts, the 6-bit scale
+ * packing, the scale-factoring identity and the mul_mat steps), plus the
+ * W4A16 group-asymmetric form of
+ *   "BitBLAS 完全拆解: 低比特权重如何在 Tensor Core 上边解码边计算"
+ * (sections "从数学表达式到真实存储" and "位级打包").
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless the argument says "host".
+ *   - W is [N, K]: N output rows of K/QK blocks each (QK = 32 for Q4_0 and
+ *     Q8_0, 256 for Q4_K and Q8_K). X is fp32 [M, K] row-major. Y is fp32
+ *     [M, N] row-major: Y[m * N + n] = sum_k W[n, k] X[m, k].
+ *   - "Canonical" blocks are the packed little-endian structs the page prints
+ *     (no padding): block_q4_0 {fp16 d; u8 qs[16]} 18 B; block_q8_0 {fp16 d;
+ *     i8 qs[32]} 34 B; block_q4_K {fp16 d; fp16 dmin; u8 scales[12];
+ *     u8 qs[128]} 144 B; block_q8_K {f32 d; i8 qs[256]; i16 bsums[16]} 292 B.
+ *     A row of K elements is K/QK consecutive blocks; rows are consecutive.
+ *     This is the interchange format. "Packed" weights are this library's
+ *     private GPU layout, made from canonical blocks by qmm_repack_weights.
+ *   - The caller owns every buffer; the library never frees caller memory.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
+ *     no call synchronizes the host except qmm_check_device_error.
+ *   - Device buffers must be 16-byte aligned, except canonical Q4_0/Q8_0
+ *     buffers (18/34-byte blocks), which need 2-byte alignment.
+ *   - Errors: arguments are validated before anything is enqueued; on any
+ *     error nothing is launched and a qmm_status other than QMM_OK is
+ *     returned (qmm_last_error() gives a one-line reason). Kernels never trap:
+ *     a device-side wait that exceeds its bound records QMM_ERR_TIMEOUT in a
+ *     device error word, read and cleared by qmm_check_device_error.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-compatible with cudaStream_t / CUstream. */
+typedef struct CUstream_st *qmm_stream_t;
+
+typedef enum {
+    QMM_TYPE_Q4_0 = 0, /* weights: 32 x 4-bit, fp16 d;       w = d (q - 8)            */
+    QMM_TYPE_Q4_K = 1, /* weights: 256 x 4-bit, 8 sub-blocks; w = d s_j q - dmin m_j  */
+    QMM_TYPE_Q8_0 = 2, /* activations: 32 x int8, fp16 d;     a = d q                  */
+    QMM_TYPE_Q8_K = 3  /* activations: 256 x int8, fp32 d, 16 sums of 16 codes        */
+} qmm_type;
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_ARG = 1,         /* null pointer, bad size, misaligned pointer, bad type */
+    QMM_ERR_UNSUPPORTED = 2, /* valid request this build does not implement          */
+    QMM_ERR_CUDA = 3,        /* a CUDA runtime call failed                           */
+    QMM_ERR_TIMEOUT = 4,     /* a device-side wait exceeded its bound                */
+    QMM_ERR_NOMEM = 5,       /* the library could not allocate its workspace         */
+    QMM_ERR_WORKSPACE = 6    /* caller workspace smaller than qmm_workspace_bytes    */
+} qmm_status;
+
+/* ---------------------------------------------------------------- sizes */
+
+/* Bytes of one canonical block: 18, 144, 34, 292; 0 for an invalid type.
+ * (Block layouts: page 1, "最基础的两块: Q4_0 与 Q8_0", "K-quant", "更低的比特".) */
+size_t qmm_block_bytes(qmm_type t);
+
+/* Elements per block: 32 or 256; 0 for an invalid type. */
+int qmm_block_elems(qmm_type t);
+
+/* Bytes of the packed (repacked) weight buffer for an [N, K] weight of type
+ * Q4_0 or Q4_K; 0 if the type or sizes are invalid. Rows are padded to a
+ * multiple of 8 with zero blocks. */
+size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K);
+
+/* Bytes of the workspace qmm_mul_mat_ws needs for M activation rows of
+ * length K against weights of type wt (Q4_0 or Q4_K); 0 if invalid. */
+size_t qmm_workspace_bytes(qmm_type wt, int64_t M, int64_t K);
+
+/* ---------------------------------------------------------------- quantizers */
+
+/* Quantize fp32 activations X [M, K] into canonical blocks Xq of type vt
+ * (Q8_0 or Q8_K), M rows of K/QK blocks (page 1, "最基础的两块" for Q8_0 and
+ * "更低的比特" for Q8_K with its bsums; the mul_mat step "激活得先变成 Q8_K").
+ * Per block: amax = max |x|, d = amax / 127, q = round-half-away(x / d)
+ * clamped to [-127, 127] (computed as x * (1/d) in fp32); Q8_0 stores d as
+ * fp16, Q8_K as fp32 plus bsums[t] = sum of codes 16t..16t+15. An all-zero
+ * block gives d = 0 and q = 0. Bit-identical to the CPU oracle.
+ * Errors: QMM_ERR_ARG if vt is not Q8_0/Q8_K, M < 0, K <= 0 or K % QK != 0,
+ * or a pointer is null while M > 0. M == 0 is a no-op. */
+qmm_status qmm_quantize_row_q8(qmm_type vt, const float *X, void *Xq, int64_t M, int64_t K,
+                               qmm_stream_t stream);
+
+/* Quantize fp32 weights W [N, K] into canonical blocks Wq of type wt (Q4_0 or
+ * Q4_K) -- the offline quantizer's job, done on the GPU.
+ * Q4_0 (page 1, "最基础的两块"): d = -x_max / 8 where x_max is the signed
+ * value of largest magnitude (the first on ties); q = clamp(floor(x * (1/d)
+ * + 8.5), 0, 15); d stored as fp16; byte l holds element l (low nibble) and
+ * element l + 16 (high nibble).
+ * Q4_K (page 1, "K-quant", "6-bit 参数", nibble packing in "正确性"): per
+ * sub-block j of 32: lo = min(0, min x), hi = max x, sc_j = (hi - lo) / 15,
+ * mn_j = -lo; d = max sc_j / 63, dmin = max mn_j / 63 (fp16);
+ * s_j = clamp(round(sc_j / d), 0, 63), m_j = clamp(round(mn_j / dmin), 0, 63);
+ * q = clamp(round((x + dmin16 m_j) / (d16 s_j)), 0, 15) with the stored fp16
+ * d16, dmin16; scales packed in 12 bytes, qs[32c + l] = q[64c + l] |
+ * q[64c + 32 + l] << 4. The pages print the format but not the scale search;
+ * this single-pass min/max search is this library's reading.
+ * Bit-identical to the CPU oracle. Errors as qmm_quantize_row_q8. */
+qmm_status qmm_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N, int64_t K,
+                                qmm_stream_t stream);
+
+/* ---------------------------------------------------------------- layout */
+
+/* Repack canonical weight blocks W_canon ([N] rows of K/QK blocks) into the
+ * private GPU layout W_packed (qmm_packed_bytes bytes), once at load time
+ * (page 3, "Ladder Permutation": permute offline so run-time reads are
+ * contiguous; page 4 on GGML_CPU_REPACK). A pure byte permutation: rows are
+ * grouped in tiles of 8 and, within a tile, blocks of the same K position are
+ * adjacent; Q4_0 blocks are split into a 16-byte nibble plane and an fp16
+ * scale plane. W_packed must not overlap W_canon.
+ * Errors: QMM_ERR_ARG for a non-weight type, N <= 0, K <= 0, K % QK != 0,
+ * null or misaligned pointers. */
+qmm_status qmm_repack_weights(qmm_type wt, const void *W_canon, void *W_packed, int64_t N,
+                              int64_t K, qmm_stream_t stream);
+
+/* Inverse of qmm_repack_weights (a test and debugging aid). */
+qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon, int64_t N,
+                                int64_t K, qmm_stream_t stream);
+
+/* ---------------------------------------------------------------- mul_mat */
+
+/* Y [M, N] = W [N, K] . X [M, K]^T, the whole method (page 1, mul_mat steps
+ * 1-3 and "正确性: 缩放系数可以提到求和号外面"): the activations are
+ * quantized once per call to Q8_0 (for Q4_0 weights) or Q8_K (for Q4_K) in
+ * the same stream, then every output is
+ *   Q4_0: sum_b fp16(d_w) fp16(d_a) sum_{i<32} (q_i - 8) y_i
+ *   Q4_K: sum_sb d_a (d * sum_j s_j sum_i q_i y_i - dmin * sum_j m_j sum_i y_i)
+ * with integer block sums and fp32 accumulation across blocks. M <= 16 runs
+ * the decode GEMV kernels; larger M the prefill GEMM.
+ * W_packed comes from qmm_repack_weights. The quantized activations live in a
+ * workspace that the library allocates stream-ordered (cudaMallocAsync) and
+ * frees after the call, in the same stream.
+ * Errors: QMM_ERR_ARG (type, sizes, null/misaligned pointers),
+ * QMM_ERR_NOMEM (workspace allocation failed), QMM_ERR_CUDA (launch failed).
+ * M == 0 or N == 0 is a no-op. */
+qmm_status qmm_mul_mat(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X,
+                       int64_t M, float *Y, qmm_stream_t stream);
+
+/* qmm_mul_mat with a caller-provided workspace of at least
+ * qmm_workspace_bytes(wt, M, K) bytes (QMM_ERR_WORKSPACE otherwise). The
+ * workspace is in use until the call's work on `stream` has finished. */
+qmm_status qmm_mul_mat_ws(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X,
+                          int64_t M, float *Y, void *workspace, size_t ws_bytes,
+                          qmm_stream_t stream);
+
+/* The two halves of qmm_mul_mat_ws, for callers that reuse one quantized
+ * activation across several weight matrices (page 1, "为什么每个任务都要重新
+ * 量化激活": a mul_mat quantizes its activations once; projections sharing an
+ * input need not each re-quantize it).
+ * qmm_quantize_activations: quantize X [M, K] for weights of type wt into
+ *   `workspace` (qmm_workspace_bytes(wt, M, K) bytes, 16-byte aligned), in
+ *   this library's private layout: int8 codes [M][K], fp32 block scales and
+ *   int16 code sums (Q8_K: 16 per super-block; Q8_0: 1 per block). The codes
+ *   and scales are those of qmm_quantize_row_q8.
+ * qmm_mul_mat_prepared: Y [M, N] from packed weights and a workspace filled
+ *   by qmm_quantize_activations with the same wt, M and K (the contents are
+ *   not checked). The workspace is read-only here, so several calls may
+ *   share it. Errors as qmm_mul_mat_ws. */
+qmm_status qmm_quantize_activations(qmm_type wt, const float *X, int64_t M, int64_t K,
+                                    void *workspace, size_t ws_bytes, qmm_stream_t stream);
+qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
+                                const void *workspace, size_t ws_bytes, int64_t M, float *Y,
+                                qmm_stream_t stream);
+
+/* Per-block integer sums of the factored form, for bit-exact checking
+ * (page 1, "正确性" and "通用实现"). Xq holds canonical activation blocks
+ * (Q8_0 for Q4_0 weights, Q8_K for Q4_K), M rows.
+ *   Q4_0: out[(m * N + n) * (K/32) + b] = sum_{i<32} (q_i - 8) y_i
+ *   Q4_K: out[((m * N + n) * (K/256) + sb) * 10 + t] with t = 0..7 the
+ *         sub-block sums S_j = sum_i q_i y_i, t = 8 the scaled sum
+ *         sum_j s_j S_j and t = 9 the min sum sum_j m_j (bs_2j + bs_2j+1).
+ * Errors as qmm_mul_mat. */
+qmm_status qmm_debug_block_sums(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
+                                const void *Xq, int64_t M, int32_t *out, qmm_stream_t stream);
+
+/* ---------------------------------------------------------------- status */
+
+/* Static string naming a status code. */
+const char *qmm_status_string(qmm_status s);
+
+/* Host: one-line description of the last error returned on this thread. */
+const char *qmm_last_error(void);
+
+/* Synchronize `stream`, then read and clear the device error word of the
+ * current device. Returns QMM_ERR_TIMEOUT if a kernel gave up a bounded
+ * wait since the last check, QMM_ERR_CUDA if the stream reported an error,
+ * QMM_OK otherwise. */
+qmm_status qmm_check_device_error(qmm_stream_t stream);
+
+/* Number of kernels this library has launched on this process (all devices).
+ * A monotone counter for accounting in benchmarks and tests. */
+uint64_t qmm_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMM_H */

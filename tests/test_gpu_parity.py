@@ -1,0 +1,239 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bar (from the method's own contract): quantized blocks, the repack round trip
+and per-block integer sums are bit-exact; fp32 outputs satisfy
+|Y_gpu - Y_ref| <= 1e-3 * sum_k |w_k a_k| element by element, with Y_ref the
+oracle's fp64 result on the same quantized operands.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def q():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_quantized_matmul_q4_gb300 as q
+    return q
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def gpu_quantize_q8(q, vt, x):
+    M, K = x.shape
+    X = dev(x.astype(np.float32))
+    Xq = q.empty_blocks(vt, M, K)
+    q.qmm_quantize_row_q8(vt, X, Xq, M, K)
+    return host(Xq).reshape(M, -1)
+
+
+def gpu_quantize_w(q, wt, w):
+    N, K = w.shape
+    Wq = q.empty_blocks(wt, N, K)
+    q.qmm_quantize_weights(wt, dev(w.astype(np.float32)), Wq, N, K)
+    return Wq
+
+
+def edge_rows(K, seed):
+    rows = [np.zeros(K), np.full(K, 0.37), np.full(K, -2.5),
+            wl.normal_flat(seed, 90, K).numpy() * 1e-30,
+            wl.normal_flat(seed, 91, K).numpy() * 1e4,
+            -np.abs(wl.normal_flat(seed, 92, K).numpy()),
+            np.where(np.arange(K) % 3 == 0, -0.0, 0.0)]
+    spike = np.zeros(K)
+    spike[K // 3] = -5.0
+    rows.append(spike)
+    return np.stack(rows).astype(np.float32)
+
+
+def check_close(y, ref, den, what):
+    err = np.abs(y.astype(np.float64) - ref)
+    bad = err > TOL * den + 1e-30
+    assert np.all(np.isfinite(y)), f"{what}: non-finite output"
+    assert not bad.any(), (f"{what}: {bad.sum()} outputs off; worst normalised error "
+                           f"{np.max(err / np.maximum(den, 1e-30)):.3e}")
+
+
+# ------------------------------------------------------------------ quantizers
+@pytest.mark.parametrize("vt,M,K", [(2, 1, 1024), (2, 5, 96), (2, 16, 4096),
+                                    (3, 1, 256), (3, 3, 4352), (3, 17, 4096)])
+def test_activation_quantizer_bit_exact(q, orc, vt, M, K):
+    x = wl.activations(7, M, K, hot_frac=0.01).numpy()
+    x = np.concatenate([x, edge_rows(K, 7)])
+    got = gpu_quantize_q8(q, vt, x)
+    assert np.array_equal(got, orc.quantize(vt, x))
+
+
+@pytest.mark.parametrize("wt,N,K", [(0, 256, 1024), (0, 13, 96), (1, 13, 512), (1, 64, 4096)])
+def test_weight_quantizer_bit_exact(q, orc, wt, N, K):
+    w = wl.weights(8, N, K, 0.02, row_offset_std=0.005, outlier_frac=1e-3).numpy()
+    w = np.concatenate([w, edge_rows(K, 8)])
+    got = host(gpu_quantize_w(q, wt, w)).reshape(w.shape[0], -1)
+    assert np.array_equal(got, orc.quantize(wt, w))
+
+
+# ------------------------------------------------------------------ layout + sums
+@pytest.mark.parametrize("wt,N,K,M", [(0, 13, 96, 3), (0, 21, 4160, 2), (1, 13, 512, 2),
+                                      (1, 9, 4352, 1)])
+def test_repack_roundtrip_and_block_sums(q, orc, wt, N, K, M):
+    w = wl.weights(9, N, K, 0.02, row_offset_std=0.005).numpy()
+    x = wl.activations(9, M, K).numpy()
+    Wc = orc.quantize(wt, w)
+    Xq = orc.quantize(orc.ACT_TYPE[wt], x)
+    Wp = q.empty_packed(wt, N, K)
+    q.qmm_repack_weights(wt, dev(Wc), Wp, N, K)
+    back = q.empty_blocks(wt, N, K)
+    q.qmm_unrepack_weights(wt, Wp, back, N, K)
+    assert np.array_equal(host(back).reshape(N, -1), Wc)
+    per = 10 if wt == 1 else 1
+    nblk = K // (256 if wt == 1 else 32)
+    out = torch.empty(M * N * nblk * per, dtype=torch.int32, device="cuda")
+    q.qmm_debug_block_sums(wt, Wp, N, K, dev(Xq), M, out)
+    got = host(out).reshape(M, N, nblk, per)
+    for m in range(M):
+        for n in range(N):
+            if wt == 0:
+                assert np.array_equal(got[m, n, :, 0], orc.block_sums(0, K, Wc[n], Xq[m]))
+            else:
+                S, isum, msum = orc.block_sums(1, K, Wc[n], Xq[m])
+                assert np.array_equal(got[m, n, :, :8], S)
+                assert np.array_equal(got[m, n, :, 8], isum)
+                assert np.array_equal(got[m, n, :, 9], msum)
+
+
+# ------------------------------------------------------------------ mul_mat
+def run_mul_mat(q, wt, Wc, N, K, x, guard=64):
+    """qmm_mul_mat on canonical blocks Wc and fp32 x; returns Y [M, N] and
+    checks that the guard words after Y are untouched."""
+    M = x.shape[0]
+    Wp = q.empty_packed(wt, N, K)
+    q.qmm_repack_weights(wt, dev(Wc) if isinstance(Wc, np.ndarray) else Wc, Wp, N, K)
+    Y = torch.full((M * N + guard,), float("nan"), dtype=torch.float32, device="cuda")
+    Y[M * N:] = 12345.0
+    q.qmm_mul_mat(wt, Wp, N, K, dev(x.astype(np.float32)), M, Y)
+    y = host(Y)
+    assert np.all(y[M * N:] == 12345.0), "write past the end of Y"
+    return y[:M * N].reshape(M, N)
+
+
+@pytest.mark.parametrize("wt,N,K,M", [
+    (0, 256, 1024, 1),    # Q4_0 x Q8_0 GEMV, 256 x 1024, M = 1
+    (0, 13, 96, 3), (0, 37, 4160, 5), (0, 64, 1024, 16), (0, 24, 512, 33),
+    (1, 13, 512, 1), (1, 37, 4352, 5), (1, 64, 4096, 16), (1, 16, 1024, 17), (1, 8, 256, 1)])
+def test_mul_mat_against_oracle(q, orc, wt, N, K, M):
+    w = wl.weights(10, N, K, 0.02, row_offset_std=0.005 if wt == 1 else 0.0).numpy()
+    x = wl.activations(10, M, K).numpy()
+    Wc = orc.quantize(wt, w)
+    y = run_mul_mat(q, wt, Wc, N, K, x)
+    ref = orc.mul_mat(wt, Wc, N, K, x, nthreads=orc.default_threads())
+    check_close(y, ref["y64"], ref["den"], f"wt={wt} N={N} K={K} M={M}")
+    # the fp32 oracle itself sits inside the same bound
+    check_close(ref["y32"], ref["y64"], ref["den"], "oracle fp32")
+
+
+def test_mul_mat_edge_inputs(q, orc):
+    for wt, K in ((0, 256), (1, 256)):
+        w = edge_rows(K, 11)
+        x = np.concatenate([edge_rows(K, 12), wl.activations(12, 2, K).numpy()])
+        N = w.shape[0]
+        Wc = orc.quantize(wt, w)
+        y = run_mul_mat(q, wt, Wc, N, K, x)
+        ref = orc.mul_mat(wt, Wc, N, K, x)
+        check_close(y, ref["y64"], ref["den"], f"edge wt={wt}")
+        assert np.all(y[:, 0] == 0) and np.all(y[0, :] == 0)  # zero weights / activations
+
+
+def test_mul_mat_empty_and_workspace_errors(q):
+    Wp = q.empty_packed(1, 8, 256)
+    Y = torch.zeros(8, device="cuda")
+    X = torch.zeros(1, 256, device="cuda")
+    q.qmm_mul_mat(1, Wp, 8, 256, X, 0, Y)  # M == 0: nothing to do
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_mul_mat_ws(1, Wp, 8, 256, X, 1, Y, torch.empty(16, dtype=torch.uint8, device="cuda"), 16)
+    assert e.value.status == 6
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_mul_mat(3, Wp, 8, 256, X, 1, Y)
+    assert e.value.status == 1
+    q.qmm_check_device_error()
+
+
+# ------------------------------------------------------------------ full sizes
+@pytest.mark.parametrize("M", wl.GEMV_Q4_K_M_SWEEP)
+def test_q4_K_4096_full_size(q, orc, M):
+    """Q4_K x Q8_K GEMV, N = K = 4096, every output of the M sweep."""
+    L = wl.GEMV_Q4_K_4096
+    w = wl.weights(0, L.N, L.K, L.wstd, row_offset_std=L.row_offset_std).numpy()
+    x = wl.activations(0, M, L.K).numpy()
+    Wc = orc.quantize(1, w, nthreads=orc.default_threads())
+    y = run_mul_mat(q, 1, Wc, L.N, L.K, x)
+    ref = orc.mul_mat(1, Wc, L.N, L.K, x, nthreads=orc.default_threads())
+    check_close(y, ref["y64"], ref["den"], f"4096x4096 M={M}")
+
+
+def test_q4_K_4096_graph_launch(q, orc):
+    """The launch configuration of the benchmark: quantizer + GEMV with a
+    caller workspace, captured once in a CUDA graph and replayed."""
+    L = wl.GEMV_Q4_K_4096
+    w = wl.weights(0, L.N, L.K, L.wstd, row_offset_std=L.row_offset_std, device="cuda")
+    x = wl.activations(0, 1, L.K, device="cuda")
+    Wq = q.empty_blocks(1, L.N, L.K)
+    q.qmm_quantize_weights(1, w, Wq, L.N, L.K)
+    Wp = q.empty_packed(1, L.N, L.K)
+    q.qmm_repack_weights(1, Wq, Wp, L.N, L.K)
+    ws_bytes = q.qmm_workspace_bytes(1, 1, L.K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    Y = torch.zeros(L.N, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        q.qmm_mul_mat_ws(1, Wp, L.N, L.K, x, 1, Y, ws, ws_bytes)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    rows = np.r_[0:8, 1000:1008, L.N - 8:L.N]
+    Wc = host(Wq).reshape(L.N, -1)
+    assert np.array_equal(Wc[rows], orc.quantize(1, w[torch.as_tensor(rows, device="cuda")].cpu().numpy()))
+    ref = orc.mul_mat(1, Wc, L.N, L.K, x.cpu().numpy(), rows=rows)
+    check_close(host(Y)[rows][None, :], ref["y64"], ref["den"], "graph replay")
+
+
+def test_70B_layer_sampled_rows(q, orc):
+    """70B-shaped decode layer (7 Q4_K projections, M = 1): weights generated
+    and quantized on the GPU at full size; sampled rows checked bit-exact
+    (blocks) and within tolerance (outputs) against the oracle, which
+    quantizes those rows itself from the same fp32 inputs."""
+    for i, L in enumerate(wl.LAYER_70B):
+        w = wl.weights(100 + i, L.N, L.K, L.wstd, outlier_frac=L.outlier_frac, device="cuda")
+        x = wl.activations(100 + i, 1, L.K, hot_frac=wl.LAYER_70B_HOT_FRAC, device="cuda")
+        Wq = q.empty_blocks(1, L.N, L.K)
+        q.qmm_quantize_weights(1, w, Wq, L.N, L.K)
+        Wp = q.empty_packed(1, L.N, L.K)
+        q.qmm_repack_weights(1, Wq, Wp, L.N, L.K)
+        del Wq
+        Y = torch.empty(L.N, device="cuda")
+        q.qmm_mul_mat(1, Wp, L.N, L.K, x, 1, Y)
+        rows = np.unique(np.r_[0:4, L.N - 4:L.N, np.linspace(0, L.N - 1, 40).astype(np.int64)])
+        w_rows = w[torch.as_tensor(rows, device="cuda")].cpu().numpy()
+        Wc_rows = orc.quantize(1, w_rows)
+        back = q.empty_blocks(1, L.N, L.K)
+        q.qmm_unrepack_weights(1, Wp, back, L.N, L.K)
+        assert np.array_equal(host(back).reshape(L.N, -1)[rows], Wc_rows), L.name
+        ref = orc.mul_mat(1, Wc_rows, len(rows), L.K, x.cpu().numpy())
+        check_close(host(Y)[rows][None, :], ref["y64"], ref["den"], L.name)
+        del w, Wp, back
+        torch.cuda.empty_cache()
