@@ -142,12 +142,19 @@ qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, cons
     Planar p;
     qmm_status st = carve(wt, M, K, ws, ws_bytes, &p);
     if (st != QMM_OK) return st;
-    return cuda_status(launch_gemv(wt, Wp, N, K, p, M, Y, /*pdl=*/true, s),
+    return cuda_status(launch_gemv(wt, Wp, N, K, p, nullptr, M, Y, /*pdl=*/true, s),
                        "mul_mat kernel launch");
 }
 
+// Decode with small M*K quantizes the activations inside the GEMV (one
+// launch); otherwise the quantizer runs first into the workspace.
 qmm_status mul_mat_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, const float *X,
                         int64_t M, float *Y, void *ws, size_t ws_bytes, cudaStream_t s) {
+    if (gemv_can_fuse(wt, M, K)) {
+        Planar none{nullptr, nullptr, nullptr};
+        return cuda_status(launch_gemv(wt, Wp, N, K, none, X, M, Y, /*pdl=*/true, s),
+                           "mul_mat kernel launch");
+    }
     qmm_status st = quantize_acts_impl(wt, X, M, K, ws, ws_bytes, s);
     if (st != QMM_OK) return st;
     return prepared_impl(wt, Wp, N, K, ws, ws_bytes, M, Y, s);

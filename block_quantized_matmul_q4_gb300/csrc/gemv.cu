@@ -1,5 +1,5 @@
 // gemv.cu -- decode-path mul_mat (M = 1..16 tokens per launch) over packed
-// Q4_0 / Q4_K weights and planar Q8_0 / Q8_K activations.
+// Q4_0 / Q4_K weights and Q8_0 / Q8_K activations.
 //
 // Page 1 sets what is computed ("正确性: 缩放系数可以提到求和号外面", the
 // generic vec_dot in "通用实现" and the min term in "min 项与最终归约"):
@@ -14,12 +14,15 @@
 //     through a 4-stage shared-memory ring with 1-D bulk async copies
 //     (cp.async.bulk + mbarrier transaction counts, L2 evict-first), so the
 //     HBM stream is a few large copies per CTA, never gated by the ALU;
-//   * eight consumer warps unpack nibbles and the 6-bit scales in registers
-//     and take the integer dot products with dp4a against the activations
-//     (read through the read-only path; they are small and L1/L2-resident);
-//   * programmatic dependent launch: the producer starts streaming weights
-//     while the activation quantizer still runs; consumers wait for it with
-//     griddepcontrol.wait before touching the activations.
+//   * the activations live in shared memory for the whole kernel, filled one
+//     of three ways (Mode): quantized from fp32 by the consumer warps in the
+//     prologue (the activation quantizer fused into the GEMV, for small M*K),
+//     bulk-copied from a workspace written by the stand-alone quantizer
+//     (after griddepcontrol.wait, so the weight stream starts first), or --
+//     when they do not fit -- read from global memory in place;
+//   * eight consumer warps, one weight row each, unpack nibbles and the 6-bit
+//     scales in registers and take the integer dot products with dp4a; each
+//     lane owns four super-blocks per stage, unrolled for independent loads.
 // Every mbarrier wait is bounded; a timeout sets the device error word and
 // the CTA leaves after draining its own copies in flight.
 #include "qmm_internal.cuh"
@@ -28,56 +31,45 @@ namespace qmm {
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;
 constexpr int kStages = 4;
 constexpr int kStageBytes = 18432;
+constexpr int kRingBytes = kStages * kStageBytes;
 constexpr int kQ4KChunk = 16;   // super-blocks per stage: 16 * 8 rows * 144 B = 18432
 constexpr int kQ40Chunk = 128;  // blocks per stage: 128 * 8 rows * 18 B = 18432
-constexpr int kBarBytes = 2 * kStages * 8;
+constexpr int kBarBytes = 64;   // full[4], empty[4], act
 constexpr int kMaxMT = 16;
-constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes;
+constexpr int kActMax = 36 * 1024;        // shared memory for staged activations
+constexpr int64_t kFuseMaxElems = 32768;  // fused quantizer up to M*K fp32 elements
 static_assert(kQ4KChunk * kTileRows * B_Q4_K == kStageBytes, "stage size");
 static_assert(kQ40Chunk * kTileRows * B_Q4_0 == kStageBytes, "stage size");
 
+enum Mode { kDirect = 0, kStaged = 1, kFused = 2 };
+
+struct GemvArgs {
+    const uint8_t *Wp;  // packed weights
+    int64_t N, nblk;    // rows, blocks per row (nsb for Q4_K, nb for Q4_0)
+    Planar x;           // planar activations (kDirect, kStaged)
+    const float *X;     // fp32 activations (kFused)
+    int64_t M, m0;      // all tokens, first token of this launch
+    float *Y;
+    unsigned *err;
+    uint32_t act_bs, act_d, act_bytes;  // shared activation layout (offsets, total)
+};
+
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ uint32_t align16(uint64_t x) {
+    return (uint32_t)((x + 15) & ~15ull);
+}
 
 __device__ __forceinline__ void my_tiles(int64_t ntiles, int64_t &tb, int64_t &te) {
     tb = (int64_t)blockIdx.x * ntiles / gridDim.x;
     te = ((int64_t)blockIdx.x + 1) * ntiles / gridDim.x;
 }
 
-__device__ __forceinline__ void init_barriers(uint64_t *full, uint64_t *empty) {
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), kConsumerWarps);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-}
-
-// Producer: for items 0 .. n_items-1, wait for the stage to be free, then
-// issue its copies (copy(item, dst, bar, policy) posts expect_tx + copies).
-template <class Copy>
-__device__ __forceinline__ void producer_loop(int64_t n_items, uint8_t *ring, uint64_t *full,
-                                              uint64_t *empty, unsigned *err, Copy copy) {
-    const uint64_t pol = policy_evict_first();
-    int64_t it = 0;
-    for (; it < n_items; ++it) {
-        const int s = (int)(it % kStages);
-        const uint32_t ph = (uint32_t)((it / kStages) & 1);
-        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, err)) break;
-        copy(it, smem_u32(ring + s * kStageBytes), smem_u32(&full[s]), pol);
-    }
-    // never leave while an issued copy may still be landing in shared memory
-    for (int64_t k = it > kStages ? it - kStages : 0; k < it; ++k)
-        mbar_wait(smem_u32(&full[k % kStages]), (uint32_t)((k / kStages) & 1), err);
-}
-
-__device__ __forceinline__ void consumer_release(uint64_t *empty, int s, int lane) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -85,6 +77,88 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+
+template <class T>
+__device__ __forceinline__ T ld(const T *p, bool global) {
+    return global ? __ldg(p) : *p;
+}
+__device__ __forceinline__ uint4 ld4(const void *p, bool global) {
+    return global ? __ldg(reinterpret_cast<const uint4 *>(p)) : *reinterpret_cast<const uint4 *>(p);
+}
+
+// ------------------------------------------------------------------ pipeline
+struct Ring {
+    uint8_t *smem;
+    uint64_t *full, *empty, *act;
+};
+
+__device__ __forceinline__ Ring ring_init(uint8_t *smem, uint32_t act_bytes) {
+    Ring r;
+    r.smem = smem;
+    r.full = reinterpret_cast<uint64_t *>(smem + kRingBytes + act_bytes);
+    r.empty = r.full + kStages;
+    r.act = r.empty + kStages;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&r.full[s]), 1);
+            mbar_init(smem_u32(&r.empty[s]), kConsumerWarps);
+        }
+        mbar_init(smem_u32(r.act), 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    return r;
+}
+
+// Producer: issue stage copies for items 0 .. n_items-1 (copy(item, dst, bar,
+// policy) posts expect_tx and the copies). The first kStages items need no
+// wait; `after_prefill` runs once they are in flight (it brings in the
+// activations, which depend on the previous kernel). Before returning, waits
+// (bounded) until no issued copy can still be landing in shared memory.
+template <class Copy, class After>
+__device__ __forceinline__ void producer_loop(const Ring &r, int64_t n_items, unsigned *err,
+                                              Copy copy, After after_prefill) {
+    const uint64_t pol = policy_evict_first();
+    int64_t it = 0;
+    bool after_done = false;
+    for (; it < n_items; ++it) {
+        const int s = (int)(it % kStages);
+        if (it == kStages) {
+            after_prefill();
+            after_done = true;
+        }
+        if (!mbar_wait(smem_u32(&r.empty[s]), (uint32_t)(((it / kStages) & 1) ^ 1), err)) break;
+        copy(it, smem_u32(r.smem + s * kStageBytes), smem_u32(&r.full[s]), pol);
+    }
+    if (!after_done) after_prefill();
+    for (int64_t k = it > kStages ? it - kStages : 0; k < it; ++k)
+        mbar_wait(smem_u32(&r.full[k % kStages]), (uint32_t)((k / kStages) & 1), err);
+}
+
+// Copies this launch's token rows of the planar workspace into shared memory.
+__device__ __forceinline__ void stage_activations(const Ring &r, const GemvArgs &a, int mc,
+                                                  int64_t K, int groups) {
+    pdl_wait();  // the workspace is written by the preceding quantizer kernel
+    const uint64_t pol = policy_evict_last();
+    const uint32_t bar = smem_u32(r.act);
+    const uint32_t base = smem_u32(r.smem + kRingBytes);
+    const uint32_t qs_bytes = (uint32_t)(mc * K);
+    const uint32_t bs_bytes = align16((uint64_t)mc * a.nblk * groups * 2);
+    const uint32_t d_bytes = align16((uint64_t)mc * a.nblk * 4);
+    mbar_arrive_expect_tx(bar, qs_bytes + bs_bytes + d_bytes);
+    bulk_g2s(base, a.x.qs + a.m0 * K, qs_bytes, bar, pol);
+    bulk_g2s(base + a.act_bs, a.x.sums + a.m0 * a.nblk * groups, bs_bytes, bar, pol);
+    bulk_g2s(base + a.act_d, a.x.d + a.m0 * a.nblk, d_bytes, bar, pol);
+}
+
+// ------------------------------------------------------------------ Q4_K
+// Stage = one tile (8 rows) x up to 16 super-blocks. Warp w owns row w of the
+// tile; lane (g, t) = (lane / 8, lane % 8) owns super-blocks g, g+4, g+8,
+// g+12 of the stage and, within each, qs bytes 16t .. 16t+15: chunk c = t / 2
+// half h = t % 2, i.e. 16 elements of sub-block 2c (low nibbles) and 16 of
+// 2c+1 (high nibbles). The planar activation layout puts exactly those 2 x 16
+// codes at bytes 16t and 128 + 16t of the super-block, and the two matching
+// 16-element sums in word t.
 
 // Scales and mins of sub-blocks j0 = 2 c and j1 = 2 c + 1 from the 12 packed
 // bytes (page 1, "6-bit 参数是怎么塞进 12 字节的"): j < 4 keeps them in the low
@@ -106,102 +180,133 @@ __device__ __forceinline__ void scale_min_pair(const uint4 &hdr, int c, int &s0,
     m1 = hi ? hm1 : lm1;
 }
 
-// ------------------------------------------------------------------ Q4_K
-// Stage = one tile (8 rows) x up to 16 super-blocks. Warp w owns row w of the
-// tile; lane (g, t) = (lane / 8, lane % 8) owns super-blocks g, g+4, ... of
-// the stage and, within each, qs bytes 16t .. 16t+15: chunk c = t / 2 half
-// h = t % 2, i.e. 16 elements of sub-block 2c (low nibbles) and 16 of 2c+1
-// (high nibbles).
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 2)
-    gemv_q4_K_kernel(const uint8_t *__restrict__ Wp, int64_t N, int64_t nsb, Planar x, int64_t M,
-                     int64_t m0, float *__restrict__ Y, unsigned *err) {
+template <int MT, int kMode>
+__global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
-    uint64_t *empty = full + kStages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nsb = a.nblk, K = nsb * QK_K;
+    const int mc = (int)min64(MT, a.M - a.m0);
     int64_t tb, te;
-    my_tiles(tiles_of(N), tb, te);
+    my_tiles(tiles_of(a.N), tb, te);
     const int64_t nchunks = (nsb + kQ4KChunk - 1) / kQ4KChunk;
     const int64_t n_items = (te - tb) * nchunks;
-    init_barriers(full, empty);
+    const Ring r = ring_init(smem, kMode == kDirect ? 0 : a.act_bytes);
 
     if (warp == kConsumerWarps) {
         if (lane == 0) {
-            producer_loop(n_items, smem, full, empty, err,
-                          [&](int64_t it, uint32_t dst, uint32_t bar, uint64_t pol) {
-                              const int64_t tile = tb + it / nchunks;
-                              const int64_t sb0 = (it % nchunks) * kQ4KChunk;
-                              const int cnt = (int)min64(kQ4KChunk, nsb - sb0);
-                              const uint32_t bytes = (uint32_t)cnt * kTileRows * B_Q4_K;
-                              mbar_arrive_expect_tx(bar, bytes);
-                              bulk_g2s(dst, Wp + (tile * nsb + sb0) * (kTileRows * B_Q4_K), bytes,
-                                       bar, pol);
-                          });
+            producer_loop(
+                r, n_items, a.err,
+                [&](int64_t it, uint32_t dst, uint32_t bar, uint64_t pol) {
+                    const int64_t tile = tb + it / nchunks;
+                    const int64_t sb0 = (it % nchunks) * kQ4KChunk;
+                    const uint32_t bytes =
+                        (uint32_t)min64(kQ4KChunk, nsb - sb0) * kTileRows * B_Q4_K;
+                    mbar_arrive_expect_tx(bar, bytes);
+                    bulk_g2s(dst, a.Wp + (tile * nsb + sb0) * (kTileRows * B_Q4_K), bytes, bar,
+                             pol);
+                },
+                [&]() {
+                    if (kMode == kStaged) stage_activations(r, a, mc, K, 16);
+                });
+            if (kMode == kStaged) mbar_wait(smem_u32(r.act), 0, a.err);
         }
         return;
     }
 
-    pdl_wait();  // the activations come from the preceding quantizer kernel
-    const int g = lane >> 3, t = lane & 7, c = t >> 1, h = t & 1;
-    const int mcount = (int)min64(MT, M - m0);
-    const int64_t K = nsb * QK_K;
+    // ---- activations: where this launch's token rows are read from
+    const uint8_t *act = smem + kRingBytes;
+    const bool gl = kMode == kDirect;
+    const int8_t *xqs = gl ? a.x.qs + a.m0 * K : reinterpret_cast<const int8_t *>(act);
+    const int32_t *xbs = gl ? reinterpret_cast<const int32_t *>(a.x.sums) + a.m0 * nsb * 8
+                            : reinterpret_cast<const int32_t *>(act + a.act_bs);
+    const float *xd = gl ? a.x.d + a.m0 * nsb : reinterpret_cast<const float *>(act + a.act_d);
+    if (kMode == kFused) {
+        pdl_wait();
+        uint8_t *aw = smem + kRingBytes;
+        for (int64_t b = warp; b < (int64_t)mc * nsb; b += kConsumerWarps) {
+            const int64_t rr = b / nsb, sb = b % nsb;
+            const float4 *src =
+                reinterpret_cast<const float4 *>(a.X + (a.m0 + rr) * K + sb * QK_K + 8 * lane);
+            const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            uint32_t lo, hi;
+            float d;
+            int bsum;
+            q8_K_warp(v, lo, hi, d, bsum);
+            *reinterpret_cast<uint2 *>(aw + rr * K + sb * QK_K + q8K_code_offset(lane)) =
+                make_uint2(lo, hi);
+            if ((lane & 1) == 0)
+                *reinterpret_cast<int16_t *>(aw + a.act_bs + b * 32 + q8K_bsum_offset(lane >> 1)) =
+                    (int16_t)bsum;
+            if (lane == 0) reinterpret_cast<float *>(aw + a.act_d)[b] = d;
+        }
+        consumer_sync();
+    } else if (kMode == kStaged) {
+        if (!mbar_wait(smem_u32(r.act), 0, a.err)) return;
+    } else {
+        pdl_wait();
+    }
+
+    const int g = lane >> 3, t = lane & 7, c = t >> 1;
     float acc[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
 
     for (int64_t it = 0; it < n_items; ++it) {
         const int s = (int)(it % kStages);
-        if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((it / kStages) & 1), err)) break;
+        if (!mbar_wait(smem_u32(&r.full[s]), (uint32_t)((it / kStages) & 1), a.err)) break;
         const int64_t tile = tb + it / nchunks;
         const int64_t chunk = it % nchunks;
         const int64_t sb0 = chunk * kQ4KChunk;
         const int cnt = (int)min64(kQ4KChunk, nsb - sb0);
-        const uint32_t base = smem_u32(smem + s * kStageBytes);
-        for (int sl = g; sl < cnt; sl += 4) {
-            const uint32_t blk = base + (uint32_t)(sl * kTileRows + warp) * B_Q4_K;
-            const uint4 hdr = lds128(blk);           // d, dmin, scales[12]
-            const uint4 q = lds128(blk + 16 + 16 * t);
-            int sc0, mn0, sc1, mn1;
-            scale_min_pair(hdr, c, sc0, mn0, sc1, mn1);
-            const float dw = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
-            const float dmw = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
-            const int l0 = q.x & 0x0F0F0F0F, l1 = q.y & 0x0F0F0F0F;
-            const int l2 = q.z & 0x0F0F0F0F, l3 = q.w & 0x0F0F0F0F;
-            const int h0 = (q.x >> 4) & 0x0F0F0F0F, h1 = (q.y >> 4) & 0x0F0F0F0F;
-            const int h2 = (q.z >> 4) & 0x0F0F0F0F, h3 = (q.w >> 4) & 0x0F0F0F0F;
-            const int64_t sbg = sb0 + sl;
+        const uint8_t *stage = smem + s * kStageBytes;
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (m < mcount) {
-                    const int64_t row = m0 + m;
-                    const int8_t *yp = x.qs + row * K + sbg * QK_K + 64 * c + 16 * h;
-                    const uint4 y0 = ldg_nc128(yp);       // sub-block 2c
-                    const uint4 y1 = ldg_nc128(yp + 32);  // sub-block 2c + 1
-                    int S0 = __dp4a(l0, (int)y0.x, 0);
-                    S0 = __dp4a(l1, (int)y0.y, S0);
-                    S0 = __dp4a(l2, (int)y0.z, S0);
-                    S0 = __dp4a(l3, (int)y0.w, S0);
-                    int S1 = __dp4a(h0, (int)y1.x, 0);
-                    S1 = __dp4a(h1, (int)y1.y, S1);
-                    S1 = __dp4a(h2, (int)y1.z, S1);
-                    S1 = __dp4a(h3, (int)y1.w, S1);
-                    // this lane's 16 codes of sub-block j are bsums[2j + h]
-                    const int16_t *bs = x.sums + (row * nsb + sbg) * 16 + 4 * c + h;
-                    const int isum = sc0 * S0 + sc1 * S1;
-                    const int msum = mn0 * (int)__ldg(bs) + mn1 * (int)__ldg(bs + 2);
-                    const float da = __ldg(x.d + row * nsb + sbg);
-                    acc[m] += da * (dw * (float)isum - dmw * (float)msum);
+        for (int i = 0; i < kQ4KChunk / 4; ++i) {
+            const int sl = g + 4 * i;
+            if (sl < cnt) {
+                const uint8_t *blk = stage + (sl * kTileRows + warp) * B_Q4_K;
+                const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);  // d, dmin, scales[12]
+                const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * t);
+                const int64_t sbg = sb0 + sl;
+                int sc0, mn0, sc1, mn1;
+                scale_min_pair(hdr, c, sc0, mn0, sc1, mn1);
+                const float dw = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
+                const float dmw = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+                const int l0 = q.x & 0x0F0F0F0F, l1 = q.y & 0x0F0F0F0F;
+                const int l2 = q.z & 0x0F0F0F0F, l3 = q.w & 0x0F0F0F0F;
+                const int h0 = (q.x >> 4) & 0x0F0F0F0F, h1 = (q.y >> 4) & 0x0F0F0F0F;
+                const int h2 = (q.z >> 4) & 0x0F0F0F0F, h3 = (q.w >> 4) & 0x0F0F0F0F;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m < mc) {
+                        const int8_t *yp = xqs + m * K + sbg * QK_K;
+                        const uint4 y0 = ld4(yp + 16 * t, gl);        // sub-block 2c
+                        const uint4 y1 = ld4(yp + 128 + 16 * t, gl);  // sub-block 2c + 1
+                        const int bw = ld(xbs + (m * nsb + sbg) * 8 + t, gl);
+                        const float da = ld(xd + m * nsb + sbg, gl);
+                        int S0 = __dp4a(l0, (int)y0.x, 0);
+                        S0 = __dp4a(l1, (int)y0.y, S0);
+                        S0 = __dp4a(l2, (int)y0.z, S0);
+                        S0 = __dp4a(l3, (int)y0.w, S0);
+                        int S1 = __dp4a(h0, (int)y1.x, 0);
+                        S1 = __dp4a(h1, (int)y1.y, S1);
+                        S1 = __dp4a(h2, (int)y1.z, S1);
+                        S1 = __dp4a(h3, (int)y1.w, S1);
+                        const int isum = sc0 * S0 + sc1 * S1;
+                        const int msum = mn0 * (int)(int16_t)(bw & 0xFFFF) + mn1 * (bw >> 16);
+                        acc[m] += da * (dw * (float)isum - dmw * (float)msum);
+                    }
                 }
             }
         }
-        consumer_release(empty, s, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&r.empty[s]));
         if (chunk == nchunks - 1) {
             const int64_t n = tile * kTileRows + warp;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 const float v = warp_sum(acc[m]);
-                if (lane == 0 && m < mcount && n < N) Y[(m0 + m) * N + n] = v;
+                if (lane == 0 && m < mc && n < a.N) a.Y[(a.m0 + m) * a.N + n] = v;
                 acc[m] = 0.0f;
             }
         }
@@ -212,116 +317,149 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Stage = one tile (8 rows) x up to 128 blocks. Shared layout: nibble rows
 // [8][128][16 B] at offset 0 (one bulk copy per row segment) and the fp16
 // scales [cnt][8] at offset kDOff (one copy). Warp w owns row w; lane l takes
-// blocks l, l + 32, ... so each 8-lane phase of a 128-bit load reads 128
-// contiguous bytes.
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 2)
-    gemv_q4_0_kernel(const uint8_t *__restrict__ Wp, int64_t N, int64_t nb, Planar x, int64_t M,
-                     int64_t m0, float *__restrict__ Y, unsigned *err) {
+// blocks l, l + 32, l + 64, l + 96, so each 8-lane phase of a 128-bit load
+// reads 128 contiguous bytes.
+template <int MT, int kMode>
+__global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
-    uint64_t *empty = full + kStages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nb = a.nblk, K = nb * QK4_0;
+    const int mc = (int)min64(MT, a.M - a.m0);
     int64_t tb, te;
-    my_tiles(tiles_of(N), tb, te);
+    my_tiles(tiles_of(a.N), tb, te);
     const int64_t nchunks = (nb + kQ40Chunk - 1) / kQ40Chunk;
     const int64_t n_items = (te - tb) * nchunks;
     const int64_t tile_bytes = nb * kTileRows * B_Q4_0;
     constexpr uint32_t kRowBytes = kQ40Chunk * 16;
     constexpr uint32_t kDOff = kTileRows * kRowBytes;
-    init_barriers(full, empty);
+    const Ring r = ring_init(smem, kMode == kDirect ? 0 : a.act_bytes);
 
     if (warp == kConsumerWarps) {
         if (lane == 0) {
-            producer_loop(n_items, smem, full, empty, err,
-                          [&](int64_t it, uint32_t dst, uint32_t bar, uint64_t pol) {
-                              const int64_t tile = tb + it / nchunks;
-                              const int64_t b0 = (it % nchunks) * kQ40Chunk;
-                              const uint32_t cnt = (uint32_t)min64(kQ40Chunk, nb - b0);
-                              const uint8_t *tbase = Wp + tile * tile_bytes;
-                              mbar_arrive_expect_tx(bar, cnt * kTileRows * B_Q4_0);
-                              for (int r = 0; r < kTileRows; ++r)
-                                  bulk_g2s(dst + r * kRowBytes, tbase + (r * nb + b0) * 16, cnt * 16,
-                                           bar, pol);
-                              bulk_g2s(dst + kDOff, tbase + nb * kTileRows * 16 + b0 * kTileRows * 2,
-                                       cnt * kTileRows * 2, bar, pol);
-                          });
+            producer_loop(
+                r, n_items, a.err,
+                [&](int64_t it, uint32_t dst, uint32_t bar, uint64_t pol) {
+                    const int64_t tile = tb + it / nchunks;
+                    const int64_t b0 = (it % nchunks) * kQ40Chunk;
+                    const uint32_t cnt = (uint32_t)min64(kQ40Chunk, nb - b0);
+                    const uint8_t *tbase = a.Wp + tile * tile_bytes;
+                    mbar_arrive_expect_tx(bar, cnt * kTileRows * B_Q4_0);
+                    for (int rr = 0; rr < kTileRows; ++rr)
+                        bulk_g2s(dst + rr * kRowBytes, tbase + (rr * nb + b0) * 16, cnt * 16, bar,
+                                 pol);
+                    bulk_g2s(dst + kDOff, tbase + nb * kTileRows * 16 + b0 * kTileRows * 2,
+                             cnt * kTileRows * 2, bar, pol);
+                },
+                [&]() {
+                    if (kMode == kStaged) stage_activations(r, a, mc, K, 1);
+                });
+            if (kMode == kStaged) mbar_wait(smem_u32(r.act), 0, a.err);
         }
         return;
     }
 
-    pdl_wait();
-    const int mcount = (int)min64(MT, M - m0);
-    const int64_t K = nb * QK4_0;
+    const uint8_t *act = smem + kRingBytes;
+    const bool gl = kMode == kDirect;
+    const int8_t *xqs = gl ? a.x.qs + a.m0 * K : reinterpret_cast<const int8_t *>(act);
+    const int16_t *xsum =
+        gl ? a.x.sums + a.m0 * nb : reinterpret_cast<const int16_t *>(act + a.act_bs);
+    const float *xd = gl ? a.x.d + a.m0 * nb : reinterpret_cast<const float *>(act + a.act_d);
+    if (kMode == kFused) {
+        pdl_wait();
+        uint8_t *aw = smem + kRingBytes;
+        for (int64_t b = warp; b < (int64_t)mc * nb; b += kConsumerWarps) {
+            const int64_t rr = b / nb, bb = b % nb;
+            const float x = __ldg(a.X + (a.m0 + rr) * K + bb * QK4_0 + lane);
+            int q, sum;
+            __half dh;
+            q8_0_warp(x, q, dh, sum);
+            aw[rr * K + bb * QK4_0 + lane] = (uint8_t)(int8_t)q;
+            if (lane == 0) {
+                reinterpret_cast<int16_t *>(aw + a.act_bs)[b] = (int16_t)sum;
+                reinterpret_cast<float *>(aw + a.act_d)[b] = __half2float(dh);
+            }
+        }
+        consumer_sync();
+    } else if (kMode == kStaged) {
+        if (!mbar_wait(smem_u32(r.act), 0, a.err)) return;
+    } else {
+        pdl_wait();
+    }
+
     float acc[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
 
     for (int64_t it = 0; it < n_items; ++it) {
         const int s = (int)(it % kStages);
-        if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((it / kStages) & 1), err)) break;
+        if (!mbar_wait(smem_u32(&r.full[s]), (uint32_t)((it / kStages) & 1), a.err)) break;
         const int64_t tile = tb + it / nchunks;
         const int64_t chunk = it % nchunks;
         const int64_t b0 = chunk * kQ40Chunk;
         const int cnt = (int)min64(kQ40Chunk, nb - b0);
-        const uint32_t base = smem_u32(smem + s * kStageBytes);
-        for (int bl = lane; bl < cnt; bl += 32) {
-            const uint4 q = lds128(base + warp * kRowBytes + (uint32_t)bl * 16);
-            unsigned short dbits;
-            asm volatile("ld.shared.u16 %0, [%1];"
-                         : "=h"(dbits)
-                         : "r"(base + kDOff + (uint32_t)(bl * kTileRows + warp) * 2));
-            const float dw = __half2float(__ushort_as_half(dbits));
-            const int l0 = q.x & 0x0F0F0F0F, l1 = q.y & 0x0F0F0F0F;
-            const int l2 = q.z & 0x0F0F0F0F, l3 = q.w & 0x0F0F0F0F;
-            const int h0 = (q.x >> 4) & 0x0F0F0F0F, h1 = (q.y >> 4) & 0x0F0F0F0F;
-            const int h2 = (q.z >> 4) & 0x0F0F0F0F, h3 = (q.w >> 4) & 0x0F0F0F0F;
-            const int64_t bg = b0 + bl;
+        const uint8_t *stage = smem + s * kStageBytes;
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (m < mcount) {
-                    const int64_t row = m0 + m;
-                    const int8_t *yp = x.qs + row * K + bg * QK4_0;
-                    const uint4 y0 = ldg_nc128(yp);       // elements 0..15
-                    const uint4 y1 = ldg_nc128(yp + 16);  // elements 16..31
-                    int sq = __dp4a(l0, (int)y0.x, 0);
-                    sq = __dp4a(l1, (int)y0.y, sq);
-                    sq = __dp4a(l2, (int)y0.z, sq);
-                    sq = __dp4a(l3, (int)y0.w, sq);
-                    sq = __dp4a(h0, (int)y1.x, sq);
-                    sq = __dp4a(h1, (int)y1.y, sq);
-                    sq = __dp4a(h2, (int)y1.z, sq);
-                    sq = __dp4a(h3, (int)y1.w, sq);
-                    // sum (q - 8) y = sum q y - 8 sum y, with sum y from the quantizer
-                    const int isum = sq - 8 * (int)__ldg(x.sums + row * nb + bg);
-                    const float da = __ldg(x.d + row * nb + bg);
-                    acc[m] += (dw * da) * (float)isum;
+        for (int i = 0; i < kQ40Chunk / 32; ++i) {
+            const int bl = lane + 32 * i;
+            if (bl < cnt) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(stage + warp * kRowBytes + bl * 16);
+                const unsigned short dbits = *reinterpret_cast<const unsigned short *>(
+                    stage + kDOff + (bl * kTileRows + warp) * 2);
+                const float dw = __half2float(__ushort_as_half(dbits));
+                const int l0 = q.x & 0x0F0F0F0F, l1 = q.y & 0x0F0F0F0F;
+                const int l2 = q.z & 0x0F0F0F0F, l3 = q.w & 0x0F0F0F0F;
+                const int h0 = (q.x >> 4) & 0x0F0F0F0F, h1 = (q.y >> 4) & 0x0F0F0F0F;
+                const int h2 = (q.z >> 4) & 0x0F0F0F0F, h3 = (q.w >> 4) & 0x0F0F0F0F;
+                const int64_t bg = b0 + bl;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m < mc) {
+                        const int8_t *yp = xqs + m * K + bg * QK4_0;
+                        const uint4 y0 = ld4(yp, gl);       // elements 0..15
+                        const uint4 y1 = ld4(yp + 16, gl);  // elements 16..31
+                        int sq = __dp4a(l0, (int)y0.x, 0);
+                        sq = __dp4a(l1, (int)y0.y, sq);
+                        sq = __dp4a(l2, (int)y0.z, sq);
+                        sq = __dp4a(l3, (int)y0.w, sq);
+                        sq = __dp4a(h0, (int)y1.x, sq);
+                        sq = __dp4a(h1, (int)y1.y, sq);
+                        sq = __dp4a(h2, (int)y1.z, sq);
+                        sq = __dp4a(h3, (int)y1.w, sq);
+                        // sum (q - 8) y = sum q y - 8 sum y, sum y from the quantizer
+                        const int isum = sq - 8 * (int)ld(xsum + m * nb + bg, gl);
+                        const float da = ld(xd + m * nb + bg, gl);
+                        acc[m] += (dw * da) * (float)isum;
+                    }
                 }
             }
         }
-        consumer_release(empty, s, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&r.empty[s]));
         if (chunk == nchunks - 1) {
             const int64_t n = tile * kTileRows + warp;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 const float v = warp_sum(acc[m]);
-                if (lane == 0 && m < mcount && n < N) Y[(m0 + m) * N + n] = v;
+                if (lane == 0 && m < mc && n < a.N) a.Y[(a.m0 + m) * a.N + n] = v;
                 acc[m] = 0.0f;
             }
         }
     }
 }
 
-template <class Kern>
-cudaError_t launch_one(Kern kern, int smem, int64_t ntiles, bool pdl, cudaStream_t s,
-                       const uint8_t *Wp, int64_t N, int64_t nblk, Planar x, int64_t M,
-                       int64_t m0, float *Y) {
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
+// ------------------------------------------------------------------ launch
+template <int MT, int kMode>
+cudaError_t launch_kernel(qmm_type wt, const GemvArgs &a, bool pdl, cudaStream_t s) {
+    const void *fn = wt == QMM_TYPE_Q4_K
+                         ? reinterpret_cast<const void *>(gemv_q4_K_kernel<MT, kMode>)
+                         : reinterpret_cast<const void *>(gemv_q4_0_kernel<MT, kMode>);
+    const int smem = kRingBytes + (kMode == kDirect ? 0 : (int)a.act_bytes) + kBarBytes;
+    cudaError_t e = ensure_smem_attr(fn, smem);
     if (e != cudaSuccess) return e;
+    const int64_t ntiles = tiles_of(a.N);
     const int64_t cap = 2LL * sm_count();
-    const int grid = (int)(ntiles < cap ? ntiles : cap);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = dim3((unsigned)(ntiles < cap ? ntiles : cap));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -330,41 +468,72 @@ cudaError_t launch_one(Kern kern, int smem, int64_t ntiles, bool pdl, cudaStream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    unsigned *err = device_error_word();
-    e = cudaLaunchKernelEx(&cfg, kern, Wp, N, nblk, x, M, m0, Y, err);
+    if (wt == QMM_TYPE_Q4_K)
+        e = cudaLaunchKernelEx(&cfg, gemv_q4_K_kernel<MT, kMode>, a);
+    else
+        e = cudaLaunchKernelEx(&cfg, gemv_q4_0_kernel<MT, kMode>, a);
     count_launch();
     return e;
 }
 
 template <int MT>
-cudaError_t launch_mt(qmm_type wt, const uint8_t *Wp, int64_t N, int64_t K, Planar x, int64_t M,
-                      int64_t m0, float *Y, bool pdl, cudaStream_t s) {
-    const int64_t ntiles = tiles_of(N);
-    if (wt == QMM_TYPE_Q4_K)
-        return launch_one(gemv_q4_K_kernel<MT>, kSmemBytes, ntiles, pdl, s, Wp, N, K / QK_K, x, M,
-                          m0, Y);
-    return launch_one(gemv_q4_0_kernel<MT>, kSmemBytes, ntiles, pdl, s, Wp, N, K / QK4_0, x, M,
-                      m0, Y);
+cudaError_t launch_mode(qmm_type wt, int mode, const GemvArgs &a, bool pdl, cudaStream_t s) {
+    if (mode == kFused) return launch_kernel<MT, kFused>(wt, a, pdl, s);
+    if (mode == kStaged) return launch_kernel<MT, kStaged>(wt, a, pdl, s);
+    return launch_kernel<MT, kDirect>(wt, a, pdl, s);
+}
+
+uint32_t act_layout(qmm_type wt, int64_t mt, int64_t K, uint32_t *bs_off, uint32_t *d_off) {
+    const int qk = wt == QMM_TYPE_Q4_K ? QK_K : QK4_0;
+    const int groups = wt == QMM_TYPE_Q4_K ? 16 : 1;
+    const uint32_t bs = align16((uint64_t)mt * K);
+    const uint32_t d = bs + align16((uint64_t)mt * (K / qk) * groups * 2);
+    if (bs_off) *bs_off = bs;
+    if (d_off) *d_off = d;
+    return d + align16((uint64_t)mt * (K / qk) * 4);
 }
 
 }  // namespace
 
-cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x, int64_t M,
-                        float *Y, bool pdl, cudaStream_t s) {
-    const uint8_t *w = static_cast<const uint8_t *>(Wp);
+bool gemv_can_fuse(qmm_type wt, int64_t M, int64_t K) {
+    const int64_t mt = min64(M, kMaxMT);
+    return act_layout(wt, mt, K, nullptr, nullptr) <= (uint32_t)kActMax && mt * K <= kFuseMaxElems;
+}
+
+// X != nullptr runs the quantizer fused into the GEMV prologue (X is the fp32
+// activation; the caller checked gemv_can_fuse); otherwise the activations
+// come from the planar workspace x written by launch_quantize_q8.
+cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x,
+                        const float *X, int64_t M, float *Y, bool pdl, cudaStream_t s) {
+    GemvArgs a;
+    a.Wp = static_cast<const uint8_t *>(Wp);
+    a.N = N;
+    a.nblk = K / (wt == QMM_TYPE_Q4_K ? QK_K : QK4_0);
+    a.x = x;
+    a.X = X;
+    a.M = M;
+    a.Y = Y;
+    a.err = device_error_word();
     for (int64_t m0 = 0; m0 < M; m0 += kMaxMT) {
-        const int64_t mt = M - m0 < kMaxMT ? M - m0 : kMaxMT;
+        const int64_t mt = min64(M - m0, kMaxMT);
+        a.m0 = m0;
+        a.act_bytes = act_layout(wt, mt, K, &a.act_bs, &a.act_d);
+        int mode = kDirect;
+        if (X)
+            mode = kFused;
+        else if (a.act_bytes <= (uint32_t)kActMax)
+            mode = kStaged;
         cudaError_t e;
         if (mt == 1)
-            e = launch_mt<1>(wt, w, N, K, x, M, m0, Y, pdl, s);
+            e = launch_mode<1>(wt, mode, a, pdl, s);
         else if (mt == 2)
-            e = launch_mt<2>(wt, w, N, K, x, M, m0, Y, pdl, s);
+            e = launch_mode<2>(wt, mode, a, pdl, s);
         else if (mt <= 4)
-            e = launch_mt<4>(wt, w, N, K, x, M, m0, Y, pdl, s);
+            e = launch_mode<4>(wt, mode, a, pdl, s);
         else if (mt <= 8)
-            e = launch_mt<8>(wt, w, N, K, x, M, m0, Y, pdl, s);
+            e = launch_mode<8>(wt, mode, a, pdl, s);
         else
-            e = launch_mt<16>(wt, w, N, K, x, M, m0, Y, pdl, s);
+            e = launch_mode<16>(wt, mode, a, pdl, s);
         if (e != cudaSuccess) return e;
         pdl = false;  // only the first launch follows the quantizer directly
     }

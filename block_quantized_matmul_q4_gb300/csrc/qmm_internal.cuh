@@ -30,9 +30,17 @@ __host__ __device__ inline int64_t tiles_of(int64_t N) { return (N + kTileRows -
 
 // Private quantized-activation layout ("planar"), written by the quantizer
 // for the mul_mat kernels:
-//   qs   : int8  [M][K]          codes, rows 16-byte aligned (K % 32 == 0)
+//   qs   : int8  [M][K]          codes, rows 16-byte aligned (K % 32 == 0).
+//                                Q8_0: natural order. Q8_K: each super-block's
+//                                256 codes permuted for the GEMV lanes (see
+//                                q8K_code_offset): bytes 16t..16t+15 hold
+//                                elements 64c + 16h + 0..15 and bytes
+//                                128 + 16t .. hold 64c + 32 + 16h + 0..15,
+//                                with c = t / 2, h = t % 2 (t = 0..7).
 //   d    : float [M][K/QK]       block scales (Q8_0: the fp16 scale widened)
-//   sums : int16 [M][K/QK][G]    Q8_K: G = 16 sums of 16 codes (bsums);
+//   sums : int16 [M][K/QK][G]    Q8_K: G = 16 sums of 16 codes (bsums),
+//                                stored as 8 words, word t = bs[4c + h] in
+//                                the low and bs[4c + 2 + h] in the high half;
 //                                Q8_0: G = 1, the sum of the block's 32 codes
 struct Planar {
     int8_t *qs;
@@ -54,6 +62,7 @@ __host__ __device__ inline size_t planar_bytes(int64_t M, int64_t K, int qk, Pla
     off = align_up(off + (size_t)M * nb * sizeof(float), 256);
     size_t o_s = off;
     off = align_up(off + (size_t)M * nb * g * sizeof(int16_t), 256);
+    off += 256;  // slack: bulk copies round their sizes up to 16 bytes
     if (p) {
         p->qs = (int8_t *)(base + o_qs);
         p->d = (float *)(base + o_d);
@@ -170,6 +179,72 @@ __device__ __forceinline__ float round_half_away(float v) {
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return min(max(v, lo), hi); }
 
+// ------------------------------------------------------------------ activation quantization
+// Shared by the stand-alone quantizer kernels and the quantizer fused into the
+// GEMV prologue, so both produce identical codes. Page 1 ("最基础的两块",
+// "更低的比特"): symmetric int8 per block, d = amax / 127, q = round-half-away
+// of x * (1/d) clamped to +-127, in IEEE fp32 with explicit rounding.
+
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+    // v >= +0 (no -0, no NaN): the IEEE bit patterns order like the values
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
+}
+
+__device__ __forceinline__ int q8_code(float x, float id) {
+    return clampi((int)round_half_away(__fmul_rn(x, id)), -127, 127);
+}
+
+// Q8_0 block held one element per lane: code, scale (fp32 value of the fp16
+// scale that is stored), and the block's code sum (all lanes).
+__device__ __forceinline__ void q8_0_warp(float x, int &q, __half &dh, int &sum) {
+    const float amax = warp_max_nonneg(fabsf(x));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+    q = q8_code(x, id);
+    dh = __float2half_rn(d);
+    sum = __reduce_add_sync(0xffffffffu, q);
+}
+
+// Q8_K super-block held 8 elements per lane (lane l: elements 8l .. 8l+7):
+// the lane's codes packed little-endian in (lo, hi), the fp32 scale d, and
+// the sum of codes 16 (l/2) .. 16 (l/2) + 15 (valid on every lane).
+__device__ __forceinline__ void q8_K_warp(const float v[8], uint32_t &lo, uint32_t &hi, float &d,
+                                          int &bsum) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+    const float amax = warp_max_nonneg(a);
+    d = __fdiv_rn(amax, 127.0f);
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+    lo = 0;
+    hi = 0;
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int q = q8_code(v[i], id);
+        s += q;
+        if (i < 4)
+            lo |= (uint32_t)(q & 0xFF) << (8 * i);
+        else
+            hi |= (uint32_t)(q & 0xFF) << (8 * (i - 4));
+    }
+    bsum = s + __shfl_xor_sync(0xffffffffu, s, 1);
+}
+
+// Byte offset, inside the planar layout's 256-byte super-block, of the 8 codes
+// lane l computed (elements 8l .. 8l+7).
+__host__ __device__ __forceinline__ int q8K_code_offset(int lane) {
+    const int c = lane >> 3, j = lane & 7;
+    const int part = j >> 2, rr = (j & 3) * 8;
+    return part * 128 + 16 * (2 * c + (rr >> 4)) + (rr & 15);
+}
+
+// Byte offset, inside the planar layout's 32-byte bsum group, of bsum b.
+__host__ __device__ __forceinline__ int q8K_bsum_offset(int b) {
+    const int c = b >> 2, w = b & 3;
+    return 4 * (2 * c + (w & 1)) + 2 * (w >> 1);
+}
+
 }  // namespace qmm
 
 // ------------------------------------------------------------------ host side
@@ -190,8 +265,10 @@ cudaError_t launch_quantize_weights(qmm_type wt, const float *W, void *Wq, int64
                                     cudaStream_t s);
 cudaError_t launch_repack(qmm_type wt, bool inverse, const void *src, void *dst, int64_t N,
                           int64_t K, cudaStream_t s);
-cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x, int64_t M,
-                        float *Y, bool pdl, cudaStream_t s);
+// X != nullptr: fused quantizer (requires gemv_can_fuse(wt, M, K)).
+cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x,
+                        const float *X, int64_t M, float *Y, bool pdl, cudaStream_t s);
+bool gemv_can_fuse(qmm_type wt, int64_t M, int64_t K);
 cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
                                     const void *Xq, int64_t M, int32_t *out, cudaStream_t s);
 }  // namespace qmm

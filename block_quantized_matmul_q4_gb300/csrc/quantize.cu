@@ -19,11 +19,6 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ float warp_max_nonneg(float v) {
-    // v >= +0 (no -0, no NaN): the IEEE bit patterns order like the values
-    return __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(v)));
-}
-
 __device__ __forceinline__ float group_min(float v, int width) {
     for (int o = 1; o < width; o <<= 1) v = fminf(v, __shfl_xor_sync(kFull, v, o));
     return v;
@@ -31,11 +26,6 @@ __device__ __forceinline__ float group_min(float v, int width) {
 __device__ __forceinline__ float group_max(float v, int width) {
     for (int o = 1; o < width; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
     return v;
-}
-
-// Code of one activation: round-half-away(x * id) clamped to [-127, 127].
-__device__ __forceinline__ int q8_code(float x, float id) {
-    return clampi((int)round_half_away(__fmul_rn(x, id)), -127, 127);
 }
 
 // ---------------------------------------------------------------- Q8_0
@@ -50,14 +40,11 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float *__restr
     for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
          b += nwarps) {
         const float x = X[b * 32 + lane];
-        const float amax = warp_max_nonneg(fabsf(x));
-        const float d = __fdiv_rn(amax, 127.0f);
-        const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
-        const int q = q8_code(x, id);
-        const __half dh = __float2half_rn(d);
+        int q, s;
+        __half dh;
+        q8_0_warp(x, q, dh, s);
         if (kPlanar) {
             p.qs[b * 32 + lane] = (int8_t)q;
-            const int s = __reduce_add_sync(kFull, q);
             if (lane == 0) {
                 p.d[b] = __half2float(dh);
                 p.sums[b] = (int16_t)s;
@@ -84,27 +71,16 @@ __global__ void __launch_bounds__(256) quantize_q8_K_kernel(const float *__restr
         const float4 *src = reinterpret_cast<const float4 *>(X + b * 256 + 8 * lane);
         const float4 v0 = src[0], v1 = src[1];
         const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
-        const float amax = warp_max_nonneg(a);
-        const float d = __fdiv_rn(amax, 127.0f);
-        const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
-        uint32_t lo = 0, hi = 0;
-        int s = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int q = q8_code(v[i], id);
-            s += q;
-            if (i < 4)
-                lo |= (uint32_t)(q & 0xFF) << (8 * i);
-            else
-                hi |= (uint32_t)(q & 0xFF) << (8 * (i - 4));
-        }
-        s += __shfl_xor_sync(kFull, s, 1);  // lanes 2t, 2t+1 cover codes 16t .. 16t+15
+        uint32_t lo, hi;
+        float d;
+        int s;
+        q8_K_warp(v, lo, hi, d, s);
         if (kPlanar) {
-            *reinterpret_cast<uint2 *>(p.qs + b * 256 + 8 * lane) = make_uint2(lo, hi);
-            if ((lane & 1) == 0) p.sums[b * 16 + (lane >> 1)] = (int16_t)s;
+            // lane-permuted private layout (see Planar)
+            *reinterpret_cast<uint2 *>(p.qs + b * 256 + q8K_code_offset(lane)) = make_uint2(lo, hi);
+            if ((lane & 1) == 0)
+                *reinterpret_cast<int16_t *>(reinterpret_cast<uint8_t *>(p.sums + b * 16) +
+                                             q8K_bsum_offset(lane >> 1)) = (int16_t)s;
             if (lane == 0) p.d[b] = d;
         } else {
             uint8_t *blk = out + b * B_Q8_K;

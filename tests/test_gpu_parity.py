@@ -145,6 +145,32 @@ def test_mul_mat_against_oracle(q, orc, wt, N, K, M):
     check_close(ref["y32"], ref["y64"], ref["den"], "oracle fp32")
 
 
+@pytest.mark.parametrize("wt,N,K,M", [(1, 40, 4096, 1), (1, 40, 4096, 4), (1, 24, 8192, 8),
+                                      (1, 16, 4096, 16), (0, 40, 1024, 1), (0, 24, 4096, 16)])
+def test_mul_mat_prepared(q, orc, wt, N, K, M):
+    """The two halves (quantize into a workspace, GEMV on it): activations
+    bulk-copied into shared memory when they fit, read in place otherwise."""
+    w = wl.weights(13, N, K, 0.02, row_offset_std=0.005).numpy()
+    x = wl.activations(13, M, K).numpy()
+    Wc = orc.quantize(wt, w)
+    Wp = q.empty_packed(wt, N, K)
+    q.qmm_repack_weights(wt, dev(Wc), Wp, N, K)
+    ws_bytes = q.qmm_workspace_bytes(wt, M, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    q.qmm_quantize_activations(wt, dev(x), M, K, ws, ws_bytes)
+    Y1 = torch.empty(M, N, device="cuda")
+    Y2 = torch.empty(M, N, device="cuda")
+    q.qmm_mul_mat_prepared(wt, Wp, N, K, ws, ws_bytes, M, Y1)
+    q.qmm_mul_mat_prepared(wt, Wp, N, K, ws, ws_bytes, M, Y2)  # workspace is read-only
+    ref = orc.mul_mat(wt, Wc, N, K, x)
+    check_close(host(Y1), ref["y64"], ref["den"], f"prepared wt={wt} K={K} M={M}")
+    assert torch.equal(Y1, Y2)
+    # the one-call path gives the same codes, so the same fp32 sums per row
+    Y3 = torch.empty(M, N, device="cuda")
+    q.qmm_mul_mat_ws(wt, Wp, N, K, dev(x), M, Y3, ws, ws_bytes)
+    check_close(host(Y3), ref["y64"], ref["den"], f"one-call wt={wt} K={K} M={M}")
+
+
 def test_mul_mat_edge_inputs(q, orc):
     for wt, K in ((0, 256), (1, 256)):
         w = edge_rows(K, 11)
@@ -199,6 +225,9 @@ def test_q4_K_4096_graph_launch(q, orc):
     Y = torch.zeros(L.N, device="cuda")
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
+    q.qmm_mul_mat_ws(1, Wp, L.N, L.K, x, 1, Y, ws, ws_bytes, s)  # warm-up before capture
+    torch.cuda.synchronize()
+    Y.zero_()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         q.qmm_mul_mat_ws(1, Wp, L.N, L.K, x, 1, Y, ws, ws_bytes)
@@ -206,6 +235,7 @@ def test_q4_K_4096_graph_launch(q, orc):
         g.replay()
     torch.cuda.synchronize()
     rows = np.r_[0:8, 1000:1008, L.N - 8:L.N]
+    assert torch.isfinite(Y).all()
     Wc = host(Wq).reshape(L.N, -1)
     assert np.array_equal(Wc[rows], orc.quantize(1, w[torch.as_tensor(rows, device="cuda")].cpu().numpy()))
     ref = orc.mul_mat(1, Wc, L.N, L.K, x.cpu().numpy(), rows=rows)
