@@ -6,7 +6,7 @@
 
 #include <atomic>
 #include <mutex>
-#include <set>
+#include <map>
 #include <utility>
 
 #include "qmm_internal.cuh"
@@ -23,7 +23,7 @@ std::mutex g_mutex;
 unsigned *g_err_ptr[kMaxDevices] = {nullptr};
 int g_sms[kMaxDevices] = {0};
 bool g_pool_ready[kMaxDevices] = {false};
-std::set<std::pair<const void *, int>> g_smem_ok;
+std::map<std::pair<const void *, int>, int> g_smem_set;  // (kernel, device) -> bytes
 std::atomic<uint64_t> g_launches{0};
 thread_local char g_msg[512] = "";
 
@@ -58,9 +58,10 @@ int sm_count() {
 cudaError_t ensure_smem_attr(const void *kernel, int bytes) {
     const int d = current_device();
     std::lock_guard<std::mutex> lk(g_mutex);
-    if (g_smem_ok.count({kernel, d})) return cudaSuccess;
+    auto it = g_smem_set.find({kernel, d});
+    if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) g_smem_ok.insert({kernel, d});
+    if (e == cudaSuccess) g_smem_set[{kernel, d}] = bytes;
     return e;
 }
 
@@ -264,6 +265,9 @@ qmm_status qmm_mul_mat_ws(qmm_type wt, const void *W_packed, int64_t N, int64_t 
     if (st != QMM_OK) return st;
     if (M == 0 || N == 0) return ok();
     QMM_CHECK_ARG(workspace && aligned(workspace, 16), "workspace must be non-null, 16-byte aligned");
+    const size_t need = qmm_workspace_bytes(wt, M, K);
+    if (ws_bytes < need)
+        return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
     return mul_mat_impl(wt, W_packed, N, K, X, M, Y, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
@@ -297,9 +301,11 @@ qmm_status qmm_mul_mat(qmm_type wt, const void *W_packed, int64_t N, int64_t K, 
     qmm_status st = check_mul_mat_args(wt, W_packed, N, K, X, M, Y);
     if (st != QMM_OK) return st;
     if (M == 0 || N == 0) return ok();
+    cudaStream_t s = (cudaStream_t)stream;
+    if (gemv_can_fuse(wt, M, K))  // one kernel, no workspace to allocate
+        return mul_mat_impl(wt, W_packed, N, K, X, M, Y, nullptr, 0, s);
     prepare_pool();
     const size_t need = qmm_workspace_bytes(wt, M, K);
-    cudaStream_t s = (cudaStream_t)stream;
     void *ws = nullptr;
     cudaError_t e = cudaMallocAsync(&ws, need, s);
     if (e != cudaSuccess || !ws) {

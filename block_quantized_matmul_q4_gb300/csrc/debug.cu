@@ -35,7 +35,8 @@ __global__ void block_sums_q4_K_kernel(const uint8_t *__restrict__ Wp, int64_t N
         const int64_t sb = i % nsb, n = (i / nsb) % N, m = i / (nsb * N);
         const uint8_t *blk =
             Wp + (((n / kTileRows) * nsb + sb) * kTileRows + n % kTileRows) * B_Q4_K;
-        const uint8_t *sc = blk + 4;
+        int sj[8], mj[8];
+        k4_scales_canonical(k4_header_to_canonical(*reinterpret_cast<const uint4 *>(blk)), sj, mj);
         const uint8_t *qs = blk + 16;
         const uint8_t *yb = Xq + (m * nsb + sb) * B_Q8_K;
         const int8_t *y = reinterpret_cast<const int8_t *>(yb + 4);
@@ -52,16 +53,8 @@ __global__ void block_sums_q4_K_kernel(const uint8_t *__restrict__ Wp, int64_t N
         }
         int32_t isum = 0, msum = 0;
         for (int j = 0; j < 8; ++j) {
-            int s, mm;
-            if (j < 4) {
-                s = sc[j] & 63;
-                mm = sc[j + 4] & 63;
-            } else {
-                s = (sc[j + 4] & 0x0F) | ((sc[j - 4] >> 6) << 4);
-                mm = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
-            }
-            isum += s * S[j];
-            msum += mm * (bs[2 * j] + bs[2 * j + 1]);
+            isum += sj[j] * S[j];
+            msum += mj[j] * (bs[2 * j] + bs[2 * j + 1]);
         }
         int32_t *o = out + i * 10;
         for (int j = 0; j < 8; ++j) o[j] = S[j];

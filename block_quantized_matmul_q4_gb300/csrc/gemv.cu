@@ -36,14 +36,16 @@ constexpr int kThreads = kConsumerThreads + 32;
 constexpr int kStages = 4;
 constexpr int kStageBytes = 18432;
 constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kQ4KChunk = 16;   // super-blocks per stage: 16 * 8 rows * 144 B = 18432
+constexpr int kQ4KChunk = 8;    // super-blocks per stage and tile: 2 tiles * 8 * 8 * 144 B = 18432
+constexpr int kHalfStage = kQ4KChunk * kTileRows * B_Q4_K;  // one tile's share of a stage
 constexpr int kQ40Chunk = 128;  // blocks per stage: 128 * 8 rows * 18 B = 18432
-constexpr int kBarBytes = 64;   // full[4], empty[4], act
+constexpr int kBarBytes = (2 * kStages + 1) * 8;  // full[4], empty[4], act
 constexpr int kMaxMT = 16;
 constexpr int kActMax = 36 * 1024;        // shared memory for staged activations
-constexpr int64_t kFuseMaxElems = 32768;  // fused quantizer up to M*K fp32 elements
-static_assert(kQ4KChunk * kTileRows * B_Q4_K == kStageBytes, "stage size");
+constexpr int64_t kFuseMaxElems = 8192;  // fused quantizer up to M*K fp32 elements
+static_assert(2 * kHalfStage == kStageBytes, "stage size");
 static_assert(kQ40Chunk * kTileRows * B_Q4_0 == kStageBytes, "stage size");
+static_assert(kBarBytes == 72, "barrier area must hold 2 * kStages + 1 mbarriers");
 
 enum Mode { kDirect = 0, kStaged = 1, kFused = 2 };
 
@@ -105,6 +107,9 @@ __device__ __forceinline__ Ring ring_init(uint8_t *smem, uint32_t act_bytes) {
         }
         mbar_init(smem_u32(r.act), 1);
         fence_barrier_init();
+        // The next kernel in the stream may launch now: it only streams
+        // weights until its griddepcontrol.wait, which waits for this grid.
+        pdl_launch_dependents();
     }
     __syncthreads();
     return r;
@@ -152,32 +157,51 @@ __device__ __forceinline__ void stage_activations(const Ring &r, const GemvArgs 
 }
 
 // ------------------------------------------------------------------ Q4_K
-// Stage = one tile (8 rows) x up to 16 super-blocks. Warp w owns row w of the
-// tile; lane (g, t) = (lane / 8, lane % 8) owns super-blocks g, g+4, g+8,
-// g+12 of the stage and, within each, qs bytes 16t .. 16t+15: chunk c = t / 2
-// half h = t % 2, i.e. 16 elements of sub-block 2c (low nibbles) and 16 of
-// 2c+1 (high nibbles). The planar activation layout puts exactly those 2 x 16
-// codes at bytes 16t and 128 + 16t of the super-block, and the two matching
-// 16-element sums in word t.
+// Stage = a pair of tiles (rows 16p .. 16p+15) x up to 8 super-blocks: tile
+// 2p's blocks [sb][8 rows][144 B] at offset 0, tile 2p+1's at kHalfStage (one
+// bulk copy each). Warp w owns row w of both tiles, so every activation value
+// it loads serves two weight rows. Lane (g, t) = (lane / 8, lane % 8) owns
+// super-blocks g and g + 4 of the stage and, within each, qs bytes 16t ..
+// 16t+15: chunk c = t / 2, half h = t % 2, i.e. 16 elements of sub-block 2c
+// (low nibbles) and 16 of sub-block 2c+1 (high nibbles). The planar
+// activation layout puts exactly those 2 x 16 codes at bytes 16t and
+// 128 + 16t of the super-block and the two matching 16-code sums in word t;
+// the packed header puts the lane's two scales and mins in 24-bit field c.
 
-// Scales and mins of sub-blocks j0 = 2 c and j1 = 2 c + 1 from the 12 packed
-// bytes (page 1, "6-bit 参数是怎么塞进 12 字节的"): j < 4 keeps them in the low
-// 6 bits of bytes j and j + 4; j >= 4 splits them into the nibbles of byte
-// j + 4 and the top 2 bits of bytes j - 4 (scale) and j (min).
-__device__ __forceinline__ void scale_min_pair(const uint4 &hdr, int c, int &s0, int &m0,
-                                               int &s1, int &m1) {
-    const int sh = 8 * ((2 * c) & 3);
-    const uint32_t y = hdr.y >> sh, z = hdr.z >> sh, w = hdr.w >> sh;
-    const int ls0 = y & 63, lm0 = z & 63, ls1 = (y >> 8) & 63, lm1 = (z >> 8) & 63;
-    const int hs0 = (w & 15) | (((y >> 6) & 3) << 4);
-    const int hm0 = ((w >> 4) & 15) | (((z >> 6) & 3) << 4);
-    const int hs1 = ((w >> 8) & 15) | (((y >> 14) & 3) << 4);
-    const int hm1 = ((w >> 12) & 15) | (((z >> 14) & 3) << 4);
-    const bool hi = c >= 2;
-    s0 = hi ? hs0 : ls0;
-    m0 = hi ? hm0 : lm0;
-    s1 = hi ? hs1 : ls1;
-    m1 = hi ? hm1 : lm1;
+// dp4a with an unsigned first operand: bytes of a are 0..255.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+struct KLane {
+    bool c_ge2, c_ge3;  // which header words hold field c
+    uint32_t fsh;       // bit offset of field c within them
+};
+
+// One (row, super-block) share of this lane: d_a (d isum - dmin msum) over
+// its 16 + 16 elements (page 1, "正确性" and "min 项与最终归约").
+__device__ __forceinline__ float q4k_dot(const uint4 &hdr, const uint4 &q, const uint4 &y0,
+                                         const uint4 &y1, int bw, float da, const KLane &L) {
+    const uint32_t f =
+        __funnelshift_r(L.c_ge3 ? hdr.w : (L.c_ge2 ? hdr.z : hdr.y), L.c_ge2 ? hdr.w : hdr.z, L.fsh);
+    const int sc0 = f & 63, mn0 = (f >> 6) & 63;
+    const int sc1 = (f >> 12) & 63, mn1 = (f >> 18) & 63;
+    const float dw = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
+    const float dmw = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+    // low nibbles as bytes; high nibbles left in place, giving 16 x their sum
+    int s0 = dp4a_us(q.x & 0x0F0F0F0Fu, y0.x, 0);
+    int s0b = dp4a_us(q.y & 0x0F0F0F0Fu, y0.y, 0);
+    s0 = dp4a_us(q.z & 0x0F0F0F0Fu, y0.z, s0);
+    s0b = dp4a_us(q.w & 0x0F0F0F0Fu, y0.w, s0b);
+    int s1 = dp4a_us(q.x & 0xF0F0F0F0u, y1.x, 0);
+    int s1b = dp4a_us(q.y & 0xF0F0F0F0u, y1.y, 0);
+    s1 = dp4a_us(q.z & 0xF0F0F0F0u, y1.z, s1);
+    s1b = dp4a_us(q.w & 0xF0F0F0F0u, y1.w, s1b);
+    const int isum = sc0 * (s0 + s0b) + sc1 * ((s1 + s1b) >> 4);
+    const int msum = mn0 * (int)(int16_t)(bw & 0xFFFF) + mn1 * (bw >> 16);
+    return da * (dw * (float)isum - dmw * (float)msum);
 }
 
 template <int MT, int kMode>
@@ -186,10 +210,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nsb = a.nblk, K = nsb * QK_K;
     const int mc = (int)min64(MT, a.M - a.m0);
-    int64_t tb, te;
-    my_tiles(tiles_of(a.N), tb, te);
+    const int64_t ntiles = tiles_of(a.N);
+    int64_t pb, pe;
+    my_tiles((ntiles + 1) / 2, pb, pe);  // this CTA's tile pairs
     const int64_t nchunks = (nsb + kQ4KChunk - 1) / kQ4KChunk;
-    const int64_t n_items = (te - tb) * nchunks;
+    const int64_t n_items = (pe - pb) * nchunks;
     const Ring r = ring_init(smem, kMode == kDirect ? 0 : a.act_bytes);
 
     if (warp == kConsumerWarps) {
@@ -197,13 +222,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
             producer_loop(
                 r, n_items, a.err,
                 [&](int64_t it, uint32_t dst, uint32_t bar, uint64_t pol) {
-                    const int64_t tile = tb + it / nchunks;
+                    const int64_t t0 = 2 * (pb + it / nchunks);
                     const int64_t sb0 = (it % nchunks) * kQ4KChunk;
                     const uint32_t bytes =
                         (uint32_t)min64(kQ4KChunk, nsb - sb0) * kTileRows * B_Q4_K;
-                    mbar_arrive_expect_tx(bar, bytes);
-                    bulk_g2s(dst, a.Wp + (tile * nsb + sb0) * (kTileRows * B_Q4_K), bytes, bar,
-                             pol);
+                    const bool has1 = t0 + 1 < ntiles;
+                    mbar_arrive_expect_tx(bar, has1 ? 2 * bytes : bytes);
+                    bulk_g2s(dst, a.Wp + (t0 * nsb + sb0) * (kTileRows * B_Q4_K), bytes, bar, pol);
+                    if (has1)
+                        bulk_g2s(dst + kHalfStage, a.Wp + ((t0 + 1) * nsb + sb0) * (kTileRows * B_Q4_K),
+                                 bytes, bar, pol);
                 },
                 [&]() {
                     if (kMode == kStaged) stage_activations(r, a, mc, K, 16);
@@ -248,66 +276,60 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
     }
 
     const int g = lane >> 3, t = lane & 7, c = t >> 1;
-    float acc[MT];
+    const KLane L{c >= 2, c >= 3, (uint32_t)((24 * c) & 31)};
+    float acc0[MT], acc1[MT];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+    for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = 0.0f;
 
     for (int64_t it = 0; it < n_items; ++it) {
         const int s = (int)(it % kStages);
         if (!mbar_wait(smem_u32(&r.full[s]), (uint32_t)((it / kStages) & 1), a.err)) break;
-        const int64_t tile = tb + it / nchunks;
+        const int64_t t0 = 2 * (pb + it / nchunks);
         const int64_t chunk = it % nchunks;
         const int64_t sb0 = chunk * kQ4KChunk;
         const int cnt = (int)min64(kQ4KChunk, nsb - sb0);
         const uint8_t *stage = smem + s * kStageBytes;
+        // super-block sl of the stage: both rows of this warp, all tokens
+        auto body = [&](int sl) {
+            const uint8_t *ba = stage + (sl * kTileRows + warp) * B_Q4_K;
+            const uint4 ha = *reinterpret_cast<const uint4 *>(ba);
+            const uint4 qa = *reinterpret_cast<const uint4 *>(ba + 16 + 16 * t);
+            const uint4 hb = *reinterpret_cast<const uint4 *>(ba + kHalfStage);
+            const uint4 qb = *reinterpret_cast<const uint4 *>(ba + kHalfStage + 16 + 16 * t);
+            const int64_t sbg = sb0 + sl;
 #pragma unroll
-        for (int i = 0; i < kQ4KChunk / 4; ++i) {
-            const int sl = g + 4 * i;
-            if (sl < cnt) {
-                const uint8_t *blk = stage + (sl * kTileRows + warp) * B_Q4_K;
-                const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);  // d, dmin, scales[12]
-                const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * t);
-                const int64_t sbg = sb0 + sl;
-                int sc0, mn0, sc1, mn1;
-                scale_min_pair(hdr, c, sc0, mn0, sc1, mn1);
-                const float dw = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
-                const float dmw = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
-                const int l0 = q.x & 0x0F0F0F0F, l1 = q.y & 0x0F0F0F0F;
-                const int l2 = q.z & 0x0F0F0F0F, l3 = q.w & 0x0F0F0F0F;
-                const int h0 = (q.x >> 4) & 0x0F0F0F0F, h1 = (q.y >> 4) & 0x0F0F0F0F;
-                const int h2 = (q.z >> 4) & 0x0F0F0F0F, h3 = (q.w >> 4) & 0x0F0F0F0F;
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (m < mc) {
-                        const int8_t *yp = xqs + m * K + sbg * QK_K;
-                        const uint4 y0 = ld4(yp + 16 * t, gl);        // sub-block 2c
-                        const uint4 y1 = ld4(yp + 128 + 16 * t, gl);  // sub-block 2c + 1
-                        const int bw = ld(xbs + (m * nsb + sbg) * 8 + t, gl);
-                        const float da = ld(xd + m * nsb + sbg, gl);
-                        int S0 = __dp4a(l0, (int)y0.x, 0);
-                        S0 = __dp4a(l1, (int)y0.y, S0);
-                        S0 = __dp4a(l2, (int)y0.z, S0);
-                        S0 = __dp4a(l3, (int)y0.w, S0);
-                        int S1 = __dp4a(h0, (int)y1.x, 0);
-                        S1 = __dp4a(h1, (int)y1.y, S1);
-                        S1 = __dp4a(h2, (int)y1.z, S1);
-                        S1 = __dp4a(h3, (int)y1.w, S1);
-                        const int isum = sc0 * S0 + sc1 * S1;
-                        const int msum = mn0 * (int)(int16_t)(bw & 0xFFFF) + mn1 * (bw >> 16);
-                        acc[m] += da * (dw * (float)isum - dmw * (float)msum);
-                    }
+            for (int m = 0; m < MT; ++m) {
+                if (m < mc) {
+                    const int8_t *yp = xqs + m * K + sbg * QK_K;
+                    const uint4 y0 = ld4(yp + 16 * t, gl);        // sub-block 2c
+                    const uint4 y1 = ld4(yp + 128 + 16 * t, gl);  // sub-block 2c + 1
+                    const int bw = ld(xbs + (m * nsb + sbg) * 8 + t, gl);
+                    const float da = ld(xd + m * nsb + sbg, gl);
+                    acc0[m] += q4k_dot(ha, qa, y0, y1, bw, da, L);
+                    acc1[m] += q4k_dot(hb, qb, y0, y1, bw, da, L);
                 }
             }
+        };
+        if (cnt == kQ4KChunk) {
+            body(g);
+            body(g + 4);
+        } else {
+            if (g < cnt) body(g);
+            if (g + 4 < cnt) body(g + 4);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&r.empty[s]));
         if (chunk == nchunks - 1) {
-            const int64_t n = tile * kTileRows + warp;
+            const int64_t n0 = t0 * kTileRows + warp, n1 = n0 + kTileRows;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                const float v = warp_sum(acc[m]);
-                if (lane == 0 && m < mc && n < a.N) a.Y[(a.m0 + m) * a.N + n] = v;
-                acc[m] = 0.0f;
+                const float v0 = warp_sum(acc0[m]);
+                const float v1 = warp_sum(acc1[m]);
+                if (lane == 0 && m < mc) {
+                    if (n0 < a.N) a.Y[(a.m0 + m) * a.N + n0] = v0;
+                    if (n1 < a.N) a.Y[(a.m0 + m) * a.N + n1] = v1;
+                }
+                acc0[m] = acc1[m] = 0.0f;
             }
         }
     }
@@ -406,10 +428,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
                 const unsigned short dbits = *reinterpret_cast<const unsigned short *>(
                     stage + kDOff + (bl * kTileRows + warp) * 2);
                 const float dw = __half2float(__ushort_as_half(dbits));
-                const int l0 = q.x & 0x0F0F0F0F, l1 = q.y & 0x0F0F0F0F;
-                const int l2 = q.z & 0x0F0F0F0F, l3 = q.w & 0x0F0F0F0F;
-                const int h0 = (q.x >> 4) & 0x0F0F0F0F, h1 = (q.y >> 4) & 0x0F0F0F0F;
-                const int h2 = (q.z >> 4) & 0x0F0F0F0F, h3 = (q.w >> 4) & 0x0F0F0F0F;
+                const uint32_t l0 = q.x & 0x0F0F0F0Fu, l1 = q.y & 0x0F0F0F0Fu;
+                const uint32_t l2 = q.z & 0x0F0F0F0Fu, l3 = q.w & 0x0F0F0F0Fu;
+                const uint32_t h0 = q.x & 0xF0F0F0F0u, h1 = q.y & 0xF0F0F0F0u;
+                const uint32_t h2 = q.z & 0xF0F0F0F0u, h3 = q.w & 0xF0F0F0F0u;
                 const int64_t bg = b0 + bl;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
@@ -417,16 +439,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
                         const int8_t *yp = xqs + m * K + bg * QK4_0;
                         const uint4 y0 = ld4(yp, gl);       // elements 0..15
                         const uint4 y1 = ld4(yp + 16, gl);  // elements 16..31
-                        int sq = __dp4a(l0, (int)y0.x, 0);
-                        sq = __dp4a(l1, (int)y0.y, sq);
-                        sq = __dp4a(l2, (int)y0.z, sq);
-                        sq = __dp4a(l3, (int)y0.w, sq);
-                        sq = __dp4a(h0, (int)y1.x, sq);
-                        sq = __dp4a(h1, (int)y1.y, sq);
-                        sq = __dp4a(h2, (int)y1.z, sq);
-                        sq = __dp4a(h3, (int)y1.w, sq);
+                        int sl = dp4a_us(l0, y0.x, 0);
+                        sl = dp4a_us(l1, y0.y, sl);
+                        sl = dp4a_us(l2, y0.z, sl);
+                        sl = dp4a_us(l3, y0.w, sl);
+                        int sh16 = dp4a_us(h0, y1.x, 0);  // 16 x the high-nibble sum
+                        sh16 = dp4a_us(h1, y1.y, sh16);
+                        sh16 = dp4a_us(h2, y1.z, sh16);
+                        sh16 = dp4a_us(h3, y1.w, sh16);
                         // sum (q - 8) y = sum q y - 8 sum y, sum y from the quantizer
-                        const int isum = sq - 8 * (int)ld(xsum + m * nb + bg, gl);
+                        const int isum =
+                            sl + (sh16 >> 4) - 8 * (int)ld(xsum + m * nb + bg, gl);
                         const float da = ld(xd + m * nb + bg, gl);
                         acc[m] += (dw * da) * (float)isum;
                     }
@@ -456,10 +479,11 @@ cudaError_t launch_kernel(qmm_type wt, const GemvArgs &a, bool pdl, cudaStream_t
     const int smem = kRingBytes + (kMode == kDirect ? 0 : (int)a.act_bytes) + kBarBytes;
     cudaError_t e = ensure_smem_attr(fn, smem);
     if (e != cudaSuccess) return e;
-    const int64_t ntiles = tiles_of(a.N);
+    // Q4_K CTAs work on pairs of tiles, Q4_0 CTAs on single tiles
+    const int64_t units = wt == QMM_TYPE_Q4_K ? (tiles_of(a.N) + 1) / 2 : tiles_of(a.N);
     const int64_t cap = 2LL * sm_count();
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(ntiles < cap ? ntiles : cap));
+    cfg.gridDim = dim3((unsigned)(units < cap ? units : cap));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

@@ -21,7 +21,8 @@ constexpr int B_Q8_K = 292;
 // Packed weight layout: rows grouped in tiles of kTileRows. Within a tile,
 // the blocks of one K position are adjacent, so a (tile, K-range) is one
 // contiguous byte range that a single bulk copy moves:
-//   Q4_K: tile t = [nsb][kTileRows][144 B]   (canonical block bytes)
+//   Q4_K: tile t = [nsb][kTileRows][144 B]   (canonical block bytes, except
+//         the 12 scale bytes, see k4_header_to_packed)
 //   Q4_0: tile t = [kTileRows][nb][16 B nibbles] then [nb][kTileRows] fp16 d
 //         (a (tile, K-range) is then 8 row segments plus one scale segment)
 constexpr int kTileRows = 8;
@@ -69,6 +70,83 @@ __host__ __device__ inline size_t planar_bytes(int64_t M, int64_t K, int qk, Pla
         p->sums = (int16_t *)(base + o_s);
     }
     return off;
+}
+
+// Q4_K block header (first 16 bytes: fp16 d, fp16 dmin, 12 bytes of scales).
+// Canonical scale bytes follow the page's 6-bit packing ("6-bit 参数是怎么塞进
+// 12 字节的"). The packed layout keeps the same 96 bits of information in an
+// order one GEMV lane can read in a few operations: four 24-bit fields, field
+// c at bit 24c of the little-endian 96-bit value, each
+//   s_{2c} | m_{2c} << 6 | s_{2c+1} << 12 | m_{2c+1} << 18.
+__host__ __device__ inline void k4_scales_canonical(const uint4 &h, int s[8], int m[8]) {
+    uint8_t q[12];
+    for (int i = 0; i < 4; ++i) {
+        q[i] = (uint8_t)(h.y >> (8 * i));
+        q[4 + i] = (uint8_t)(h.z >> (8 * i));
+        q[8 + i] = (uint8_t)(h.w >> (8 * i));
+    }
+    for (int j = 0; j < 8; ++j) {
+        if (j < 4) {
+            s[j] = q[j] & 63;
+            m[j] = q[j + 4] & 63;
+        } else {
+            s[j] = (q[j + 4] & 0x0F) | ((q[j - 4] >> 6) << 4);
+            m[j] = (q[j + 4] >> 4) | ((q[j] >> 6) << 4);
+        }
+    }
+}
+
+__host__ __device__ inline uint4 k4_header_to_packed(const uint4 &h) {
+    int s[8], m[8];
+    k4_scales_canonical(h, s, m);
+    uint64_t lo = 0;
+    uint32_t hi = 0;
+    for (int c = 0; c < 4; ++c) {
+        const uint64_t f = (uint64_t)(s[2 * c] | (m[2 * c] << 6) | (s[2 * c + 1] << 12) |
+                                      (m[2 * c + 1] << 18));
+        if (c < 2) {
+            lo |= f << (24 * c);
+        } else if (c == 2) {
+            lo |= f << 48;
+            hi |= (uint32_t)(f >> 16);
+        } else {
+            hi |= (uint32_t)(f << 8);
+        }
+    }
+    return make_uint4(h.x, (uint32_t)lo, (uint32_t)(lo >> 32), hi);
+}
+
+// Field c (24 bits) of a packed header; w1..w3 are its scale words.
+__host__ __device__ __forceinline__ uint32_t k4_field(uint32_t w1, uint32_t w2, uint32_t w3, int c) {
+    const uint64_t v = c < 2 ? ((uint64_t)w2 << 32 | w1) : ((uint64_t)w3 << 32 | w2);
+    const int sh = c < 2 ? 24 * c : 24 * c - 32;
+    return (uint32_t)(v >> sh) & 0xFFFFFFu;
+}
+
+__host__ __device__ inline uint4 k4_header_to_canonical(const uint4 &h) {
+    uint8_t q[12] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t f = k4_field(h.y, h.z, h.w, c);
+        const int sv[2] = {(int)(f & 63), (int)((f >> 12) & 63)};
+        const int mv[2] = {(int)((f >> 6) & 63), (int)((f >> 18) & 63)};
+        for (int e = 0; e < 2; ++e) {
+            const int j = 2 * c + e;
+            if (j < 4) {
+                q[j] |= (uint8_t)sv[e];
+                q[j + 4] |= (uint8_t)mv[e];
+            } else {
+                q[j + 4] = (uint8_t)((sv[e] & 15) | ((mv[e] & 15) << 4));
+                q[j - 4] |= (uint8_t)((sv[e] >> 4) << 6);
+                q[j] |= (uint8_t)((mv[e] >> 4) << 6);
+            }
+        }
+    }
+    uint4 o;
+    o.x = h.x;
+    o.y = q[0] | (q[1] << 8) | (q[2] << 16) | ((uint32_t)q[3] << 24);
+    o.z = q[4] | (q[5] << 8) | (q[6] << 16) | ((uint32_t)q[7] << 24);
+    o.w = q[8] | (q[9] << 8) | (q[10] << 16) | ((uint32_t)q[11] << 24);
+    return o;
 }
 
 // ------------------------------------------------------------------ errors

@@ -6,6 +6,8 @@
 // It is a pure byte permutation:
 //   Q4_K: canonical [N][nsb][144 B] -> tiles of 8 rows, [T][nsb][8][144 B].
 //         One (tile, super-block range) is then one contiguous byte range.
+//         The 12 scale bytes are re-ordered into four 24-bit lane fields
+//         (k4_header_to_packed), the same 96 bits in another order.
 //   Q4_0: canonical [N][nb][18 B]   -> per tile [8][nb][16 B nibbles] followed
 //         by [nb][8] fp16 scales, so the nibbles are 16-byte aligned (the
 //         18-byte block defeats 128-bit loads).
@@ -32,9 +34,13 @@ __global__ void repack_q4_K_kernel(const uint4 *__restrict__ src, uint4 *__restr
         const int64_t n = tile * kTileRows + rem % kTileRows;
         const int64_t cblk = n * nsb + sb;  // canonical block index
         if (!kInverse) {
-            dst[i] = n < N ? src[cblk * 9 + chunk] : make_uint4(0, 0, 0, 0);
+            uint4 v = n < N ? src[cblk * 9 + chunk] : make_uint4(0, 0, 0, 0);
+            if (chunk == 0) v = k4_header_to_packed(v);
+            dst[i] = v;
         } else if (n < N) {
-            dst[cblk * 9 + chunk] = src[i];
+            uint4 v = src[i];
+            if (chunk == 0) v = k4_header_to_canonical(v);
+            dst[cblk * 9 + chunk] = v;
         }
     }
 }

@@ -142,11 +142,13 @@ qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon
  * the same stream, then every output is
  *   Q4_0: sum_b fp16(d_w) fp16(d_a) sum_{i<32} (q_i - 8) y_i
  *   Q4_K: sum_sb d_a (d * sum_j s_j sum_i q_i y_i - dmin * sum_j m_j sum_i y_i)
- * with integer block sums and fp32 accumulation across blocks. M <= 16 runs
- * the decode GEMV kernels; larger M the prefill GEMM.
- * W_packed comes from qmm_repack_weights. The quantized activations live in a
- * workspace that the library allocates stream-ordered (cudaMallocAsync) and
- * frees after the call, in the same stream.
+ * with integer block sums and fp32 accumulation across blocks. Tokens are
+ * processed 16 at a time by the decode GEMV kernels. When M*K is small (one
+ * 16-token group of at most 8192 elements) the activation quantizer runs
+ * inside the GEMV kernel (one launch, no workspace); otherwise the quantized activations go to a workspace that the
+ * library allocates stream-ordered (cudaMallocAsync) and frees after the
+ * call, in the same stream.
+ * W_packed comes from qmm_repack_weights.
  * Errors: QMM_ERR_ARG (type, sizes, null/misaligned pointers),
  * QMM_ERR_NOMEM (workspace allocation failed), QMM_ERR_CUDA (launch failed).
  * M == 0 or N == 0 is a no-op. */
