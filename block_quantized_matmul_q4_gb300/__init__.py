@@ -47,6 +47,7 @@ _SIGS = {
     "qmm_mul_mat_ws": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _sz, _vp]),
     "qmm_quantize_activations": (_i32, [_i32, _vp, _i64, _i64, _vp, _sz, _vp]),
     "qmm_mul_mat_prepared": (_i32, [_i32, _vp, _i64, _i64, _vp, _sz, _i64, _vp, _vp]),
+    "qmm_mul_mat_static": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_debug_block_sums": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_status_string": (ctypes.c_char_p, [_i32]),
     "qmm_last_error": (ctypes.c_char_p, []),
@@ -151,6 +152,14 @@ def qmm_mul_mat_prepared(wt: int, W_packed, N: int, K: int, workspace, ws_bytes:
     _check("qmm_mul_mat_prepared",
            _lib.qmm_mul_mat_prepared(wt, _ptr(W_packed), N, K, _ptr(workspace), ws_bytes, M,
                                      _ptr(Y), _stream(stream)))
+
+
+def qmm_mul_mat_static(wt: int, W_packed, N: int, K: int, X, M: int, Y, stream=None):
+    """qmm_mul_mat without any allocation: the activation scratch is a fixed
+    4 MiB device array inside libqmm (see include/qmm.h)."""
+    _check("qmm_mul_mat_static",
+           _lib.qmm_mul_mat_static(wt, _ptr(W_packed), N, K, _ptr(X), M, _ptr(Y),
+                                   _stream(stream)))
 
 
 def qmm_debug_block_sums(wt: int, W_packed, N: int, K: int, Xq, M: int, out, stream=None):

@@ -181,6 +181,29 @@ qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, in
                                 const void *workspace, size_t ws_bytes, int64_t M, float *Y,
                                 qmm_stream_t stream);
 
+/* qmm_mul_mat for callers that cannot allocate device memory. The pages have
+ * no counterpart: this is a deployment variant of the same computation.
+ * Some callers may not allocate once they are running: a serving loop whose
+ * allocator is frozen after start-up, a host runtime that gives this library
+ * no allocator to draw from, or a latency-critical step that must never block
+ * in cudaMalloc/cudaFree. This call allocates nothing: the quantized
+ * activations go to a fixed 4 MiB device array inside libqmm (reserved on
+ * every GPU that loads the library, until the process exits), then the same
+ * decode GEMV as qmm_mul_mat runs on them. The caller still owns and passes
+ * X, W_packed and Y (same layouts, alignment and errors as qmm_mul_mat).
+ *   - Limit: qmm_workspace_bytes(wt, M, K) must be <= 4 MiB (about M*K <= 3.6
+ *     million elements); larger requests return QMM_ERR_WORKSPACE and launch
+ *     nothing.
+ *   - The first call on a device looks up the array's device address (once,
+ *     with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero. Calls whose GPU work overlaps
+ *     (different streams, or graphs replayed concurrently) race on it: order
+ *     them on one stream or use qmm_mul_mat_ws with separate workspaces. */
+qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
+                              const float *X, int64_t M, float *Y, qmm_stream_t stream);
+
 /* Per-block integer sums of the factored form, for bit-exact checking
  * (page 1, "正确性" and "通用实现"). Xq holds canonical activation blocks
  * (Q8_0 for Q4_0 weights, Q8_K for Q4_K), M rows.
