@@ -122,6 +122,15 @@ void prepare_pool() {
     g_pool_ready[d] = true;
 }
 
+// Q4_K with more than 16 tokens runs the tensor-core GEMM and its workspace
+// layout; everything else the decode GEMV and the planar layout.
+bool use_gemm(qmm_type wt, int64_t M) { return wt == QMM_TYPE_Q4_K && M >= kGemmMinM; }
+
+size_t ws_bytes_for(qmm_type wt, int64_t M, int64_t K) {
+    return use_gemm(wt, M) ? prefill_bytes(M, K, nullptr, nullptr)
+                           : planar_bytes(M, K, elems(wt), nullptr, nullptr);
+}
+
 qmm_status carve(qmm_type wt, int64_t M, int64_t K, const void *ws, size_t ws_bytes, Planar *p) {
     const size_t need = planar_bytes(M, K, elems(wt), p, (uint8_t *)ws);
     if (ws_bytes < need)
@@ -131,6 +140,13 @@ qmm_status carve(qmm_type wt, int64_t M, int64_t K, const void *ws, size_t ws_by
 
 qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K, void *ws,
                               size_t ws_bytes, cudaStream_t s) {
+    if (use_gemm(wt, M)) {
+        PrefillWs pw;
+        const size_t need = prefill_bytes(M, K, &pw, (uint8_t *)ws);
+        if (ws_bytes < need)
+            return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+        return cuda_status(launch_quantize_prefill(X, pw, M, K, s), "prefill quantizer launch");
+    }
     Planar p;
     qmm_status st = carve(wt, M, K, ws, ws_bytes, &p);
     if (st != QMM_OK) return st;
@@ -140,6 +156,13 @@ qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K,
 
 qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, const void *ws,
                          size_t ws_bytes, int64_t M, float *Y, cudaStream_t s) {
+    if (use_gemm(wt, M)) {
+        PrefillWs pw;
+        const size_t need = prefill_bytes(M, K, &pw, (uint8_t *)ws);
+        if (ws_bytes < need)
+            return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+        return cuda_status(launch_gemm_q4_K(Wp, N, K, pw, M, Y, s), "prefill GEMM launch");
+    }
     Planar p;
     qmm_status st = carve(wt, M, K, ws, ws_bytes, &p);
     if (st != QMM_OK) return st;
@@ -201,7 +224,7 @@ size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K) {
 
 size_t qmm_workspace_bytes(qmm_type wt, int64_t M, int64_t K) {
     if (!is_weight(wt) || M < 0 || K <= 0 || K % elems(wt)) return 0;
-    return planar_bytes(M, K, elems(wt), nullptr, nullptr);
+    return ws_bytes_for(wt, M, K);
 }
 
 qmm_status qmm_quantize_row_q8(qmm_type vt, const float *X, void *Xq, int64_t M, int64_t K,

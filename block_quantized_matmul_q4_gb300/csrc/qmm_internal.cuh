@@ -51,6 +51,18 @@ struct Planar {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Prefill (GEMM) activation layout for Q4_K weights, written by the prefill
+// quantizer: Q8_K codes as exact fp16 [M][K] (the MMA operand, loaded by
+// TMA), 16-code sums as fp16 [M][K/256 * 16] (exact: |sum| <= 2032), block
+// scales as fp32 [K/256][M] (token-contiguous for the epilogue).
+struct PrefillWs {
+    __half *y16;
+    __half *bs16;
+    float *daT;
+};
+// Tokens per call above which Q4_K mul_mat runs the tensor-core GEMM.
+constexpr int64_t kGemmMinM = 17;
+
 // Workspace carve-up for M rows of K activations with block size qk.
 __host__ __device__ inline size_t planar_bytes(int64_t M, int64_t K, int qk, Planar *p,
                                                uint8_t *base) {
@@ -347,6 +359,11 @@ cudaError_t launch_repack(qmm_type wt, bool inverse, const void *src, void *dst,
 cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x,
                         const float *X, int64_t M, float *Y, bool pdl, cudaStream_t s);
 bool gemv_can_fuse(qmm_type wt, int64_t M, int64_t K);
+size_t prefill_bytes(int64_t M, int64_t K, PrefillWs *p, uint8_t *base);
+cudaError_t launch_quantize_prefill(const float *X, PrefillWs p, int64_t M, int64_t K,
+                                    cudaStream_t s);
+cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, int64_t M,
+                             float *Y, cudaStream_t s);
 cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
                                     const void *Xq, int64_t M, int32_t *out, cudaStream_t s);
 }  // namespace qmm

@@ -1,0 +1,76 @@
+"""GPU parity of the prefill path (Q4_K weights, M > 16 tokens): the prefill
+quantizer and the tcgen05 GEMM, through the C ABI, against the oracle.
+Bar: |Y_gpu - Y_fp64| <= 1e-3 * sum_k |w_k a_k| per element."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def q():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_quantized_matmul_q4_gb300 as q
+    return q
+
+
+def check(y, ref, den, what):
+    err = np.abs(y.astype(np.float64) - ref)
+    assert np.all(np.isfinite(y)), f"{what}: non-finite"
+    bad = err > TOL * den + 1e-30
+    assert not bad.any(), f"{what}: {bad.sum()} off, worst {np.max(err / np.maximum(den, 1e-30)):.3e}"
+
+
+def packed(q, orc, w, N, K):
+    Wc = orc.quantize(q.QMM_TYPE_Q4_K, w, nthreads=orc.default_threads())
+    Wp = q.empty_packed(q.QMM_TYPE_Q4_K, N, K)
+    q.qmm_repack_weights(q.QMM_TYPE_Q4_K, torch.from_numpy(Wc).cuda(), Wp, N, K)
+    return Wc, Wp
+
+
+@pytest.mark.parametrize("N,K,M", [(128, 256, 17), (200, 512, 300), (384, 1024, 256),
+                                   (136, 2304, 129), (64, 256, 64)])
+def test_prefill_gemm_small(q, orc, N, K, M):
+    w = wl.weights(30, N, K, 0.02, row_offset_std=0.005).numpy()
+    x = wl.activations(30, M, K).numpy()
+    Wc, Wp = packed(q, orc, w, N, K)
+    Y = torch.full((M * N + 64,), float("nan"), device="cuda")
+    Y[M * N:] = 777.0
+    q.qmm_mul_mat(q.QMM_TYPE_Q4_K, Wp, N, K, torch.from_numpy(x).cuda(), M, Y)
+    q.qmm_check_device_error()
+    y = Y.cpu().numpy()
+    assert np.all(y[M * N:] == 777.0), "write past the end of Y"
+    ref = orc.mul_mat(q.QMM_TYPE_Q4_K, Wc, N, K, x, nthreads=orc.default_threads())
+    check(y[:M * N].reshape(M, N), ref["y64"], ref["den"], f"N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("shape", wl.PREFILL_SHAPES, ids=lambda L: L.name)
+@pytest.mark.parametrize("M", wl.PREFILL_M)
+def test_prefill_full_size_sampled(q, orc, shape, M):
+    """Prefill shapes at full size (M in {512, 2048}, 11008x4096 and
+    4096x11008), weights quantized on the GPU; sampled rows checked against
+    the oracle, which quantizes those rows itself from the same fp32."""
+    L = shape
+    w = wl.weights(31, L.N, L.K, L.wstd, row_offset_std=L.row_offset_std, device="cuda")
+    x = wl.activations(31, M, L.K, device="cuda")
+    Wq = q.empty_blocks(q.QMM_TYPE_Q4_K, L.N, L.K)
+    q.qmm_quantize_weights(q.QMM_TYPE_Q4_K, w, Wq, L.N, L.K)
+    Wp = q.empty_packed(q.QMM_TYPE_Q4_K, L.N, L.K)
+    q.qmm_repack_weights(q.QMM_TYPE_Q4_K, Wq, Wp, L.N, L.K)
+    Y = torch.empty(M, L.N, device="cuda")
+    q.qmm_mul_mat(q.QMM_TYPE_Q4_K, Wp, L.N, L.K, x, M, Y)
+    q.qmm_check_device_error()
+    rows = np.unique(np.r_[0:3, 127:130, L.N - 3:L.N, np.linspace(0, L.N - 1, 24).astype(np.int64)])
+    w_rows = w[torch.as_tensor(rows, device="cuda")].cpu().numpy()
+    Wc_rows = orc.quantize(q.QMM_TYPE_Q4_K, w_rows)
+    assert np.array_equal(Wq.view(L.N, -1)[torch.as_tensor(rows, device="cuda")].cpu().numpy(),
+                          Wc_rows)
+    ref = orc.mul_mat(q.QMM_TYPE_Q4_K, Wc_rows, len(rows), L.K, x.cpu().numpy(),
+                      nthreads=orc.default_threads())
+    check(Y[:, torch.as_tensor(rows, device="cuda")].cpu().numpy(), ref["y64"], ref["den"],
+          f"{L.name} M={M}")
