@@ -332,8 +332,56 @@ def gemv_rate(q, dev, stream, wt, N, K, M, seed, L=None, steps=6400, copies=None
     return t, b
 
 
-def gpu_extras(q, dev, stream, args):
+def prefill_rate(q, dev, stream, L, M, seed, reps=6, graph_steps=4):
+    """Prefill mul_mat (prefill quantizer + tcgen05 GEMM) on one shape: us per
+    call and TOPS (2 M N K integer multiply-adds per call), plus the GEMM
+    alone on prepared activations."""
+    wt = q.QMM_TYPE_Q4_K
+    N, K = L.N, L.K
+    w = wl.weights(seed, N, K, L.wstd, row_offset_std=L.row_offset_std, device=dev)
+    Wq = q.empty_blocks(wt, N, K)
+    q.qmm_quantize_weights(wt, w, Wq, N, K)
+    del w
+    Wp = q.empty_packed(wt, N, K)
+    q.qmm_repack_weights(wt, Wq, Wp, N, K)
+    del Wq
+    X = wl.activations(seed, M, K, device=dev)
+    ws_bytes = q.qmm_workspace_bytes(wt, M, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    Y = torch.empty(M, N, device=dev)
+    step = lambda i: q.qmm_mul_mat_ws(wt, Wp, N, K, X, M, Y, ws, ws_bytes, stream)
+    gemm = lambda i: q.qmm_mul_mat_prepared(wt, Wp, N, K, ws, ws_bytes, M, Y, stream)
+    for i in range(2):
+        step(i)
+    g1 = capture(step, graph_steps, stream)
+    g2 = capture(gemm, graph_steps, stream)
+    with torch.cuda.stream(stream):
+        g1.replay()
+        g2.replay()
+    t1 = timed(stream, lambda: run_graphs(g1, None, reps)) / (reps * graph_steps)
+    t2 = timed(stream, lambda: run_graphs(g2, None, reps)) / (reps * graph_steps)
+    ops = 2.0 * M * N * K
+    return {"us": round(t1 * 1e6, 2), "TOPS": round(ops / t1 / 1e12, 1),
+            "gemm_us": round(t2 * 1e6, 2), "gemm_TOPS": round(ops / t2 / 1e12, 1)}
+
+
+def prefill_extras(q, dev, stream):
+    peaks = load_peaks()
     out = {}
+    for L in wl.PREFILL_SHAPES:
+        for M in wl.PREFILL_M:
+            r = prefill_rate(q, dev, stream, L, M, 31)
+            r["frac_of_fp16_peak"] = round(r["gemm_TOPS"] / peaks["bf16_tflops"], 4)
+            out[f"{L.name}_M{M}"] = r
+            torch.cuda.empty_cache()
+    out["peak"] = {"value": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                   "note": "measured bf16 dense GEMM peak; kind::f16 with fp16 operands has "
+                           "the same nominal rate"}
+    return out
+
+
+def gpu_extras(q, dev, stream, args):
+    out = {"prefill_q4_K": prefill_extras(q, dev, stream)}
     # M sweep of the headline GEMV
     sweep = {}
     L = wl.GEMV_Q4_K_4096
@@ -416,6 +464,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--case", choices=["decode", "prefill"], default="decode",
+                    help="prefill: only the prefill measurement (for profiler captures)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -447,6 +497,11 @@ def main():
         torch.distributed.init_process_group("nccl")
     else:
         torch.cuda.set_device(0)
+    if args.case == "prefill":
+        import block_quantized_matmul_q4_gb300 as q
+        print(json.dumps(prefill_extras(q, torch.device("cuda", torch.cuda.current_device()),
+                                        torch.cuda.Stream())), flush=True)
+        return
     res = gpu_arm(args, rank, world)
     if rank == 0:
         cpu, _ = cpu_arm(args.cpu_seconds)

@@ -18,13 +18,18 @@
 //               (one per 8-row packed tile) and 2-D TMA tiles of the fp16 codes
 //               (128B swizzle) and the fp16 bsums (32B swizzle);
 //   warp 1      MMA issuer (one thread) and TMEM owner (512 columns);
-//   warps 2..5  converters: one weight row per thread, nibbles x s_j -> fp16
-//               written in the K-major 128B-swizzled layout the MMA reads (the
-//               page-3 "decode in registers, feed the MMA" idea, with the
-//               operand staged in shared memory as tcgen05 requires), plus
-//               the row's mins for the bsum MMA;
-//   warps 6..13 epilogue: tcgen05.ld both accumulators, y += d_a (d A -
-//               dmin B) into 64 fp32 registers per thread, final store.
+//   warps 2..9  converters, two sets of four: one weight row per thread (its
+//               TMEM lane), set 0 takes K-chunks 0 and 2 of a super-block,
+//               set 1 chunks 1 and 3. Nibbles x s_j -> fp16 in registers,
+//               stored straight into a TMEM operand ring with tcgen05.st (the
+//               page-3 "decode in registers, feed the MMA" idea; the expanded
+//               weights never touch shared memory). Set 0 also writes the
+//               row's mins for the bsum MMA and its d, dmin;
+//   warps 10..25 epilogue: tcgen05.ld both accumulators, y += d_a (d A -
+//               dmin B) into 32 fp32 registers per thread, final store. The
+//               per-super-block scales come from a small shared-memory ring:
+//               d_a by TMA from the workspace, d and dmin from the converters
+//               (who read those block headers anyway).
 // All mbarrier waits are bounded; on a timeout the CTA drains its copies and
 // MMAs, frees its TMEM and returns with the device error word set.
 #include <mutex>
@@ -39,41 +44,41 @@ constexpr int kBN = 128;  // tokens per CTA (MMA N)
 constexpr int kBK = 64;   // K per operand chunk: one 128-byte swizzle row of fp16
 constexpr int kChunksPerSB = QK_K / kBK;  // 4
 constexpr int kAStages = 4, kBStages = 4, kMStages = 2, kRawStages = 2;
-constexpr int kChunkBytes = kBM * kBK * 2;  // 16 KB (A) ; B: kBN * kBK * 2 = 16 KB
+constexpr int kChunkBytes = kBN * kBK * 2;  // 16 KB activation tile
 constexpr int kMinBytes = kBM * 16 * 2;     // 4 KB per min operand (K = 16)
 constexpr int kRawBytes = (kBM / kTileRows) * kTileRows * B_Q4_K;  // 18432
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kAStages * kChunkBytes;
+constexpr int kOffB = 0;
 constexpr int kOffM = kOffB + kBStages * kChunkBytes;
 constexpr int kOffRaw = kOffM + kMStages * 2 * kMinBytes;
-constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
-constexpr int kNumBars = 2 * (kRawStages + kAStages + kBStages + kMStages + 2) + 1;
+constexpr int kScBytes = kBN * 4 + 2 * kBM * 4;  // d_a[128], d[128], dmin[128]
+constexpr int kOffSc = kOffRaw + kRawStages * kRawBytes;
+constexpr int kOffBar = kOffSc + 2 * kScBytes;
+constexpr int kNumBars = 2 * (kRawStages + kAStages + kBStages + kMStages + 2 + 2) + 2;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot + alignment
-constexpr int kThreads = 14 * 32;
-constexpr uint32_t kTmemCols = 512;  // A acc x2, B acc x2, kBN columns each
-static_assert(kBN == kBM, "TMEM and operand buffers assume square tiles");
-static_assert(4 * kBN <= (int)kTmemCols, "TMEM budget");
+constexpr int kConvWarps = 8, kEpiWarps = 16;
+constexpr int kThreads = (2 + kConvWarps + kEpiWarps) * 32;
+constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // columns per epilogue thread
+// TMEM columns: A accumulators (x2), the bsum accumulator, the A operand ring
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColAccA = 0, kColAccB = 2 * kBN, kColARing = 3 * kBN;
+constexpr uint32_t kARingCols = kBK / 2;  // two fp16 per 32-bit column
+static_assert(kColARing + kAStages * kARingCols <= kTmemCols, "TMEM budget");
+static_assert(kBN == kBM, "square tiles");
 
 struct GemmArgs {
     const uint8_t *Wp;  // packed Q4_K weights
     int64_t N, nsb, M;
-    const float *daT;  // [nsb][M] activation scales
-    float *Y;          // [M][N]
+    float *Y;  // [M][N]
     unsigned *err;
 };
 
 struct Bars {
     uint64_t *raw_full, *raw_empty, *a_full, *a_empty, *b_full, *b_empty, *m_full, *m_empty,
-        *acc_full, *acc_empty, *done;
+        *acc_full, *acc_empty, *sc_full, *sc_empty, *bacc_empty, *done;
 };
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
 // (x & mask) | 0x64006400: two fp16 values 1024 + field
 __device__ __forceinline__ uint32_t magic(uint32_t x, uint32_t mask) {
     uint32_t d;
@@ -81,23 +86,40 @@ __device__ __forceinline__ uint32_t magic(uint32_t x, uint32_t mask) {
     return d;
 }
 
-// Eight fp16 values s * q from 8 nibbles of one byte set: bytes of (w0, w1),
-// low nibbles (hi = false) or high nibbles (hi = true). mul/add are the
-// per-half scale terms: low: (s, -1024 s); high: (s/16, -64 s).
-__device__ __forceinline__ uint4 expand8(uint32_t w0, uint32_t w1, bool hi, __half2 mul,
-                                         __half2 add) {
-    const uint32_t mask = hi ? 0x00F000F0u : 0x000F000Fu;
-    uint4 o;
-    o.x = h2_bits(__hfma2(bits_h2(magic(prmt(w0, 0, 0x4140), mask)), mul, add));
-    o.y = h2_bits(__hfma2(bits_h2(magic(prmt(w0, 0, 0x4342), mask)), mul, add));
-    o.z = h2_bits(__hfma2(bits_h2(magic(prmt(w1, 0, 0x4140), mask)), mul, add));
-    o.w = h2_bits(__hfma2(bits_h2(magic(prmt(w1, 0, 0x4342), mask)), mul, add));
-    return o;
+// fp16 values s * q from the nibbles of one 32-bit word of qs (bytes b0..b3;
+// low nibbles are elements k0..k3 of a sub-block, high nibbles the same
+// positions of the next sub-block). A nibble at bits 0-3 or 4-7 of a 16-bit
+// half, or'ed into 0x6400 (1024.0, one unit in the last place), reads as
+// 1024 + q or 1024 + 16 q; one fused fp16 FMA with (s, -1024 s) or
+// (s / 16, -64 s) leaves q s exactly (an integer <= 945). Bytes b0, b2 sit at
+// bits 0 and 16 of w, bytes b1, b3 at bits 0 and 16 of w >> 8, so the halves
+// come out as the pairs (k0, k2), (k1, k3): the activation codes are stored
+// with elements 1 and 2 of every group of 4 swapped to match, which leaves
+// the dot product unchanged.
+struct ScaleLH {
+    __half2 ml, al, mh, ah;  // low nibbles: s_lo, -1024 s_lo; high: s_hi / 16, -64 s_hi
+};
+__device__ __forceinline__ ScaleLH make_scales(float s_lo, float s_hi) {
+    ScaleLH c;
+    c.ml = __float2half2_rn(s_lo);
+    c.al = __float2half2_rn(-1024.0f * s_lo);
+    c.mh = __float2half2_rn(s_hi * 0.0625f);
+    c.ah = __float2half2_rn(-64.0f * s_hi);
+    return c;
+}
+__device__ __forceinline__ void expand_word(uint32_t w, const ScaleLH &c, uint32_t &l02,
+                                            uint32_t &l13, uint32_t &h02, uint32_t &h13) {
+    const uint32_t v = w >> 8;
+    l02 = h2_bits(__hfma2(bits_h2(magic(w, 0x000F000Fu)), c.ml, c.al));
+    l13 = h2_bits(__hfma2(bits_h2(magic(v, 0x000F000Fu)), c.ml, c.al));
+    h02 = h2_bits(__hfma2(bits_h2(magic(w, 0x00F000F0u)), c.mh, c.ah));
+    h13 = h2_bits(__hfma2(bits_h2(magic(v, 0x00F000F0u)), c.mh, c.ah));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_q4_K_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmap_y,
-                     const __grid_constant__ CUtensorMap tmap_bs) {
+                     const __grid_constant__ CUtensorMap tmap_bs,
+                     const __grid_constant__ CUtensorMap tmap_da) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the 128B-swizzled tiles
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -122,13 +144,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     B.m_empty = B.m_full + kMStages;
     B.acc_full = B.m_empty + kMStages;
     B.acc_empty = B.acc_full + 2;
-    B.done = B.acc_empty + 2;
+    B.sc_full = B.acc_empty + 2;
+    B.sc_empty = B.sc_full + 2;
+    B.bacc_empty = B.sc_empty + 2;
+    B.done = B.bacc_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(B.done + 1);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kRawStages; ++i) {
             mbar_init(smem_u32(&B.raw_full[i]), 1);
-            mbar_init(smem_u32(&B.raw_empty[i]), 4);
+            mbar_init(smem_u32(&B.raw_empty[i]), kConvWarps);
         }
         for (int i = 0; i < kAStages; ++i) {
             mbar_init(smem_u32(&B.a_full[i]), 4);
@@ -144,8 +169,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&B.acc_full[i]), 1);
-            mbar_init(smem_u32(&B.acc_empty[i]), 8);
+            mbar_init(smem_u32(&B.acc_empty[i]), kEpiWarps);
+            mbar_init(smem_u32(&B.sc_full[i]), 1 + 4);
+            mbar_init(smem_u32(&B.sc_empty[i]), kEpiWarps);
         }
+        mbar_init(smem_u32(B.bacc_empty), kEpiWarps);
         mbar_init(smem_u32(B.done), 1);
         fence_barrier_init();
     }
@@ -160,9 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tc::prefetch_tensormap(&tmap_y);
             tc::prefetch_tensormap(&tmap_bs);
+            tc::prefetch_tensormap(&tmap_da);
             const uint64_t pol = policy_evict_last();  // weights and codes are reused by other CTAs
             pdl_wait();  // the codes come from the preceding quantizer kernel
-            int64_t issued_raw = 0, issued_b = 0, issued_m = 0;
+            int64_t issued_raw = 0, issued_b = 0, issued_m = 0, issued_sc = 0;
             bool ok = true;
             for (int64_t sb = 0; sb < nsb && ok; ++sb) {
                 const int rs = (int)(sb % kRawStages);
@@ -195,6 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tma_load_2d(smem_u32(smem + kOffM + ms * 2 * kMinBytes + kMinBytes), &tmap_bs,
                                 (int32_t)(sb * 16), (int32_t)m0, mbar, pol);
                 ++issued_m;
+                // activation scales d_a[m0 .. m0+127] of this super-block
+                const int sbuf = (int)(sb & 1);
+                ok = mbar_wait(smem_u32(&B.sc_empty[sbuf]), (uint32_t)(((sb >> 1) & 1) ^ 1), a.err);
+                if (!ok) break;
+                const uint32_t sbar = smem_u32(&B.sc_full[sbuf]);
+                mbar_arrive_expect_tx(sbar, kBN * 4);
+                tc::tma_load_2d(smem_u32(smem + kOffSc + sbuf * kScBytes), &tmap_da, (int32_t)m0,
+                                (int32_t)sb, sbar, pol);
+                ++issued_sc;
             }
             // drain: no copy may still be landing when the CTA exits
             for (int64_t k = issued_raw > kRawStages ? issued_raw - kRawStages : 0; k < issued_raw; ++k)
@@ -203,6 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(smem_u32(&B.b_full[k % kBStages]), (uint32_t)((k / kBStages) & 1), a.err);
             for (int64_t k = issued_m > kMStages ? issued_m - kMStages : 0; k < issued_m; ++k)
                 mbar_wait(smem_u32(&B.m_full[k % kMStages]), (uint32_t)((k / kMStages) & 1), a.err);
+            for (int64_t k = issued_sc > 2 ? issued_sc - 2 : 0; k < issued_sc; ++k)
+                mbar_wait(smem_u32(&B.sc_full[k & 1]), (uint32_t)((k >> 1) & 1), a.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -215,8 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(smem_u32(&B.acc_empty[buf]), (uint32_t)(((sb >> 1) & 1) ^ 1), a.err);
                 if (!ok) break;
                 tc::fence_after_sync();
-                const uint32_t dA = tmem + (uint32_t)(buf * kBN);
-                const uint32_t dB = tmem + (uint32_t)(2 * kBN + buf * kBN);
+                const uint32_t dA = tmem + kColAccA + (uint32_t)(buf * kBN);
+                const uint32_t dB = tmem + kColAccB;
                 for (int kc = 0; kc < kChunksPerSB && ok; ++kc) {
                     const int64_t it = sb * kChunksPerSB + kc;
                     const int as = (int)(it % kAStages), bs = (int)(it % kBStages);
@@ -224,13 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                          mbar_wait(smem_u32(&B.b_full[bs]), (uint32_t)((it / kBStages) & 1), a.err);
                     if (!ok) break;
                     tc::fence_after_sync();
-                    const uint32_t abase = smem_u32(smem + kOffA + as * kChunkBytes);
+                    const uint32_t acol = tmem + kColARing + (uint32_t)as * kARingCols;
                     const uint32_t bbase = smem_u32(smem + kOffB + bs * kChunkBytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        tc::mma_f16(dA, tc::smem_desc(abase + 32 * kk, 1024, 2),
-                                    tc::smem_desc(bbase + 32 * kk, 1024, 2), idesc,
-                                    (kc | kk) != 0);
+                        tc::mma_f16_ta(dA, acol + 8 * kk, tc::smem_desc(bbase + 32 * kk, 1024, 2),
+                                       idesc, (kc | kk) != 0);
                     }
                     tc::commit(smem_u32(&B.a_empty[as]));
                     tc::commit(smem_u32(&B.b_empty[bs]));
@@ -238,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 const int ms = (int)(sb % kMStages);
-                ok = mbar_wait(smem_u32(&B.m_full[ms]), (uint32_t)((sb / kMStages) & 1), a.err);
+                ok = mbar_wait(smem_u32(&B.m_full[ms]), (uint32_t)((sb / kMStages) & 1), a.err) &&
+                     mbar_wait(smem_u32(B.bacc_empty), (uint32_t)((sb & 1) ^ 1), a.err);
                 if (!ok) break;
                 tc::fence_after_sync();
                 const uint32_t mbase = smem_u32(smem + kOffM + ms * 2 * kMinBytes);
@@ -251,9 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::commit(smem_u32(B.done));
             mbar_wait(smem_u32(B.done), 0, a.err);
         }
-    } else if (warp < 6) {
+    } else if (warp < 2 + kConvWarps) {
         // ------------------------------------------------------------ converters
-        const int ct = (warp - 2) * 32 + lane;  // weight row within the tile
+        // warp w may only touch TMEM lanes 32 (w % 4) .. +31: those are its rows
+        const int ct = 32 * (warp & 3) + lane;  // weight row within the tile
+        const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
+        const int set = (warp - 2) >> 2;  // K-chunks set, set + 2
         const int ti = ct / kTileRows, r = ct % kTileRows;
         const bool valid = ti < nt;
         bool ok = true;
@@ -272,23 +315,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s[2 * c + 1] = (f >> 12) & 63;
                 m[2 * c + 1] = (f >> 18) & 63;
             }
-            // mins operand, K = 16: column t holds m_{t/2}; 32B-swizzled rows
-            const int ms = (int)(sb % kMStages);
-            ok = mbar_wait(smem_u32(&B.m_empty[ms]), (uint32_t)(((sb / kMStages) & 1) ^ 1), a.err);
-            if (!ok) break;
-            {
-                uint32_t hm[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) hm[j] = h2_bits(__float2half2_rn((float)m[j]));
-                uint8_t *row = smem + kOffM + ms * 2 * kMinBytes + ct * 32;
-                const int sw = (ct >> 2) & 1;
-                *reinterpret_cast<uint4 *>(row + 16 * (0 ^ sw)) = make_uint4(hm[0], hm[1], hm[2], hm[3]);
-                *reinterpret_cast<uint4 *>(row + 16 * (1 ^ sw)) = make_uint4(hm[4], hm[5], hm[6], hm[7]);
+            // this row's d and dmin for the epilogue (set 0)
+            const int sbuf = (int)(sb & 1);
+            if (set == 0) {
+                ok = mbar_wait(smem_u32(&B.sc_empty[sbuf]), (uint32_t)(((sb >> 1) & 1) ^ 1), a.err);
+                if (!ok) break;
+                {
+                    float *scd = reinterpret_cast<float *>(smem + kOffSc + sbuf * kScBytes + kBN * 4);
+                    scd[ct] = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
+                    scd[kBM + ct] = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&B.sc_full[sbuf]));
+                // mins operand, K = 16: column t holds m_{t/2}; 32B-swizzled rows
+                const int ms = (int)(sb % kMStages);
+                ok = mbar_wait(smem_u32(&B.m_empty[ms]), (uint32_t)(((sb / kMStages) & 1) ^ 1), a.err);
+                if (!ok) break;
+                {
+                    uint32_t hm[8];
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) hm[j] = h2_bits(__float2half2_rn((float)m[j]));
+                    uint8_t *row = smem + kOffM + ms * 2 * kMinBytes + ct * 32;
+                    const int sw = (ct >> 2) & 1;
+                    *reinterpret_cast<uint4 *>(row + 16 * (0 ^ sw)) = make_uint4(hm[0], hm[1], hm[2], hm[3]);
+                    *reinterpret_cast<uint4 *>(row + 16 * (1 ^ sw)) = make_uint4(hm[4], hm[5], hm[6], hm[7]);
+                }
+                tc::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&B.m_full[ms]));
             }
-            tc::fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&B.m_full[ms]));
-            for (int kc = 0; kc < kChunksPerSB && ok; ++kc) {
+            for (int kc = set; kc < kChunksPerSB && ok; kc += 2) {
                 const int64_t it = sb * kChunksPerSB + kc;
                 const int as = (int)(it % kAStages);
                 ok = mbar_wait(smem_u32(&B.a_empty[as]), (uint32_t)(((it / kAStages) & 1) ^ 1), a.err);
@@ -300,20 +356,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * kc);
                     q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * kc);
                 }
-                const float sl = (float)s[2 * kc], sh = (float)s[2 * kc + 1];
-                const __half2 mul_l = __float2half2_rn(sl), add_l = __float2half2_rn(-1024.0f * sl);
-                const __half2 mul_h = __float2half2_rn(sh * 0.0625f), add_h = __float2half2_rn(-64.0f * sh);
+                tc::fence_after_sync();
+                const ScaleLH sc = make_scales((float)s[2 * kc], (float)s[2 * kc + 1]);
                 const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                uint8_t *row = smem + kOffA + as * kChunkBytes + ct * 128;
-                const int sw = ct & 7;
+                // columns 0..15: k = 0..31 (low nibbles), 16..31: k = 32..63 (high),
+                // column pairs in the (0, 2), (1, 3) order of every group of 4
+                uint32_t lo[16], hi[16];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int jj = j & 3;
-                    const uint4 v = j < 4 ? expand8(w[2 * jj], w[2 * jj + 1], false, mul_l, add_l)
-                                          : expand8(w[2 * jj], w[2 * jj + 1], true, mul_h, add_h);
-                    *reinterpret_cast<uint4 *>(row + 16 * (j ^ sw)) = v;
-                }
-                tc::fence_proxy_async();
+                for (int j = 0; j < 8; ++j)
+                    expand_word(w[j], sc, lo[2 * j], lo[2 * j + 1], hi[2 * j], hi[2 * j + 1]);
+                const uint32_t acol = tmem + lane_addr + kColARing + (uint32_t)as * kARingCols;
+                tc::tmem_st16(acol, lo);
+                tc::tmem_st16(acol + 16, hi);
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&B.a_full[as]));
             }
@@ -322,52 +378,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 6;
+        const int ew = warp - 2 - kConvWarps;
         const int quarter = warp & 3;  // TMEM lanes 32 * (warp % 4) ..
-        const int half = ew >> 2;      // columns 64 * half ..
+        const int part = ew >> 2;      // columns kEpiCols * part ..
         const int nl = quarter * 32 + lane;
         const int64_t n = n0 + nl;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        pdl_wait();  // the activation scales come from the preceding quantizer
-        float run[64];
+        float run[kEpiCols];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) run[j] = 0.0f;
+        for (int j = 0; j < kEpiCols; ++j) run[j] = 0.0f;
         bool ok = true;
         for (int64_t sb = 0; sb < nsb && ok; ++sb) {
             const int buf = (int)(sb & 1);
-            ok = mbar_wait(smem_u32(&B.acc_full[buf]), (uint32_t)((sb >> 1) & 1), a.err);
+            ok = mbar_wait(smem_u32(&B.sc_full[buf]), (uint32_t)((sb >> 1) & 1), a.err) &&
+                 mbar_wait(smem_u32(&B.acc_full[buf]), (uint32_t)((sb >> 1) & 1), a.err);
             if (!ok) break;
             tc::fence_after_sync();
-            float dw = 0.0f, dmw = 0.0f;
-            if (n < a.N) {
-                const uint32_t h = __ldg(reinterpret_cast<const uint32_t *>(
-                    a.Wp + (((n >> 3) * nsb + sb) * kTileRows + (n & 7)) * B_Q4_K));
-                dw = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
-                dmw = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
-            }
-            const float *da = a.daT + sb * a.M + m0 + half * 64;
+            const float *sc = reinterpret_cast<const float *>(smem + kOffSc + buf * kScBytes);
+            const float dw = sc[kBN + nl], dmw = sc[kBN + kBM + nl];
 #pragma unroll
-            for (int c16 = 0; c16 < 4; ++c16) {
-                const uint32_t col = (uint32_t)(half * 64 + c16 * 16);
+            for (int c16 = 0; c16 < kEpiCols / 16; ++c16) {
+                const uint32_t col = (uint32_t)(part * kEpiCols + c16 * 16);
                 float A[16], Bv[16];
-                tc::tmem_ld16(tmem + lane_addr + (uint32_t)(buf * kBN) + col, A);
-                tc::tmem_ld16(tmem + lane_addr + (uint32_t)(2 * kBN + buf * kBN) + col, Bv);
+                tc::tmem_ld16(tmem + lane_addr + kColAccA + (uint32_t)(buf * kBN) + col, A);
+                tc::tmem_ld16(tmem + lane_addr + kColAccB + col, Bv);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int64_t m = m0 + half * 64 + c16 * 16 + j;
-                    const float dav = m < a.M ? __ldg(da + c16 * 16 + j) : 0.0f;
-                    run[c16 * 16 + j] += dav * (dw * A[j] - dmw * Bv[j]);
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    const float4 da = *reinterpret_cast<const float4 *>(sc + col + 4 * j4);
+                    const float dv[4] = {da.x, da.y, da.z, da.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 4 * j4 + e;
+                        run[c16 * 16 + j] += dv[e] * (dw * A[j] - dmw * Bv[j]);
+                    }
                 }
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&B.acc_empty[buf]));
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&B.acc_empty[buf]));
+                mbar_arrive(smem_u32(B.bacc_empty));
+                mbar_arrive(smem_u32(&B.sc_empty[buf]));
+            }
         }
         if (n < a.N) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const int64_t m = m0 + half * 64 + j;
+            for (int j = 0; j < kEpiCols; ++j) {
+                const int64_t m = m0 + part * kEpiCols + j;
                 if (m < a.M) a.Y[m * a.N + n] = run[j];
             }
         }
@@ -404,26 +462,29 @@ __global__ void __launch_bounds__(256) quantize_q8K_prefill_kernel(const float *
         float d;
         int bsum;
         q8_K_warp(v, lo, hi, d, bsum);
+        // the MMA operand order: elements 1 and 2 of every group of 4 swapped
         uint4 o;
         uint32_t *po = &o.x;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t wsrc = i < 2 ? lo : hi;
-            const int8_t c0 = (int8_t)(wsrc >> (16 * (i & 1)));
-            const int8_t c1 = (int8_t)(wsrc >> (16 * (i & 1) + 8));
+            const int sh = 8 * (i & 1);  // pair (e0, e2), then (e1, e3)
+            const int8_t c0 = (int8_t)(wsrc >> sh);
+            const int8_t c1 = (int8_t)(wsrc >> (16 + sh));
             po[i] = h2_bits(__halves2half2(__int2half_rn(c0), __int2half_rn(c1)));
         }
         *reinterpret_cast<uint4 *>(y16 + b * QK_K + 8 * lane) = o;
         if ((lane & 1) == 0) bs16[b * 16 + (lane >> 1)] = __int2half_rn(bsum);
-        if (lane == 0) daT[sb * M + m] = d;
+        if (lane == 0) daT[sb * ((M + 3) & ~(int64_t)3) + m] = d;
     }
 }
 
 }  // namespace
 
 namespace tc {
-bool make_tmap_2d_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                      uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle) {
+bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                  uint32_t elem_bytes, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                  uint32_t box_cols, CUtensorMapSwizzle swizzle) {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     std::call_once(once, [] {
@@ -436,10 +497,10 @@ bool make_tmap_2d_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_
     });
     if (!encode) return false;
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint64_t strides[1] = {cols * elem_bytes};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
+    return encode(map, dtype, 2, const_cast<void *>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
@@ -456,7 +517,7 @@ size_t prefill_bytes(int64_t M, int64_t K, PrefillWs *p, uint8_t *base) {
     const size_t o_bs = off;
     off = align_up(off + (size_t)M * nsb * 16 * 2, 256);
     const size_t o_d = off;
-    off = align_up(off + (size_t)M * nsb * 4, 256);
+    off = align_up(off + (size_t)((M + 3) & ~(int64_t)3) * nsb * 4, 256);
     if (p) {
         p->y16 = reinterpret_cast<__half *>(base + o_y);
         p->bs16 = reinterpret_cast<__half *>(base + o_bs);
@@ -480,11 +541,14 @@ cudaError_t launch_quantize_prefill(const float *X, PrefillWs p, int64_t M, int6
 cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, int64_t M,
                              float *Y, cudaStream_t s) {
     const int64_t nsb = K / QK_K;
-    CUtensorMap tmap_y, tmap_bs;
-    if (!tc::make_tmap_2d_f16(&tmap_y, p.y16, (uint64_t)M, (uint64_t)K, kBN, kBK,
-                              CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tc::make_tmap_2d_f16(&tmap_bs, p.bs16, (uint64_t)M, (uint64_t)nsb * 16, kBN, 16,
-                              CU_TENSOR_MAP_SWIZZLE_32B))
+    CUtensorMap tmap_y, tmap_bs, tmap_da;
+    const uint64_t Mpad = (uint64_t)((M + 3) & ~(int64_t)3);
+    if (!tc::make_tmap_2d(&tmap_y, p.y16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M,
+                          (uint64_t)K, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tc::make_tmap_2d(&tmap_bs, p.bs16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M,
+                          (uint64_t)nsb * 16, kBN, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !tc::make_tmap_2d(&tmap_da, p.daT, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)nsb, Mpad,
+                          1, kBN, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_q4_K_kernel), kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -493,7 +557,6 @@ cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, 
     a.N = N;
     a.nsb = nsb;
     a.M = M;
-    a.daT = p.daT;
     a.Y = Y;
     a.err = device_error_word();
     cudaLaunchConfig_t cfg = {};
@@ -506,7 +569,7 @@ cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemm_q4_K_kernel, a, tmap_y, tmap_bs);
+    e = cudaLaunchKernelEx(&cfg, gemm_q4_K_kernel, a, tmap_y, tmap_bs, tmap_da);
     count_launch();
     return e;
 }

@@ -54,7 +54,8 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 // Prefill (GEMM) activation layout for Q4_K weights, written by the prefill
 // quantizer: Q8_K codes as exact fp16 [M][K] (the MMA operand, loaded by
 // TMA), 16-code sums as fp16 [M][K/256 * 16] (exact: |sum| <= 2032), block
-// scales as fp32 [K/256][M] (token-contiguous for the epilogue).
+// scales as fp32 [K/256][Mpad], Mpad = M rounded up to a multiple of 4
+// (token-contiguous rows, 16-byte aligned for TMA).
 struct PrefillWs {
     __half *y16;
     __half *bs16;

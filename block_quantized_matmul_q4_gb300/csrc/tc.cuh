@@ -47,6 +47,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] x B[smem desc], kind::f16: A is M lanes x K, two
+// 16-bit elements per 32-bit column (element 2c in the low half of column c).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
 // Arrive once on an mbarrier when all earlier tcgen05 async ops of this
 // thread have completed.
 __device__ __forceinline__ void commit(uint32_t mbar) {
@@ -90,6 +101,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 32 lanes x 32-bit, 16 consecutive columns per thread.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -108,10 +132,11 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 }
 
 // ------------------------------------------------------------------ host
-// 2-D tensor map over a row-major [rows, cols] array of 2-byte elements,
-// box {box_cols, box_rows}, the given swizzle. Returns false on failure.
-bool make_tmap_2d_f16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                      uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle);
+// 2-D tensor map over a row-major [rows, cols] array, box {box_cols,
+// box_rows}, the given swizzle. Returns false on failure.
+bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                  uint32_t elem_bytes, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                  uint32_t box_cols, CUtensorMapSwizzle swizzle);
 
 }  // namespace tc
 }  // namespace qmm
