@@ -13,25 +13,30 @@
 // Each super-block accumulates into its own TMEM buffers (double-buffered),
 // and the epilogue warps apply the per-super-block scales in fp32 registers.
 //
-// CTA = 128 weight rows (MMA M) x 128 tokens (MMA N), 14 warps:
-//   warp 0      producer: bulk copies of the raw Q4_K blocks of a super-block
-//               (one per 8-row packed tile) and 2-D TMA tiles of the fp16 codes
-//               (128B swizzle) and the fp16 bsums (32B swizzle);
+// CTA = 128 weight rows (MMA M) x 128 tokens (MMA N), 27 warps:
+//   warp 0      producer: per super-block one 3-D TMA copy of the raw Q4_K
+//               blocks (16 packed 8-row tiles) and one activation stage: four
+//               2-D TMA tiles of fp16 codes (128B swizzle) plus the fp16 bsums
+//               (32B swizzle), all on one barrier;
 //   warp 1      MMA issuer (one thread) and TMEM owner (512 columns);
-//   warps 2..9  converters, two sets of four: one weight row per thread (its
+//   warp 2      MMA waiter: all the issuer's barrier waits, handed over per
+//               group of MMAs through a named barrier;
+//   warps 3..10 converters, two sets of four: one weight row per thread (its
 //               TMEM lane), set 0 takes K-chunks 0 and 2 of a super-block,
 //               set 1 chunks 1 and 3. Nibbles x s_j -> fp16 in registers,
 //               stored straight into a TMEM operand ring with tcgen05.st (the
 //               page-3 "decode in registers, feed the MMA" idea; the expanded
 //               weights never touch shared memory). Set 0 also writes the
-//               row's mins for the bsum MMA and its d, dmin;
-//   warps 10..25 epilogue: tcgen05.ld both accumulators, y += d_a (d A -
-//               dmin B) into 32 fp32 registers per thread, final store. The
-//               per-super-block scales come from a small shared-memory ring:
-//               d_a by TMA from the workspace, d and dmin from the converters
-//               (who read those block headers anyway).
-// All mbarrier waits are bounded; on a timeout the CTA drains its copies and
-// MMAs, frees its TMEM and returns with the device error word set.
+//               row's mins, the A operand of the bsum MMA;
+//   warps 11..26 epilogue: tcgen05.ld both accumulators, y += d_a (d A -
+//               dmin B) in packed fp32 pairs, 32 columns per thread, final
+//               store. d, dmin (block header) and d_a (workspace) are read
+//               from global memory one super-block ahead.
+// Every wait costs a shared-memory round trip, so the pipeline is built to
+// need few of them per super-block: one barrier per activation stage, one
+// per pair of A chunks. All mbarrier waits are bounded; on a timeout the
+// CTA drains its copies and MMAs, frees its TMEM and returns with the
+// device error word set.
 #include <mutex>
 
 #include "tc.cuh"
@@ -43,42 +48,79 @@ constexpr int kBM = 128;  // weight rows per CTA (MMA M)
 constexpr int kBN = 128;  // tokens per CTA (MMA N)
 constexpr int kBK = 64;   // K per operand chunk: one 128-byte swizzle row of fp16
 constexpr int kChunksPerSB = QK_K / kBK;  // 4
-constexpr int kAStages = 4, kBStages = 4, kMStages = 2, kRawStages = 2;
+constexpr int kGroups = 2;                // A handed over in pairs of chunks
+constexpr int kActStages = 2, kRawStages = 4, kMinStages = 2;
 constexpr int kChunkBytes = kBN * kBK * 2;  // 16 KB activation tile
-constexpr int kMinBytes = kBM * 16 * 2;     // 4 KB per min operand (K = 16)
+constexpr int kBsBytes = kBN * 16 * 2;      // 4 KB bsum tile (K = 16)
+constexpr int kActBytes = kChunksPerSB * kChunkBytes + kBsBytes;  // one super-block
+constexpr int kMinBytes = kBM * 16 * 2;     // 4 KB mins operand (K = 16)
 constexpr int kRawBytes = (kBM / kTileRows) * kTileRows * B_Q4_K;  // 18432
-constexpr int kOffB = 0;
-constexpr int kOffM = kOffB + kBStages * kChunkBytes;
-constexpr int kOffRaw = kOffM + kMStages * 2 * kMinBytes;
-constexpr int kScBytes = kBN * 4 + 2 * kBM * 4;  // d_a[128], d[128], dmin[128]
-constexpr int kOffSc = kOffRaw + kRawStages * kRawBytes;
-constexpr int kOffBar = kOffSc + 2 * kScBytes;
-constexpr int kNumBars = 2 * (kRawStages + kAStages + kBStages + kMStages + 2 + 2) + 2;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot + alignment
 constexpr int kConvWarps = 8, kEpiWarps = 16;
-constexpr int kThreads = (2 + kConvWarps + kEpiWarps) * 32;
+constexpr int kThreads = (3 + kConvWarps + kEpiWarps) * 32;
 constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // columns per epilogue thread
+constexpr int kOffAct = 0;
+constexpr int kOffMin = kOffAct + kActStages * kActBytes;
+constexpr int kOffRaw = kOffMin + kMinStages * kMinBytes;
+constexpr int kOffDa = kOffRaw + kRawStages * kRawBytes;  // per epilogue warp: its 32 d_a
+constexpr int kOffBar = kOffDa + kEpiWarps * kEpiCols * 4;
+constexpr int kNumBars = 2 * (kRawStages + kActStages + kGroups + 2) + 2;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot + alignment
+static_assert(kActBytes % 1024 == 0 && kOffMin % 1024 == 0, "128B-swizzle tiles need 1 KB alignment");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 // TMEM columns: A accumulators (x2), the bsum accumulator, the A operand ring
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColAccA = 0, kColAccB = 2 * kBN, kColARing = 3 * kBN;
 constexpr uint32_t kARingCols = kBK / 2;  // two fp16 per 32-bit column
-static_assert(kColARing + kAStages * kARingCols <= kTmemCols, "TMEM budget");
+static_assert(kColARing + kChunksPerSB * kARingCols <= kTmemCols, "TMEM budget");
 static_assert(kBN == kBM, "square tiles");
 
 struct GemmArgs {
     const uint8_t *Wp;  // packed Q4_K weights
+    const float *daT;   // activation scales [nsb][Mpad]
     int64_t N, nsb, M;
     float *Y;  // [M][N]
     unsigned *err;
 };
 
 struct Bars {
-    uint64_t *raw_full, *raw_empty, *a_full, *a_empty, *b_full, *b_empty, *m_full, *m_empty,
-        *acc_full, *acc_empty, *sc_full, *sc_empty, *bacc_empty, *done;
+    uint64_t *raw_full, *raw_empty, *act_full, *act_empty, *a_full, *a_empty, *acc_full,
+        *acc_empty, *bacc_empty, *done;
 };
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+// Packed fp32 pairs (sm_100 family f32x2 arithmetic): half the FP
+// instructions of the per-super-block epilogue.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t ldg_nc_u32(const void *p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ldg_nc_f32(const float *p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+// Named barrier 1: the MMA waiter and issuer warps (64 threads).
+__device__ __forceinline__ void handoff_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 // (x & mask) | 0x64006400: two fp16 values 1024 + field
 __device__ __forceinline__ uint32_t magic(uint32_t x, uint32_t mask) {
     uint32_t d;
@@ -117,9 +159,9 @@ __device__ __forceinline__ void expand_word(uint32_t w, const ScaleLH &c, uint32
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_q4_K_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmap_y,
-                     const __grid_constant__ CUtensorMap tmap_bs,
-                     const __grid_constant__ CUtensorMap tmap_da) {
+    gemm_q4_K_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmap_w,
+                     const __grid_constant__ CUtensorMap tmap_y,
+                     const __grid_constant__ CUtensorMap tmap_bs) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the 128B-swizzled tiles
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -136,17 +178,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars B;
     B.raw_full = bar;
     B.raw_empty = B.raw_full + kRawStages;
-    B.a_full = B.raw_empty + kRawStages;
-    B.a_empty = B.a_full + kAStages;
-    B.b_full = B.a_empty + kAStages;
-    B.b_empty = B.b_full + kBStages;
-    B.m_full = B.b_empty + kBStages;
-    B.m_empty = B.m_full + kMStages;
-    B.acc_full = B.m_empty + kMStages;
+    B.act_full = B.raw_empty + kRawStages;
+    B.act_empty = B.act_full + kActStages;
+    B.a_full = B.act_empty + kActStages;
+    B.a_empty = B.a_full + kGroups;
+    B.acc_full = B.a_empty + kGroups;
     B.acc_empty = B.acc_full + 2;
-    B.sc_full = B.acc_empty + 2;
-    B.sc_empty = B.sc_full + 2;
-    B.bacc_empty = B.sc_empty + 2;
+    B.bacc_empty = B.acc_empty + 2;
     B.done = B.bacc_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(B.done + 1);
 
@@ -155,23 +193,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&B.raw_full[i]), 1);
             mbar_init(smem_u32(&B.raw_empty[i]), kConvWarps);
         }
-        for (int i = 0; i < kAStages; ++i) {
-            mbar_init(smem_u32(&B.a_full[i]), 4);
+        for (int i = 0; i < kActStages; ++i) {
+            mbar_init(smem_u32(&B.act_full[i]), 1);
+            mbar_init(smem_u32(&B.act_empty[i]), 1);
+        }
+        for (int i = 0; i < kGroups; ++i) {
+            mbar_init(smem_u32(&B.a_full[i]), kConvWarps);  // both sets, one chunk each
             mbar_init(smem_u32(&B.a_empty[i]), 1);
-        }
-        for (int i = 0; i < kBStages; ++i) {
-            mbar_init(smem_u32(&B.b_full[i]), 1);
-            mbar_init(smem_u32(&B.b_empty[i]), 1);
-        }
-        for (int i = 0; i < kMStages; ++i) {
-            mbar_init(smem_u32(&B.m_full[i]), 1 + 4);
-            mbar_init(smem_u32(&B.m_empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&B.acc_full[i]), 1);
             mbar_init(smem_u32(&B.acc_empty[i]), kEpiWarps);
-            mbar_init(smem_u32(&B.sc_full[i]), 1 + 4);
-            mbar_init(smem_u32(&B.sc_empty[i]), kEpiWarps);
         }
         mbar_init(smem_u32(B.bacc_empty), kEpiWarps);
         mbar_init(smem_u32(B.done), 1);
@@ -186,122 +218,126 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            tc::prefetch_tensormap(&tmap_w);
             tc::prefetch_tensormap(&tmap_y);
             tc::prefetch_tensormap(&tmap_bs);
-            tc::prefetch_tensormap(&tmap_da);
             const uint64_t pol = policy_evict_last();  // weights and codes are reused by other CTAs
             pdl_wait();  // the codes come from the preceding quantizer kernel
-            int64_t issued_raw = 0, issued_b = 0, issued_m = 0, issued_sc = 0;
+            int64_t issued_raw = 0, issued_act = 0;
             bool ok = true;
             for (int64_t sb = 0; sb < nsb && ok; ++sb) {
                 const int rs = (int)(sb % kRawStages);
                 ok = mbar_wait(smem_u32(&B.raw_empty[rs]), (uint32_t)(((sb / kRawStages) & 1) ^ 1), a.err);
                 if (!ok) break;
+                // tiles past the last one read as zeros (and are never stored)
                 const uint32_t rbar = smem_u32(&B.raw_full[rs]);
-                mbar_arrive_expect_tx(rbar, (uint32_t)nt * kTileRows * B_Q4_K);
-                for (int i = 0; i < nt; ++i)
-                    bulk_g2s(smem_u32(smem + kOffRaw + rs * kRawBytes + i * kTileRows * B_Q4_K),
-                             a.Wp + ((t0 + i) * nsb + sb) * (kTileRows * B_Q4_K),
-                             kTileRows * B_Q4_K, rbar, pol);
+                mbar_arrive_expect_tx(rbar, kRawBytes);
+                tc::tma_load_3d(smem_u32(smem + kOffRaw + rs * kRawBytes), &tmap_w, 0, (int32_t)sb,
+                                (int32_t)t0, rbar, pol);
                 ++issued_raw;
-                for (int kc = 0; kc < kChunksPerSB && ok; ++kc) {
-                    const int64_t it = sb * kChunksPerSB + kc;
-                    const int bs = (int)(it % kBStages);
-                    ok = mbar_wait(smem_u32(&B.b_empty[bs]), (uint32_t)(((it / kBStages) & 1) ^ 1), a.err);
-                    if (!ok) break;
-                    const uint32_t bbar = smem_u32(&B.b_full[bs]);
-                    mbar_arrive_expect_tx(bbar, kBN * kBK * 2);
-                    tc::tma_load_2d(smem_u32(smem + kOffB + bs * kChunkBytes), &tmap_y,
-                                    (int32_t)(sb * QK_K + kc * kBK), (int32_t)m0, bbar, pol);
-                    ++issued_b;
-                }
+                const int st = (int)(sb % kActStages);
+                ok = mbar_wait(smem_u32(&B.act_empty[st]), (uint32_t)(((sb / kActStages) & 1) ^ 1), a.err);
                 if (!ok) break;
-                const int ms = (int)(sb % kMStages);
-                ok = mbar_wait(smem_u32(&B.m_empty[ms]), (uint32_t)(((sb / kMStages) & 1) ^ 1), a.err);
-                if (!ok) break;
-                const uint32_t mbar = smem_u32(&B.m_full[ms]);
-                mbar_arrive_expect_tx(mbar, kBN * 16 * 2);
-                tc::tma_load_2d(smem_u32(smem + kOffM + ms * 2 * kMinBytes + kMinBytes), &tmap_bs,
-                                (int32_t)(sb * 16), (int32_t)m0, mbar, pol);
-                ++issued_m;
-                // activation scales d_a[m0 .. m0+127] of this super-block
-                const int sbuf = (int)(sb & 1);
-                ok = mbar_wait(smem_u32(&B.sc_empty[sbuf]), (uint32_t)(((sb >> 1) & 1) ^ 1), a.err);
-                if (!ok) break;
-                const uint32_t sbar = smem_u32(&B.sc_full[sbuf]);
-                mbar_arrive_expect_tx(sbar, kBN * 4);
-                tc::tma_load_2d(smem_u32(smem + kOffSc + sbuf * kScBytes), &tmap_da, (int32_t)m0,
-                                (int32_t)sb, sbar, pol);
-                ++issued_sc;
+                const uint32_t abar = smem_u32(&B.act_full[st]);
+                uint8_t *stage = smem + kOffAct + st * kActBytes;
+                mbar_arrive_expect_tx(abar, kActBytes);
+                for (int kc = 0; kc < kChunksPerSB; ++kc)
+                    tc::tma_load_2d(smem_u32(stage + kc * kChunkBytes), &tmap_y,
+                                    (int32_t)(sb * QK_K + kc * kBK), (int32_t)m0, abar, pol);
+                tc::tma_load_2d(smem_u32(stage + kChunksPerSB * kChunkBytes), &tmap_bs,
+                                (int32_t)(sb * 16), (int32_t)m0, abar, pol);
+                ++issued_act;
             }
             // drain: no copy may still be landing when the CTA exits
             for (int64_t k = issued_raw > kRawStages ? issued_raw - kRawStages : 0; k < issued_raw; ++k)
                 mbar_wait(smem_u32(&B.raw_full[k % kRawStages]), (uint32_t)((k / kRawStages) & 1), a.err);
-            for (int64_t k = issued_b > kBStages ? issued_b - kBStages : 0; k < issued_b; ++k)
-                mbar_wait(smem_u32(&B.b_full[k % kBStages]), (uint32_t)((k / kBStages) & 1), a.err);
-            for (int64_t k = issued_m > kMStages ? issued_m - kMStages : 0; k < issued_m; ++k)
-                mbar_wait(smem_u32(&B.m_full[k % kMStages]), (uint32_t)((k / kMStages) & 1), a.err);
-            for (int64_t k = issued_sc > 2 ? issued_sc - 2 : 0; k < issued_sc; ++k)
-                mbar_wait(smem_u32(&B.sc_full[k & 1]), (uint32_t)((k >> 1) & 1), a.err);
+            for (int64_t k = issued_act > kActStages ? issued_act - kActStages : 0; k < issued_act; ++k)
+                mbar_wait(smem_u32(&B.act_full[k % kActStages]), (uint32_t)((k / kActStages) & 1), a.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
-            int64_t issued = 0;
-            bool ok = true;
-            for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-                const int buf = (int)(sb & 1);
-                ok = mbar_wait(smem_u32(&B.acc_empty[buf]), (uint32_t)(((sb >> 1) & 1) ^ 1), a.err);
-                if (!ok) break;
-                tc::fence_after_sync();
-                const uint32_t dA = tmem + kColAccA + (uint32_t)(buf * kBN);
-                const uint32_t dB = tmem + kColAccB;
-                for (int kc = 0; kc < kChunksPerSB && ok; ++kc) {
-                    const int64_t it = sb * kChunksPerSB + kc;
-                    const int as = (int)(it % kAStages), bs = (int)(it % kBStages);
-                    ok = mbar_wait(smem_u32(&B.a_full[as]), (uint32_t)((it / kAStages) & 1), a.err) &&
-                         mbar_wait(smem_u32(&B.b_full[bs]), (uint32_t)((it / kBStages) & 1), a.err);
-                    if (!ok) break;
+        // Never touches an mbarrier on the way: a shared-memory access by the
+        // issuing thread waits for its MMAs in flight, which would drain the
+        // tensor pipe at every chunk. The waiter warp does the waiting and
+        // hands over each group through a named barrier. Both warps pass it
+        // the same number of times whatever happens, so neither can hang; after
+        // a timeout the MMAs run on stale operands and the error word reports it.
+        constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
+        const uint64_t bdesc0 = tc::smem_desc(smem_u32(smem + kOffAct), 1024, 2);
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const int buf = (int)(sb & 1), st = (int)(sb % kActStages);
+            const uint32_t dA = tmem + kColAccA + (uint32_t)(buf * kBN);
+#pragma unroll 1
+            for (int g = 0; g < kGroups; ++g) {
+                handoff_sync();
+                if (lane == 0) {
                     tc::fence_after_sync();
-                    const uint32_t acol = tmem + kColARing + (uint32_t)as * kARingCols;
-                    const uint32_t bbase = smem_u32(smem + kOffB + bs * kChunkBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        tc::mma_f16_ta(dA, acol + 8 * kk, tc::smem_desc(bbase + 32 * kk, 1024, 2),
-                                       idesc, (kc | kk) != 0);
+                    for (int h = 0; h < kChunksPerSB / kGroups; ++h) {
+                        const int kc = g * (kChunksPerSB / kGroups) + h;
+                        const uint32_t acol = tmem + kColARing + (uint32_t)kc * kARingCols;
+                        // K step of 16 fp16 = 32 bytes = 2 in the descriptor's address field
+                        const uint64_t bdesc = bdesc0 + (uint64_t)((st * kActBytes + kc * kChunkBytes) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc::mma_f16_ta(dA, acol + 8 * kk, bdesc + 2 * kk, idesc, (kc | kk) != 0);
                     }
-                    tc::commit(smem_u32(&B.a_empty[as]));
-                    tc::commit(smem_u32(&B.b_empty[bs]));
-                    ++issued;
+                    tc::commit(smem_u32(&B.a_empty[g]));
                 }
-                if (!ok) break;
-                const int ms = (int)(sb % kMStages);
-                ok = mbar_wait(smem_u32(&B.m_full[ms]), (uint32_t)((sb / kMStages) & 1), a.err) &&
-                     mbar_wait(smem_u32(B.bacc_empty), (uint32_t)((sb & 1) ^ 1), a.err);
-                if (!ok) break;
+                __syncwarp();
+            }
+            handoff_sync();
+            if (lane == 0) {
                 tc::fence_after_sync();
-                const uint32_t mbase = smem_u32(smem + kOffM + ms * 2 * kMinBytes);
-                tc::mma_f16(dB, tc::smem_desc(mbase, 256, 6), tc::smem_desc(mbase + kMinBytes, 256, 6),
+                const uint32_t mins = smem_u32(smem + kOffMin + (int)(sb % kMinStages) * kMinBytes);
+                const uint32_t bsum = smem_u32(smem + kOffAct + st * kActBytes + kChunksPerSB * kChunkBytes);
+                tc::mma_f16(tmem + kColAccB, tc::smem_desc(mins, 256, 6), tc::smem_desc(bsum, 256, 6),
                             idesc, false);
-                tc::commit(smem_u32(&B.m_empty[ms]));
+                tc::commit(smem_u32(&B.act_empty[st]));
                 tc::commit(smem_u32(&B.acc_full[buf]));
             }
+            __syncwarp();
+        }
+        if (lane == 0) {
             // no MMA may still be running when TMEM is freed
             tc::commit(smem_u32(B.done));
             mbar_wait(smem_u32(B.done), 0, a.err);
         }
-    } else if (warp < 2 + kConvWarps) {
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ MMA waiter
+        // Waits for the operands (and free accumulators) of each group, then
+        // meets the issuer at the named barrier. After a timeout it stops
+        // waiting but keeps meeting the issuer.
+        bool ok = true;
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const int buf = (int)(sb & 1), st = (int)(sb % kActStages);
+            const uint32_t par = (uint32_t)(sb & 1);
+            if (lane == 0 && ok)
+                ok = mbar_wait(smem_u32(&B.acc_empty[buf]), (uint32_t)(((sb >> 1) & 1) ^ 1), a.err) &&
+                     mbar_wait(smem_u32(&B.act_full[st]), (uint32_t)((sb / kActStages) & 1), a.err);
+#pragma unroll 1
+            for (int g = 0; g < kGroups; ++g) {
+                if (lane == 0 && ok) ok = mbar_wait(smem_u32(&B.a_full[g]), par, a.err);
+                __syncwarp();
+                handoff_sync();
+            }
+            if (lane == 0 && ok) ok = mbar_wait(smem_u32(B.bacc_empty), par ^ 1, a.err);
+            __syncwarp();
+            handoff_sync();
+        }
+    } else if (warp < 3 + kConvWarps) {
         // ------------------------------------------------------------ converters
         // warp w may only touch TMEM lanes 32 (w % 4) .. +31: those are its rows
         const int ct = 32 * (warp & 3) + lane;  // weight row within the tile
         const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
-        const int set = (warp - 2) >> 2;  // K-chunks set, set + 2
+        const int set = (warp - 3) >> 2;  // chunk `set` of each group
         const int ti = ct / kTileRows, r = ct % kTileRows;
         const bool valid = ti < nt;
         bool ok = true;
         for (int64_t sb = 0; sb < nsb && ok; ++sb) {
             const int rs = (int)(sb % kRawStages);
+            const uint32_t par = (uint32_t)(sb & 1);
             ok = mbar_wait(smem_u32(&B.raw_full[rs]), (uint32_t)((sb / kRawStages) & 1), a.err);
             if (!ok) break;
             const uint8_t *blk = smem + kOffRaw + rs * kRawBytes + (ti * kTileRows + r) * B_Q4_K;
@@ -315,40 +351,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s[2 * c + 1] = (f >> 12) & 63;
                 m[2 * c + 1] = (f >> 18) & 63;
             }
-            // this row's d and dmin for the epilogue (set 0)
-            const int sbuf = (int)(sb & 1);
-            if (set == 0) {
-                ok = mbar_wait(smem_u32(&B.sc_empty[sbuf]), (uint32_t)(((sb >> 1) & 1) ^ 1), a.err);
+#pragma unroll 1
+            for (int g = 0; g < kGroups && ok; ++g) {
+                const int kc = g * (kChunksPerSB / kGroups) + set;
+                // the slots of group g are free once the MMAs of group g of the
+                // previous super-block are done -- and with them every MMA
+                // issued before, including the bsum MMA two super-blocks back
+                // that read the mins slot reused below
+                ok = mbar_wait(smem_u32(&B.a_empty[g]), par ^ 1, a.err);
                 if (!ok) break;
-                {
-                    float *scd = reinterpret_cast<float *>(smem + kOffSc + sbuf * kScBytes + kBN * 4);
-                    scd[ct] = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
-                    scd[kBM + ct] = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&B.sc_full[sbuf]));
-                // mins operand, K = 16: column t holds m_{t/2}; 32B-swizzled rows
-                const int ms = (int)(sb % kMStages);
-                ok = mbar_wait(smem_u32(&B.m_empty[ms]), (uint32_t)(((sb / kMStages) & 1) ^ 1), a.err);
-                if (!ok) break;
-                {
+                if (g == 0 && set == 0) {
+                    // mins operand, K = 16: column t holds m_{t/2}; 32B-swizzled rows
                     uint32_t hm[8];
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 8; ++j) hm[j] = h2_bits(__float2half2_rn((float)m[j]));
-                    uint8_t *row = smem + kOffM + ms * 2 * kMinBytes + ct * 32;
+                    uint8_t *row = smem + kOffMin + (int)(sb % kMinStages) * kMinBytes + ct * 32;
                     const int sw = (ct >> 2) & 1;
                     *reinterpret_cast<uint4 *>(row + 16 * (0 ^ sw)) = make_uint4(hm[0], hm[1], hm[2], hm[3]);
                     *reinterpret_cast<uint4 *>(row + 16 * (1 ^ sw)) = make_uint4(hm[4], hm[5], hm[6], hm[7]);
+                    tc::fence_proxy_async();
                 }
-                tc::fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&B.m_full[ms]));
-            }
-            for (int kc = set; kc < kChunksPerSB && ok; kc += 2) {
-                const int64_t it = sb * kChunksPerSB + kc;
-                const int as = (int)(it % kAStages);
-                ok = mbar_wait(smem_u32(&B.a_empty[as]), (uint32_t)(((it / kAStages) & 1) ^ 1), a.err);
-                if (!ok) break;
                 // 32 nibble bytes: low nibbles are k = 64kc + 0..31 (sub-block
                 // 2kc), high nibbles k = 64kc + 32..63 (sub-block 2kc + 1)
                 uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
@@ -365,52 +387,73 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     expand_word(w[j], sc, lo[2 * j], lo[2 * j + 1], hi[2 * j], hi[2 * j + 1]);
-                const uint32_t acol = tmem + lane_addr + kColARing + (uint32_t)as * kARingCols;
+                const uint32_t acol = tmem + lane_addr + kColARing + (uint32_t)kc * kARingCols;
                 tc::tmem_st16(acol, lo);
                 tc::tmem_st16(acol + 16, hi);
                 tc::tmem_st_wait();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&B.a_full[as]));
+                if (lane == 0) mbar_arrive(smem_u32(&B.a_full[g]));
             }
             __syncwarp();
             if (lane == 0 && ok) mbar_arrive(smem_u32(&B.raw_empty[rs]));
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 2 - kConvWarps;
+        const int ew = warp - 3 - kConvWarps;
         const int quarter = warp & 3;  // TMEM lanes 32 * (warp % 4) ..
         const int part = ew >> 2;      // columns kEpiCols * part ..
         const int nl = quarter * 32 + lane;
         const int64_t n = n0 + nl;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        float run[kEpiCols];
+        float *da_stage = reinterpret_cast<float *>(smem + kOffDa) + ew * kEpiCols;
+        // this row's block headers (d, dmin as two fp16) and this warp's 32
+        // activation scales, read one super-block ahead
+        const bool row_ok = n < a.N;
+        const uint8_t *hdr_ptr = a.Wp + ((n / kTileRows) * nsb * kTileRows + (n % kTileRows)) * B_Q4_K;
+        const int64_t Mpad = (a.M + 3) & ~(int64_t)3;
+        const int64_t mcol = m0 + part * kEpiCols + lane;
+        pdl_wait();  // d_a comes from the preceding quantizer kernel
+        uint32_t hdr_next = row_ok ? ldg_nc_u32(hdr_ptr) : 0u;
+        float da_next = mcol < Mpad ? ldg_nc_f32(a.daT + mcol) : 0.0f;
+        uint64_t run[kEpiCols / 2];  // column pairs
 #pragma unroll
-        for (int j = 0; j < kEpiCols; ++j) run[j] = 0.0f;
+        for (int j = 0; j < kEpiCols / 2; ++j) run[j] = 0;  // (+0.0f, +0.0f)
         bool ok = true;
         for (int64_t sb = 0; sb < nsb && ok; ++sb) {
             const int buf = (int)(sb & 1);
-            ok = mbar_wait(smem_u32(&B.sc_full[buf]), (uint32_t)((sb >> 1) & 1), a.err) &&
-                 mbar_wait(smem_u32(&B.acc_full[buf]), (uint32_t)((sb >> 1) & 1), a.err);
+            const uint32_t hdr = hdr_next;
+            const float da = da_next;
+            if (sb + 1 < nsb) {
+                if (row_ok) hdr_next = ldg_nc_u32(hdr_ptr + (sb + 1) * (kTileRows * B_Q4_K));
+                if (mcol < Mpad) da_next = ldg_nc_f32(a.daT + (sb + 1) * Mpad + mcol);
+            }
+            da_stage[lane] = da;
+            __syncwarp();
+            ok = mbar_wait(smem_u32(&B.acc_full[buf]), (uint32_t)((sb >> 1) & 1), a.err);
             if (!ok) break;
             tc::fence_after_sync();
-            const float *sc = reinterpret_cast<const float *>(smem + kOffSc + buf * kScBytes);
-            const float dw = sc[kBN + nl], dmw = sc[kBN + kBM + nl];
+            const float dw = __half2float(__ushort_as_half((unsigned short)(hdr & 0xFFFFu)));
+            const float dmw = __half2float(__ushort_as_half((unsigned short)(hdr >> 16)));
+            const uint64_t dw2 = pk2(dw, dw), ndmw2 = pk2(-dmw, -dmw);
 #pragma unroll
-            for (int c16 = 0; c16 < kEpiCols / 16; ++c16) {
-                const uint32_t col = (uint32_t)(part * kEpiCols + c16 * 16);
-                float A[16], Bv[16];
-                tc::tmem_ld16(tmem + lane_addr + kColAccA + (uint32_t)(buf * kBN) + col, A);
-                tc::tmem_ld16(tmem + lane_addr + kColAccB + col, Bv);
+            for (int c8 = 0; c8 < kEpiCols / 8; ++c8) {
+                const uint32_t col = (uint32_t)(part * kEpiCols + c8 * 8);
+                float A[8], Bv[8];
+                tc::tmem_ld8(tmem + lane_addr + kColAccA + (uint32_t)(buf * kBN) + col, A);
+                tc::tmem_ld8(tmem + lane_addr + kColAccB + col, Bv);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int j4 = 0; j4 < 4; ++j4) {
-                    const float4 da = *reinterpret_cast<const float4 *>(sc + col + 4 * j4);
-                    const float dv[4] = {da.x, da.y, da.z, da.w};
+                for (int j4 = 0; j4 < 2; ++j4) {
+                    const float4 dav = *reinterpret_cast<const float4 *>(da_stage + c8 * 8 + 4 * j4);
+                    const uint64_t dv[2] = {pk2(dav.x, dav.y), pk2(dav.z, dav.w)};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 4 * j4 + e;
-                        run[c16 * 16 + j] += dv[e] * (dw * A[j] - dmw * Bv[j]);
+                    for (int e = 0; e < 2; ++e) {
+                        const int j = 4 * j4 + 2 * e;
+                        // run += d_a (d A - dmin B), two columns at a time
+                        const uint64_t t = fma2(pk2(A[j], A[j + 1]), dw2,
+                                                mul2(pk2(Bv[j], Bv[j + 1]), ndmw2));
+                        run[(c8 * 8 + j) / 2] = fma2(dv[e], t, run[(c8 * 8 + j) / 2]);
                     }
                 }
             }
@@ -419,14 +462,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 mbar_arrive(smem_u32(&B.acc_empty[buf]));
                 mbar_arrive(smem_u32(B.bacc_empty));
-                mbar_arrive(smem_u32(&B.sc_empty[buf]));
             }
         }
-        if (n < a.N) {
+        if (row_ok) {
 #pragma unroll
-            for (int j = 0; j < kEpiCols; ++j) {
+            for (int j = 0; j < kEpiCols; j += 2) {
+                float lo, hi;
+                upk2(run[j / 2], lo, hi);
                 const int64_t m = m0 + part * kEpiCols + j;
-                if (m < a.M) a.Y[m * a.N + n] = run[j];
+                if (m < a.M) a.Y[m * a.N + n] = lo;
+                if (m + 1 < a.M) a.Y[(m + 1) * a.N + n] = hi;
             }
         }
     }
@@ -482,9 +527,8 @@ __global__ void __launch_bounds__(256) quantize_q8K_prefill_kernel(const float *
 }  // namespace
 
 namespace tc {
-bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
-                  uint32_t elem_bytes, uint64_t rows, uint64_t cols, uint32_t box_rows,
-                  uint32_t box_cols, CUtensorMapSwizzle swizzle) {
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     std::call_once(once, [] {
@@ -495,6 +539,28 @@ bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
             q == cudaDriverEntryPointSuccess)
             encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
+    return encode;
+}
+}  // namespace
+
+bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                  const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3]) {
+    const auto encode = encoder();
+    if (!encode) return false;
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t st[2] = {strides[0], strides[1]};
+    const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode(map, dtype, 3, const_cast<void *>(base), d, st, bx, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                  uint32_t elem_bytes, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                  uint32_t box_cols, CUtensorMapSwizzle swizzle) {
+    const auto encode = encoder();
     if (!encode) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * elem_bytes};
@@ -541,24 +607,27 @@ cudaError_t launch_quantize_prefill(const float *X, PrefillWs p, int64_t M, int6
 cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, int64_t M,
                              float *Y, cudaStream_t s) {
     const int64_t nsb = K / QK_K;
-    CUtensorMap tmap_y, tmap_bs, tmap_da;
-    const uint64_t Mpad = (uint64_t)((M + 3) & ~(int64_t)3);
-    if (!tc::make_tmap_2d(&tmap_y, p.y16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M,
-                          (uint64_t)K, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tc::make_tmap_2d(&tmap_bs, p.bs16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M,
-                          (uint64_t)nsb * 16, kBN, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !tc::make_tmap_2d(&tmap_da, p.daT, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)nsb, Mpad,
-                          1, kBN, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_q4_K_kernel), kSmemBytes);
-    if (e != cudaSuccess) return e;
     GemmArgs a;
     a.Wp = static_cast<const uint8_t *>(Wp);
+    a.daT = p.daT;
     a.N = N;
     a.nsb = nsb;
     a.M = M;
     a.Y = Y;
     a.err = device_error_word();
+    CUtensorMap tmap_w, tmap_y, tmap_bs;
+    // packed weights as [tile][super-block][8 rows x 144 bytes], in 8-byte units
+    const uint64_t wdims[3] = {kTileRows * B_Q4_K / 8, (uint64_t)nsb, (uint64_t)tiles_of(N)};
+    const uint64_t wstrides[2] = {kTileRows * B_Q4_K, (uint64_t)nsb * kTileRows * B_Q4_K};
+    const uint32_t wbox[3] = {kTileRows * B_Q4_K / 8, 1, kBM / kTileRows};
+    if (!tc::make_tmap_3d(&tmap_w, Wp, CU_TENSOR_MAP_DATA_TYPE_UINT64, wdims, wstrides, wbox) ||
+        !tc::make_tmap_2d(&tmap_y, p.y16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M,
+                          (uint64_t)K, kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tc::make_tmap_2d(&tmap_bs, p.bs16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M,
+                          (uint64_t)nsb * 16, kBN, 16, CU_TENSOR_MAP_SWIZZLE_32B))
+        return cudaErrorInvalidValue;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_q4_K_kernel), kSmemBytes);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + kBN - 1) / kBN));
     cfg.blockDim = dim3(kThreads);
@@ -569,7 +638,7 @@ cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemm_q4_K_kernel, a, tmap_y, tmap_bs, tmap_da);
+    e = cudaLaunchKernelEx(&cfg, gemm_q4_K_kernel, a, tmap_w, tmap_y, tmap_bs);
     count_launch();
     return e;
 }
