@@ -16,7 +16,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqmm.so")
 
-QMM_TYPE_Q4_0, QMM_TYPE_Q4_K, QMM_TYPE_Q8_0, QMM_TYPE_Q8_K = 0, 1, 2, 3
+QMM_TYPE_Q4_0, QMM_TYPE_Q4_K, QMM_TYPE_Q8_0, QMM_TYPE_Q8_K, QMM_TYPE_W4A16 = 0, 1, 2, 3, 4
 QMM_OK = 0
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "QMM_ERR_CUDA",
           4: "QMM_ERR_TIMEOUT", 5: "QMM_ERR_NOMEM", 6: "QMM_ERR_WORKSPACE"}
@@ -49,6 +49,7 @@ _SIGS = {
     "qmm_mul_mat_prepared": (_i32, [_i32, _vp, _i64, _i64, _vp, _sz, _i64, _vp, _vp]),
     "qmm_mul_mat_static": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_debug_block_sums": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "qmm_w4a16": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _vp]),
     "qmm_status_string": (ctypes.c_char_p, [_i32]),
     "qmm_last_error": (ctypes.c_char_p, []),
     "qmm_check_device_error": (_i32, [_vp]),
@@ -166,6 +167,14 @@ def qmm_debug_block_sums(wt: int, W_packed, N: int, K: int, Xq, M: int, out, str
     _check("qmm_debug_block_sums",
            _lib.qmm_debug_block_sums(wt, _ptr(W_packed), N, K, _ptr(Xq), M, _ptr(out),
                                      _stream(stream)))
+
+
+def qmm_w4a16(W_packed, scales, zeros, G: int, A, C, M: int, N: int, K: int, stream=None):
+    """C [M, N] fp16 = A [M, K] fp16 x W^T for packed W4A16 weights (scales fp16
+    and zeros uint8 [N, K/G]); see include/qmm.h."""
+    _check("qmm_w4a16",
+           _lib.qmm_w4a16(_ptr(W_packed), _ptr(scales), _ptr(zeros), G, _ptr(A), _ptr(C), M, N, K,
+                          _stream(stream)))
 
 
 def qmm_status_string(status: int) -> str:

@@ -209,15 +209,21 @@ size_t qmm_block_bytes(qmm_type t) {
     case QMM_TYPE_Q4_K: return B_Q4_K;
     case QMM_TYPE_Q8_0: return B_Q8_0;
     case QMM_TYPE_Q8_K: return B_Q8_K;
+    case QMM_TYPE_W4A16: return 4;
     default: return 0;
     }
 }
 
 int qmm_block_elems(qmm_type t) {
+    if (t == QMM_TYPE_W4A16) return 8;
     return (is_weight(t) || is_act(t)) ? elems(t) : 0;
 }
 
 size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K) {
+    if (wt == QMM_TYPE_W4A16)
+        return (N > 0 && K > 0 && K % 8 == 0 && K <= ((int64_t)1 << 30) && N <= ((int64_t)1 << 31))
+                   ? (size_t)N * (size_t)(K / 2)
+                   : 0;
     if (!is_weight(wt) || N <= 0 || K <= 0 || K % elems(wt)) return 0;
     return (size_t)tiles_of(N) * kTileRows * (size_t)(K / elems(wt)) * qmm_block_bytes(wt);
 }
@@ -256,6 +262,18 @@ qmm_status qmm_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N
 
 static qmm_status repack_common(qmm_type wt, const void *src, void *dst, int64_t N, int64_t K,
                                 bool inverse, qmm_stream_t stream) {
+    if (wt == QMM_TYPE_W4A16) {
+        QMM_CHECK_ARG(N > 0 && K > 0 && K % 8 == 0, "W4A16 needs N > 0, K > 0, K %% 8 == 0 "
+                      "(N=%lld K=%lld)", (long long)N, (long long)K);
+        QMM_CHECK_ARG(qmm_packed_bytes(wt, N, K) > 0, "sizes too large");
+        QMM_CHECK_ARG(src && dst, "null pointer argument");
+        QMM_CHECK_ARG(aligned(src, 16) && aligned(dst, 16), "W4A16 buffers must be 16-byte aligned");
+        const uintptr_t a = (uintptr_t)src, b = (uintptr_t)dst;
+        const size_t pb = qmm_packed_bytes(wt, N, K);
+        QMM_CHECK_ARG(a + pb <= b || b + pb <= a, "source and destination overlap");
+        return cuda_status(launch_w4a16_repack(inverse, src, dst, N, K, (cudaStream_t)stream),
+                           "repack launch");
+    }
     qmm_status st = check_weight_args(wt, N, K);
     if (st != QMM_OK) return st;
     QMM_CHECK_ARG(N > 0, "N must be > 0");
@@ -388,5 +406,36 @@ qmm_status qmm_check_device_error(qmm_stream_t stream) {
 }
 
 uint64_t qmm_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t *zeros, int64_t G,
+                     const uint16_t *A, uint16_t *C, int64_t M, int64_t N, int64_t K,
+                     qmm_stream_t stream) {
+    QMM_CHECK_ARG(M >= 0 && N >= 0 && K > 0 && G > 0,
+                  "sizes must satisfy M, N >= 0, K, G > 0 (M=%lld N=%lld K=%lld G=%lld)",
+                  (long long)M, (long long)N, (long long)K, (long long)G);
+    QMM_CHECK_ARG(K % G == 0 && G % 8 == 0, "need K %% G == 0 and G %% 8 == 0 (K=%lld G=%lld)",
+                  (long long)K, (long long)G);
+    QMM_CHECK_ARG(K <= ((int64_t)1 << 30) && N <= ((int64_t)1 << 31) && M <= ((int64_t)1 << 31),
+                  "sizes too large");
+    if (G % 128 != 0)
+        return set_error(QMM_ERR_UNSUPPORTED, "W4A16 group size %lld: this build needs G %% 128 == 0",
+                         (long long)G);
+    if (M == 0 || N == 0) return ok();
+    QMM_CHECK_ARG(W_packed && scales && zeros && A && C, "null pointer argument");
+    QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(A, 16), "W_packed and A must be 16-byte aligned");
+    QMM_CHECK_ARG(aligned(scales, 2) && aligned(C, 2), "scales and C must be 2-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    const __half *S = reinterpret_cast<const __half *>(scales);
+    const __half *Ah = reinterpret_cast<const __half *>(A);
+    __half *Ch = reinterpret_cast<__half *>(C);
+    // decode kernel on up to 16 tokens at a time
+    for (int64_t m0 = 0; m0 < M; m0 += 16) {
+        const int64_t mt = M - m0 < 16 ? M - m0 : 16;
+        cudaError_t e = launch_w4a16_decode(W_packed, S, zeros, G, Ah + m0 * K, Ch + m0 * N, mt, N,
+                                            K, s);
+        if (e != cudaSuccess) return cuda_status(e, "W4A16 kernel launch");
+    }
+    return ok();
+}
 
 }  // extern "C"

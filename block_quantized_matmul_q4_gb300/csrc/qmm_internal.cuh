@@ -365,6 +365,13 @@ cudaError_t launch_quantize_prefill(const float *X, PrefillWs p, int64_t M, int6
                                     cudaStream_t s);
 cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, int64_t M,
                              float *Y, cudaStream_t s);
+// W4A16: nibble interleave of the packed layout (or its inverse), the decode
+// kernel (M <= 16) and the tensor-core GEMM (M > 16).
+cudaError_t launch_w4a16_repack(bool inverse, const void *src, void *dst, int64_t N, int64_t K,
+                                cudaStream_t s);
+cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z, int64_t G,
+                                const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
+                                cudaStream_t s);
 cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
                                     const void *Xq, int64_t M, int32_t *out, cudaStream_t s);
 }  // namespace qmm

@@ -53,7 +53,10 @@ typedef enum {
     QMM_TYPE_Q4_0 = 0, /* weights: 32 x 4-bit, fp16 d;       w = d (q - 8)            */
     QMM_TYPE_Q4_K = 1, /* weights: 256 x 4-bit, 8 sub-blocks; w = d s_j q - dmin m_j  */
     QMM_TYPE_Q8_0 = 2, /* activations: 32 x int8, fp16 d;     a = d q                  */
-    QMM_TYPE_Q8_K = 3  /* activations: 256 x int8, fp32 d, 16 sums of 16 codes        */
+    QMM_TYPE_Q8_K = 3, /* activations: 256 x int8, fp32 d, 16 sums of 16 codes        */
+    QMM_TYPE_W4A16 = 4 /* weights: 4-bit codes q, 8 per uint32 word; per row and group
+                          of G elements an fp16 scale s and a uint8 zero z:
+                          w = s (q - z). Used by qmm_w4a16 only.               */
 } qmm_type;
 
 typedef enum {
@@ -68,16 +71,19 @@ typedef enum {
 
 /* ---------------------------------------------------------------- sizes */
 
-/* Bytes of one canonical block: 18, 144, 34, 292; 0 for an invalid type.
- * (Block layouts: page 1, "最基础的两块: Q4_0 与 Q8_0", "K-quant", "更低的比特".) */
+/* Bytes of one canonical block: 18, 144, 34, 292, and 4 for W4A16 (one
+ * uint32 word of 8 codes); 0 for an invalid type.
+ * (Block layouts: page 1, "最基础的两块: Q4_0 与 Q8_0", "K-quant", "更低的比特";
+ * W4A16: page 3, "位级打包".) */
 size_t qmm_block_bytes(qmm_type t);
 
-/* Elements per block: 32 or 256; 0 for an invalid type. */
+/* Elements per block: 32, 256, or 8 for W4A16; 0 for an invalid type. */
 int qmm_block_elems(qmm_type t);
 
 /* Bytes of the packed (repacked) weight buffer for an [N, K] weight of type
- * Q4_0 or Q4_K; 0 if the type or sizes are invalid. Rows are padded to a
- * multiple of 8 with zero blocks. */
+ * Q4_0, Q4_K or W4A16; 0 if the type or sizes are invalid. Q4_0/Q4_K rows
+ * are padded to a multiple of 8 with zero blocks; W4A16 takes N * K / 2
+ * bytes (K % 8 == 0), no padding. */
 size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K);
 
 /* Bytes of the workspace qmm_mul_mat_ws needs for M activation rows of
@@ -129,6 +135,15 @@ qmm_status qmm_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N
  * null or misaligned pointers. */
 qmm_status qmm_repack_weights(qmm_type wt, const void *W_canon, void *W_packed, int64_t N,
                               int64_t K, qmm_stream_t stream);
+
+/* W4A16 (wt = QMM_TYPE_W4A16): W_canon is qweight [N][K/8] uint32, element
+ * k = 8c + i of a row in bits 4i..4i+3 of word c (page 3, "位级打包"); the
+ * packed layout keeps every word in place and interleaves its nibbles, the
+ * even elements in the low 16 bits and the odd ones in the high 16 bits
+ * (nibble slots 0..7 hold elements 0, 2, 4, 6, 1, 3, 5, 7), so that one
+ * mask turns a word into fp16 pairs (k, k + 1) (page 3, "Ladder": the
+ * weight is laid out once for the decoder). Needs K % 8 == 0; both buffers
+ * 16-byte aligned. */
 
 /* Inverse of qmm_repack_weights (a test and debugging aid). */
 qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon, int64_t N,
@@ -203,6 +218,26 @@ qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, in
  *     them on one stream or use qmm_mul_mat_ws with separate workspaces. */
 qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
                               const float *X, int64_t M, float *Y, qmm_stream_t stream);
+
+/* ---------------------------------------------------------------- W4A16 */
+
+/* W4A16 group-asymmetric linear layer (page 3, "从数学表达式到真实存储"):
+ *   C[m, n] = sum_k A[m, k] * s[n, k/G] * (q[n, k] - z[n, k/G])
+ * W_packed: [N, K] codes from qmm_repack_weights(QMM_TYPE_W4A16, ...);
+ * scales: fp16 bit patterns [N][K/G]; zeros: uint8 [N][K/G] (0..15);
+ * A: fp16 [M, K] row-major; C: fp16 [M, N] row-major (written).
+ * Arithmetic: q - z is exact in fp16 and every product A (q - z) exact in
+ * fp32. M <= 16 (decode, mma.sync): fp32 sums over each 128-element step,
+ * times s in fp32. M > 16 (tensor-core GEMM): the weight s (q - z) is
+ * rounded once to fp16 (relative error <= 2^-11) and multiplied on the
+ * tensor cores with fp32 accumulation. C is the fp32 sum rounded to fp16.
+ * Needs G % 128 == 0 and K % G == 0 (QMM_ERR_UNSUPPORTED for other G that
+ * divide K); W_packed and A 16-byte aligned, scales and C 2-byte aligned.
+ * Errors: QMM_ERR_ARG for sizes (M, N >= 0, K > 0, G > 0, K % G == 0) or
+ * null/misaligned pointers. M == 0 or N == 0 is a no-op. */
+qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t *zeros, int64_t G,
+                     const uint16_t *A, uint16_t *C, int64_t M, int64_t N, int64_t K,
+                     qmm_stream_t stream);
 
 /* Per-block integer sums of the factored form, for bit-exact checking
  * (page 1, "正确性" and "通用实现"). Xq holds canonical activation blocks

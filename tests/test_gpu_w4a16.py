@@ -1,0 +1,129 @@
+"""GPU parity of the W4A16 path (page 3: C = A (s (q - z))^T per group),
+through the C ABI, against the oracle's exact (fp64) result.
+
+Bar per element: |C_gpu - C_fp64| <= 1e-3 * sum_k |A[m,k] w[n,k]| + half an
+fp16 ulp of |C_fp64| (C is returned in fp16) + 2^-24 (the fp16 subnormal
+step). The repack is a bit permutation, checked bit-exact by a round trip."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+W = 4  # qmm type id of W4A16
+
+
+@pytest.fixture(scope="module")
+def q():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_quantized_matmul_q4_gb300 as q
+    assert q.QMM_TYPE_W4A16 == W
+    return q
+
+
+def check(c16, ref, den, what):
+    c = c16.astype(np.float64)
+    assert np.all(np.isfinite(c)), f"{what}: non-finite"
+    err = np.abs(c - ref)
+    bound = TOL * den + np.abs(ref) * 2.0 ** -11 + 2.0 ** -24
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} off, worst "
+                           f"{np.max(err / np.maximum(den, 1e-30)):.3e} of den")
+
+
+def pack_torch(qcodes: torch.Tensor) -> torch.Tensor:
+    """Canonical qweight [N, K/8] int32 from codes [N, K] (element 8c + i in
+    bits 4i of word c), for inputs built on the device."""
+    N, K = qcodes.shape
+    v = qcodes.view(N, K // 8, 8).to(torch.int64)
+    word = torch.zeros(N, K // 8, dtype=torch.int64, device=qcodes.device)
+    for i in range(8):
+        word |= v[:, :, i] << (4 * i)
+    return (word - ((word >> 31) << 32)).to(torch.int32).contiguous()
+
+
+def packed_from_canon(q, qweight_dev, N, K):
+    Wp = torch.empty(q.qmm_packed_bytes(W, N, K), dtype=torch.uint8, device="cuda")
+    q.qmm_repack_weights(W, qweight_dev, Wp, N, K)
+    return Wp
+
+
+def run(q, Wp, s16, z, G, A16, M, N, K):
+    C = torch.full((M * N + 32,), float("nan"), dtype=torch.float16, device="cuda")
+    C[M * N:] = 77.0
+    q.qmm_w4a16(Wp, s16, z, G, A16, C, M, N, K)
+    q.qmm_check_device_error()
+    c = C.cpu()
+    assert torch.all(c[M * N:] == 77.0), "write past the end of C"
+    return c[:M * N].view(M, N).numpy()
+
+
+def test_repack_round_trip(q):
+    N, K = 37, 1024
+    g = torch.Generator().manual_seed(5)
+    canon = torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), generator=g, dtype=torch.int64)
+    canon = canon.to(torch.int32).cuda()
+    Wp = packed_from_canon(q, canon, N, K)
+    back = torch.empty_like(canon)
+    q.qmm_unrepack_weights(W, Wp, back, N, K)
+    torch.cuda.synchronize()
+    assert torch.equal(back, canon)
+    assert not torch.equal(Wp.view(torch.int32).view(N, K // 8), canon), "repack is not the identity"
+
+
+@pytest.mark.parametrize("N,K,G,M", [(64, 256, 128, 1), (100, 512, 128, 5), (48, 1024, 256, 16),
+                                     (33, 384, 128, 9), (16, 128, 128, 3), (40, 512, 128, 8),
+                                     (24, 640, 128, 12), (40, 512, 128, 17), (64, 256, 128, 40)])
+def test_w4a16_small(q, orc, N, K, G, M):
+    qc, s16, z, A16 = wl.w4a16_inputs(40, N, K, G, M)
+    qweight = orc.w4a16_pack(qc.numpy())
+    Wp = packed_from_canon(q, torch.from_numpy(qweight.view(np.int32)).cuda(), N, K)
+    c = run(q, Wp, s16.cuda(), z.cuda(), G, A16.cuda(), M, N, K)
+    ref = orc.w4a16_matmul(qweight, s16.view(torch.int16).numpy().view(np.uint16), z.numpy(), G,
+                           A16.view(torch.int16).numpy().view(np.uint16),
+                           nthreads=orc.default_threads())
+    check(c, ref["c64"], ref["den"], f"N={N} K={K} G={G} M={M}")
+
+
+@pytest.mark.parametrize("M", wl.W4A16_M)
+def test_w4a16_full_size_sampled(q, orc, M):
+    """N = K = 8192, G = 128 at M in {1, 16, 256}: inputs generated on the
+    device, every output row computed, 48 sampled rows checked."""
+    N = K = wl.W4A16_N
+    G = wl.W4A16_G
+    qc, s16, z, A16 = wl.w4a16_inputs(41, N, K, G, M, device="cuda")
+    qweight = pack_torch(qc)
+    del qc
+    Wp = packed_from_canon(q, qweight, N, K)
+    c = run(q, Wp, s16, z, G, A16, M, N, K)
+    rows = np.random.default_rng(7).choice(N, 48, replace=False)
+    rows[:2] = (0, N - 1)
+    ref = orc.w4a16_matmul(qweight.cpu().numpy().view(np.uint32), s16.cpu().view(torch.int16).numpy()
+                           .view(np.uint16), z.cpu().numpy(), G,
+                           A16.cpu().view(torch.int16).numpy().view(np.uint16), rows=rows,
+                           nthreads=orc.default_threads())
+    check(c[:, rows], ref["c64"], ref["den"], f"8192x8192 M={M}")
+
+
+def test_w4a16_errors(q):
+    N, K, G, M = 16, 256, 128, 2
+    Wp = torch.zeros(N * K // 2, dtype=torch.uint8, device="cuda")
+    s = torch.ones(N, K // G, dtype=torch.float16, device="cuda")
+    z = torch.zeros(N, K // G, dtype=torch.uint8, device="cuda")
+    A = torch.zeros(M, K, dtype=torch.float16, device="cuda")
+    C = torch.zeros(M, N, dtype=torch.float16, device="cuda")
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_w4a16(Wp, s, z, 64, A, C, M, N, K)  # G % 128 != 0
+    assert e.value.status == 2
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_w4a16(Wp, s, z, 96, A, C, M, N, K)  # K % G != 0
+    assert e.value.status == 1
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_w4a16(Wp, s, z, G, A.view(-1)[1:].data_ptr(), C, M, N, K)  # misaligned A
+    assert e.value.status == 1
+    q.qmm_w4a16(Wp, s, z, G, A, C, 0, N, K)  # M == 0: no-op
+    q.qmm_w4a16(Wp, s, z, G, A, C, M, 0, K)  # N == 0: no-op
+    q.qmm_check_device_error()
