@@ -380,8 +380,50 @@ def prefill_extras(q, dev, stream):
     return out
 
 
+def w4a16_extras(q, dev, stream, reps=8, graph_steps=16):
+    """W4A16 on the 8192 x 8192, G = 128 layer at M in {1, 16, 256}: us per
+    call, GB/s of algorithmic bytes (codes + scales + zeros + A + C) and
+    TOPS (2 M N K). Rotating weight copies larger than L2 at M <= 16."""
+    N = K = wl.W4A16_N
+    G = wl.W4A16_G
+    qc, s16, z, _ = wl.w4a16_inputs(9, N, K, G, 1, device=dev)
+    v = qc.view(N, K // 8, 8).to(torch.int64)
+    del qc
+    word = torch.zeros(N, K // 8, dtype=torch.int64, device=dev)
+    for i in range(8):
+        word |= v[:, :, i] << (4 * i)
+    del v
+    qweight = (word - ((word >> 31) << 32)).to(torch.int32)
+    del word
+    Wp = torch.empty(q.qmm_packed_bytes(q.QMM_TYPE_W4A16, N, K), dtype=torch.uint8, device=dev)
+    q.qmm_repack_weights(q.QMM_TYPE_W4A16, qweight, Wp, N, K)
+    del qweight
+    ncopies = 5  # 5 x 35 MB > the 129 MB L2
+    sets = [(Wp, s16, z)] + [(Wp.clone(), s16.clone(), z.clone()) for _ in range(ncopies - 1)]
+    wbytes = Wp.numel() + s16.numel() * 2 + z.numel()
+    out = {}
+    for M in wl.W4A16_M:
+        A = wl.normal_rows(9, wl.S_A, M, K, device=dev).to(torch.float16)
+        C = torch.empty(M, N, dtype=torch.float16, device=dev)
+        nset = ncopies if M <= 16 else 1
+        step = lambda i: q.qmm_w4a16(*sets[i % nset], G, A, C, M, N, K, stream)
+        for i in range(nset):
+            step(i)
+        g = capture(step, graph_steps, stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        t = timed(stream, lambda: run_graphs(g, None, reps)) / (reps * graph_steps)
+        b = wbytes + 2 * M * K + 2 * M * N
+        out[f"M{M}"] = {"us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
+                        "TOPS": round(2.0 * M * N * K / t / 1e12, 2)}
+    out["shape"] = {"N": N, "K": K, "G": G}
+    return out
+
+
 def gpu_extras(q, dev, stream, args):
     out = {"prefill_q4_K": prefill_extras(q, dev, stream)}
+    out["w4a16_8192"] = w4a16_extras(q, dev, stream)
+    torch.cuda.empty_cache()
     # M sweep of the headline GEMV
     sweep = {}
     L = wl.GEMV_Q4_K_4096
@@ -464,8 +506,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--case", choices=["decode", "prefill"], default="decode",
-                    help="prefill: only the prefill measurement (for profiler captures)")
+    ap.add_argument("--case", choices=["decode", "prefill", "w4a16"], default="decode",
+                    help="prefill / w4a16: only that measurement (for profiler captures)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -497,10 +539,11 @@ def main():
         torch.distributed.init_process_group("nccl")
     else:
         torch.cuda.set_device(0)
-    if args.case == "prefill":
+    if args.case in ("prefill", "w4a16"):
         import block_quantized_matmul_q4_gb300 as q
-        print(json.dumps(prefill_extras(q, torch.device("cuda", torch.cuda.current_device()),
-                                        torch.cuda.Stream())), flush=True)
+        fn = prefill_extras if args.case == "prefill" else w4a16_extras
+        print(json.dumps(fn(q, torch.device("cuda", torch.cuda.current_device()),
+                            torch.cuda.Stream())), flush=True)
         return
     res = gpu_arm(args, rank, world)
     if rank == 0:

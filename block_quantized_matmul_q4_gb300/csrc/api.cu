@@ -221,8 +221,8 @@ int qmm_block_elems(qmm_type t) {
 
 size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K) {
     if (wt == QMM_TYPE_W4A16)
-        return (N > 0 && K > 0 && K % 8 == 0 && K <= ((int64_t)1 << 30) && N <= ((int64_t)1 << 31))
-                   ? (size_t)N * (size_t)(K / 2)
+        return (N > 0 && K > 0 && K % 128 == 0 && K <= ((int64_t)1 << 30) && N <= ((int64_t)1 << 31))
+                   ? (size_t)((N + 15) / 16 * 16) * (size_t)(K / 2)
                    : 0;
     if (!is_weight(wt) || N <= 0 || K <= 0 || K % elems(wt)) return 0;
     return (size_t)tiles_of(N) * kTileRows * (size_t)(K / elems(wt)) * qmm_block_bytes(wt);
@@ -263,14 +263,15 @@ qmm_status qmm_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N
 static qmm_status repack_common(qmm_type wt, const void *src, void *dst, int64_t N, int64_t K,
                                 bool inverse, qmm_stream_t stream) {
     if (wt == QMM_TYPE_W4A16) {
-        QMM_CHECK_ARG(N > 0 && K > 0 && K % 8 == 0, "W4A16 needs N > 0, K > 0, K %% 8 == 0 "
+        QMM_CHECK_ARG(N > 0 && K > 0 && K % 128 == 0, "W4A16 needs N > 0, K > 0, K %% 128 == 0 "
                       "(N=%lld K=%lld)", (long long)N, (long long)K);
         QMM_CHECK_ARG(qmm_packed_bytes(wt, N, K) > 0, "sizes too large");
         QMM_CHECK_ARG(src && dst, "null pointer argument");
         QMM_CHECK_ARG(aligned(src, 16) && aligned(dst, 16), "W4A16 buffers must be 16-byte aligned");
         const uintptr_t a = (uintptr_t)src, b = (uintptr_t)dst;
-        const size_t pb = qmm_packed_bytes(wt, N, K);
-        QMM_CHECK_ARG(a + pb <= b || b + pb <= a, "source and destination overlap");
+        const size_t pb = qmm_packed_bytes(wt, N, K), cb = (size_t)N * (size_t)(K / 2);
+        const size_t sb = inverse ? pb : cb, db = inverse ? cb : pb;
+        QMM_CHECK_ARG(a + sb <= b || b + db <= a, "source and destination overlap");
         return cuda_status(launch_w4a16_repack(inverse, src, dst, N, K, (cudaStream_t)stream),
                            "repack launch");
     }
@@ -422,8 +423,13 @@ qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t
                          (long long)G);
     if (M == 0 || N == 0) return ok();
     QMM_CHECK_ARG(W_packed && scales && zeros && A && C, "null pointer argument");
-    QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(A, 16), "W_packed and A must be 16-byte aligned");
-    QMM_CHECK_ARG(aligned(scales, 2) && aligned(C, 2), "scales and C must be 2-byte aligned");
+    QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(A, 16) && aligned(scales, 16) &&
+                      aligned(zeros, 16),
+                  "W_packed, scales, zeros and A must be 16-byte aligned");
+    QMM_CHECK_ARG(aligned(C, 2), "C must be 2-byte aligned");
+    if (K / G > 256)
+        return set_error(QMM_ERR_UNSUPPORTED, "W4A16 with %lld groups per row: this build stages "
+                         "at most 256 (K / G)", (long long)(K / G));
     cudaStream_t s = (cudaStream_t)stream;
     const __half *S = reinterpret_cast<const __half *>(scales);
     const __half *Ah = reinterpret_cast<const __half *>(A);

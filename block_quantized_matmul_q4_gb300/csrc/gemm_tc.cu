@@ -544,7 +544,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }  // namespace
 
 bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
-                  const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3]) {
+                  const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3],
+                  CUtensorMapSwizzle swizzle) {
     const auto encode = encoder();
     if (!encode) return false;
     const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
@@ -552,7 +553,7 @@ bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
     const cuuint32_t bx[3] = {box[0], box[1], box[2]};
     const cuuint32_t estr[3] = {1, 1, 1};
     return encode(map, dtype, 3, const_cast<void *>(base), d, st, bx, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }

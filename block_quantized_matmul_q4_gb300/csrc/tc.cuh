@@ -157,10 +157,11 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
                   uint32_t elem_bytes, uint64_t rows, uint64_t cols, uint32_t box_rows,
                   uint32_t box_cols, CUtensorMapSwizzle swizzle);
-// 3-D tensor map, no swizzle: dims[0] innermost (elements), byte strides of
-// dims 1 and 2, box extents per dimension.
+// 3-D tensor map: dims[0] innermost (elements), byte strides of dims 1 and
+// 2, box extents per dimension.
 bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
-                  const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3]);
+                  const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3],
+                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
 }  // namespace tc
 }  // namespace qmm

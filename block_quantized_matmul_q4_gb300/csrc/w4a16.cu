@@ -4,28 +4,43 @@
 // with A and C fp16, q 4-bit codes (8 per uint32 word, element 8c + i in
 // bits 4i of word c), s fp16 and z uint8 per (row, group).
 //
-// Layout (qmm_repack_weights, QMM_TYPE_W4A16): the same words, with the
-// nibbles of each word interleaved -- even elements in the low 16 bits,
-// odd ones in the high 16 bits (slots 0..7 hold elements 0,2,4,6,1,3,5,7).
-// One lop3 then turns a word into fp16 pairs (k, k+1) laid out exactly as
-// the tensor-core operands want them (page 3, "Ladder": lay the bits out
-// offline for the decoder), so neither kernel permutes the activations.
+// Layout (qmm_repack_weights, QMM_TYPE_W4A16): rows in tiles of 16 (the
+// last one padded with zero rows); a tile is stored step by step, each
+// 128-element step as its 16 rows x 16 words (1 KB contiguous), so a CTA
+// streams long contiguous runs. Within every word the nibbles are
+// interleaved -- even elements in the low 16 bits, odd ones in the high 16
+// bits (slots 0..7 hold elements 0,2,4,6,1,3,5,7) -- so one lop3 turns a
+// word into fp16 pairs (k, k+1) laid out as the tensor-core operands want
+// them (page 3, "Ladder": lay the bits out offline for the decoder), and no
+// kernel permutes the activations.
 //
 // Decode (M <= 16): mma.sync m16n8k16, weights as the A operand (16 rows per
 // warp), tokens as B (8 per MMA). q - z is exact in fp16 (1024 + q minus
 // 1024 + z, or the x16 form through one fp16 FMA), the products are exact in
 // the fp32 accumulator, and each 128-element step of a group is scaled by s
-// in fp32. Weight and activation words stream from global memory with
-// one step of register prefetch; eight warps split K, then reduce.
-#include "qmm_internal.cuh"
+// in fp32. Decode reads every weight once, so it is bound by HBM: each CTA
+// takes a contiguous range of 16-row tiles, and a producer warp streams
+// them through a 5-stage shared-memory ring (one 16 KB bulk copy of 16
+// steps per stage, so 80 KB in flight per CTA; 64-byte rows, so the
+// consumers' 16-byte reads hit distinct banks), together with each tile's
+// scales and zeros (two slots) and, when small, all activations. Eight
+// consumer warps split each stage's K, then reduce per tile; every load in
+// their loop is from shared memory.
+#include "tc.cuh"
 
 namespace qmm {
 namespace {
 
-constexpr int kStepK = 128;  // elements per warp step (16 words per row)
+constexpr int kStepK = 128;  // elements per warp step: 16 words = 64 bytes per row
 constexpr int kDecodeWarps = 8;
-constexpr int kDecodeThreads = kDecodeWarps * 32;
-constexpr int kRowsPerCta = 16;
+constexpr int kDecodeThreads = (kDecodeWarps + 1) * 32;  // + producer warp
+constexpr int kRowsPerTile = 16;
+constexpr int kStepsPerStage = 16;  // 2048 elements per stage
+constexpr int kDStages = 5;
+constexpr int kDStageBytes = kStepsPerStage * kRowsPerTile * 64;  // 16 KB: [step][row][64 B]
+constexpr int kDRingBytes = kDStages * kDStageBytes;
+constexpr size_t kActStageMax = 16 * 1024;  // activations staged in shared memory up to this
+constexpr int kSzSlots = 2;                // tiles whose scales and zeros are staged at once
 
 __device__ __forceinline__ uint32_t lop_or(uint32_t x, uint32_t mask) {
     uint32_t d;  // (x & mask) | 0x64006400
@@ -50,10 +65,8 @@ struct Zero2 {
     uint32_t zz, zh;
 };
 __device__ __forceinline__ Zero2 make_zero2(uint32_t z) {
-    const uint32_t a = 0x6400u | z;  // fp16 1024 + z (z <= 15)
-    const __half h = __float2half_rn(-64.0f - (float)z);
-    const uint32_t b = (uint32_t)__half_as_ushort(h);
-    return Zero2{a | (a << 16), b | (b << 16)};
+    // z <= 15: fp16 1024 + z is 0x6400 + z, fp16 -(64 + z) is 0xD400 + 16 z
+    return Zero2{0x64006400u + z * 0x00010001u, 0xD400D400u + z * 0x00100010u};
 }
 __device__ __forceinline__ void dequant_word(uint32_t w, const Zero2 &z, uint32_t &p01,
                                              uint32_t &p23, uint32_t &p45, uint32_t &p67) {
@@ -74,125 +87,289 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kDecodeWarps * 32) : "memory");
+}
+
 struct DecodeArgs {
-    const uint32_t *W;  // packed [N][K/8]
-    const __half *S;    // [N][K/G]
-    const uint8_t *Z;   // [N][K/G]
-    const __half *A;    // [M][K]
-    __half *C;          // [M][N]
+    const uint8_t *W;  // packed, tile-major
+    const __half *S;   // [N][K/G]
+    const uint8_t *Z;  // [N][K/G]
+    const __half *A;   // [M][K]
+    __half *C;         // [M][N]
     int64_t M, N, K, G;
+    int ng, spg;  // groups per row, 128-element steps per group
+    unsigned *err;
+    uint32_t act_bytes;  // > 0: all of A staged in shared memory (M * K * 2 bytes)
 };
 
-// One step's operands for one thread: its 4 words of rows r0 and r1, the
-// scale and zero of each row for the step's group, and its 32 activation
-// elements of tokens t/4 (+8 for the second N tile).
+// What one thread needs for one step besides the weights: its 32 activation
+// elements of token t/4 (and t/4 + 8 for the second N tile), the scales of
+// rows r0, r1 and their zeros as the fp16 constants of dequant_word.
 template <int NT>
-struct StepRegs {
-    uint4 w0, w1;
-    __half s0, s1;
-    uint8_t z0, z1;
+struct Operands {
     uint4 x[NT][4];
+    float s0, s1;
+    Zero2 z0, z1;
 };
 
 template <int NT>
-__device__ __forceinline__ void load_step(const DecodeArgs &a, int64_t st, int64_t r0, int64_t r1,
-                                          int j, int tok, StepRegs<NT> &R) {
-    const int64_t kw = a.K / 8, ng = a.K / a.G;
-    const int64_t g = st * kStepK / a.G;
-    const int64_t word = st * (kStepK / 8) + 4 * j;
-    R.w0 = r0 < a.N ? ldg_nc128(a.W + r0 * kw + word) : make_uint4(0, 0, 0, 0);
-    R.w1 = r1 < a.N ? ldg_nc128(a.W + r1 * kw + word) : make_uint4(0, 0, 0, 0);
-    R.s0 = r0 < a.N ? a.S[r0 * ng + g] : __float2half_rn(0.0f);
-    R.s1 = r1 < a.N ? a.S[r1 * ng + g] : __float2half_rn(0.0f);
-    R.z0 = r0 < a.N ? a.Z[r0 * ng + g] : 0;
-    R.z1 = r1 < a.N ? a.Z[r1 * ng + g] : 0;
+__device__ __forceinline__ void load_ops(const DecodeArgs &a, const __half *xs,
+                                         const __half *const (&x_t)[NT], const __half *s_r0,
+                                         const __half *s_r1, const uint8_t *z_r0,
+                                         const uint8_t *z_r1, int st, Operands<NT> &P) {
+    const int g = a.spg == 1 ? st : st / a.spg;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const __half *xp = x_t[nt] + st * kStepK + 8 * q;
+            P.x[nt][q] = a.act_bytes ? *reinterpret_cast<const uint4 *>(xp) : ldg_nc128(xp);
+        }
+    P.s0 = __half2float(s_r0[g * kRowsPerTile]);
+    P.s1 = __half2float(s_r1[g * kRowsPerTile]);
+    P.z0 = make_zero2(z_r0[g * kRowsPerTile]);
+    P.z1 = make_zero2(z_r1[g * kRowsPerTile]);
+}
+
+// One 128-element step of rows r0, r1 against tokens t/4 (+8): 8 (or 16)
+// MMAs on exact q - z, scaled by s once in fp32. Two accumulator chains
+// (even and odd words) halve the dependent MMA latency.
+template <int NT>
+__device__ __forceinline__ void step_mma(const Operands<NT> &P, const uint8_t *wrow, int tok, int j,
+                                         float (&tot)[NT][4]) {
+    const uint4 wv0 = *reinterpret_cast<const uint4 *>(wrow + tok * 64 + 16 * j);
+    const uint4 wv1 = *reinterpret_cast<const uint4 *>(wrow + (tok + 8) * 64 + 16 * j);
+    const uint32_t w0[4] = {wv0.x, wv0.y, wv0.z, wv0.w};
+    const uint32_t w1[4] = {wv1.x, wv1.y, wv1.z, wv1.w};
+    float acc[2][NT][4];
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.0f;
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        // (q - z) pairs of row r0 (u*) and row r1 (v*) for this word
+        uint32_t u01, u23, u45, u67, v01, v23, v45, v67;
+        dequant_word(w0[wi], P.z0, u01, u23, u45, u67);
+        dequant_word(w1[wi], P.z1, v01, v23, v45, v67);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint4 xv = P.x[nt][wi];
+            // MMA 2wi takes elements 8wi + 0..3 of each thread's 32 as the
+            // fragment columns 2j, 2j+1, 2j+8, 2j+9; MMA 2wi + 1 elements
+            // 8wi + 4..7. A (rows r0, r1) and B (token t/4) agree, so the
+            // step's sum is unchanged.
+            mma_16816(acc[wi & 1][nt], u01, v01, u23, v23, xv.x, xv.y);
+            mma_16816(acc[wi & 1][nt], u45, v45, u67, v67, xv.z, xv.w);
+        }
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const int64_t m = nt * 8 + tok;
-        const __half *xp = a.A + m * a.K + st * kStepK + 32 * j;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            R.x[nt][q] = m < a.M ? ldg_nc128(xp + 8 * q) : make_uint4(0, 0, 0, 0);
+        tot[nt][0] = fmaf(P.s0, acc[0][nt][0] + acc[1][nt][0], tot[nt][0]);
+        tot[nt][1] = fmaf(P.s0, acc[0][nt][1] + acc[1][nt][1], tot[nt][1]);
+        tot[nt][2] = fmaf(P.s1, acc[0][nt][2] + acc[1][nt][2], tot[nt][2]);
+        tot[nt][3] = fmaf(P.s1, acc[0][nt][3] + acc[1][nt][3], tot[nt][3]);
     }
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kDecodeThreads, 2) w4a16_decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
+    w4a16_decode_kernel(const DecodeArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ float red[kDecodeWarps][NT][4][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int j = lane & 3, tok = lane >> 2;
-    const int64_t n0 = (int64_t)blockIdx.x * kRowsPerCta;
-    const int64_t r0 = n0 + tok, r1 = n0 + tok + 8;
+    const int64_t ntiles = (a.N + kRowsPerTile - 1) / kRowsPerTile;
+    const int64_t tb = (int64_t)blockIdx.x * ntiles / gridDim.x;
+    const int64_t te = ((int64_t)blockIdx.x + 1) * ntiles / gridDim.x;
     const int64_t nsteps = a.K / kStepK;
-    float tot[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tot[nt][i] = 0.0f;
+    const int64_t spt = (nsteps + kStepsPerStage - 1) / kStepsPerStage;  // stages per tile
+    // a tile's scales (16 rows x ng fp16) and zeros (16 x ng bytes), contiguous
+    // in global memory and in its shared-memory slot
+    const uint32_t s_bytes = (uint32_t)kRowsPerTile * (uint32_t)a.ng * 2u;
+    const uint32_t z_bytes = (uint32_t)kRowsPerTile * (uint32_t)a.ng;
+    const uint32_t sz_slot = s_bytes + z_bytes;  // multiple of 48
 
-    StepRegs<NT> cur, nxt;
-    int64_t st = warp;
-    if (st < nsteps) load_step<NT>(a, st, r0, r1, j, tok, cur);
-    for (; st < nsteps; st += kDecodeWarps) {
-        if (st + kDecodeWarps < nsteps) load_step<NT>(a, st + kDecodeWarps, r0, r1, j, tok, nxt);
-        const Zero2 z0 = make_zero2(cur.z0), z1 = make_zero2(cur.z1);
-        const uint32_t w0[4] = {cur.w0.x, cur.w0.y, cur.w0.z, cur.w0.w};
-        const uint32_t w1[4] = {cur.w1.x, cur.w1.y, cur.w1.z, cur.w1.w};
-        float acc[NT][4];
+    // shared memory: weight ring | activations | scale/zero slots | barriers
+    __half *x_sm = reinterpret_cast<__half *>(smem + kDRingBytes);
+    uint8_t *sz_sm = smem + kDRingBytes + a.act_bytes;
+    // the current tile's scales and zeros transposed to [group][16 rows], so
+    // that the 8 rows a warp reads at once sit in neighbouring banks
+    __half *s_tr = reinterpret_cast<__half *>(sz_sm + kSzSlots * sz_slot);
+    uint8_t *z_tr = reinterpret_cast<uint8_t *>(s_tr) + s_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(z_tr + z_bytes);
+    uint64_t *empty = full + kDStages;
+    uint64_t *szfull = empty + kDStages;
+    uint64_t *szempty = szfull + kSzSlots;
+    uint64_t *actb = szempty + kSzSlots;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kDStages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), kDecodeWarps);
+        }
+        for (int i = 0; i < kSzSlots; ++i) {
+            mbar_init(smem_u32(&szfull[i]), 1);
+            mbar_init(smem_u32(&szempty[i]), kDecodeWarps);
+        }
+        mbar_init(smem_u32(actb), 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kDecodeWarps) {
+        // ------------------------------------------------------------ producer
+        // Per tile: its scales and zeros, then its weight stages; the ring
+        // holds five stages, so every CTA keeps 80 KB of weights in flight.
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();  // every weight is read once
+            if (a.act_bytes) {
+                pdl_wait();  // the activations may come from the preceding kernel
+                mbar_arrive_expect_tx(smem_u32(actb), a.act_bytes);
+                bulk_g2s(smem_u32(x_sm), a.A, a.act_bytes, smem_u32(actb), policy_evict_last());
+            }
+            int64_t it = 0;
+            bool ok = true;
+            for (int64_t tile = tb; tile < te && ok; ++tile) {
+                const int64_t ti = tile - tb;
+                const int zs = (int)(ti % kSzSlots);
+                ok = mbar_wait(smem_u32(&szempty[zs]), (uint32_t)(((ti / kSzSlots) & 1) ^ 1), a.err);
+                if (!ok) break;
+                {
+                    // the tile's rows of scales and zeros: the 16-byte multiple by
+                    // bulk copy, a short tail (a partial last tile) by this thread
+                    // before its arrival publishes the slot
+                    const int64_t rows = a.N - tile * kRowsPerTile < kRowsPerTile
+                                             ? a.N - tile * kRowsPerTile : kRowsPerTile;
+                    const uint32_t sb = (uint32_t)rows * (uint32_t)a.ng * 2u, zb = (uint32_t)rows * (uint32_t)a.ng;
+                    const uint32_t sb16 = sb & ~15u, zb16 = zb & ~15u;
+                    const uint8_t *ssrc = reinterpret_cast<const uint8_t *>(a.S + tile * kRowsPerTile * a.ng);
+                    const uint8_t *zsrc = a.Z + tile * kRowsPerTile * a.ng;
+                    uint8_t *dst = sz_sm + zs * sz_slot;
+                    for (uint32_t b = sb16; b < sb; ++b) dst[b] = ssrc[b];
+                    for (uint32_t b = zb16; b < zb; ++b) dst[s_bytes + b] = zsrc[b];
+                    const uint32_t bar = smem_u32(&szfull[zs]);
+                    mbar_arrive_expect_tx(bar, sb16 + zb16);
+                    if (sb16) bulk_g2s(smem_u32(dst), ssrc, sb16, bar, pol);
+                    if (zb16) bulk_g2s(smem_u32(dst + s_bytes), zsrc, zb16, bar, pol);
+                }
+                for (int64_t sg = 0; sg < spt; ++sg, ++it) {
+                    const int s = (int)(it % kDStages);
+                    ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((it / kDStages) & 1) ^ 1), a.err);
+                    if (!ok) break;
+                    const int64_t step0 = sg * kStepsPerStage;
+                    const int64_t nst = nsteps - step0 < kStepsPerStage ? nsteps - step0 : kStepsPerStage;
+                    const uint32_t bar = smem_u32(&full[s]);
+                    // steps past K are not copied (and never read)
+                    mbar_arrive_expect_tx(bar, (uint32_t)nst * 1024u);
+                    bulk_g2s(smem_u32(smem + s * kDStageBytes), a.W + (tile * nsteps + step0) * 1024,
+                             (uint32_t)nst * 1024u, bar, pol);
+                }
+            }
+            // drain: nothing may still be landing when the CTA exits
+            for (int64_t k = it > kDStages ? it - kDStages : 0; k < it; ++k)
+                mbar_wait(smem_u32(&full[k % kDStages]), (uint32_t)((k / kDStages) & 1), a.err);
+            const int64_t nt_issued = te - tb;
+            for (int64_t k = nt_issued > kSzSlots ? nt_issued - kSzSlots : 0; k < nt_issued; ++k)
+                mbar_wait(smem_u32(&szfull[k % kSzSlots]), (uint32_t)((k / kSzSlots) & 1), a.err);
+            if (a.act_bytes) mbar_wait(smem_u32(actb), 0, a.err);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // After a timed-out wait a warp stops waiting but keeps its place in the
+    // per-tile barriers (results are garbage, the error word says so), so no
+    // warp can be left waiting for another.
+    const int j = lane & 3, tok = lane >> 2;
+    bool ok = true;
+    const __half *xs = a.A;
+    if (a.act_bytes) {
+        ok = mbar_wait(smem_u32(actb), 0, a.err);
+        xs = x_sm;
+    } else {
+        pdl_wait();  // the activations may come from the preceding kernel
+    }
+    int64_t it = 0;
+    for (int64_t tile = tb; tile < te; ++tile) {
+        const int64_t ti = tile - tb;
+        const int zs = (int)(ti % kSzSlots);
+        if (ok) ok = mbar_wait(smem_u32(&szfull[zs]), (uint32_t)((ti / kSzSlots) & 1), a.err);
+        const int64_t r0 = tile * kRowsPerTile + tok, r1 = r0 + 8;
+        // Rows past N (zero weights) and tokens past M read valid addresses
+        // (clamped tokens, stale scale slots); they only feed outputs that are
+        // never stored, so no load needs a predicate.
+        {
+            const __half *s_all = reinterpret_cast<const __half *>(sz_sm + zs * sz_slot);
+            const uint8_t *z_all = sz_sm + zs * sz_slot + s_bytes;
+            for (int i = threadIdx.x; i < kRowsPerTile * a.ng; i += kDecodeWarps * 32) {
+                const int r = i / a.ng, g = i - r * a.ng;
+                s_tr[g * kRowsPerTile + r] = s_all[i];
+                z_tr[g * kRowsPerTile + r] = z_all[i];
+            }
+            consumers_sync();
+            if (lane == 0) mbar_arrive(smem_u32(&szempty[zs]));  // slot free again
+        }
+        // scales / zeros of rows r0, r1 for group g at index g * 16 (stride 16)
+        const __half *s_r0 = s_tr + tok, *s_r1 = s_tr + tok + 8;
+        const uint8_t *z_r0 = z_tr + tok, *z_r1 = z_tr + tok + 8;
+        const __half *x_t[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int64_t m = nt * 8 + tok < a.M ? nt * 8 + tok : a.M - 1;
+            x_t[nt] = xs + m * a.K + 32 * j;
+        }
+        float tot[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+            for (int i = 0; i < 4; ++i) tot[nt][i] = 0.0f;
+        // This warp's steps are warp + 8k, k = 0 .. nk-1, two per stage. While
+        // it computes step k it has the operands of step k + 1 in flight (two
+        // register sets, alternating).
+        constexpr int kPerStage = kStepsPerStage / kDecodeWarps;
+        const int nk = warp < nsteps ? (int)((nsteps - 1 - warp) / kDecodeWarps) + 1 : 0;
+        Operands<NT> P[2];
+        if (nk > 0) load_ops<NT>(a, xs, x_t, s_r0, s_r1, z_r0, z_r1, warp, P[0]);
+        for (int64_t sg = 0; sg < spt; ++sg, ++it) {
+            const int s = (int)(it % kDStages);
+            if (ok) ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((it / kDStages) & 1), a.err);
+            const uint8_t *stage = smem + s * kDStageBytes;
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-            // (q - z) pairs of row r0 (u*) and row r1 (v*) for this word
-            uint32_t u01, u23, u45, u67, v01, v23, v45, v67;
-            dequant_word(w0[wi], z0, u01, u23, u45, u67);
-            dequant_word(w1[wi], z1, v01, v23, v45, v67);
+            for (int h = 0; h < kPerStage; ++h) {
+                const int k = (int)sg * kPerStage + h;
+                if (k < nk) {
+                    const int ls = warp + h * kDecodeWarps;
+                    if (k + 1 < nk)
+                        load_ops<NT>(a, xs, x_t, s_r0, s_r1, z_r0, z_r1, warp + (k + 1) * kDecodeWarps,
+                                     P[(h + 1) & 1]);
+                    step_mma<NT>(P[h & 1], stage + ls * 1024, tok, j, tot);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        }
+        // reduce the consumer warps' partial sums of this tile
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const uint32_t xs[4] = {cur.x[nt][wi].x, cur.x[nt][wi].y, cur.x[nt][wi].z,
-                                        cur.x[nt][wi].w};
-                // MMA 2wi takes elements 8wi + 0..3 of each thread's 32 as the
-                // fragment columns 2j, 2j+1, 2j+8, 2j+9; MMA 2wi + 1 elements
-                // 8wi + 4..7. A (rows r0, r1) and B (token t/4) agree, so the
-                // sum over the step is unchanged.
-                mma_16816(acc[nt], u01, v01, u23, v23, xs[0], xs[1]);
-                mma_16816(acc[nt], u45, v45, u67, v67, xs[2], xs[3]);
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red[warp][nt][i][lane] = tot[nt][i];
+        consumers_sync();
+        if (warp < NT) {
+            const int nt = warp;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float sum = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kDecodeWarps; ++w) sum += red[w][nt][i][lane];
+                // c0, c1: row t/4, tokens 2j, 2j+1; c2, c3: row t/4 + 8
+                const int64_t n = (i < 2) ? r0 : r1;
+                const int64_t m = nt * 8 + 2 * j + (i & 1);
+                if (n < a.N && m < a.M) a.C[m * a.N + n] = __float2half_rn(sum);
             }
         }
-        const float s0 = __half2float(cur.s0), s1 = __half2float(cur.s1);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            tot[nt][0] = fmaf(s0, acc[nt][0], tot[nt][0]);
-            tot[nt][1] = fmaf(s0, acc[nt][1], tot[nt][1]);
-            tot[nt][2] = fmaf(s1, acc[nt][2], tot[nt][2]);
-            tot[nt][3] = fmaf(s1, acc[nt][3], tot[nt][3]);
-        }
-        cur = nxt;
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) red[warp][nt][i][lane] = tot[nt][i];
-    __syncthreads();
-    if (warp < NT) {
-        const int nt = warp;
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float sum = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kDecodeWarps; ++w) sum += red[w][nt][i][lane];
-            v[i] = sum;
-        }
-        // c0, c1: row t/4, tokens 2j, 2j+1; c2, c3: row t/4 + 8, same tokens
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t n = (i < 2) ? r0 : r1;
-            const int64_t m = nt * 8 + 2 * j + (i & 1);
-            if (n < a.N && m < a.M) a.C[m * a.N + n] = __float2half_rn(v[i]);
-        }
+        consumers_sync();
     }
 }
 
@@ -216,24 +393,41 @@ __device__ __forceinline__ uint32_t unpack_word(uint32_t p) {
     }
     return c;
 }
+// Word index in the packed buffer of word c of row n (K/8 words per row).
+__host__ __device__ __forceinline__ int64_t packed_index(int64_t n, int64_t c, int64_t nsteps) {
+    const int64_t t = n / kRowsPerTile, r = n % kRowsPerTile;
+    const int64_t st = c / (kStepK / 8), w = c % (kStepK / 8);
+    return ((t * nsteps + st) * kRowsPerTile + r) * (kStepK / 8) + w;
+}
+// One thread per packed word (padding rows included): forward reads the
+// canonical word (or writes zero for a padding row), inverse writes it back.
 __global__ void w4a16_repack_kernel(const uint32_t *__restrict__ src, uint32_t *__restrict__ dst,
-                                    int64_t nwords, bool inverse) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nwords;
-         i += (int64_t)gridDim.x * blockDim.x)
-        dst[i] = inverse ? unpack_word(src[i]) : pack_word(src[i]);
+                                    int64_t N, int64_t K, bool inverse) {
+    const int64_t kw = K / 8, nsteps = K / kStepK;
+    const int64_t npad = (N + kRowsPerTile - 1) / kRowsPerTile * kRowsPerTile;
+    const int64_t total = npad * kw;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / kw, c = i % kw;
+        const int64_t pi = packed_index(n, c, nsteps);
+        if (!inverse)
+            dst[pi] = n < N ? pack_word(src[n * kw + c]) : 0u;
+        else if (n < N)
+            dst[n * kw + c] = unpack_word(src[pi]);
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_w4a16_repack(bool inverse, const void *src, void *dst, int64_t N, int64_t K,
                                 cudaStream_t s) {
-    const int64_t nwords = N * (K / 8);
+    const int64_t nwords = (N + kRowsPerTile - 1) / kRowsPerTile * kRowsPerTile * (K / 8);
     int64_t grid = (nwords + 255) / 256;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     w4a16_repack_kernel<<<(int)grid, 256, 0, s>>>(static_cast<const uint32_t *>(src),
-                                                  static_cast<uint32_t *>(dst), nwords, inverse);
+                                                  static_cast<uint32_t *>(dst), N, K, inverse);
     count_launch();
     return cudaGetLastError();
 }
@@ -242,7 +436,7 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
                                 const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
                                 cudaStream_t s) {
     DecodeArgs a;
-    a.W = static_cast<const uint32_t *>(W);
+    a.W = static_cast<const uint8_t *>(W);
     a.S = S;
     a.Z = Z;
     a.A = A;
@@ -251,11 +445,27 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
     a.N = N;
     a.K = K;
     a.G = G;
-    const unsigned grid = (unsigned)((N + kRowsPerCta - 1) / kRowsPerCta);
-    if (M <= 8)
-        w4a16_decode_kernel<1><<<grid, kDecodeThreads, 0, s>>>(a);
-    else
-        w4a16_decode_kernel<2><<<grid, kDecodeThreads, 0, s>>>(a);
+    a.ng = (int)(K / G);
+    a.spg = (int)(G / kStepK);
+    a.err = device_error_word();
+    const int64_t ntiles = (N + kRowsPerTile - 1) / kRowsPerTile;
+    int64_t grid = (M <= 8 ? 2 : 1) * (int64_t)sm_count();
+    if (grid > ntiles) grid = ntiles;
+    // all of A in shared memory when it is small (one bulk copy per CTA)
+    const size_t act = (size_t)M * K * 2;
+    a.act_bytes = act <= kActStageMax ? (uint32_t)act : 0u;
+    const size_t sz = (size_t)(kSzSlots + 1) * kRowsPerTile * a.ng * 3;
+    const size_t smem = kDRingBytes + a.act_bytes + sz + (2 * kDStages + 2 * kSzSlots + 1) * 8;
+    cudaError_t e;
+    if (M <= 8) {
+        e = ensure_smem_attr(reinterpret_cast<const void *>(w4a16_decode_kernel<1>), smem);
+        if (e != cudaSuccess) return e;
+        w4a16_decode_kernel<1><<<(unsigned)grid, kDecodeThreads, smem, s>>>(a);
+    } else {
+        e = ensure_smem_attr(reinterpret_cast<const void *>(w4a16_decode_kernel<2>), smem);
+        if (e != cudaSuccess) return e;
+        w4a16_decode_kernel<2><<<(unsigned)grid, kDecodeThreads, smem, s>>>(a);
+    }
     count_launch();
     return cudaGetLastError();
 }

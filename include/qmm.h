@@ -82,8 +82,8 @@ int qmm_block_elems(qmm_type t);
 
 /* Bytes of the packed (repacked) weight buffer for an [N, K] weight of type
  * Q4_0, Q4_K or W4A16; 0 if the type or sizes are invalid. Q4_0/Q4_K rows
- * are padded to a multiple of 8 with zero blocks; W4A16 takes N * K / 2
- * bytes (K % 8 == 0), no padding. */
+ * are padded to a multiple of 8 with zero blocks, W4A16 rows to a multiple
+ * of 16 (K % 128 == 0): ceil(N / 16) * 16 * K / 2 bytes. */
 size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K);
 
 /* Bytes of the workspace qmm_mul_mat_ws needs for M activation rows of
@@ -137,13 +137,15 @@ qmm_status qmm_repack_weights(qmm_type wt, const void *W_canon, void *W_packed, 
                               int64_t K, qmm_stream_t stream);
 
 /* W4A16 (wt = QMM_TYPE_W4A16): W_canon is qweight [N][K/8] uint32, element
- * k = 8c + i of a row in bits 4i..4i+3 of word c (page 3, "位级打包"); the
- * packed layout keeps every word in place and interleaves its nibbles, the
- * even elements in the low 16 bits and the odd ones in the high 16 bits
- * (nibble slots 0..7 hold elements 0, 2, 4, 6, 1, 3, 5, 7), so that one
- * mask turns a word into fp16 pairs (k, k + 1) (page 3, "Ladder": the
- * weight is laid out once for the decoder). Needs K % 8 == 0; both buffers
- * 16-byte aligned. */
+ * k = 8c + i of a row in bits 4i..4i+3 of word c (page 3, "位级打包"). The
+ * packed layout groups rows in tiles of 16 (zero rows pad the last one) and
+ * stores a tile as consecutive 1 KB pieces, one per 128 elements of K (its
+ * 16 rows x 16 words), and interleaves the nibbles of every word, even
+ * elements in the low 16 bits and odd ones in the high 16 bits (nibble
+ * slots 0..7 hold elements 0, 2, 4, 6, 1, 3, 5, 7), so that one mask turns
+ * a word into fp16 pairs (k, k + 1) (page 3, "Ladder": the weight is laid
+ * out once for the decoder). Needs K % 128 == 0; both buffers 16-byte
+ * aligned; the packed buffer has qmm_packed_bytes bytes. */
 
 /* Inverse of qmm_repack_weights (a test and debugging aid). */
 qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon, int64_t N,
@@ -232,7 +234,8 @@ qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int64_t N, int6
  * rounded once to fp16 (relative error <= 2^-11) and multiplied on the
  * tensor cores with fp32 accumulation. C is the fp32 sum rounded to fp16.
  * Needs G % 128 == 0 and K % G == 0 (QMM_ERR_UNSUPPORTED for other G that
- * divide K); W_packed and A 16-byte aligned, scales and C 2-byte aligned.
+ * divide K) and K / G <= 256 (QMM_ERR_UNSUPPORTED above); W_packed,
+ * scales, zeros and A 16-byte aligned, C 2-byte aligned.
  * Errors: QMM_ERR_ARG for sizes (M, N >= 0, K > 0, G > 0, K % G == 0) or
  * null/misaligned pointers. M == 0 or N == 0 is a no-op. */
 qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t *zeros, int64_t G,
