@@ -434,14 +434,10 @@ qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t
     const __half *S = reinterpret_cast<const __half *>(scales);
     const __half *Ah = reinterpret_cast<const __half *>(A);
     __half *Ch = reinterpret_cast<__half *>(C);
-    // decode kernel on up to 16 tokens at a time
-    for (int64_t m0 = 0; m0 < M; m0 += 16) {
-        const int64_t mt = M - m0 < 16 ? M - m0 : 16;
-        cudaError_t e = launch_w4a16_decode(W_packed, S, zeros, G, Ah + m0 * K, Ch + m0 * N, mt, N,
-                                            K, s);
-        if (e != cudaSuccess) return cuda_status(e, "W4A16 kernel launch");
-    }
-    return ok();
+    // up to 16 tokens: the decode kernel (HBM-bound); more: the tensor-core GEMM
+    cudaError_t e = M <= 16 ? launch_w4a16_decode(W_packed, S, zeros, G, Ah, Ch, M, N, K, s)
+                            : launch_w4a16_gemm(W_packed, S, zeros, G, Ah, Ch, M, N, K, s);
+    return cuda_status(e, "W4A16 kernel launch");
 }
 
 }  // extern "C"

@@ -372,6 +372,9 @@ cudaError_t launch_w4a16_repack(bool inverse, const void *src, void *dst, int64_
 cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z, int64_t G,
                                 const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
                                 cudaStream_t s);
+cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, int64_t G,
+                              const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
+                              cudaStream_t s);
 cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
                                     const void *Xq, int64_t M, int32_t *out, cudaStream_t s);
 }  // namespace qmm

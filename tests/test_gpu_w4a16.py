@@ -77,7 +77,9 @@ def test_repack_round_trip(q):
 
 @pytest.mark.parametrize("N,K,G,M", [(64, 256, 128, 1), (100, 512, 128, 5), (48, 1024, 256, 16),
                                      (33, 384, 128, 9), (16, 128, 128, 3), (40, 512, 128, 8),
-                                     (24, 640, 128, 12), (40, 512, 128, 17), (64, 256, 128, 40)])
+                                     (24, 640, 128, 12), (40, 512, 128, 17), (64, 256, 128, 40),
+                                     (100, 384, 128, 130), (200, 640, 128, 33), (48, 1024, 256, 200),
+                                     (136, 1152, 384, 257)])
 def test_w4a16_small(q, orc, N, K, G, M):
     qc, s16, z, A16 = wl.w4a16_inputs(40, N, K, G, M)
     qweight = orc.w4a16_pack(qc.numpy())
