@@ -122,13 +122,14 @@ void prepare_pool() {
     g_pool_ready[d] = true;
 }
 
-// Q4_K with more than 16 tokens runs the tensor-core GEMM and its workspace
-// layout; everything else the decode GEMV and the planar layout.
-bool use_gemm(qmm_type wt, int64_t M) { return wt == QMM_TYPE_Q4_K && M >= kGemmMinM; }
+// More than 16 tokens run the tensor-core GEMMs and their workspace layouts
+// (Q4_K: integer-valued fp16 codes; Q4_0: fp16 dequantized activations);
+// fewer the decode GEMV and the planar layout.
+bool use_gemm(qmm_type wt, int64_t M) { return M >= kGemmMinM; }
 
 size_t ws_bytes_for(qmm_type wt, int64_t M, int64_t K) {
-    return use_gemm(wt, M) ? prefill_bytes(M, K, nullptr, nullptr)
-                           : planar_bytes(M, K, elems(wt), nullptr, nullptr);
+    if (!use_gemm(wt, M)) return planar_bytes(M, K, elems(wt), nullptr, nullptr);
+    return wt == QMM_TYPE_Q4_K ? prefill_bytes(M, K, nullptr, nullptr) : q4_0_prefill_bytes(M, K);
 }
 
 qmm_status carve(qmm_type wt, int64_t M, int64_t K, const void *ws, size_t ws_bytes, Planar *p) {
@@ -141,10 +142,13 @@ qmm_status carve(qmm_type wt, int64_t M, int64_t K, const void *ws, size_t ws_by
 qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K, void *ws,
                               size_t ws_bytes, cudaStream_t s) {
     if (use_gemm(wt, M)) {
-        PrefillWs pw;
-        const size_t need = prefill_bytes(M, K, &pw, (uint8_t *)ws);
+        const size_t need = ws_bytes_for(wt, M, K);
         if (ws_bytes < need)
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+        if (wt == QMM_TYPE_Q4_0)
+            return cuda_status(launch_quantize_q4_0_prefill(X, ws, M, K, s), "prefill quantizer launch");
+        PrefillWs pw;
+        prefill_bytes(M, K, &pw, (uint8_t *)ws);
         return cuda_status(launch_quantize_prefill(X, pw, M, K, s), "prefill quantizer launch");
     }
     Planar p;
@@ -157,10 +161,13 @@ qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K,
 qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, const void *ws,
                          size_t ws_bytes, int64_t M, float *Y, cudaStream_t s) {
     if (use_gemm(wt, M)) {
-        PrefillWs pw;
-        const size_t need = prefill_bytes(M, K, &pw, (uint8_t *)ws);
+        const size_t need = ws_bytes_for(wt, M, K);
         if (ws_bytes < need)
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+        if (wt == QMM_TYPE_Q4_0)
+            return cuda_status(launch_gemm_q4_0(Wp, N, K, ws, M, Y, s), "prefill GEMM launch");
+        PrefillWs pw;
+        prefill_bytes(M, K, &pw, (uint8_t *)ws);
         return cuda_status(launch_gemm_q4_K(Wp, N, K, pw, M, Y, s), "prefill GEMM launch");
     }
     Planar p;

@@ -1,0 +1,495 @@
+// gemm_f16.cu -- tensor-core GEMMs whose weights are decoded to fp16 on the
+// way into the operand (page 3, "BitBLAS 完全拆解": "边解码边计算"), for the
+// formats whose scales cannot be taken out of the sum once per 256
+// elements:
+//   W4A16 (page 3, "从数学表达式到真实存储"): C = A w^T, w = fp16(s (q - z)),
+//     A fp16 as given, C fp16.
+//   Q4_0 prefill (page 1, "最基础的两块"): Y = a w^T, w = fp16(d_w (q - 8)),
+//     a = fp16(d_a y) from the Q8_0 codes y of X (both sides carry a scale
+//     per 32 elements, so no integer sum spans more than one MMA K step;
+//     both operands are rounded once to fp16 instead), Y fp32.
+// In both, q - z (q - 8) is exact in fp16 and the product with the scale is
+// rounded once (relative error <= 2^-11); the MMA accumulates in fp32 over
+// all of K.
+//
+// CTA = 128 weight rows (MMA M) x 128 tokens (MMA N), 15 warps:
+//   warp 0      producer: per 256 elements of K one weight stage (TMA copies
+//               of the packed tiles of the CTA's 128 rows) and one activation
+//               stage of four 2-D TMA tiles (128B swizzle, 64 KB);
+//   warp 1      MMA issuer (one thread) and TMEM owner;
+//   warp 2      MMA waiter: the issuer's barrier waits, handed over per pair
+//               of K chunks through a named barrier (a shared-memory access
+//               by the issuing thread would drain the tensor pipe);
+//   warps 3..10 converters, two sets of four: one weight row per thread
+//               (its TMEM lane), fp16 weights built in registers and stored
+//               into a TMEM operand ring with tcgen05.st;
+//   warps 11..14 epilogue: one tcgen05.ld pass over the accumulator at the
+//               end.
+// All mbarrier waits are bounded; on a timeout the CTA drains its copies and
+// MMAs, frees its TMEM and returns with the device error word set.
+#include "tc.cuh"
+
+namespace qmm {
+namespace {
+
+enum Format { kW4A16 = 0, kQ40 = 1 };
+
+constexpr int kBM = 128, kBN = 128, kBK = 64;  // rows, tokens, K per chunk
+constexpr int kSB = 256;                       // K per pipeline round
+constexpr int kChunks = kSB / kBK;             // 4
+constexpr int kGroups = 2;                     // A handed over in pairs of chunks
+constexpr int kWStages = 3, kActStages = 2;
+constexpr int kWBytesMax = 16384 + 2048;       // Q4_0: nibbles + scales
+constexpr int kChunkBytes = kBN * kBK * 2;     // 16 KB
+constexpr int kActBytes = kChunks * kChunkBytes;  // 64 KB
+constexpr int kConvWarps = 8, kEpiWarps = 4;
+constexpr int kThreads = (3 + kConvWarps + kEpiWarps) * 32;
+constexpr int kOffAct = 0;
+constexpr int kOffW = kOffAct + kActStages * kActBytes;
+constexpr int kOffBar = kOffW + kWStages * kWBytesMax;
+constexpr int kNumBars = 2 * (kWStages + kActStages + kGroups) + 2;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColAcc = 0, kColARing = kBN;
+constexpr uint32_t kARingCols = kBK / 2;
+static_assert(kColARing + kChunks * kARingCols <= kTmemCols, "TMEM budget");
+
+// W4A16 packed tiles: 16 rows, steps of 128 elements (1 KB each).
+constexpr int kW4StepK = 128, kW4Tile = 16;
+// Q4_0 packed tiles: 8 rows; per tile [8][nb][16 B nibbles] then [nb][8] fp16.
+constexpr int kQ4Tile = kTileRows;
+constexpr int kQ4Blocks = kSB / QK4_0;  // blocks per stage: 8
+constexpr int kQ4NibBytes = (kBM / kQ4Tile) * kQ4Blocks * kQ4Tile * 16;  // 16 KB
+
+template <int F>
+struct FmtInfo {
+    static constexpr int kWBytes = F == kW4A16 ? (kBM / kW4Tile) * (kSB / kW4StepK) * 1024
+                                               : kQ4NibBytes + (kBM / kQ4Tile) * kQ4Blocks * 16;
+};
+
+struct Args {
+    const __half *S;   // W4A16: [N][ng]
+    const uint8_t *Z;  // W4A16: [N][ng]
+    void *C;           // W4A16: fp16 [M][N]; Q4_0: fp32 [M][N]
+    int64_t M, N, K;
+    int ng, spg;  // W4A16: groups per row, 128-element steps per group
+    unsigned *err;
+};
+
+__device__ __forceinline__ uint32_t lop_or(uint32_t x, uint32_t mask) {
+    uint32_t d;  // (x & mask) | 0x64006400
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(mask), "r"(0x64006400u));
+    return d;
+}
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ void handoff_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+
+// fp16 scale * (q - zero) for the 8 codes of one word, as four pairs of
+// (low 16 bits, high 16 bits) fields: fields at bits 0-3 | 16-19, 8-11 |
+// 24-27 (via w >> 8), 4-7 | 20-23 and 12-15 | 28-31. zz = fp16(1024 + zero)
+// twice, zh = fp16(-(64 + zero)) twice, ss = the scale twice. q - zero is
+// exact (1024 + q minus 1024 + zero, or the x16 form through one FMA); the
+// product with the scale is one rounding.
+__device__ __forceinline__ void scaled_word(uint32_t w, uint32_t zz, uint32_t zh, uint32_t ss,
+                                            uint32_t &f0, uint32_t &f8, uint32_t &f4,
+                                            uint32_t &f12) {
+    constexpr uint32_t kSixteenth = 0x2C002C00u;  // fp16 1/16 twice
+    const uint32_t v = w >> 8;
+    f0 = hmul2_u(hsub2_u(lop_or(w, 0x000F000Fu), zz), ss);
+    f8 = hmul2_u(hsub2_u(lop_or(v, 0x000F000Fu), zz), ss);
+    f4 = hmul2_u(hfma2_u(lop_or(w, 0x00F000F0u), kSixteenth, zh), ss);
+    f12 = hmul2_u(hfma2_u(lop_or(v, 0x00F000F0u), kSixteenth, zh), ss);
+}
+
+template <int F>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_f16_kernel(const Args a, const __grid_constant__ CUtensorMap tmap_w,
+                    const __grid_constant__ CUtensorMap tmap_d,
+                    const __grid_constant__ CUtensorMap tmap_a) {
+    constexpr int kWBytes = FmtInfo<F>::kWBytes;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw_base);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n0 = (int64_t)blockIdx.x * kBM, m0 = (int64_t)blockIdx.y * kBN;
+    const int64_t nsb = (a.K + kSB - 1) / kSB;
+
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *w_full = bar, *w_empty = w_full + kWStages;
+    uint64_t *act_full = w_empty + kWStages, *act_empty = act_full + kActStages;
+    uint64_t *a_full = act_empty + kActStages, *a_empty = a_full + kGroups;
+    uint64_t *acc_full = a_empty + kGroups, *done = acc_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kWStages; ++i) {
+            mbar_init(smem_u32(&w_full[i]), 1);
+            mbar_init(smem_u32(&w_empty[i]), kConvWarps);
+        }
+        for (int i = 0; i < kActStages; ++i) {
+            mbar_init(smem_u32(&act_full[i]), 1);
+            mbar_init(smem_u32(&act_empty[i]), 1);
+        }
+        for (int i = 0; i < kGroups; ++i) {
+            mbar_init(smem_u32(&a_full[i]), kConvWarps);  // both sets, one chunk each
+            mbar_init(smem_u32(&a_empty[i]), 1);
+        }
+        mbar_init(smem_u32(acc_full), 1);
+        mbar_init(smem_u32(done), 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tc::prefetch_tensormap(&tmap_w);
+            if (F == kQ40) tc::prefetch_tensormap(&tmap_d);
+            tc::prefetch_tensormap(&tmap_a);
+            const uint64_t pol = policy_evict_last();  // weights and A are reused by other CTAs
+            pdl_wait();  // the activations may come from the preceding kernel
+            int64_t issued_w = 0, issued_a = 0;
+            bool ok = true;
+            for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+                const int ws = (int)(sb % kWStages);
+                ok = mbar_wait(smem_u32(&w_empty[ws]), (uint32_t)(((sb / kWStages) & 1) ^ 1), a.err);
+                if (!ok) break;
+                // rows past the last tile and K past the end read as zeros
+                const uint32_t wbar = smem_u32(&w_full[ws]);
+                uint8_t *wdst = smem + kOffW + ws * kWBytesMax;
+                mbar_arrive_expect_tx(wbar, kWBytes);
+                if (F == kW4A16) {
+                    // 8 tiles x 2 steps: [tile][step][16 rows x 64 B]
+                    tc::tma_load_3d(smem_u32(wdst), &tmap_w, 0, (int32_t)(2 * sb),
+                                    (int32_t)(n0 / kW4Tile), wbar, pol);
+                } else {
+                    // 16 tiles x 8 blocks: nibbles [tile][block][8 rows][16 B],
+                    // scales [tile][block][8 rows fp16]
+                    tc::tma_load_4d(smem_u32(wdst), &tmap_w, 0, 0, (int32_t)(sb * kQ4Blocks),
+                                    (int32_t)(n0 / kQ4Tile), wbar, pol);
+                    tc::tma_load_3d(smem_u32(wdst + kQ4NibBytes), &tmap_d, 0, (int32_t)(sb * kQ4Blocks),
+                                    (int32_t)(n0 / kQ4Tile), wbar, pol);
+                }
+                ++issued_w;
+                const int st = (int)(sb % kActStages);
+                ok = mbar_wait(smem_u32(&act_empty[st]), (uint32_t)(((sb / kActStages) & 1) ^ 1), a.err);
+                if (!ok) break;
+                const uint32_t abar = smem_u32(&act_full[st]);
+                mbar_arrive_expect_tx(abar, kActBytes);
+                for (int c = 0; c < kChunks; ++c)
+                    tc::tma_load_2d(smem_u32(smem + kOffAct + st * kActBytes + c * kChunkBytes), &tmap_a,
+                                    (int32_t)(sb * kSB + c * kBK), (int32_t)m0, abar, pol);
+                ++issued_a;
+            }
+            for (int64_t k = issued_w > kWStages ? issued_w - kWStages : 0; k < issued_w; ++k)
+                mbar_wait(smem_u32(&w_full[k % kWStages]), (uint32_t)((k / kWStages) & 1), a.err);
+            for (int64_t k = issued_a > kActStages ? issued_a - kActStages : 0; k < issued_a; ++k)
+                mbar_wait(smem_u32(&act_full[k % kActStages]), (uint32_t)((k / kActStages) & 1), a.err);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // Meets the waiter at the named barrier the same number of times
+        // whatever happens; after a timeout the MMAs run on stale operands and
+        // the error word reports it.
+        constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
+        const uint64_t bdesc0 = tc::smem_desc(smem_u32(smem + kOffAct), 1024, 2);
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const int st = (int)(sb % kActStages);
+#pragma unroll 1
+            for (int g = 0; g < kGroups; ++g) {
+                handoff_sync();
+                if (lane == 0) {
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int h = 0; h < kChunks / kGroups; ++h) {
+                        const int c = g * (kChunks / kGroups) + h;
+                        const uint32_t acol = tmem + kColARing + (uint32_t)c * kARingCols;
+                        // K step of 16 fp16 = 32 bytes = 2 in the descriptor's address field
+                        const uint64_t bdesc = bdesc0 + (uint64_t)((st * kActBytes + c * kChunkBytes) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc::mma_f16_ta(tmem + kColAcc, acol + 8 * kk, bdesc + 2 * kk, idesc,
+                                           (sb | c | kk) != 0);
+                    }
+                    tc::commit(smem_u32(&a_empty[g]));
+                    if (g == kGroups - 1) tc::commit(smem_u32(&act_empty[st]));
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0) {
+            tc::commit(smem_u32(acc_full));
+            tc::commit(smem_u32(done));
+            mbar_wait(smem_u32(done), 0, a.err);  // no MMA may run when TMEM is freed
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ MMA waiter
+        bool ok = true;
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const int st = (int)(sb % kActStages);
+            const uint32_t par = (uint32_t)(sb & 1);
+            if (lane == 0 && ok)
+                ok = mbar_wait(smem_u32(&act_full[st]), (uint32_t)((sb / kActStages) & 1), a.err);
+#pragma unroll 1
+            for (int g = 0; g < kGroups; ++g) {
+                if (lane == 0 && ok) ok = mbar_wait(smem_u32(&a_full[g]), par, a.err);
+                __syncwarp();
+                handoff_sync();
+            }
+        }
+    } else if (warp < 3 + kConvWarps) {
+        // ------------------------------------------------------------ converters
+        const int ct = 32 * (warp & 3) + lane;  // weight row within the CTA = TMEM lane
+        const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
+        const int set = (warp - 3) >> 2;  // chunk `set` of each group
+        const int64_t n = n0 + ct;
+        const int64_t nc = n < a.N ? n : a.N - 1;  // rows past N: zero codes, clamped scales
+        const int64_t nsteps = a.K / kW4StepK;
+        bool ok = true;
+        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+            const int ws = (int)(sb % kWStages);
+            const uint32_t par = (uint32_t)(sb & 1);
+            ok = mbar_wait(smem_u32(&w_full[ws]), (uint32_t)((sb / kWStages) & 1), a.err);
+            if (!ok) break;
+            const uint8_t *wst = smem + kOffW + ws * kWBytesMax;
+#pragma unroll 1
+            for (int g = 0; g < kGroups && ok; ++g) {
+                const int c = g * (kChunks / kGroups) + set;  // chunk of this round
+                uint32_t lo[16], hi[16];  // TMEM columns 0..15 and 16..31 of the chunk
+                if (F == kW4A16) {
+                    // chunk c = half (c & 1) of step 2 sb + (c >> 1); columns hold
+                    // elements (2i, 2i + 1): the packed words put even elements
+                    // in the low half, odd in the high half
+                    const int sl = c >> 1;
+                    int64_t step = 2 * sb + sl;
+                    if (step >= nsteps) step = nsteps - 1;  // past K the activations are zero
+                    const int grp = a.spg == 1 ? (int)step : (int)step / a.spg;
+                    const uint32_t zv = a.Z[nc * a.ng + grp];
+                    const uint32_t sv = (uint32_t)__half_as_ushort(a.S[nc * a.ng + grp]);
+                    const uint32_t zz = 0x64006400u + zv * 0x00010001u;  // fp16 1024 + z twice
+                    const uint32_t zh = 0xD400D400u + zv * 0x00100010u;  // fp16 -(64 + z) twice
+                    const uint32_t ss = sv | (sv << 16);
+                    const uint8_t *src = wst + ((ct >> 4) * (kSB / kW4StepK) + sl) * 1024 + (ct & 15) * 64 +
+                                         (c & 1) * 32;
+                    const uint4 w0 = *reinterpret_cast<const uint4 *>(src);
+                    const uint4 w1 = *reinterpret_cast<const uint4 *>(src + 16);
+                    const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        // W4A16 word: (k0,k1) at 0|16, (k2,k3) at 4|20, (k4,k5) at 8|24, (k6,k7) at 12|28
+                        scaled_word(wv[i], zz, zh, ss, lo[4 * i], lo[4 * i + 2], lo[4 * i + 1], lo[4 * i + 3]);
+                        scaled_word(wv[i + 4], zz, zh, ss, hi[4 * i], hi[4 * i + 2], hi[4 * i + 1],
+                                    hi[4 * i + 3]);
+                    }
+                } else {
+                    // chunk c = blocks 2c, 2c + 1 of the round. Byte l of a block
+                    // holds elements l (low nibble) and l + 16 (high); word i
+                    // gives columns 4i .. 4i+3 = (e4i, e4i+2), (e4i+1, e4i+3),
+                    // (e16+4i, e18+4i), (e17+4i, e19+4i) -- the order the Q4_0
+                    // prefill quantizer writes the activations of a block in.
+                    constexpr uint32_t zz = 0x64086408u;  // fp16 1024 + 8 twice
+                    constexpr uint32_t zh = 0xD480D480u;  // fp16 -(64 + 8) twice
+                    const int tt = ct >> 3, r = ct & 7;
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        const int blk = 2 * c + b;
+                        const uint4 q = *reinterpret_cast<const uint4 *>(wst + tt * 1024 + blk * 128 + r * 16);
+                        const uint32_t dv = *reinterpret_cast<const uint16_t *>(
+                            wst + kQ4NibBytes + tt * (kQ4Blocks * 16) + blk * 16 + r * 2);
+                        const uint32_t ss = dv | (dv << 16);
+                        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+                        uint32_t *out = b == 0 ? lo : hi;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            scaled_word(wv[i], zz, zh, ss, out[4 * i], out[4 * i + 1], out[4 * i + 2],
+                                        out[4 * i + 3]);
+                    }
+                }
+                ok = mbar_wait(smem_u32(&a_empty[g]), par ^ 1, a.err);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const uint32_t acol = tmem + lane_addr + kColARing + (uint32_t)c * kARingCols;
+                tc::tmem_st16(acol, lo);
+                tc::tmem_st16(acol + 16, hi);
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&a_full[g]));
+            }
+            __syncwarp();
+            if (lane == 0 && ok) mbar_arrive(smem_u32(&w_empty[ws]));
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;  // TMEM lanes 32 * (warp % 4) ..
+        const int64_t n = n0 + quarter * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const bool ok = mbar_wait(smem_u32(acc_full), 0, a.err);
+        tc::fence_after_sync();
+        if (ok) {
+#pragma unroll 1
+            for (int c16 = 0; c16 < kBN / 16; ++c16) {
+                float v[16];
+                tc::tmem_ld16(tmem + lane_addr + kColAcc + (uint32_t)(c16 * 16), v);
+                tc::tmem_ld_wait();
+                if (n < a.N) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int64_t m = m0 + c16 * 16 + i;
+                        if (m < a.M) {
+                            if (F == kW4A16)
+                                static_cast<__half *>(a.C)[m * a.N + n] = __float2half_rn(v[i]);
+                            else
+                                static_cast<float *>(a.C)[m * a.N + n] = v[i];
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ Q4_0 prefill quantizer
+// X fp32 -> Q8_0 codes y and fp16 scale d per 32 (the same arithmetic as the
+// Q8_0 quantizer, shared q8_0_warp), then a = fp16(f32(d) * y) written with
+// the elements of each block permuted to the order the Q4_0 converter puts
+// the weights in: element e (e' = e mod 16, i = e' / 4, r = e' mod 4) goes to
+// position 8 i + 4 (e >= 16) + 2 (r mod 2) + r / 2.
+__global__ void __launch_bounds__(256) quantize_q4_0_prefill_kernel(const float *__restrict__ X,
+                                                                    __half *__restrict__ out,
+                                                                    int64_t nblocks) {
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int e = lane, ep = e & 15, i = ep >> 2, r = ep & 3;
+    const int pos = 8 * i + ((e >> 4) << 2) + 2 * (r & 1) + (r >> 1);
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += nwarps) {
+        int q, sum;
+        __half dh;
+        q8_0_warp(X[b * QK4_0 + lane], q, dh, sum);
+        out[b * QK4_0 + pos] = __float2half_rn(__half2float(dh) * (float)q);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, int64_t G,
+                              const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
+                              cudaStream_t s) {
+    Args a;
+    a.S = S;
+    a.Z = Z;
+    a.C = C;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ng = (int)(K / G);
+    a.spg = (int)(G / kW4StepK);
+    a.err = device_error_word();
+    const int64_t nsteps = K / kW4StepK, ntiles16 = (N + kW4Tile - 1) / kW4Tile;
+    CUtensorMap tmap_w, tmap_a;
+    // packed weights as [16-row tile][step][1 KB], in 4-byte units
+    const uint64_t wdims[3] = {256, (uint64_t)nsteps, (uint64_t)ntiles16};
+    const uint64_t wstrides[2] = {1024, (uint64_t)nsteps * 1024};
+    const uint32_t wbox[3] = {256, kSB / kW4StepK, kBM / kW4Tile};
+    if (!tc::make_tmap_3d(&tmap_w, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, wdims, wstrides, wbox) ||
+        !tc::make_tmap_2d(&tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M, (uint64_t)K,
+                          kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_f16_kernel<kW4A16>), kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + kBN - 1) / kBN));
+    gemm_f16_kernel<kW4A16><<<grid, kThreads, kSmemBytes, s>>>(a, tmap_w, tmap_w, tmap_a);
+    count_launch();
+    return cudaGetLastError();
+}
+
+size_t q4_0_prefill_bytes(int64_t M, int64_t K) { return align_up((size_t)M * K * 2, 256); }
+
+cudaError_t launch_quantize_q4_0_prefill(const float *X, void *ws, int64_t M, int64_t K,
+                                         cudaStream_t s) {
+    const int64_t nblocks = M * (K / QK4_0);
+    int64_t grid = (nblocks + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    quantize_q4_0_prefill_kernel<<<(int)grid, 256, 0, s>>>(X, static_cast<__half *>(ws), nblocks);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *ws, int64_t M,
+                             float *Y, cudaStream_t s) {
+    Args a;
+    a.S = nullptr;
+    a.Z = nullptr;
+    a.C = Y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ng = 0;
+    a.spg = 1;
+    a.err = device_error_word();
+    const int64_t nb = K / QK4_0, ntiles = tiles_of(N);
+    const uint64_t tile_bytes = (uint64_t)nb * kQ4Tile * B_Q4_0;
+    CUtensorMap tmap_w, tmap_d, tmap_a;
+    // nibble planes as [tile][row][block][4 words], read as [tile][block][row][16 B]
+    const uint64_t ndims[4] = {4, (uint64_t)kQ4Tile, (uint64_t)nb, (uint64_t)ntiles};
+    const uint64_t nstrides[3] = {(uint64_t)nb * 16, 16, tile_bytes};
+    const uint32_t nbox[4] = {4, (uint32_t)kQ4Tile, kQ4Blocks, kBM / kQ4Tile};
+    // scale planes as [tile][block][8 fp16]
+    const uint64_t ddims[3] = {(uint64_t)kQ4Tile, (uint64_t)nb, (uint64_t)ntiles};
+    const uint64_t dstrides[2] = {16, tile_bytes};
+    const uint32_t dbox[3] = {(uint32_t)kQ4Tile, kQ4Blocks, kBM / kQ4Tile};
+    const uint8_t *dplane = static_cast<const uint8_t *>(Wp) + (size_t)nb * kQ4Tile * 16;
+    if (!tc::make_tmap_4d(&tmap_w, Wp, CU_TENSOR_MAP_DATA_TYPE_UINT32, ndims, nstrides, nbox) ||
+        !tc::make_tmap_3d(&tmap_d, dplane, CU_TENSOR_MAP_DATA_TYPE_UINT16, ddims, dstrides, dbox) ||
+        !tc::make_tmap_2d(&tmap_a, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M, (uint64_t)K,
+                          kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_f16_kernel<kQ40>), kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + kBN - 1) / kBN));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_f16_kernel<kQ40>, a, tmap_w, tmap_d, tmap_a);
+    count_launch();
+    return e;
+}
+
+}  // namespace qmm

@@ -558,6 +558,20 @@ bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
            CUDA_SUCCESS;
 }
 
+bool make_tmap_4d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                  const uint64_t dims[4], const uint64_t strides[3], const uint32_t box[4]) {
+    const auto encode = encoder();
+    if (!encode) return false;
+    const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+    const cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
+    const cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return encode(map, dtype, 4, const_cast<void *>(base), d, st, bx, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
                   uint32_t elem_bytes, uint64_t rows, uint64_t cols, uint32_t box_rows,
                   uint32_t box_cols, CUtensorMapSwizzle swizzle) {

@@ -375,6 +375,13 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
 cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, int64_t G,
                               const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
                               cudaStream_t s);
+// Q4_0 prefill (M > 16): fp16(d_a y) activations (permuted per block) in a
+// workspace of q4_0_prefill_bytes, then the fp16-operand tensor-core GEMM.
+size_t q4_0_prefill_bytes(int64_t M, int64_t K);
+cudaError_t launch_quantize_q4_0_prefill(const float *X, void *ws, int64_t M, int64_t K,
+                                         cudaStream_t s);
+cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *ws, int64_t M,
+                             float *Y, cudaStream_t s);
 cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
                                     const void *Xq, int64_t M, int32_t *out, cudaStream_t s);
 }  // namespace qmm

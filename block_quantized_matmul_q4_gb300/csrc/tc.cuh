@@ -147,6 +147,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar), "l"(policy)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3, uint32_t mbar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(mbar),
+        "l"(policy)
+        : "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -162,6 +172,9 @@ bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
 bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
                   const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3],
                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
+// 4-D tensor map, no swizzle: dims[0] innermost, byte strides of dims 1..3.
+bool make_tmap_4d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                  const uint64_t dims[4], const uint64_t strides[3], const uint32_t box[4]);
 
 }  // namespace tc
 }  // namespace qmm

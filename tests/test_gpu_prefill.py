@@ -1,5 +1,6 @@
-"""GPU parity of the prefill path (Q4_K weights, M > 16 tokens): the prefill
-quantizer and the tcgen05 GEMM, through the C ABI, against the oracle.
+"""GPU parity of the prefill path (M > 16 tokens): the prefill quantizers and
+the tcgen05 GEMMs (Q4_K: integer-valued fp16 operands; Q4_0: fp16
+dequantized operands), through the C ABI, against the oracle.
 Bar: |Y_gpu - Y_fp64| <= 1e-3 * sum_k |w_k a_k| per element."""
 import numpy as np
 import pytest
@@ -26,10 +27,11 @@ def check(y, ref, den, what):
     assert not bad.any(), f"{what}: {bad.sum()} off, worst {np.max(err / np.maximum(den, 1e-30)):.3e}"
 
 
-def packed(q, orc, w, N, K):
-    Wc = orc.quantize(q.QMM_TYPE_Q4_K, w, nthreads=orc.default_threads())
-    Wp = q.empty_packed(q.QMM_TYPE_Q4_K, N, K)
-    q.qmm_repack_weights(q.QMM_TYPE_Q4_K, torch.from_numpy(Wc).cuda(), Wp, N, K)
+def packed(q, orc, w, N, K, wt=None):
+    wt = q.QMM_TYPE_Q4_K if wt is None else wt
+    Wc = orc.quantize(wt, w, nthreads=orc.default_threads())
+    Wp = q.empty_packed(wt, N, K)
+    q.qmm_repack_weights(wt, torch.from_numpy(Wc).cuda(), Wp, N, K)
     return Wc, Wp
 
 
@@ -74,3 +76,42 @@ def test_prefill_full_size_sampled(q, orc, shape, M):
                       nthreads=orc.default_threads())
     check(Y[:, torch.as_tensor(rows, device="cuda")].cpu().numpy(), ref["y64"], ref["den"],
           f"{L.name} M={M}")
+
+
+@pytest.mark.parametrize("N,K,M", [(128, 256, 17), (200, 512, 300), (136, 2304, 129), (64, 96, 40),
+                                   (300, 1056, 130)])
+def test_prefill_q4_0_small(q, orc, N, K, M):
+    """Q4_0 prefill GEMM: ragged N, M and K (K a multiple of 32 only)."""
+    wt = q.QMM_TYPE_Q4_0
+    w = wl.weights(32, N, K, 0.02).numpy()
+    x = wl.activations(32, M, K).numpy()
+    Wc, Wp = packed(q, orc, w, N, K, wt)
+    Y = torch.full((M * N + 64,), float("nan"), device="cuda")
+    Y[M * N:] = 777.0
+    q.qmm_mul_mat(wt, Wp, N, K, torch.from_numpy(x).cuda(), M, Y)
+    q.qmm_check_device_error()
+    y = Y.cpu().numpy()
+    assert np.all(y[M * N:] == 777.0), "write past the end of Y"
+    ref = orc.mul_mat(wt, Wc, N, K, x, nthreads=orc.default_threads())
+    check(y[:M * N].reshape(M, N), ref["y64"], ref["den"], f"Q4_0 N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("shape", wl.PREFILL_SHAPES, ids=lambda L: L.name)
+def test_prefill_q4_0_full_size_sampled(q, orc, shape):
+    """Q4_0 prefill at full size, M = 512: weights quantized on the GPU,
+    sampled rows checked against the oracle."""
+    L, M, wt = shape, 512, q.QMM_TYPE_Q4_0
+    w = wl.weights(33, L.N, L.K, L.wstd, device="cuda")
+    x = wl.activations(33, M, L.K, device="cuda")
+    Wq = q.empty_blocks(wt, L.N, L.K)
+    q.qmm_quantize_weights(wt, w, Wq, L.N, L.K)
+    Wp = q.empty_packed(wt, L.N, L.K)
+    q.qmm_repack_weights(wt, Wq, Wp, L.N, L.K)
+    Y = torch.empty(M, L.N, device="cuda")
+    q.qmm_mul_mat(wt, Wp, L.N, L.K, x, M, Y)
+    q.qmm_check_device_error()
+    rows = np.unique(np.r_[0:3, 127:130, L.N - 3:L.N, np.linspace(0, L.N - 1, 24).astype(np.int64)])
+    Wc_rows = Wq.view(L.N, -1)[torch.as_tensor(rows, device="cuda")].cpu().numpy()
+    ref = orc.mul_mat(wt, Wc_rows, len(rows), L.K, x.cpu().numpy(), nthreads=orc.default_threads())
+    check(Y[:, torch.as_tensor(rows, device="cuda")].cpu().numpy(), ref["y64"], ref["den"],
+          f"Q4_0 {L.name} M={M}")
