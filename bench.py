@@ -332,13 +332,14 @@ def gemv_rate(q, dev, stream, wt, N, K, M, seed, L=None, steps=6400, copies=None
     return t, b
 
 
-def prefill_rate(q, dev, stream, L, M, seed, reps=6, graph_steps=4):
+def prefill_rate(q, dev, stream, L, M, seed, reps=6, graph_steps=4, wt=None):
     """Prefill mul_mat (prefill quantizer + tcgen05 GEMM) on one shape: us per
-    call and TOPS (2 M N K integer multiply-adds per call), plus the GEMM
-    alone on prepared activations."""
-    wt = q.QMM_TYPE_Q4_K
+    call and TOPS (2 M N K multiply-adds per call), plus the GEMM alone on
+    prepared activations."""
+    wt = q.QMM_TYPE_Q4_K if wt is None else wt
     N, K = L.N, L.K
-    w = wl.weights(seed, N, K, L.wstd, row_offset_std=L.row_offset_std, device=dev)
+    off = L.row_offset_std if wt == q.QMM_TYPE_Q4_K else 0.0
+    w = wl.weights(seed, N, K, L.wstd, row_offset_std=off, device=dev)
     Wq = q.empty_blocks(wt, N, K)
     q.qmm_quantize_weights(wt, w, Wq, N, K)
     del w
@@ -368,12 +369,13 @@ def prefill_rate(q, dev, stream, L, M, seed, reps=6, graph_steps=4):
 def prefill_extras(q, dev, stream):
     peaks = load_peaks()
     out = {}
-    for L in wl.PREFILL_SHAPES:
-        for M in wl.PREFILL_M:
-            r = prefill_rate(q, dev, stream, L, M, 31)
-            r["frac_of_fp16_peak"] = round(r["gemm_TOPS"] / peaks["bf16_tflops"], 4)
-            out[f"{L.name}_M{M}"] = r
-            torch.cuda.empty_cache()
+    for wt, tag in ((q.QMM_TYPE_Q4_K, "q4_K"), (q.QMM_TYPE_Q4_0, "q4_0")):
+        for L in wl.PREFILL_SHAPES:
+            for M in wl.PREFILL_M:
+                r = prefill_rate(q, dev, stream, L, M, 31, wt=wt)
+                r["frac_of_fp16_peak"] = round(r["gemm_TOPS"] / peaks["bf16_tflops"], 4)
+                out[f"{tag}_{L.name}_M{M}"] = r
+                torch.cuda.empty_cache()
     out["peak"] = {"value": peaks["bf16_tflops"], "unit": "TFLOP/s",
                    "note": "measured bf16 dense GEMM peak; kind::f16 with fp16 operands has "
                            "the same nominal rate"}
@@ -421,7 +423,7 @@ def w4a16_extras(q, dev, stream, reps=8, graph_steps=16):
 
 
 def gpu_extras(q, dev, stream, args):
-    out = {"prefill_q4_K": prefill_extras(q, dev, stream)}
+    out = {"prefill": prefill_extras(q, dev, stream)}
     out["w4a16_8192"] = w4a16_extras(q, dev, stream)
     torch.cuda.empty_cache()
     # M sweep of the headline GEMV

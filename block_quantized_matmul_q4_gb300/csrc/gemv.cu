@@ -481,9 +481,8 @@ cudaError_t launch_kernel(qmm_type wt, const GemvArgs &a, bool pdl, cudaStream_t
     if (e != cudaSuccess) return e;
     // Q4_K CTAs work on pairs of tiles, Q4_0 CTAs on single tiles
     const int64_t units = wt == QMM_TYPE_Q4_K ? (tiles_of(a.N) + 1) / 2 : tiles_of(a.N);
-    const int64_t cap = 2LL * sm_count();
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(units < cap ? units : cap));
+    cfg.gridDim = dim3((unsigned)balanced_grid(units, 2LL * sm_count()));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

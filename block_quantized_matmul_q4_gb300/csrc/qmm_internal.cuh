@@ -350,6 +350,17 @@ void count_launch(unsigned n = 1);       // bump the launch counter
 qmm_status set_error(qmm_status s, const char *fmt, ...);
 
 // Kernel launchers (each .cu file); all return cudaSuccess or the launch error.
+// Grid for `units` equal work items on at most `cap` CTAs that each take a
+// contiguous range: the fewest items per CTA the cap allows, then the fewest
+// CTAs with that many, so that no CTA has more items than another by more
+// than one and the grid is not padded with CTAs that hold fewer. (A memory-
+// bound kernel finishes when its busiest CTA does.)
+inline int64_t balanced_grid(int64_t units, int64_t cap) {
+    if (units <= 0) return 1;
+    const int64_t per = (units + cap - 1) / cap;
+    return (units + per - 1) / per;
+}
+
 cudaError_t launch_quantize_q8(qmm_type vt, bool planar, const float *X, void *out, Planar p,
                                int64_t M, int64_t K, cudaStream_t s);
 cudaError_t launch_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N, int64_t K,

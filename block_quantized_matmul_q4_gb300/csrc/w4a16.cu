@@ -449,8 +449,7 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
     a.spg = (int)(G / kStepK);
     a.err = device_error_word();
     const int64_t ntiles = (N + kRowsPerTile - 1) / kRowsPerTile;
-    int64_t grid = (M <= 8 ? 2 : 1) * (int64_t)sm_count();
-    if (grid > ntiles) grid = ntiles;
+    const int64_t grid = balanced_grid(ntiles, (M <= 8 ? 2 : 1) * (int64_t)sm_count());
     // all of A in shared memory when it is small (one bulk copy per CTA)
     const size_t act = (size_t)M * K * 2;
     a.act_bytes = act <= kActStageMax ? (uint32_t)act : 0u;
