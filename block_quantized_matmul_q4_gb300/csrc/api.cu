@@ -124,10 +124,12 @@ void prepare_pool() {
 
 // More than 16 tokens run the tensor-core GEMMs and their workspace layouts
 // (Q4_K: integer-valued fp16 codes; Q4_0: fp16 dequantized activations);
-// fewer the decode GEMV and the planar layout.
+// fewer the decode GEMVs: Q4_K from 2 tokens on the mma.sync kernel and its
+// activation images, otherwise the scalar GEMV and the planar layout.
 bool use_gemm(qmm_type wt, int64_t M) { return M >= kGemmMinM; }
 
 size_t ws_bytes_for(qmm_type wt, int64_t M, int64_t K) {
+    if (!use_gemm(wt, M) && gemv_use_mma(wt, M, K)) return gemv_mma_image_bytes(M, K);
     if (!use_gemm(wt, M)) return planar_bytes(M, K, elems(wt), nullptr, nullptr);
     return wt == QMM_TYPE_Q4_K ? prefill_bytes(M, K, nullptr, nullptr) : q4_0_prefill_bytes(M, K);
 }
@@ -151,6 +153,12 @@ qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K,
         prefill_bytes(M, K, &pw, (uint8_t *)ws);
         return cuda_status(launch_quantize_prefill(X, pw, M, K, s), "prefill quantizer launch");
     }
+    if (gemv_use_mma(wt, M, K)) {
+        const size_t need = ws_bytes_for(wt, M, K);
+        if (ws_bytes < need)
+            return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+        return cuda_status(launch_quantize_mma_image(X, ws, M, K, s), "activation quantizer launch");
+    }
     Planar p;
     qmm_status st = carve(wt, M, K, ws, ws_bytes, &p);
     if (st != QMM_OK) return st;
@@ -169,6 +177,13 @@ qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, cons
         PrefillWs pw;
         prefill_bytes(M, K, &pw, (uint8_t *)ws);
         return cuda_status(launch_gemm_q4_K(Wp, N, K, pw, M, Y, s), "prefill GEMM launch");
+    }
+    if (gemv_use_mma(wt, M, K)) {
+        const size_t need = ws_bytes_for(wt, M, K);
+        if (ws_bytes < need)
+            return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+        return cuda_status(launch_gemv_mma_q4_K(Wp, N, K, nullptr, ws, M, Y, /*pdl=*/true, s),
+                           "mul_mat kernel launch");
     }
     Planar p;
     qmm_status st = carve(wt, M, K, ws, ws_bytes, &p);

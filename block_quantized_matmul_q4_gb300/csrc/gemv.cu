@@ -518,7 +518,12 @@ uint32_t act_layout(qmm_type wt, int64_t mt, int64_t K, uint32_t *bs_off, uint32
 
 }  // namespace
 
+bool gemv_use_mma(qmm_type wt, int64_t M, int64_t K) {
+    return wt == QMM_TYPE_Q4_K && M >= kMmaMinM && gemv_mma_max_tokens(K) >= 1;
+}
+
 bool gemv_can_fuse(qmm_type wt, int64_t M, int64_t K) {
+    if (gemv_use_mma(wt, M, K)) return M * K <= kMmaFuseElems;
     const int64_t mt = min64(M, kMaxMT);
     return act_layout(wt, mt, K, nullptr, nullptr) <= (uint32_t)kActMax && mt * K <= kFuseMaxElems;
 }
@@ -528,6 +533,7 @@ bool gemv_can_fuse(qmm_type wt, int64_t M, int64_t K) {
 // come from the planar workspace x written by launch_quantize_q8.
 cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x,
                         const float *X, int64_t M, float *Y, bool pdl, cudaStream_t s) {
+    if (X && gemv_use_mma(wt, M, K)) return launch_gemv_mma_q4_K(Wp, N, K, X, nullptr, M, Y, pdl, s);
     GemvArgs a;
     a.Wp = static_cast<const uint8_t *>(Wp);
     a.N = N;

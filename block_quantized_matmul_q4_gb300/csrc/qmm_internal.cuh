@@ -371,6 +371,20 @@ cudaError_t launch_repack(qmm_type wt, bool inverse, const void *src, void *dst,
 cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x,
                         const float *X, int64_t M, float *Y, bool pdl, cudaStream_t s);
 bool gemv_can_fuse(qmm_type wt, int64_t M, int64_t K);
+// Tensor-core decode GEMV for Q4_K (gemv_mma.cu): used from kMmaMinM tokens
+// on while one token's activations fit its shared memory
+// (gemv_mma_max_tokens(K) >= 1). Up to kMmaFuseElems activation elements per
+// call it quantizes inside the kernel; beyond, launch_quantize_mma_image
+// writes the activation images (gemv_mma_image_bytes) into the workspace.
+constexpr int64_t kMmaMinM = 2;
+constexpr int64_t kMmaFuseElems = 8192;
+int gemv_mma_max_tokens(int64_t K);
+bool gemv_use_mma(qmm_type wt, int64_t M, int64_t K);
+size_t gemv_mma_image_bytes(int64_t M, int64_t K);
+cudaError_t launch_quantize_mma_image(const float *X, void *img, int64_t M, int64_t K,
+                                      cudaStream_t s);
+cudaError_t launch_gemv_mma_q4_K(const void *Wp, int64_t N, int64_t K, const float *X,
+                                 const void *img, int64_t M, float *Y, bool pdl, cudaStream_t s);
 size_t prefill_bytes(int64_t M, int64_t K, PrefillWs *p, uint8_t *base);
 cudaError_t launch_quantize_prefill(const float *X, PrefillWs p, int64_t M, int64_t K,
                                     cudaStream_t s);

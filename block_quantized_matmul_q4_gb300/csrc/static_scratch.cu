@@ -63,7 +63,16 @@ extern "C" qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int6
     if (!W_packed || !X || !Y) return set_error(QMM_ERR_ARG, "null pointer argument");
     if (!aligned16(W_packed) || !aligned16(X) || ((uintptr_t)Y & 3))
         return set_error(QMM_ERR_ARG, "W_packed and X must be 16-byte aligned, Y 4-byte aligned");
-    const size_t need = planar_bytes(M, K, qk, nullptr, nullptr);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (gemv_can_fuse(wt, M, K)) {  // one kernel, no scratch
+        Planar none{nullptr, nullptr, nullptr};
+        cudaError_t e = launch_gemv(wt, W_packed, N, K, none, X, M, Y, /*pdl=*/true, s);
+        if (e != cudaSuccess)
+            return set_error(QMM_ERR_CUDA, "mul_mat kernel launch: %s", cudaGetErrorString(e));
+        return set_error(QMM_OK, "");
+    }
+    const bool mma = gemv_use_mma(wt, M, K);
+    const size_t need = mma ? gemv_mma_image_bytes(M, K) : planar_bytes(M, K, qk, nullptr, nullptr);
     if (need > kStaticScratchBytes)
         return set_error(QMM_ERR_WORKSPACE,
                          "qmm_mul_mat_static: M=%lld x K=%lld needs %zu bytes of scratch, more than "
@@ -74,9 +83,15 @@ extern "C" qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int6
     if (st != QMM_OK) return st;
     // Nothing in the scratch has to start at zero: the quantizer writes every
     // byte the GEMV reads.
+    if (mma) {
+        cudaError_t e = launch_quantize_mma_image(X, scratch, M, K, s);
+        if (e == cudaSuccess) e = launch_gemv_mma_q4_K(W_packed, N, K, nullptr, scratch, M, Y, true, s);
+        if (e != cudaSuccess)
+            return set_error(QMM_ERR_CUDA, "mul_mat launch: %s", cudaGetErrorString(e));
+        return set_error(QMM_OK, "");
+    }
     Planar p;
     planar_bytes(M, K, qk, &p, scratch);
-    cudaStream_t s = (cudaStream_t)stream;
     const qmm_type at = wt == QMM_TYPE_Q4_K ? QMM_TYPE_Q8_K : QMM_TYPE_Q8_0;
     cudaError_t e = launch_quantize_q8(at, true, X, nullptr, p, M, K, s);
     if (e != cudaSuccess)

@@ -171,6 +171,24 @@ def test_mul_mat_prepared(q, orc, wt, N, K, M):
     check_close(host(Y3), ref["y64"], ref["den"], f"one-call wt={wt} K={K} M={M}")
 
 
+@pytest.mark.parametrize("N,K,M", [
+    (10000, 256, 3),     # 625 tile pairs: several pairs per CTA
+    (8, 2304, 9),        # one tile (no second tile in the pair), 9 super-blocks, two n8 token tiles
+    (40, 4096, 2), (200, 1536, 16), (72, 8192, 12),
+    (24, 65536, 3),      # one token per launch fits shared memory: three launches, planar workspace
+    (8, 1048576, 2)])    # no token fits: the scalar GEMV reads the workspace in place
+def test_q4_K_decode_tensor_core_shapes(q, orc, N, K, M):
+    """Q4_K decode with M >= 2 runs on mma.sync (integer-valued fp16
+    operands); shapes that exercise its work split, token tiles, launch
+    chunking and the fallback."""
+    w = wl.weights(14, N, K, 0.02, row_offset_std=0.005).numpy()
+    x = wl.activations(14, M, K).numpy()
+    Wc = orc.quantize(1, w, nthreads=orc.default_threads())
+    y = run_mul_mat(q, 1, Wc, N, K, x)
+    ref = orc.mul_mat(1, Wc, N, K, x, nthreads=orc.default_threads())
+    check_close(y, ref["y64"], ref["den"], f"N={N} K={K} M={M}")
+
+
 def test_mul_mat_edge_inputs(q, orc):
     for wt, K in ((0, 256), (1, 256)):
         w = edge_rows(K, 11)
