@@ -426,32 +426,97 @@ def gpu_extras(q, dev, stream, args):
     out = {"prefill": prefill_extras(q, dev, stream)}
     out["w4a16_8192"] = w4a16_extras(q, dev, stream)
     torch.cuda.empty_cache()
-    # M sweep of the headline GEMV
+    out["q4_K_4096_M_sweep"] = sweep_rate(q, dev, stream)
+    # Q4_0 x Q8_0 GEMV, 256 x 1024, M = 1 (L2-resident correctness case)
+    Ls = wl.GEMV_Q4_0_SMALL
+    t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q4_0, Ls.N, Ls.K, 1, 0, Ls, copies=1)
+    out["q4_0_256x1024_m1"] = {"us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
+                               "note": "147 KB of weights stay in L2; latency-bound"}
+    # 70B-shaped decode layer
+    out["layer_70B_q4_K_m1"] = layer_rate(q, dev, stream)
+    torch.cuda.empty_cache()
+    per = {}
+    for i, Lp in enumerate(wl.LAYER_70B):
+        t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q4_K, Lp.N, Lp.K, 1, 100 + i, Lp,
+                         steps=640, hot=wl.LAYER_70B_HOT_FRAC)
+        per[Lp.name] = {"us": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1)}
+        torch.cuda.empty_cache()
+    out["layer_70B_q4_K_m1"]["per_projection_alone"] = per
+    return out
+
+
+def sweep_rate(q, dev, stream):
+    """The headline GEMV (Q4_K, N = K = 4096) at M in {1, 2, 4, 8, 16}: M = 1
+    runs the scalar GEMV, M >= 2 the tensor-core one."""
     sweep = {}
     L = wl.GEMV_Q4_K_4096
     for M in wl.GEMV_Q4_K_M_SWEEP:
         t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q4_K, L.N, L.K, M, 0, L)
         sweep[str(M)] = {"us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
                          "TOPS": round(2 * M * L.N * L.K / t / 1e12, 3)}
-    out["q4_K_4096_M_sweep"] = sweep
-    # Q4_0 x Q8_0 GEMV, 256 x 1024, M = 1 (L2-resident correctness case)
-    Ls = wl.GEMV_Q4_0_SMALL
-    t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q4_0, Ls.N, Ls.K, 1, 0, Ls, copies=1)
-    out["q4_0_256x1024_m1"] = {"us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
-                               "note": "147 KB of weights stay in L2; latency-bound"}
-    # 70B-shaped decode layer: the 7 projections back to back
-    tot_t, tot_b = 0.0, 0
-    per = {}
+    return sweep
+
+
+def layer_rate(q, dev, stream, reps=20, graph_steps=16):
+    """The 70B-shaped decode layer (M = 1) as one step: q, k, v from one input
+    (qmm_mul_mat_multi: one quantization, one launch), o, gate and up from one
+    input (multi), down; and the same seven projections as seven qmm_mul_mat
+    calls. The 481 MB of weights exceed L2, so each step reads them from HBM."""
+    wt = q.QMM_TYPE_Q4_K
+    Wp, Y = {}, {}
+    wbytes = 0
     for i, Lp in enumerate(wl.LAYER_70B):
-        t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q4_K, Lp.N, Lp.K, 1, 100 + i, Lp,
-                         steps=640, hot=wl.LAYER_70B_HOT_FRAC)
-        per[Lp.name] = {"us": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1)}
-        tot_t += t
-        tot_b += b
-        torch.cuda.empty_cache()
-    out["layer_70B_q4_K_m1"] = {"us": round(tot_t * 1e6, 2), "GB/s": round(tot_b / tot_t / 1e9, 1),
-                                "bytes": tot_b, "per_projection": per}
-    return out
+        w = wl.weights(100 + i, Lp.N, Lp.K, Lp.wstd, outlier_frac=Lp.outlier_frac, device=dev)
+        Wq = q.empty_blocks(wt, Lp.N, Lp.K)
+        q.qmm_quantize_weights(wt, w, Wq, Lp.N, Lp.K)
+        del w
+        Wp[Lp.name] = q.empty_packed(wt, Lp.N, Lp.K)
+        q.qmm_repack_weights(wt, Wq, Wp[Lp.name], Lp.N, Lp.K)
+        del Wq
+        wbytes += Lp.N * (Lp.K // 256) * 144
+        Y[Lp.name] = torch.empty(Lp.N, device=dev)
+    torch.cuda.empty_cache()
+    L = {Lp.name: Lp for Lp in wl.LAYER_70B}
+    hot = wl.LAYER_70B_HOT_FRAC
+    X = {name: wl.activations(100 + i, 1, L[name].K, hot_frac=hot, device=dev)
+         for i, name in enumerate(L)}
+    ws_bytes = q.qmm_workspace_bytes(wt, 1, L["down_proj"].K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def one(name, x):
+        q.qmm_mul_mat_ws(wt, Wp[name], L[name].N, L[name].K, x, 1, Y[name], ws, ws_bytes, stream)
+
+    def multi(names, x):
+        q.qmm_mul_mat_multi(wt, [Wp[n] for n in names], [L[n].N for n in names], L[names[0]].K, x, 1,
+                            [Y[n] for n in names], stream)
+
+    def shared(i):
+        multi(("q_proj", "k_proj", "v_proj"), X["q_proj"])
+        one("o_proj", X["o_proj"])
+        multi(("gate_proj", "up_proj"), X["gate_proj"])
+        one("down_proj", X["down_proj"])
+
+    def separate(i):
+        for name in L:
+            one(name, X[name])
+
+    res = {"bytes": wbytes}
+    for key, fn, launches in (("shared", shared, 4), ("separate", separate, 7)):
+        for i in range(3):
+            fn(i)
+        g = capture(fn, graph_steps, stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        t = timed(stream, lambda: run_graphs(g, None, reps)) / (reps * graph_steps)
+        res[key] = {"us": round(t * 1e6, 2), "GB/s": round(wbytes / t / 1e9, 1),
+                    "calls": launches}
+    res["us"] = res["shared"]["us"]
+    res["GB/s"] = res["shared"]["GB/s"]
+    res["note"] = ("one step = the whole layer in a CUDA graph; 'shared': q/k/v and gate/up as "
+                   "qmm_mul_mat_multi calls on one input each (one quantization, one launch); "
+                   "'separate': seven qmm_mul_mat calls; GB/s counts weight bytes")
+    del Wp, Y, X, ws
+    return res
 
 
 # ------------------------------------------------------------------ oracle (CPU)
@@ -508,8 +573,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--case", choices=["decode", "prefill", "w4a16"], default="decode",
-                    help="prefill / w4a16: only that measurement (for profiler captures)")
+    ap.add_argument("--case", choices=["decode", "prefill", "w4a16", "layer", "sweep"],
+                    default="decode",
+                    help="prefill / w4a16 / layer / sweep: only that measurement (for profiler "
+                         "captures)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -541,9 +608,10 @@ def main():
         torch.distributed.init_process_group("nccl")
     else:
         torch.cuda.set_device(0)
-    if args.case in ("prefill", "w4a16"):
+    if args.case != "decode":
         import block_quantized_matmul_q4_gb300 as q
-        fn = prefill_extras if args.case == "prefill" else w4a16_extras
+        fn = {"prefill": prefill_extras, "w4a16": w4a16_extras, "layer": layer_rate,
+              "sweep": sweep_rate}[args.case]
         print(json.dumps(fn(q, torch.device("cuda", torch.cuda.current_device()),
                             torch.cuda.Stream())), flush=True)
         return

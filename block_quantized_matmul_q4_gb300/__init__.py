@@ -45,6 +45,8 @@ _SIGS = {
     "qmm_unrepack_weights": (_i32, [_i32, _vp, _vp, _i64, _i64, _vp]),
     "qmm_mul_mat": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_mul_mat_ws": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "qmm_mul_mat_multi": (_i32, [_i32, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_i64), _i64, _vp,
+                                 _i64, ctypes.POINTER(_vp), _vp]),
     "qmm_quantize_activations": (_i32, [_i32, _vp, _i64, _i64, _vp, _sz, _vp]),
     "qmm_mul_mat_prepared": (_i32, [_i32, _vp, _i64, _i64, _vp, _sz, _i64, _vp, _vp]),
     "qmm_mul_mat_static": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
@@ -133,6 +135,17 @@ def qmm_unrepack_weights(wt: int, W_packed, W_canon, N: int, K: int, stream=None
 def qmm_mul_mat(wt: int, W_packed, N: int, K: int, X, M: int, Y, stream=None):
     _check("qmm_mul_mat",
            _lib.qmm_mul_mat(wt, _ptr(W_packed), N, K, _ptr(X), M, _ptr(Y), _stream(stream)))
+
+
+def qmm_mul_mat_multi(wt: int, W_packed: list, N: list, K: int, X, M: int, Y: list, stream=None):
+    """Y[i] = X W_packed[i]^T for every i, X quantized once, one decode launch."""
+    n = len(W_packed)
+    if not (len(N) == n == len(Y)):
+        raise ValueError("W_packed, N and Y must have the same length")
+    w = (_vp * n)(*[_ptr(t) for t in W_packed])
+    nn = (_i64 * n)(*N)
+    y = (_vp * n)(*[_ptr(t) for t in Y])
+    _check("qmm_mul_mat_multi", _lib.qmm_mul_mat_multi(wt, n, w, nn, K, _ptr(X), M, y, _stream(stream)))
 
 
 def qmm_mul_mat_ws(wt: int, W_packed, N: int, K: int, X, M: int, Y, workspace, ws_bytes: int,

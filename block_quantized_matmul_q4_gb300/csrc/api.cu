@@ -182,7 +182,7 @@ qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, cons
         const size_t need = ws_bytes_for(wt, M, K);
         if (ws_bytes < need)
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
-        return cuda_status(launch_gemv_mma_q4_K(Wp, N, K, nullptr, ws, M, Y, /*pdl=*/true, s),
+        return cuda_status(launch_gemv_mma_q4_K(single_mat(Wp, N, Y), K, nullptr, ws, M, /*pdl=*/true, s),
                            "mul_mat kernel launch");
     }
     Planar p;
@@ -377,6 +377,57 @@ qmm_status qmm_mul_mat(qmm_type wt, const void *W_packed, int64_t N, int64_t K, 
         return set_error(QMM_ERR_NOMEM, "cudaMallocAsync(%zu): %s", need, cudaGetErrorString(e));
     }
     st = mul_mat_impl(wt, W_packed, N, K, X, M, Y, ws, need, s);
+    cudaError_t ef = cudaFreeAsync(ws, s);
+    if (st == QMM_OK && ef != cudaSuccess) return cuda_status(ef, "cudaFreeAsync");
+    return st;
+}
+
+qmm_status qmm_mul_mat_multi(qmm_type wt, int n, const void *const *W_packed, const int64_t *N,
+                             int64_t K, const float *X, int64_t M, float *const *Y,
+                             qmm_stream_t stream) {
+    QMM_CHECK_ARG(n >= 1 && n <= kMaxMats, "n must be 1..%d (got %d)", kMaxMats, n);
+    QMM_CHECK_ARG(W_packed && N && Y, "null array argument");
+    MatSet ms = {};
+    for (int i = 0; i < n; ++i) {
+        qmm_status st = check_mul_mat_args(wt, W_packed[i], N[i], K, X, M, Y[i]);
+        if (st != QMM_OK) return st;
+        if (N[i] == 0) continue;
+        ms.W[ms.n] = static_cast<const uint8_t *>(W_packed[i]);
+        ms.N[ms.n] = N[i];
+        ms.Y[ms.n] = Y[i];
+        ++ms.n;
+    }
+    if (M == 0 || ms.n == 0) return ok();
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!use_gemm(wt, M) && gemv_can_fuse(wt, M, K)) {  // one kernel, no workspace
+        Planar none{nullptr, nullptr, nullptr};
+        return cuda_status(launch_gemv(wt, ms, K, none, X, M, /*pdl=*/true, s), "mul_mat kernel launch");
+    }
+    prepare_pool();
+    const size_t need = qmm_workspace_bytes(wt, M, K);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess || !ws) {
+        cudaGetLastError();
+        return set_error(QMM_ERR_NOMEM, "cudaMallocAsync(%zu): %s", need, cudaGetErrorString(e));
+    }
+    // one quantization of X serves every matrix
+    qmm_status st = quantize_acts_impl(wt, X, M, K, ws, need, s);
+    if (st == QMM_OK) {
+        if (use_gemm(wt, M)) {
+            for (int i = 0; i < ms.n && st == QMM_OK; ++i)
+                st = prepared_impl(wt, ms.W[i], ms.N[i], K, ws, need, M, ms.Y[i], s);
+        } else if (gemv_use_mma(wt, M, K)) {
+            st = cuda_status(launch_gemv_mma_q4_K(ms, K, nullptr, ws, M, /*pdl=*/true, s),
+                             "mul_mat kernel launch");
+        } else {
+            Planar p;
+            st = carve(wt, M, K, ws, need, &p);
+            if (st == QMM_OK)
+                st = cuda_status(launch_gemv(wt, ms, K, p, nullptr, M, /*pdl=*/true, s),
+                                 "mul_mat kernel launch");
+        }
+    }
     cudaError_t ef = cudaFreeAsync(ws, s);
     if (st == QMM_OK && ef != cudaSuccess) return cuda_status(ef, "cudaFreeAsync");
     return st;

@@ -50,12 +50,11 @@ static_assert(kBarBytes == 72, "barrier area must hold 2 * kStages + 1 mbarriers
 enum Mode { kDirect = 0, kStaged = 1, kFused = 2 };
 
 struct GemvArgs {
-    const uint8_t *Wp;  // packed weights
-    int64_t N, nblk;    // rows, blocks per row (nsb for Q4_K, nb for Q4_0)
+    MatSet ms;          // packed weights, outputs and rows of each matrix
+    int64_t nblk;       // blocks per row (nsb for Q4_K, nb for Q4_0)
     Planar x;           // planar activations (kDirect, kStaged)
     const float *X;     // fp32 activations (kFused)
     int64_t M, m0;      // all tokens, first token of this launch
-    float *Y;
     unsigned *err;
     uint32_t act_bs, act_d, act_bytes;  // shared activation layout (offsets, total)
 };
@@ -210,9 +209,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nsb = a.nblk, K = nsb * QK_K;
     const int mc = (int)min64(MT, a.M - a.m0);
-    const int64_t ntiles = tiles_of(a.N);
     int64_t pb, pe;
-    my_tiles((ntiles + 1) / 2, pb, pe);  // this CTA's tile pairs
+    my_tiles(a.ms.off[a.ms.n], pb, pe);  // this CTA's tile pairs (over all matrices)
     const int64_t nchunks = (nsb + kQ4KChunk - 1) / kQ4KChunk;
     const int64_t n_items = (pe - pb) * nchunks;
     const Ring r = ring_init(smem, kMode == kDirect ? 0 : a.act_bytes);
@@ -222,15 +220,18 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
             producer_loop(
                 r, n_items, a.err,
                 [&](int64_t it, uint32_t dst, uint32_t bar, uint64_t pol) {
-                    const int64_t t0 = 2 * (pb + it / nchunks);
+                    const int64_t p = pb + it / nchunks;
+                    const int mi = mat_of(a.ms, p);
+                    const int64_t t0 = 2 * (p - a.ms.off[mi]);
                     const int64_t sb0 = (it % nchunks) * kQ4KChunk;
                     const uint32_t bytes =
                         (uint32_t)min64(kQ4KChunk, nsb - sb0) * kTileRows * B_Q4_K;
-                    const bool has1 = t0 + 1 < ntiles;
+                    const bool has1 = t0 + 1 < tiles_of(a.ms.N[mi]);
+                    const uint8_t *W = a.ms.W[mi];
                     mbar_arrive_expect_tx(bar, has1 ? 2 * bytes : bytes);
-                    bulk_g2s(dst, a.Wp + (t0 * nsb + sb0) * (kTileRows * B_Q4_K), bytes, bar, pol);
+                    bulk_g2s(dst, W + (t0 * nsb + sb0) * (kTileRows * B_Q4_K), bytes, bar, pol);
                     if (has1)
-                        bulk_g2s(dst + kHalfStage, a.Wp + ((t0 + 1) * nsb + sb0) * (kTileRows * B_Q4_K),
+                        bulk_g2s(dst + kHalfStage, W + ((t0 + 1) * nsb + sb0) * (kTileRows * B_Q4_K),
                                  bytes, bar, pol);
                 },
                 [&]() {
@@ -284,7 +285,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
     for (int64_t it = 0; it < n_items; ++it) {
         const int s = (int)(it % kStages);
         if (!mbar_wait(smem_u32(&r.full[s]), (uint32_t)((it / kStages) & 1), a.err)) break;
-        const int64_t t0 = 2 * (pb + it / nchunks);
         const int64_t chunk = it % nchunks;
         const int64_t sb0 = chunk * kQ4KChunk;
         const int cnt = (int)min64(kQ4KChunk, nsb - sb0);
@@ -320,14 +320,18 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&r.empty[s]));
         if (chunk == nchunks - 1) {
-            const int64_t n0 = t0 * kTileRows + warp, n1 = n0 + kTileRows;
+            const int64_t p = pb + it / nchunks;
+            const int mi = mat_of(a.ms, p);
+            const int64_t N = a.ms.N[mi];
+            float *Y = a.ms.Y[mi];
+            const int64_t n0 = 2 * (p - a.ms.off[mi]) * kTileRows + warp, n1 = n0 + kTileRows;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 const float v0 = warp_sum(acc0[m]);
                 const float v1 = warp_sum(acc1[m]);
                 if (lane == 0 && m < mc) {
-                    if (n0 < a.N) a.Y[(a.m0 + m) * a.N + n0] = v0;
-                    if (n1 < a.N) a.Y[(a.m0 + m) * a.N + n1] = v1;
+                    if (n0 < N) Y[(a.m0 + m) * N + n0] = v0;
+                    if (n1 < N) Y[(a.m0 + m) * N + n1] = v1;
                 }
                 acc0[m] = acc1[m] = 0.0f;
             }
@@ -348,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
     const int64_t nb = a.nblk, K = nb * QK4_0;
     const int mc = (int)min64(MT, a.M - a.m0);
     int64_t tb, te;
-    my_tiles(tiles_of(a.N), tb, te);
+    my_tiles(a.ms.off[a.ms.n], tb, te);  // this CTA's tiles (over all matrices)
     const int64_t nchunks = (nb + kQ40Chunk - 1) / kQ40Chunk;
     const int64_t n_items = (te - tb) * nchunks;
     const int64_t tile_bytes = nb * kTileRows * B_Q4_0;
@@ -362,9 +366,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
                 r, n_items, a.err,
                 [&](int64_t it, uint32_t dst, uint32_t bar, uint64_t pol) {
                     const int64_t tile = tb + it / nchunks;
+                    const int mi = mat_of(a.ms, tile);
                     const int64_t b0 = (it % nchunks) * kQ40Chunk;
                     const uint32_t cnt = (uint32_t)min64(kQ40Chunk, nb - b0);
-                    const uint8_t *tbase = a.Wp + tile * tile_bytes;
+                    const uint8_t *tbase = a.ms.W[mi] + (tile - a.ms.off[mi]) * tile_bytes;
                     mbar_arrive_expect_tx(bar, cnt * kTileRows * B_Q4_0);
                     for (int rr = 0; rr < kTileRows; ++rr)
                         bulk_g2s(dst + rr * kRowBytes, tbase + (rr * nb + b0) * 16, cnt * 16, bar,
@@ -415,7 +420,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
     for (int64_t it = 0; it < n_items; ++it) {
         const int s = (int)(it % kStages);
         if (!mbar_wait(smem_u32(&r.full[s]), (uint32_t)((it / kStages) & 1), a.err)) break;
-        const int64_t tile = tb + it / nchunks;
         const int64_t chunk = it % nchunks;
         const int64_t b0 = chunk * kQ40Chunk;
         const int cnt = (int)min64(kQ40Chunk, nb - b0);
@@ -459,11 +463,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&r.empty[s]));
         if (chunk == nchunks - 1) {
-            const int64_t n = tile * kTileRows + warp;
+            const int64_t tile = tb + it / nchunks;
+            const int mi = mat_of(a.ms, tile);
+            const int64_t N = a.ms.N[mi];
+            const int64_t n = (tile - a.ms.off[mi]) * kTileRows + warp;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 const float v = warp_sum(acc[m]);
-                if (lane == 0 && m < mc && n < a.N) a.Y[(a.m0 + m) * a.N + n] = v;
+                if (lane == 0 && m < mc && n < N) a.ms.Y[mi][(a.m0 + m) * N + n] = v;
                 acc[m] = 0.0f;
             }
         }
@@ -480,7 +487,7 @@ cudaError_t launch_kernel(qmm_type wt, const GemvArgs &a, bool pdl, cudaStream_t
     cudaError_t e = ensure_smem_attr(fn, smem);
     if (e != cudaSuccess) return e;
     // Q4_K CTAs work on pairs of tiles, Q4_0 CTAs on single tiles
-    const int64_t units = wt == QMM_TYPE_Q4_K ? (tiles_of(a.N) + 1) / 2 : tiles_of(a.N);
+    const int64_t units = a.ms.off[a.ms.n];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)balanced_grid(units, 2LL * sm_count()));
     cfg.blockDim = dim3(kThreads);
@@ -528,20 +535,31 @@ bool gemv_can_fuse(qmm_type wt, int64_t M, int64_t K) {
     return act_layout(wt, mt, K, nullptr, nullptr) <= (uint32_t)kActMax && mt * K <= kFuseMaxElems;
 }
 
+MatSet single_mat(const void *Wp, int64_t N, float *Y) {
+    MatSet ms = {};
+    ms.n = 1;
+    ms.W[0] = static_cast<const uint8_t *>(Wp);
+    ms.N[0] = N;
+    ms.Y[0] = Y;
+    return ms;
+}
+
 // X != nullptr runs the quantizer fused into the GEMV prologue (X is the fp32
 // activation; the caller checked gemv_can_fuse); otherwise the activations
 // come from the planar workspace x written by launch_quantize_q8.
-cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x,
-                        const float *X, int64_t M, float *Y, bool pdl, cudaStream_t s) {
-    if (X && gemv_use_mma(wt, M, K)) return launch_gemv_mma_q4_K(Wp, N, K, X, nullptr, M, Y, pdl, s);
+cudaError_t launch_gemv(qmm_type wt, MatSet ms, int64_t K, Planar x, const float *X, int64_t M,
+                        bool pdl, cudaStream_t s) {
+    if (X && gemv_use_mma(wt, M, K)) return launch_gemv_mma_q4_K(ms, K, X, nullptr, M, pdl, s);
+    // work units: tile pairs (Q4_K CTAs work on two 8-row tiles) or tiles
+    ms.off[0] = 0;
+    for (int i = 0; i < ms.n; ++i)
+        ms.off[i + 1] = ms.off[i] + (wt == QMM_TYPE_Q4_K ? (tiles_of(ms.N[i]) + 1) / 2 : tiles_of(ms.N[i]));
     GemvArgs a;
-    a.Wp = static_cast<const uint8_t *>(Wp);
-    a.N = N;
+    a.ms = ms;
     a.nblk = K / (wt == QMM_TYPE_Q4_K ? QK_K : QK4_0);
     a.x = x;
     a.X = X;
     a.M = M;
-    a.Y = Y;
     a.err = device_error_word();
     for (int64_t m0 = 0; m0 < M; m0 += kMaxMT) {
         const int64_t mt = min64(M - m0, kMaxMT);
@@ -567,6 +585,11 @@ cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Plana
         pdl = false;  // only the first launch follows the quantizer directly
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x,
+                        const float *X, int64_t M, float *Y, bool pdl, cudaStream_t s) {
+    return launch_gemv(wt, single_mat(Wp, N, Y), K, x, X, M, pdl, s);
 }
 
 }  // namespace qmm

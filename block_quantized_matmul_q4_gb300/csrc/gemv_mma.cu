@@ -55,14 +55,13 @@ constexpr int kSbCodes = 512;                // fp16 codes of one (super-block, 
 constexpr int kSbSums = 32;                  // fp16 16-code sums of one (super-block, token)
 
 struct MmaArgs {
-    const uint8_t *Wp;  // packed Q4_K
-    int64_t N, nsb;     // rows, super-blocks per row
+    MatSet ms;          // packed Q4_K weights, outputs, rows; units = tile pairs
+    int64_t nsb;        // super-blocks per row
     const float *X;     // fp32 activations (fused quantizer) or nullptr
     const uint8_t *img; // activation image of this launch (when X == nullptr)
     int64_t m0;         // first token of this launch
     int mc;             // tokens in this launch (1..16)
     int stages;         // ring depth
-    float *Y;
     unsigned *err;
     uint32_t act_off, act_warp;  // per-warp activation areas: offset, bytes each
     uint32_t bs_off, d_off;      // inside one warp's area
@@ -216,8 +215,7 @@ __global__ void __launch_bounds__(kMThreads, NT == 1 ? 2 : 1) gemv_mma_q4_K_kern
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nsb = a.nsb, K = nsb * QK_K;
-    const int64_t ntiles = tiles_of(a.N);
-    const int64_t npairs = (ntiles + 1) / 2;
+    const int64_t npairs = a.ms.off[a.ms.n];
     const int64_t pb = (int64_t)blockIdx.x * npairs / gridDim.x;
     const int64_t pe = ((int64_t)blockIdx.x + 1) * npairs / gridDim.x;
     const int64_t nchunks = (nsb + kSbStage - 1) / kSbStage;
@@ -270,15 +268,17 @@ __global__ void __launch_bounds__(kMThreads, NT == 1 ? 2 : 1) gemv_mma_q4_K_kern
                     *abort_flag = 1;
                     break;
                 }
-                const int64_t t0 = 2 * pair;
+                const int mi = mat_of(a.ms, pair);
+                const int64_t t0 = 2 * (pair - a.ms.off[mi]);
                 const int64_t sb0 = chunk * kSbStage;
                 const uint32_t bytes = (uint32_t)(nsb - sb0 < kSbStage ? nsb - sb0 : kSbStage) * kTileRows * B_Q4_K;
-                const bool has1 = t0 + 1 < ntiles;
+                const bool has1 = t0 + 1 < tiles_of(a.ms.N[mi]);
+                const uint8_t *W = a.ms.W[mi];
                 const uint32_t dst = smem_u32(smem + (size_t)s * kMStage), bar = smem_u32(&full[s]);
                 mbar_arrive_expect_tx(bar, has1 ? 2 * bytes : bytes);
-                bulk_g2s(dst, a.Wp + (t0 * nsb + sb0) * (kTileRows * B_Q4_K), bytes, bar, pol);
+                bulk_g2s(dst, W + (t0 * nsb + sb0) * (kTileRows * B_Q4_K), bytes, bar, pol);
                 if (has1)
-                    bulk_g2s(dst + kMHalf, a.Wp + ((t0 + 1) * nsb + sb0) * (kTileRows * B_Q4_K),
+                    bulk_g2s(dst + kMHalf, W + ((t0 + 1) * nsb + sb0) * (kTileRows * B_Q4_K),
                              bytes, bar, pol);
                 if (++s == S) s = 0, ph ^= 1u;
                 if (++chunk == nchunks) chunk = 0, ++pair;
@@ -428,8 +428,10 @@ __global__ void __launch_bounds__(kMThreads, NT == 1 ? 2 : 1) gemv_mma_q4_K_kern
 #pragma unroll
                 for (int w = 0; w < kMWarps; ++w) v += rb[((w * NT + n) * 4 + e) * 32 + l];
                 const int m = n * 8 + 2 * (l & 3) + (e & 1);
-                const int64_t row = pair * 16 + (e >> 1) * 8 + (l >> 2);
-                if (m < mc && row < a.N) a.Y[(a.m0 + m) * a.N + row] = v;
+                const int mi = mat_of(a.ms, pair);
+                const int64_t N = a.ms.N[mi];
+                const int64_t row = (pair - a.ms.off[mi]) * 16 + (e >> 1) * 8 + (l >> 2);
+                if (m < mc && row < N) a.ms.Y[mi][(a.m0 + m) * N + row] = v;
             }
             ++pair_no;
         }
@@ -565,18 +567,18 @@ cudaError_t launch_quantize_mma_image(const float *X, void *img, int64_t M, int6
 
 // X != nullptr: the activation quantizer runs inside the kernel; otherwise the
 // activations are the images written by launch_quantize_mma_image at img.
-cudaError_t launch_gemv_mma_q4_K(const void *Wp, int64_t N, int64_t K, const float *X,
-                                 const void *img, int64_t M, float *Y, bool pdl, cudaStream_t s) {
+cudaError_t launch_gemv_mma_q4_K(MatSet ms, int64_t K, const float *X, const void *img, int64_t M,
+                                 bool pdl, cudaStream_t s) {
+    ms.off[0] = 0;
+    for (int i = 0; i < ms.n; ++i) ms.off[i + 1] = ms.off[i] + (tiles_of(ms.N[i]) + 1) / 2;
     MmaArgs a;
-    a.Wp = static_cast<const uint8_t *>(Wp);
-    a.N = N;
+    a.ms = ms;
     a.nsb = K / QK_K;
     a.X = X;
-    a.Y = Y;
     a.err = device_error_word();
     const int per = gemv_mma_max_tokens(K);
     if (per == 0) return cudaErrorInvalidValue;
-    const int64_t npairs = (tiles_of(N) + 1) / 2;
+    const int64_t npairs = ms.off[ms.n];
     const uint8_t *im = static_cast<const uint8_t *>(img);
     for (int64_t m0 = 0; m0 < M; m0 += per) {
         Plan p;

@@ -49,6 +49,24 @@ struct Planar {
     int16_t *sums;
 };
 
+// Weight matrices that share K and the activations X of one decode launch
+// (a layer's q/k/v or gate/up projections): Y_i = X W_i^T. Their work units
+// (tile pairs for Q4_K, tiles for Q4_0) are numbered one after another:
+// matrix i owns units off[i] .. off[i+1]-1.
+constexpr int kMaxMats = 8;
+struct MatSet {
+    int n;
+    const uint8_t *W[kMaxMats];
+    float *Y[kMaxMats];
+    int64_t N[kMaxMats];
+    int64_t off[kMaxMats + 1];
+};
+__host__ __device__ __forceinline__ int mat_of(const MatSet &s, int64_t unit) {
+    int i = 0;
+    while (i + 1 < s.n && unit >= s.off[i + 1]) ++i;
+    return i;
+}
+
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Prefill (GEMM) activation layout for Q4_K weights, written by the prefill
@@ -367,9 +385,14 @@ cudaError_t launch_quantize_weights(qmm_type wt, const float *W, void *Wq, int64
                                     cudaStream_t s);
 cudaError_t launch_repack(qmm_type wt, bool inverse, const void *src, void *dst, int64_t N,
                           int64_t K, cudaStream_t s);
-// X != nullptr: fused quantizer (requires gemv_can_fuse(wt, M, K)).
+// X != nullptr: fused quantizer (requires gemv_can_fuse(wt, M, K)). The
+// MatSet form runs all its matrices in one launch (n, W, Y, N filled by the
+// caller; off is computed here).
+cudaError_t launch_gemv(qmm_type wt, MatSet ms, int64_t K, Planar x, const float *X, int64_t M,
+                        bool pdl, cudaStream_t s);
 cudaError_t launch_gemv(qmm_type wt, const void *Wp, int64_t N, int64_t K, Planar x,
                         const float *X, int64_t M, float *Y, bool pdl, cudaStream_t s);
+MatSet single_mat(const void *Wp, int64_t N, float *Y);
 bool gemv_can_fuse(qmm_type wt, int64_t M, int64_t K);
 // Tensor-core decode GEMV for Q4_K (gemv_mma.cu): used from kMmaMinM tokens
 // on while one token's activations fit its shared memory
@@ -383,8 +406,8 @@ bool gemv_use_mma(qmm_type wt, int64_t M, int64_t K);
 size_t gemv_mma_image_bytes(int64_t M, int64_t K);
 cudaError_t launch_quantize_mma_image(const float *X, void *img, int64_t M, int64_t K,
                                       cudaStream_t s);
-cudaError_t launch_gemv_mma_q4_K(const void *Wp, int64_t N, int64_t K, const float *X,
-                                 const void *img, int64_t M, float *Y, bool pdl, cudaStream_t s);
+cudaError_t launch_gemv_mma_q4_K(MatSet ms, int64_t K, const float *X, const void *img, int64_t M,
+                                 bool pdl, cudaStream_t s);
 size_t prefill_bytes(int64_t M, int64_t K, PrefillWs *p, uint8_t *base);
 cudaError_t launch_quantize_prefill(const float *X, PrefillWs p, int64_t M, int64_t K,
                                     cudaStream_t s);

@@ -85,7 +85,7 @@ extern "C" qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int6
     // byte the GEMV reads.
     if (mma) {
         cudaError_t e = launch_quantize_mma_image(X, scratch, M, K, s);
-        if (e == cudaSuccess) e = launch_gemv_mma_q4_K(W_packed, N, K, nullptr, scratch, M, Y, true, s);
+        if (e == cudaSuccess) e = launch_gemv_mma_q4_K(single_mat(W_packed, N, Y), K, nullptr, scratch, M, true, s);
         if (e != cudaSuccess)
             return set_error(QMM_ERR_CUDA, "mul_mat launch: %s", cudaGetErrorString(e));
         return set_error(QMM_OK, "");

@@ -172,6 +172,22 @@ qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon
 qmm_status qmm_mul_mat(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X,
                        int64_t M, float *Y, qmm_stream_t stream);
 
+/* Several weight matrices that read the same activations (a layer's q, k and
+ * v projections, or gate and up): Y_i [M, N_i] = W_i [N_i, K] . X [M, K]^T for
+ * i < n, 1 <= n <= 8. X is quantized once for all of them (page 1, "为什么
+ * 每个任务都要重新量化激活": re-quantizing one input per projection is
+ * repeated work), and up to 16 tokens run as ONE decode launch whose work is
+ * the rows of all the matrices, so the small ones no longer pay a launch and
+ * a tail each. Results equal n qmm_mul_mat calls (same codes, same sums).
+ * W_packed, N and Y are HOST arrays of n entries (device pointers to packed
+ * weights / outputs, row counts); K, X, M, stream and the errors are those of
+ * qmm_mul_mat, checked for every i. Matrices with N_i == 0 are skipped.
+ * Above 16 tokens the prefill GEMM runs once per matrix on the shared
+ * quantized activations. */
+qmm_status qmm_mul_mat_multi(qmm_type wt, int n, const void *const *W_packed, const int64_t *N,
+                             int64_t K, const float *X, int64_t M, float *const *Y,
+                             qmm_stream_t stream);
+
 /* qmm_mul_mat with a caller-provided workspace of at least
  * qmm_workspace_bytes(wt, M, K) bytes (QMM_ERR_WORKSPACE otherwise). The
  * workspace is in use until the call's work on `stream` has finished. */
@@ -185,8 +201,10 @@ qmm_status qmm_mul_mat_ws(qmm_type wt, const void *W_packed, int64_t N, int64_t 
  * input need not each re-quantize it).
  * qmm_quantize_activations: quantize X [M, K] for weights of type wt into
  *   `workspace` (qmm_workspace_bytes(wt, M, K) bytes, 16-byte aligned), in
- *   this library's private layout: int8 codes [M][K], fp32 block scales and
- *   int16 code sums (Q8_K: 16 per super-block; Q8_0: 1 per block). The codes
+ *   a private layout chosen by (wt, M, K) for the kernel that will read it:
+ *   int8 codes with fp32 block scales and int16 code sums for the scalar
+ *   decode GEMV; the fp16 codes, fp16 16-code sums and fp32 scales of the
+ *   tensor-core kernels (Q4_K decode from 2 tokens, and prefill). The codes
  *   and scales are those of qmm_quantize_row_q8.
  * qmm_mul_mat_prepared: Y [M, N] from packed weights and a workspace filled
  *   by qmm_quantize_activations with the same wt, M and K (the contents are

@@ -285,3 +285,43 @@ def test_70B_layer_sampled_rows(q, orc):
         check_close(host(Y)[rows][None, :], ref["y64"], ref["den"], L.name)
         del w, Wp, back
         torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ several projections, one launch
+@pytest.mark.parametrize("wt,Ns,K,M", [
+    (1, (96, 40, 37), 4096, 1),        # scalar GEMV, quantizer fused
+    (1, (96, 40, 37), 4096, 2),        # tensor-core GEMV, quantizer fused
+    (1, (200, 16, 8, 56), 2304, 5),    # tensor-core GEMV on the activation image
+    (1, (64, 0, 24), 8192, 1),         # a matrix with no rows is skipped
+    (0, (64, 40, 13), 1024, 1), (0, (64, 40), 4160, 3),
+    (1, (48, 32), 1024, 40), (0, (40, 24), 1024, 33)])  # prefill GEMM per matrix
+def test_mul_mat_multi(q, orc, wt, Ns, K, M):
+    """qmm_mul_mat_multi: Y_i = X W_i^T for all i from one quantization of X
+    (and one decode launch); each Y_i equals a qmm_mul_mat call bit for bit
+    and the oracle within tolerance."""
+    x = wl.activations(15, M, K).numpy()
+    X = dev(x)
+    Wcs, Wps, Ys = [], [], []
+    for i, N in enumerate(Ns):
+        w = wl.weights(30 + i, max(N, 1), K, 0.02, row_offset_std=0.005 if wt == 1 else 0.0).numpy()[:N]
+        Wc = orc.quantize(wt, w) if N else np.zeros((0, K // (256 if wt == 1 else 32) * (144 if wt == 1 else 18)), np.uint8)
+        Wp = q.empty_packed(wt, max(N, 1), K)
+        if N:
+            q.qmm_repack_weights(wt, dev(Wc), Wp, N, K)
+        Wcs.append(Wc)
+        Wps.append(Wp)
+        Ys.append(torch.full((max(M * N, 1),), float("nan"), device="cuda"))
+    q.qmm_mul_mat_multi(wt, Wps, list(Ns), K, X, M, Ys)
+    for N, Wc, Wp, Y in zip(Ns, Wcs, Wps, Ys):
+        if N == 0:
+            assert torch.isnan(Y).all()  # untouched
+            continue
+        Y1 = torch.empty(M * N, device="cuda")
+        q.qmm_mul_mat(wt, Wp, N, K, X, M, Y1)
+        assert torch.equal(Y, Y1), f"N={N}: multi differs from a single call"
+        ref = orc.mul_mat(wt, Wc, N, K, x, nthreads=orc.default_threads())
+        check_close(host(Y).reshape(M, N), ref["y64"], ref["den"], f"multi wt={wt} N={N} M={M}")
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_mul_mat_multi(wt, Wps * 5, list(Ns) * 5, K, X, M, Ys * 5)  # more than 8
+    assert e.value.status == 1
+    q.qmm_check_device_error()
