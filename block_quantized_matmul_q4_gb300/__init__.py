@@ -45,6 +45,7 @@ _SIGS = {
     "qmm_unrepack_weights": (_i32, [_i32, _vp, _vp, _i64, _i64, _vp]),
     "qmm_mul_mat": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_mul_mat_ws": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "qmm_mul_mat_q8": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_mul_mat_multi": (_i32, [_i32, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_i64), _i64, _vp,
                                  _i64, ctypes.POINTER(_vp), _vp]),
     "qmm_quantize_activations": (_i32, [_i32, _vp, _i64, _i64, _vp, _sz, _vp]),
@@ -135,6 +136,12 @@ def qmm_unrepack_weights(wt: int, W_packed, W_canon, N: int, K: int, stream=None
 def qmm_mul_mat(wt: int, W_packed, N: int, K: int, X, M: int, Y, stream=None):
     _check("qmm_mul_mat",
            _lib.qmm_mul_mat(wt, _ptr(W_packed), N, K, _ptr(X), M, _ptr(Y), _stream(stream)))
+
+
+def qmm_mul_mat_q8(wt: int, W_packed, N: int, K: int, Xq, M: int, Y, stream=None):
+    """Y = Xq W^T from canonical Q8 activation blocks (qmm_quantize_row_q8)."""
+    _check("qmm_mul_mat_q8",
+           _lib.qmm_mul_mat_q8(wt, _ptr(W_packed), N, K, _ptr(Xq), M, _ptr(Y), _stream(stream)))
 
 
 def qmm_mul_mat_multi(wt: int, W_packed: list, N: list, K: int, X, M: int, Y: list, stream=None):

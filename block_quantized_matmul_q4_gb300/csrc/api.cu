@@ -382,6 +382,48 @@ qmm_status qmm_mul_mat(qmm_type wt, const void *W_packed, int64_t N, int64_t K, 
     return st;
 }
 
+qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const void *Xq,
+                          int64_t M, float *Y, qmm_stream_t stream) {
+    qmm_status st = check_weight_args(wt, N, K);
+    if (st != QMM_OK) return st;
+    QMM_CHECK_ARG(M >= 0, "M must be >= 0 (got %lld)", (long long)M);
+    if (M == 0 || N == 0) return ok();
+    QMM_CHECK_ARG(W_packed && Xq && Y, "null pointer argument");
+    QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(Y, 4), "W_packed must be 16-byte aligned, Y 4-byte");
+    QMM_CHECK_ARG(aligned(Xq, wt == QMM_TYPE_Q4_K ? 4 : 2),
+                  "Xq must be aligned like its blocks (Q8_K: 4 bytes, Q8_0: 2 bytes)");
+    cudaStream_t s = (cudaStream_t)stream;
+    prepare_pool();
+    const size_t need = qmm_workspace_bytes(wt, M, K);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess || !ws) {
+        cudaGetLastError();
+        return set_error(QMM_ERR_NOMEM, "cudaMallocAsync(%zu): %s", need, cudaGetErrorString(e));
+    }
+    // the caller's blocks, rewritten into the layout the kernel for (wt, M, K) reads
+    if (use_gemm(wt, M)) {
+        if (wt == QMM_TYPE_Q4_0) {
+            e = launch_import_q4_0_prefill(Xq, ws, M, K, s);
+        } else {
+            PrefillWs pw;
+            prefill_bytes(M, K, &pw, (uint8_t *)ws);
+            e = launch_import_prefill(Xq, pw, M, K, s);
+        }
+    } else if (gemv_use_mma(wt, M, K)) {
+        e = launch_import_mma_image(Xq, ws, M, K, s);
+    } else {
+        Planar p;
+        planar_bytes(M, K, elems(wt), &p, (uint8_t *)ws);
+        e = launch_import_q8_planar(act_of(wt), Xq, p, M, K, s);
+    }
+    st = cuda_status(e, "activation import launch");
+    if (st == QMM_OK) st = prepared_impl(wt, W_packed, N, K, ws, need, M, Y, s);
+    cudaError_t ef = cudaFreeAsync(ws, s);
+    if (st == QMM_OK && ef != cudaSuccess) return cuda_status(ef, "cudaFreeAsync");
+    return st;
+}
+
 qmm_status qmm_mul_mat_multi(qmm_type wt, int n, const void *const *W_packed, const int64_t *N,
                              int64_t K, const float *X, int64_t M, float *const *Y,
                              qmm_stream_t stream) {

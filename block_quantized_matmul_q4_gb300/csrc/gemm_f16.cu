@@ -399,7 +399,38 @@ __global__ void __launch_bounds__(256) quantize_q4_0_prefill_kernel(const float 
     }
 }
 
+// The same operand from canonical Q8_0 blocks [M][nb] x 34 B, for
+// qmm_mul_mat_q8.
+__global__ void __launch_bounds__(256) import_q8_0_prefill_kernel(const uint8_t *__restrict__ Xq,
+                                                                  __half *__restrict__ out,
+                                                                  int64_t nblocks) {
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int e = lane, ep = e & 15, i = ep >> 2, r = ep & 3;
+    const int pos = 8 * i + ((e >> 4) << 2) + 2 * (r & 1) + (r >> 1);
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += nwarps) {
+        const uint8_t *blk = Xq + b * B_Q8_0;
+        const int q = (int8_t)blk[2 + lane];
+        const float d = __half2float(*reinterpret_cast<const __half *>(blk));
+        out[b * QK4_0 + pos] = __float2half_rn(d * (float)q);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_import_q4_0_prefill(const void *Xq, void *ws, int64_t M, int64_t K,
+                                       cudaStream_t s) {
+    const int64_t nblocks = M * (K / QK4_0);
+    int64_t grid = (nblocks + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    import_q8_0_prefill_kernel<<<(int)grid, 256, 0, s>>>(static_cast<const uint8_t *>(Xq),
+                                                         static_cast<__half *>(ws), nblocks);
+    count_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, int64_t G,
                               const __half *A, __half *C, int64_t M, int64_t N, int64_t K,

@@ -524,6 +524,40 @@ __global__ void __launch_bounds__(256) quantize_q8K_prefill_kernel(const float *
     }
 }
 
+// The same layout from canonical Q8_K blocks [M][nsb] x 292 B (codes, scale
+// and stored 16-code sums), for qmm_mul_mat_q8.
+__global__ void __launch_bounds__(256) import_q8K_prefill_kernel(const uint8_t *__restrict__ Xq,
+                                                                 __half *__restrict__ y16,
+                                                                 __half *__restrict__ bs16,
+                                                                 float *__restrict__ daT,
+                                                                 int64_t M, int64_t nsb) {
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t nblocks = M * nsb;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
+         b += nwarps) {
+        const int64_t m = b / nsb, sb = b % nsb;
+        const uint8_t *blk = Xq + b * B_Q8_K;
+        const uint32_t *qw = reinterpret_cast<const uint32_t *>(blk + 4 + 8 * lane);
+        const uint32_t lo = qw[0], hi = qw[1];
+        uint4 o;
+        uint32_t *po = &o.x;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t wsrc = i < 2 ? lo : hi;
+            const int sh = 8 * (i & 1);  // pair (e0, e2), then (e1, e3)
+            const int8_t c0 = (int8_t)(wsrc >> sh);
+            const int8_t c1 = (int8_t)(wsrc >> (16 + sh));
+            po[i] = h2_bits(__halves2half2(__int2half_rn(c0), __int2half_rn(c1)));
+        }
+        *reinterpret_cast<uint4 *>(y16 + b * QK_K + 8 * lane) = o;
+        if (lane < 16)
+            bs16[b * 16 + lane] = __int2half_rn(reinterpret_cast<const int16_t *>(blk + 260)[lane]);
+        if (lane == 0) daT[sb * ((M + 3) & ~(int64_t)3) + m] = *reinterpret_cast<const float *>(blk);
+    }
+}
+
 }  // namespace
 
 namespace tc {
@@ -615,6 +649,19 @@ cudaError_t launch_quantize_prefill(const float *X, PrefillWs p, int64_t M, int6
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     quantize_q8K_prefill_kernel<<<(int)grid, 256, 0, s>>>(X, p.y16, p.bs16, p.daT, M, K / QK_K);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_import_prefill(const void *Xq, PrefillWs p, int64_t M, int64_t K,
+                                  cudaStream_t s) {
+    const int64_t nblocks = M * (K / QK_K);
+    int64_t grid = (nblocks + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    import_q8K_prefill_kernel<<<(int)grid, 256, 0, s>>>(static_cast<const uint8_t *>(Xq), p.y16,
+                                                        p.bs16, p.daT, M, K / QK_K);
     count_launch();
     return cudaGetLastError();
 }

@@ -487,6 +487,38 @@ __global__ void __launch_bounds__(256) quantize_mma_image_kernel(const float *X,
     if (ml == 0 && lane < L.nt * 8 - mc) dsl[mc + lane] = 0.0f;
 }
 
+// The same image from canonical Q8_K blocks [M][nsb] x 292 B (their codes,
+// scale and stored 16-code sums), for qmm_mul_mat_q8.
+__global__ void __launch_bounds__(256) import_mma_image_kernel(const uint8_t *Xq, uint8_t *img,
+                                                               int64_t M, int64_t nsb, int per) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    if (gw >= M * nsb) return;
+    pdl_wait();
+    const int64_t m = gw / nsb, sb = gw % nsb;
+    const int64_t chunk = m / per;
+    const int ml = (int)(m - chunk * per);
+    const int mc = (int)(M - chunk * per < per ? M - chunk * per : per);
+    const Layout full = act_layout(nsb, per), L = act_layout(nsb, mc);
+    uint8_t *area = img + (size_t)chunk * kMWarps * full.warp_bytes + (sb % kMWarps) * L.warp_bytes;
+    const int64_t j = sb / kMWarps;
+    const uint8_t *blk = Xq + gw * B_Q8_K;
+    const uint32_t *qw = reinterpret_cast<const uint32_t *>(blk + 4 + 8 * lane);
+    const uint32_t w[2] = {qw[0], qw[1]};
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = (float)(int8_t)(w[i >> 2] >> (8 * (i & 3)));
+    const uint32_t h[4] = {half2_bits(q[0], q[2]), half2_bits(q[1], q[3]), half2_bits(q[4], q[6]),
+                           half2_bits(q[5], q[7])};
+    const float bsum = (float)reinterpret_cast<const int16_t *>(blk + 260)[lane >> 1];
+    const float d = *reinterpret_cast<const float *>(blk);
+    float *dsl = reinterpret_cast<float *>(area + L.d_off) + j * (L.nt * 8);
+    put_sb(area + (j * mc + ml) * kSbCodes, area + L.bs_off + (j * mc + ml) * kSbSums, dsl + ml, ml,
+           lane, h, bsum, d);
+    if (ml == 0 && lane < L.nt * 8 - mc) dsl[mc + lane] = 0.0f;
+}
+
 struct Plan {
     Layout L;
     int stages, ctas_per_sm;
@@ -563,6 +595,16 @@ cudaError_t launch_quantize_mma_image(const float *X, void *img, int64_t M, int6
                                        M, nsb, per);
     count_launch();
     return e;
+}
+
+cudaError_t launch_import_mma_image(const void *Xq, void *img, int64_t M, int64_t K, cudaStream_t s) {
+    const int per = gemv_mma_max_tokens(K);
+    if (per == 0) return cudaErrorInvalidValue;
+    const int64_t nsb = K / QK_K;
+    import_mma_image_kernel<<<(unsigned)((M * nsb + 7) / 8), 256, 0, s>>>(
+        static_cast<const uint8_t *>(Xq), static_cast<uint8_t *>(img), M, nsb, per);
+    count_launch();
+    return cudaGetLastError();
 }
 
 // X != nullptr: the activation quantizer runs inside the kernel; otherwise the

@@ -383,6 +383,14 @@ cudaError_t launch_quantize_q8(qmm_type vt, bool planar, const float *X, void *o
                                int64_t M, int64_t K, cudaStream_t s);
 cudaError_t launch_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N, int64_t K,
                                     cudaStream_t s);
+// Canonical Q8 blocks (qmm_mul_mat_q8) into each private activation layout:
+// planar (scalar GEMV), image (tensor-core GEMV), the two prefill operands.
+cudaError_t launch_import_q8_planar(qmm_type vt, const void *Xq, Planar p, int64_t M, int64_t K,
+                                    cudaStream_t s);
+cudaError_t launch_import_mma_image(const void *Xq, void *img, int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_import_prefill(const void *Xq, PrefillWs p, int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_import_q4_0_prefill(const void *Xq, void *ws, int64_t M, int64_t K,
+                                       cudaStream_t s);
 cudaError_t launch_repack(qmm_type wt, bool inverse, const void *src, void *dst, int64_t N,
                           int64_t K, cudaStream_t s);
 // X != nullptr: fused quantizer (requires gemv_can_fuse(wt, M, K)). The

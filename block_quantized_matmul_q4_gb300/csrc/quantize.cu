@@ -93,6 +93,45 @@ __global__ void __launch_bounds__(256) quantize_q8_K_kernel(const float *__restr
     }
 }
 
+// ---------------------------------------------------------------- canonical Q8 -> planar
+// qmm_mul_mat_q8: the caller's canonical blocks (their codes, scales and, for
+// Q8_K, the stored 16-code sums) rewritten into the planar layout.
+__global__ void __launch_bounds__(256) import_q8_0_planar_kernel(const uint8_t *__restrict__ Xq,
+                                                                 Planar p, int64_t nblocks) {
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
+         b += nwarps) {
+        const uint8_t *blk = Xq + b * B_Q8_0;
+        const int q = (int8_t)blk[2 + lane];
+        const int s = __reduce_add_sync(kFull, q);
+        p.qs[b * 32 + lane] = (int8_t)q;
+        if (lane == 0) {
+            p.d[b] = __half2float(*reinterpret_cast<const __half *>(blk));
+            p.sums[b] = (int16_t)s;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) import_q8_K_planar_kernel(const uint8_t *__restrict__ Xq,
+                                                                 Planar p, int64_t nblocks) {
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
+         b += nwarps) {
+        const uint8_t *blk = Xq + b * B_Q8_K;
+        const uint32_t *qw = reinterpret_cast<const uint32_t *>(blk + 4 + 8 * lane);
+        *reinterpret_cast<uint2 *>(p.qs + b * 256 + q8K_code_offset(lane)) = make_uint2(qw[0], qw[1]);
+        if (lane < 16)
+            *reinterpret_cast<int16_t *>(reinterpret_cast<uint8_t *>(p.sums + b * 16) +
+                                         q8K_bsum_offset(lane)) =
+                reinterpret_cast<const int16_t *>(blk + 260)[lane];
+        if (lane == 0) p.d[b] = *reinterpret_cast<const float *>(blk);
+    }
+}
+
 // ---------------------------------------------------------------- Q4_0 weights
 // One warp per block. d = -x_max / 8, x_max the signed value of largest
 // magnitude (first index on ties); q = clamp(floor(x * (1/d) + 8.5), 0, 15).
@@ -229,6 +268,18 @@ cudaError_t launch_quantize_q8(qmm_type vt, bool planar, const float *X, void *o
         else
             quantize_q8_K_kernel<false><<<grid, 256, 0, s>>>(X, o, p, nblocks);
     }
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_import_q8_planar(qmm_type vt, const void *Xq, Planar p, int64_t M, int64_t K,
+                                    cudaStream_t s) {
+    const int64_t nblocks = M * (K / (vt == QMM_TYPE_Q8_0 ? QK4_0 : QK_K));
+    const uint8_t *x = static_cast<const uint8_t *>(Xq);
+    if (vt == QMM_TYPE_Q8_0)
+        import_q8_0_planar_kernel<<<grid_for(nblocks), 256, 0, s>>>(x, p, nblocks);
+    else
+        import_q8_K_planar_kernel<<<grid_for(nblocks), 256, 0, s>>>(x, p, nblocks);
     count_launch();
     return cudaGetLastError();
 }

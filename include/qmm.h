@@ -172,6 +172,18 @@ qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon
 qmm_status qmm_mul_mat(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X,
                        int64_t M, float *Y, qmm_stream_t stream);
 
+/* qmm_mul_mat on activations that are already quantized: Xq holds M rows of
+ * canonical blocks as qmm_quantize_row_q8 writes them -- Q8_0 [M][K/32] x 34 B
+ * for Q4_0 weights, Q8_K [M][K/256] x 292 B for Q4_K (page 1: vec_dot takes
+ * the weight row and the Q8 activation row; for Q8_K the stored 16-code sums
+ * are used for the min term as they are). The blocks are rewritten into the
+ * private layout of the kernel that runs (in a workspace allocated like
+ * qmm_mul_mat's) and the result is that of qmm_mul_mat on any X that
+ * quantizes to Xq. Xq: device, aligned like its blocks (Q8_K 4 bytes, Q8_0
+ * 2 bytes); other arguments and errors as qmm_mul_mat. */
+qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const void *Xq,
+                          int64_t M, float *Y, qmm_stream_t stream);
+
 /* Several weight matrices that read the same activations (a layer's q, k and
  * v projections, or gate and up): Y_i [M, N_i] = W_i [N_i, K] . X [M, K]^T for
  * i < n, 1 <= n <= 8. X is quantized once for all of them (page 1, "为什么

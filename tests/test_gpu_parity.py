@@ -325,3 +325,35 @@ def test_mul_mat_multi(q, orc, wt, Ns, K, M):
         q.qmm_mul_mat_multi(wt, Wps * 5, list(Ns) * 5, K, X, M, Ys * 5)  # more than 8
     assert e.value.status == 1
     q.qmm_check_device_error()
+
+
+# ------------------------------------------------------------------ canonical Q8 input
+@pytest.mark.parametrize("wt,N,K,M", [(1, 40, 4096, 1), (1, 37, 2304, 2), (1, 64, 4096, 7),
+                                      (1, 24, 65536, 2), (1, 48, 1024, 33), (0, 40, 1024, 1),
+                                      (0, 13, 4160, 5), (0, 40, 1024, 40)])
+def test_mul_mat_q8(q, orc, wt, N, K, M):
+    """qmm_mul_mat_q8 on the canonical blocks of qmm_quantize_row_q8 equals
+    qmm_mul_mat on the fp32 input bit for bit (same codes, scales and sums,
+    same kernels), and so the oracle within tolerance; blocks written by the
+    oracle itself give the same result."""
+    vt = 3 if wt == 1 else 2
+    w = wl.weights(16, N, K, 0.02, row_offset_std=0.005 if wt == 1 else 0.0).numpy()
+    x = wl.activations(16, M, K).numpy()
+    Wc = orc.quantize(wt, w)
+    Wp = q.empty_packed(wt, N, K)
+    q.qmm_repack_weights(wt, dev(Wc), Wp, N, K)
+    X = dev(x)
+    Xq = q.empty_blocks(vt, M, K)
+    q.qmm_quantize_row_q8(vt, X, Xq, M, K)
+    Y = torch.full((M, N), float("nan"), device="cuda")
+    q.qmm_mul_mat_q8(wt, Wp, N, K, Xq, M, Y)
+    Yref = torch.empty(M, N, device="cuda")
+    q.qmm_mul_mat(wt, Wp, N, K, X, M, Yref)
+    assert torch.equal(Y, Yref), "mul_mat_q8 differs from mul_mat"
+    ref = orc.mul_mat(wt, Wc, N, K, x, nthreads=orc.default_threads())
+    check_close(host(Y), ref["y64"], ref["den"], f"q8 wt={wt} N={N} K={K} M={M}")
+    Xo = dev(orc.quantize(vt, x))  # the oracle's own blocks
+    Y2 = torch.empty(M, N, device="cuda")
+    q.qmm_mul_mat_q8(wt, Wp, N, K, Xo, M, Y2)
+    assert torch.equal(Y2, Y)
+    q.qmm_check_device_error()
