@@ -172,6 +172,21 @@ def timed(stream, fn):
     return a.elapsed_time(b) / 1e3
 
 
+def job_rate(t_local: float, units_local: float, world: int, device) -> tuple:
+    """Whole-job throughput of a weak-scaling run: every rank processed
+    units_local units in t_local seconds; the job took the slowest rank's
+    time, and value = (units of all ranks) / that time / 1e9. Collective over
+    the default process group when world > 1 (each rank ran the same K steps,
+    so the unit counts are equal)."""
+    t = t_local
+    if world > 1:
+        tt = torch.tensor([t_local], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        t = float(tt.item())
+    return t, units_local * world / t / 1e9
+
+
 def gpu_arm(args, rank, world):
     import block_quantized_matmul_q4_gb300 as q
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -228,15 +243,9 @@ def gpu_arm(args, rank, world):
     t = timed(stream, lambda: run_graphs(g_big, g_small, args.steps // GRAPH_STEPS))
     clk = clocks.stop()
     torch.cuda.synchronize()
-    if world > 1:
-        tt = torch.tensor([t], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.barrier()
-        t = float(tt.item())
-
     bw, bxq, by, bx = step_bytes(q, N, K, M)
     per_step = bw + bxq + by + bx
-    value = per_step * args.steps * world / t / 1e9
+    t, value = job_rate(t, per_step * args.steps, world, dev)
 
     # dominant kernel. With M*K this small the activation quantizer runs inside
     # the GEMV (one kernel per step), so the step's event timing is the
@@ -445,12 +454,12 @@ def gpu_extras(q, dev, stream, args):
     return out
 
 
-def sweep_rate(q, dev, stream):
+def sweep_rate(q, dev, stream, Ms=None):
     """The headline GEMV (Q4_K, N = K = 4096) at M in {1, 2, 4, 8, 16}: M = 1
     runs the scalar GEMV, M >= 2 the tensor-core one."""
     sweep = {}
     L = wl.GEMV_Q4_K_4096
-    for M in wl.GEMV_Q4_K_M_SWEEP:
+    for M in Ms or wl.GEMV_Q4_K_M_SWEEP:
         t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q4_K, L.N, L.K, M, 0, L)
         sweep[str(M)] = {"us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
                          "TOPS": round(2 * M * L.N * L.K / t / 1e12, 3)}
@@ -577,6 +586,8 @@ def main():
                     default="decode",
                     help="prefill / w4a16 / layer / sweep: only that measurement (for profiler "
                          "captures)")
+    ap.add_argument("--m", type=int, action="append",
+                    help="with --case sweep: only these token counts")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -611,7 +622,7 @@ def main():
     if args.case != "decode":
         import block_quantized_matmul_q4_gb300 as q
         fn = {"prefill": prefill_extras, "w4a16": w4a16_extras, "layer": layer_rate,
-              "sweep": sweep_rate}[args.case]
+              "sweep": lambda q, d, s: sweep_rate(q, d, s, args.m)}[args.case]
         print(json.dumps(fn(q, torch.device("cuda", torch.cuda.current_device()),
                             torch.cuda.Stream())), flush=True)
         return
