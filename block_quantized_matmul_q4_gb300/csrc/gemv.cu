@@ -219,11 +219,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
         if (lane == 0) {
             producer_loop(
                 r, n_items, a.err,
-                [&](int64_t it, uint32_t dst, uint32_t bar, uint64_t pol) {
-                    const int64_t p = pb + it / nchunks;
+                [&, chunk = (int64_t)0, p = pb](int64_t, uint32_t dst, uint32_t bar,
+                                                 uint64_t pol) mutable {
+                    // items in order: (pair, chunk) counted, not divided out
                     const int mi = mat_of(a.ms, p);
                     const int64_t t0 = 2 * (p - a.ms.off[mi]);
-                    const int64_t sb0 = (it % nchunks) * kQ4KChunk;
+                    const int64_t sb0 = chunk * kQ4KChunk;
+                    if (++chunk == nchunks) chunk = 0, ++p;
                     const uint32_t bytes =
                         (uint32_t)min64(kQ4KChunk, nsb - sb0) * kTileRows * B_Q4_K;
                     const bool has1 = t0 + 1 < tiles_of(a.ms.N[mi]);
@@ -282,10 +284,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = 0.0f;
 
+    int64_t chunk = 0, p = pb;  // the item's K chunk and tile pair, counted
     for (int64_t it = 0; it < n_items; ++it) {
         const int s = (int)(it % kStages);
         if (!mbar_wait(smem_u32(&r.full[s]), (uint32_t)((it / kStages) & 1), a.err)) break;
-        const int64_t chunk = it % nchunks;
         const int64_t sb0 = chunk * kQ4KChunk;
         const int cnt = (int)min64(kQ4KChunk, nsb - sb0);
         const uint8_t *stage = smem + s * kStageBytes;
@@ -320,7 +322,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&r.empty[s]));
         if (chunk == nchunks - 1) {
-            const int64_t p = pb + it / nchunks;
             const int mi = mat_of(a.ms, p);
             const int64_t N = a.ms.N[mi];
             float *Y = a.ms.Y[mi];
@@ -336,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
                 acc0[m] = acc1[m] = 0.0f;
             }
         }
+        if (++chunk == nchunks) chunk = 0, ++p;
     }
 }
 
@@ -364,10 +366,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
         if (lane == 0) {
             producer_loop(
                 r, n_items, a.err,
-                [&](int64_t it, uint32_t dst, uint32_t bar, uint64_t pol) {
-                    const int64_t tile = tb + it / nchunks;
+                [&, chunk = (int64_t)0, tile = tb](int64_t, uint32_t dst, uint32_t bar,
+                                                    uint64_t pol) mutable {
                     const int mi = mat_of(a.ms, tile);
-                    const int64_t b0 = (it % nchunks) * kQ40Chunk;
+                    const int64_t b0 = chunk * kQ40Chunk;
                     const uint32_t cnt = (uint32_t)min64(kQ40Chunk, nb - b0);
                     const uint8_t *tbase = a.ms.W[mi] + (tile - a.ms.off[mi]) * tile_bytes;
                     mbar_arrive_expect_tx(bar, cnt * kTileRows * B_Q4_0);
@@ -376,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
                                  pol);
                     bulk_g2s(dst + kDOff, tbase + nb * kTileRows * 16 + b0 * kTileRows * 2,
                              cnt * kTileRows * 2, bar, pol);
+                    if (++chunk == nchunks) chunk = 0, ++tile;
                 },
                 [&]() {
                     if (kMode == kStaged) stage_activations(r, a, mc, K, 1);
@@ -417,10 +420,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
 
+    int64_t chunk = 0, tile = tb;  // the item's K chunk and tile, counted
     for (int64_t it = 0; it < n_items; ++it) {
         const int s = (int)(it % kStages);
         if (!mbar_wait(smem_u32(&r.full[s]), (uint32_t)((it / kStages) & 1), a.err)) break;
-        const int64_t chunk = it % nchunks;
         const int64_t b0 = chunk * kQ40Chunk;
         const int cnt = (int)min64(kQ40Chunk, nb - b0);
         const uint8_t *stage = smem + s * kStageBytes;
@@ -463,7 +466,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&r.empty[s]));
         if (chunk == nchunks - 1) {
-            const int64_t tile = tb + it / nchunks;
             const int mi = mat_of(a.ms, tile);
             const int64_t N = a.ms.N[mi];
             const int64_t n = (tile - a.ms.off[mi]) * kTileRows + warp;
@@ -474,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
                 acc[m] = 0.0f;
             }
         }
+        if (++chunk == nchunks) chunk = 0, ++tile;
     }
 }
 
