@@ -38,7 +38,6 @@ constexpr int kRowsPerTile = 16;
 constexpr int kStepsPerStage = 16;  // 2048 elements per stage
 constexpr int kDStages = 5;
 constexpr int kDStageBytes = kStepsPerStage * kRowsPerTile * 64;  // 16 KB: [step][row][64 B]
-constexpr int kDRingBytes = kDStages * kDStageBytes;
 constexpr size_t kActStageMax = 16 * 1024;  // activations staged in shared memory up to this
 constexpr int kSzSlots = 2;                // tiles whose scales and zeros are staged at once
 
@@ -100,7 +99,8 @@ struct DecodeArgs {
     int64_t M, N, K, G;
     int ng, spg;  // groups per row, 128-element steps per group
     unsigned *err;
-    uint32_t act_bytes;  // > 0: all of A staged in shared memory (M * K * 2 bytes)
+    uint32_t act_bytes;  // > 0: all of A staged in shared memory (M * K * 2 bytes);
+                         // 0: A is read from global memory (L2) in place
 };
 
 // What one thread needs for one step besides the weights: its 32 activation
@@ -113,19 +113,18 @@ struct Operands {
     Zero2 z0, z1;
 };
 
+// xq[nt]: this thread's 32 activation elements of the step (shared or global
+// memory, generic addressing).
 template <int NT>
-__device__ __forceinline__ void load_ops(const DecodeArgs &a, const __half *xs,
-                                         const __half *const (&x_t)[NT], const __half *s_r0,
-                                         const __half *s_r1, const uint8_t *z_r0,
-                                         const uint8_t *z_r1, int st, Operands<NT> &P) {
+__device__ __forceinline__ void load_ops(const DecodeArgs &a, const __half *const (&xq)[NT],
+                                         const __half *s_r0, const __half *s_r1,
+                                         const uint8_t *z_r0, const uint8_t *z_r1, int st,
+                                         Operands<NT> &P) {
     const int g = a.spg == 1 ? st : st / a.spg;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const __half *xp = x_t[nt] + st * kStepK + 8 * q;
-            P.x[nt][q] = a.act_bytes ? *reinterpret_cast<const uint4 *>(xp) : ldg_nc128(xp);
-        }
+        for (int q = 0; q < 4; ++q) P.x[nt][q] = *reinterpret_cast<const uint4 *>(xq[nt] + 8 * q);
     P.s0 = __half2float(s_r0[g * kRowsPerTile]);
     P.s1 = __half2float(s_r1[g * kRowsPerTile]);
     P.z0 = make_zero2(z_r0[g * kRowsPerTile]);
@@ -185,16 +184,18 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
     const int64_t tb = (int64_t)blockIdx.x * ntiles / gridDim.x;
     const int64_t te = ((int64_t)blockIdx.x + 1) * ntiles / gridDim.x;
     const int64_t nsteps = a.K / kStepK;
-    const int64_t spt = (nsteps + kStepsPerStage - 1) / kStepsPerStage;  // stages per tile
+    constexpr int sps = kStepsPerStage, S = kDStages;
+    const int64_t spt = (nsteps + sps - 1) / sps;  // stages per tile
     // a tile's scales (16 rows x ng fp16) and zeros (16 x ng bytes), contiguous
     // in global memory and in its shared-memory slot
     const uint32_t s_bytes = (uint32_t)kRowsPerTile * (uint32_t)a.ng * 2u;
     const uint32_t z_bytes = (uint32_t)kRowsPerTile * (uint32_t)a.ng;
     const uint32_t sz_slot = s_bytes + z_bytes;  // multiple of 48
+    constexpr uint32_t ring_bytes = (uint32_t)S * kDStageBytes;
 
     // shared memory: weight ring | activations | scale/zero slots | barriers
-    __half *x_sm = reinterpret_cast<__half *>(smem + kDRingBytes);
-    uint8_t *sz_sm = smem + kDRingBytes + a.act_bytes;
+    __half *x_sm = reinterpret_cast<__half *>(smem + ring_bytes);
+    uint8_t *sz_sm = smem + ring_bytes + a.act_bytes;
     // the current tile's scales and zeros transposed to [group][16 rows], so
     // that the 8 rows a warp reads at once sit in neighbouring banks
     __half *s_tr = reinterpret_cast<__half *>(sz_sm + kSzSlots * sz_slot);
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
     uint64_t *szempty = szfull + kSzSlots;
     uint64_t *actb = szempty + kSzSlots;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kDStages; ++i) {
+        for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
             mbar_init(smem_u32(&empty[i]), kDecodeWarps);
         }
@@ -230,6 +231,8 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
                 bulk_g2s(smem_u32(x_sm), a.A, a.act_bytes, smem_u32(actb), policy_evict_last());
             }
             int64_t it = 0;
+            int s = 0;
+            uint32_t ph = 0;
             bool ok = true;
             for (int64_t tile = tb; tile < te && ok; ++tile) {
                 const int64_t ti = tile - tb;
@@ -255,21 +258,21 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
                     if (zb16) bulk_g2s(smem_u32(dst + s_bytes), zsrc, zb16, bar, pol);
                 }
                 for (int64_t sg = 0; sg < spt; ++sg, ++it) {
-                    const int s = (int)(it % kDStages);
-                    ok = mbar_wait(smem_u32(&empty[s]), (uint32_t)(((it / kDStages) & 1) ^ 1), a.err);
+                    ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u, a.err);
                     if (!ok) break;
-                    const int64_t step0 = sg * kStepsPerStage;
-                    const int64_t nst = nsteps - step0 < kStepsPerStage ? nsteps - step0 : kStepsPerStage;
+                    const int64_t step0 = sg * sps;
+                    const int64_t nst = nsteps - step0 < sps ? nsteps - step0 : sps;
                     const uint32_t bar = smem_u32(&full[s]);
                     // steps past K are not copied (and never read)
                     mbar_arrive_expect_tx(bar, (uint32_t)nst * 1024u);
-                    bulk_g2s(smem_u32(smem + s * kDStageBytes), a.W + (tile * nsteps + step0) * 1024,
+                    bulk_g2s(smem_u32(smem + (size_t)s * kDStageBytes), a.W + (tile * nsteps + step0) * 1024,
                              (uint32_t)nst * 1024u, bar, pol);
+                    if (++s == S) s = 0, ph ^= 1u;
                 }
             }
             // drain: nothing may still be landing when the CTA exits
-            for (int64_t k = it > kDStages ? it - kDStages : 0; k < it; ++k)
-                mbar_wait(smem_u32(&full[k % kDStages]), (uint32_t)((k / kDStages) & 1), a.err);
+            for (int64_t k = it > S ? it - S : 0; k < it; ++k)
+                mbar_wait(smem_u32(&full[k % S]), (uint32_t)((k / S) & 1), a.err);
             const int64_t nt_issued = te - tb;
             for (int64_t k = nt_issued > kSzSlots ? nt_issued - kSzSlots : 0; k < nt_issued; ++k)
                 mbar_wait(smem_u32(&szfull[k % kSzSlots]), (uint32_t)((k / kSzSlots) & 1), a.err);
@@ -291,7 +294,15 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
     } else {
         pdl_wait();  // the activations may come from the preceding kernel
     }
+    // tokens past M read a valid token's activations (they only feed outputs
+    // that are never stored)
+    int mt[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mt[nt] = nt * 8 + tok < a.M ? nt * 8 + tok : (int)a.M - 1;
     int64_t it = 0;
+    int s = 0;
+    uint32_t ph = 0;
+    constexpr int kps = sps / kDecodeWarps;  // this warp's steps per stage
     for (int64_t tile = tb; tile < te; ++tile) {
         const int64_t ti = tile - tb;
         const int zs = (int)(ti % kSzSlots);
@@ -314,12 +325,6 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
         // scales / zeros of rows r0, r1 for group g at index g * 16 (stride 16)
         const __half *s_r0 = s_tr + tok, *s_r1 = s_tr + tok + 8;
         const uint8_t *z_r0 = z_tr + tok, *z_r1 = z_tr + tok + 8;
-        const __half *x_t[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int64_t m = nt * 8 + tok < a.M ? nt * 8 + tok : a.M - 1;
-            x_t[nt] = xs + m * a.K + 32 * j;
-        }
         float tot[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -328,27 +333,30 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
         // This warp's steps are warp + 8k, k = 0 .. nk-1, two per stage. While
         // it computes step k it has the operands of step k + 1 in flight (two
         // register sets, alternating).
-        constexpr int kPerStage = kStepsPerStage / kDecodeWarps;
         const int nk = warp < nsteps ? (int)((nsteps - 1 - warp) / kDecodeWarps) + 1 : 0;
         Operands<NT> P[2];
-        if (nk > 0) load_ops<NT>(a, xs, x_t, s_r0, s_r1, z_r0, z_r1, warp, P[0]);
-        for (int64_t sg = 0; sg < spt; ++sg, ++it) {
-            const int s = (int)(it % kDStages);
-            if (ok) ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((it / kDStages) & 1), a.err);
-            const uint8_t *stage = smem + s * kDStageBytes;
+        auto ops = [&](int k, Operands<NT> &Q) {
+            const int64_t st = warp + (int64_t)k * kDecodeWarps;
+            const __half *xq[NT];
 #pragma unroll
-            for (int h = 0; h < kPerStage; ++h) {
-                const int k = (int)sg * kPerStage + h;
+            for (int nt = 0; nt < NT; ++nt) xq[nt] = xs + (int64_t)mt[nt] * a.K + st * kStepK + 32 * j;
+            load_ops<NT>(a, xq, s_r0, s_r1, z_r0, z_r1, (int)st, Q);
+        };
+        if (nk > 0) ops(0, P[0]);
+        for (int64_t sg = 0; sg < spt; ++sg, ++it) {
+            if (ok) ok = mbar_wait(smem_u32(&full[s]), ph, a.err);
+            const uint8_t *stage = smem + (size_t)s * kDStageBytes;
+#pragma unroll
+            for (int h = 0; h < kps; ++h) {
+                const int k = (int)sg * kps + h;
                 if (k < nk) {
-                    const int ls = warp + h * kDecodeWarps;
-                    if (k + 1 < nk)
-                        load_ops<NT>(a, xs, x_t, s_r0, s_r1, z_r0, z_r1, warp + (k + 1) * kDecodeWarps,
-                                     P[(h + 1) & 1]);
-                    step_mma<NT>(P[h & 1], stage + ls * 1024, tok, j, tot);
+                    if (k + 1 < nk) ops(k + 1, P[(h + 1) & 1]);
+                    step_mma<NT>(P[h & 1], stage + (warp + h * kDecodeWarps) * 1024, tok, j, tot);
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            if (++s == S) s = 0, ph ^= 1u;
         }
         // reduce the consumer warps' partial sums of this tile
 #pragma unroll
@@ -449,12 +457,13 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
     a.spg = (int)(G / kStepK);
     a.err = device_error_word();
     const int64_t ntiles = (N + kRowsPerTile - 1) / kRowsPerTile;
-    const int64_t grid = balanced_grid(ntiles, (M <= 8 ? 2 : 1) * (int64_t)sm_count());
     // all of A in shared memory when it is small (one bulk copy per CTA)
     const size_t act = (size_t)M * K * 2;
     a.act_bytes = act <= kActStageMax ? (uint32_t)act : 0u;
     const size_t sz = (size_t)(kSzSlots + 1) * kRowsPerTile * a.ng * 3;
-    const size_t smem = kDRingBytes + a.act_bytes + sz + (2 * kDStages + 2 * kSzSlots + 1) * 8;
+    const size_t bars = (2 * kDStages + 2 * kSzSlots + 1) * 8;
+    const int64_t grid = balanced_grid(ntiles, (M <= 8 ? 2 : 1) * (int64_t)sm_count());
+    const size_t smem = (size_t)kDStages * kDStageBytes + a.act_bytes + sz + bars;
     cudaError_t e;
     if (M <= 8) {
         e = ensure_smem_attr(reinterpret_cast<const void *>(w4a16_decode_kernel<1>), smem);
