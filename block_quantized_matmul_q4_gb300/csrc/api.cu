@@ -489,6 +489,13 @@ qmm_status qmm_debug_block_sums(qmm_type wt, const void *W_packed, int64_t N, in
         "debug kernel launch");
 }
 
+qmm_status qmm_debug_wait_timeout(int64_t limit_cycles, qmm_stream_t stream) {
+    QMM_CHECK_ARG(limit_cycles > 0 && limit_cycles <= 20000000000LL,
+                  "limit_cycles must be in (0, 2e10] (got %lld)", (long long)limit_cycles);
+    return cuda_status(launch_debug_wait_timeout(limit_cycles, (cudaStream_t)stream),
+                       "debug kernel launch");
+}
+
 const char *qmm_status_string(qmm_status s) {
     switch (s) {
     case QMM_OK: return "QMM_OK";

@@ -82,4 +82,26 @@ cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int6
     return cudaGetLastError();
 }
 
+// A bounded wait that is made to run out: one CTA waits on an mbarrier that
+// nothing completes, with the same helper as every pipeline wait of the
+// library and a short limit, so the failure path (error word set, kernel
+// returns, context usable) can be checked without any fault.
+namespace {
+__global__ void wait_timeout_kernel(unsigned *err, long long limit_cycles) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    mbar_wait_for(smem_u32(&bar), 0, err, limit_cycles);
+}
+}  // namespace
+
+cudaError_t launch_debug_wait_timeout(int64_t limit_cycles, cudaStream_t s) {
+    wait_timeout_kernel<<<1, 32, 0, s>>>(device_error_word(), (long long)limit_cycles);
+    count_launch();
+    return cudaGetLastError();
+}
+
 }  // namespace qmm

@@ -223,16 +223,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase of `bar` with the given parity to complete. Returns
 // false (and records a timeout in *err) if it has not after the bound.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned *err,
+                                              long long limit_cycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitTimeoutCycles) {
+        if (clock64() - t0 > limit_cycles) {
             atomicOr(err, kDevErrTimeout);
             return false;
         }
     }
     return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err) {
+    return mbar_wait_for(bar, parity, err, kWaitTimeoutCycles);
 }
 
 // 1-D bulk async copy global -> shared, completing on an mbarrier.
@@ -440,4 +444,5 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
                              float *Y, cudaStream_t s);
 cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
                                     const void *Xq, int64_t M, int32_t *out, cudaStream_t s);
+cudaError_t launch_debug_wait_timeout(int64_t limit_cycles, cudaStream_t s);
 }  // namespace qmm

@@ -283,6 +283,15 @@ qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t
 qmm_status qmm_debug_block_sums(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
                                 const void *Xq, int64_t M, int32_t *out, qmm_stream_t stream);
 
+/* Failure-detection check without a fault: launches one CTA that waits, with
+ * the same bounded-wait helper as every pipeline wait of this library but a
+ * limit of limit_cycles SM clocks (0 < limit_cycles <= 2e10), on an mbarrier
+ * that nothing completes. The wait gives up, records QMM_ERR_TIMEOUT in the
+ * device error word and the kernel returns; the next qmm_check_device_error
+ * on the stream reports it (and clears it). The CUDA context stays usable.
+ * Returns QMM_ERR_ARG for a bad limit, QMM_ERR_CUDA if the launch failed. */
+qmm_status qmm_debug_wait_timeout(int64_t limit_cycles, qmm_stream_t stream);
+
 /* ---------------------------------------------------------------- status */
 
 /* Static string naming a status code. */

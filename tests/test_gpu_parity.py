@@ -357,3 +357,28 @@ def test_mul_mat_q8(q, orc, wt, N, K, M):
     q.qmm_mul_mat_q8(wt, Wp, N, K, Xo, M, Y2)
     assert torch.equal(Y2, Y)
     q.qmm_check_device_error()
+
+
+# ------------------------------------------------------------------ failure detection
+def test_bounded_wait_times_out_and_context_survives(q, orc):
+    """A device-side wait that nothing completes gives up after its bound,
+    records QMM_ERR_TIMEOUT in the device error word (reported once, then
+    cleared) and the context keeps working: no fault, no hang."""
+    q.qmm_check_device_error()  # start clean
+    q.qmm_debug_wait_timeout(2_000_000)  # about 1 ms of SM clocks
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_check_device_error()
+    assert e.value.status == 4
+    q.qmm_check_device_error()  # cleared
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_debug_wait_timeout(0)
+    assert e.value.status == 1
+    # the same context still computes
+    N, K, M = 24, 512, 1
+    w = wl.weights(17, N, K, 0.02, row_offset_std=0.005).numpy()
+    x = wl.activations(17, M, K).numpy()
+    Wc = orc.quantize(1, w)
+    y = run_mul_mat(q, 1, Wc, N, K, x)
+    ref = orc.mul_mat(1, Wc, N, K, x)
+    check_close(y, ref["y64"], ref["den"], "after a timed-out wait")
+    q.qmm_check_device_error()
