@@ -80,6 +80,10 @@ struct GemmArgs {
     int64_t N, nsb, M;
     float *Y;  // [M][N]
     unsigned *err;
+    // stream-K: tile t = (row block t / mblocks, token block t % mblocks);
+    // unit u = t * nsb + super-block; CTA c takes units [c U / G, (c+1) U / G)
+    int64_t mblocks, units;
+    float *part;  // partial tiles: [CTA][slot 0: first tile, 1: last tile][col][row]
 };
 
 struct Bars {
@@ -169,10 +173,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + (sbase - raw_base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nsb = a.nsb;
-    const int64_t n0 = (int64_t)blockIdx.x * kBM, m0 = (int64_t)blockIdx.y * kBN;
-    const int64_t t0 = n0 / kTileRows;  // first packed tile
     const int64_t ntiles = tiles_of(a.N);
-    const int nt = (int)(ntiles - t0 < kBM / kTileRows ? ntiles - t0 : kBM / kTileRows);
+    // this CTA's units (stream-K): a contiguous range of (tile, super-block)
+    const int64_t u0 = (int64_t)blockIdx.x * a.units / gridDim.x;
+    const int64_t u1 = ((int64_t)blockIdx.x + 1) * a.units / gridDim.x;
+    const int64_t nunits = u1 - u0;
+    const int64_t first_tile = u0 / nsb;
 
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
     Bars B;
@@ -225,9 +231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             pdl_wait();  // the codes come from the preceding quantizer kernel
             int64_t issued_raw = 0, issued_act = 0;
             bool ok = true;
-            for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-                const int rs = (int)(sb % kRawStages);
-                ok = mbar_wait(smem_u32(&B.raw_empty[rs]), (uint32_t)(((sb / kRawStages) & 1) ^ 1), a.err);
+            for (int64_t i = 0; i < nunits && ok; ++i) {
+                const int64_t u = u0 + i, tile = u / nsb, sb = u - tile * nsb;
+                const int64_t t0 = (tile / a.mblocks) * (kBM / kTileRows);  // first packed tile
+                const int64_t m0 = (tile % a.mblocks) * kBN;
+                const int rs = (int)(i % kRawStages);
+                ok = mbar_wait(smem_u32(&B.raw_empty[rs]), (uint32_t)(((i / kRawStages) & 1) ^ 1), a.err);
                 if (!ok) break;
                 // tiles past the last one read as zeros (and are never stored)
                 const uint32_t rbar = smem_u32(&B.raw_full[rs]);
@@ -235,8 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tma_load_3d(smem_u32(smem + kOffRaw + rs * kRawBytes), &tmap_w, 0, (int32_t)sb,
                                 (int32_t)t0, rbar, pol);
                 ++issued_raw;
-                const int st = (int)(sb % kActStages);
-                ok = mbar_wait(smem_u32(&B.act_empty[st]), (uint32_t)(((sb / kActStages) & 1) ^ 1), a.err);
+                const int st = (int)(i % kActStages);
+                ok = mbar_wait(smem_u32(&B.act_empty[st]), (uint32_t)(((i / kActStages) & 1) ^ 1), a.err);
                 if (!ok) break;
                 const uint32_t abar = smem_u32(&B.act_full[st]);
                 uint8_t *stage = smem + kOffAct + st * kActBytes;
@@ -264,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a timeout the MMAs run on stale operands and the error word reports it.
         constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
         const uint64_t bdesc0 = tc::smem_desc(smem_u32(smem + kOffAct), 1024, 2);
-        for (int64_t sb = 0; sb < nsb; ++sb) {
-            const int buf = (int)(sb & 1), st = (int)(sb % kActStages);
+        for (int64_t i = 0; i < nunits; ++i) {
+            const int buf = (int)(i & 1), st = (int)(i % kActStages);
             const uint32_t dA = tmem + kColAccA + (uint32_t)(buf * kBN);
 #pragma unroll 1
             for (int g = 0; g < kGroups; ++g) {
@@ -289,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             handoff_sync();
             if (lane == 0) {
                 tc::fence_after_sync();
-                const uint32_t mins = smem_u32(smem + kOffMin + (int)(sb % kMinStages) * kMinBytes);
+                const uint32_t mins = smem_u32(smem + kOffMin + (int)(i % kMinStages) * kMinBytes);
                 const uint32_t bsum = smem_u32(smem + kOffAct + st * kActBytes + kChunksPerSB * kChunkBytes);
                 tc::mma_f16(tmem + kColAccB, tc::smem_desc(mins, 256, 6), tc::smem_desc(bsum, 256, 6),
                             idesc, false);
@@ -310,12 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // meets the issuer at the named barrier. After a timeout it stops
         // waiting but keeps meeting the issuer.
         bool ok = true;
-        for (int64_t sb = 0; sb < nsb; ++sb) {
-            const int buf = (int)(sb & 1), st = (int)(sb % kActStages);
-            const uint32_t par = (uint32_t)(sb & 1);
+        for (int64_t i = 0; i < nunits; ++i) {
+            const int buf = (int)(i & 1), st = (int)(i % kActStages);
+            const uint32_t par = (uint32_t)(i & 1);
             if (lane == 0 && ok)
-                ok = mbar_wait(smem_u32(&B.acc_empty[buf]), (uint32_t)(((sb >> 1) & 1) ^ 1), a.err) &&
-                     mbar_wait(smem_u32(&B.act_full[st]), (uint32_t)((sb / kActStages) & 1), a.err);
+                ok = mbar_wait(smem_u32(&B.acc_empty[buf]), (uint32_t)(((i >> 1) & 1) ^ 1), a.err) &&
+                     mbar_wait(smem_u32(&B.act_full[st]), (uint32_t)((i / kActStages) & 1), a.err);
 #pragma unroll 1
             for (int g = 0; g < kGroups; ++g) {
                 if (lane == 0 && ok) ok = mbar_wait(smem_u32(&B.a_full[g]), par, a.err);
@@ -333,12 +342,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
         const int set = (warp - 3) >> 2;  // chunk `set` of each group
         const int ti = ct / kTileRows, r = ct % kTileRows;
-        const bool valid = ti < nt;
         bool ok = true;
-        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-            const int rs = (int)(sb % kRawStages);
-            const uint32_t par = (uint32_t)(sb & 1);
-            ok = mbar_wait(smem_u32(&B.raw_full[rs]), (uint32_t)((sb / kRawStages) & 1), a.err);
+        int i = 0;  // units done: the pipeline position
+        // the CTA's units as pieces of tiles; per piece, its super-blocks
+        for (int64_t u = u0; u < u1 && ok;) {
+            const int64_t tile = u / nsb;
+            const int sb_begin = (int)(u - tile * nsb);
+            const int sb_end = (int)(nsb < sb_begin + (u1 - u) ? nsb : sb_begin + (u1 - u));
+            const bool valid = (tile / a.mblocks) * (kBM / kTileRows) + ti < ntiles;
+            u += sb_end - sb_begin;
+        for (int sb = sb_begin; sb < sb_end && ok; ++sb, ++i) {
+            const int rs = (int)(i % kRawStages);
+            const uint32_t par = (uint32_t)(i & 1);
+            ok = mbar_wait(smem_u32(&B.raw_full[rs]), (uint32_t)((i / kRawStages) & 1), a.err);
             if (!ok) break;
             const uint8_t *blk = smem + kOffRaw + rs * kRawBytes + (ti * kTileRows + r) * B_Q4_K;
             const uint4 hdr = valid ? *reinterpret_cast<const uint4 *>(blk) : make_uint4(0, 0, 0, 0);
@@ -365,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t hm[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) hm[j] = h2_bits(__float2half2_rn((float)m[j]));
-                    uint8_t *row = smem + kOffMin + (int)(sb % kMinStages) * kMinBytes + ct * 32;
+                    uint8_t *row = smem + kOffMin + (int)(i % kMinStages) * kMinBytes + ct * 32;
                     const int sw = (ct >> 2) & 1;
                     *reinterpret_cast<uint4 *>(row + 16 * (0 ^ sw)) = make_uint4(hm[0], hm[1], hm[2], hm[3]);
                     *reinterpret_cast<uint4 *>(row + 16 * (1 ^ sw)) = make_uint4(hm[4], hm[5], hm[6], hm[7]);
@@ -398,80 +414,104 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0 && ok) mbar_arrive(smem_u32(&B.raw_empty[rs]));
         }
+        }
     } else {
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 3 - kConvWarps;
         const int quarter = warp & 3;  // TMEM lanes 32 * (warp % 4) ..
-        const int part = ew >> 2;      // columns kEpiCols * part ..
+        const int cpart = ew >> 2;     // columns kEpiCols * cpart ..
         const int nl = quarter * 32 + lane;
-        const int64_t n = n0 + nl;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         float *da_stage = reinterpret_cast<float *>(smem + kOffDa) + ew * kEpiCols;
-        // this row's block headers (d, dmin as two fp16) and this warp's 32
-        // activation scales, read one super-block ahead
-        const bool row_ok = n < a.N;
-        const uint8_t *hdr_ptr = a.Wp + ((n / kTileRows) * nsb * kTileRows + (n % kTileRows)) * B_Q4_K;
         const int64_t Mpad = (a.M + 3) & ~(int64_t)3;
-        const int64_t mcol = m0 + part * kEpiCols + lane;
         pdl_wait();  // d_a comes from the preceding quantizer kernel
-        uint32_t hdr_next = row_ok ? ldg_nc_u32(hdr_ptr) : 0u;
-        float da_next = mcol < Mpad ? ldg_nc_f32(a.daT + mcol) : 0.0f;
-        uint64_t run[kEpiCols / 2];  // column pairs
-#pragma unroll
-        for (int j = 0; j < kEpiCols / 2; ++j) run[j] = 0;  // (+0.0f, +0.0f)
         bool ok = true;
-        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-            const int buf = (int)(sb & 1);
-            const uint32_t hdr = hdr_next;
-            const float da = da_next;
-            if (sb + 1 < nsb) {
-                if (row_ok) hdr_next = ldg_nc_u32(hdr_ptr + (sb + 1) * (kTileRows * B_Q4_K));
-                if (mcol < Mpad) da_next = ldg_nc_f32(a.daT + (sb + 1) * Mpad + mcol);
-            }
-            da_stage[lane] = da;
-            __syncwarp();
-            ok = mbar_wait(smem_u32(&B.acc_full[buf]), (uint32_t)((sb >> 1) & 1), a.err);
-            if (!ok) break;
-            tc::fence_after_sync();
-            const float dw = __half2float(__ushort_as_half((unsigned short)(hdr & 0xFFFFu)));
-            const float dmw = __half2float(__ushort_as_half((unsigned short)(hdr >> 16)));
-            const uint64_t dw2 = pk2(dw, dw), ndmw2 = pk2(-dmw, -dmw);
+        int i = 0;  // units done: the pipeline position
+        // the CTA's units as pieces of tiles: a whole tile goes to Y, a part of
+        // one to this CTA's slot (0: its first tile, 1: its last) for the fixup
+        for (int64_t u = u0; u < u1 && ok;) {
+            const int64_t tile = u / nsb;
+            const int sb_begin = (int)(u - tile * nsb);
+            const int sb_end = (int)(nsb < sb_begin + (u1 - u) ? nsb : sb_begin + (u1 - u));
+            u += sb_end - sb_begin;
+            const int64_t n = (tile / a.mblocks) * kBM + nl;
+            const int64_t mb0 = (tile % a.mblocks) * kBN + cpart * kEpiCols;
+            // this row's block headers (d, dmin as two fp16) and this warp's 32
+            // activation scales, read one super-block ahead
+            const bool row_ok = n < a.N;
+            const uint8_t *hdr_ptr = a.Wp + ((n / kTileRows) * nsb * kTileRows + (n % kTileRows)) * B_Q4_K;
+            const int64_t mcol = mb0 + lane;
+            uint32_t hdr_next = row_ok ? ldg_nc_u32(hdr_ptr + sb_begin * (kTileRows * B_Q4_K)) : 0u;
+            float da_next = mcol < Mpad ? ldg_nc_f32(a.daT + sb_begin * Mpad + mcol) : 0.0f;
+            uint64_t run[kEpiCols / 2];  // column pairs
 #pragma unroll
-            for (int c8 = 0; c8 < kEpiCols / 8; ++c8) {
-                const uint32_t col = (uint32_t)(part * kEpiCols + c8 * 8);
-                float A[8], Bv[8];
-                tc::tmem_ld8(tmem + lane_addr + kColAccA + (uint32_t)(buf * kBN) + col, A);
-                tc::tmem_ld8(tmem + lane_addr + kColAccB + col, Bv);
-                tc::tmem_ld_wait();
+            for (int j = 0; j < kEpiCols / 2; ++j) run[j] = 0;  // (+0.0f, +0.0f)
+            for (int sb = sb_begin; sb < sb_end && ok; ++sb, ++i) {
+                const int buf = i & 1;
+                const uint32_t hdr = hdr_next;
+                const float da = da_next;
+                if (sb + 1 < sb_end) {
+                    if (row_ok) hdr_next = ldg_nc_u32(hdr_ptr + (sb + 1) * (kTileRows * B_Q4_K));
+                    if (mcol < Mpad) da_next = ldg_nc_f32(a.daT + (sb + 1) * Mpad + mcol);
+                }
+                da_stage[lane] = da;
+                __syncwarp();
+                ok = mbar_wait(smem_u32(&B.acc_full[buf]), (uint32_t)((i >> 1) & 1), a.err);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const float dw = __half2float(__ushort_as_half((unsigned short)(hdr & 0xFFFFu)));
+                const float dmw = __half2float(__ushort_as_half((unsigned short)(hdr >> 16)));
+                const uint64_t dw2 = pk2(dw, dw), ndmw2 = pk2(-dmw, -dmw);
 #pragma unroll
-                for (int j4 = 0; j4 < 2; ++j4) {
-                    const float4 dav = *reinterpret_cast<const float4 *>(da_stage + c8 * 8 + 4 * j4);
-                    const uint64_t dv[2] = {pk2(dav.x, dav.y), pk2(dav.z, dav.w)};
+                for (int c8 = 0; c8 < kEpiCols / 8; ++c8) {
+                    const uint32_t col = (uint32_t)(cpart * kEpiCols + c8 * 8);
+                    float A[8], Bv[8];
+                    tc::tmem_ld8(tmem + lane_addr + kColAccA + (uint32_t)(buf * kBN) + col, A);
+                    tc::tmem_ld8(tmem + lane_addr + kColAccB + col, Bv);
+                    tc::tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = 4 * j4 + 2 * e;
-                        // run += d_a (d A - dmin B), two columns at a time
-                        const uint64_t t = fma2(pk2(A[j], A[j + 1]), dw2,
-                                                mul2(pk2(Bv[j], Bv[j + 1]), ndmw2));
-                        run[(c8 * 8 + j) / 2] = fma2(dv[e], t, run[(c8 * 8 + j) / 2]);
+                    for (int j4 = 0; j4 < 2; ++j4) {
+                        const float4 dav = *reinterpret_cast<const float4 *>(da_stage + c8 * 8 + 4 * j4);
+                        const uint64_t dv[2] = {pk2(dav.x, dav.y), pk2(dav.z, dav.w)};
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int j = 4 * j4 + 2 * e;
+                            // run += d_a (d A - dmin B), two columns at a time
+                            const uint64_t t = fma2(pk2(A[j], A[j + 1]), dw2,
+                                                    mul2(pk2(Bv[j], Bv[j + 1]), ndmw2));
+                            run[(c8 * 8 + j) / 2] = fma2(dv[e], t, run[(c8 * 8 + j) / 2]);
+                        }
                     }
                 }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&B.acc_empty[buf]));
+                    mbar_arrive(smem_u32(B.bacc_empty));
+                }
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_u32(&B.acc_empty[buf]));
-                mbar_arrive(smem_u32(B.bacc_empty));
-            }
-        }
-        if (row_ok) {
+            if (!ok) break;
+            if (sb_begin == 0 && sb_end == nsb) {
+                if (row_ok) {
 #pragma unroll
-            for (int j = 0; j < kEpiCols; j += 2) {
-                float lo, hi;
-                upk2(run[j / 2], lo, hi);
-                const int64_t m = m0 + part * kEpiCols + j;
-                if (m < a.M) a.Y[m * a.N + n] = lo;
-                if (m + 1 < a.M) a.Y[(m + 1) * a.N + n] = hi;
+                    for (int j = 0; j < kEpiCols; j += 2) {
+                        float lo, hi;
+                        upk2(run[j / 2], lo, hi);
+                        const int64_t m = mb0 + j;
+                        if (m < a.M) a.Y[m * a.N + n] = lo;
+                        if (m + 1 < a.M) a.Y[(m + 1) * a.N + n] = hi;
+                    }
+                }
+            } else {
+                float *dst = a.part + ((int64_t)blockIdx.x * 2 + (tile == first_tile ? 0 : 1)) * (kBM * kBN) +
+                             (int64_t)(cpart * kEpiCols) * kBM + nl;
+#pragma unroll
+                for (int j = 0; j < kEpiCols; j += 2) {
+                    float lo, hi;
+                    upk2(run[j / 2], lo, hi);
+                    dst[j * kBM] = lo;
+                    dst[(j + 1) * kBM] = hi;
+                }
             }
         }
     }
@@ -558,6 +598,75 @@ __global__ void __launch_bounds__(256) import_q8K_prefill_kernel(const uint8_t *
     }
 }
 
+// At most this many CTAs share a tile: the pieces of a tile belong to
+// distinct CTAs, and the launcher caps the grid at this many.
+constexpr int kMaxPieces = 1024;
+
+// Stream-K fixup: a tile whose super-blocks were split over several CTAs
+// gets the sum of their partial tiles, in CTA order (deterministic). Tiles
+// held whole by one CTA were written by it and are skipped.
+__global__ void __launch_bounds__(512) stream_k_fixup_kernel(const float *__restrict__ part,
+                                                             float *__restrict__ Y, int64_t N,
+                                                             int64_t M, int64_t mblocks,
+                                                             int64_t nsb, int64_t units, int64_t G) {
+    pdl_wait();  // the GEMM's partial tiles
+    const int64_t tile = blockIdx.x;
+    auto cta_of = [&](int64_t u) {  // the CTA whose range [c U / G, (c+1) U / G) holds u
+        int64_t c = u * G / units;
+        while (c > 0 && c * units / G > u) --c;
+        while ((c + 1) * units / G <= u) ++c;
+        return c;
+    };
+    const int64_t ca = cta_of(tile * nsb), cb = cta_of(tile * nsb + nsb - 1);
+    if (ca == cb) return;
+    // the pieces' partial tiles, in CTA order (slot 0 when the tile is the CTA's first)
+    __shared__ int64_t off[kMaxPieces];
+    const int np = (int)(cb - ca + 1);
+    for (int k = threadIdx.x; k < np; k += blockDim.x) {
+        const int64_t c = ca + k;
+        off[k] = (c * 2 + ((c * units / G) / nsb == tile ? 0 : 1)) * (kBM * kBN);
+    }
+    __syncthreads();
+    const int64_t n0 = (tile / mblocks) * kBM, m0 = (tile % mblocks) * kBN;
+    // 4 rows per thread and 4 independent columns in flight: the pieces are
+    // read with 16-byte loads, the output rows of a column are contiguous
+    constexpr int kQuads = kBM * kBN / 4;
+    for (int e0 = threadIdx.x; e0 < kQuads; e0 += 4 * blockDim.x) {
+        float4 v[4];
+        int rr[4], cc[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int e = e0 + h * blockDim.x;
+            rr[h] = (e % (kBM / 4)) * 4;
+            cc[h] = e / (kBM / 4);
+            v[h] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+        for (int k = 0; k < np; ++k) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                if (e0 + h * (int)blockDim.x < kQuads) {
+                    const float4 p = *reinterpret_cast<const float4 *>(part + off[k] + (int64_t)cc[h] * kBM + rr[h]);
+                    v[h].x += p.x;
+                    v[h].y += p.y;
+                    v[h].z += p.z;
+                    v[h].w += p.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int64_t m = m0 + cc[h], n = n0 + rr[h];
+            if (e0 + h * (int)blockDim.x < kQuads && m < M) {
+                float *y = Y + m * N + n;
+                if (n < N) y[0] = v[h].x;
+                if (n + 1 < N) y[1] = v[h].y;
+                if (n + 2 < N) y[2] = v[h].z;
+                if (n + 3 < N) y[3] = v[h].w;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 namespace tc {
@@ -633,10 +742,13 @@ size_t prefill_bytes(int64_t M, int64_t K, PrefillWs *p, uint8_t *base) {
     off = align_up(off + (size_t)M * nsb * 16 * 2, 256);
     const size_t o_d = off;
     off = align_up(off + (size_t)((M + 3) & ~(int64_t)3) * nsb * 4, 256);
+    const size_t o_p = off;  // stream-K partial tiles: two per CTA, one CTA per SM
+    off = align_up(off + (size_t)2 * sm_count() * kBM * kBN * 4, 256);
     if (p) {
         p->y16 = reinterpret_cast<__half *>(base + o_y);
         p->bs16 = reinterpret_cast<__half *>(base + o_bs);
         p->daT = reinterpret_cast<float *>(base + o_d);
+        p->part = reinterpret_cast<float *>(base + o_p);
     }
     return off;
 }
@@ -690,8 +802,15 @@ cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, 
         return cudaErrorInvalidValue;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_q4_K_kernel), kSmemBytes);
     if (e != cudaSuccess) return e;
+    // stream-K over (tile, super-block) units: one persistent CTA per SM
+    const int64_t nblocks = (N + kBM - 1) / kBM;
+    a.mblocks = (M + kBN - 1) / kBN;
+    a.units = nblocks * a.mblocks * nsb;
+    a.part = p.part;
+    int64_t G = a.units < sm_count() ? a.units : sm_count();
+    if (G > kMaxPieces) G = kMaxPieces;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + kBN - 1) / kBN));
+    cfg.gridDim = dim3((unsigned)G);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
@@ -702,6 +821,15 @@ cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, 
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gemm_q4_K_kernel, a, tmap_w, tmap_y, tmap_bs);
     count_launch();
+    if (e != cudaSuccess) return e;
+    {  // tiles split over several CTAs get the sum of their pieces (the others return at once)
+        cfg.gridDim = dim3((unsigned)(nblocks * a.mblocks));
+        cfg.blockDim = dim3(512);
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel, (const float *)p.part, Y, N, M, a.mblocks,
+                               nsb, a.units, G);
+        count_launch();
+    }
     return e;
 }
 

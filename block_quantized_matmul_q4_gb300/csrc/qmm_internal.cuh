@@ -78,6 +78,7 @@ struct PrefillWs {
     __half *y16;
     __half *bs16;
     float *daT;
+    float *part;  // stream-K partial tiles of the GEMM: [CTA][2][kBN cols][kBM rows]
 };
 // Tokens per call above which Q4_K mul_mat runs the tensor-core GEMM.
 constexpr int64_t kGemmMinM = 17;

@@ -36,7 +36,9 @@ def packed(q, orc, w, N, K, wt=None):
 
 
 @pytest.mark.parametrize("N,K,M", [(128, 256, 17), (200, 512, 300), (384, 1024, 256),
-                                   (136, 2304, 129), (64, 256, 64)])
+                                   (136, 2304, 129), (64, 256, 64),
+                                   (128, 16384, 40),   # one tile over 64 CTAs (stream-K pieces)
+                                   (1000, 4096, 300)])  # CTA ranges straddling tiles
 def test_prefill_gemm_small(q, orc, N, K, M):
     w = wl.weights(30, N, K, 0.02, row_offset_std=0.005).numpy()
     x = wl.activations(30, M, K).numpy()
