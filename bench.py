@@ -363,6 +363,7 @@ def prefill_rate(q, dev, stream, L, M, seed, reps=6, graph_steps=4, wt=None):
     gemm = lambda i: q.qmm_mul_mat_prepared(wt, Wp, N, K, ws, ws_bytes, M, Y, stream)
     for i in range(2):
         step(i)
+        gemm(i)
     g1 = capture(step, graph_steps, stream)
     g2 = capture(gemm, graph_steps, stream)
     with torch.cuda.stream(stream):

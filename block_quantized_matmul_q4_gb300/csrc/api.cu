@@ -109,8 +109,12 @@ qmm_status check_weight_args(qmm_type wt, int64_t N, int64_t K) {
 }
 
 // Default mem pool: keep freed workspace instead of returning it to the
-// driver at every synchronization.
-void prepare_pool() {
+// driver at every synchronization. Skipped while `s` is being captured (a
+// pool attribute change would end the capture; allocations in a graph come
+// from the graph's own memory anyway) and done by the next call outside one.
+void prepare_pool(cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
     const int d = current_device();
     std::lock_guard<std::mutex> lk(g_mutex);
     if (g_pool_ready[d]) return;
@@ -128,10 +132,21 @@ void prepare_pool() {
 // activation images, otherwise the scalar GEMV and the planar layout.
 bool use_gemm(qmm_type wt, int64_t M) { return M >= kGemmMinM; }
 
+// Prefill workspaces: the quantized activations (read-only in the GEMM),
+// then the stream-K partial area that calls owning the workspace use.
+size_t prefill_act_bytes(qmm_type wt, int64_t M, int64_t K) {
+    return align_up(wt == QMM_TYPE_Q4_K ? prefill_bytes(M, K, nullptr, nullptr) : q4_0_prefill_bytes(M, K),
+                    256);
+}
+
 size_t ws_bytes_for(qmm_type wt, int64_t M, int64_t K) {
     if (!use_gemm(wt, M) && gemv_use_mma(wt, M, K)) return gemv_mma_image_bytes(M, K);
     if (!use_gemm(wt, M)) return planar_bytes(M, K, elems(wt), nullptr, nullptr);
-    return wt == QMM_TYPE_Q4_K ? prefill_bytes(M, K, nullptr, nullptr) : q4_0_prefill_bytes(M, K);
+    return prefill_act_bytes(wt, M, K) + stream_k_part_bytes();
+}
+
+float *ws_part(qmm_type wt, int64_t M, int64_t K, void *ws) {
+    return reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + prefill_act_bytes(wt, M, K));
 }
 
 qmm_status carve(qmm_type wt, int64_t M, int64_t K, const void *ws, size_t ws_bytes, Planar *p) {
@@ -166,17 +181,19 @@ qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K,
                        "activation quantizer launch");
 }
 
+// part: for the prefill GEMMs, stream_k_part_bytes() of device memory that
+// no other work uses until this call's work on `s` is done.
 qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, const void *ws,
-                         size_t ws_bytes, int64_t M, float *Y, cudaStream_t s) {
+                         size_t ws_bytes, int64_t M, float *Y, float *part, cudaStream_t s) {
     if (use_gemm(wt, M)) {
-        const size_t need = ws_bytes_for(wt, M, K);
+        const size_t need = prefill_act_bytes(wt, M, K);
         if (ws_bytes < need)
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
         if (wt == QMM_TYPE_Q4_0)
-            return cuda_status(launch_gemm_q4_0(Wp, N, K, ws, M, Y, s), "prefill GEMM launch");
+            return cuda_status(launch_gemm_q4_0(Wp, N, K, ws, part, M, Y, s), "prefill GEMM launch");
         PrefillWs pw;
         prefill_bytes(M, K, &pw, (uint8_t *)ws);
-        return cuda_status(launch_gemm_q4_K(Wp, N, K, pw, M, Y, s), "prefill GEMM launch");
+        return cuda_status(launch_gemm_q4_K(Wp, N, K, pw, part, M, Y, s), "prefill GEMM launch");
     }
     if (gemv_use_mma(wt, M, K)) {
         const size_t need = ws_bytes_for(wt, M, K);
@@ -203,7 +220,26 @@ qmm_status mul_mat_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, const
     }
     qmm_status st = quantize_acts_impl(wt, X, M, K, ws, ws_bytes, s);
     if (st != QMM_OK) return st;
-    return prepared_impl(wt, Wp, N, K, ws, ws_bytes, M, Y, s);
+    return prepared_impl(wt, Wp, N, K, ws, ws_bytes, M, Y, use_gemm(wt, M) ? ws_part(wt, M, K, ws) : nullptr,
+                         s);
+}
+
+// A stream-K partial area of its own for a call whose workspace is shared
+// read-only (or that has none): allocated on the stream, freed after `run`.
+template <class F>
+qmm_status with_own_part(cudaStream_t s, F run) {
+    prepare_pool(s);
+    void *mem = nullptr;
+    const size_t need = stream_k_part_bytes();
+    cudaError_t e = cudaMallocAsync(&mem, need, s);
+    if (e != cudaSuccess || !mem) {
+        cudaGetLastError();
+        return set_error(QMM_ERR_NOMEM, "cudaMallocAsync(%zu): %s", need, cudaGetErrorString(e));
+    }
+    qmm_status st = run(static_cast<float *>(mem));
+    cudaError_t ef = cudaFreeAsync(mem, s);
+    if (st == QMM_OK && ef != cudaSuccess) return cuda_status(ef, "cudaFreeAsync");
+    return st;
 }
 
 qmm_status check_mul_mat_args(qmm_type wt, const void *Wp, int64_t N, int64_t K, const float *X,
@@ -357,7 +393,15 @@ qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, in
     QMM_CHECK_ARG(W_packed && workspace && Y, "null pointer argument");
     QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(workspace, 16) && aligned(Y, 4),
                   "W_packed and workspace must be 16-byte aligned, Y 4-byte aligned");
-    return prepared_impl(wt, W_packed, N, K, workspace, ws_bytes, M, Y, (cudaStream_t)stream);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!use_gemm(wt, M) || !stream_k_splits(N, M))  // nothing to allocate
+        return prepared_impl(wt, W_packed, N, K, workspace, ws_bytes, M, Y, nullptr, s);
+    if (ws_bytes < prefill_act_bytes(wt, M, K))  // before allocating anything
+        return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes,
+                         prefill_act_bytes(wt, M, K));
+    return with_own_part(s, [&](float *part) {
+        return prepared_impl(wt, W_packed, N, K, workspace, ws_bytes, M, Y, part, s);
+    });
 }
 
 qmm_status qmm_mul_mat(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X,
@@ -368,7 +412,7 @@ qmm_status qmm_mul_mat(qmm_type wt, const void *W_packed, int64_t N, int64_t K, 
     cudaStream_t s = (cudaStream_t)stream;
     if (gemv_can_fuse(wt, M, K))  // one kernel, no workspace to allocate
         return mul_mat_impl(wt, W_packed, N, K, X, M, Y, nullptr, 0, s);
-    prepare_pool();
+    prepare_pool(s);
     const size_t need = qmm_workspace_bytes(wt, M, K);
     void *ws = nullptr;
     cudaError_t e = cudaMallocAsync(&ws, need, s);
@@ -393,7 +437,7 @@ qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t 
     QMM_CHECK_ARG(aligned(Xq, wt == QMM_TYPE_Q4_K ? 4 : 2),
                   "Xq must be aligned like its blocks (Q8_K: 4 bytes, Q8_0: 2 bytes)");
     cudaStream_t s = (cudaStream_t)stream;
-    prepare_pool();
+    prepare_pool(s);
     const size_t need = qmm_workspace_bytes(wt, M, K);
     void *ws = nullptr;
     cudaError_t e = cudaMallocAsync(&ws, need, s);
@@ -418,7 +462,8 @@ qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t 
         e = launch_import_q8_planar(act_of(wt), Xq, p, M, K, s);
     }
     st = cuda_status(e, "activation import launch");
-    if (st == QMM_OK) st = prepared_impl(wt, W_packed, N, K, ws, need, M, Y, s);
+    if (st == QMM_OK)
+        st = prepared_impl(wt, W_packed, N, K, ws, need, M, Y, use_gemm(wt, M) ? ws_part(wt, M, K, ws) : nullptr, s);
     cudaError_t ef = cudaFreeAsync(ws, s);
     if (st == QMM_OK && ef != cudaSuccess) return cuda_status(ef, "cudaFreeAsync");
     return st;
@@ -445,7 +490,7 @@ qmm_status qmm_mul_mat_multi(qmm_type wt, int n, const void *const *W_packed, co
         Planar none{nullptr, nullptr, nullptr};
         return cuda_status(launch_gemv(wt, ms, K, none, X, M, /*pdl=*/true, s), "mul_mat kernel launch");
     }
-    prepare_pool();
+    prepare_pool(s);
     const size_t need = qmm_workspace_bytes(wt, M, K);
     void *ws = nullptr;
     cudaError_t e = cudaMallocAsync(&ws, need, s);
@@ -453,12 +498,13 @@ qmm_status qmm_mul_mat_multi(qmm_type wt, int n, const void *const *W_packed, co
         cudaGetLastError();
         return set_error(QMM_ERR_NOMEM, "cudaMallocAsync(%zu): %s", need, cudaGetErrorString(e));
     }
-    // one quantization of X serves every matrix
+    // one quantization of X serves every matrix; the GEMMs take the
+    // stream-K partial area in turn, in stream order
     qmm_status st = quantize_acts_impl(wt, X, M, K, ws, need, s);
     if (st == QMM_OK) {
         if (use_gemm(wt, M)) {
             for (int i = 0; i < ms.n && st == QMM_OK; ++i)
-                st = prepared_impl(wt, ms.W[i], ms.N[i], K, ws, need, M, ms.Y[i], s);
+                st = prepared_impl(wt, ms.W[i], ms.N[i], K, ws, need, M, ms.Y[i], ws_part(wt, M, K, ws), s);
         } else if (gemv_use_mma(wt, M, K)) {
             st = cuda_status(launch_gemv_mma_q4_K(ms, K, nullptr, ws, M, /*pdl=*/true, s),
                              "mul_mat kernel launch");
@@ -556,10 +602,18 @@ qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t
     const __half *S = reinterpret_cast<const __half *>(scales);
     const __half *Ah = reinterpret_cast<const __half *>(A);
     __half *Ch = reinterpret_cast<__half *>(C);
-    // up to 16 tokens: the decode kernel (HBM-bound); more: the tensor-core GEMM
-    cudaError_t e = M <= 16 ? launch_w4a16_decode(W_packed, S, zeros, G, Ah, Ch, M, N, K, s)
-                            : launch_w4a16_gemm(W_packed, S, zeros, G, Ah, Ch, M, N, K, s);
-    return cuda_status(e, "W4A16 kernel launch");
+    // up to 16 tokens: the decode kernel (HBM-bound); more: the tensor-core
+    // GEMM, whose split tiles go through a stream-ordered partial area
+    if (M <= 16)
+        return cuda_status(launch_w4a16_decode(W_packed, S, zeros, G, Ah, Ch, M, N, K, s),
+                           "W4A16 kernel launch");
+    if (!stream_k_splits(N, M))  // one CTA per tile: no partial area
+        return cuda_status(launch_w4a16_gemm(W_packed, S, zeros, G, Ah, Ch, M, N, K, nullptr, s),
+                           "W4A16 kernel launch");
+    return with_own_part(s, [&](float *part) {
+        return cuda_status(launch_w4a16_gemm(W_packed, S, zeros, G, Ah, Ch, M, N, K, part, s),
+                           "W4A16 kernel launch");
+    });
 }
 
 }  // extern "C"

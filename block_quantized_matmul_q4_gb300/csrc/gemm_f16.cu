@@ -12,7 +12,12 @@
 // rounded once (relative error <= 2^-11); the MMA accumulates in fp32 over
 // all of K.
 //
-// CTA = 128 weight rows (MMA M) x 128 tokens (MMA N), 15 warps:
+// Tile = 128 weight rows (MMA M) x 128 tokens (MMA N). Up to one tile per SM
+// the grid has one CTA per tile; with more, one CTA per SM walks a
+// contiguous range of (tile, 256-element K round) units (stream-K): pieces
+// of tiles that span two or more CTAs go to partial slots and a fixup
+// kernel adds them (streamk.cu). Two TMEM accumulators let the MMAs of the
+// next piece start while the epilogue drains the last one. 15 warps:
 //   warp 0      producer: per 256 elements of K one weight stage (TMA copies
 //               of the packed tiles of the CTA's 128 rows) and one activation
 //               stage of four 2-D TMA tiles (128B swizzle, 64 KB);
@@ -23,8 +28,8 @@
 //   warps 3..10 converters, two sets of four: one weight row per thread
 //               (its TMEM lane), fp16 weights built in registers and stored
 //               into a TMEM operand ring with tcgen05.st;
-//   warps 11..14 epilogue: one tcgen05.ld pass over the accumulator at the
-//               end.
+//   warps 11..14 epilogue: one tcgen05.ld pass over the accumulator per
+//               piece.
 // All mbarrier waits are bounded; on a timeout the CTA drains its copies and
 // MMAs, frees its TMEM and returns with the device error word set.
 #include "tc.cuh"
@@ -47,11 +52,11 @@ constexpr int kThreads = (3 + kConvWarps + kEpiWarps) * 32;
 constexpr int kOffAct = 0;
 constexpr int kOffW = kOffAct + kActStages * kActBytes;
 constexpr int kOffBar = kOffW + kWStages * kWBytesMax;
-constexpr int kNumBars = 2 * (kWStages + kActStages + kGroups) + 2;
+constexpr int kNumBars = 2 * (kWStages + kActStages + kGroups) + 5;  // + acc_full[2], acc_empty[2], done
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColAcc = 0, kColARing = kBN;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColAcc = 0, kColARing = 2 * kBN;  // two accumulators (stream-K pieces), A ring
 constexpr uint32_t kARingCols = kBK / 2;
 static_assert(kColARing + kChunks * kARingCols <= kTmemCols, "TMEM budget");
 
@@ -75,6 +80,10 @@ struct Args {
     int64_t M, N, K;
     int ng, spg;  // W4A16: groups per row, 128-element steps per group
     unsigned *err;
+    // stream-K: tile t = (row block t / mblocks, token block t % mblocks);
+    // unit u = t * nsb + round; CTA c takes units [c U / G, (c+1) U / G)
+    int64_t mblocks, units;
+    float *part;  // split tiles: [CTA][slot 0: first tile, 1: last tile][128 cols][128 rows]
 };
 
 __device__ __forceinline__ uint32_t lop_or(uint32_t x, uint32_t mask) {
@@ -97,6 +106,7 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ void handoff_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
 // fp16 scale * (q - zero) for the 8 codes of one word, as four pairs of
@@ -116,6 +126,22 @@ __device__ __forceinline__ void scaled_word(uint32_t w, uint32_t zz, uint32_t zh
     f12 = hmul2_u(hfma2_u(lop_or(v, 0x00F000F0u), kSixteenth, zh), ss);
 }
 
+// Columns m0 .. m0+15 of output row n (C is [M][N]: fp16 for W4A16, fp32 for
+// Q4_0); columns past M are skipped.
+template <int F>
+__device__ __forceinline__ void store_cols(const Args &a, int64_t m0, int64_t n, const float v[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int64_t m = m0 + j;
+        if (m < a.M) {
+            if (F == kW4A16)
+                static_cast<__half *>(a.C)[m * a.N + n] = __float2half_rn(v[j]);
+            else
+                static_cast<float *>(a.C)[m * a.N + n] = v[j];
+        }
+    }
+}
+
 template <int F>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_kernel(const Args a, const __grid_constant__ CUtensorMap tmap_w,
@@ -127,14 +153,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (sbase - raw_base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n0 = (int64_t)blockIdx.x * kBM, m0 = (int64_t)blockIdx.y * kBN;
     const int64_t nsb = (a.K + kSB - 1) / kSB;
+    // this CTA's units (stream-K): a contiguous range of (tile, round)
+    const int64_t u0 = (int64_t)blockIdx.x * a.units / gridDim.x;
+    const int64_t u1 = ((int64_t)blockIdx.x + 1) * a.units / gridDim.x;
 
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *w_full = bar, *w_empty = w_full + kWStages;
     uint64_t *act_full = w_empty + kWStages, *act_empty = act_full + kActStages;
     uint64_t *a_full = act_empty + kActStages, *a_empty = a_full + kGroups;
-    uint64_t *acc_full = a_empty + kGroups, *done = acc_full + 1;
+    uint64_t *acc_full = a_empty + kGroups, *acc_empty = acc_full + 2, *done = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
 
     if (threadIdx.x == 0) {
@@ -150,10 +178,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&a_full[i]), kConvWarps);  // both sets, one chunk each
             mbar_init(smem_u32(&a_empty[i]), 1);
         }
-        mbar_init(smem_u32(acc_full), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&acc_full[i]), 1);
+            mbar_init(smem_u32(&acc_empty[i]), kEpiWarps);
+        }
         mbar_init(smem_u32(done), 1);
         fence_barrier_init();
     }
+    __syncwarp();  // warps meet converged at every CTA barrier below
     if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc::fence_before_sync();
     __syncthreads();
@@ -170,9 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             pdl_wait();  // the activations may come from the preceding kernel
             int64_t issued_w = 0, issued_a = 0;
             bool ok = true;
-            for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-                const int ws = (int)(sb % kWStages);
-                ok = mbar_wait(smem_u32(&w_empty[ws]), (uint32_t)(((sb / kWStages) & 1) ^ 1), a.err);
+            for (int64_t i = 0; i < u1 - u0 && ok; ++i) {
+                const int64_t tile = (u0 + i) / nsb, sb = u0 + i - tile * nsb;
+                const int64_t n0 = (tile / a.mblocks) * kBM, m0 = (tile % a.mblocks) * kBN;
+                const int ws = (int)(i % kWStages);
+                ok = mbar_wait(smem_u32(&w_empty[ws]), (uint32_t)(((i / kWStages) & 1) ^ 1), a.err);
                 if (!ok) break;
                 // rows past the last tile and K past the end read as zeros
                 const uint32_t wbar = smem_u32(&w_full[ws]);
@@ -191,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (int32_t)(n0 / kQ4Tile), wbar, pol);
                 }
                 ++issued_w;
-                const int st = (int)(sb % kActStages);
-                ok = mbar_wait(smem_u32(&act_empty[st]), (uint32_t)(((sb / kActStages) & 1) ^ 1), a.err);
+                const int st = (int)(i % kActStages);
+                ok = mbar_wait(smem_u32(&act_empty[st]), (uint32_t)(((i / kActStages) & 1) ^ 1), a.err);
                 if (!ok) break;
                 const uint32_t abar = smem_u32(&act_full[st]);
                 mbar_arrive_expect_tx(abar, kActBytes);
@@ -206,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t k = issued_a > kActStages ? issued_a - kActStages : 0; k < issued_a; ++k)
                 mbar_wait(smem_u32(&act_full[k % kActStages]), (uint32_t)((k / kActStages) & 1), a.err);
         }
+        __syncwarp();  // lanes 1..31 wait here for the producer lane
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Meets the waiter at the named barrier the same number of times
@@ -213,49 +248,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the error word reports it.
         constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
         const uint64_t bdesc0 = tc::smem_desc(smem_u32(smem + kOffAct), 1024, 2);
-        for (int64_t sb = 0; sb < nsb; ++sb) {
-            const int st = (int)(sb % kActStages);
+        int64_t i = 0;  // units done: the pipeline position
+        int pc = 0;     // pieces done: accumulator pc & 1
+        for (int64_t u = u0; u < u1; ++pc) {
+            const int64_t tile = u / nsb;
+            const int sb_begin = (int)(u - tile * nsb);
+            const int sb_end = (int)(nsb < sb_begin + (u1 - u) ? nsb : sb_begin + (u1 - u));
+            u += sb_end - sb_begin;
+            const uint32_t dacc = tmem + kColAcc + (uint32_t)((pc & 1) * kBN);
+            for (int sb = sb_begin; sb < sb_end; ++sb, ++i) {
+                const int st = (int)(i % kActStages);
 #pragma unroll 1
-            for (int g = 0; g < kGroups; ++g) {
-                handoff_sync();
-                if (lane == 0) {
-                    tc::fence_after_sync();
+                for (int g = 0; g < kGroups; ++g) {
+                    handoff_sync();
+                    if (lane == 0) {
+                        tc::fence_after_sync();
 #pragma unroll
-                    for (int h = 0; h < kChunks / kGroups; ++h) {
-                        const int c = g * (kChunks / kGroups) + h;
-                        const uint32_t acol = tmem + kColARing + (uint32_t)c * kARingCols;
-                        // K step of 16 fp16 = 32 bytes = 2 in the descriptor's address field
-                        const uint64_t bdesc = bdesc0 + (uint64_t)((st * kActBytes + c * kChunkBytes) >> 4);
+                        for (int h = 0; h < kChunks / kGroups; ++h) {
+                            const int c = g * (kChunks / kGroups) + h;
+                            const uint32_t acol = tmem + kColARing + (uint32_t)c * kARingCols;
+                            // K step of 16 fp16 = 32 bytes = 2 in the descriptor's address field
+                            const uint64_t bdesc = bdesc0 + (uint64_t)((st * kActBytes + c * kChunkBytes) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk)
-                            tc::mma_f16_ta(tmem + kColAcc, acol + 8 * kk, bdesc + 2 * kk, idesc,
-                                           (sb | c | kk) != 0);
+                            for (int kk = 0; kk < kBK / 16; ++kk)
+                                tc::mma_f16_ta(dacc, acol + 8 * kk, bdesc + 2 * kk, idesc,
+                                               ((sb - sb_begin) | c | kk) != 0);
+                        }
+                        tc::commit(smem_u32(&a_empty[g]));
+                        if (g == kGroups - 1) tc::commit(smem_u32(&act_empty[st]));
                     }
-                    tc::commit(smem_u32(&a_empty[g]));
-                    if (g == kGroups - 1) tc::commit(smem_u32(&act_empty[st]));
+                    __syncwarp();
                 }
-                __syncwarp();
             }
+            if (lane == 0) tc::commit(smem_u32(&acc_full[pc & 1]));
+            __syncwarp();
         }
         if (lane == 0) {
-            tc::commit(smem_u32(acc_full));
             tc::commit(smem_u32(done));
             mbar_wait(smem_u32(done), 0, a.err);  // no MMA may run when TMEM is freed
         }
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------ MMA waiter
+        // Before a piece's first MMA: its accumulator has been read by the
+        // epilogue (two pieces back); before each group: its operands.
         bool ok = true;
-        for (int64_t sb = 0; sb < nsb; ++sb) {
-            const int st = (int)(sb % kActStages);
-            const uint32_t par = (uint32_t)(sb & 1);
+        int64_t i = 0;
+        int pc = 0;
+        for (int64_t u = u0; u < u1; ++pc) {
+            const int64_t tile = u / nsb;
+            const int sb_begin = (int)(u - tile * nsb);
+            const int sb_end = (int)(nsb < sb_begin + (u1 - u) ? nsb : sb_begin + (u1 - u));
+            u += sb_end - sb_begin;
             if (lane == 0 && ok)
-                ok = mbar_wait(smem_u32(&act_full[st]), (uint32_t)((sb / kActStages) & 1), a.err);
+                ok = mbar_wait(smem_u32(&acc_empty[pc & 1]), (uint32_t)(((pc >> 1) & 1) ^ 1), a.err);
+            for (int sb = sb_begin; sb < sb_end; ++sb, ++i) {
+                const int st = (int)(i % kActStages);
+                const uint32_t par = (uint32_t)(i & 1);
+                if (lane == 0 && ok)
+                    ok = mbar_wait(smem_u32(&act_full[st]), (uint32_t)((i / kActStages) & 1), a.err);
 #pragma unroll 1
-            for (int g = 0; g < kGroups; ++g) {
-                if (lane == 0 && ok) ok = mbar_wait(smem_u32(&a_full[g]), par, a.err);
-                __syncwarp();
-                handoff_sync();
+                for (int g = 0; g < kGroups; ++g) {
+                    if (lane == 0 && ok) ok = mbar_wait(smem_u32(&a_full[g]), par, a.err);
+                    __syncwarp();
+                    handoff_sync();
+                }
             }
         }
     } else if (warp < 3 + kConvWarps) {
@@ -263,108 +320,142 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ct = 32 * (warp & 3) + lane;  // weight row within the CTA = TMEM lane
         const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
         const int set = (warp - 3) >> 2;  // chunk `set` of each group
-        const int64_t n = n0 + ct;
-        const int64_t nc = n < a.N ? n : a.N - 1;  // rows past N: zero codes, clamped scales
         const int64_t nsteps = a.K / kW4StepK;
         bool ok = true;
-        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-            const int ws = (int)(sb % kWStages);
-            const uint32_t par = (uint32_t)(sb & 1);
-            ok = mbar_wait(smem_u32(&w_full[ws]), (uint32_t)((sb / kWStages) & 1), a.err);
-            if (!ok) break;
-            const uint8_t *wst = smem + kOffW + ws * kWBytesMax;
-#pragma unroll 1
-            for (int g = 0; g < kGroups && ok; ++g) {
-                const int c = g * (kChunks / kGroups) + set;  // chunk of this round
-                uint32_t lo[16], hi[16];  // TMEM columns 0..15 and 16..31 of the chunk
-                if (F == kW4A16) {
-                    // chunk c = half (c & 1) of step 2 sb + (c >> 1); columns hold
-                    // elements (2i, 2i + 1): the packed words put even elements
-                    // in the low half, odd in the high half
-                    const int sl = c >> 1;
-                    int64_t step = 2 * sb + sl;
-                    if (step >= nsteps) step = nsteps - 1;  // past K the activations are zero
-                    const int grp = a.spg == 1 ? (int)step : (int)step / a.spg;
-                    const uint32_t zv = a.Z[nc * a.ng + grp];
-                    const uint32_t sv = (uint32_t)__half_as_ushort(a.S[nc * a.ng + grp]);
-                    const uint32_t zz = 0x64006400u + zv * 0x00010001u;  // fp16 1024 + z twice
-                    const uint32_t zh = 0xD400D400u + zv * 0x00100010u;  // fp16 -(64 + z) twice
-                    const uint32_t ss = sv | (sv << 16);
-                    const uint8_t *src = wst + ((ct >> 4) * (kSB / kW4StepK) + sl) * 1024 + (ct & 15) * 64 +
-                                         (c & 1) * 32;
-                    const uint4 w0 = *reinterpret_cast<const uint4 *>(src);
-                    const uint4 w1 = *reinterpret_cast<const uint4 *>(src + 16);
-                    const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        // W4A16 word: (k0,k1) at 0|16, (k2,k3) at 4|20, (k4,k5) at 8|24, (k6,k7) at 12|28
-                        scaled_word(wv[i], zz, zh, ss, lo[4 * i], lo[4 * i + 2], lo[4 * i + 1], lo[4 * i + 3]);
-                        scaled_word(wv[i + 4], zz, zh, ss, hi[4 * i], hi[4 * i + 2], hi[4 * i + 1],
-                                    hi[4 * i + 3]);
-                    }
-                } else {
-                    // chunk c = blocks 2c, 2c + 1 of the round. Byte l of a block
-                    // holds elements l (low nibble) and l + 16 (high); word i
-                    // gives columns 4i .. 4i+3 = (e4i, e4i+2), (e4i+1, e4i+3),
-                    // (e16+4i, e18+4i), (e17+4i, e19+4i) -- the order the Q4_0
-                    // prefill quantizer writes the activations of a block in.
-                    constexpr uint32_t zz = 0x64086408u;  // fp16 1024 + 8 twice
-                    constexpr uint32_t zh = 0xD480D480u;  // fp16 -(64 + 8) twice
-                    const int tt = ct >> 3, r = ct & 7;
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        const int blk = 2 * c + b;
-                        const uint4 q = *reinterpret_cast<const uint4 *>(wst + tt * 1024 + blk * 128 + r * 16);
-                        const uint32_t dv = *reinterpret_cast<const uint16_t *>(
-                            wst + kQ4NibBytes + tt * (kQ4Blocks * 16) + blk * 16 + r * 2);
-                        const uint32_t ss = dv | (dv << 16);
-                        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-                        uint32_t *out = b == 0 ? lo : hi;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            scaled_word(wv[i], zz, zh, ss, out[4 * i], out[4 * i + 1], out[4 * i + 2],
-                                        out[4 * i + 3]);
-                    }
-                }
-                ok = mbar_wait(smem_u32(&a_empty[g]), par ^ 1, a.err);
+        int64_t pos = 0;  // units done: the pipeline position
+        for (int64_t u = u0; u < u1 && ok;) {
+            const int64_t tile = u / nsb;
+            const int sb_begin = (int)(u - tile * nsb);
+            const int sb_end = (int)(nsb < sb_begin + (u1 - u) ? nsb : sb_begin + (u1 - u));
+            u += sb_end - sb_begin;
+            const int64_t n = (tile / a.mblocks) * kBM + ct;
+            const int64_t nc = n < a.N ? n : a.N - 1;  // rows past N: zero codes, clamped scales
+            for (int64_t sb = sb_begin; sb < sb_end && ok; ++sb, ++pos) {
+                const int ws = (int)(pos % kWStages);
+                const uint32_t par = (uint32_t)(pos & 1);
+                ok = mbar_wait_warp(smem_u32(&w_full[ws]), (uint32_t)((pos / kWStages) & 1), a.err);
                 if (!ok) break;
-                tc::fence_after_sync();
-                const uint32_t acol = tmem + lane_addr + kColARing + (uint32_t)c * kARingCols;
-                tc::tmem_st16(acol, lo);
-                tc::tmem_st16(acol + 16, hi);
-                tc::tmem_st_wait();
-                tc::fence_before_sync();
+                const uint8_t *wst = smem + kOffW + ws * kWBytesMax;
+#pragma unroll 1
+                for (int g = 0; g < kGroups && ok; ++g) {
+                    const int c = g * (kChunks / kGroups) + set;  // chunk of this round
+                    uint32_t lo[16], hi[16];  // TMEM columns 0..15 and 16..31 of the chunk
+                    if (F == kW4A16) {
+                        // chunk c = half (c & 1) of step 2 sb + (c >> 1); columns hold
+                        // elements (2i, 2i + 1): the packed words put even elements
+                        // in the low half, odd in the high half
+                        const int sl = c >> 1;
+                        int64_t step = 2 * sb + sl;
+                        if (step >= nsteps) step = nsteps - 1;  // past K the activations are zero
+                        const int grp = a.spg == 1 ? (int)step : (int)step / a.spg;
+                        const uint32_t zv = a.Z[nc * a.ng + grp];
+                        const uint32_t sv = (uint32_t)__half_as_ushort(a.S[nc * a.ng + grp]);
+                        const uint32_t zz = 0x64006400u + zv * 0x00010001u;  // fp16 1024 + z twice
+                        const uint32_t zh = 0xD400D400u + zv * 0x00100010u;  // fp16 -(64 + z) twice
+                        const uint32_t ss = sv | (sv << 16);
+                        const uint8_t *src = wst + ((ct >> 4) * (kSB / kW4StepK) + sl) * 1024 + (ct & 15) * 64 +
+                                             (c & 1) * 32;
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(src);
+                        const uint4 w1 = *reinterpret_cast<const uint4 *>(src + 16);
+                        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            // W4A16 word: (k0,k1) at 0|16, (k2,k3) at 4|20, (k4,k5) at 8|24, (k6,k7) at 12|28
+                            scaled_word(wv[i], zz, zh, ss, lo[4 * i], lo[4 * i + 2], lo[4 * i + 1], lo[4 * i + 3]);
+                            scaled_word(wv[i + 4], zz, zh, ss, hi[4 * i], hi[4 * i + 2], hi[4 * i + 1],
+                                        hi[4 * i + 3]);
+                        }
+                    } else {
+                        // chunk c = blocks 2c, 2c + 1 of the round. Byte l of a block
+                        // holds elements l (low nibble) and l + 16 (high); word i
+                        // gives columns 4i .. 4i+3 = (e4i, e4i+2), (e4i+1, e4i+3),
+                        // (e16+4i, e18+4i), (e17+4i, e19+4i) -- the order the Q4_0
+                        // prefill quantizer writes the activations of a block in.
+                        constexpr uint32_t zz = 0x64086408u;  // fp16 1024 + 8 twice
+                        constexpr uint32_t zh = 0xD480D480u;  // fp16 -(64 + 8) twice
+                        const int tt = ct >> 3, r = ct & 7;
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const int blk = 2 * c + b;
+                            const uint4 q = *reinterpret_cast<const uint4 *>(wst + tt * 1024 + blk * 128 + r * 16);
+                            const uint32_t dv = *reinterpret_cast<const uint16_t *>(
+                                wst + kQ4NibBytes + tt * (kQ4Blocks * 16) + blk * 16 + r * 2);
+                            const uint32_t ss = dv | (dv << 16);
+                            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+                            uint32_t *out = b == 0 ? lo : hi;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                scaled_word(wv[i], zz, zh, ss, out[4 * i], out[4 * i + 1], out[4 * i + 2],
+                                            out[4 * i + 3]);
+                        }
+                    }
+                    ok = mbar_wait_warp(smem_u32(&a_empty[g]), par ^ 1, a.err);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint32_t acol = tmem + lane_addr + kColARing + (uint32_t)c * kARingCols;
+                    tc::tmem_st16(acol, lo);
+                    tc::tmem_st16(acol + 16, hi);
+                    tc::tmem_st_wait();
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&a_full[g]));
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&a_full[g]));
+                if (lane == 0 && ok) mbar_arrive(smem_u32(&w_empty[ws]));
             }
-            __syncwarp();
-            if (lane == 0 && ok) mbar_arrive(smem_u32(&w_empty[ws]));
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // Per piece: a whole tile goes to C, a part of one to this CTA's
+        // partial slot for the fixup kernel; then the accumulator is free for
+        // the piece after next. After a timed-out wait the loop still walks
+        // the pieces, without waits or stores.
         const int quarter = warp & 3;  // TMEM lanes 32 * (warp % 4) ..
-        const int64_t n = n0 + quarter * 32 + lane;
+        const int nl = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        const bool ok = mbar_wait(smem_u32(acc_full), 0, a.err);
-        tc::fence_after_sync();
-        if (ok) {
+        bool ok = true;
+        int pc = 0;
+        for (int64_t u = u0; u < u1; ++pc) {
+            const int64_t tile = u / nsb;
+            const int sb_begin = (int)(u - tile * nsb);
+            const int sb_end = (int)(nsb < sb_begin + (u1 - u) ? nsb : sb_begin + (u1 - u));
+            u += sb_end - sb_begin;
+            const int64_t n = (tile / a.mblocks) * kBM + nl, m0 = (tile % a.mblocks) * kBN;
+            const uint32_t acc = tmem + lane_addr + kColAcc + (uint32_t)((pc & 1) * kBN);
+            if (ok) ok = mbar_wait_warp(smem_u32(&acc_full[pc & 1]), (uint32_t)((pc >> 1) & 1), a.err);
+            if (ok) tc::fence_after_sync();
+            // TMEM loads are warp-collective: every lane takes them (ok is
+            // warp-uniform); only the stores depend on the row
+            const bool row_ok = n < a.N;
+            if (sb_begin == 0 && sb_end == nsb) {
+                if (ok) {
 #pragma unroll 1
-            for (int c16 = 0; c16 < kBN / 16; ++c16) {
-                float v[16];
-                tc::tmem_ld16(tmem + lane_addr + kColAcc + (uint32_t)(c16 * 16), v);
-                tc::tmem_ld_wait();
-                if (n < a.N) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int64_t m = m0 + c16 * 16 + i;
-                        if (m < a.M) {
-                            if (F == kW4A16)
-                                static_cast<__half *>(a.C)[m * a.N + n] = __float2half_rn(v[i]);
-                            else
-                                static_cast<float *>(a.C)[m * a.N + n] = v[i];
-                        }
+                    for (int c16 = 0; c16 < kBN / 16; ++c16) {
+                        float v[16];
+                        tc::tmem_ld16(acc + (uint32_t)(c16 * 16), v);
+                        tc::tmem_ld_wait();
+                        if (row_ok) store_cols<F>(a, m0 + c16 * 16, n, v);
                     }
                 }
+            } else {
+                // a part of a split tile: to this CTA's slot (column-major:
+                // column j of this row at j * kBM) for the fixup kernel
+                float *mine = a.part + sk_slot(blockIdx.x, tile, a.units, gridDim.x, nsb) + nl;
+                if (ok) {
+#pragma unroll 1
+                    for (int c16 = 0; c16 < kBN / 16; ++c16) {
+                        float v[16];
+                        tc::tmem_ld16(acc + (uint32_t)(c16 * 16), v);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) mine[(c16 * 16 + j) * kBM] = v[j];
+                    }
+                }
+            }
+            if (ok) {
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[pc & 1]));
             }
         }
     }
@@ -378,24 +469,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ Q4_0 prefill quantizer
-// X fp32 -> Q8_0 codes y and fp16 scale d per 32 (the same arithmetic as the
-// Q8_0 quantizer, shared q8_0_warp), then a = fp16(f32(d) * y) written with
-// the elements of each block permuted to the order the Q4_0 converter puts
-// the weights in: element e (e' = e mod 16, i = e' / 4, r = e' mod 4) goes to
-// position 8 i + 4 (e >= 16) + 2 (r mod 2) + r / 2.
+// X fp32 -> Q8_0 codes y and fp16 scale d per 32 (the arithmetic of the Q8_0
+// quantizer: amax / 127, codes rounded half away from zero), then
+// a = fp16(f32(d) * y) written with the elements of each block permuted to
+// the order the Q4_0 converter puts the weights in: element e (e' = e mod 16,
+// i = e' / 4, r = e' mod 4) goes to position 8 i + 4 (e >= 16) + 2 (r mod 2)
+// + r / 2. A warp takes 8 blocks per step, 4 lanes per block and 8
+// consecutive elements per lane (two 16-byte loads); the 4 elements
+// 4i .. 4i+3 of a lane land at positions 8 i + 4 (e >= 16) + (0, 2, 1, 3),
+// so each lane writes two 8-byte groups.
 __global__ void __launch_bounds__(256) quantize_q4_0_prefill_kernel(const float *__restrict__ X,
                                                                     __half *__restrict__ out,
                                                                     int64_t nblocks) {
     pdl_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int e = lane, ep = e & 15, i = ep >> 2, r = ep & 3;
-    const int pos = 8 * i + ((e >> 4) << 2) + 2 * (r & 1) + (r >> 1);
+    const int lane = threadIdx.x & 31, j = lane & 3;  // j: elements 8j .. 8j+7 of the block
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += nwarps) {
-        int q, sum;
-        __half dh;
-        q8_0_warp(X[b * QK4_0 + lane], q, dh, sum);
-        out[b * QK4_0 + pos] = __float2half_rn(__half2float(dh) * (float)q);
+    // positions of this lane's two groups: elements 8j + 4g .. 8j + 4g + 3
+    const int e0 = 8 * j, base0 = 8 * ((e0 & 15) >> 2) + ((e0 >> 4) << 2);
+    const int e1 = e0 + 4, base1 = 8 * ((e1 & 15) >> 2) + ((e1 >> 4) << 2);
+    for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w * 8 < nblocks; w += nwarps) {
+        const int64_t b = w * 8 + (lane >> 2);
+        const bool live = b < nblocks;
+        float4 v0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), v1 = v0;
+        if (live) {
+            const float4 *src = reinterpret_cast<const float4 *>(X + b * QK4_0 + e0);
+            v0 = src[0];
+            v1 = src[1];
+        }
+        float a = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                        fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+        // max over the block's 4 lanes (non-negative floats order like their bits)
+        uint32_t ab = __float_as_uint(a);
+        ab = max(ab, __shfl_xor_sync(0xffffffffu, ab, 1));
+        ab = max(ab, __shfl_xor_sync(0xffffffffu, ab, 2));
+        const float d = __fdiv_rn(__uint_as_float(ab), 127.0f);
+        const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+        const float df = __half2float(__float2half_rn(d));
+        auto val = [&](float x) { return __float2half_rn(df * (float)q8_code(x, id)); };
+        if (live) {
+            __half *dst = out + b * QK4_0;
+            const __half2 p0 = __halves2half2(val(v0.x), val(v0.z)), p1 = __halves2half2(val(v0.y), val(v0.w));
+            const __half2 p2 = __halves2half2(val(v1.x), val(v1.z)), p3 = __halves2half2(val(v1.y), val(v1.w));
+            *reinterpret_cast<uint2 *>(dst + base0) = make_uint2(h2_bits(p0), h2_bits(p1));
+            *reinterpret_cast<uint2 *>(dst + base1) = make_uint2(h2_bits(p2), h2_bits(p3));
+        }
     }
 }
 
@@ -417,6 +534,34 @@ __global__ void __launch_bounds__(256) import_q8_0_prefill_kernel(const uint8_t 
     }
 }
 
+// The GEMM (programmatic dependent launch): one CTA per tile, or with more
+// tiles than SMs a persistent stream-K grid and the fixup of its split tiles.
+template <int F>
+cudaError_t launch_stream_k(Args a, const CUtensorMap &tmap_w, const CUtensorMap &tmap_d,
+                            const CUtensorMap &tmap_a, cudaStream_t s) {
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_f16_kernel<F>), kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t nsb = (a.K + kSB - 1) / kSB;
+    a.mblocks = (a.M + kBN - 1) / kBN;
+    const int64_t tiles = ((a.N + kBM - 1) / kBM) * a.mblocks;
+    a.units = tiles * nsb;
+    const int64_t G = stream_k_grid(tiles);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_f16_kernel<F>, a, tmap_w, tmap_d, tmap_a);
+    count_launch();
+    if (e != cudaSuccess || G == tiles) return e;
+    return launch_stream_k_fixup(a.part, a.C, F == kW4A16, a.N, a.M, a.mblocks, nsb, a.units, G, s);
+}
+
 }  // namespace
 
 cudaError_t launch_import_q4_0_prefill(const void *Xq, void *ws, int64_t M, int64_t K,
@@ -434,7 +579,7 @@ cudaError_t launch_import_q4_0_prefill(const void *Xq, void *ws, int64_t M, int6
 
 cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, int64_t G,
                               const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
-                              cudaStream_t s) {
+                              float *part, cudaStream_t s) {
     Args a;
     a.S = S;
     a.Z = Z;
@@ -445,6 +590,7 @@ cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, 
     a.ng = (int)(K / G);
     a.spg = (int)(G / kW4StepK);
     a.err = device_error_word();
+    a.part = part;
     const int64_t nsteps = K / kW4StepK, ntiles16 = (N + kW4Tile - 1) / kW4Tile;
     CUtensorMap tmap_w, tmap_a;
     // packed weights as [16-row tile][step][1 KB], in 4-byte units
@@ -455,20 +601,16 @@ cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, 
         !tc::make_tmap_2d(&tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M, (uint64_t)K,
                           kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_f16_kernel<kW4A16>), kSmemBytes);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + kBN - 1) / kBN));
-    gemm_f16_kernel<kW4A16><<<grid, kThreads, kSmemBytes, s>>>(a, tmap_w, tmap_w, tmap_a);
-    count_launch();
-    return cudaGetLastError();
+    return launch_stream_k<kW4A16>(a, tmap_w, tmap_w, tmap_a, s);
 }
 
+// fp16 activations [M][K]
 size_t q4_0_prefill_bytes(int64_t M, int64_t K) { return align_up((size_t)M * K * 2, 256); }
 
 cudaError_t launch_quantize_q4_0_prefill(const float *X, void *ws, int64_t M, int64_t K,
                                          cudaStream_t s) {
     const int64_t nblocks = M * (K / QK4_0);
-    int64_t grid = (nblocks + 7) / 8;
+    int64_t grid = (nblocks + 63) / 64;  // 8 warps x 8 blocks
     const int64_t cap = (int64_t)sm_count() * 16;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
@@ -477,8 +619,8 @@ cudaError_t launch_quantize_q4_0_prefill(const float *X, void *ws, int64_t M, in
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *ws, int64_t M,
-                             float *Y, cudaStream_t s) {
+cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *ws, float *part,
+                             int64_t M, float *Y, cudaStream_t s) {
     Args a;
     a.S = nullptr;
     a.Z = nullptr;
@@ -489,6 +631,7 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
     a.ng = 0;
     a.spg = 1;
     a.err = device_error_word();
+    a.part = part;
     const int64_t nb = K / QK4_0, ntiles = tiles_of(N);
     const uint64_t tile_bytes = (uint64_t)nb * kQ4Tile * B_Q4_0;
     CUtensorMap tmap_w, tmap_d, tmap_a;
@@ -506,21 +649,7 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
         !tc::make_tmap_2d(&tmap_a, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M, (uint64_t)K,
                           kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_f16_kernel<kQ40>), kSmemBytes);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + kBN - 1) / kBN));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemm_f16_kernel<kQ40>, a, tmap_w, tmap_d, tmap_a);
-    count_launch();
-    return e;
+    return launch_stream_k<kQ40>(a, tmap_w, tmap_d, tmap_a, s);
 }
 
 }  // namespace qmm

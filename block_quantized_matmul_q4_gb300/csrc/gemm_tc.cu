@@ -63,7 +63,7 @@ constexpr int kOffMin = kOffAct + kActStages * kActBytes;
 constexpr int kOffRaw = kOffMin + kMinStages * kMinBytes;
 constexpr int kOffDa = kOffRaw + kRawStages * kRawBytes;  // per epilogue warp: its 32 d_a
 constexpr int kOffBar = kOffDa + kEpiWarps * kEpiCols * 4;
-constexpr int kNumBars = 2 * (kRawStages + kActStages + kGroups + 2) + 2;
+constexpr int kNumBars = 2 * (kRawStages + kActStages + kGroups + 2) + 2;  // + bacc_empty, done
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot + alignment
 static_assert(kActBytes % 1024 == 0 && kOffMin % 1024 == 0, "128B-swizzle tiles need 1 KB alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -83,7 +83,7 @@ struct GemmArgs {
     // stream-K: tile t = (row block t / mblocks, token block t % mblocks);
     // unit u = t * nsb + super-block; CTA c takes units [c U / G, (c+1) U / G)
     int64_t mblocks, units;
-    float *part;  // partial tiles: [CTA][slot 0: first tile, 1: last tile][col][row]
+    float *part;  // split tiles: [CTA][slot 0: first tile, 1: last tile][128 cols][128 rows]
 };
 
 struct Bars {
@@ -178,7 +178,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t u0 = (int64_t)blockIdx.x * a.units / gridDim.x;
     const int64_t u1 = ((int64_t)blockIdx.x + 1) * a.units / gridDim.x;
     const int64_t nunits = u1 - u0;
-    const int64_t first_tile = u0 / nsb;
 
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
     Bars B;
@@ -215,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(B.done), 1);
         fence_barrier_init();
     }
+    __syncwarp();  // warps meet converged at every CTA barrier below
     if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc::fence_before_sync();
     __syncthreads();
@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t k = issued_act > kActStages ? issued_act - kActStages : 0; k < issued_act; ++k)
                 mbar_wait(smem_u32(&B.act_full[k % kActStages]), (uint32_t)((k / kActStages) & 1), a.err);
         }
+        __syncwarp();  // lanes 1..31 wait here for the producer lane
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Never touches an mbarrier on the way: a shared-memory access by the
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int sb = sb_begin; sb < sb_end && ok; ++sb, ++i) {
             const int rs = (int)(i % kRawStages);
             const uint32_t par = (uint32_t)(i & 1);
-            ok = mbar_wait(smem_u32(&B.raw_full[rs]), (uint32_t)((i / kRawStages) & 1), a.err);
+            ok = mbar_wait_warp(smem_u32(&B.raw_full[rs]), (uint32_t)((i / kRawStages) & 1), a.err);
             if (!ok) break;
             const uint8_t *blk = smem + kOffRaw + rs * kRawBytes + (ti * kTileRows + r) * B_Q4_K;
             const uint4 hdr = valid ? *reinterpret_cast<const uint4 *>(blk) : make_uint4(0, 0, 0, 0);
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // previous super-block are done -- and with them every MMA
                 // issued before, including the bsum MMA two super-blocks back
                 // that read the mins slot reused below
-                ok = mbar_wait(smem_u32(&B.a_empty[g]), par ^ 1, a.err);
+                ok = mbar_wait_warp(smem_u32(&B.a_empty[g]), par ^ 1, a.err);
                 if (!ok) break;
                 if (g == 0 && set == 0) {
                     // mins operand, K = 16: column t holds m_{t/2}; 32B-swizzled rows
@@ -427,9 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();  // d_a comes from the preceding quantizer kernel
         bool ok = true;
         int i = 0;  // units done: the pipeline position
-        // the CTA's units as pieces of tiles: a whole tile goes to Y, a part of
-        // one to this CTA's slot (0: its first tile, 1: its last) for the fixup
-        for (int64_t u = u0; u < u1 && ok;) {
+        // the CTA's units as pieces of tiles: a whole tile goes to Y, a part
+        // of one to this CTA's partial slot for the fixup kernel
+        for (int64_t u = u0; u < u1;) {
             const int64_t tile = u / nsb;
             const int sb_begin = (int)(u - tile * nsb);
             const int sb_end = (int)(nsb < sb_begin + (u1 - u) ? nsb : sb_begin + (u1 - u));
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 da_stage[lane] = da;
                 __syncwarp();
-                ok = mbar_wait(smem_u32(&B.acc_full[buf]), (uint32_t)((i >> 1) & 1), a.err);
+                ok = mbar_wait_warp(smem_u32(&B.acc_full[buf]), (uint32_t)((i >> 1) & 1), a.err);
                 if (!ok) break;
                 tc::fence_after_sync();
                 const float dw = __half2float(__ushort_as_half((unsigned short)(hdr & 0xFFFFu)));
@@ -490,9 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(smem_u32(B.bacc_empty));
                 }
             }
-            if (!ok) break;
             if (sb_begin == 0 && sb_end == nsb) {
-                if (row_ok) {
+                if (row_ok && ok) {
 #pragma unroll
                     for (int j = 0; j < kEpiCols; j += 2) {
                         float lo, hi;
@@ -502,15 +502,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (m + 1 < a.M) a.Y[(m + 1) * a.N + n] = hi;
                     }
                 }
-            } else {
-                float *dst = a.part + ((int64_t)blockIdx.x * 2 + (tile == first_tile ? 0 : 1)) * (kBM * kBN) +
-                             (int64_t)(cpart * kEpiCols) * kBM + nl;
+            } else if (ok) {
+                // a part of a split tile: to this CTA's slot (column-major:
+                // column j of this row at j * kBM) for the fixup kernel
+                float *mine = a.part + sk_slot(blockIdx.x, tile, a.units, gridDim.x, nsb) +
+                              (int64_t)(cpart * kEpiCols) * kBM + nl;
 #pragma unroll
                 for (int j = 0; j < kEpiCols; j += 2) {
                     float lo, hi;
                     upk2(run[j / 2], lo, hi);
-                    dst[j * kBM] = lo;
-                    dst[(j + 1) * kBM] = hi;
+                    mine[j * kBM] = lo;
+                    mine[(j + 1) * kBM] = hi;
                 }
             }
         }
@@ -598,75 +600,6 @@ __global__ void __launch_bounds__(256) import_q8K_prefill_kernel(const uint8_t *
     }
 }
 
-// At most this many CTAs share a tile: the pieces of a tile belong to
-// distinct CTAs, and the launcher caps the grid at this many.
-constexpr int kMaxPieces = 1024;
-
-// Stream-K fixup: a tile whose super-blocks were split over several CTAs
-// gets the sum of their partial tiles, in CTA order (deterministic). Tiles
-// held whole by one CTA were written by it and are skipped.
-__global__ void __launch_bounds__(512) stream_k_fixup_kernel(const float *__restrict__ part,
-                                                             float *__restrict__ Y, int64_t N,
-                                                             int64_t M, int64_t mblocks,
-                                                             int64_t nsb, int64_t units, int64_t G) {
-    pdl_wait();  // the GEMM's partial tiles
-    const int64_t tile = blockIdx.x;
-    auto cta_of = [&](int64_t u) {  // the CTA whose range [c U / G, (c+1) U / G) holds u
-        int64_t c = u * G / units;
-        while (c > 0 && c * units / G > u) --c;
-        while ((c + 1) * units / G <= u) ++c;
-        return c;
-    };
-    const int64_t ca = cta_of(tile * nsb), cb = cta_of(tile * nsb + nsb - 1);
-    if (ca == cb) return;
-    // the pieces' partial tiles, in CTA order (slot 0 when the tile is the CTA's first)
-    __shared__ int64_t off[kMaxPieces];
-    const int np = (int)(cb - ca + 1);
-    for (int k = threadIdx.x; k < np; k += blockDim.x) {
-        const int64_t c = ca + k;
-        off[k] = (c * 2 + ((c * units / G) / nsb == tile ? 0 : 1)) * (kBM * kBN);
-    }
-    __syncthreads();
-    const int64_t n0 = (tile / mblocks) * kBM, m0 = (tile % mblocks) * kBN;
-    // 4 rows per thread and 4 independent columns in flight: the pieces are
-    // read with 16-byte loads, the output rows of a column are contiguous
-    constexpr int kQuads = kBM * kBN / 4;
-    for (int e0 = threadIdx.x; e0 < kQuads; e0 += 4 * blockDim.x) {
-        float4 v[4];
-        int rr[4], cc[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const int e = e0 + h * blockDim.x;
-            rr[h] = (e % (kBM / 4)) * 4;
-            cc[h] = e / (kBM / 4);
-            v[h] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        }
-        for (int k = 0; k < np; ++k) {
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                if (e0 + h * (int)blockDim.x < kQuads) {
-                    const float4 p = *reinterpret_cast<const float4 *>(part + off[k] + (int64_t)cc[h] * kBM + rr[h]);
-                    v[h].x += p.x;
-                    v[h].y += p.y;
-                    v[h].z += p.z;
-                    v[h].w += p.w;
-                }
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const int64_t m = m0 + cc[h], n = n0 + rr[h];
-            if (e0 + h * (int)blockDim.x < kQuads && m < M) {
-                float *y = Y + m * N + n;
-                if (n < N) y[0] = v[h].x;
-                if (n + 1 < N) y[1] = v[h].y;
-                if (n + 2 < N) y[2] = v[h].z;
-                if (n + 3 < N) y[3] = v[h].w;
-            }
-        }
-    }
-}
-
 }  // namespace
 
 namespace tc {
@@ -742,13 +675,10 @@ size_t prefill_bytes(int64_t M, int64_t K, PrefillWs *p, uint8_t *base) {
     off = align_up(off + (size_t)M * nsb * 16 * 2, 256);
     const size_t o_d = off;
     off = align_up(off + (size_t)((M + 3) & ~(int64_t)3) * nsb * 4, 256);
-    const size_t o_p = off;  // stream-K partial tiles: two per CTA, one CTA per SM
-    off = align_up(off + (size_t)2 * sm_count() * kBM * kBN * 4, 256);
     if (p) {
         p->y16 = reinterpret_cast<__half *>(base + o_y);
         p->bs16 = reinterpret_cast<__half *>(base + o_bs);
         p->daT = reinterpret_cast<float *>(base + o_d);
-        p->part = reinterpret_cast<float *>(base + o_p);
     }
     return off;
 }
@@ -778,7 +708,7 @@ cudaError_t launch_import_prefill(const void *Xq, PrefillWs p, int64_t M, int64_
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, int64_t M,
+cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, float *part, int64_t M,
                              float *Y, cudaStream_t s) {
     const int64_t nsb = K / QK_K;
     GemmArgs a;
@@ -802,13 +732,14 @@ cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, 
         return cudaErrorInvalidValue;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_q4_K_kernel), kSmemBytes);
     if (e != cudaSuccess) return e;
-    // stream-K over (tile, super-block) units: one persistent CTA per SM
+    // one CTA per tile, or with more tiles than SMs stream-K over (tile,
+    // super-block) units with one persistent CTA per SM
     const int64_t nblocks = (N + kBM - 1) / kBM;
     a.mblocks = (M + kBN - 1) / kBN;
-    a.units = nblocks * a.mblocks * nsb;
-    a.part = p.part;
-    int64_t G = a.units < sm_count() ? a.units : sm_count();
-    if (G > kMaxPieces) G = kMaxPieces;
+    const int64_t tiles = nblocks * a.mblocks;
+    a.units = tiles * nsb;
+    a.part = part;
+    const int64_t G = stream_k_grid(tiles);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
     cfg.blockDim = dim3(kThreads);
@@ -821,16 +752,8 @@ cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, 
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gemm_q4_K_kernel, a, tmap_w, tmap_y, tmap_bs);
     count_launch();
-    if (e != cudaSuccess) return e;
-    {  // tiles split over several CTAs get the sum of their pieces (the others return at once)
-        cfg.gridDim = dim3((unsigned)(nblocks * a.mblocks));
-        cfg.blockDim = dim3(512);
-        cfg.dynamicSmemBytes = 0;
-        e = cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel, (const float *)p.part, Y, N, M, a.mblocks,
-                               nsb, a.units, G);
-        count_launch();
-    }
-    return e;
+    if (e != cudaSuccess || G == tiles) return e;
+    return launch_stream_k_fixup(part, Y, false, N, M, a.mblocks, nsb, a.units, G, s);
 }
 
 }  // namespace qmm

@@ -78,7 +78,6 @@ struct PrefillWs {
     __half *y16;
     __half *bs16;
     float *daT;
-    float *part;  // stream-K partial tiles of the GEMM: [CTA][2][kBN cols][kBM rows]
 };
 // Tokens per call above which Q4_K mul_mat runs the tensor-core GEMM.
 constexpr int64_t kGemmMinM = 17;
@@ -239,6 +238,11 @@ __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uns
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err) {
     return mbar_wait_for(bar, parity, err, kWaitTimeoutCycles);
 }
+// The same wait by every lane of a warp, with one answer for the whole warp:
+// warps that go on to warp-collective tcgen05 loads or stores must agree.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, unsigned *err) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
 
 // 1-D bulk async copy global -> shared, completing on an mbarrier.
 // dst, src 16-byte aligned, bytes a multiple of 16.
@@ -292,6 +296,27 @@ __device__ __forceinline__ float round_half_away(float v) {
 }
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return min(max(v, lo), hi); }
+
+// ------------------------------------------------------------------ stream-K
+// The tensor-core GEMMs run a grid of G CTAs over units u = tile * nsb +
+// k-round (U units), CTA c taking [c U / G, (c+1) U / G). With at most as
+// many tiles as SMs, G = tiles: one whole tile per CTA. With more, G = the
+// SM count and a tile may span several CTAs: each CTA that holds only part of
+// it writes that piece to its partial slot (slot 0 when the tile is the
+// CTA's first, 1 when its last), and the fixup kernel (streamk.cu) adds the
+// pieces in CTA order and writes the tile.
+constexpr int kSkTile = 128;  // tile rows = tile columns
+
+// The CTA whose range holds unit u.
+__host__ __device__ __forceinline__ int64_t sk_cta_of(int64_t u, int64_t U, int64_t G) {
+    return ((u + 1) * G - 1) / U;
+}
+// Float offset of CTA c's slot for `tile` in the partial area
+// [G][2][128 cols][128 rows] (a column's 128 rows contiguous).
+__host__ __device__ __forceinline__ int64_t sk_slot(int64_t c, int64_t tile, int64_t U, int64_t G,
+                                                    int64_t nsb) {
+    return (c * 2 + ((c * U / G) / nsb == tile ? 0 : 1)) * (int64_t)(kSkTile * kSkTile);
+}
 
 // ------------------------------------------------------------------ activation quantization
 // Shared by the stand-alone quantizer kernels and the quantizer fused into the
@@ -424,7 +449,8 @@ cudaError_t launch_gemv_mma_q4_K(MatSet ms, int64_t K, const float *X, const voi
 size_t prefill_bytes(int64_t M, int64_t K, PrefillWs *p, uint8_t *base);
 cudaError_t launch_quantize_prefill(const float *X, PrefillWs p, int64_t M, int64_t K,
                                     cudaStream_t s);
-cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, int64_t M,
+// part: stream_k_part_bytes() of device memory for split tiles
+cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, float *part, int64_t M,
                              float *Y, cudaStream_t s);
 // W4A16: nibble interleave of the packed layout (or its inverse), the decode
 // kernel (M <= 16) and the tensor-core GEMM (M > 16).
@@ -435,15 +461,27 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
                                 cudaStream_t s);
 cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, int64_t G,
                               const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
-                              cudaStream_t s);
+                              float *part, cudaStream_t s);
 // Q4_0 prefill (M > 16): fp16(d_a y) activations (permuted per block) in a
 // workspace of q4_0_prefill_bytes, then the fp16-operand tensor-core GEMM.
 size_t q4_0_prefill_bytes(int64_t M, int64_t K);
 cudaError_t launch_quantize_q4_0_prefill(const float *X, void *ws, int64_t M, int64_t K,
                                          cudaStream_t s);
-cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *ws, int64_t M,
-                             float *Y, cudaStream_t s);
+cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *ws, float *part,
+                             int64_t M, float *Y, cudaStream_t s);
 cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
                                     const void *Xq, int64_t M, int32_t *out, cudaStream_t s);
 cudaError_t launch_debug_wait_timeout(int64_t limit_cycles, cudaStream_t s);
+// Stream-K GEMMs (streamk.cu): CTAs for `tiles` tiles (tiles itself up to
+// the SM count, else the SM count); bytes of the partial area; the fixup
+// that adds the split tiles' pieces into C (fp32, or fp16 when half_out),
+// launched only when G < tiles.
+int64_t stream_k_grid(int64_t tiles);
+size_t stream_k_part_bytes();
+// Whether an N x M output (128 x 128 tiles) runs split tiles, i.e. needs the
+// partial area.
+bool stream_k_splits(int64_t N, int64_t M);
+cudaError_t launch_stream_k_fixup(const float *part, void *C, bool half_out, int64_t N, int64_t M,
+                                  int64_t mblocks, int64_t nsb, int64_t units, int64_t G,
+                                  cudaStream_t s);
 }  // namespace qmm

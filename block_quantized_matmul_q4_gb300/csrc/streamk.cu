@@ -1,0 +1,124 @@
+// streamk.cu -- grid size, partial area and fixup of the stream-K GEMMs
+// (gemm_tc.cu, gemm_f16.cu). With more tiles than SMs, a persistent grid of
+// one CTA per SM takes the units u = tile * nsb + k-round in equal
+// contiguous ranges (CTA c: [c U / G, (c+1) U / G)); a CTA that holds all of
+// a tile's units writes it, otherwise its piece went to its partial slot
+// (slot 0 when the tile is the CTA's first, 1 when its last), fp32
+// [G][2][128 cols][128 rows]. Here every split tile gets the sum of its
+// pieces, added in CTA order (the same order every run), written to C.
+#include "qmm_internal.cuh"
+
+namespace qmm {
+namespace {
+
+constexpr int kTM = kSkTile, kTN = kSkTile;  // tile rows (weights) and columns (tokens)
+constexpr int64_t kMaxGrid = 1024;           // CTAs of a persistent grid at most
+constexpr int kFixupThreads = 512;
+
+int64_t max_grid() {
+    const int64_t n = sm_count();
+    return n < kMaxGrid ? n : kMaxGrid;
+}
+
+template <class T>
+__device__ __forceinline__ T out_cast(float v);
+template <>
+__device__ __forceinline__ float out_cast<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half out_cast<__half>(float v) { return __float2half_rn(v); }
+
+// One CTA per tile (whole tiles return at once). Each thread takes 4
+// consecutive rows of a column (one 16-byte load per piece) and keeps 4
+// columns in flight; a warp covers 128 rows of one column = 512 contiguous
+// bytes of every slot.
+template <class T>
+__global__ void __launch_bounds__(kFixupThreads) stream_k_fixup_kernel(const float *__restrict__ part,
+                                                                       T *__restrict__ C, int64_t N,
+                                                                       int64_t M, int64_t mblocks,
+                                                                       int64_t nsb, int64_t units,
+                                                                       int64_t G) {
+    pdl_wait();  // the GEMM's pieces
+    const int64_t tile = blockIdx.x;
+    const int64_t ca = sk_cta_of(tile * nsb, units, G), cb = sk_cta_of(tile * nsb + nsb - 1, units, G);
+    if (ca == cb) return;  // written whole by its CTA
+    const int64_t n0 = (tile / mblocks) * kTM, m0 = (tile % mblocks) * kTN;
+    constexpr int kQuads = kTM * kTN / 4;
+    for (int e0 = threadIdx.x; e0 < kQuads; e0 += 4 * kFixupThreads) {
+        float4 v[4];
+        int rr[4], cc[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int e = e0 + h * kFixupThreads;  // kQuads is a multiple of 4 * kFixupThreads
+            rr[h] = (e % (kTM / 4)) * 4;
+            cc[h] = e / (kTM / 4);
+        }
+        for (int64_t k = ca; k <= cb; ++k) {
+            const float *slot = part + sk_slot(k, tile, units, G, nsb);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float4 p = __ldcg(reinterpret_cast<const float4 *>(slot + cc[h] * kTM + rr[h]));
+                if (k == ca) {
+                    v[h] = p;
+                } else {
+                    v[h].x += p.x;
+                    v[h].y += p.y;
+                    v[h].z += p.z;
+                    v[h].w += p.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int64_t m = m0 + cc[h], n = n0 + rr[h];
+            if (m < M) {
+                T *y = C + m * N + n;
+                if (n < N) y[0] = out_cast<T>(v[h].x);
+                if (n + 1 < N) y[1] = out_cast<T>(v[h].y);
+                if (n + 2 < N) y[2] = out_cast<T>(v[h].z);
+                if (n + 3 < N) y[3] = out_cast<T>(v[h].w);
+            }
+        }
+    }
+}
+static_assert((kTM * kTN / 4) % (4 * kFixupThreads) == 0, "fixup tiling");
+
+}  // namespace
+
+int64_t stream_k_grid(int64_t tiles) {
+    if (tiles <= max_grid()) return tiles < 1 ? 1 : tiles;
+    return max_grid();
+}
+
+bool stream_k_splits(int64_t N, int64_t M) {
+    const int64_t tiles = ((N + kTM - 1) / kTM) * ((M + kTN - 1) / kTN);
+    return stream_k_grid(tiles) < tiles;
+}
+
+// Two 128 x 128 fp32 slots per CTA of the largest grid.
+size_t stream_k_part_bytes() { return align_up((size_t)2 * max_grid() * kTM * kTN * 4, 256); }
+
+cudaError_t launch_stream_k_fixup(const float *part, void *C, bool half_out, int64_t N, int64_t M,
+                                  int64_t mblocks, int64_t nsb, int64_t units, int64_t G,
+                                  cudaStream_t s) {
+    const int64_t nblocks = (N + kTM - 1) / kTM;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(nblocks * mblocks));
+    cfg.blockDim = dim3(kFixupThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (half_out)
+        e = cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<__half>, part, static_cast<__half *>(C), N, M,
+                               mblocks, nsb, units, G);
+    else
+        e = cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<float>, part, static_cast<float *>(C), N, M,
+                               mblocks, nsb, units, G);
+    count_launch();
+    return e;
+}
+
+}  // namespace qmm

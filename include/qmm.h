@@ -87,7 +87,11 @@ int qmm_block_elems(qmm_type t);
 size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K);
 
 /* Bytes of the workspace qmm_mul_mat_ws needs for M activation rows of
- * length K against weights of type wt (Q4_0 or Q4_K); 0 if invalid. */
+ * length K against weights of type wt (Q4_0 or Q4_K); 0 if invalid. Above 16
+ * tokens it ends with a partial area of about 20 MB: with more 128 x 128
+ * output tiles than SMs the tensor-core GEMM gives each SM an equal share of
+ * the (tile, K-step) work (stream-K), and the parts of tiles that several
+ * CTAs computed meet there before a second kernel adds them. */
 size_t qmm_workspace_bytes(qmm_type wt, int64_t M, int64_t K);
 
 /* ---------------------------------------------------------------- quantizers */
@@ -221,7 +225,11 @@ qmm_status qmm_mul_mat_ws(qmm_type wt, const void *W_packed, int64_t N, int64_t 
  * qmm_mul_mat_prepared: Y [M, N] from packed weights and a workspace filled
  *   by qmm_quantize_activations with the same wt, M and K (the contents are
  *   not checked). The workspace is read-only here, so several calls may
- *   share it. Errors as qmm_mul_mat_ws. */
+ *   share it; above 16 tokens, when the output has more 128 x 128 tiles
+ *   than SMs, the call therefore takes the GEMM's stream-K partial area
+ *   (about 20 MB) from the device's default memory pool,
+ *   stream-ordered, and frees it after the call on the same stream.
+ *   Errors as qmm_mul_mat_ws, plus QMM_ERR_NOMEM for that area. */
 qmm_status qmm_quantize_activations(qmm_type wt, const float *X, int64_t M, int64_t K,
                                     void *workspace, size_t ws_bytes, qmm_stream_t stream);
 qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
@@ -266,8 +274,13 @@ qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int64_t N, int6
  * Needs G % 128 == 0 and K % G == 0 (QMM_ERR_UNSUPPORTED for other G that
  * divide K) and K / G <= 256 (QMM_ERR_UNSUPPORTED above); W_packed,
  * scales, zeros and A 16-byte aligned, C 2-byte aligned.
+ * M > 16 with more 128 x 128 output tiles than SMs runs over a persistent
+ * grid (stream-K); tiles split across CTAs are added up, in a fixed order,
+ * through a partial area of about 20 MB that such a call allocates and
+ * frees stream-ordered on `stream` (the device's default memory pool).
  * Errors: QMM_ERR_ARG for sizes (M, N >= 0, K > 0, G > 0, K % G == 0) or
- * null/misaligned pointers. M == 0 or N == 0 is a no-op. */
+ * null/misaligned pointers; QMM_ERR_NOMEM if the partial area cannot be
+ * allocated. M == 0 or N == 0 is a no-op. */
 qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t *zeros, int64_t G,
                      const uint16_t *A, uint16_t *C, int64_t M, int64_t N, int64_t K,
                      qmm_stream_t stream);

@@ -146,10 +146,12 @@ def test_mul_mat_against_oracle(q, orc, wt, N, K, M):
 
 
 @pytest.mark.parametrize("wt,N,K,M", [(1, 40, 4096, 1), (1, 40, 4096, 4), (1, 24, 8192, 8),
-                                      (1, 16, 4096, 16), (0, 40, 1024, 1), (0, 24, 4096, 16)])
+                                      (1, 16, 4096, 16), (0, 40, 1024, 1), (0, 24, 4096, 16),
+                                      (1, 200, 4096, 40), (0, 136, 8192, 33)])  # prefill GEMMs
 def test_mul_mat_prepared(q, orc, wt, N, K, M):
-    """The two halves (quantize into a workspace, GEMV on it): activations
-    bulk-copied into shared memory when they fit, read in place otherwise."""
+    """The two halves (quantize into a workspace, GEMV or GEMM on it):
+    activations bulk-copied into shared memory when they fit, read in place
+    otherwise; the prefill GEMMs take stream-K scratch of their own."""
     w = wl.weights(13, N, K, 0.02, row_offset_std=0.005).numpy()
     x = wl.activations(13, M, K).numpy()
     Wc = orc.quantize(wt, w)
@@ -294,7 +296,8 @@ def test_70B_layer_sampled_rows(q, orc):
     (1, (200, 16, 8, 56), 2304, 5),    # tensor-core GEMV on the activation image
     (1, (64, 0, 24), 8192, 1),         # a matrix with no rows is skipped
     (0, (64, 40, 13), 1024, 1), (0, (64, 40), 4160, 3),
-    (1, (48, 32), 1024, 40), (0, (40, 24), 1024, 33)])  # prefill GEMM per matrix
+    (1, (48, 32), 1024, 40), (0, (40, 24), 1024, 33),  # prefill GEMM per matrix
+    (1, (1000, 300), 4096, 300), (0, (1000, 300), 2048, 200)])  # ... with split tiles
 def test_mul_mat_multi(q, orc, wt, Ns, K, M):
     """qmm_mul_mat_multi: Y_i = X W_i^T for all i from one quantization of X
     (and one decode launch); each Y_i equals a qmm_mul_mat call bit for bit
@@ -382,3 +385,33 @@ def test_bounded_wait_times_out_and_context_survives(q, orc):
     ref = orc.mul_mat(1, Wc, N, K, x)
     check_close(y, ref["y64"], ref["den"], "after a timed-out wait")
     q.qmm_check_device_error()
+
+
+@pytest.mark.parametrize("wt", [0, 1])
+def test_prepared_shared_workspace_two_streams(q, orc, wt):
+    """Prefill GEMMs on two streams at once from one read-only workspace:
+    each call's split tiles go through scratch of its own, so both results
+    equal the single-stream one bit for bit."""
+    N, K, M = 1000, 4096, 300
+    w = wl.weights(16, N, K, 0.02).numpy()
+    x = wl.activations(16, M, K).numpy()
+    Wc = orc.quantize(wt, w, nthreads=orc.default_threads())
+    Wp = q.empty_packed(wt, N, K)
+    q.qmm_repack_weights(wt, dev(Wc), Wp, N, K)
+    ws_bytes = q.qmm_workspace_bytes(wt, M, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    q.qmm_quantize_activations(wt, dev(x), M, K, ws, ws_bytes)
+    Y0 = torch.empty(M, N, device="cuda")
+    q.qmm_mul_mat_prepared(wt, Wp, N, K, ws, ws_bytes, M, Y0)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    Ys = [torch.full((M, N), float("nan"), device="cuda") for _ in range(6)]
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    for i, Y in enumerate(Ys):
+        st = s1 if i % 2 == 0 else s2
+        q.qmm_mul_mat_prepared(wt, Wp, N, K, ws, ws_bytes, M, Y, st.cuda_stream)
+    torch.cuda.synchronize()
+    q.qmm_check_device_error()
+    for Y in Ys:
+        assert torch.equal(Y.view(torch.int32), Y0.view(torch.int32))

@@ -81,7 +81,10 @@ def test_prefill_full_size_sampled(q, orc, shape, M):
 
 
 @pytest.mark.parametrize("N,K,M", [(128, 256, 17), (200, 512, 300), (136, 2304, 129), (64, 96, 40),
-                                   (300, 1056, 130)])
+                                   (300, 1056, 130),
+                                   (128, 16384, 40),   # one tile over 64 CTAs (stream-K pieces)
+                                   (1000, 4096, 300),  # CTA ranges straddling tiles
+                                   (72, 8224, 20)])    # ragged last round in every piece
 def test_prefill_q4_0_small(q, orc, N, K, M):
     """Q4_0 prefill GEMM: ragged N, M and K (K a multiple of 32 only)."""
     wt = q.QMM_TYPE_Q4_0
@@ -117,3 +120,54 @@ def test_prefill_q4_0_full_size_sampled(q, orc, shape):
     ref = orc.mul_mat(wt, Wc_rows, len(rows), L.K, x.cpu().numpy(), nthreads=orc.default_threads())
     check(Y[:, torch.as_tensor(rows, device="cuda")].cpu().numpy(), ref["y64"], ref["den"],
           f"Q4_0 {L.name} M={M}")
+
+
+@pytest.mark.parametrize("wt_name", ["Q4_K", "Q4_0"])
+def test_stream_k_deterministic(q, orc, wt_name):
+    """Split tiles are summed in a fixed order: two calls give the same bits."""
+    wt = getattr(q, "QMM_TYPE_" + wt_name)
+    N, K, M = 1000, 4096, 300
+    w = wl.weights(34, N, K, 0.02).numpy()
+    x = torch.from_numpy(wl.activations(34, M, K).numpy()).cuda()
+    _, Wp = packed(q, orc, w, N, K, wt)
+    Y1 = torch.empty(M, N, device="cuda")
+    Y2 = torch.full((M, N), float("nan"), device="cuda")
+    q.qmm_mul_mat(wt, Wp, N, K, x, M, Y1)
+    q.qmm_mul_mat(wt, Wp, N, K, x, M, Y2)
+    q.qmm_check_device_error()
+    assert torch.equal(Y1.view(torch.int32), Y2.view(torch.int32))
+
+
+def dequant_f64(orc, t, blocks, K):
+    """Rows of canonical blocks -> fp64 values, by the oracle's dequantizer."""
+    return torch.from_numpy(orc.dequantize(t, blocks, K, f64=True))
+
+
+@pytest.mark.parametrize("wt_name", ["Q4_K", "Q4_0"])
+@pytest.mark.parametrize("shape", wl.PREFILL_SHAPES, ids=lambda L: L.name)
+def test_prefill_full_output(q, orc, wt_name, shape):
+    """Every element of a full-size prefill output (M = 512: the stream-K
+    grid and its fixup on 11008 x 4096, one CTA per tile on 4096 x 11008)
+    against sum_k w_k a_k in fp64 over the oracle's dequantized weights and
+    activations (the factored sums the kernels use equal that product up to
+    fp64 rounding). Bar: 1e-3 sum_k |w_k a_k| per element."""
+    wt, L, M = getattr(q, "QMM_TYPE_" + wt_name), shape, 512
+    w = wl.weights(35, L.N, L.K, L.wstd, row_offset_std=L.row_offset_std if wt_name == "Q4_K" else 0.0,
+                   device="cuda")
+    x = wl.activations(35, M, L.K, device="cuda")
+    Wq = q.empty_blocks(wt, L.N, L.K)
+    q.qmm_quantize_weights(wt, w, Wq, L.N, L.K)
+    Wp = q.empty_packed(wt, L.N, L.K)
+    q.qmm_repack_weights(wt, Wq, Wp, L.N, L.K)
+    Y = torch.full((M, L.N), float("nan"), device="cuda")
+    q.qmm_mul_mat(wt, Wp, L.N, L.K, x, M, Y)
+    q.qmm_check_device_error()
+    act = orc.ACT_TYPE[wt]
+    Wd = dequant_f64(orc, wt, Wq.view(L.N, -1).cpu().numpy(), L.K).cuda()
+    Xd = dequant_f64(orc, act, orc.quantize(act, x.cpu().numpy(), nthreads=orc.default_threads()), L.K).cuda()
+    ref = Xd @ Wd.T
+    den = Xd.abs() @ Wd.abs().T
+    err = (Y.double() - ref).abs()
+    assert torch.isfinite(Y).all(), "non-finite output"
+    bad = err > TOL * den + 1e-30
+    assert not bad.any(), f"{int(bad.sum())} off, worst {float((err / den.clamp_min(1e-30)).max()):.3e}"

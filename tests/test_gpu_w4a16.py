@@ -79,7 +79,9 @@ def test_repack_round_trip(q):
                                      (33, 384, 128, 9), (16, 128, 128, 3), (40, 512, 128, 8),
                                      (24, 640, 128, 12), (40, 512, 128, 17), (64, 256, 128, 40),
                                      (100, 384, 128, 130), (200, 640, 128, 33), (48, 1024, 256, 200),
-                                     (136, 1152, 384, 257)])
+                                     (136, 1152, 384, 257),
+                                     (128, 8192, 128, 40),    # one tile over 32 CTAs (stream-K pieces)
+                                     (1000, 4096, 128, 300)])  # CTA ranges straddling tiles
 def test_w4a16_small(q, orc, N, K, G, M):
     qc, s16, z, A16 = wl.w4a16_inputs(40, N, K, G, M)
     qweight = orc.w4a16_pack(qc.numpy())
@@ -130,3 +132,27 @@ def test_w4a16_errors(q):
     q.qmm_w4a16(Wp, s, z, G, A, C, 0, N, K)  # M == 0: no-op
     q.qmm_w4a16(Wp, s, z, G, A, C, M, 0, K)  # N == 0: no-op
     q.qmm_check_device_error()
+
+
+@pytest.mark.parametrize("M", [256, 512])
+def test_w4a16_full_output(q, orc, M):
+    """Every element of the 8192 x 8192, G = 128 layer (M = 256: one CTA per
+    tile; M = 512: the stream-K grid and its fixup) against sum_k A w in fp64
+    with w = s (q - z) from the oracle's unpacking of the same codes.
+    Bar as test_w4a16_small."""
+    N = K = wl.W4A16_N
+    G = wl.W4A16_G
+    qc, s16, z, A16 = wl.w4a16_inputs(42, N, K, G, M, device="cuda")
+    qweight = pack_torch(qc)
+    del qc
+    Wp = packed_from_canon(q, qweight, N, K)
+    c = run(q, Wp, s16, z, G, A16, M, N, K)
+    codes = torch.from_numpy(orc.w4a16_unpack(qweight.cpu().numpy().view(np.uint32), K).astype(np.float64)).cuda()
+    sz = s16.double().repeat_interleave(G, dim=1)
+    zz = z.double().repeat_interleave(G, dim=1)
+    w = sz * (codes - zz)
+    del codes, sz, zz
+    a = A16.double()
+    ref = (a @ w.T).cpu().numpy()
+    den = (a.abs() @ w.abs().T).cpu().numpy()
+    check(c, ref, den, f"8192x8192 M={M} full")
