@@ -254,22 +254,40 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
     if (kMode == kFused) {
         pdl_wait();
         uint8_t *aw = smem + kRingBytes;
-        for (int64_t b = warp; b < (int64_t)mc * nsb; b += kConsumerWarps) {
-            const int64_t rr = b / nsb, sb = b % nsb;
-            const float4 *src =
-                reinterpret_cast<const float4 *>(a.X + (a.m0 + rr) * K + sb * QK_K + 8 * lane);
-            const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
-            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            uint32_t lo, hi;
-            float d;
-            int bsum;
-            q8_K_warp(v, lo, hi, d, bsum);
-            *reinterpret_cast<uint2 *>(aw + rr * K + sb * QK_K + q8K_code_offset(lane)) =
-                make_uint2(lo, hi);
-            if ((lane & 1) == 0)
-                *reinterpret_cast<int16_t *>(aw + a.act_bs + b * 32 + q8K_bsum_offset(lane >> 1)) =
-                    (int16_t)bsum;
-            if (lane == 0) reinterpret_cast<float *>(aw + a.act_d)[b] = d;
+        // super-blocks b = warp + 8 j of all the tokens' rows (b = row * nsb +
+        // sb, X rows contiguous, so b * QK_K is the element offset): up to
+        // kQBatch per warp with all their loads issued before any reduction
+        constexpr int kQBatch = 4;
+        const int nq = (int)(mc * nsb);  // at most 16 x 4096 blocks
+        for (int b0 = warp; b0 < nq; b0 += kQBatch * kConsumerWarps) {
+            float4 v[kQBatch][2];
+#pragma unroll
+            for (int j = 0; j < kQBatch; ++j) {
+                const int b = b0 + j * kConsumerWarps;
+                if (b < nq) {
+                    const float4 *src = reinterpret_cast<const float4 *>(a.X + a.m0 * K + (int64_t)b * QK_K) +
+                                        2 * lane;
+                    v[j][0] = __ldg(src);
+                    v[j][1] = __ldg(src + 1);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kQBatch; ++j) {
+                const int b = b0 + j * kConsumerWarps;
+                if (b < nq) {
+                    const float x[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w,
+                                        v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
+                    uint32_t lo, hi;
+                    float d;
+                    int bsum;
+                    q8_K_warp(x, lo, hi, d, bsum);
+                    *reinterpret_cast<uint2 *>(aw + (int64_t)b * QK_K + q8K_code_offset(lane)) = make_uint2(lo, hi);
+                    if ((lane & 1) == 0)
+                        *reinterpret_cast<int16_t *>(aw + a.act_bs + b * 32 + q8K_bsum_offset(lane >> 1)) =
+                            (int16_t)bsum;
+                    if (lane == 0) reinterpret_cast<float *>(aw + a.act_d)[b] = d;
+                }
+            }
         }
         consumer_sync();
     } else if (kMode == kStaged) {
@@ -397,16 +415,30 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
     if (kMode == kFused) {
         pdl_wait();
         uint8_t *aw = smem + kRingBytes;
-        for (int64_t b = warp; b < (int64_t)mc * nb; b += kConsumerWarps) {
-            const int64_t rr = b / nb, bb = b % nb;
-            const float x = __ldg(a.X + (a.m0 + rr) * K + bb * QK4_0 + lane);
-            int q, sum;
-            __half dh;
-            q8_0_warp(x, q, dh, sum);
-            aw[rr * K + bb * QK4_0 + lane] = (uint8_t)(int8_t)q;
-            if (lane == 0) {
-                reinterpret_cast<int16_t *>(aw + a.act_bs)[b] = (int16_t)sum;
-                reinterpret_cast<float *>(aw + a.act_d)[b] = __half2float(dh);
+        // blocks b = warp + 8 j of all the tokens' rows (b * QK4_0 is the
+        // element offset): up to kQBatch per warp, loads issued first
+        constexpr int kQBatch = 8;
+        const int nq = (int)(mc * nb);
+        for (int b0 = warp; b0 < nq; b0 += kQBatch * kConsumerWarps) {
+            float xv[kQBatch];
+#pragma unroll
+            for (int j = 0; j < kQBatch; ++j) {
+                const int b = b0 + j * kConsumerWarps;
+                if (b < nq) xv[j] = __ldg(a.X + a.m0 * K + (int64_t)b * QK4_0 + lane);
+            }
+#pragma unroll
+            for (int j = 0; j < kQBatch; ++j) {
+                const int b = b0 + j * kConsumerWarps;
+                if (b < nq) {
+                    int q, sum;
+                    __half dh;
+                    q8_0_warp(xv[j], q, dh, sum);
+                    aw[(int64_t)b * QK4_0 + lane] = (uint8_t)(int8_t)q;
+                    if (lane == 0) {
+                        reinterpret_cast<int16_t *>(aw + a.act_bs)[b] = (int16_t)sum;
+                        reinterpret_cast<float *>(aw + a.act_d)[b] = __half2float(dh);
+                    }
+                }
             }
         }
         consumer_sync();
