@@ -355,18 +355,17 @@ __device__ __forceinline__ void q8_K_warp(const float v[8], uint32_t &lo, uint32
     const float amax = warp_max_nonneg(a);
     d = __fdiv_rn(amax, 127.0f);
     const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
-    lo = 0;
-    hi = 0;
-    int s = 0;
+    // |x| <= amax, so |x * id| <= 127 (1 + 2^-23)^3 < 127.5: the clamp to
+    // +-127 of q8_code never acts here and is left out
+    int q[8], s = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int q = q8_code(v[i], id);
-        s += q;
-        if (i < 4)
-            lo |= (uint32_t)(q & 0xFF) << (8 * i);
-        else
-            hi |= (uint32_t)(q & 0xFF) << (8 * (i - 4));
+        q[i] = (int)round_half_away(__fmul_rn(v[i], id));
+        s += q[i];
     }
+    // low bytes of q[0..3] and q[4..7], little-endian
+    lo = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
+    hi = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
     bsum = s + __shfl_xor_sync(0xffffffffu, s, 1);
 }
 
