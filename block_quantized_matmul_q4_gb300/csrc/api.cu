@@ -521,6 +521,17 @@ qmm_status qmm_mul_mat_multi(qmm_type wt, int n, const void *const *W_packed, co
     return st;
 }
 
+qmm_status qmm_w4a16_unpack_zeros(const uint32_t *zeros_packed, uint8_t *zeros, int64_t N,
+                                  int64_t ngroups, qmm_stream_t stream) {
+    QMM_CHECK_ARG(N >= 0 && ngroups >= 1, "need N >= 0 and ngroups >= 1 (N=%lld ngroups=%lld)",
+                  (long long)N, (long long)ngroups);
+    QMM_CHECK_ARG(N <= ((int64_t)1 << 31) && ngroups <= ((int64_t)1 << 30), "sizes too large");
+    if (N == 0) return ok();
+    QMM_CHECK_ARG(zeros_packed && zeros, "null pointer argument");
+    return cuda_status(launch_w4a16_unpack_zeros(zeros_packed, zeros, N, ngroups, (cudaStream_t)stream),
+                       "W4A16 zero unpack launch");
+}
+
 qmm_status qmm_debug_block_sums(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
                                 const void *Xq, int64_t M, int32_t *out, qmm_stream_t stream) {
     qmm_status st = check_weight_args(wt, N, K);

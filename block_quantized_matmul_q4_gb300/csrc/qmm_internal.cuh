@@ -461,6 +461,8 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
 cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, int64_t G,
                               const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
                               float *part, cudaStream_t s);
+cudaError_t launch_w4a16_unpack_zeros(const uint32_t *zp, uint8_t *z, int64_t N, int64_t ng,
+                                      cudaStream_t s);
 // Q4_0 prefill (M > 16): fp16(d_a y) activations (permuted per block) in a
 // workspace of q4_0_prefill_bytes, then the fp16-operand tensor-core GEMM.
 size_t q4_0_prefill_bytes(int64_t M, int64_t K);

@@ -478,4 +478,30 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
     return cudaGetLastError();
 }
 
+// Zero points packed 8 per word like the codes ([N][ceil(ng/8)] words,
+// group g of row n at bits 4 (g mod 8) of word g / 8) -> uint8 [N][ng], the
+// layout the W4A16 kernels read; once, at load time, like the repack.
+__global__ void __launch_bounds__(256) w4a16_unpack_zeros_kernel(const uint32_t *__restrict__ zp,
+                                                                 uint8_t *__restrict__ z, int64_t N,
+                                                                 int64_t ng) {
+    const int64_t words = (ng + 7) / 8, total = N * ng;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / ng, g = i - n * ng;
+        z[i] = (uint8_t)((zp[n * words + g / 8] >> (4 * (g % 8))) & 15u);
+    }
+}
+
+cudaError_t launch_w4a16_unpack_zeros(const uint32_t *zp, uint8_t *z, int64_t N, int64_t ng,
+                                      cudaStream_t s) {
+    const int64_t total = N * ng;
+    int64_t grid = (total + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    w4a16_unpack_zeros_kernel<<<(unsigned)grid, 256, 0, s>>>(zp, z, N, ng);
+    count_launch();
+    return cudaGetLastError();
+}
+
 }  // namespace qmm

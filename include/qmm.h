@@ -285,6 +285,19 @@ qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t
                      const uint16_t *A, uint16_t *C, int64_t M, int64_t N, int64_t K,
                      qmm_stream_t stream);
 
+/* W4A16 zero points stored 4-bit packed (page 3, "从数学表达式到真实存储": a
+ * zero point packed in low bits needs one more bit extraction), unpacked
+ * once at load time into the uint8 [N][ngroups] array qmm_w4a16 reads.
+ * zeros_packed: [N][ceil(ngroups / 8)] uint32, row-major; group g of row n
+ * at bits 4 (g mod 8) .. 4 (g mod 8) + 3 of word g / 8 (the nibble order of
+ * the codes, page 3, "位级打包"); unused high nibbles of a row's last word
+ * are ignored. zeros: [N][ngroups] uint8 (written, values 0..15). Device
+ * pointers; both owned by the caller; the call only enqueues on `stream`.
+ * Errors: QMM_ERR_ARG for N < 0, ngroups < 1 or null pointers (N == 0 is
+ * a no-op). */
+qmm_status qmm_w4a16_unpack_zeros(const uint32_t *zeros_packed, uint8_t *zeros, int64_t N,
+                                  int64_t ngroups, qmm_stream_t stream);
+
 /* Per-block integer sums of the factored form, for bit-exact checking
  * (page 1, "正确性" and "通用实现"). Xq holds canonical activation blocks
  * (Q8_0 for Q4_0 weights, Q8_K for Q4_K), M rows.

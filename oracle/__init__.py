@@ -82,6 +82,7 @@ def lib():
                                          f32p, f64p, f64p, ctypes.c_int]
             L.orc_w4a16_pack.argtypes = [vp, vp, i64, i64]
             L.orc_w4a16_unpack.argtypes = [vp, vp, i64, i64]
+            L.orc_w4a16_unpack_zeros.argtypes = [vp, vp, i64, i64]
             L.orc_w4a16_matmul.argtypes = [vp, vp, vp, i64, vp, i64, i64, i64, vp, i64,
                                            vp, f64p, f64p, ctypes.c_int]
             _lib = L
@@ -240,6 +241,17 @@ def w4a16_unpack(qweight: np.ndarray, K: int) -> np.ndarray:
     N = qw.shape[0]
     out = np.zeros((N, K), np.uint8)
     lib().orc_w4a16_unpack(_ptr(qw), _ptr(out), N, K)
+    return out
+
+
+def w4a16_unpack_zeros(zp: np.ndarray, ng: int) -> np.ndarray:
+    """Zero points packed 8 per uint32 word like the codes, [N, ceil(ng/8)]
+    -> uint8 [N, ng]."""
+    w = _c(zp, np.uint32)
+    N = w.shape[0]
+    assert w.shape[1] == (ng + 7) // 8
+    out = np.zeros((N, ng), np.uint8)
+    lib().orc_w4a16_unpack_zeros(_ptr(w), _ptr(out), N, ng)
     return out
 
 

@@ -613,6 +613,17 @@ void orc_w4a16_unpack(const uint32_t *qweight, uint8_t *q, int64_t N, int64_t K)
     }
 }
 
+/* Zero points packed like the codes ([P3] "从数学表达式到真实存储": a zero
+ * point packed in low bits needs one more bit extraction; "位级打包" gives the
+ * nibble order): row n's groups 8c .. 8c+7 sit in word c, group g at bits
+ * 4 (g mod 8) .. 4 (g mod 8) + 3; a row has ceil(ng / 8) words. */
+void orc_w4a16_unpack_zeros(const uint32_t *zp, uint8_t *z, int64_t N, int64_t ng) {
+    const int64_t words = (ng + 7) / 8;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < ng; ++g)
+            z[n * ng + g] = (uint8_t)((zp[n * words + g / 8] >> (4 * (g % 8))) & 15u);
+}
+
 void orc_w4a16_matmul(const uint32_t *qweight, const uint16_t *scales, const uint8_t *zeros,
                       int64_t G, const uint16_t *A, int64_t M, int64_t N, int64_t K,
                       const int64_t *rows, int64_t nrows, uint16_t *C16, double *C64, double *den,

@@ -100,6 +100,8 @@ void orc_mul_mat_q8(int wtype, const void *W, int64_t N, int64_t K, const void *
  * qweight is [N][K/8] uint32 with k = 8c + i in bits 4i..4i+3 of word c. */
 void orc_w4a16_pack(const uint8_t *q, uint32_t *qweight, int64_t N, int64_t K);
 void orc_w4a16_unpack(const uint32_t *qweight, uint8_t *q, int64_t N, int64_t K);
+/* Zero points packed 8 per word like the codes: [N][ceil(ng/8)] -> [N][ng]. */
+void orc_w4a16_unpack_zeros(const uint32_t *zp, uint8_t *z, int64_t N, int64_t ng);
 /* C[m,n] = sum_k A[m,k] * s[n,g] * (q[n,k] - z[n,g]), g = k / G.
  * scales, A hold fp16 bit patterns; zeros is uint8 [N][K/G].
  * Outputs [M][nrows]: C16 (fp16 bits of the fp64 sum), C64, den (any may be NULL). */

@@ -156,3 +156,35 @@ def test_w4a16_full_output(q, orc, M):
     ref = (a @ w.T).cpu().numpy()
     den = (a.abs() @ w.abs().T).cpu().numpy()
     check(c, ref, den, f"8192x8192 M={M} full")
+
+
+@pytest.mark.parametrize("N,ng", [(37, 3), (64, 8), (100, 9), (8192, 64)])
+def test_w4a16_unpack_zeros(q, orc, N, ng):
+    """Packed zero points unpacked on the GPU equal the oracle's reading bit
+    for bit, and a W4A16 call on them equals the call on the original
+    zeros."""
+    g = torch.Generator().manual_seed(N * 131 + ng)
+    words = (ng + 7) // 8
+    zp = torch.randint(-2 ** 31, 2 ** 31 - 1, (N, words), generator=g, dtype=torch.int64).to(torch.int32)
+    z = torch.empty(N, ng, dtype=torch.uint8, device="cuda")
+    q.qmm_w4a16_unpack_zeros(zp.cuda(), z, N, ng)
+    torch.cuda.synchronize()
+    ref = orc.w4a16_unpack_zeros(zp.numpy().view(np.uint32), ng)
+    assert np.array_equal(z.cpu().numpy(), ref)
+    if N <= 100:
+        G = 128
+        K = ng * G
+        qc, s16, _, A16 = wl.w4a16_inputs(43, N, K, G, 5)
+        qweight = orc.w4a16_pack(qc.numpy())
+        Wp = packed_from_canon(q, torch.from_numpy(qweight.view(np.int32)).cuda(), N, K)
+        c1 = run(q, Wp, s16.cuda(), z, G, A16.cuda(), 5, N, K)
+        c2 = run(q, Wp, s16.cuda(), torch.from_numpy(ref).cuda(), G, A16.cuda(), 5, N, K)
+        assert np.array_equal(c1.view(np.uint16), c2.view(np.uint16))
+
+
+def test_w4a16_unpack_zeros_errors(q):
+    z = torch.empty(4, 4, dtype=torch.uint8, device="cuda")
+    zp = torch.zeros(4, 1, dtype=torch.int32, device="cuda")
+    with pytest.raises(q.QmmError):
+        q.qmm_w4a16_unpack_zeros(zp, z, 4, 0)
+    q.qmm_w4a16_unpack_zeros(zp, z, 0, 4)  # N == 0: no-op

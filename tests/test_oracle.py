@@ -417,6 +417,16 @@ def test_w4a16_pack_golden(orc):
         assert orc.w4a16_unpack(u, 8).tolist() == [case["q"]]
 
 
+def test_w4a16_zeros_pack_golden(orc):
+    """Packed zero points (8 per word, like the codes) read back from
+    hand-derived words, rows whose group count is not a multiple of 8
+    included."""
+    g = json.load(open(os.path.join(GOLD, "w4a16_zeros_pack.json")))
+    for case in g["cases"]:
+        words = np.array([case["words"]], np.uint32)
+        assert orc.w4a16_unpack_zeros(words, len(case["z"])).tolist() == [case["z"]]
+
+
 def test_w4a16_pack_roundtrip(orc):
     q, _, _, _ = wl.w4a16_inputs(0, 8, 256, 128, 1)
     qn = q.numpy()
