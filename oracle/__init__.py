@@ -23,10 +23,10 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _HDR = os.path.join(_HERE, "oracle.h")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-Q4_0, Q4_K, Q8_0, Q8_K = 0, 1, 2, 3
-BLOCK_BYTES = {Q4_0: 18, Q4_K: 144, Q8_0: 34, Q8_K: 292}
-BLOCK_ELEMS = {Q4_0: 32, Q4_K: 256, Q8_0: 32, Q8_K: 256}
-ACT_TYPE = {Q4_0: Q8_0, Q4_K: Q8_K}
+Q4_0, Q4_K, Q8_0, Q8_K, Q6_K = 0, 1, 2, 3, 5
+BLOCK_BYTES = {Q4_0: 18, Q4_K: 144, Q8_0: 34, Q8_K: 292, Q6_K: 210}
+BLOCK_ELEMS = {Q4_0: 32, Q4_K: 256, Q8_0: 32, Q8_K: 256, Q6_K: 256}
+ACT_TYPE = {Q4_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K}
 
 _lock = threading.Lock()
 _lib = None
@@ -74,10 +74,13 @@ def lib():
             L.orc_vec_dot_q4_0_q8_0.argtypes = [i64, vp, vp]
             L.orc_vec_dot_q4_K_q8_K.restype = ctypes.c_float
             L.orc_vec_dot_q4_K_q8_K.argtypes = [i64, vp, vp]
+            L.orc_vec_dot_q6_K_q8_K.restype = ctypes.c_float
+            L.orc_vec_dot_q6_K_q8_K.argtypes = [i64, vp, vp]
             L.orc_vec_dot_f64.restype = ctypes.c_double
             L.orc_vec_dot_f64.argtypes = [ctypes.c_int, i64, vp, vp]
             L.orc_block_sums_q4_0.argtypes = [i64, vp, vp, vp]
             L.orc_block_sums_q4_K.argtypes = [i64, vp, vp, vp, vp, vp]
+            L.orc_block_sums_q6_K.argtypes = [i64, vp, vp, vp, vp]
             L.orc_mul_mat_q8.argtypes = [ctypes.c_int, vp, i64, i64, vp, i64, vp, i64,
                                          f32p, f64p, f64p, ctypes.c_int]
             L.orc_w4a16_pack.argtypes = [vp, vp, i64, i64]
@@ -167,6 +170,8 @@ def vec_dot(wt: int, k: int, w_row: np.ndarray, a_row: np.ndarray) -> float:
     a = _c(a_row, np.uint8)
     if wt == Q4_0:
         return float(lib().orc_vec_dot_q4_0_q8_0(k, _ptr(w), _ptr(a)))
+    if wt == Q6_K:
+        return float(lib().orc_vec_dot_q6_K_q8_K(k, _ptr(w), _ptr(a)))
     return float(lib().orc_vec_dot_q4_K_q8_K(k, _ptr(w), _ptr(a)))
 
 
@@ -180,6 +185,7 @@ def block_sums(wt: int, k: int, w_row: np.ndarray, a_row: np.ndarray):
     """Per-block integer sums of one (weight row, activation row) pair.
 
     Q4_0: returns isum [k/32]. Q4_K: returns (S [k/256, 8], isum [k/256], msum [k/256]).
+    Q6_K: returns (S [k/256, 16], isum [k/256]).
     """
     w = _c(w_row, np.uint8)
     a = _c(a_row, np.uint8)
@@ -187,6 +193,11 @@ def block_sums(wt: int, k: int, w_row: np.ndarray, a_row: np.ndarray):
         isum = np.zeros(k // 32, np.int32)
         lib().orc_block_sums_q4_0(k, _ptr(w), _ptr(a), _ptr(isum))
         return isum
+    if wt == Q6_K:
+        S = np.zeros((k // 256, 16), np.int32)
+        isum = np.zeros(k // 256, np.int32)
+        lib().orc_block_sums_q6_K(k, _ptr(w), _ptr(a), _ptr(S), _ptr(isum))
+        return S, isum
     S = np.zeros((k // 256, 8), np.int32)
     isum = np.zeros(k // 256, np.int32)
     msum = np.zeros(k // 256, np.int32)

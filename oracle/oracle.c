@@ -41,12 +41,20 @@ typedef struct {
     int16_t bsums[16];  /* sums of 16 consecutive codes */
 } orc_block_q8_K;
 
+typedef struct {
+    uint8_t ql[128];    /* low 4 bits of the 256 6-bit codes */
+    uint8_t qh[64];     /* high 2 bits */
+    int8_t scales[16];  /* one int8 scale per 16 elements */
+    uint16_t d;         /* super-block scale */
+} orc_block_q6_K;
+
 /* Sizes the pages state: 2+16 = 18 B, 2+32 = 34 B, 2+2+12+128 = 144 B,
- * 4+256+32 = 292 B. */
+ * 4+256+32 = 292 B, 128+64+16+2 = 210 B. */
 _Static_assert(sizeof(orc_block_q4_0) == 18, "block_q4_0 must be 18 bytes");
 _Static_assert(sizeof(orc_block_q8_0) == 34, "block_q8_0 must be 34 bytes");
 _Static_assert(sizeof(orc_block_q4_K) == 144, "block_q4_K must be 144 bytes");
 _Static_assert(sizeof(orc_block_q8_K) == 292, "block_q8_K must be 292 bytes");
+_Static_assert(sizeof(orc_block_q6_K) == 210, "block_q6_K must be 210 bytes");
 
 size_t orc_block_bytes(int type) {
     switch (type) {
@@ -54,6 +62,7 @@ size_t orc_block_bytes(int type) {
     case ORC_Q4_K: return sizeof(orc_block_q4_K);
     case ORC_Q8_0: return sizeof(orc_block_q8_0);
     case ORC_Q8_K: return sizeof(orc_block_q8_K);
+    case ORC_Q6_K: return sizeof(orc_block_q6_K);
     default: return 0;
     }
 }
@@ -63,7 +72,8 @@ int orc_block_elems(int type) {
     case ORC_Q4_0:
     case ORC_Q8_0: return 32;
     case ORC_Q4_K:
-    case ORC_Q8_K: return 256;
+    case ORC_Q8_K:
+    case ORC_Q6_K: return 256;
     default: return 0;
     }
 }
@@ -345,6 +355,67 @@ void orc_quantize_row_q4_K(const float *x, void *blocks, int64_t k) {
     }
 }
 
+/* Q6_K ([P1] "更低的比特: Q6_K 与 Q2_K 的取舍"): w = d * s_j * q with q in
+ * -32..31, 16 groups j of 16 elements, int8 s_j, fp16 d, no min. The pages
+ * give the format, not the scale search; the reading used extends the Q4_0
+ * rule to two levels:
+ *   sc_j = -x_max,j / 32 (x_max,j the signed value of largest magnitude in
+ *          group j, first one on ties), d = max_j |sc_j| / 127 (fp16),
+ *   s_j  = clamp(round(sc_j / d), -127, 127),
+ *   q    = clamp(round(x / (d16 * s_j)), -32, 31), stored as u = q + 32,
+ * with the stored d16 for the codes (round = half away from zero). Bit
+ * order, the Q4_K pairing (fields 32 elements apart) applied to both arrays:
+ *   ql[32c + l] = (u[64c + l] & 15) | (u[64c + 32 + l] & 15) << 4, c < 4
+ *   qh[32h + l] = sum_i (u[128h + 32i + l] >> 4) << 2i,            h < 2. */
+static void q6_K_pack(const uint8_t *u, orc_block_q6_K *blk) {
+    for (int c = 0; c < 4; ++c)
+        for (int l = 0; l < 32; ++l)
+            blk->ql[32 * c + l] = (uint8_t)((u[64 * c + l] & 15) | ((u[64 * c + 32 + l] & 15) << 4));
+    for (int h = 0; h < 2; ++h) {
+        for (int l = 0; l < 32; ++l) {
+            uint8_t v = 0;
+            for (int i = 0; i < 4; ++i) v = (uint8_t)(v | ((u[128 * h + 32 * i + l] >> 4) << (2 * i)));
+            blk->qh[32 * h + l] = v;
+        }
+    }
+}
+
+void orc_quantize_row_q6_K(const float *x, void *blocks, int64_t k) {
+    orc_block_q6_K *y = (orc_block_q6_K *)blocks;
+    const int64_t nb = k / 256;
+    for (int64_t b = 0; b < nb; ++b) {
+        const float *xb = x + b * 256;
+        float sc[16], max_sc = 0.0f;
+        for (int j = 0; j < 16; ++j) {
+            float amax = 0.0f, vmax = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                const float a = fabsf(xb[16 * j + i]);
+                if (a > amax) {
+                    amax = a;
+                    vmax = xb[16 * j + i];
+                }
+            }
+            sc[j] = vmax / -32.0f;
+            if (fabsf(sc[j]) > max_sc) max_sc = fabsf(sc[j]);
+        }
+        const float d = max_sc / 127.0f;
+        y[b].d = orc_fp32_to_fp16(d);
+        const float d16 = orc_fp16_to_fp32(y[b].d);
+        uint8_t u[256];
+        for (int j = 0; j < 16; ++j) {
+            const int s = d > 0.0f ? clampi((int)rha(sc[j] / d), -127, 127) : 0;
+            y[b].scales[j] = (int8_t)s;
+            const float D = d16 * (float)s;
+            for (int i = 0; i < 16; ++i) {
+                int q = 0;
+                if (D != 0.0f) q = clampi((int)rha(xb[16 * j + i] / D), -32, 31);
+                u[16 * j + i] = (uint8_t)(q + 32);
+            }
+        }
+        q6_K_pack(u, &y[b]);
+    }
+}
+
 void orc_quantize_rows(int type, const float *x, void *blocks, int64_t rows, int64_t k,
                        int nthreads) {
     const size_t row_bytes = orc_block_bytes(type) * (size_t)(k / orc_block_elems(type));
@@ -358,6 +429,7 @@ void orc_quantize_rows(int type, const float *x, void *blocks, int64_t rows, int
         case ORC_Q4_K: orc_quantize_row_q4_K(xr, yr, k); break;
         case ORC_Q8_0: orc_quantize_row_q8_0(xr, yr, k); break;
         case ORC_Q8_K: orc_quantize_row_q8_K(xr, yr, k); break;
+        case ORC_Q6_K: orc_quantize_row_q6_K(xr, yr, k); break;
         default: break;
         }
     }
@@ -378,6 +450,15 @@ static void q4_K_fields(const orc_block_q4_K *blk, int i, int *q, int *s, int *m
     orc_get_scale_min_k4(i / 32, blk->scales, &sj, &mj);
     *s = sj;
     *m = mj;
+}
+
+/* Signed 6-bit code of element i (-32..31), read back from ql and qh. */
+static int q6_K_code(const orc_block_q6_K *blk, int i) {
+    const int c = i / 64, l = i % 64, h = i / 128, r = i % 128;
+    const uint8_t lo_byte = blk->ql[32 * c + (l % 32)];
+    const int lo = l < 32 ? (lo_byte & 15) : (lo_byte >> 4);
+    const int hi = (blk->qh[32 * h + (r % 32)] >> (2 * (r / 32))) & 3;
+    return (lo | (hi << 4)) - 32;
 }
 
 static int q4_0_code(const orc_block_q4_0 *blk, int i) {
@@ -401,6 +482,13 @@ void orc_dequantize_row(int type, const void *blocks, float *y, int64_t k) {
                 q4_K_fields(&x[b], i, &q, &s, &m);
                 y[b * 256 + i] = d * (float)s * (float)q - dmin * (float)m;
             }
+        }
+    } else if (type == ORC_Q6_K) {
+        const orc_block_q6_K *x = (const orc_block_q6_K *)blocks;
+        for (int64_t b = 0; b < k / 256; ++b) {
+            const float d = orc_fp16_to_fp32(x[b].d);
+            for (int i = 0; i < 256; ++i)
+                y[b * 256 + i] = d * (float)x[b].scales[i / 16] * (float)q6_K_code(&x[b], i);
         }
     } else if (type == ORC_Q8_0) {
         const orc_block_q8_0 *x = (const orc_block_q8_0 *)blocks;
@@ -433,6 +521,13 @@ void orc_dequantize_row_f64(int type, const void *blocks, double *y, int64_t k) 
                 q4_K_fields(&x[b], i, &q, &s, &m);
                 y[b * 256 + i] = d * (double)s * (double)q - dmin * (double)m;
             }
+        }
+    } else if (type == ORC_Q6_K) {
+        const orc_block_q6_K *x = (const orc_block_q6_K *)blocks;
+        for (int64_t b = 0; b < k / 256; ++b) {
+            const double d = orc_fp16_to_fp32(x[b].d);
+            for (int i = 0; i < 256; ++i)
+                y[b * 256 + i] = d * (double)x[b].scales[i / 16] * (double)q6_K_code(&x[b], i);
         }
     } else if (type == ORC_Q8_0) {
         const orc_block_q8_0 *x = (const orc_block_q8_0 *)blocks;
@@ -494,6 +589,36 @@ void orc_block_sums_q4_K(int64_t k, const void *w, const void *a, int32_t *S, in
     }
 }
 
+/* Q6_K x Q8_K ([P1] "更低的比特": no min term, so no bsums): per super-block
+ * S_j = sum_{i in group j} q_i y_i over the 16 elements of group j, and
+ * isum = sum_j s_j S_j; the dot adds d_a d isum. */
+void orc_block_sums_q6_K(int64_t k, const void *w, const void *a, int32_t *S, int32_t *isum) {
+    const orc_block_q6_K *x = (const orc_block_q6_K *)w;
+    const orc_block_q8_K *y = (const orc_block_q8_K *)a;
+    for (int64_t b = 0; b < k / 256; ++b) {
+        int32_t is = 0;
+        for (int j = 0; j < 16; ++j) {
+            int32_t Sj = 0;
+            for (int i = 0; i < 16; ++i) Sj += q6_K_code(&x[b], 16 * j + i) * y[b].qs[16 * j + i];
+            is += (int32_t)x[b].scales[j] * Sj;
+            if (S) S[b * 16 + j] = Sj;
+        }
+        if (isum) isum[b] = is;
+    }
+}
+
+float orc_vec_dot_q6_K_q8_K(int64_t k, const void *w, const void *a) {
+    const orc_block_q6_K *x = (const orc_block_q6_K *)w;
+    const orc_block_q8_K *y = (const orc_block_q8_K *)a;
+    float acc = 0.0f;
+    for (int64_t b = 0; b < k / 256; ++b) {
+        int32_t isum;
+        orc_block_sums_q6_K(256, &x[b], &y[b], NULL, &isum);
+        acc += (y[b].d * orc_fp16_to_fp32(x[b].d)) * (float)isum;
+    }
+    return acc;
+}
+
 float orc_vec_dot_q4_0_q8_0(int64_t k, const void *w, const void *a) {
     const orc_block_q4_0 *x = (const orc_block_q4_0 *)w;
     const orc_block_q8_0 *y = (const orc_block_q8_0 *)a;
@@ -539,6 +664,13 @@ double orc_vec_dot_f64(int wtype, int64_t k, const void *w, const void *a) {
             orc_block_sums_q4_K(256, &x[b], &y[b], NULL, &isum, &msum);
             acc += (double)y[b].d * (double)orc_fp16_to_fp32(x[b].d) * (double)isum -
                    (double)y[b].d * (double)orc_fp16_to_fp32(x[b].dmin) * (double)msum;
+        }    } else if (wtype == ORC_Q6_K) {
+        const orc_block_q6_K *x = (const orc_block_q6_K *)w;
+        const orc_block_q8_K *y = (const orc_block_q8_K *)a;
+        for (int64_t b = 0; b < k / 256; ++b) {
+            int32_t isum;
+            orc_block_sums_q6_K(256, &x[b], &y[b], NULL, &isum);
+            acc += (double)y[b].d * (double)orc_fp16_to_fp32(x[b].d) * (double)isum;
         }
     }
     return acc;
@@ -571,8 +703,9 @@ void orc_mul_mat_q8(int wtype, const void *W, int64_t N, int64_t K, const void *
             for (int64_t m = 0; m < M; ++m) {
                 const uint8_t *ar = (const uint8_t *)Xq + (size_t)m * arow;
                 if (Y32) {
-                    Y32[m * nrows + r] = wtype == ORC_Q4_0 ? orc_vec_dot_q4_0_q8_0(K, wr, ar)
-                                                           : orc_vec_dot_q4_K_q8_K(K, wr, ar);
+                    Y32[m * nrows + r] = wtype == ORC_Q4_0   ? orc_vec_dot_q4_0_q8_0(K, wr, ar)
+                                         : wtype == ORC_Q6_K ? orc_vec_dot_q6_K_q8_K(K, wr, ar)
+                                                             : orc_vec_dot_q4_K_q8_K(K, wr, ar);
                 }
                 if (need_f64) {
                     orc_dequantize_row_f64(atype, ar, ad, K);

@@ -24,9 +24,11 @@
  *
  * Parity pins: every function here is pinned by tests/test_oracle.py against
  * facts the pages print or mathematics fixes. None is "parity unpinned"
- * except the Q4_K scale/min search, whose pages describe only the packing;
- * the single-pass min/max reading used here is pinned by its reconstruction
- * bound and invariants, but not against any other implementation's blocks.
+ * except the Q4_K and Q6_K scale searches, whose pages describe only the
+ * format; the readings used here are pinned by their reconstruction bounds
+ * and invariants, but not against any other implementation's blocks. The
+ * Q6_K bit order within ql and qh is a reading too (the pages give the field
+ * sizes only), pinned by a hand-derived golden block.
  */
 #ifndef QMM_ORACLE_H
 #define QMM_ORACLE_H
@@ -38,9 +40,10 @@
 extern "C" {
 #endif
 
-enum { ORC_Q4_0 = 0, ORC_Q4_K = 1, ORC_Q8_0 = 2, ORC_Q8_K = 3 };
+enum { ORC_Q4_0 = 0, ORC_Q4_K = 1, ORC_Q8_0 = 2, ORC_Q8_K = 3, ORC_Q6_K = 5 };
 
-/* Bytes per block: 18 (Q4_0), 144 (Q4_K), 34 (Q8_0), 292 (Q8_K); 0 otherwise. */
+/* Bytes per block: 18 (Q4_0), 144 (Q4_K), 34 (Q8_0), 292 (Q8_K), 210 (Q6_K);
+ * 0 otherwise. */
 size_t orc_block_bytes(int type);
 /* Elements per block: 32 or 256. */
 int orc_block_elems(int type);
@@ -59,6 +62,7 @@ void orc_quantize_row_q4_0(const float *x, void *blocks, int64_t k);
 void orc_quantize_row_q4_K(const float *x, void *blocks, int64_t k);
 void orc_quantize_row_q8_0(const float *x, void *blocks, int64_t k);
 void orc_quantize_row_q8_K(const float *x, void *blocks, int64_t k);
+void orc_quantize_row_q6_K(const float *x, void *blocks, int64_t k);
 /* Quantize rows [r0, r1) of a row-major [rows, k] fp32 matrix. */
 void orc_quantize_rows(int type, const float *x, void *blocks, int64_t rows, int64_t k,
                        int nthreads);
@@ -70,6 +74,7 @@ void orc_dequantize_row_f64(int type, const void *blocks, double *y, int64_t k);
 /* vec_dot of one weight row with one activation row, fp32 accumulation. */
 float orc_vec_dot_q4_0_q8_0(int64_t k, const void *w, const void *a);
 float orc_vec_dot_q4_K_q8_K(int64_t k, const void *w, const void *a);
+float orc_vec_dot_q6_K_q8_K(int64_t k, const void *w, const void *a);
 /* Same factored form, accumulated in fp64. */
 double orc_vec_dot_f64(int wtype, int64_t k, const void *w, const void *a);
 
@@ -80,11 +85,15 @@ double orc_vec_dot_f64(int wtype, int64_t k, const void *w, const void *a);
 void orc_block_sums_q4_0(int64_t k, const void *w, const void *a, int32_t *isum);
 void orc_block_sums_q4_K(int64_t k, const void *w, const void *a, int32_t *S, int32_t *isum,
                          int32_t *msum);
+/* Q6_K x Q8_K: S[sb*16 + j] = sum_i q_i * y_i over group j (q signed, -32..31),
+ *              isum[sb] = sum_j s_j S_j (no min term). */
+void orc_block_sums_q6_K(int64_t k, const void *w, const void *a, int32_t *S, int32_t *isum);
 
 /*
  * mul_mat over already-quantized activations.
  *   W   : [N] rows of k/QK weight blocks (canonical byte layout)
- *   Xq  : [M] rows of activation blocks (Q8_0 for Q4_0 weights, Q8_K for Q4_K)
+ *   Xq  : [M] rows of activation blocks (Q8_0 for Q4_0 weights, Q8_K for Q4_K
+ *         and Q6_K)
  *   rows: optional list of nrows weight-row indices (NULL = all N rows)
  * Outputs, [M][nrows] row-major:
  *   Y32 : fp32 vec_dot (factored integer form, fp32 accumulation)

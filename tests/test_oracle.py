@@ -22,6 +22,7 @@ DT_Q4_0 = np.dtype([("d", "<u2"), ("qs", "u1", 16)])
 DT_Q8_0 = np.dtype([("d", "<u2"), ("qs", "i1", 32)])
 DT_Q4_K = np.dtype([("d", "<u2"), ("dmin", "<u2"), ("scales", "u1", 12), ("qs", "u1", 128)])
 DT_Q8_K = np.dtype([("d", "<f4"), ("qs", "i1", 256), ("bsums", "<i2", 16)])
+DT_Q6_K = np.dtype([("ql", "u1", 128), ("qh", "u1", 64), ("scales", "i1", 16), ("d", "<u2")])
 
 
 def h2f(bits):
@@ -45,6 +46,9 @@ def test_block_sizes_and_bits_per_weight(orc):
     assert [orc.block_bytes(t) * 8 / orc.BLOCK_ELEMS[t] for t in (0, 1, 2, 3)] == [4.5, 4.5, 8.5, 9.125]
     assert DT_Q4_0.itemsize == 18 and DT_Q8_0.itemsize == 34
     assert DT_Q4_K.itemsize == 144 and DT_Q8_K.itemsize == 292
+    # Q6_K: 128 + 64 + 16 + 2 = 210 B per 256 elements = 6.5625 bpw
+    assert orc.block_bytes(orc.Q6_K) == 210 and DT_Q6_K.itemsize == 210
+    assert orc.block_bytes(orc.Q6_K) * 8 / orc.BLOCK_ELEMS[orc.Q6_K] == 6.5625
 
 
 # --------------------------------------------------------------- fp16
@@ -336,7 +340,8 @@ def test_worked_example(orc):
 
 
 def test_factored_form_equals_bruteforce_fp64(orc):
-    for wt, K in ((orc.Q4_0, 96), (orc.Q4_0, 512), (orc.Q4_K, 256), (orc.Q4_K, 512)):
+    for wt, K in ((orc.Q4_0, 96), (orc.Q4_0, 512), (orc.Q4_K, 256), (orc.Q4_K, 512),
+                  (orc.Q6_K, 256), (orc.Q6_K, 768)):
         w = wl.weights(3, 4, K, 0.02, row_offset_std=0.005).numpy()
         x = rng_normal(3, 60, (3, K))
         Wq = orc.quantize(wt, w)
@@ -389,7 +394,8 @@ def test_integer_sum_bounds():
 
 
 def test_mul_mat_q8_against_numpy(orc):
-    for wt, N, K, M in ((orc.Q4_0, 7, 96, 3), (orc.Q4_K, 5, 512, 2), (orc.Q4_K, 1, 256, 1)):
+    for wt, N, K, M in ((orc.Q4_0, 7, 96, 3), (orc.Q4_K, 5, 512, 2), (orc.Q4_K, 1, 256, 1),
+                        (orc.Q6_K, 6, 512, 3)):
         w = wl.weights(5, N, K, 0.02, row_offset_std=0.005).numpy()
         x = rng_normal(5, 62, (M, K))
         Wq = orc.quantize(wt, w)
@@ -405,6 +411,106 @@ def test_mul_mat_q8_against_numpy(orc):
         rows = [N - 1, 0]
         sub = orc.mul_mat_q8(wt, Wq, N, K, res["xq"], M, rows=rows)
         assert np.array_equal(sub["y32"], res["y32"][:, rows])
+
+
+# --------------------------------------------------------------- Q6_K
+def _q6_K_golden():
+    g = json.load(open(os.path.join(GOLD, "q6_K_layout.json")))
+    q = np.full(256, g["codes_default"], np.int64)
+    for e, v in g["codes"].items():
+        q[int(e)] = v
+    return g, q
+
+
+def test_q6_K_golden_pack(orc):
+    # x = d s_j q exactly (d = 2^-10); each group holds a -32, so the scale
+    # rule gives back d and s_j, and the bytes must be the hand-derived ones
+    g, q = _q6_K_golden()
+    s = np.array(g["scales"], np.int64)
+    x = (g["d"] * s[np.arange(256) // 16] * q).astype(np.float32)
+    blk = orc.quantize(orc.Q6_K, x).view(DT_Q6_K)[0, 0]
+    assert int(blk["d"]) == g["d_bits"]
+    assert blk["scales"].tolist() == g["scales"]
+    ql = np.zeros(128, np.int64)
+    for i, v in g["ql_nonzero"].items():
+        ql[int(i)] = v
+    qh = np.full(64, 0xAA, np.int64)
+    for i, v in g["qh_not_0xAA"].items():
+        qh[int(i)] = v
+    assert blk["ql"].tolist() == ql.tolist()
+    assert blk["qh"].tolist() == qh.tolist()
+
+
+def test_q6_K_golden_dequantize(orc):
+    # the golden bytes, built by hand, read back as the hand-computed values
+    g, q = _q6_K_golden()
+    blk = np.zeros(1, DT_Q6_K)
+    blk["d"] = g["d_bits"]
+    blk["scales"] = g["scales"]
+    ql = np.zeros(128, np.uint8)
+    for i, v in g["ql_nonzero"].items():
+        ql[int(i)] = v
+    qh = np.full(64, 0xAA, np.uint8)
+    for i, v in g["qh_not_0xAA"].items():
+        qh[int(i)] = v
+    blk["ql"] = ql
+    blk["qh"] = qh
+    for f64 in (False, True):
+        w = orc.dequantize(orc.Q6_K, blk.view(np.uint8), 256, f64=f64)[0]
+        for e, v in g["dequantized"].items():
+            assert w[int(e)] == v, (e, w[int(e)], v)
+        s = np.array(g["scales"], np.int64)
+        assert np.array_equal(w, g["d"] * s[np.arange(256) // 16] * q)
+
+
+def test_q6_K_reconstruction_bound(orc):
+    rows = 16
+    x = wl.weights(7, rows, 1024, 0.02, row_offset_std=0.005, outlier_frac=2e-3).numpy()
+    x[3, :256] = -np.abs(x[3, :256])  # an all-negative super-block
+    x[5, 256:272] = 0.0               # an all-zero group
+    blocks = orc.quantize(orc.Q6_K, x).view(DT_Q6_K).reshape(rows, -1)
+    w = orc.dequantize(orc.Q6_K, orc.quantize(orc.Q6_K, x), 1024, f64=True)
+    for r in range(rows):
+        for b in range(4):
+            blk = blocks[r, b]
+            d16 = float(h2f(blk["d"]))
+            s = blk["scales"].astype(np.int64)
+            assert np.abs(s).max() == 127 or d16 == 0.0  # the largest group sets d
+            for j in range(16):
+                sl = slice(256 * b + 16 * j, 256 * b + 16 * j + 16)
+                xs = x[r, sl].astype(np.float64)
+                sc = np.abs(xs).max() / 32.0           # |sc_j|
+                D = d16 * abs(s[j])
+                err = np.abs(w[r, sl] - xs)
+                # half a grid step, plus up to 32 x the scale's own error
+                # (fp16 d, 8-bit s_j), plus one step where +32 clamps to 31
+                bound = D + 32 * abs(sc - D) + 1e-9
+                assert np.all(err <= bound), (r, b, j, err.max(), bound)
+        assert np.sqrt(np.mean((w[r] - x[r]) ** 2)) < 0.05 * np.std(x[r]) + 1e-9
+    assert np.all(w[5, 256:272] == 0.0)
+
+
+def test_q6_K_block_sums_onehot_probe(orc):
+    # a one-hot activation reads back the code at that position, in its group
+    K = 256
+    g, q = _q6_K_golden()
+    s = np.array(g["scales"], np.int64)
+    x = (g["d"] * s[np.arange(256) // 16] * q).astype(np.float32)
+    wq = orc.quantize(orc.Q6_K, x)[0]
+    for p in range(K):
+        y = np.zeros(K, np.int64)
+        y[p] = 1
+        S, isum = orc.block_sums(orc.Q6_K, K, wq, _q8_K_block(1.0, y))
+        assert S[0, p // 16] == q[p] and S[0].sum() == q[p]
+        assert isum[0] == s[p // 16] * q[p]
+    # all-ones activation: S_j is the sum of group j's codes
+    S, isum = orc.block_sums(orc.Q6_K, K, wq, _q8_K_block(1.0, np.ones(K, np.int64)))
+    assert S[0].tolist() == q.reshape(16, 16).sum(1).tolist()
+
+
+def test_q6_K_integer_sum_bound():
+    # |S_j| <= 16 * 32 * 127 and |isum| <= 16 * 127 * that: int32 holds it
+    assert 16 * 127 * (16 * 32 * 127) == 132_128_768 < 2 ** 31
 
 
 # --------------------------------------------------------------- W4A16

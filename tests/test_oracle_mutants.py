@@ -25,6 +25,16 @@ MUTANTS = {
     "mul_mat output transposed": ("Y32[m * nrows + r] =", "Y32[r * M + m] ="),
     "fp16 ties away from zero": ("if (rem > half || (rem == half && (q & 1))) q += 1;",
                                  "if (rem >= half) q += 1;"),
+    "q6_K ql high nibble from wrong element": (
+        "((u[64 * c + 32 + l] & 15) << 4)", "((u[64 * c + 16 + l] & 15) << 4)"),
+    "q6_K qh field order reversed": ("(blk->qh[32 * h + (r % 32)] >> (2 * (r / 32))) & 3",
+                                     "(blk->qh[32 * h + (r % 32)] >> (6 - 2 * (r / 32))) & 3"),
+    "q6_K code offset off by one": ("return (lo | (hi << 4)) - 32;", "return (lo | (hi << 4)) - 31;"),
+    "q6_K group index transposed": ("q6_K_code(&x[b], 16 * j + i) * y[b].qs[16 * j + i];",
+                                    "q6_K_code(&x[b], 16 * j + i) * y[b].qs[16 * i + j];"),
+    "q6_K scale sign dropped": ("sc[j] = vmax / -32.0f;", "sc[j] = fabsf(vmax) / 32.0f;"),
+    "q6_K activation scale dropped": ("acc += (y[b].d * orc_fp16_to_fp32(x[b].d)) * (float)isum;",
+                                      "acc += orc_fp16_to_fp32(x[b].d) * (float)isum;"),
     "q4_0 zero point off by one": ("int q0 = clampi((int)floorf(v0 + 8.5f), 0, 15);",
                                    "int q0 = clampi((int)floorf(v0 + 7.5f), 0, 15);"),
 }
