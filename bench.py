@@ -334,8 +334,8 @@ def gemv_rate(q, dev, stream, wt, N, K, M, seed, L=None, steps=6400, copies=None
     with torch.cuda.stream(stream):
         g.replay()
     t = timed(stream, lambda: run_graphs(g, None, reps)) / (reps * GRAPH_STEPS)
-    qk = 256 if wt == q.QMM_TYPE_Q4_K else 32
-    bq = 292 if wt == q.QMM_TYPE_Q4_K else 34
+    qk = 32 if wt == q.QMM_TYPE_Q4_0 else 256
+    bq = 34 if wt == q.QMM_TYPE_Q4_0 else 292
     b = nbytes * N // (-(-N // 8) * 8) + M * (K // qk) * bq + M * N * 4 + M * K * 4
     del cps, Wp
     return t, b
@@ -436,6 +436,7 @@ def gpu_extras(q, dev, stream, args):
     out = {"prefill": prefill_extras(q, dev, stream)}
     out["w4a16_8192"] = w4a16_extras(q, dev, stream)
     torch.cuda.empty_cache()
+    out["q6_K"] = q6_K_rate(q, dev, stream)
     out["q4_K_4096_M_sweep"] = sweep_rate(q, dev, stream)
     # Q4_0 x Q8_0 GEMV, 256 x 1024, M = 1 (L2-resident correctness case)
     Ls = wl.GEMV_Q4_0_SMALL
@@ -452,6 +453,22 @@ def gpu_extras(q, dev, stream, args):
         per[Lp.name] = {"us": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1)}
         torch.cuda.empty_cache()
     out["layer_70B_q4_K_m1"]["per_projection_alone"] = per
+    return out
+
+
+def q6_K_rate(q, dev, stream):
+    """Q6_K x Q8_K decode (scalar GEMV, 6.5625 bits per weight): the 4096 x
+    4096 shape at M in {1, 4, 16} and the 70B layer's largest projection
+    (28672 x 8192) at M = 1; GB/s of algorithmic bytes."""
+    out = {}
+    L = wl.GEMV_Q4_K_4096
+    for M in (1, 4, 16):
+        t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q6_K, L.N, L.K, M, 0, L)
+        out[f"4096x4096_m{M}"] = {"us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1)}
+    Lp = [x for x in wl.LAYER_70B if x.name == "gate_proj"][0]
+    t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q6_K, Lp.N, Lp.K, 1, 7, Lp, steps=640)
+    out[f"{Lp.N}x{Lp.K}_m1"] = {"us": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1)}
+    torch.cuda.empty_cache()
     return out
 
 
@@ -583,10 +600,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--case", choices=["decode", "prefill", "w4a16", "layer", "sweep"],
+    ap.add_argument("--case", choices=["decode", "prefill", "w4a16", "layer", "sweep", "q6_K"],
                     default="decode",
-                    help="prefill / w4a16 / layer / sweep: only that measurement (for profiler "
-                         "captures)")
+                    help="prefill / w4a16 / layer / sweep / q6_K: only that measurement (for "
+                         "profiler captures)")
     ap.add_argument("--m", type=int, action="append",
                     help="with --case sweep: only these token counts")
     args = ap.parse_args()
@@ -622,7 +639,7 @@ def main():
         torch.cuda.set_device(0)
     if args.case != "decode":
         import block_quantized_matmul_q4_gb300 as q
-        fn = {"prefill": prefill_extras, "w4a16": w4a16_extras, "layer": layer_rate,
+        fn = {"prefill": prefill_extras, "w4a16": w4a16_extras, "layer": layer_rate, "q6_K": q6_K_rate,
               "sweep": lambda q, d, s: sweep_rate(q, d, s, args.m)}[args.case]
         print(json.dumps(fn(q, torch.device("cuda", torch.cuda.current_device()),
                             torch.cuda.Stream())), flush=True)

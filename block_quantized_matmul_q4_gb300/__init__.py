@@ -16,7 +16,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqmm.so")
 
-QMM_TYPE_Q4_0, QMM_TYPE_Q4_K, QMM_TYPE_Q8_0, QMM_TYPE_Q8_K, QMM_TYPE_W4A16 = 0, 1, 2, 3, 4
+QMM_TYPE_Q4_0, QMM_TYPE_Q4_K, QMM_TYPE_Q8_0, QMM_TYPE_Q8_K, QMM_TYPE_W4A16, QMM_TYPE_Q6_K = 0, 1, 2, 3, 4, 5
 QMM_OK = 0
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "QMM_ERR_CUDA",
           4: "QMM_ERR_TIMEOUT", 5: "QMM_ERR_NOMEM", 6: "QMM_ERR_WORKSPACE"}

@@ -77,7 +77,7 @@ qmm_status set_error(qmm_status s, const char *fmt, ...) {
 
 namespace {
 
-bool is_weight(qmm_type t) { return t == QMM_TYPE_Q4_0 || t == QMM_TYPE_Q4_K; }
+bool is_weight(qmm_type t) { return t == QMM_TYPE_Q4_0 || t == QMM_TYPE_Q4_K || t == QMM_TYPE_Q6_K; }
 bool is_act(qmm_type t) { return t == QMM_TYPE_Q8_0 || t == QMM_TYPE_Q8_K; }
 int elems(qmm_type t) { return (t == QMM_TYPE_Q4_0 || t == QMM_TYPE_Q8_0) ? QK4_0 : QK_K; }
 qmm_type act_of(qmm_type wt) { return wt == QMM_TYPE_Q4_0 ? QMM_TYPE_Q8_0 : QMM_TYPE_Q8_K; }
@@ -99,7 +99,7 @@ qmm_status cuda_status(cudaError_t e, const char *what) {
     } while (0)
 
 qmm_status check_weight_args(qmm_type wt, int64_t N, int64_t K) {
-    QMM_CHECK_ARG(is_weight(wt), "weight type must be Q4_0 or Q4_K (got %d)", (int)wt);
+    QMM_CHECK_ARG(is_weight(wt), "weight type must be Q4_0, Q4_K or Q6_K (got %d)", (int)wt);
     QMM_CHECK_ARG(N >= 0 && K > 0, "sizes must satisfy N >= 0, K > 0 (N=%lld K=%lld)",
                   (long long)N, (long long)K);
     QMM_CHECK_ARG(K % elems(wt) == 0, "K=%lld is not a multiple of the block size %d",
@@ -129,8 +129,9 @@ void prepare_pool(cudaStream_t s) {
 // More than 16 tokens run the tensor-core GEMMs and their workspace layouts
 // (Q4_K: integer-valued fp16 codes; Q4_0: fp16 dequantized activations);
 // fewer the decode GEMVs: Q4_K from 2 tokens on the mma.sync kernel and its
-// activation images, otherwise the scalar GEMV and the planar layout.
-bool use_gemm(qmm_type wt, int64_t M) { return M >= kGemmMinM; }
+// activation images, otherwise the scalar GEMV and the planar layout. Q6_K
+// runs the scalar GEMV at every M (16 tokens per launch).
+bool use_gemm(qmm_type wt, int64_t M) { return M >= kGemmMinM && wt != QMM_TYPE_Q6_K; }
 
 // Prefill workspaces: the quantized activations (read-only in the GEMM),
 // then the stream-K partial area that calls owning the workspace use.
@@ -268,6 +269,7 @@ size_t qmm_block_bytes(qmm_type t) {
     case QMM_TYPE_Q8_0: return B_Q8_0;
     case QMM_TYPE_Q8_K: return B_Q8_K;
     case QMM_TYPE_W4A16: return 4;
+    case QMM_TYPE_Q6_K: return B_Q6_K;
     default: return 0;
     }
 }
@@ -434,7 +436,7 @@ qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t 
     if (M == 0 || N == 0) return ok();
     QMM_CHECK_ARG(W_packed && Xq && Y, "null pointer argument");
     QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(Y, 4), "W_packed must be 16-byte aligned, Y 4-byte");
-    QMM_CHECK_ARG(aligned(Xq, wt == QMM_TYPE_Q4_K ? 4 : 2),
+    QMM_CHECK_ARG(aligned(Xq, act_of(wt) == QMM_TYPE_Q8_K ? 4 : 2),
                   "Xq must be aligned like its blocks (Q8_K: 4 bytes, Q8_0: 2 bytes)");
     cudaStream_t s = (cudaStream_t)stream;
     prepare_pool(s);
@@ -540,7 +542,7 @@ qmm_status qmm_debug_block_sums(qmm_type wt, const void *W_packed, int64_t N, in
     if (M == 0 || N == 0) return ok();
     QMM_CHECK_ARG(W_packed && Xq && out, "null pointer argument");
     QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(out, 4), "misaligned pointer");
-    QMM_CHECK_ARG(aligned(Xq, wt == QMM_TYPE_Q4_K ? 4 : 2), "Xq misaligned");
+    QMM_CHECK_ARG(aligned(Xq, act_of(wt) == QMM_TYPE_Q8_K ? 4 : 2), "Xq misaligned");
     return cuda_status(
         launch_debug_block_sums(wt, W_packed, N, K, Xq, M, out, (cudaStream_t)stream),
         "debug kernel launch");

@@ -63,6 +63,45 @@ __global__ void block_sums_q4_K_kernel(const uint8_t *__restrict__ Wp, int64_t N
     }
 }
 
+// Q6_K: each element decoded from the packed record through the lane
+// geometry the GEMV uses (ql bytes 16t.., high-bit words, scale bytes 2t,
+// 2t + 1), summed per group of 16 in natural element order.
+__global__ void block_sums_q6_K_kernel(const uint8_t *__restrict__ Wp, int64_t N, int64_t nsb,
+                                       const uint8_t *__restrict__ Xq, int64_t M,
+                                       int32_t *__restrict__ out) {
+    const int64_t total = M * N * nsb;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t sb = i % nsb, n = (i / nsb) % N, m = i / (nsb * N);
+        const uint8_t *rec = Wp + ((n / kTileRows) * nsb + sb) * kQ6Rec;
+        const int r = (int)(n % kTileRows);
+        const uint8_t *row = rec + r * kQ6Codes;
+        const int8_t *ps = reinterpret_cast<const int8_t *>(rec + kQ6ScOff + 16 * r);
+        const int8_t *y = reinterpret_cast<const int8_t *>(Xq + (m * nsb + sb) * B_Q8_K + 4);
+        int32_t S[16], isum = 0;
+        for (int j = 0; j < 16; ++j) S[j] = 0;
+        int sj[16];
+        for (int t = 0; t < 8; ++t) {
+            for (int hi = 0; hi < 2; ++hi) {
+                const uint32_t hw = reinterpret_cast<const uint32_t *>(row + 128 + 8 * t)[hi];
+                sj[q6k_elem(t, hi, 0) / 16] = ps[2 * t + hi];
+                for (int k = 0; k < 16; ++k) {
+                    const int e = q6k_elem(t, hi, k);
+                    const int nib = hi ? (row[16 * t + k] >> 4) : (row[16 * t + k] & 15);
+                    const int u = nib | (int)(((hw >> q6k_hbit_pos(k)) & 3) << 4);
+                    S[e / 16] += (u - 32) * y[e];
+                }
+            }
+        }
+        int32_t *o = out + i * 17;
+        for (int j = 0; j < 16; ++j) {
+            o[j] = S[j];
+            isum += sj[j] * S[j];
+        }
+        o[16] = isum;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
@@ -74,6 +113,9 @@ cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int6
     if (grid < 1) grid = 1;
     if (wt == QMM_TYPE_Q4_0)
         block_sums_q4_0_kernel<<<(int)grid, 256, 0, s>>>((const uint8_t *)Wp, N, nblk,
+                                                         (const uint8_t *)Xq, M, out);
+    else if (wt == QMM_TYPE_Q6_K)
+        block_sums_q6_K_kernel<<<(int)grid, 256, 0, s>>>((const uint8_t *)Wp, N, nblk,
                                                          (const uint8_t *)Xq, M, out);
     else
         block_sums_q4_K_kernel<<<(int)grid, 256, 0, s>>>((const uint8_t *)Wp, N, nblk,

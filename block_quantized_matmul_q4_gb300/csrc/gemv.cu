@@ -203,6 +203,47 @@ __device__ __forceinline__ float q4k_dot(const uint4 &hdr, const uint4 &q, const
     return da * (dw * (float)isum - dmw * (float)msum);
 }
 
+// The Q8_K quantizer fused into the GEMV prologue (K-quant weights): the
+// launch's mc token rows of X into the planar layout in shared memory at aw.
+// Super-blocks b = warp + 8 j of all the tokens' rows (b = row * nsb + sb, X
+// rows contiguous, so b * QK_K is the element offset): up to kQBatch per
+// warp with all their loads issued before any reduction.
+__device__ __forceinline__ void fused_q8K(const GemvArgs &a, int mc, int64_t nsb, int64_t K, int warp,
+                                          int lane, uint8_t *aw) {
+    constexpr int kQBatch = 4;
+    const int nq = (int)(mc * nsb);  // at most 16 x 4096 blocks
+    for (int b0 = warp; b0 < nq; b0 += kQBatch * kConsumerWarps) {
+        float4 v[kQBatch][2];
+#pragma unroll
+        for (int j = 0; j < kQBatch; ++j) {
+            const int b = b0 + j * kConsumerWarps;
+            if (b < nq) {
+                const float4 *src = reinterpret_cast<const float4 *>(a.X + a.m0 * K + (int64_t)b * QK_K) +
+                                    2 * lane;
+                v[j][0] = __ldg(src);
+                v[j][1] = __ldg(src + 1);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kQBatch; ++j) {
+            const int b = b0 + j * kConsumerWarps;
+            if (b < nq) {
+                const float x[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w,
+                                    v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
+                uint32_t lo, hi;
+                float d;
+                int bsum;
+                q8_K_warp(x, lo, hi, d, bsum);
+                *reinterpret_cast<uint2 *>(aw + (int64_t)b * QK_K + q8K_code_offset(lane)) = make_uint2(lo, hi);
+                if ((lane & 1) == 0)
+                    *reinterpret_cast<int16_t *>(aw + a.act_bs + b * 32 + q8K_bsum_offset(lane >> 1)) =
+                        (int16_t)bsum;
+                if (lane == 0) reinterpret_cast<float *>(aw + a.act_d)[b] = d;
+            }
+        }
+    }
+}
+
 template <int MT, int kMode>
 __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -253,42 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
     const float *xd = gl ? a.x.d + a.m0 * nsb : reinterpret_cast<const float *>(act + a.act_d);
     if (kMode == kFused) {
         pdl_wait();
-        uint8_t *aw = smem + kRingBytes;
-        // super-blocks b = warp + 8 j of all the tokens' rows (b = row * nsb +
-        // sb, X rows contiguous, so b * QK_K is the element offset): up to
-        // kQBatch per warp with all their loads issued before any reduction
-        constexpr int kQBatch = 4;
-        const int nq = (int)(mc * nsb);  // at most 16 x 4096 blocks
-        for (int b0 = warp; b0 < nq; b0 += kQBatch * kConsumerWarps) {
-            float4 v[kQBatch][2];
-#pragma unroll
-            for (int j = 0; j < kQBatch; ++j) {
-                const int b = b0 + j * kConsumerWarps;
-                if (b < nq) {
-                    const float4 *src = reinterpret_cast<const float4 *>(a.X + a.m0 * K + (int64_t)b * QK_K) +
-                                        2 * lane;
-                    v[j][0] = __ldg(src);
-                    v[j][1] = __ldg(src + 1);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kQBatch; ++j) {
-                const int b = b0 + j * kConsumerWarps;
-                if (b < nq) {
-                    const float x[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w,
-                                        v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
-                    uint32_t lo, hi;
-                    float d;
-                    int bsum;
-                    q8_K_warp(x, lo, hi, d, bsum);
-                    *reinterpret_cast<uint2 *>(aw + (int64_t)b * QK_K + q8K_code_offset(lane)) = make_uint2(lo, hi);
-                    if ((lane & 1) == 0)
-                        *reinterpret_cast<int16_t *>(aw + a.act_bs + b * 32 + q8K_bsum_offset(lane >> 1)) =
-                            (int16_t)bsum;
-                    if (lane == 0) reinterpret_cast<float *>(aw + a.act_d)[b] = d;
-                }
-            }
-        }
+        fused_q8K(a, mc, nsb, K, warp, lane, smem + kRingBytes);
         consumer_sync();
     } else if (kMode == kStaged) {
         if (!mbar_wait(smem_u32(r.act), 0, a.err)) return;
@@ -336,6 +342,153 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_K_kernel(const GemvArgs a
         } else {
             if (g < cnt) body(g);
             if (g + 4 < cnt) body(g + 4);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&r.empty[s]));
+        if (chunk == nchunks - 1) {
+            const int mi = mat_of(a.ms, p);
+            const int64_t N = a.ms.N[mi];
+            float *Y = a.ms.Y[mi];
+            const int64_t n0 = 2 * (p - a.ms.off[mi]) * kTileRows + warp, n1 = n0 + kTileRows;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const float v0 = warp_sum(acc0[m]);
+                const float v1 = warp_sum(acc1[m]);
+                if (lane == 0 && m < mc) {
+                    if (n0 < N) Y[(a.m0 + m) * N + n0] = v0;
+                    if (n1 < N) Y[(a.m0 + m) * N + n1] = v1;
+                }
+                acc0[m] = acc1[m] = 0.0f;
+            }
+        }
+        if (++chunk == nchunks) chunk = 0, ++p;
+    }
+}
+
+// ------------------------------------------------------------------ Q6_K
+// Page 1, "更低的比特: Q6_K 与 Q2_K 的取舍": w = d s_j q, q = u - 32 in
+// -32..31, 16 groups of 16, no min term. Per super-block and lane t:
+//   S_g = sum_i q_i y_i = sum_i u_i y_i - 32 bs_g   (bs_g the group's code sum)
+//   isum = s_lo S_lo + s_hi S_hi,   y += d_a (d isum)
+// Stage = a pair of tiles x up to 4 super-blocks (records of kQ6Rec bytes:
+// tile 2p's at offset 0, tile 2p+1's at kQ6Half). Warp w owns row w of both
+// tiles; lane (g, t) takes super-block g of the stage and ql bytes 16t ..
+// 16t+15, whose elements are exactly the planar activation bytes 16t.. and
+// 128 + 16t.. of the super-block and whose two groups' code sums are word t.
+constexpr int kQ6KChunk = 4;
+constexpr int kQ6Half = kQ6KChunk * kQ6Rec;  // 6720
+static_assert(2 * kQ6Half <= kStageBytes, "stage size");
+
+// The 6-bit codes of ql word w (4 bytes, low or high nibbles) as bytes 0..63.
+__device__ __forceinline__ uint32_t q6k_u(uint32_t nib, uint32_t hbits, int w) {
+    return (nib & 0x0F0F0F0Fu) | (((hbits >> (2 * w)) & 0x03030303u) << 4);
+}
+
+__device__ __forceinline__ float q6k_dot(const uint4 &q, const uint2 &h, uint32_t sc, float dw,
+                                         const uint4 &y0, const uint4 &y1, int bw, float da) {
+    int s0 = dp4a_us(q6k_u(q.x, h.x, 0), y0.x, 0);
+    int s0b = dp4a_us(q6k_u(q.y, h.x, 1), y0.y, 0);
+    s0 = dp4a_us(q6k_u(q.z, h.x, 2), y0.z, s0);
+    s0b = dp4a_us(q6k_u(q.w, h.x, 3), y0.w, s0b);
+    int s1 = dp4a_us(q6k_u(q.x >> 4, h.y, 0), y1.x, 0);
+    int s1b = dp4a_us(q6k_u(q.y >> 4, h.y, 1), y1.y, 0);
+    s1 = dp4a_us(q6k_u(q.z >> 4, h.y, 2), y1.z, s1);
+    s1b = dp4a_us(q6k_u(q.w >> 4, h.y, 3), y1.w, s1b);
+    const int S0 = s0 + s0b - 32 * (int)(int16_t)(bw & 0xFFFF);
+    const int S1 = s1 + s1b - 32 * (bw >> 16);
+    const int isum = (int)(int8_t)(sc & 0xFF) * S0 + (int)(int8_t)(sc >> 8) * S1;
+    return da * (dw * (float)isum);
+}
+
+template <int MT, int kMode>
+__global__ void __launch_bounds__(kThreads, 2) gemv_q6_K_kernel(const GemvArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nsb = a.nblk, K = nsb * QK_K;
+    const int mc = (int)min64(MT, a.M - a.m0);
+    int64_t pb, pe;
+    my_tiles(a.ms.off[a.ms.n], pb, pe);  // this CTA's tile pairs (over all matrices)
+    const int64_t nchunks = (nsb + kQ6KChunk - 1) / kQ6KChunk;
+    const int64_t n_items = (pe - pb) * nchunks;
+    const Ring r = ring_init(smem, kMode == kDirect ? 0 : a.act_bytes);
+
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            producer_loop(
+                r, n_items, a.err,
+                [&, chunk = (int64_t)0, p = pb](int64_t, uint32_t dst, uint32_t bar,
+                                                 uint64_t pol) mutable {
+                    const int mi = mat_of(a.ms, p);
+                    const int64_t t0 = 2 * (p - a.ms.off[mi]);
+                    const int64_t sb0 = chunk * kQ6KChunk;
+                    if (++chunk == nchunks) chunk = 0, ++p;
+                    const uint32_t bytes = (uint32_t)min64(kQ6KChunk, nsb - sb0) * kQ6Rec;
+                    const bool has1 = t0 + 1 < tiles_of(a.ms.N[mi]);
+                    const uint8_t *W = a.ms.W[mi];
+                    mbar_arrive_expect_tx(bar, has1 ? 2 * bytes : bytes);
+                    bulk_g2s(dst, W + (t0 * nsb + sb0) * kQ6Rec, bytes, bar, pol);
+                    if (has1)
+                        bulk_g2s(dst + kQ6Half, W + ((t0 + 1) * nsb + sb0) * kQ6Rec, bytes, bar, pol);
+                },
+                [&]() {
+                    if (kMode == kStaged) stage_activations(r, a, mc, K, 16);
+                });
+            if (kMode == kStaged) mbar_wait(smem_u32(r.act), 0, a.err);
+        }
+        return;
+    }
+
+    const uint8_t *act = smem + kRingBytes;
+    const bool gl = kMode == kDirect;
+    const int8_t *xqs = gl ? a.x.qs + a.m0 * K : reinterpret_cast<const int8_t *>(act);
+    const int32_t *xbs = gl ? reinterpret_cast<const int32_t *>(a.x.sums) + a.m0 * nsb * 8
+                            : reinterpret_cast<const int32_t *>(act + a.act_bs);
+    const float *xd = gl ? a.x.d + a.m0 * nsb : reinterpret_cast<const float *>(act + a.act_d);
+    if (kMode == kFused) {
+        pdl_wait();
+        fused_q8K(a, mc, nsb, K, warp, lane, smem + kRingBytes);
+        consumer_sync();
+    } else if (kMode == kStaged) {
+        if (!mbar_wait(smem_u32(r.act), 0, a.err)) return;
+    } else {
+        pdl_wait();
+    }
+
+    const int g = lane >> 3, t = lane & 7;
+    float acc0[MT], acc1[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = 0.0f;
+
+    int64_t chunk = 0, p = pb;  // the item's K chunk and tile pair, counted
+    for (int64_t it = 0; it < n_items; ++it) {
+        const int s = (int)(it % kStages);
+        if (!mbar_wait(smem_u32(&r.full[s]), (uint32_t)((it / kStages) & 1), a.err)) break;
+        const int64_t sb0 = chunk * kQ6KChunk;
+        const int cnt = (int)min64(kQ6KChunk, nsb - sb0);
+        if (g < cnt) {
+            const uint8_t *ra = smem + s * kStageBytes + g * kQ6Rec;
+            const uint8_t *rb = ra + kQ6Half;
+            const uint4 qa = *reinterpret_cast<const uint4 *>(ra + warp * kQ6Codes + 16 * t);
+            const uint2 ha = *reinterpret_cast<const uint2 *>(ra + warp * kQ6Codes + 128 + 8 * t);
+            const uint32_t sca = *reinterpret_cast<const uint16_t *>(ra + kQ6ScOff + 16 * warp + 2 * t);
+            const float dwa = __half2float(*reinterpret_cast<const __half *>(ra + kQ6DOff + 2 * warp));
+            const uint4 qb = *reinterpret_cast<const uint4 *>(rb + warp * kQ6Codes + 16 * t);
+            const uint2 hb = *reinterpret_cast<const uint2 *>(rb + warp * kQ6Codes + 128 + 8 * t);
+            const uint32_t scb = *reinterpret_cast<const uint16_t *>(rb + kQ6ScOff + 16 * warp + 2 * t);
+            const float dwb = __half2float(*reinterpret_cast<const __half *>(rb + kQ6DOff + 2 * warp));
+            const int64_t sbg = sb0 + g;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < mc) {
+                    const int8_t *yp = xqs + m * K + sbg * QK_K;
+                    const uint4 y0 = ld4(yp + 16 * t, gl);        // group 4c + h
+                    const uint4 y1 = ld4(yp + 128 + 16 * t, gl);  // group 4c + 2 + h
+                    const int bw = ld(xbs + (m * nsb + sbg) * 8 + t, gl);
+                    const float da = ld(xd + m * nsb + sbg, gl);
+                    acc0[m] += q6k_dot(qa, ha, sca, dwa, y0, y1, bw, da);
+                    acc1[m] += q6k_dot(qb, hb, scb, dwb, y0, y1, bw, da);
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&r.empty[s]));
@@ -515,13 +668,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
 // ------------------------------------------------------------------ launch
 template <int MT, int kMode>
 cudaError_t launch_kernel(qmm_type wt, const GemvArgs &a, bool pdl, cudaStream_t s) {
-    const void *fn = wt == QMM_TYPE_Q4_K
-                         ? reinterpret_cast<const void *>(gemv_q4_K_kernel<MT, kMode>)
-                         : reinterpret_cast<const void *>(gemv_q4_0_kernel<MT, kMode>);
+    const void *fn = wt == QMM_TYPE_Q4_K   ? reinterpret_cast<const void *>(gemv_q4_K_kernel<MT, kMode>)
+                     : wt == QMM_TYPE_Q6_K ? reinterpret_cast<const void *>(gemv_q6_K_kernel<MT, kMode>)
+                                           : reinterpret_cast<const void *>(gemv_q4_0_kernel<MT, kMode>);
     const int smem = kRingBytes + (kMode == kDirect ? 0 : (int)a.act_bytes) + kBarBytes;
     cudaError_t e = ensure_smem_attr(fn, smem);
     if (e != cudaSuccess) return e;
-    // Q4_K CTAs work on pairs of tiles, Q4_0 CTAs on single tiles
+    // K-quant CTAs work on pairs of tiles, Q4_0 CTAs on single tiles
     const int64_t units = a.ms.off[a.ms.n];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)balanced_grid(units, 2LL * sm_count()));
@@ -535,6 +688,8 @@ cudaError_t launch_kernel(qmm_type wt, const GemvArgs &a, bool pdl, cudaStream_t
     cfg.numAttrs = pdl ? 1 : 0;
     if (wt == QMM_TYPE_Q4_K)
         e = cudaLaunchKernelEx(&cfg, gemv_q4_K_kernel<MT, kMode>, a);
+    else if (wt == QMM_TYPE_Q6_K)
+        e = cudaLaunchKernelEx(&cfg, gemv_q6_K_kernel<MT, kMode>, a);
     else
         e = cudaLaunchKernelEx(&cfg, gemv_q4_0_kernel<MT, kMode>, a);
     count_launch();
@@ -549,8 +704,8 @@ cudaError_t launch_mode(qmm_type wt, int mode, const GemvArgs &a, bool pdl, cuda
 }
 
 uint32_t act_layout(qmm_type wt, int64_t mt, int64_t K, uint32_t *bs_off, uint32_t *d_off) {
-    const int qk = wt == QMM_TYPE_Q4_K ? QK_K : QK4_0;
-    const int groups = wt == QMM_TYPE_Q4_K ? 16 : 1;
+    const int qk = wt == QMM_TYPE_Q4_0 ? QK4_0 : QK_K;
+    const int groups = wt == QMM_TYPE_Q4_0 ? 1 : 16;
     const uint32_t bs = align16((uint64_t)mt * K);
     const uint32_t d = bs + align16((uint64_t)mt * (K / qk) * groups * 2);
     if (bs_off) *bs_off = bs;
@@ -585,13 +740,14 @@ MatSet single_mat(const void *Wp, int64_t N, float *Y) {
 cudaError_t launch_gemv(qmm_type wt, MatSet ms, int64_t K, Planar x, const float *X, int64_t M,
                         bool pdl, cudaStream_t s) {
     if (X && gemv_use_mma(wt, M, K)) return launch_gemv_mma_q4_K(ms, K, X, nullptr, M, pdl, s);
-    // work units: tile pairs (Q4_K CTAs work on two 8-row tiles) or tiles
+    // work units: tile pairs (K-quant CTAs work on two 8-row tiles) or tiles
+    const bool pairs = wt != QMM_TYPE_Q4_0;
     ms.off[0] = 0;
     for (int i = 0; i < ms.n; ++i)
-        ms.off[i + 1] = ms.off[i] + (wt == QMM_TYPE_Q4_K ? (tiles_of(ms.N[i]) + 1) / 2 : tiles_of(ms.N[i]));
+        ms.off[i + 1] = ms.off[i] + (pairs ? (tiles_of(ms.N[i]) + 1) / 2 : tiles_of(ms.N[i]));
     GemvArgs a;
     a.ms = ms;
-    a.nblk = K / (wt == QMM_TYPE_Q4_K ? QK_K : QK4_0);
+    a.nblk = K / (pairs ? QK_K : QK4_0);
     a.x = x;
     a.X = X;
     a.M = M;

@@ -17,6 +17,7 @@ constexpr int B_Q4_0 = 18;  // canonical bytes per block (page 1 block layouts)
 constexpr int B_Q8_0 = 34;
 constexpr int B_Q4_K = 144;
 constexpr int B_Q8_K = 292;
+constexpr int B_Q6_K = 210;  // ql[128] qh[64] int8 scales[16] fp16 d
 
 // Packed weight layout: rows grouped in tiles of kTileRows. Within a tile,
 // the blocks of one K position are adjacent, so a (tile, K-range) is one
@@ -25,7 +26,29 @@ constexpr int B_Q8_K = 292;
 //         the 12 scale bytes, see k4_header_to_packed)
 //   Q4_0: tile t = [kTileRows][nb][16 B nibbles] then [nb][kTileRows] fp16 d
 //         (a (tile, K-range) is then 8 row segments plus one scale segment)
+//   Q6_K: tile t = [nsb] records of kQ6Rec = 8 x 210 B:
+//         [8 rows][192 B codes] [8 rows][16 B scales] [8 rows] fp16 d.
+//         Codes of a row: the canonical ql (bytes 16t.. serve GEMV lane t),
+//         then per lane t two words of high bits (q6k_* below); the scales
+//         re-ordered so lane t's two are bytes 2t, 2t + 1.
 constexpr int kTileRows = 8;
+constexpr int kQ6Codes = 192;                            // ql 128 B + qh 64 B per row
+constexpr int kQ6ScOff = kTileRows * kQ6Codes;           // 1536
+constexpr int kQ6DOff = kQ6ScOff + kTileRows * 16;       // 1664
+constexpr int kQ6Rec = kQ6DOff + kTileRows * 2;          // 1680 = 8 x 210
+static_assert(kQ6Rec == kTileRows * B_Q6_K && kQ6Rec % 16 == 0, "Q6_K record");
+
+// Q6_K lane geometry, shared by the repack and the GEMV. Lane t (0..7) of a
+// row reads ql bytes 16t + i (i < 16): with c = t / 2, h = t % 2, the low
+// nibbles are elements 64c + 16h + i (group 4c + h) and the high nibbles
+// elements 64c + 32 + 16h + i (group 4c + 2 + h) -- the Q8_K planar order.
+// Its high-bit word for either set holds element i's 2 bits at bit
+// 8 (i % 4) + 2 (i / 4), so (word >> 2w) & 0x03030303 lines them up with
+// the 4 code bytes of ql word w.
+__host__ __device__ inline int q6k_elem(int t, int hi, int i) {
+    return 64 * (t >> 1) + 32 * hi + 16 * (t & 1) + i;
+}
+__host__ __device__ inline int q6k_hbit_pos(int i) { return 8 * (i & 3) + 2 * (i >> 2); }
 
 __host__ __device__ inline int64_t tiles_of(int64_t N) { return (N + kTileRows - 1) / kTileRows; }
 

@@ -244,6 +244,89 @@ __global__ void __launch_bounds__(256) quantize_q4_K_kernel(const float *__restr
     }
 }
 
+// ---------------------------------------------------------------- Q6_K weights
+// One warp per super-block; lane l holds elements 8l .. 8l+7, half of group
+// l / 2. Reading of the unprinted scale search (page 1 gives the format):
+// sc_j = -x_max,j / 32 with x_max,j the signed value of largest magnitude in
+// group j (the first on ties), d = max |sc_j| / 127, s_j = round(sc_j / d)
+// clamped to int8 +-127, codes q = clamp(round(x / (d16 s_j)), -32, 31) from
+// the stored fp16 d, stored as u = q + 32. Canonical bit order: ql[32c + l] =
+// low(u[64c + l]) | low(u[64c + 32 + l]) << 4, qh[32h + l] = sum_i
+// high2(u[128h + 32i + l]) << 2i (the pairing of Q4_K's nibbles, fields 32
+// elements apart).
+__global__ void __launch_bounds__(256) quantize_q6_K_kernel(const float *__restrict__ W,
+                                                            uint8_t *__restrict__ out,
+                                                            int64_t nblocks) {
+    __shared__ __align__(16) uint8_t us_all[8][256];
+    const int lane = threadIdx.x & 31;
+    uint8_t *us = us_all[threadIdx.x >> 5];
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
+         b += nwarps) {
+        const float4 *src = reinterpret_cast<const float4 *>(W + b * 256 + 8 * lane);
+        const float4 v0 = src[0], v1 = src[1];
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        float amax = 0.0f, vmax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float a = fabsf(v[i]);
+            if (a > amax) {
+                amax = a;
+                vmax = v[i];
+            }
+        }
+        // the group's first half (even lane) wins ties, as in a scan from 0
+        const float amax_o = __shfl_xor_sync(kFull, amax, 1);
+        const float vmax_o = __shfl_xor_sync(kFull, vmax, 1);
+        const bool first = (lane & 1) == 0;
+        const float a0 = first ? amax : amax_o, a1 = first ? amax_o : amax;
+        const float x0 = first ? vmax : vmax_o, x1 = first ? vmax_o : vmax;
+        const float vg = a1 > a0 ? x1 : x0;
+        const float sc = __fdiv_rn(vg, -32.0f);
+        const float max_sc = warp_max_nonneg(fabsf(sc));
+        const float d = __fdiv_rn(max_sc, 127.0f);
+        const __half d16 = __float2half_rn(d);
+        const int s = d > 0.0f ? clampi((int)round_half_away(__fdiv_rn(sc, d)), -127, 127) : 0;
+        const float D = __fmul_rn(__half2float(d16), (float)s);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int q = 0;
+            if (D != 0.0f) q = clampi((int)round_half_away(__fdiv_rn(v[i], D)), -32, 31);
+            const uint32_t u = (uint32_t)(q + 32);
+            if (i < 4)
+                lo |= u << (8 * i);
+            else
+                hi |= u << (8 * (i - 4));
+        }
+        *reinterpret_cast<uint2 *>(us + 8 * lane) = make_uint2(lo, hi);
+        __syncwarp();
+        uint8_t *blk = out + b * B_Q6_K;
+        uint32_t ql = 0;  // ql bytes 4 lane .. 4 lane + 3
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int idx = 4 * lane + k, c = idx >> 5, l = idx & 31;
+            ql |= (uint32_t)((us[64 * c + l] & 15) | ((us[64 * c + 32 + l] & 15) << 4)) << (8 * k);
+        }
+        uint32_t qh = 0;  // qh bytes 2 lane, 2 lane + 1
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int idx = 2 * lane + k, h = idx >> 5, l = idx & 31;
+            uint32_t byte = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) byte |= (uint32_t)(us[128 * h + 32 * i + l] >> 4) << (2 * i);
+            qh |= byte << (8 * k);
+        }
+        // 210-byte blocks: 2-byte stores only
+        reinterpret_cast<uint16_t *>(blk)[2 * lane] = (uint16_t)ql;
+        reinterpret_cast<uint16_t *>(blk)[2 * lane + 1] = (uint16_t)(ql >> 16);
+        reinterpret_cast<uint16_t *>(blk + 128)[lane] = (uint16_t)qh;
+        if (first) blk[192 + (lane >> 1)] = (uint8_t)(int8_t)s;
+        if (lane == 0) *reinterpret_cast<uint16_t *>(blk + 208) = __half_as_ushort(d16);
+        __syncwarp();  // us is rewritten by the next super-block
+    }
+}
+
 int grid_for(int64_t nwarp_items) {
     const int64_t ctas = (nwarp_items + 7) / 8;
     const int64_t cap = (int64_t)sm_count() * 16;
@@ -290,6 +373,9 @@ cudaError_t launch_quantize_weights(qmm_type wt, const float *W, void *Wq, int64
     if (wt == QMM_TYPE_Q4_0) {
         const int64_t nblocks = N * (K / QK4_0);
         quantize_q4_0_kernel<<<grid_for(nblocks), 256, 0, s>>>(W, o, nblocks);
+    } else if (wt == QMM_TYPE_Q6_K) {
+        const int64_t nblocks = N * (K / QK_K);
+        quantize_q6_K_kernel<<<grid_for(nblocks), 256, 0, s>>>(W, o, nblocks);
     } else {
         const int64_t nblocks = N * (K / QK_K);
         quantize_q4_K_kernel<<<grid_for(nblocks), 256, 0, s>>>(W, o, nblocks);

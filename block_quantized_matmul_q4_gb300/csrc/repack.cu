@@ -11,6 +11,9 @@
 //   Q4_0: canonical [N][nb][18 B]   -> per tile [8][nb][16 B nibbles] followed
 //         by [nb][8] fp16 scales, so the nibbles are 16-byte aligned (the
 //         18-byte block defeats 128-bit loads).
+//   Q6_K: canonical [N][nsb][210 B] -> records of 8 rows per (tile,
+//         super-block), [T][nsb][1680 B] (qmm_internal.cuh): ql unchanged,
+//         the high bits and the scales re-ordered for the GEMV lanes.
 // Padding rows (N not a multiple of 8) are zero blocks: d = 0 contributes 0.
 #include "qmm_internal.cuh"
 
@@ -92,6 +95,94 @@ __global__ void repack_q4_0_kernel(const uint8_t *__restrict__ src, uint8_t *__r
     }
 }
 
+// Canonical Q6_K high bits of element e (page 1's qh[64], in the order the
+// oracle states: qh[32 (e / 128) + e % 32] bits 2 ((e % 128) / 32)).
+__device__ __forceinline__ int q6k_qh_byte(int e) { return 32 * (e >> 7) + (e & 31); }
+__device__ __forceinline__ int q6k_qh_shift(int e) { return 2 * ((e & 127) >> 5); }
+
+// Q6_K: one thread per (row, super-block).
+template <bool kInverse>
+__global__ void repack_q6_K_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
+                                   int64_t N, int64_t nsb) {
+    const int64_t Npad = tiles_of(N) * kTileRows;
+    const int64_t total = Npad * nsb;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / nsb, sb = i % nsb;
+        const int r = (int)(n % kTileRows);
+        const int64_t rec_off = ((n / kTileRows) * nsb + sb) * kQ6Rec;
+        if (!kInverse) {
+            uint8_t *rec = dst + rec_off;
+            uint8_t ql[128], qh[64], sc[16];
+            uint16_t d = 0;
+            if (n < N) {
+                const uint8_t *c = src + (n * nsb + sb) * B_Q6_K;
+                for (int k = 0; k < 128; ++k) ql[k] = c[k];
+                for (int k = 0; k < 64; ++k) qh[k] = c[128 + k];
+                for (int k = 0; k < 16; ++k) sc[k] = c[192 + k];
+                d = *reinterpret_cast<const uint16_t *>(c + 208);
+            } else {
+                for (int k = 0; k < 128; ++k) ql[k] = 0;
+                for (int k = 0; k < 64; ++k) qh[k] = 0;
+                for (int k = 0; k < 16; ++k) sc[k] = 0;
+            }
+            uint8_t *row = rec + r * kQ6Codes;
+            for (int k = 0; k < 8; ++k) {
+                uint4 v;
+                v.x = ql[16 * k] | (ql[16 * k + 1] << 8) | (ql[16 * k + 2] << 16) | ((uint32_t)ql[16 * k + 3] << 24);
+                v.y = ql[16 * k + 4] | (ql[16 * k + 5] << 8) | (ql[16 * k + 6] << 16) | ((uint32_t)ql[16 * k + 7] << 24);
+                v.z = ql[16 * k + 8] | (ql[16 * k + 9] << 8) | (ql[16 * k + 10] << 16) | ((uint32_t)ql[16 * k + 11] << 24);
+                v.w = ql[16 * k + 12] | (ql[16 * k + 13] << 8) | (ql[16 * k + 14] << 16) | ((uint32_t)ql[16 * k + 15] << 24);
+                *reinterpret_cast<uint4 *>(row + 16 * k) = v;
+            }
+            for (int t = 0; t < 8; ++t) {
+                uint32_t h[2] = {0, 0};
+                for (int hi = 0; hi < 2; ++hi)
+                    for (int k = 0; k < 16; ++k) {
+                        const int e = q6k_elem(t, hi, k);
+                        h[hi] |= (uint32_t)((qh[q6k_qh_byte(e)] >> q6k_qh_shift(e)) & 3) << q6k_hbit_pos(k);
+                    }
+                *reinterpret_cast<uint2 *>(row + 128 + 8 * t) = make_uint2(h[0], h[1]);
+            }
+            uint8_t ps[16];
+            for (int t = 0; t < 8; ++t) {
+                ps[2 * t] = sc[q6k_elem(t, 0, 0) / 16];
+                ps[2 * t + 1] = sc[q6k_elem(t, 1, 0) / 16];
+            }
+            uint4 v;
+            v.x = ps[0] | (ps[1] << 8) | (ps[2] << 16) | ((uint32_t)ps[3] << 24);
+            v.y = ps[4] | (ps[5] << 8) | (ps[6] << 16) | ((uint32_t)ps[7] << 24);
+            v.z = ps[8] | (ps[9] << 8) | (ps[10] << 16) | ((uint32_t)ps[11] << 24);
+            v.w = ps[12] | (ps[13] << 8) | (ps[14] << 16) | ((uint32_t)ps[15] << 24);
+            *reinterpret_cast<uint4 *>(rec + kQ6ScOff + 16 * r) = v;
+            *reinterpret_cast<uint16_t *>(rec + kQ6DOff + 2 * r) = d;
+        } else if (n < N) {
+            const uint8_t *rec = src + rec_off;
+            const uint8_t *row = rec + r * kQ6Codes;
+            uint8_t *c = dst + (n * nsb + sb) * B_Q6_K;
+            for (int k = 0; k < 128; ++k) c[k] = row[k];
+            uint8_t qh[64];
+            for (int k = 0; k < 64; ++k) qh[k] = 0;
+            for (int t = 0; t < 8; ++t) {
+                const uint2 hw = *reinterpret_cast<const uint2 *>(row + 128 + 8 * t);
+                const uint32_t h[2] = {hw.x, hw.y};
+                for (int hi = 0; hi < 2; ++hi)
+                    for (int k = 0; k < 16; ++k) {
+                        const int e = q6k_elem(t, hi, k);
+                        qh[q6k_qh_byte(e)] |= (uint8_t)(((h[hi] >> q6k_hbit_pos(k)) & 3) << q6k_qh_shift(e));
+                    }
+            }
+            for (int k = 0; k < 64; ++k) c[128 + k] = qh[k];
+            const uint8_t *ps = rec + kQ6ScOff + 16 * r;
+            for (int t = 0; t < 8; ++t) {
+                c[192 + q6k_elem(t, 0, 0) / 16] = ps[2 * t];
+                c[192 + q6k_elem(t, 1, 0) / 16] = ps[2 * t + 1];
+            }
+            *reinterpret_cast<uint16_t *>(c + 208) = *reinterpret_cast<const uint16_t *>(rec + kQ6DOff + 2 * r);
+        }
+    }
+}
+
 int grid_1d(int64_t n, int threads) {
     const int64_t ctas = (n + threads - 1) / threads;
     const int64_t cap = (int64_t)sm_count() * 32;
@@ -110,6 +201,13 @@ cudaError_t launch_repack(qmm_type wt, bool inverse, const void *src, void *dst,
             repack_q4_K_kernel<true><<<grid, 256, 0, s>>>((const uint4 *)src, (uint4 *)dst, N, nsb);
         else
             repack_q4_K_kernel<false><<<grid, 256, 0, s>>>((const uint4 *)src, (uint4 *)dst, N, nsb);
+    } else if (wt == QMM_TYPE_Q6_K) {
+        const int64_t nsb = K / QK_K;
+        const int grid = grid_1d(Npad * nsb, 128);
+        if (inverse)
+            repack_q6_K_kernel<true><<<grid, 128, 0, s>>>((const uint8_t *)src, (uint8_t *)dst, N, nsb);
+        else
+            repack_q6_K_kernel<false><<<grid, 128, 0, s>>>((const uint8_t *)src, (uint8_t *)dst, N, nsb);
     } else {
         const int64_t nb = K / QK4_0;
         const int grid = grid_1d(Npad * nb, 256);

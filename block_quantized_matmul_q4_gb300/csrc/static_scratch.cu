@@ -53,9 +53,9 @@ using namespace qmm;
 extern "C" qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
                                          const float *X, int64_t M, float *Y,
                                          qmm_stream_t stream) {
-    if (wt != QMM_TYPE_Q4_0 && wt != QMM_TYPE_Q4_K)
-        return set_error(QMM_ERR_ARG, "weight type must be Q4_0 or Q4_K (got %d)", (int)wt);
-    const int qk = wt == QMM_TYPE_Q4_K ? QK_K : QK4_0;
+    if (wt != QMM_TYPE_Q4_0 && wt != QMM_TYPE_Q4_K && wt != QMM_TYPE_Q6_K)
+        return set_error(QMM_ERR_ARG, "weight type must be Q4_0, Q4_K or Q6_K (got %d)", (int)wt);
+    const int qk = wt == QMM_TYPE_Q4_0 ? QK4_0 : QK_K;
     if (N < 0 || M < 0 || K <= 0 || K % qk != 0 || K > ((int64_t)1 << 30) || N > ((int64_t)1 << 31))
         return set_error(QMM_ERR_ARG, "bad sizes N=%lld K=%lld M=%lld (K must be a multiple of %d)",
                          (long long)N, (long long)K, (long long)M, qk);
@@ -92,7 +92,7 @@ extern "C" qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int6
     }
     Planar p;
     planar_bytes(M, K, qk, &p, scratch);
-    const qmm_type at = wt == QMM_TYPE_Q4_K ? QMM_TYPE_Q8_K : QMM_TYPE_Q8_0;
+    const qmm_type at = wt == QMM_TYPE_Q4_0 ? QMM_TYPE_Q8_0 : QMM_TYPE_Q8_K;
     cudaError_t e = launch_quantize_q8(at, true, X, nullptr, p, M, K, s);
     if (e != cudaSuccess)
         return set_error(QMM_ERR_CUDA, "activation quantizer launch: %s", cudaGetErrorString(e));

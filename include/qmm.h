@@ -54,9 +54,13 @@ typedef enum {
     QMM_TYPE_Q4_K = 1, /* weights: 256 x 4-bit, 8 sub-blocks; w = d s_j q - dmin m_j  */
     QMM_TYPE_Q8_0 = 2, /* activations: 32 x int8, fp16 d;     a = d q                  */
     QMM_TYPE_Q8_K = 3, /* activations: 256 x int8, fp32 d, 16 sums of 16 codes        */
-    QMM_TYPE_W4A16 = 4 /* weights: 4-bit codes q, 8 per uint32 word; per row and group
+    QMM_TYPE_W4A16 = 4, /* weights: 4-bit codes q, 8 per uint32 word; per row and group
                           of G elements an fp16 scale s and a uint8 zero z:
                           w = s (q - z). Used by qmm_w4a16 only.               */
+    QMM_TYPE_Q6_K = 5   /* weights: 256 x 6-bit (ql[128] low 4 bits, qh[64] high 2),
+                          16 int8 scales, fp16 d; w = d s_j q, q in -32..31, no
+                          min (page 1, "更低的比特: Q6_K 与 Q2_K 的取舍"); 210 B.
+                          Activations Q8_K.                                    */
 } qmm_type;
 
 typedef enum {
@@ -71,8 +75,8 @@ typedef enum {
 
 /* ---------------------------------------------------------------- sizes */
 
-/* Bytes of one canonical block: 18, 144, 34, 292, and 4 for W4A16 (one
- * uint32 word of 8 codes); 0 for an invalid type.
+/* Bytes of one canonical block: 18, 144, 34, 292, 210 (Q6_K), and 4 for
+ * W4A16 (one uint32 word of 8 codes); 0 for an invalid type.
  * (Block layouts: page 1, "最基础的两块: Q4_0 与 Q8_0", "K-quant", "更低的比特";
  * W4A16: page 3, "位级打包".) */
 size_t qmm_block_bytes(qmm_type t);
@@ -81,14 +85,14 @@ size_t qmm_block_bytes(qmm_type t);
 int qmm_block_elems(qmm_type t);
 
 /* Bytes of the packed (repacked) weight buffer for an [N, K] weight of type
- * Q4_0, Q4_K or W4A16; 0 if the type or sizes are invalid. Q4_0/Q4_K rows
- * are padded to a multiple of 8 with zero blocks, W4A16 rows to a multiple
+ * Q4_0, Q4_K, Q6_K or W4A16; 0 if the type or sizes are invalid. Q4_0, Q4_K
+ * and Q6_K rows are padded to a multiple of 8 with zero blocks, W4A16 rows to a multiple
  * of 16 (K % 128 == 0): ceil(N / 16) * 16 * K / 2 bytes. */
 size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K);
 
 /* Bytes of the workspace qmm_mul_mat_ws needs for M activation rows of
- * length K against weights of type wt (Q4_0 or Q4_K); 0 if invalid. Above 16
- * tokens it ends with a partial area of about 20 MB: with more 128 x 128
+ * length K against weights of type wt (Q4_0, Q4_K or Q6_K); 0 if invalid.
+ * Above 16 tokens (Q4_0, Q4_K) it ends with a partial area of about 20 MB: with more 128 x 128
  * output tiles than SMs the tensor-core GEMM gives each SM an equal share of
  * the (tile, K-step) work (stream-K), and the parts of tiles that several
  * CTAs computed meet there before a second kernel adds them. */
@@ -108,8 +112,8 @@ size_t qmm_workspace_bytes(qmm_type wt, int64_t M, int64_t K);
 qmm_status qmm_quantize_row_q8(qmm_type vt, const float *X, void *Xq, int64_t M, int64_t K,
                                qmm_stream_t stream);
 
-/* Quantize fp32 weights W [N, K] into canonical blocks Wq of type wt (Q4_0 or
- * Q4_K) -- the offline quantizer's job, done on the GPU.
+/* Quantize fp32 weights W [N, K] into canonical blocks Wq of type wt (Q4_0,
+ * Q4_K or Q6_K) -- the offline quantizer's job, done on the GPU.
  * Q4_0 (page 1, "最基础的两块"): d = -x_max / 8 where x_max is the signed
  * value of largest magnitude (the first on ties); q = clamp(floor(x * (1/d)
  * + 8.5), 0, 15); d stored as fp16; byte l holds element l (low nibble) and
@@ -122,6 +126,13 @@ qmm_status qmm_quantize_row_q8(qmm_type vt, const float *X, void *Xq, int64_t M,
  * d16, dmin16; scales packed in 12 bytes, qs[32c + l] = q[64c + l] |
  * q[64c + 32 + l] << 4. The pages print the format but not the scale search;
  * this single-pass min/max search is this library's reading.
+ * Q6_K (page 1, "更低的比特"): per group j of 16: sc_j = -x_max,j / 32 (x_max,j
+ * the signed value of largest magnitude, the first on ties); d = max |sc_j|
+ * / 127 (fp16); s_j = clamp(round(sc_j / d), -127, 127) (int8); q =
+ * clamp(round(x / (d16 s_j)), -32, 31), stored u = q + 32 with
+ * ql[32c + l] = (u[64c + l] & 15) | (u[64c + 32 + l] & 15) << 4 and
+ * qh[32h + l] = sum_i (u[128h + 32i + l] >> 4) << 2i. The scale search and
+ * the bit order are this library's readings (the page gives the fields).
  * Bit-identical to the CPU oracle. Errors as qmm_quantize_row_q8. */
 qmm_status qmm_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N, int64_t K,
                                 qmm_stream_t stream);
@@ -134,7 +145,10 @@ qmm_status qmm_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N
  * contiguous; page 4 on GGML_CPU_REPACK). A pure byte permutation: rows are
  * grouped in tiles of 8 and, within a tile, blocks of the same K position are
  * adjacent; Q4_0 blocks are split into a 16-byte nibble plane and an fp16
- * scale plane. W_packed must not overlap W_canon.
+ * scale plane; Q6_K blocks of a tile and super-block form one 1680-byte
+ * record (8 x 192 bytes of codes, the high bits regrouped per 16-byte ql
+ * slice; 8 x 16 scale bytes, regrouped likewise; 8 fp16 d). W_packed must
+ * not overlap W_canon.
  * Errors: QMM_ERR_ARG for a non-weight type, N <= 0, K <= 0, K % QK != 0,
  * null or misaligned pointers. */
 qmm_status qmm_repack_weights(qmm_type wt, const void *W_canon, void *W_packed, int64_t N,
@@ -159,10 +173,11 @@ qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon
 
 /* Y [M, N] = W [N, K] . X [M, K]^T, the whole method (page 1, mul_mat steps
  * 1-3 and "正确性: 缩放系数可以提到求和号外面"): the activations are
- * quantized once per call to Q8_0 (for Q4_0 weights) or Q8_K (for Q4_K) in
- * the same stream, then every output is
+ * quantized once per call to Q8_0 (for Q4_0 weights) or Q8_K (for Q4_K and
+ * Q6_K) in the same stream, then every output is
  *   Q4_0: sum_b fp16(d_w) fp16(d_a) sum_{i<32} (q_i - 8) y_i
  *   Q4_K: sum_sb d_a (d * sum_j s_j sum_i q_i y_i - dmin * sum_j m_j sum_i y_i)
+ *   Q6_K: sum_sb d_a d sum_j s_j sum_i q_i y_i  (16 groups j of 16, no min)
  * with integer block sums and fp32 accumulation across blocks. Tokens are
  * processed 16 at a time by the decode GEMV kernels. When M*K is small (one
  * 16-token group of at most 8192 elements) the activation quantizer runs
@@ -300,11 +315,13 @@ qmm_status qmm_w4a16_unpack_zeros(const uint32_t *zeros_packed, uint8_t *zeros, 
 
 /* Per-block integer sums of the factored form, for bit-exact checking
  * (page 1, "正确性" and "通用实现"). Xq holds canonical activation blocks
- * (Q8_0 for Q4_0 weights, Q8_K for Q4_K), M rows.
+ * (Q8_0 for Q4_0 weights, Q8_K for Q4_K and Q6_K), M rows.
  *   Q4_0: out[(m * N + n) * (K/32) + b] = sum_{i<32} (q_i - 8) y_i
  *   Q4_K: out[((m * N + n) * (K/256) + sb) * 10 + t] with t = 0..7 the
  *         sub-block sums S_j = sum_i q_i y_i, t = 8 the scaled sum
  *         sum_j s_j S_j and t = 9 the min sum sum_j m_j (bs_2j + bs_2j+1).
+ *   Q6_K: out[((m * N + n) * (K/256) + sb) * 17 + t] with t = 0..15 the
+ *         group sums S_j = sum_i q_i y_i (q in -32..31), t = 16 sum_j s_j S_j.
  * Errors as qmm_mul_mat. */
 qmm_status qmm_debug_block_sums(qmm_type wt, const void *W_packed, int64_t N, int64_t K,
                                 const void *Xq, int64_t M, int32_t *out, qmm_stream_t stream);

@@ -46,6 +46,7 @@ def test_binding_names_match_header(built_lib):
 def test_block_sizes(lib):
     assert [lib.qmm_block_bytes(t) for t in range(4)] == [18, 144, 34, 292]
     assert [lib.qmm_block_elems(t) for t in range(4)] == [32, 256, 32, 256]
+    assert lib.qmm_block_bytes(5) == 210 and lib.qmm_block_elems(5) == 256  # Q6_K
     assert lib.qmm_block_bytes(7) == 0
 
 
@@ -56,6 +57,9 @@ def test_packed_and_workspace_sizes(lib):
     assert lib.qmm_packed_bytes(0, 256, 1024) == 256 * 32 * 18
     assert lib.qmm_packed_bytes(1, 10, 100) == 0  # K not a multiple of 256
     assert lib.qmm_packed_bytes(3, 10, 256) == 0  # activation type is not a weight type
+    assert lib.qmm_packed_bytes(5, 13, 512) == 16 * 2 * 210  # Q6_K: 8-row records of 1680 B
+    assert lib.qmm_packed_bytes(5, 8, 300) == 0
+    assert lib.qmm_workspace_bytes(5, 40, 4096) >= 40 * 4096 + 40 * 16 * 4 + 40 * 16 * 16 * 2
     ws = lib.qmm_workspace_bytes(1, 16, 4096)
     assert ws >= 16 * 4096 + 16 * 16 * 4 + 16 * 16 * 16 * 2
     assert lib.qmm_workspace_bytes(0, 1, 1000) == 0
