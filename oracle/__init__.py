@@ -88,6 +88,8 @@ def lib():
             L.orc_w4a16_unpack_zeros.argtypes = [vp, vp, i64, i64]
             L.orc_w4a16_matmul.argtypes = [vp, vp, vp, i64, vp, i64, i64, i64, vp, i64,
                                            vp, f64p, f64p, ctypes.c_int]
+            L.orc_w4a16_lut_matmul.argtypes = [vp, vp, vp, i64, vp, i64, i64, i64, vp, i64,
+                                               vp, f64p, f64p, ctypes.c_int]
             _lib = L
     return _lib
 
@@ -281,4 +283,24 @@ def w4a16_matmul(qweight, scales16, zeros, G: int, A16, rows=None, nthreads: int
     den = np.zeros((M, nrows), np.float64)
     lib().orc_w4a16_matmul(_ptr(qw), _ptr(s), _ptr(z), G, _ptr(A), M, N, K, _ptr(r), nrows,
                            _ptr(c16), _ptr(c64), _ptr(den), nthreads)
+    return {"c16": c16, "c64": c64, "den": den}
+
+
+def w4a16_lut_matmul(qweight, scales16, lut16, G: int, A16, rows=None, nthreads: int = 1):
+    """C [M, nrows] with W-hat = s * LUT(q): fp16 bits of the fp64 result, the
+    fp64 value and den."""
+    qw = _c(qweight, np.uint32)
+    s = _c(scales16, np.uint16)
+    lut = _c(lut16, np.uint16)
+    assert lut.shape == (16,)
+    A = _c(A16, np.uint16)
+    M, K = A.shape
+    N = qw.shape[0]
+    r = None if rows is None else _c(rows, np.int64)
+    nrows = N if r is None else r.shape[0]
+    c16 = np.zeros((M, nrows), np.uint16)
+    c64 = np.zeros((M, nrows), np.float64)
+    den = np.zeros((M, nrows), np.float64)
+    lib().orc_w4a16_lut_matmul(_ptr(qw), _ptr(s), _ptr(lut), G, _ptr(A), M, N, K, _ptr(r), nrows,
+                               _ptr(c16), _ptr(c64), _ptr(den), nthreads)
     return {"c16": c16, "c64": c64, "den": den}

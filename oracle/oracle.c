@@ -792,3 +792,42 @@ void orc_w4a16_matmul(const uint32_t *qweight, const uint16_t *scales, const uin
         free(wh);
     }
 }
+
+/* Non-uniform 4-bit codes ([P3] "从数学表达式到真实存储": for NF4-like
+ * formats q is an index into a code table, W-hat = s * LUT(q), no zero
+ * point). lut holds the 16 table values as fp16 bit patterns. Outputs as
+ * orc_w4a16_matmul. */
+void orc_w4a16_lut_matmul(const uint32_t *qweight, const uint16_t *scales, const uint16_t *lut,
+                          int64_t G, const uint16_t *A, int64_t M, int64_t N, int64_t K,
+                          const int64_t *rows, int64_t nrows, uint16_t *C16, double *C64,
+                          double *den, int nthreads) {
+    const int64_t ng = K / G;
+    if (!rows) nrows = N;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *wh = (double *)malloc(sizeof(double) * (size_t)K);
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < nrows; ++r) {
+            const int64_t n = rows ? rows[r] : r;
+            for (int64_t kk = 0; kk < K; ++kk) {
+                const int64_t g = kk / G;
+                const uint32_t u = qweight[n * (K / 8) + kk / 8];
+                const int q = (int)((u >> (4 * (kk % 8))) & 15u);
+                wh[kk] = (double)orc_fp16_to_fp32(scales[n * ng + g]) * (double)orc_fp16_to_fp32(lut[q]);
+            }
+            for (int64_t m = 0; m < M; ++m) {
+                double s = 0.0, sa = 0.0;
+                for (int64_t kk = 0; kk < K; ++kk) {
+                    const double t = (double)orc_fp16_to_fp32(A[m * K + kk]) * wh[kk];
+                    s += t;
+                    sa += fabs(t);
+                }
+                if (C64) C64[m * nrows + r] = s;
+                if (den) den[m * nrows + r] = sa;
+                if (C16) C16[m * nrows + r] = orc_fp64_to_fp16(s);
+            }
+        }
+        free(wh);
+    }
+}

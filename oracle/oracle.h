@@ -118,6 +118,12 @@ void orc_w4a16_matmul(const uint32_t *qweight, const uint16_t *scales, const uin
                       int64_t G, const uint16_t *A, int64_t M, int64_t N, int64_t K,
                       const int64_t *rows, int64_t nrows, uint16_t *C16, double *C64, double *den,
                       int nthreads);
+/* C[m,n] = sum_k A[m,k] * s[n,g] * LUT[q[n,k]] (NF4-like code table, no zero
+ * point); lut holds 16 fp16 bit patterns. Outputs as orc_w4a16_matmul. */
+void orc_w4a16_lut_matmul(const uint32_t *qweight, const uint16_t *scales, const uint16_t *lut,
+                          int64_t G, const uint16_t *A, int64_t M, int64_t N, int64_t K,
+                          const int64_t *rows, int64_t nrows, uint16_t *C16, double *C64,
+                          double *den, int nthreads);
 
 #ifdef __cplusplus
 }

@@ -553,6 +553,50 @@ def test_w4a16_matmul_against_numpy(orc):
     assert np.allclose(res["den"], den, rtol=1e-12)
 
 
+def test_w4a16_lut_reduces_to_zero_point(orc):
+    # the table LUT(q) = q - 8 is the zero-point form with every z = 8: the
+    # same products in fp64, so identical results
+    N, K, G, M = 7, 512, 128, 3
+    q, s, z, A = wl.w4a16_inputs(2, N, K, G, M)
+    qw = orc.w4a16_pack(q.numpy())
+    s16, A16 = s.numpy().view(np.uint16), A.numpy().view(np.uint16)
+    lut = (np.arange(16) - 8).astype(np.float16).view(np.uint16)
+    a = orc.w4a16_lut_matmul(qw, s16, lut, G, A16)
+    b = orc.w4a16_matmul(qw, s16, np.full((N, K // G), 8, np.uint8), G, A16)
+    for key in ("c16", "c64", "den"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_w4a16_lut_onehot_and_relabel(orc):
+    N, K, G = 5, 256, 128
+    q, s, _, _ = wl.w4a16_inputs(3, N, K, G, 1)
+    qn = q.numpy()
+    lut = wl.nf4_like_table().numpy()
+    qw = orc.w4a16_pack(qn)
+    s16 = s.numpy().view(np.uint16)
+    # a one-hot activation reads back s[n, k / G] * LUT[q[n, k]] for every row
+    for k in (0, 1, 7, 127, 128, 200, 255):
+        A = np.zeros((1, K), np.float16)
+        A[0, k] = 1.0
+        c = orc.w4a16_lut_matmul(qw, s16, lut.view(np.uint16), G, A.view(np.uint16))["c64"][0]
+        expect = s.numpy()[:, k // G].astype(np.float64) * lut[qn[:, k]].astype(np.float64)
+        assert np.array_equal(c, expect), k
+    # relabelling the codes and permuting the table alike changes nothing
+    A = wl.w4a16_inputs(3, N, K, G, 4)[3].numpy().view(np.uint16)
+    perm = np.array([(7 * i + 3) % 16 for i in range(16)])
+    lut2 = np.zeros(16, np.float16)
+    lut2[perm] = lut
+    a = orc.w4a16_lut_matmul(qw, s16, lut.view(np.uint16), G, A)
+    b = orc.w4a16_lut_matmul(orc.w4a16_pack(perm[qn].astype(np.uint8)), s16, lut2.view(np.uint16), G, A)
+    assert np.array_equal(a["c64"], b["c64"])
+
+
+def test_nf4_like_table_is_sorted_and_symmetric():
+    t = wl.nf4_like_table().numpy().astype(np.float64)
+    assert np.all(np.diff(t) > 0) and t[0] == -1.0 and t[-1] == 1.0
+    assert np.array_equal(t, -t[::-1])
+
+
 # --------------------------------------------------------------- edge cases
 @pytest.mark.parametrize("scale", [0.0, 1e-30, 1e-3, 1.0, 1e4])
 def test_edge_magnitudes(orc, scale):

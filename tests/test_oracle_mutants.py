@@ -35,6 +35,9 @@ MUTANTS = {
     "q6_K scale sign dropped": ("sc[j] = vmax / -32.0f;", "sc[j] = fabsf(vmax) / 32.0f;"),
     "q6_K activation scale dropped": ("acc += (y[b].d * orc_fp16_to_fp32(x[b].d)) * (float)isum;",
                                       "acc += orc_fp16_to_fp32(x[b].d) * (float)isum;"),
+    "w4a16 lut indexed by the wrong nibble": (
+        "wh[kk] = (double)orc_fp16_to_fp32(scales[n * ng + g]) * (double)orc_fp16_to_fp32(lut[q]);",
+        "wh[kk] = (double)orc_fp16_to_fp32(scales[n * ng + g]) * (double)orc_fp16_to_fp32(lut[q ^ 1]);"),
     "q4_0 zero point off by one": ("int q0 = clampi((int)floorf(v0 + 8.5f), 0, 15);",
                                    "int q0 = clampi((int)floorf(v0 + 7.5f), 0, 15);"),
 }

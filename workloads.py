@@ -196,6 +196,18 @@ W4A16_G = 128
 W4A16_M = (1, 16, 256)
 
 
+def nf4_like_table() -> torch.Tensor:
+    """A 16-entry code table for the non-uniform W4A16 form (W-hat = s LUT(q)):
+    the standard normal's quantiles at probabilities (i + 1/2) / 16, scaled so
+    the largest magnitude is 1, as fp16. Equal-probability levels, so codes of
+    normally distributed weights are uniform over 0..15 (the q recipe of
+    w4a16_inputs). An input table, not the method: any 16 values will do."""
+    from statistics import NormalDist
+    lv = [NormalDist().inv_cdf((i + 0.5) / 16) for i in range(16)]
+    m = max(abs(v) for v in lv)
+    return torch.tensor([v / m for v in lv], dtype=torch.float32).to(torch.float16)
+
+
 def w4a16_inputs(seed: int, N: int, K: int, G: int, M: int, rows=None, device="cpu"):
     """q [N, K] uint8 ~ U{0..15}; s [N, K/G] fp16 ~ U(0.005, 0.02); z [N, K/G]
     uint8 ~ U{0..15}; A [M, K] fp16 ~ N(0, 1). Returns (q, s16, z, A16)."""
