@@ -428,6 +428,19 @@ def w4a16_extras(q, dev, stream, reps=8, graph_steps=16):
         b = wbytes + 2 * M * K + 2 * M * N
         out[f"M{M}"] = {"us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
                         "TOPS": round(2.0 * M * N * K / t / 1e12, 2)}
+        # the same codes and scales through a 16-entry code table (NF4-like)
+        lut = wl.nf4_like_table().to(dev)
+        step = lambda i: q.qmm_w4a16_lut(sets[i % nset][0], sets[i % nset][1], lut, G, A, C, M, N, K,
+                                         stream)
+        for i in range(nset):
+            step(i)
+        g = capture(step, graph_steps, stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        t = timed(stream, lambda: run_graphs(g, None, reps)) / (reps * graph_steps)
+        b = Wp.numel() + s16.numel() * 2 + 32 + 2 * M * K + 2 * M * N
+        out[f"lut_M{M}"] = {"us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
+                            "TOPS": round(2.0 * M * N * K / t / 1e12, 2)}
     out["shape"] = {"N": N, "K": K, "G": G}
     return out
 

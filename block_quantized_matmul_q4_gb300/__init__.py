@@ -53,6 +53,7 @@ _SIGS = {
     "qmm_mul_mat_static": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_debug_block_sums": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_w4a16": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "qmm_w4a16_lut": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _vp]),
     "qmm_w4a16_unpack_zeros": (_i32, [_vp, _vp, _i64, _i64, _vp]),
     "qmm_debug_wait_timeout": (_i32, [_i64, _vp]),
     "qmm_status_string": (ctypes.c_char_p, [_i32]),
@@ -197,6 +198,14 @@ def qmm_w4a16(W_packed, scales, zeros, G: int, A, C, M: int, N: int, K: int, str
     _check("qmm_w4a16",
            _lib.qmm_w4a16(_ptr(W_packed), _ptr(scales), _ptr(zeros), G, _ptr(A), _ptr(C), M, N, K,
                           _stream(stream)))
+
+
+def qmm_w4a16_lut(W_packed, scales, lut, G: int, A, C, M: int, N: int, K: int, stream=None):
+    """C [M, N] fp16 = A [M, K] fp16 x W^T with W = s LUT(q): packed codes,
+    scales fp16 [N, K/G], a 16-entry fp16 code table; see include/qmm.h."""
+    _check("qmm_w4a16_lut",
+           _lib.qmm_w4a16_lut(_ptr(W_packed), _ptr(scales), _ptr(lut), G, _ptr(A), _ptr(C), M, N, K,
+                              _stream(stream)))
 
 
 def qmm_w4a16_unpack_zeros(zeros_packed, zeros, N: int, ngroups: int, stream=None):

@@ -589,44 +589,61 @@ qmm_status qmm_check_device_error(qmm_stream_t stream) {
 
 uint64_t qmm_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t *zeros, int64_t G,
-                     const uint16_t *A, uint16_t *C, int64_t M, int64_t N, int64_t K,
-                     qmm_stream_t stream) {
+// Both W4A16 forms: zeros != nullptr, W-hat = s (q - z); lut != nullptr,
+// W-hat = s LUT(q).
+static qmm_status w4a16_impl(const char *fn, const void *W_packed, const uint16_t *scales,
+                             const uint8_t *zeros, const uint16_t *lut, int64_t G, const uint16_t *A,
+                             uint16_t *C, int64_t M, int64_t N, int64_t K, qmm_stream_t stream) {
     QMM_CHECK_ARG(M >= 0 && N >= 0 && K > 0 && G > 0,
-                  "sizes must satisfy M, N >= 0, K, G > 0 (M=%lld N=%lld K=%lld G=%lld)",
+                  "%s: sizes must satisfy M, N >= 0, K, G > 0 (M=%lld N=%lld K=%lld G=%lld)", fn,
                   (long long)M, (long long)N, (long long)K, (long long)G);
-    QMM_CHECK_ARG(K % G == 0 && G % 8 == 0, "need K %% G == 0 and G %% 8 == 0 (K=%lld G=%lld)",
-                  (long long)K, (long long)G);
+    QMM_CHECK_ARG(K % G == 0 && G % 8 == 0, "%s: need K %% G == 0 and G %% 8 == 0 (K=%lld G=%lld)",
+                  fn, (long long)K, (long long)G);
     QMM_CHECK_ARG(K <= ((int64_t)1 << 30) && N <= ((int64_t)1 << 31) && M <= ((int64_t)1 << 31),
-                  "sizes too large");
+                  "%s: sizes too large", fn);
     if (G % 128 != 0)
-        return set_error(QMM_ERR_UNSUPPORTED, "W4A16 group size %lld: this build needs G %% 128 == 0",
+        return set_error(QMM_ERR_UNSUPPORTED, "%s: group size %lld: this build needs G %% 128 == 0", fn,
                          (long long)G);
     if (M == 0 || N == 0) return ok();
-    QMM_CHECK_ARG(W_packed && scales && zeros && A && C, "null pointer argument");
+    QMM_CHECK_ARG(W_packed && scales && (zeros || lut) && A && C, "%s: null pointer argument", fn);
     QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(A, 16) && aligned(scales, 16) &&
-                      aligned(zeros, 16),
-                  "W_packed, scales, zeros and A must be 16-byte aligned");
-    QMM_CHECK_ARG(aligned(C, 2), "C must be 2-byte aligned");
+                      (lut ? aligned(lut, 2) : aligned(zeros, 16)),
+                  "%s: W_packed, scales, zeros and A must be 16-byte aligned, lut 2-byte", fn);
+    QMM_CHECK_ARG(aligned(C, 2), "%s: C must be 2-byte aligned", fn);
     if (K / G > 256)
-        return set_error(QMM_ERR_UNSUPPORTED, "W4A16 with %lld groups per row: this build stages "
-                         "at most 256 (K / G)", (long long)(K / G));
+        return set_error(QMM_ERR_UNSUPPORTED, "%s: %lld groups per row: this build stages "
+                         "at most 256 (K / G)", fn, (long long)(K / G));
     cudaStream_t s = (cudaStream_t)stream;
     const __half *S = reinterpret_cast<const __half *>(scales);
+    const __half *L = reinterpret_cast<const __half *>(lut);
     const __half *Ah = reinterpret_cast<const __half *>(A);
     __half *Ch = reinterpret_cast<__half *>(C);
     // up to 16 tokens: the decode kernel (HBM-bound); more: the tensor-core
     // GEMM, whose split tiles go through a stream-ordered partial area
     if (M <= 16)
-        return cuda_status(launch_w4a16_decode(W_packed, S, zeros, G, Ah, Ch, M, N, K, s),
+        return cuda_status(launch_w4a16_decode(W_packed, S, zeros, L, G, Ah, Ch, M, N, K, s),
                            "W4A16 kernel launch");
     if (!stream_k_splits(N, M))  // one CTA per tile: no partial area
-        return cuda_status(launch_w4a16_gemm(W_packed, S, zeros, G, Ah, Ch, M, N, K, nullptr, s),
+        return cuda_status(launch_w4a16_gemm(W_packed, S, zeros, L, G, Ah, Ch, M, N, K, nullptr, s),
                            "W4A16 kernel launch");
     return with_own_part(s, [&](float *part) {
-        return cuda_status(launch_w4a16_gemm(W_packed, S, zeros, G, Ah, Ch, M, N, K, part, s),
+        return cuda_status(launch_w4a16_gemm(W_packed, S, zeros, L, G, Ah, Ch, M, N, K, part, s),
                            "W4A16 kernel launch");
     });
+}
+
+qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t *zeros, int64_t G,
+                     const uint16_t *A, uint16_t *C, int64_t M, int64_t N, int64_t K,
+                     qmm_stream_t stream) {
+    if (M > 0 && N > 0 && !zeros) return set_error(QMM_ERR_ARG, "qmm_w4a16: null pointer argument");
+    return w4a16_impl("qmm_w4a16", W_packed, scales, zeros, nullptr, G, A, C, M, N, K, stream);
+}
+
+qmm_status qmm_w4a16_lut(const void *W_packed, const uint16_t *scales, const uint16_t *lut, int64_t G,
+                         const uint16_t *A, uint16_t *C, int64_t M, int64_t N, int64_t K,
+                         qmm_stream_t stream) {
+    if (M > 0 && N > 0 && !lut) return set_error(QMM_ERR_ARG, "qmm_w4a16_lut: null pointer argument");
+    return w4a16_impl("qmm_w4a16_lut", W_packed, scales, nullptr, lut, G, A, C, M, N, K, stream);
 }
 
 }  // extern "C"

@@ -51,7 +51,8 @@ constexpr int kConvWarps = 8, kEpiWarps = 4;
 constexpr int kThreads = (3 + kConvWarps + kEpiWarps) * 32;
 constexpr int kOffAct = 0;
 constexpr int kOffW = kOffAct + kActStages * kActBytes;
-constexpr int kOffBar = kOffW + kWStages * kWBytesMax;
+constexpr int kOffLut = kOffW + kWStages * kWBytesMax;  // W4A16 code table: 256 fp16 pairs
+constexpr int kOffBar = kOffLut + 1024;
 constexpr int kNumBars = 2 * (kWStages + kActStages + kGroups) + 5;  // + acc_full[2], acc_empty[2], done
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -75,7 +76,8 @@ struct FmtInfo {
 
 struct Args {
     const __half *S;   // W4A16: [N][ng]
-    const uint8_t *Z;  // W4A16: [N][ng]
+    const uint8_t *Z;  // W4A16: [N][ng], unused with a table
+    const __half *lut; // W4A16: 16 fp16 code values (W-hat = s LUT(q)), or null
     void *C;           // W4A16: fp16 [M][N]; Q4_0: fp32 [M][N]
     int64_t M, N, K;
     int ng, spg;  // W4A16: groups per row, 128-element steps per group
@@ -124,6 +126,22 @@ __device__ __forceinline__ void scaled_word(uint32_t w, uint32_t zz, uint32_t zh
     f8 = hmul2_u(hsub2_u(lop_or(v, 0x000F000Fu), zz), ss);
     f4 = hmul2_u(hfma2_u(lop_or(w, 0x00F000F0u), kSixteenth, zh), ss);
     f12 = hmul2_u(hfma2_u(lop_or(v, 0x00F000F0u), kSixteenth, zh), ss);
+}
+
+// fp16 scale * LUT(q) for the 8 codes of one word (non-uniform codes, page
+// 3: W-hat = s LUT(q)), the pairs (k0,k1), (k2,k3), (k4,k5), (k6,k7) in that
+// order: slots j and j + 4 of the word hold elements 2j and 2j + 1, so one
+// byte q_2j | q_2j+1 << 4 per pair indexes the table tbl[i] = (LUT[i & 15],
+// LUT[i >> 4]). One rounding, the product with the scale.
+__device__ __forceinline__ void lut_scaled_word(uint32_t w, const uint32_t *tbl, uint32_t ss,
+                                                uint32_t &p01, uint32_t &p23, uint32_t &p45,
+                                                uint32_t &p67) {
+    const uint32_t t = (w & 0x0F0Fu) | ((w >> 12) & 0xF0F0u);          // pairs (0,1), (4,5)
+    const uint32_t t2 = ((w >> 4) & 0x0F0Fu) | ((w >> 16) & 0xF0F0u);  // pairs (2,3), (6,7)
+    p01 = hmul2_u(tbl[t & 0xFF], ss);
+    p45 = hmul2_u(tbl[(t >> 8) & 0xFF], ss);
+    p23 = hmul2_u(tbl[t2 & 0xFF], ss);
+    p67 = hmul2_u(tbl[(t2 >> 8) & 0xFF], ss);
 }
 
 // Columns m0 .. m0+15 of output row n (C is [M][N]: fp16 for W4A16, fp32 for
@@ -184,6 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(done), 1);
         fence_barrier_init();
+    }
+    uint32_t *pair_tbl = reinterpret_cast<uint32_t *>(smem + kOffLut);
+    if (F == kW4A16 && a.lut) {
+        // the table is weight data, like the scales: ready before the launch
+        for (int i = threadIdx.x; i < 256; i += kThreads)
+            pair_tbl[i] = (uint32_t)__half_as_ushort(a.lut[i & 15]) |
+                          ((uint32_t)__half_as_ushort(a.lut[i >> 4]) << 16);
     }
     __syncwarp();  // warps meet converged at every CTA barrier below
     if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -348,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         int64_t step = 2 * sb + sl;
                         if (step >= nsteps) step = nsteps - 1;  // past K the activations are zero
                         const int grp = a.spg == 1 ? (int)step : (int)step / a.spg;
-                        const uint32_t zv = a.Z[nc * a.ng + grp];
+                        const uint32_t zv = a.lut ? 0u : (uint32_t)a.Z[nc * a.ng + grp];
                         const uint32_t sv = (uint32_t)__half_as_ushort(a.S[nc * a.ng + grp]);
                         const uint32_t zz = 0x64006400u + zv * 0x00010001u;  // fp16 1024 + z twice
                         const uint32_t zh = 0xD400D400u + zv * 0x00100010u;  // fp16 -(64 + z) twice
@@ -358,12 +383,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint4 w0 = *reinterpret_cast<const uint4 *>(src);
                         const uint4 w1 = *reinterpret_cast<const uint4 *>(src + 16);
                         const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        if (a.lut) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            // W4A16 word: (k0,k1) at 0|16, (k2,k3) at 4|20, (k4,k5) at 8|24, (k6,k7) at 12|28
-                            scaled_word(wv[i], zz, zh, ss, lo[4 * i], lo[4 * i + 2], lo[4 * i + 1], lo[4 * i + 3]);
-                            scaled_word(wv[i + 4], zz, zh, ss, hi[4 * i], hi[4 * i + 2], hi[4 * i + 1],
-                                        hi[4 * i + 3]);
+                            for (int i = 0; i < 4; ++i) {
+                                lut_scaled_word(wv[i], pair_tbl, ss, lo[4 * i], lo[4 * i + 1], lo[4 * i + 2],
+                                                lo[4 * i + 3]);
+                                lut_scaled_word(wv[i + 4], pair_tbl, ss, hi[4 * i], hi[4 * i + 1],
+                                                hi[4 * i + 2], hi[4 * i + 3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                // W4A16 word: (k0,k1) at 0|16, (k2,k3) at 4|20, (k4,k5) at 8|24, (k6,k7) at 12|28
+                                scaled_word(wv[i], zz, zh, ss, lo[4 * i], lo[4 * i + 2], lo[4 * i + 1],
+                                            lo[4 * i + 3]);
+                                scaled_word(wv[i + 4], zz, zh, ss, hi[4 * i], hi[4 * i + 2], hi[4 * i + 1],
+                                            hi[4 * i + 3]);
+                            }
                         }
                     } else {
                         // chunk c = blocks 2c, 2c + 1 of the round. Byte l of a block
@@ -577,12 +613,13 @@ cudaError_t launch_import_q4_0_prefill(const void *Xq, void *ws, int64_t M, int6
     return cudaGetLastError();
 }
 
-cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, int64_t G,
+cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, const __half *lut, int64_t G,
                               const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
                               float *part, cudaStream_t s) {
     Args a;
     a.S = S;
     a.Z = Z;
+    a.lut = lut;
     a.C = C;
     a.M = M;
     a.N = N;
@@ -624,6 +661,7 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
     Args a;
     a.S = nullptr;
     a.Z = nullptr;
+    a.lut = nullptr;
     a.C = Y;
     a.M = M;
     a.N = N;

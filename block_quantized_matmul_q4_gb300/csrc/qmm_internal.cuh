@@ -478,11 +478,12 @@ cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, 
 // kernel (M <= 16) and the tensor-core GEMM (M > 16).
 cudaError_t launch_w4a16_repack(bool inverse, const void *src, void *dst, int64_t N, int64_t K,
                                 cudaStream_t s);
-cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z, int64_t G,
-                                const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
+// lut == nullptr: W-hat = s (q - z); otherwise W-hat = s LUT(q) (Z unused).
+cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z, const __half *lut,
+                                int64_t G, const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
                                 cudaStream_t s);
-cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, int64_t G,
-                              const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
+cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, const __half *lut,
+                              int64_t G, const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
                               float *part, cudaStream_t s);
 cudaError_t launch_w4a16_unpack_zeros(const uint32_t *zp, uint8_t *z, int64_t N, int64_t ng,
                                       cudaStream_t s);

@@ -2,7 +2,9 @@
 // "从数学表达式到真实存储" and "位级打包"):
 //   C[m, n] = sum_k A[m, k] * s[n, g] * (q[n, k] - z[n, g]),  g = k / G,
 // with A and C fp16, q 4-bit codes (8 per uint32 word, element 8c + i in
-// bits 4i of word c), s fp16 and z uint8 per (row, group).
+// bits 4i of word c), s fp16 and z uint8 per (row, group); or, for
+// non-uniform codes like NF4 (same section), W-hat = s LUT(q) with a
+// 16-entry fp16 table and no zero point.
 //
 // Layout (qmm_repack_weights, QMM_TYPE_W4A16): rows in tiles of 16 (the
 // last one padded with zero rows); a tile is stored step by step, each
@@ -77,6 +79,21 @@ __device__ __forceinline__ void dequant_word(uint32_t w, const Zero2 &z, uint32_
     p67 = hfma2_u(lop_or(v, 0x00F000F0u), kSixteenth, z.zh);
 }
 
+// LUT(q) for the 8 codes of one packed word as the same four fp16 pairs.
+// Slots j and j + 4 hold the pair (k, k + 1) = (2j, 2j + 1): one byte
+// index q_k | q_k+1 << 4 per pair (two per word in t, two in t2) into the
+// 256-entry pair table tbl[i] = (LUT[i & 15], LUT[i >> 4]). Values of the
+// table are exact fp16, so the MMA products stay exact in fp32.
+__device__ __forceinline__ void lut_word(uint32_t w, const uint32_t *tbl, uint32_t &p01,
+                                         uint32_t &p23, uint32_t &p45, uint32_t &p67) {
+    const uint32_t t = (w & 0x0F0Fu) | ((w >> 12) & 0xF0F0u);          // pairs (0,1), (4,5)
+    const uint32_t t2 = ((w >> 4) & 0x0F0Fu) | ((w >> 16) & 0xF0F0u);  // pairs (2,3), (6,7)
+    p01 = tbl[t & 0xFF];
+    p45 = tbl[(t >> 8) & 0xFF];
+    p23 = tbl[t2 & 0xFF];
+    p67 = tbl[(t2 >> 8) & 0xFF];
+}
+
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -93,7 +110,8 @@ __device__ __forceinline__ void consumers_sync() {
 struct DecodeArgs {
     const uint8_t *W;  // packed, tile-major
     const __half *S;   // [N][K/G]
-    const uint8_t *Z;  // [N][K/G]
+    const uint8_t *Z;  // [N][K/G]; unused with a table
+    const __half *lut; // 16 fp16 code values (W-hat = s LUT(q)), or null
     const __half *A;   // [M][K]
     __half *C;         // [M][N]
     int64_t M, N, K, G;
@@ -106,7 +124,7 @@ struct DecodeArgs {
 // What one thread needs for one step besides the weights: its 32 activation
 // elements of token t/4 (and t/4 + 8 for the second N tile), the scales of
 // rows r0, r1 and their zeros as the fp16 constants of dequant_word.
-template <int NT>
+template <int NT, bool kLut>
 struct Operands {
     uint4 x[NT][4];
     float s0, s1;
@@ -115,11 +133,11 @@ struct Operands {
 
 // xq[nt]: this thread's 32 activation elements of the step (shared or global
 // memory, generic addressing).
-template <int NT>
+template <int NT, bool kLut>
 __device__ __forceinline__ void load_ops(const DecodeArgs &a, const __half *const (&xq)[NT],
                                          const __half *s_r0, const __half *s_r1,
                                          const uint8_t *z_r0, const uint8_t *z_r1, int st,
-                                         Operands<NT> &P) {
+                                         Operands<NT, kLut> &P) {
     const int g = a.spg == 1 ? st : st / a.spg;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -127,16 +145,18 @@ __device__ __forceinline__ void load_ops(const DecodeArgs &a, const __half *cons
         for (int q = 0; q < 4; ++q) P.x[nt][q] = *reinterpret_cast<const uint4 *>(xq[nt] + 8 * q);
     P.s0 = __half2float(s_r0[g * kRowsPerTile]);
     P.s1 = __half2float(s_r1[g * kRowsPerTile]);
-    P.z0 = make_zero2(z_r0[g * kRowsPerTile]);
-    P.z1 = make_zero2(z_r1[g * kRowsPerTile]);
+    if (!kLut) {
+        P.z0 = make_zero2(z_r0[g * kRowsPerTile]);
+        P.z1 = make_zero2(z_r1[g * kRowsPerTile]);
+    }
 }
 
 // One 128-element step of rows r0, r1 against tokens t/4 (+8): 8 (or 16)
 // MMAs on exact q - z, scaled by s once in fp32. Two accumulator chains
 // (even and odd words) halve the dependent MMA latency.
-template <int NT>
-__device__ __forceinline__ void step_mma(const Operands<NT> &P, const uint8_t *wrow, int tok, int j,
-                                         float (&tot)[NT][4]) {
+template <int NT, bool kLut>
+__device__ __forceinline__ void step_mma(const Operands<NT, kLut> &P, const uint32_t *tbl,
+                                         const uint8_t *wrow, int tok, int j, float (&tot)[NT][4]) {
     const uint4 wv0 = *reinterpret_cast<const uint4 *>(wrow + tok * 64 + 16 * j);
     const uint4 wv1 = *reinterpret_cast<const uint4 *>(wrow + (tok + 8) * 64 + 16 * j);
     const uint32_t w0[4] = {wv0.x, wv0.y, wv0.z, wv0.w};
@@ -152,8 +172,13 @@ __device__ __forceinline__ void step_mma(const Operands<NT> &P, const uint8_t *w
     for (int wi = 0; wi < 4; ++wi) {
         // (q - z) pairs of row r0 (u*) and row r1 (v*) for this word
         uint32_t u01, u23, u45, u67, v01, v23, v45, v67;
-        dequant_word(w0[wi], P.z0, u01, u23, u45, u67);
-        dequant_word(w1[wi], P.z1, v01, v23, v45, v67);
+        if (kLut) {
+            lut_word(w0[wi], tbl, u01, u23, u45, u67);
+            lut_word(w1[wi], tbl, v01, v23, v45, v67);
+        } else {
+            dequant_word(w0[wi], P.z0, u01, u23, u45, u67);
+            dequant_word(w1[wi], P.z1, v01, v23, v45, v67);
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const uint4 xv = P.x[nt][wi];
@@ -174,11 +199,12 @@ __device__ __forceinline__ void step_mma(const Operands<NT> &P, const uint8_t *w
     }
 }
 
-template <int NT>
+template <int NT, bool kLut>
 __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
     w4a16_decode_kernel(const DecodeArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ float red[kDecodeWarps][NT][4][32];
+    __shared__ uint32_t pair_tbl[kLut ? 256 : 1];  // (LUT[i & 15], LUT[i >> 4]) as fp16 pairs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t ntiles = (a.N + kRowsPerTile - 1) / kRowsPerTile;
     const int64_t tb = (int64_t)blockIdx.x * ntiles / gridDim.x;
@@ -189,8 +215,8 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
     // a tile's scales (16 rows x ng fp16) and zeros (16 x ng bytes), contiguous
     // in global memory and in its shared-memory slot
     const uint32_t s_bytes = (uint32_t)kRowsPerTile * (uint32_t)a.ng * 2u;
-    const uint32_t z_bytes = (uint32_t)kRowsPerTile * (uint32_t)a.ng;
-    const uint32_t sz_slot = s_bytes + z_bytes;  // multiple of 48
+    const uint32_t z_bytes = kLut ? 0u : (uint32_t)kRowsPerTile * (uint32_t)a.ng;
+    const uint32_t sz_slot = s_bytes + z_bytes;  // multiple of 32
     constexpr uint32_t ring_bytes = (uint32_t)S * kDStageBytes;
 
     // shared memory: weight ring | activations | scale/zero slots | barriers
@@ -216,6 +242,12 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
         }
         mbar_init(smem_u32(actb), 1);
         fence_barrier_init();
+    }
+    if (kLut) {
+        // the table is weight data, like the scales: ready before the launch
+        for (int i = threadIdx.x; i < 256; i += kDecodeThreads)
+            pair_tbl[i] = (uint32_t)__half_as_ushort(a.lut[i & 15]) |
+                          ((uint32_t)__half_as_ushort(a.lut[i >> 4]) << 16);
     }
     __syncthreads();
 
@@ -245,10 +277,11 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
                     // before its arrival publishes the slot
                     const int64_t rows = a.N - tile * kRowsPerTile < kRowsPerTile
                                              ? a.N - tile * kRowsPerTile : kRowsPerTile;
-                    const uint32_t sb = (uint32_t)rows * (uint32_t)a.ng * 2u, zb = (uint32_t)rows * (uint32_t)a.ng;
+                    const uint32_t sb = (uint32_t)rows * (uint32_t)a.ng * 2u;
+                    const uint32_t zb = kLut ? 0u : (uint32_t)rows * (uint32_t)a.ng;
                     const uint32_t sb16 = sb & ~15u, zb16 = zb & ~15u;
                     const uint8_t *ssrc = reinterpret_cast<const uint8_t *>(a.S + tile * kRowsPerTile * a.ng);
-                    const uint8_t *zsrc = a.Z + tile * kRowsPerTile * a.ng;
+                    const uint8_t *zsrc = kLut ? nullptr : a.Z + tile * kRowsPerTile * a.ng;
                     uint8_t *dst = sz_sm + zs * sz_slot;
                     for (uint32_t b = sb16; b < sb; ++b) dst[b] = ssrc[b];
                     for (uint32_t b = zb16; b < zb; ++b) dst[s_bytes + b] = zsrc[b];
@@ -317,7 +350,7 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
             for (int i = threadIdx.x; i < kRowsPerTile * a.ng; i += kDecodeWarps * 32) {
                 const int r = i / a.ng, g = i - r * a.ng;
                 s_tr[g * kRowsPerTile + r] = s_all[i];
-                z_tr[g * kRowsPerTile + r] = z_all[i];
+                if (!kLut) z_tr[g * kRowsPerTile + r] = z_all[i];
             }
             consumers_sync();
             if (lane == 0) mbar_arrive(smem_u32(&szempty[zs]));  // slot free again
@@ -334,13 +367,13 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
         // it computes step k it has the operands of step k + 1 in flight (two
         // register sets, alternating).
         const int nk = warp < nsteps ? (int)((nsteps - 1 - warp) / kDecodeWarps) + 1 : 0;
-        Operands<NT> P[2];
-        auto ops = [&](int k, Operands<NT> &Q) {
+        Operands<NT, kLut> P[2];
+        auto ops = [&](int k, Operands<NT, kLut> &Q) {
             const int64_t st = warp + (int64_t)k * kDecodeWarps;
             const __half *xq[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) xq[nt] = xs + (int64_t)mt[nt] * a.K + st * kStepK + 32 * j;
-            load_ops<NT>(a, xq, s_r0, s_r1, z_r0, z_r1, (int)st, Q);
+            load_ops<NT, kLut>(a, xq, s_r0, s_r1, z_r0, z_r1, (int)st, Q);
         };
         if (nk > 0) ops(0, P[0]);
         for (int64_t sg = 0; sg < spt; ++sg, ++it) {
@@ -351,7 +384,8 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
                 const int k = (int)sg * kps + h;
                 if (k < nk) {
                     if (k + 1 < nk) ops(k + 1, P[(h + 1) & 1]);
-                    step_mma<NT>(P[h & 1], stage + (warp + h * kDecodeWarps) * 1024, tok, j, tot);
+                    step_mma<NT, kLut>(P[h & 1], pair_tbl, stage + (warp + h * kDecodeWarps) * 1024, tok, j,
+                                       tot);
                 }
             }
             __syncwarp();
@@ -440,13 +474,22 @@ cudaError_t launch_w4a16_repack(bool inverse, const void *src, void *dst, int64_
     return cudaGetLastError();
 }
 
-cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z, int64_t G,
-                                const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
+template <int NT, bool kLut>
+cudaError_t launch_decode_nt(const DecodeArgs &a, int64_t grid, size_t smem, cudaStream_t s) {
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(w4a16_decode_kernel<NT, kLut>), (int)smem);
+    if (e != cudaSuccess) return e;
+    w4a16_decode_kernel<NT, kLut><<<(unsigned)grid, kDecodeThreads, smem, s>>>(a);
+    return cudaSuccess;
+}
+
+cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z, const __half *lut,
+                                int64_t G, const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
                                 cudaStream_t s) {
     DecodeArgs a;
     a.W = static_cast<const uint8_t *>(W);
     a.S = S;
     a.Z = Z;
+    a.lut = lut;
     a.A = A;
     a.C = C;
     a.M = M;
@@ -465,15 +508,11 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
     const int64_t grid = balanced_grid(ntiles, (M <= 8 ? 2 : 1) * (int64_t)sm_count());
     const size_t smem = (size_t)kDStages * kDStageBytes + a.act_bytes + sz + bars;
     cudaError_t e;
-    if (M <= 8) {
-        e = ensure_smem_attr(reinterpret_cast<const void *>(w4a16_decode_kernel<1>), smem);
-        if (e != cudaSuccess) return e;
-        w4a16_decode_kernel<1><<<(unsigned)grid, kDecodeThreads, smem, s>>>(a);
-    } else {
-        e = ensure_smem_attr(reinterpret_cast<const void *>(w4a16_decode_kernel<2>), smem);
-        if (e != cudaSuccess) return e;
-        w4a16_decode_kernel<2><<<(unsigned)grid, kDecodeThreads, smem, s>>>(a);
-    }
+    if (M <= 8)
+        e = lut ? launch_decode_nt<1, true>(a, grid, smem, s) : launch_decode_nt<1, false>(a, grid, smem, s);
+    else
+        e = lut ? launch_decode_nt<2, true>(a, grid, smem, s) : launch_decode_nt<2, false>(a, grid, smem, s);
+    if (e != cudaSuccess) return e;
     count_launch();
     return cudaGetLastError();
 }

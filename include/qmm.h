@@ -16,20 +16,22 @@
  * Conventions for every entry point
  *   - Pointers are DEVICE pointers unless the argument says "host".
  *   - W is [N, K]: N output rows of K/QK blocks each (QK = 32 for Q4_0 and
- *     Q8_0, 256 for Q4_K and Q8_K). X is fp32 [M, K] row-major. Y is fp32
+ *     Q8_0, 256 for Q4_K, Q6_K and Q8_K). X is fp32 [M, K] row-major. Y is fp32
  *     [M, N] row-major: Y[m * N + n] = sum_k W[n, k] X[m, k].
  *   - "Canonical" blocks are the packed little-endian structs the page prints
  *     (no padding): block_q4_0 {fp16 d; u8 qs[16]} 18 B; block_q8_0 {fp16 d;
  *     i8 qs[32]} 34 B; block_q4_K {fp16 d; fp16 dmin; u8 scales[12];
- *     u8 qs[128]} 144 B; block_q8_K {f32 d; i8 qs[256]; i16 bsums[16]} 292 B.
+ *     u8 qs[128]} 144 B; block_q8_K {f32 d; i8 qs[256]; i16 bsums[16]} 292 B;
+ *     block_q6_K {u8 ql[128]; u8 qh[64]; i8 scales[16]; fp16 d} 210 B
+ *     (field order as the page lists them; bit order in qmm_quantize_weights).
  *     A row of K elements is K/QK consecutive blocks; rows are consecutive.
  *     This is the interchange format. "Packed" weights are this library's
  *     private GPU layout, made from canonical blocks by qmm_repack_weights.
  *   - The caller owns every buffer; the library never frees caller memory.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
  *     no call synchronizes the host except qmm_check_device_error.
- *   - Device buffers must be 16-byte aligned, except canonical Q4_0/Q8_0
- *     buffers (18/34-byte blocks), which need 2-byte alignment.
+ *   - Device buffers must be 16-byte aligned, except canonical Q4_0/Q8_0/Q6_K
+ *     buffers (18/34/210-byte blocks), which need 2-byte alignment.
  *   - Errors: arguments are validated before anything is enqueued; on any
  *     error nothing is launched and a qmm_status other than QMM_OK is
  *     returned (qmm_last_error() gives a one-line reason). Kernels never trap:
@@ -299,6 +301,23 @@ qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int64_t N, int6
 qmm_status qmm_w4a16(const void *W_packed, const uint16_t *scales, const uint8_t *zeros, int64_t G,
                      const uint16_t *A, uint16_t *C, int64_t M, int64_t N, int64_t K,
                      qmm_stream_t stream);
+
+/* W4A16 with non-uniform 4-bit codes (page 3, "从数学表达式到真实存储": for
+ * NF4-like formats q indexes a code table, W-hat = s LUT(q), one more table
+ * lookup after the bit extraction, no zero point):
+ *   C[m, n] = sum_k A[m, k] * s[n, k/G] * LUT[q[n, k]]
+ * lut: device pointer to the 16 table values as fp16 bit patterns (2-byte
+ * aligned), read by every launch like the weights and scales (it must be
+ * written before the call is issued on `stream`). Weights, scales, A and C
+ * as qmm_w4a16; the same packed codes serve both forms.
+ * Arithmetic: table values are exact fp16, so every product A LUT(q) is
+ * exact in fp32. M <= 16: fp32 sums over each 128-element step, times s in
+ * fp32. M > 16: s LUT(q) rounded once to fp16, tensor cores, fp32
+ * accumulation. C is the fp32 sum rounded to fp16.
+ * Errors, sizes and the partial area as qmm_w4a16. */
+qmm_status qmm_w4a16_lut(const void *W_packed, const uint16_t *scales, const uint16_t *lut, int64_t G,
+                         const uint16_t *A, uint16_t *C, int64_t M, int64_t N, int64_t K,
+                         qmm_stream_t stream);
 
 /* W4A16 zero points stored 4-bit packed (page 3, "从数学表达式到真实存储": a
  * zero point packed in low bits needs one more bit extraction), unpacked

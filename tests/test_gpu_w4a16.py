@@ -188,3 +188,86 @@ def test_w4a16_unpack_zeros_errors(q):
     with pytest.raises(q.QmmError):
         q.qmm_w4a16_unpack_zeros(zp, z, 4, 0)
     q.qmm_w4a16_unpack_zeros(zp, z, 0, 4)  # N == 0: no-op
+
+
+# ------------------------------------------------------------------ code table (NF4-like)
+def run_lut(q, Wp, s16, lut16, G, A16, M, N, K):
+    C = torch.full((M * N + 32,), float("nan"), dtype=torch.float16, device="cuda")
+    C[M * N:] = 77.0
+    q.qmm_w4a16_lut(Wp, s16, lut16, G, A16, C, M, N, K)
+    q.qmm_check_device_error()
+    c = C.cpu()
+    assert torch.all(c[M * N:] == 77.0), "write past the end of C"
+    return c[:M * N].view(M, N).numpy()
+
+
+@pytest.mark.parametrize("N,K,G,M", [(64, 256, 128, 1), (100, 512, 128, 5), (48, 1024, 256, 16),
+                                     (33, 384, 128, 9), (40, 512, 128, 17), (200, 640, 128, 33),
+                                     (136, 1152, 384, 257), (1000, 4096, 128, 300)])
+def test_w4a16_lut_small(q, orc, N, K, G, M):
+    """W-hat = s LUT(q) with the NF4-like table: decode (M <= 16) and the
+    tensor-core GEMM (M > 16, stream-K when tiles outnumber SMs)."""
+    qc, s16, _, A16 = wl.w4a16_inputs(43, N, K, G, M)
+    lut = wl.nf4_like_table()
+    qweight = orc.w4a16_pack(qc.numpy())
+    Wp = packed_from_canon(q, torch.from_numpy(qweight.view(np.int32)).cuda(), N, K)
+    c = run_lut(q, Wp, s16.cuda(), lut.cuda(), G, A16.cuda(), M, N, K)
+    ref = orc.w4a16_lut_matmul(qweight, s16.view(torch.int16).numpy().view(np.uint16),
+                               lut.view(torch.int16).numpy().view(np.uint16), G,
+                               A16.view(torch.int16).numpy().view(np.uint16),
+                               nthreads=orc.default_threads())
+    check(c, ref["c64"], ref["den"], f"lut N={N} K={K} G={G} M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 16, 256])
+def test_w4a16_lut_equals_zero_point_form(q, M):
+    """The table LUT(q) = q - 8 gives the zero-point kernels' bits with every
+    zero point 8 (same exact products, same sums)."""
+    N = K = 2048
+    G = 128
+    qc, s16, _, A16 = wl.w4a16_inputs(44, N, K, G, M, device="cuda")
+    Wp = packed_from_canon(q, pack_torch(qc), N, K)
+    z = torch.full((N, K // G), 8, dtype=torch.uint8, device="cuda")
+    lut = (torch.arange(16) - 8).to(torch.float16).cuda()
+    a = run(q, Wp, s16, z, G, A16, M, N, K)
+    b = run_lut(q, Wp, s16, lut, G, A16, M, N, K)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+@pytest.mark.parametrize("M", wl.W4A16_M)
+def test_w4a16_lut_full_size_sampled(q, orc, M):
+    """N = K = 8192, G = 128, the NF4-like table, at M in {1, 16, 256}: 48
+    sampled rows against the oracle."""
+    N = K = wl.W4A16_N
+    G = wl.W4A16_G
+    qc, s16, _, A16 = wl.w4a16_inputs(45, N, K, G, M, device="cuda")
+    qweight = pack_torch(qc)
+    del qc
+    Wp = packed_from_canon(q, qweight, N, K)
+    lut = wl.nf4_like_table()
+    c = run_lut(q, Wp, s16, lut.cuda(), G, A16, M, N, K)
+    rows = np.random.default_rng(8).choice(N, 48, replace=False)
+    rows[:2] = (0, N - 1)
+    ref = orc.w4a16_lut_matmul(qweight.cpu().numpy().view(np.uint32),
+                               s16.cpu().view(torch.int16).numpy().view(np.uint16),
+                               lut.view(torch.int16).numpy().view(np.uint16), G,
+                               A16.cpu().view(torch.int16).numpy().view(np.uint16), rows=rows,
+                               nthreads=orc.default_threads())
+    check(c[:, rows], ref["c64"], ref["den"], f"lut 8192x8192 M={M}")
+
+
+def test_w4a16_lut_errors(q):
+    N, K, G, M = 16, 256, 128, 2
+    Wp = torch.zeros(N * K // 2, dtype=torch.uint8, device="cuda")
+    s = torch.ones(N, K // G, dtype=torch.float16, device="cuda")
+    lut = torch.zeros(16, dtype=torch.float16, device="cuda")
+    A = torch.zeros(M, K, dtype=torch.float16, device="cuda")
+    C = torch.zeros(M, N, dtype=torch.float16, device="cuda")
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_w4a16_lut(Wp, s, None, G, A, C, M, N, K)  # no table
+    assert e.value.status == 1
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_w4a16_lut(Wp, s, lut, 64, A, C, M, N, K)  # G % 128 != 0
+    assert e.value.status == 2
+    q.qmm_w4a16_lut(Wp, s, lut, G, A, C, 0, N, K)  # M == 0: no-op
+    q.qmm_check_device_error()
