@@ -347,7 +347,7 @@ def prefill_rate(q, dev, stream, L, M, seed, reps=6, graph_steps=4, wt=None):
     prepared activations."""
     wt = q.QMM_TYPE_Q4_K if wt is None else wt
     N, K = L.N, L.K
-    off = L.row_offset_std if wt == q.QMM_TYPE_Q4_K else 0.0
+    off = L.row_offset_std if wt != q.QMM_TYPE_Q4_0 else 0.0
     w = wl.weights(seed, N, K, L.wstd, row_offset_std=off, device=dev)
     Wq = q.empty_blocks(wt, N, K)
     q.qmm_quantize_weights(wt, w, Wq, N, K)
@@ -379,7 +379,7 @@ def prefill_rate(q, dev, stream, L, M, seed, reps=6, graph_steps=4, wt=None):
 def prefill_extras(q, dev, stream):
     peaks = load_peaks()
     out = {}
-    for wt, tag in ((q.QMM_TYPE_Q4_K, "q4_K"), (q.QMM_TYPE_Q4_0, "q4_0")):
+    for wt, tag in ((q.QMM_TYPE_Q4_K, "q4_K"), (q.QMM_TYPE_Q4_0, "q4_0"), (q.QMM_TYPE_Q6_K, "q6_K")):
         for L in wl.PREFILL_SHAPES:
             for M in wl.PREFILL_M:
                 r = prefill_rate(q, dev, stream, L, M, 31, wt=wt)

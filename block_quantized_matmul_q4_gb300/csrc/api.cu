@@ -130,14 +130,14 @@ void prepare_pool(cudaStream_t s) {
 // (Q4_K: integer-valued fp16 codes; Q4_0: fp16 dequantized activations);
 // fewer the decode GEMVs: Q4_K from 2 tokens on the mma.sync kernel and its
 // activation images, otherwise the scalar GEMV and the planar layout. Q6_K
-// runs the scalar GEMV at every M (16 tokens per launch).
-bool use_gemm(qmm_type wt, int64_t M) { return M >= kGemmMinM && wt != QMM_TYPE_Q6_K; }
+// prefill shares Q4_0's fp16-operand GEMM and its workspace layout.
+bool use_gemm(qmm_type wt, int64_t M) { return M >= kGemmMinM; }
 
 // Prefill workspaces: the quantized activations (read-only in the GEMM),
 // then the stream-K partial area that calls owning the workspace use.
 size_t prefill_act_bytes(qmm_type wt, int64_t M, int64_t K) {
     return align_up(wt == QMM_TYPE_Q4_K ? prefill_bytes(M, K, nullptr, nullptr) : q4_0_prefill_bytes(M, K),
-                    256);
+                    256);  // Q4_0 and Q6_K: fp16 [M][K]
 }
 
 size_t ws_bytes_for(qmm_type wt, int64_t M, int64_t K) {
@@ -165,6 +165,8 @@ qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K,
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
         if (wt == QMM_TYPE_Q4_0)
             return cuda_status(launch_quantize_q4_0_prefill(X, ws, M, K, s), "prefill quantizer launch");
+        if (wt == QMM_TYPE_Q6_K)
+            return cuda_status(launch_quantize_q6_K_prefill(X, ws, M, K, s), "prefill quantizer launch");
         PrefillWs pw;
         prefill_bytes(M, K, &pw, (uint8_t *)ws);
         return cuda_status(launch_quantize_prefill(X, pw, M, K, s), "prefill quantizer launch");
@@ -192,6 +194,8 @@ qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, cons
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
         if (wt == QMM_TYPE_Q4_0)
             return cuda_status(launch_gemm_q4_0(Wp, N, K, ws, part, M, Y, s), "prefill GEMM launch");
+        if (wt == QMM_TYPE_Q6_K)
+            return cuda_status(launch_gemm_q6_K(Wp, N, K, ws, part, M, Y, s), "prefill GEMM launch");
         PrefillWs pw;
         prefill_bytes(M, K, &pw, (uint8_t *)ws);
         return cuda_status(launch_gemm_q4_K(Wp, N, K, pw, part, M, Y, s), "prefill GEMM launch");
@@ -451,6 +455,8 @@ qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t 
     if (use_gemm(wt, M)) {
         if (wt == QMM_TYPE_Q4_0) {
             e = launch_import_q4_0_prefill(Xq, ws, M, K, s);
+        } else if (wt == QMM_TYPE_Q6_K) {
+            e = launch_import_q6_K_prefill(Xq, ws, M, K, s);
         } else {
             PrefillWs pw;
             prefill_bytes(M, K, &pw, (uint8_t *)ws);

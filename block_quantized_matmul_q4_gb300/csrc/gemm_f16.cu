@@ -8,6 +8,12 @@
 //     a = fp16(d_a y) from the Q8_0 codes y of X (both sides carry a scale
 //     per 32 elements, so no integer sum spans more than one MMA K step;
 //     both operands are rounded once to fp16 instead), Y fp32.
+//   Q6_K prefill (page 1, "更低的比特: Q6_K 与 Q2_K 的取舍"): Y = a w^T,
+//     w = fp16(fp16(d s_j) q) with q = u - 32 per group of 16, a = fp16(d_a
+//     y) from the Q8_K codes y of X (d_a per 256), Y fp32. s_j q reaches
+//     4064, past fp16's exact integers, so the integer-valued form of the
+//     Q4_K GEMM does not carry over; each operand element is rounded instead
+//     (relative error <= 2^-10 for w, 2^-11 for a).
 // In both, q - z (q - 8) is exact in fp16 and the product with the scale is
 // rounded once (relative error <= 2^-11); the MMA accumulates in fp32 over
 // all of K.
@@ -37,14 +43,14 @@
 namespace qmm {
 namespace {
 
-enum Format { kW4A16 = 0, kQ40 = 1 };
+enum Format { kW4A16 = 0, kQ40 = 1, kQ6K = 2 };
 
 constexpr int kBM = 128, kBN = 128, kBK = 64;  // rows, tokens, K per chunk
 constexpr int kSB = 256;                       // K per pipeline round
 constexpr int kChunks = kSB / kBK;             // 4
 constexpr int kGroups = 2;                     // A handed over in pairs of chunks
 constexpr int kWStages = 3, kActStages = 2;
-constexpr int kWBytesMax = 16384 + 2048;       // Q4_0: nibbles + scales
+constexpr int kWBytesMax = 16 * kQ6Rec;         // Q6_K: 16 records of 8 rows (26880 B)
 constexpr int kChunkBytes = kBN * kBK * 2;     // 16 KB
 constexpr int kActBytes = kChunks * kChunkBytes;  // 64 KB
 constexpr int kConvWarps = 8, kEpiWarps = 4;
@@ -71,7 +77,9 @@ constexpr int kQ4NibBytes = (kBM / kQ4Tile) * kQ4Blocks * kQ4Tile * 16;  // 16 K
 template <int F>
 struct FmtInfo {
     static constexpr int kWBytes = F == kW4A16 ? (kBM / kW4Tile) * (kSB / kW4StepK) * 1024
+                                   : F == kQ6K ? (kBM / kTileRows) * kQ6Rec
                                                : kQ4NibBytes + (kBM / kQ4Tile) * kQ4Blocks * 16;
+    static_assert(kWBytes <= kWBytesMax, "weight stage");
 };
 
 struct Args {
@@ -142,6 +150,16 @@ __device__ __forceinline__ void lut_scaled_word(uint32_t w, const uint32_t *tbl,
     p45 = hmul2_u(tbl[(t >> 8) & 0xFF], ss);
     p23 = hmul2_u(tbl[t2 & 0xFF], ss);
     p67 = hmul2_u(tbl[(t2 >> 8) & 0xFF], ss);
+}
+
+// The 4 Q6_K codes of one byte word u (bytes 0..63, stored u = q + 32) as two
+// fp16 pairs (bytes 0, 1) and (2, 3), times ds (fp16(d s_j) twice): each
+// byte becomes fp16(1024 + u) by placing 0x64 above it, 1024 + 32 comes
+// off exactly, and the product with ds is one rounding.
+__device__ __forceinline__ void q6k_pairs(uint32_t u, uint32_t ds, uint32_t &p01, uint32_t &p23) {
+    constexpr uint32_t k1056 = 0x64206420u;  // fp16 1024 + 32 twice
+    p01 = hmul2_u(hsub2_u(__byte_perm(u, 0x64646464u, 0x4140), k1056), ds);
+    p23 = hmul2_u(hsub2_u(__byte_perm(u, 0x64646464u, 0x4342), k1056), ds);
 }
 
 // Columns m0 .. m0+15 of output row n (C is [M][N]: fp16 for W4A16, fp32 for
@@ -241,6 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // 8 tiles x 2 steps: [tile][step][16 rows x 64 B]
                     tc::tma_load_3d(smem_u32(wdst), &tmap_w, 0, (int32_t)(2 * sb),
                                     (int32_t)(n0 / kW4Tile), wbar, pol);
+                } else if (F == kQ6K) {
+                    // 16 records of 8 rows for super-block sb: [tile][1680 B]
+                    tc::tma_load_3d(smem_u32(wdst), &tmap_w, 0, (int32_t)sb, (int32_t)(n0 / kTileRows),
+                                    wbar, pol);
                 } else {
                     // 16 tiles x 8 blocks: nibbles [tile][block][8 rows][16 B],
                     // scales [tile][block][8 rows fp16]
@@ -400,6 +422,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 scaled_word(wv[i + 4], zz, zh, ss, hi[4 * i], hi[4 * i + 2], hi[4 * i + 1],
                                             hi[4 * i + 3]);
                             }
+                        }
+                    } else if (F == kQ6K) {
+                        // chunk c = elements 64c .. 64c+63 of super-block sb: the
+                        // low nibbles of ql bytes 32c .. 32c+31 are its elements
+                        // 0..31, the high nibbles 32..63; their high bits are in
+                        // the words of GEMV lanes 2c, 2c+1 (16 elements each), the
+                        // scales of groups 4c + tl (low) and 4c + 2 + tl (high) in
+                        // bytes 4c .. 4c+3 (tl = lane 2c + tl)
+                        const uint8_t *rec = wst + (ct >> 3) * kQ6Rec;
+                        const int r = ct & 7;
+                        const uint8_t *row = rec + r * kQ6Codes;
+                        const uint4 qa = *reinterpret_cast<const uint4 *>(row + 32 * c);
+                        const uint4 qb = *reinterpret_cast<const uint4 *>(row + 32 * c + 16);
+                        const uint4 hw = *reinterpret_cast<const uint4 *>(row + 128 + 16 * c);
+                        const uint32_t sc4 = *reinterpret_cast<const uint32_t *>(rec + kQ6ScOff + 16 * r + 4 * c);
+                        const float dw = __half2float(*reinterpret_cast<const __half *>(rec + kQ6DOff + 2 * r));
+                        uint32_t ds[4];  // fp16(d s) twice: (tl 0, low), (tl 0, high), (tl 1, low), (tl 1, high)
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const float v = __fmul_rn(dw, (float)(int)(int8_t)(uint8_t)(sc4 >> (8 * b)));
+                            const uint32_t h = __half_as_ushort(__float2half_rn(v));
+                            ds[b] = h | (h << 16);
+                        }
+                        const uint32_t qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            const int tl = w >> 2, ww = w & 3;
+                            const uint32_t ul = q6k_u(qv[w], tl ? hw.z : hw.x, ww);
+                            const uint32_t uh = q6k_u(qv[w] >> 4, tl ? hw.w : hw.y, ww);
+                            q6k_pairs(ul, ds[2 * tl], lo[2 * w], lo[2 * w + 1]);
+                            q6k_pairs(uh, ds[2 * tl + 1], hi[2 * w], hi[2 * w + 1]);
                         }
                     } else {
                         // chunk c = blocks 2c, 2c + 1 of the round. Byte l of a block
@@ -570,6 +623,62 @@ __global__ void __launch_bounds__(256) import_q8_0_prefill_kernel(const uint8_t 
     }
 }
 
+// ------------------------------------------------------------------ Q6_K prefill activations
+// X fp32 -> Q8_K codes y and fp32 scale d per 256 (the Q8_K quantizer's
+// arithmetic: amax / 127, codes rounded half away from zero), then
+// a = fp16(d * y) in natural order [M][K]. One warp per super-block, 8
+// consecutive elements per lane (two 16-byte loads, one 16-byte store).
+__global__ void __launch_bounds__(256) quantize_q6_K_prefill_kernel(const float *__restrict__ X,
+                                                                    __half *__restrict__ out,
+                                                                    int64_t nblocks) {
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += nwarps) {
+        const float4 *src = reinterpret_cast<const float4 *>(X + b * QK_K + 8 * lane);
+        const float4 v0 = src[0], v1 = src[1];
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+        const float d = __fdiv_rn(warp_max_nonneg(a), 127.0f);
+        const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+        uint32_t h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half lo = __float2half_rn(__fmul_rn(d, (float)q8_code(v[2 * i], id)));
+            const __half hi = __float2half_rn(__fmul_rn(d, (float)q8_code(v[2 * i + 1], id)));
+            h[i] = h2_bits(__halves2half2(lo, hi));
+        }
+        *reinterpret_cast<uint4 *>(out + b * QK_K + 8 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
+// The same operand from canonical Q8_K blocks [M][nsb] x 292 B, for
+// qmm_mul_mat_q8: one warp per block, 8 codes per lane.
+__global__ void __launch_bounds__(256) import_q8_K_f16_kernel(const uint8_t *__restrict__ Xq,
+                                                              __half *__restrict__ out, int64_t nblocks) {
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += nwarps) {
+        const uint8_t *blk = Xq + b * B_Q8_K;
+        const float d = *reinterpret_cast<const float *>(blk);
+        // 292-byte blocks: 4-byte loads only
+        const uint32_t cw[2] = {*reinterpret_cast<const uint32_t *>(blk + 4 + 8 * lane),
+                                *reinterpret_cast<const uint32_t *>(blk + 8 + 8 * lane)};
+        uint32_t h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int q0 = (int)(int8_t)(uint8_t)(cw[i >> 1] >> (16 * (i & 1)));
+            const int q1 = (int)(int8_t)(uint8_t)(cw[i >> 1] >> (16 * (i & 1) + 8));
+            h[i] = h2_bits(__halves2half2(__float2half_rn(__fmul_rn(d, (float)q0)),
+                                          __float2half_rn(__fmul_rn(d, (float)q1))));
+        }
+        *reinterpret_cast<uint4 *>(out + b * QK_K + 8 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
 // The GEMM (programmatic dependent launch): one CTA per tile, or with more
 // tiles than SMs a persistent stream-K grid and the fixup of its split tiles.
 template <int F>
@@ -688,6 +797,56 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
                           kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     return launch_stream_k<kQ40>(a, tmap_w, tmap_d, tmap_a, s);
+}
+
+// ------------------------------------------------------------------ Q6_K prefill
+static int warp_grid(int64_t nblocks) {
+    int64_t grid = (nblocks + 7) / 8;  // 8 warps per CTA, one block each
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (grid > cap) grid = cap;
+    return (int)(grid < 1 ? 1 : grid);
+}
+
+cudaError_t launch_quantize_q6_K_prefill(const float *X, void *ws, int64_t M, int64_t K, cudaStream_t s) {
+    const int64_t nblocks = M * (K / QK_K);
+    quantize_q6_K_prefill_kernel<<<warp_grid(nblocks), 256, 0, s>>>(X, static_cast<__half *>(ws), nblocks);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_import_q6_K_prefill(const void *Xq, void *ws, int64_t M, int64_t K, cudaStream_t s) {
+    const int64_t nblocks = M * (K / QK_K);
+    import_q8_K_f16_kernel<<<warp_grid(nblocks), 256, 0, s>>>(static_cast<const uint8_t *>(Xq),
+                                                               static_cast<__half *>(ws), nblocks);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_q6_K(const void *Wp, int64_t N, int64_t K, const void *ws, float *part, int64_t M,
+                             float *Y, cudaStream_t s) {
+    Args a;
+    a.S = nullptr;
+    a.Z = nullptr;
+    a.lut = nullptr;
+    a.C = Y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ng = 0;
+    a.spg = 1;
+    a.err = device_error_word();
+    a.part = part;
+    const int64_t nsb = K / QK_K;
+    CUtensorMap tmap_w, tmap_a;
+    // packed records as [8-row tile][super-block][1680 B], in 8-byte units
+    const uint64_t wdims[3] = {kQ6Rec / 8, (uint64_t)nsb, (uint64_t)tiles_of(N)};
+    const uint64_t wstrides[2] = {(uint64_t)kQ6Rec, (uint64_t)nsb * kQ6Rec};
+    const uint32_t wbox[3] = {kQ6Rec / 8, 1, kBM / kTileRows};
+    if (!tc::make_tmap_3d(&tmap_w, Wp, CU_TENSOR_MAP_DATA_TYPE_UINT64, wdims, wstrides, wbox) ||
+        !tc::make_tmap_2d(&tmap_a, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M, (uint64_t)K, kBN, kBK,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    return launch_stream_k<kQ6K>(a, tmap_w, tmap_w, tmap_a, s);
 }
 
 }  // namespace qmm

@@ -379,11 +379,6 @@ constexpr int kQ6KChunk = 4;
 constexpr int kQ6Half = kQ6KChunk * kQ6Rec;  // 6720
 static_assert(2 * kQ6Half <= kStageBytes, "stage size");
 
-// The 6-bit codes of ql word w (4 bytes, low or high nibbles) as bytes 0..63.
-__device__ __forceinline__ uint32_t q6k_u(uint32_t nib, uint32_t hbits, int w) {
-    return (nib & 0x0F0F0F0Fu) | (((hbits >> (2 * w)) & 0x03030303u) << 4);
-}
-
 __device__ __forceinline__ float q6k_dot(const uint4 &q, const uint2 &h, uint32_t sc, float dw,
                                          const uint4 &y0, const uint4 &y1, int bw, float da) {
     int s0 = dp4a_us(q6k_u(q.x, h.x, 0), y0.x, 0);

@@ -49,6 +49,11 @@ __host__ __device__ inline int q6k_elem(int t, int hi, int i) {
     return 64 * (t >> 1) + 32 * hi + 16 * (t & 1) + i;
 }
 __host__ __device__ inline int q6k_hbit_pos(int i) { return 8 * (i & 3) + 2 * (i >> 2); }
+// The stored 6-bit codes u (0..63) of ql word w of a lane (its 4 bytes' low
+// nibbles, or the high nibbles after a shift by 4) as 4 bytes.
+__host__ __device__ inline uint32_t q6k_u(uint32_t nib, uint32_t hbits, int w) {
+    return (nib & 0x0F0F0F0Fu) | (((hbits >> (2 * w)) & 0x03030303u) << 4);
+}
 
 __host__ __device__ inline int64_t tiles_of(int64_t N) { return (N + kTileRows - 1) / kTileRows; }
 
@@ -478,6 +483,12 @@ cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, 
 // kernel (M <= 16) and the tensor-core GEMM (M > 16).
 cudaError_t launch_w4a16_repack(bool inverse, const void *src, void *dst, int64_t N, int64_t K,
                                 cudaStream_t s);
+// Q6_K prefill: activations as fp16(d_a y) [M][K] (q4_0_prefill_bytes), from
+// fp32 X or from canonical Q8_K blocks, then the fp16-operand GEMM.
+cudaError_t launch_quantize_q6_K_prefill(const float *X, void *ws, int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_import_q6_K_prefill(const void *Xq, void *ws, int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_gemm_q6_K(const void *Wp, int64_t N, int64_t K, const void *ws, float *part, int64_t M,
+                             float *Y, cudaStream_t s);
 // lut == nullptr: W-hat = s (q - z); otherwise W-hat = s LUT(q) (Z unused).
 cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z, const __half *lut,
                                 int64_t G, const __half *A, __half *C, int64_t M, int64_t N, int64_t K,

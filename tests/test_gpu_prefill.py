@@ -122,7 +122,7 @@ def test_prefill_q4_0_full_size_sampled(q, orc, shape):
           f"Q4_0 {L.name} M={M}")
 
 
-@pytest.mark.parametrize("wt_name", ["Q4_K", "Q4_0"])
+@pytest.mark.parametrize("wt_name", ["Q4_K", "Q4_0", "Q6_K"])
 def test_stream_k_deterministic(q, orc, wt_name):
     """Split tiles are summed in a fixed order: two calls give the same bits."""
     wt = getattr(q, "QMM_TYPE_" + wt_name)
@@ -143,7 +143,7 @@ def dequant_f64(orc, t, blocks, K):
     return torch.from_numpy(orc.dequantize(t, blocks, K, f64=True))
 
 
-@pytest.mark.parametrize("wt_name", ["Q4_K", "Q4_0"])
+@pytest.mark.parametrize("wt_name", ["Q4_K", "Q4_0", "Q6_K"])
 @pytest.mark.parametrize("shape", wl.PREFILL_SHAPES, ids=lambda L: L.name)
 def test_prefill_full_output(q, orc, wt_name, shape):
     """Every element of a full-size prefill output (M = 512: the stream-K
@@ -152,7 +152,7 @@ def test_prefill_full_output(q, orc, wt_name, shape):
     activations (the factored sums the kernels use equal that product up to
     fp64 rounding). Bar: 1e-3 sum_k |w_k a_k| per element."""
     wt, L, M = getattr(q, "QMM_TYPE_" + wt_name), shape, 512
-    w = wl.weights(35, L.N, L.K, L.wstd, row_offset_std=L.row_offset_std if wt_name == "Q4_K" else 0.0,
+    w = wl.weights(35, L.N, L.K, L.wstd, row_offset_std=L.row_offset_std if wt_name != "Q4_0" else 0.0,
                    device="cuda")
     x = wl.activations(35, M, L.K, device="cuda")
     Wq = q.empty_blocks(wt, L.N, L.K)
