@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libqmm.so")
 
-SOURCES = ["api.cu", "quantize.cu", "repack.cu", "gemv.cu", "debug.cu", "static_scratch.cu", "gemm_tc.cu",
+SOURCES = ["api.cu", "quantize.cu", "repack.cu", "gemv.cu", "debug.cu", "static_scratch.cu", "tmap.cu",
            "w4a16.cu", "gemm_f16.cu", "gemv_mma.cu", "streamk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,

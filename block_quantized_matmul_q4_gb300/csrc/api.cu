@@ -126,18 +126,18 @@ void prepare_pool(cudaStream_t s) {
     g_pool_ready[d] = true;
 }
 
-// More than 16 tokens run the tensor-core GEMMs and their workspace layouts
-// (Q4_K: integer-valued fp16 codes; Q4_0: fp16 dequantized activations);
-// fewer the decode GEMVs: Q4_K from 2 tokens on the mma.sync kernel and its
-// activation images, otherwise the scalar GEMV and the planar layout. Q6_K
-// prefill shares Q4_0's fp16-operand GEMM and its workspace layout.
+// More than 16 tokens run the fp16-operand tensor-core GEMM on fp16(d_a y)
+// activations (Q4_0: 32-blocks, permuted for its converter; Q4_K and Q6_K:
+// Q8_K codes in natural order); fewer the decode GEMVs: Q4_K from 2 tokens
+// on the mma.sync kernel and its activation images, otherwise the scalar
+// GEMV and the planar layout.
 bool use_gemm(qmm_type wt, int64_t M) { return M >= kGemmMinM; }
 
 // Prefill workspaces: the quantized activations (read-only in the GEMM),
 // then the stream-K partial area that calls owning the workspace use.
 size_t prefill_act_bytes(qmm_type wt, int64_t M, int64_t K) {
-    return align_up(wt == QMM_TYPE_Q4_K ? prefill_bytes(M, K, nullptr, nullptr) : q4_0_prefill_bytes(M, K),
-                    256);  // Q4_0 and Q6_K: fp16 [M][K]
+    (void)wt;
+    return align_up(q4_0_prefill_bytes(M, K), 256);  // fp16 [M][K] for every weight type
 }
 
 size_t ws_bytes_for(qmm_type wt, int64_t M, int64_t K) {
@@ -165,11 +165,7 @@ qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K,
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
         if (wt == QMM_TYPE_Q4_0)
             return cuda_status(launch_quantize_q4_0_prefill(X, ws, M, K, s), "prefill quantizer launch");
-        if (wt == QMM_TYPE_Q6_K)
-            return cuda_status(launch_quantize_q6_K_prefill(X, ws, M, K, s), "prefill quantizer launch");
-        PrefillWs pw;
-        prefill_bytes(M, K, &pw, (uint8_t *)ws);
-        return cuda_status(launch_quantize_prefill(X, pw, M, K, s), "prefill quantizer launch");
+        return cuda_status(launch_quantize_q8_K_f16(X, ws, M, K, s), "prefill quantizer launch");
     }
     if (gemv_use_mma(wt, M, K)) {
         const size_t need = ws_bytes_for(wt, M, K);
@@ -196,9 +192,7 @@ qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, cons
             return cuda_status(launch_gemm_q4_0(Wp, N, K, ws, part, M, Y, s), "prefill GEMM launch");
         if (wt == QMM_TYPE_Q6_K)
             return cuda_status(launch_gemm_q6_K(Wp, N, K, ws, part, M, Y, s), "prefill GEMM launch");
-        PrefillWs pw;
-        prefill_bytes(M, K, &pw, (uint8_t *)ws);
-        return cuda_status(launch_gemm_q4_K(Wp, N, K, pw, part, M, Y, s), "prefill GEMM launch");
+        return cuda_status(launch_gemm_q4_K_f16(Wp, N, K, ws, part, M, Y, s), "prefill GEMM launch");
     }
     if (gemv_use_mma(wt, M, K)) {
         const size_t need = ws_bytes_for(wt, M, K);
@@ -455,12 +449,8 @@ qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t 
     if (use_gemm(wt, M)) {
         if (wt == QMM_TYPE_Q4_0) {
             e = launch_import_q4_0_prefill(Xq, ws, M, K, s);
-        } else if (wt == QMM_TYPE_Q6_K) {
-            e = launch_import_q6_K_prefill(Xq, ws, M, K, s);
         } else {
-            PrefillWs pw;
-            prefill_bytes(M, K, &pw, (uint8_t *)ws);
-            e = launch_import_prefill(Xq, pw, M, K, s);
+            e = launch_import_q8_K_f16(Xq, ws, M, K, s);
         }
     } else if (gemv_use_mma(wt, M, K)) {
         e = launch_import_mma_image(Xq, ws, M, K, s);

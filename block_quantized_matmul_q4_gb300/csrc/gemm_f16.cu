@@ -8,15 +8,17 @@
 //     a = fp16(d_a y) from the Q8_0 codes y of X (both sides carry a scale
 //     per 32 elements, so no integer sum spans more than one MMA K step;
 //     both operands are rounded once to fp16 instead), Y fp32.
+//   Q4_K prefill (page 1, "K-quant", "6-bit 参数"): Y = a w^T, w =
+//     fp16(q fp16(d s_j) - fp16(dmin m_j)) per sub-block of 32 (one fused
+//     multiply-add), a = fp16(d_a y) from the Q8_K codes y of X, Y fp32.
 //   Q6_K prefill (page 1, "更低的比特: Q6_K 与 Q2_K 的取舍"): Y = a w^T,
 //     w = fp16(fp16(d s_j) q) with q = u - 32 per group of 16, a = fp16(d_a
 //     y) from the Q8_K codes y of X (d_a per 256), Y fp32. s_j q reaches
 //     4064, past fp16's exact integers, so the integer-valued form of the
 //     Q4_K GEMM does not carry over; each operand element is rounded instead
 //     (relative error <= 2^-10 for w, 2^-11 for a).
-// In both, q - z (q - 8) is exact in fp16 and the product with the scale is
-// rounded once (relative error <= 2^-11); the MMA accumulates in fp32 over
-// all of K.
+// In all, the codes are exact in fp16 and the weight is rounded once or
+// twice (relative error <= 2^-10); the MMA accumulates in fp32 over all of K.
 //
 // Tile = 128 weight rows (MMA M) x 128 tokens (MMA N). Up to one tile per SM
 // the grid has one CTA per tile; with more, one CTA per SM walks a
@@ -43,7 +45,7 @@
 namespace qmm {
 namespace {
 
-enum Format { kW4A16 = 0, kQ40 = 1, kQ6K = 2 };
+enum Format { kW4A16 = 0, kQ40 = 1, kQ6K = 2, kQ4K = 3 };
 
 constexpr int kBM = 128, kBN = 128, kBK = 64;  // rows, tokens, K per chunk
 constexpr int kSB = 256;                       // K per pipeline round
@@ -78,6 +80,7 @@ template <int F>
 struct FmtInfo {
     static constexpr int kWBytes = F == kW4A16 ? (kBM / kW4Tile) * (kSB / kW4StepK) * 1024
                                    : F == kQ6K ? (kBM / kTileRows) * kQ6Rec
+                                   : F == kQ4K ? (kBM / kTileRows) * kTileRows * B_Q4_K
                                                : kQ4NibBytes + (kBM / kQ4Tile) * kQ4Blocks * 16;
     static_assert(kWBytes <= kWBytesMax, "weight stage");
 };
@@ -160,6 +163,17 @@ __device__ __forceinline__ void q6k_pairs(uint32_t u, uint32_t ds, uint32_t &p01
     constexpr uint32_t k1056 = 0x64206420u;  // fp16 1024 + 32 twice
     p01 = hmul2_u(hsub2_u(__byte_perm(u, 0x64646464u, 0x4140), k1056), ds);
     p23 = hmul2_u(hsub2_u(__byte_perm(u, 0x64646464u, 0x4342), k1056), ds);
+}
+
+// The 4 Q4_K codes q (0..15) of one byte word as two fp16 pairs (bytes 0, 1)
+// and (2, 3) of q fp16(d s_j) - fp16(dmin m_j): q is exact (1024 + q less
+// 1024) and the fused multiply-add rounds once. ds = fp16(d s_j) twice,
+// ndm = -fp16(dmin m_j) twice.
+__device__ __forceinline__ void q4k_pairs(uint32_t q, uint32_t ds, uint32_t ndm, uint32_t &p01,
+                                          uint32_t &p23) {
+    constexpr uint32_t k1024 = 0x64006400u;
+    p01 = hfma2_u(hsub2_u(__byte_perm(q, 0x64646464u, 0x4140), k1024), ds, ndm);
+    p23 = hfma2_u(hsub2_u(__byte_perm(q, 0x64646464u, 0x4342), k1024), ds, ndm);
 }
 
 // Columns m0 .. m0+15 of output row n (C is [M][N]: fp16 for W4A16, fp32 for
@@ -259,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // 8 tiles x 2 steps: [tile][step][16 rows x 64 B]
                     tc::tma_load_3d(smem_u32(wdst), &tmap_w, 0, (int32_t)(2 * sb),
                                     (int32_t)(n0 / kW4Tile), wbar, pol);
-                } else if (F == kQ6K) {
-                    // 16 records of 8 rows for super-block sb: [tile][1680 B]
+                } else if (F == kQ6K || F == kQ4K) {
+                    // 16 records of 8 rows for super-block sb: [tile][8 x 210 or 144 B]
                     tc::tma_load_3d(smem_u32(wdst), &tmap_w, 0, (int32_t)sb, (int32_t)(n0 / kTileRows),
                                     wbar, pol);
                 } else {
@@ -422,6 +436,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 scaled_word(wv[i + 4], zz, zh, ss, hi[4 * i], hi[4 * i + 2], hi[4 * i + 1],
                                             hi[4 * i + 3]);
                             }
+                        }
+                    } else if (F == kQ4K) {
+                        // chunk c = sub-blocks 2c (low nibbles of qs bytes 32c ..
+                        // 32c+31, chunk elements 0..31) and 2c + 1 (high nibbles,
+                        // 32..63); their scales and mins are header field c
+                        const uint8_t *blk = wst + (ct >> 3) * (kTileRows * B_Q4_K) + (ct & 7) * B_Q4_K;
+                        const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+                        const uint4 qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
+                        const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
+                        const uint32_t f = k4_field(hdr.y, hdr.z, hdr.w, c);
+                        const float dw = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
+                        const float dmw = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+                        uint32_t ds[2], dm[2];  // fp16(d s_j), -fp16(dmin m_j), twice; low then high sub-block
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t sv = (f >> (12 * h)) & 63u, mv = (f >> (12 * h + 6)) & 63u;
+                            const uint32_t hs = __half_as_ushort(__float2half_rn(__fmul_rn(dw, (float)sv)));
+                            const uint32_t hm = __half_as_ushort(__float2half_rn(__fmul_rn(dmw, (float)mv))) ^ 0x8000u;
+                            ds[h] = hs | (hs << 16);
+                            dm[h] = hm | (hm << 16);
+                        }
+                        const uint32_t qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            q4k_pairs(qv[w] & 0x0F0F0F0Fu, ds[0], dm[0], lo[2 * w], lo[2 * w + 1]);
+                            q4k_pairs((qv[w] >> 4) & 0x0F0F0F0Fu, ds[1], dm[1], hi[2 * w], hi[2 * w + 1]);
                         }
                     } else if (F == kQ6K) {
                         // chunk c = elements 64c .. 64c+63 of super-block sb: the
@@ -628,7 +668,7 @@ __global__ void __launch_bounds__(256) import_q8_0_prefill_kernel(const uint8_t 
 // arithmetic: amax / 127, codes rounded half away from zero), then
 // a = fp16(d * y) in natural order [M][K]. One warp per super-block, 8
 // consecutive elements per lane (two 16-byte loads, one 16-byte store).
-__global__ void __launch_bounds__(256) quantize_q6_K_prefill_kernel(const float *__restrict__ X,
+__global__ void __launch_bounds__(256) quantize_q8_K_f16_kernel(const float *__restrict__ X,
                                                                     __half *__restrict__ out,
                                                                     int64_t nblocks) {
     pdl_launch_dependents();
@@ -807,19 +847,46 @@ static int warp_grid(int64_t nblocks) {
     return (int)(grid < 1 ? 1 : grid);
 }
 
-cudaError_t launch_quantize_q6_K_prefill(const float *X, void *ws, int64_t M, int64_t K, cudaStream_t s) {
+cudaError_t launch_quantize_q8_K_f16(const float *X, void *ws, int64_t M, int64_t K, cudaStream_t s) {
     const int64_t nblocks = M * (K / QK_K);
-    quantize_q6_K_prefill_kernel<<<warp_grid(nblocks), 256, 0, s>>>(X, static_cast<__half *>(ws), nblocks);
+    quantize_q8_K_f16_kernel<<<warp_grid(nblocks), 256, 0, s>>>(X, static_cast<__half *>(ws), nblocks);
     count_launch();
     return cudaGetLastError();
 }
 
-cudaError_t launch_import_q6_K_prefill(const void *Xq, void *ws, int64_t M, int64_t K, cudaStream_t s) {
+cudaError_t launch_import_q8_K_f16(const void *Xq, void *ws, int64_t M, int64_t K, cudaStream_t s) {
     const int64_t nblocks = M * (K / QK_K);
     import_q8_K_f16_kernel<<<warp_grid(nblocks), 256, 0, s>>>(static_cast<const uint8_t *>(Xq),
                                                                static_cast<__half *>(ws), nblocks);
     count_launch();
     return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_q4_K_f16(const void *Wp, int64_t N, int64_t K, const void *ws, float *part,
+                                 int64_t M, float *Y, cudaStream_t s) {
+    Args a;
+    a.S = nullptr;
+    a.Z = nullptr;
+    a.lut = nullptr;
+    a.C = Y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ng = 0;
+    a.spg = 1;
+    a.err = device_error_word();
+    a.part = part;
+    const int64_t nsb = K / QK_K;
+    constexpr int kRec = kTileRows * B_Q4_K;  // 1152 B: one (tile, super-block)
+    CUtensorMap tmap_w, tmap_a;
+    const uint64_t wdims[3] = {kRec / 8, (uint64_t)nsb, (uint64_t)tiles_of(N)};
+    const uint64_t wstrides[2] = {(uint64_t)kRec, (uint64_t)nsb * kRec};
+    const uint32_t wbox[3] = {kRec / 8, 1, kBM / kTileRows};
+    if (!tc::make_tmap_3d(&tmap_w, Wp, CU_TENSOR_MAP_DATA_TYPE_UINT64, wdims, wstrides, wbox) ||
+        !tc::make_tmap_2d(&tmap_a, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M, (uint64_t)K, kBN, kBK,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    return launch_stream_k<kQ4K>(a, tmap_w, tmap_w, tmap_a, s);
 }
 
 cudaError_t launch_gemm_q6_K(const void *Wp, int64_t N, int64_t K, const void *ws, float *part, int64_t M,

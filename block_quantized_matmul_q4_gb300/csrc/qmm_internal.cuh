@@ -97,17 +97,7 @@ __host__ __device__ __forceinline__ int mat_of(const MatSet &s, int64_t unit) {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Prefill (GEMM) activation layout for Q4_K weights, written by the prefill
-// quantizer: Q8_K codes as exact fp16 [M][K] (the MMA operand, loaded by
-// TMA), 16-code sums as fp16 [M][K/256 * 16] (exact: |sum| <= 2032), block
-// scales as fp32 [K/256][Mpad], Mpad = M rounded up to a multiple of 4
-// (token-contiguous rows, 16-byte aligned for TMA).
-struct PrefillWs {
-    __half *y16;
-    __half *bs16;
-    float *daT;
-};
-// Tokens per call above which Q4_K mul_mat runs the tensor-core GEMM.
+// Tokens per call from which mul_mat runs the tensor-core GEMM.
 constexpr int64_t kGemmMinM = 17;
 
 // Workspace carve-up for M rows of K activations with block size qk.
@@ -441,11 +431,10 @@ cudaError_t launch_quantize_q8(qmm_type vt, bool planar, const float *X, void *o
 cudaError_t launch_quantize_weights(qmm_type wt, const float *W, void *Wq, int64_t N, int64_t K,
                                     cudaStream_t s);
 // Canonical Q8 blocks (qmm_mul_mat_q8) into each private activation layout:
-// planar (scalar GEMV), image (tensor-core GEMV), the two prefill operands.
+// planar (scalar GEMV), image (tensor-core GEMV), the fp16 prefill operands.
 cudaError_t launch_import_q8_planar(qmm_type vt, const void *Xq, Planar p, int64_t M, int64_t K,
                                     cudaStream_t s);
 cudaError_t launch_import_mma_image(const void *Xq, void *img, int64_t M, int64_t K, cudaStream_t s);
-cudaError_t launch_import_prefill(const void *Xq, PrefillWs p, int64_t M, int64_t K, cudaStream_t s);
 cudaError_t launch_import_q4_0_prefill(const void *Xq, void *ws, int64_t M, int64_t K,
                                        cudaStream_t s);
 cudaError_t launch_repack(qmm_type wt, bool inverse, const void *src, void *dst, int64_t N,
@@ -473,22 +462,19 @@ cudaError_t launch_quantize_mma_image(const float *X, void *img, int64_t M, int6
                                       cudaStream_t s);
 cudaError_t launch_gemv_mma_q4_K(MatSet ms, int64_t K, const float *X, const void *img, int64_t M,
                                  bool pdl, cudaStream_t s);
-size_t prefill_bytes(int64_t M, int64_t K, PrefillWs *p, uint8_t *base);
-cudaError_t launch_quantize_prefill(const float *X, PrefillWs p, int64_t M, int64_t K,
-                                    cudaStream_t s);
-// part: stream_k_part_bytes() of device memory for split tiles
-cudaError_t launch_gemm_q4_K(const void *Wp, int64_t N, int64_t K, PrefillWs p, float *part, int64_t M,
-                             float *Y, cudaStream_t s);
 // W4A16: nibble interleave of the packed layout (or its inverse), the decode
 // kernel (M <= 16) and the tensor-core GEMM (M > 16).
 cudaError_t launch_w4a16_repack(bool inverse, const void *src, void *dst, int64_t N, int64_t K,
                                 cudaStream_t s);
-// Q6_K prefill: activations as fp16(d_a y) [M][K] (q4_0_prefill_bytes), from
-// fp32 X or from canonical Q8_K blocks, then the fp16-operand GEMM.
-cudaError_t launch_quantize_q6_K_prefill(const float *X, void *ws, int64_t M, int64_t K, cudaStream_t s);
-cudaError_t launch_import_q6_K_prefill(const void *Xq, void *ws, int64_t M, int64_t K, cudaStream_t s);
+// Q4_K and Q6_K prefill: activations as fp16(d_a y) [M][K] (Q8_K codes y, d_a
+// per 256; q4_0_prefill_bytes), from fp32 X or from canonical Q8_K blocks,
+// then the fp16-operand GEMM.
+cudaError_t launch_quantize_q8_K_f16(const float *X, void *ws, int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_import_q8_K_f16(const void *Xq, void *ws, int64_t M, int64_t K, cudaStream_t s);
 cudaError_t launch_gemm_q6_K(const void *Wp, int64_t N, int64_t K, const void *ws, float *part, int64_t M,
                              float *Y, cudaStream_t s);
+cudaError_t launch_gemm_q4_K_f16(const void *Wp, int64_t N, int64_t K, const void *ws, float *part,
+                                 int64_t M, float *Y, cudaStream_t s);
 // lut == nullptr: W-hat = s (q - z); otherwise W-hat = s LUT(q) (Z unused).
 cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z, const __half *lut,
                                 int64_t G, const __half *A, __half *C, int64_t M, int64_t N, int64_t K,

@@ -1,5 +1,5 @@
 // streamk.cu -- grid size, partial area and fixup of the stream-K GEMMs
-// (gemm_tc.cu, gemm_f16.cu). With more tiles than SMs, a persistent grid of
+// (gemm_f16.cu). With more tiles than SMs, a persistent grid of
 // one CTA per SM takes the units u = tile * nsb + k-round in equal
 // contiguous ranges (CTA c: [c U / G, (c+1) U / G)); a CTA that holds all of
 // a tile's units writes it, otherwise its piece went to its partial slot

@@ -180,12 +180,17 @@ qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon
  *   Q4_0: sum_b fp16(d_w) fp16(d_a) sum_{i<32} (q_i - 8) y_i
  *   Q4_K: sum_sb d_a (d * sum_j s_j sum_i q_i y_i - dmin * sum_j m_j sum_i y_i)
  *   Q6_K: sum_sb d_a d sum_j s_j sum_i q_i y_i  (16 groups j of 16, no min)
- * with integer block sums and fp32 accumulation across blocks. Tokens are
- * processed 16 at a time by the decode GEMV kernels. When M*K is small (one
- * 16-token group of at most 8192 elements) the activation quantizer runs
- * inside the GEMV kernel (one launch, no workspace); otherwise the quantized activations go to a workspace that the
- * library allocates stream-ordered (cudaMallocAsync) and frees after the
- * call, in the same stream.
+ * Up to 16 tokens (decode) the GEMV kernels take integer block sums with
+ * fp32 accumulation across blocks. When M*K is small (one 16-token group of
+ * at most 8192 elements) the activation quantizer runs inside the GEMV
+ * kernel (one launch, no workspace). Above 16 tokens (prefill) the
+ * tensor-core GEMM multiplies fp16 operands with fp32 accumulation: the
+ * weights decoded to fp16 (Q4_0 d (q - 8), Q4_K q fp16(d s_j) - fp16(dmin m_j),
+ * Q6_K fp16(d s_j) q, each rounded once more to fp16) and the activations
+ * as fp16(d_a y) from the same Q8 codes; every product is then within
+ * 2^-10 of the factored form's. Otherwise the quantized activations go to
+ * a workspace that the library allocates stream-ordered (cudaMallocAsync)
+ * and frees after the call, in the same stream.
  * W_packed comes from qmm_repack_weights.
  * Errors: QMM_ERR_ARG (type, sizes, null/misaligned pointers),
  * QMM_ERR_NOMEM (workspace allocation failed), QMM_ERR_CUDA (launch failed).
@@ -195,7 +200,7 @@ qmm_status qmm_mul_mat(qmm_type wt, const void *W_packed, int64_t N, int64_t K, 
 
 /* qmm_mul_mat on activations that are already quantized: Xq holds M rows of
  * canonical blocks as qmm_quantize_row_q8 writes them -- Q8_0 [M][K/32] x 34 B
- * for Q4_0 weights, Q8_K [M][K/256] x 292 B for Q4_K (page 1: vec_dot takes
+ * for Q4_0 weights, Q8_K [M][K/256] x 292 B for Q4_K and Q6_K (page 1: vec_dot takes
  * the weight row and the Q8 activation row; for Q8_K the stored 16-code sums
  * are used for the min term as they are). The blocks are rewritten into the
  * private layout of the kernel that runs (in a workspace allocated like
