@@ -485,6 +485,44 @@ def q6_K_rate(q, dev, stream):
     return out
 
 
+def small_m_rate(q, dev, stream):
+    """Q4_0 and Q6_K at 4096 x 4096, M in {2, 4, 8, 16}: qmm_mul_mat_ws (the
+    path mul_mat takes) against qmm_mul_mat_static (always the 16-token
+    scalar GEMV); us per call, weights rotating over 32 copies."""
+    out = {}
+    L = wl.GEMV_Q4_K_4096
+    for wt, tag in ((q.QMM_TYPE_Q4_0, "q4_0"), (q.QMM_TYPE_Q6_K, "q6_K")):
+        w = wl.weights(0, L.N, L.K, 0.02, row_offset_std=0.0 if wt == q.QMM_TYPE_Q4_0 else 0.005,
+                       device=dev)
+        Wq = q.empty_blocks(wt, L.N, L.K)
+        q.qmm_quantize_weights(wt, w, Wq, L.N, L.K)
+        Wp = q.empty_packed(wt, L.N, L.K)
+        q.qmm_repack_weights(wt, Wq, Wp, L.N, L.K)
+        del w, Wq
+        cps = [Wp] + [Wp.clone() for _ in range(31)]
+        for M in (2, 4, 8, 16):
+            X = wl.activations(0, M, L.K, device=dev)
+            Y = torch.empty(M, L.N, device=dev)
+            ws_bytes = q.qmm_workspace_bytes(wt, M, L.K)
+            ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+            res = {}
+            for name, fn in (("mul_mat", lambda i: q.qmm_mul_mat_ws(wt, cps[i % 32], L.N, L.K, X, M, Y, ws,
+                                                                    ws_bytes, stream)),
+                             ("gemv", lambda i: q.qmm_mul_mat_static(wt, cps[i % 32], L.N, L.K, X, M, Y,
+                                                                     stream))):
+                for i in range(3):
+                    fn(i)
+                g = capture(fn, GRAPH_STEPS, stream)
+                with torch.cuda.stream(stream):
+                    g.replay()
+                t = timed(stream, lambda: run_graphs(g, None, 20)) / (20 * GRAPH_STEPS)
+                res[name + "_us"] = round(t * 1e6, 3)
+            out[f"{tag}_m{M}"] = res
+        del cps, Wp
+        torch.cuda.empty_cache()
+    return out
+
+
 def sweep_rate(q, dev, stream, Ms=None):
     """The headline GEMV (Q4_K, N = K = 4096) at M in {1, 2, 4, 8, 16}: M = 1
     runs the scalar GEMV, M >= 2 the tensor-core one."""
@@ -613,7 +651,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--case", choices=["decode", "prefill", "w4a16", "layer", "sweep", "q6_K"],
+    ap.add_argument("--case", choices=["decode", "prefill", "w4a16", "layer", "sweep", "q6_K", "small_m"],
                     default="decode",
                     help="prefill / w4a16 / layer / sweep / q6_K: only that measurement (for "
                          "profiler captures)")
@@ -653,6 +691,7 @@ def main():
     if args.case != "decode":
         import block_quantized_matmul_q4_gb300 as q
         fn = {"prefill": prefill_extras, "w4a16": w4a16_extras, "layer": layer_rate, "q6_K": q6_K_rate,
+              "small_m": small_m_rate,
               "sweep": lambda q, d, s: sweep_rate(q, d, s, args.m)}[args.case]
         print(json.dumps(fn(q, torch.device("cuda", torch.cuda.current_device()),
                             torch.cuda.Stream())), flush=True)

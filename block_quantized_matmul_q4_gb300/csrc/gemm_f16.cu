@@ -50,6 +50,7 @@ enum Format { kW4A16 = 0, kQ40 = 1, kQ6K = 2, kQ4K = 3 };
 constexpr int kBM = 128, kBN = 128, kBK = 64;  // rows, tokens, K per chunk
 constexpr int kSB = 256;                       // K per pipeline round
 constexpr int kChunks = kSB / kBK;             // 4
+static_assert(kSB == kSkRound && kBM == kSkTile && kBN == kSkTile, "stream-K units");
 constexpr int kGroups = 2;                     // A handed over in pairs of chunks
 constexpr int kWStages = 3, kActStages = 2;
 constexpr int kWBytesMax = 16 * kQ6Rec;         // Q6_K: 16 records of 8 rows (26880 B)
@@ -730,7 +731,7 @@ cudaError_t launch_stream_k(Args a, const CUtensorMap &tmap_w, const CUtensorMap
     a.mblocks = (a.M + kBN - 1) / kBN;
     const int64_t tiles = ((a.N + kBM - 1) / kBM) * a.mblocks;
     a.units = tiles * nsb;
-    const int64_t G = stream_k_grid(tiles);
+    const int64_t G = stream_k_grid(tiles, a.units);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
     cfg.blockDim = dim3(kThreads);

@@ -97,8 +97,13 @@ __host__ __device__ __forceinline__ int mat_of(const MatSet &s, int64_t unit) {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Tokens per call from which mul_mat runs the tensor-core GEMM.
+// Tokens per call from which mul_mat runs the tensor-core GEMM: Q4_K keeps
+// its tensor-core GEMV up to 16 tokens; Q4_0 and Q6_K, whose decode GEMV is
+// scalar, switch where that GEMV moves to its 16-token form (4096 x 4096,
+// measured: the split-K GEMM takes 20-22 us from 4 to 16 tokens, the scalar
+// GEMV 9-11 us at 4, 18-24 at 8, 30-42 at 16).
 constexpr int64_t kGemmMinM = 17;
+constexpr int64_t kGemmMinMScalar = 9;
 
 // Workspace carve-up for M rows of K activations with block size qk.
 __host__ __device__ inline size_t planar_bytes(int64_t M, int64_t K, int qk, Planar *p,
@@ -323,7 +328,8 @@ __device__ __forceinline__ int clampi(int v, int lo, int hi) { return min(max(v,
 // it writes that piece to its partial slot (slot 0 when the tile is the
 // CTA's first, 1 when its last), and the fixup kernel (streamk.cu) adds the
 // pieces in CTA order and writes the tile.
-constexpr int kSkTile = 128;  // tile rows = tile columns
+constexpr int kSkTile = 128;   // tile rows = tile columns
+constexpr int kSkRound = 256;  // K elements per unit
 
 // The CTA whose range holds unit u.
 __host__ __device__ __forceinline__ int64_t sk_cta_of(int64_t u, int64_t U, int64_t G) {
@@ -494,15 +500,16 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
 cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
                                     const void *Xq, int64_t M, int32_t *out, cudaStream_t s);
 cudaError_t launch_debug_wait_timeout(int64_t limit_cycles, cudaStream_t s);
-// Stream-K GEMMs (streamk.cu): CTAs for `tiles` tiles (tiles itself up to
-// the SM count, else the SM count); bytes of the partial area; the fixup
-// that adds the split tiles' pieces into C (fp32, or fp16 when half_out),
-// launched only when G < tiles.
-int64_t stream_k_grid(int64_t tiles);
+// Stream-K GEMMs (streamk.cu): CTAs for `tiles` tiles of `units` units (the
+// SM count above it, one per tile from half of it, else split K over up to
+// the SM count); bytes of the partial area; the fixup that adds the split
+// tiles' pieces into C (fp32, or fp16 when half_out), launched only when
+// G != tiles.
+int64_t stream_k_grid(int64_t tiles, int64_t units);
 size_t stream_k_part_bytes();
-// Whether an N x M output (128 x 128 tiles) runs split tiles, i.e. needs the
-// partial area.
-bool stream_k_splits(int64_t N, int64_t M);
+// Whether an N x M output of depth K (128 x 128 tiles, 256-element units)
+// runs split tiles, i.e. needs the partial area.
+bool stream_k_splits(int64_t N, int64_t M, int64_t K);
 cudaError_t launch_stream_k_fixup(const float *part, void *C, bool half_out, int64_t N, int64_t M,
                                   int64_t mblocks, int64_t nsb, int64_t units, int64_t G,
                                   cudaStream_t s);

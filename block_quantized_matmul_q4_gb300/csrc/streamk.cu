@@ -84,14 +84,22 @@ static_assert((kTM * kTN / 4) % (4 * kFixupThreads) == 0, "fixup tiling");
 
 }  // namespace
 
-int64_t stream_k_grid(int64_t tiles) {
-    if (tiles <= max_grid()) return tiles < 1 ? 1 : tiles;
-    return max_grid();
+// Grid of the stream-K GEMMs for `tiles` output tiles of `units` (tile,
+// round) units: one CTA per SM when tiles outnumber SMs; one CTA per tile
+// from half the SM count up (no split: measured no faster split than whole
+// at 128 tiles); below that the units of the few tiles spread over the SMs
+// (split K), which the same piece/fixup machinery sums.
+int64_t stream_k_grid(int64_t tiles, int64_t units) {
+    const int64_t g = max_grid();
+    if (tiles > g) return g;
+    if (2 * tiles >= g) return tiles < 1 ? 1 : tiles;
+    return units < g ? (units < 1 ? 1 : units) : g;
 }
 
-bool stream_k_splits(int64_t N, int64_t M) {
+bool stream_k_splits(int64_t N, int64_t M, int64_t K) {
     const int64_t tiles = ((N + kTM - 1) / kTM) * ((M + kTN - 1) / kTN);
-    return stream_k_grid(tiles) < tiles;
+    const int64_t units = tiles * ((K + kSkRound - 1) / kSkRound);
+    return stream_k_grid(tiles, units) != tiles;
 }
 
 // Two 128 x 128 fp32 slots per CTA of the largest grid.
