@@ -53,18 +53,14 @@ constexpr int kChunks = kSB / kBK;             // 4
 static_assert(kSB == kSkRound && kBM == kSkTile && kBN == kSkTile, "stream-K units");
 constexpr int kGroups = 2;                     // A handed over in pairs of chunks
 constexpr int kWStages = 3, kActStages = 2;
-constexpr int kWBytesMax = 16 * kQ6Rec;         // Q6_K: 16 records of 8 rows (26880 B)
+constexpr int kWBytesMax = 16 * kQ6Rec;         // largest weight stage: Q6_K, 16 records of 8 rows
 constexpr int kChunkBytes = kBN * kBK * 2;     // 16 KB
 constexpr int kActBytes = kChunks * kChunkBytes;  // 64 KB
 constexpr int kConvWarps = 8, kEpiWarps = 4;
 constexpr int kThreads = (3 + kConvWarps + kEpiWarps) * 32;
 constexpr int kOffAct = 0;
 constexpr int kOffW = kOffAct + kActStages * kActBytes;
-constexpr int kOffLut = kOffW + kWStages * kWBytesMax;  // W4A16 code table: 256 fp16 pairs
-constexpr int kOffBar = kOffLut + 1024;
 constexpr int kNumBars = 2 * (kWStages + kActStages + kGroups) + 5;  // + acc_full[2], acc_empty[2], done
-constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColAcc = 0, kColARing = 2 * kBN;  // two accumulators (stream-K pieces), A ring
 constexpr uint32_t kARingCols = kBK / 2;
@@ -84,6 +80,14 @@ struct FmtInfo {
                                    : F == kQ4K ? (kBM / kTileRows) * kTileRows * B_Q4_K
                                                : kQ4NibBytes + (kBM / kQ4Tile) * kQ4Blocks * 16;
     static_assert(kWBytes <= kWBytesMax, "weight stage");
+    // Shared memory: activation stages | weight stages (this format's size:
+    // the unused rest of the SM's 228 KB stays L1, where the W4A16
+    // converters' scale and zero reads hit) | code table | barriers.
+    static constexpr int kWStage = (kWBytes + 127) / 128 * 128;
+    static constexpr int kOffLut = kOffW + kWStages * kWStage;  // W4A16 code table: 256 fp16 pairs
+    static constexpr int kOffBar = kOffLut + 1024;
+    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 struct Args {
@@ -209,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t u0 = (int64_t)blockIdx.x * a.units / gridDim.x;
     const int64_t u1 = ((int64_t)blockIdx.x + 1) * a.units / gridDim.x;
 
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + FmtInfo<F>::kOffBar);
     uint64_t *w_full = bar, *w_empty = w_full + kWStages;
     uint64_t *act_full = w_empty + kWStages, *act_empty = act_full + kActStages;
     uint64_t *a_full = act_empty + kActStages, *a_empty = a_full + kGroups;
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(done), 1);
         fence_barrier_init();
     }
-    uint32_t *pair_tbl = reinterpret_cast<uint32_t *>(smem + kOffLut);
+    uint32_t *pair_tbl = reinterpret_cast<uint32_t *>(smem + FmtInfo<F>::kOffLut);
     if (F == kW4A16 && a.lut) {
         // the table is weight data, like the scales: ready before the launch
         for (int i = threadIdx.x; i < 256; i += kThreads)
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 // rows past the last tile and K past the end read as zeros
                 const uint32_t wbar = smem_u32(&w_full[ws]);
-                uint8_t *wdst = smem + kOffW + ws * kWBytesMax;
+                uint8_t *wdst = smem + kOffW + ws * FmtInfo<F>::kWStage;
                 mbar_arrive_expect_tx(wbar, kWBytes);
                 if (F == kW4A16) {
                     // 8 tiles x 2 steps: [tile][step][16 rows x 64 B]
@@ -397,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t par = (uint32_t)(pos & 1);
                 ok = mbar_wait_warp(smem_u32(&w_full[ws]), (uint32_t)((pos / kWStages) & 1), a.err);
                 if (!ok) break;
-                const uint8_t *wst = smem + kOffW + ws * kWBytesMax;
+                const uint8_t *wst = smem + kOffW + ws * FmtInfo<F>::kWStage;
 #pragma unroll 1
                 for (int g = 0; g < kGroups && ok; ++g) {
                     const int c = g * (kChunks / kGroups) + set;  // chunk of this round
@@ -557,10 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // TMEM loads are warp-collective: every lane takes them (ok is
             // warp-uniform); only the stores depend on the row
             const bool row_ok = n < a.N;
+            // column groups holding tokens < M (warp-uniform): the rest is padding
+            const int ncg = (int)((a.M - m0 < kBN ? a.M - m0 + 15 : kBN) / 16);
             if (sb_begin == 0 && sb_end == nsb) {
                 if (ok) {
 #pragma unroll 1
-                    for (int c16 = 0; c16 < kBN / 16; ++c16) {
+                    for (int c16 = 0; c16 < ncg; ++c16) {
                         float v[16];
                         tc::tmem_ld16(acc + (uint32_t)(c16 * 16), v);
                         tc::tmem_ld_wait();
@@ -573,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *mine = a.part + sk_slot(blockIdx.x, tile, a.units, gridDim.x, nsb) + nl;
                 if (ok) {
 #pragma unroll 1
-                    for (int c16 = 0; c16 < kBN / 16; ++c16) {
+                    for (int c16 = 0; c16 < ncg; ++c16) {
                         float v[16];
                         tc::tmem_ld16(acc + (uint32_t)(c16 * 16), v);
                         tc::tmem_ld_wait();
@@ -725,7 +731,7 @@ __global__ void __launch_bounds__(256) import_q8_K_f16_kernel(const uint8_t *__r
 template <int F>
 cudaError_t launch_stream_k(Args a, const CUtensorMap &tmap_w, const CUtensorMap &tmap_d,
                             const CUtensorMap &tmap_a, cudaStream_t s) {
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_f16_kernel<F>), kSmemBytes);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_f16_kernel<F>), FmtInfo<F>::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t nsb = (a.K + kSB - 1) / kSB;
     a.mblocks = (a.M + kBN - 1) / kBN;
@@ -735,7 +741,7 @@ cudaError_t launch_stream_k(Args a, const CUtensorMap &tmap_w, const CUtensorMap
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = FmtInfo<F>::kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

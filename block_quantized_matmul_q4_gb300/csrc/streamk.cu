@@ -27,35 +27,32 @@ __device__ __forceinline__ float out_cast<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __half out_cast<__half>(float v) { return __float2half_rn(v); }
 
-// One CTA per tile (whole tiles return at once). Each thread takes 4
-// consecutive rows of a column (one 16-byte load per piece) and keeps 4
-// columns in flight; a warp covers 128 rows of one column = 512 contiguous
-// bytes of every slot.
-template <class T>
-__global__ void __launch_bounds__(kFixupThreads) stream_k_fixup_kernel(const float *__restrict__ part,
-                                                                       T *__restrict__ C, int64_t N,
-                                                                       int64_t M, int64_t mblocks,
-                                                                       int64_t nsb, int64_t units,
-                                                                       int64_t G) {
-    pdl_wait();  // the GEMM's pieces
-    const int64_t tile = blockIdx.x;
-    const int64_t ca = sk_cta_of(tile * nsb, units, G), cb = sk_cta_of(tile * nsb + nsb - 1, units, G);
-    if (ca == cb) return;  // written whole by its CTA
-    const int64_t n0 = (tile / mblocks) * kTM, m0 = (tile % mblocks) * kTN;
+// The pieces of one split tile, added in CTA order and stored. Each thread
+// takes 4 consecutive rows of a column (one 16-byte load per piece) and keeps
+// 4 columns in flight; a warp covers 128 rows of one column = 512 contiguous
+// bytes of every slot. kFull: all 128 columns hold tokens (the bound is a
+// constant); otherwise the first nq quads only (the columns the GEMM
+// epilogue wrote, tokens < M rounded up to 16).
+template <bool kFull, class T>
+__device__ __forceinline__ void fixup_tile(const float *__restrict__ part, T *__restrict__ C, int64_t N,
+                                           int64_t M, int64_t tile, int64_t n0, int64_t m0, int nq,
+                                           int64_t ca, int64_t cb, int64_t nsb, int64_t units, int64_t G) {
     constexpr int kQuads = kTM * kTN / 4;
-    for (int e0 = threadIdx.x; e0 < kQuads; e0 += 4 * kFixupThreads) {
+    const int nquads = kFull ? kQuads : nq;
+    for (int e0 = threadIdx.x; e0 < nquads; e0 += 4 * kFixupThreads) {
         float4 v[4];
         int rr[4], cc[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             const int e = e0 + h * kFixupThreads;  // kQuads is a multiple of 4 * kFixupThreads
             rr[h] = (e % (kTM / 4)) * 4;
-            cc[h] = e / (kTM / 4);
+            cc[h] = (kFull || e < nquads) ? e / (kTM / 4) : kTN;  // kTN: not written, skipped
         }
         for (int64_t k = ca; k <= cb; ++k) {
             const float *slot = part + sk_slot(k, tile, units, G, nsb);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
+                if (!kFull && cc[h] >= kTN) continue;
                 const float4 p = __ldcg(reinterpret_cast<const float4 *>(slot + cc[h] * kTM + rr[h]));
                 if (k == ca) {
                     v[h] = p;
@@ -70,7 +67,7 @@ __global__ void __launch_bounds__(kFixupThreads) stream_k_fixup_kernel(const flo
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             const int64_t m = m0 + cc[h], n = n0 + rr[h];
-            if (m < M) {
+            if ((kFull || cc[h] < kTN) && m < M) {
                 T *y = C + m * N + n;
                 if (n < N) y[0] = out_cast<T>(v[h].x);
                 if (n + 1 < N) y[1] = out_cast<T>(v[h].y);
@@ -79,6 +76,26 @@ __global__ void __launch_bounds__(kFixupThreads) stream_k_fixup_kernel(const flo
             }
         }
     }
+}
+
+// One CTA per tile (whole tiles return at once).
+template <class T>
+__global__ void __launch_bounds__(kFixupThreads) stream_k_fixup_kernel(const float *__restrict__ part,
+                                                                       T *__restrict__ C, int64_t N,
+                                                                       int64_t M, int64_t mblocks,
+                                                                       int64_t nsb, int64_t units,
+                                                                       int64_t G) {
+    pdl_wait();  // the GEMM's pieces
+    const int64_t tile = blockIdx.x;
+    const int64_t ca = sk_cta_of(tile * nsb, units, G), cb = sk_cta_of(tile * nsb + nsb - 1, units, G);
+    if (ca == cb) return;  // written whole by its CTA
+    const int64_t n0 = (tile / mblocks) * kTM, m0 = (tile % mblocks) * kTN;
+    const int64_t mv = M - m0 < kTN ? M - m0 : kTN;  // columns holding tokens
+    if (mv == kTN)
+        fixup_tile<true>(part, C, N, M, tile, n0, m0, 0, ca, cb, nsb, units, G);
+    else
+        fixup_tile<false>(part, C, N, M, tile, n0, m0, (int)((mv + 15) / 16 * 16) * (kTM / 4), ca, cb, nsb,
+                          units, G);
 }
 static_assert((kTM * kTN / 4) % (4 * kFixupThreads) == 0, "fixup tiling");
 
