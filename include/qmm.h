@@ -94,10 +94,12 @@ size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K);
 
 /* Bytes of the workspace qmm_mul_mat_ws needs for M activation rows of
  * length K against weights of type wt (Q4_0, Q4_K or Q6_K); 0 if invalid.
- * Above 16 tokens (Q4_0, Q4_K) it ends with a partial area of about 20 MB: with more 128 x 128
- * output tiles than SMs the tensor-core GEMM gives each SM an equal share of
- * the (tile, K-step) work (stream-K), and the parts of tiles that several
- * CTAs computed meet there before a second kernel adds them. */
+ * When the call runs the tensor-core GEMM (Q4_K above 16 tokens, Q4_0 and
+ * Q6_K above 8) it ends with a partial area of about 20 MB: with more 128 x
+ * 128 output tiles than SMs the GEMM gives each SM an equal share of the
+ * (tile, K-step) work (stream-K), with fewer than half as many it splits K
+ * over the SMs, and the parts of tiles that several CTAs computed meet
+ * there before a second kernel adds them. */
 size_t qmm_workspace_bytes(qmm_type wt, int64_t M, int64_t K);
 
 /* ---------------------------------------------------------------- quantizers */
@@ -180,11 +182,12 @@ qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon
  *   Q4_0: sum_b fp16(d_w) fp16(d_a) sum_{i<32} (q_i - 8) y_i
  *   Q4_K: sum_sb d_a (d * sum_j s_j sum_i q_i y_i - dmin * sum_j m_j sum_i y_i)
  *   Q6_K: sum_sb d_a d sum_j s_j sum_i q_i y_i  (16 groups j of 16, no min)
- * Up to 16 tokens (decode) the GEMV kernels take integer block sums with
- * fp32 accumulation across blocks. When M*K is small (one 16-token group of
- * at most 8192 elements) the activation quantizer runs inside the GEMV
- * kernel (one launch, no workspace). Above 16 tokens (prefill) the
- * tensor-core GEMM multiplies fp16 operands with fp32 accumulation: the
+ * Decode (Q4_K up to 16 tokens, Q4_0 and Q6_K up to 8): the GEMV kernels
+ * take integer block sums with fp32 accumulation across blocks. When M*K is
+ * small (16-token groups of at most 8192 elements) the activation quantizer
+ * runs inside the GEMV kernel (one launch per 16 tokens, no workspace), at
+ * any M. Otherwise, above those counts (prefill), the tensor-core GEMM
+ * multiplies fp16 operands with fp32 accumulation: the
  * weights decoded to fp16 (Q4_0 d (q - 8), Q4_K q fp16(d s_j) - fp16(dmin m_j),
  * Q6_K fp16(d s_j) q, each rounded once more to fp16) and the activations
  * as fp16(d_a y) from the same Q8 codes; every product is then within
@@ -220,8 +223,8 @@ qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t 
  * W_packed, N and Y are HOST arrays of n entries (device pointers to packed
  * weights / outputs, row counts); K, X, M, stream and the errors are those of
  * qmm_mul_mat, checked for every i. Matrices with N_i == 0 are skipped.
- * Above 16 tokens the prefill GEMM runs once per matrix on the shared
- * quantized activations. */
+ * Where qmm_mul_mat would run the tensor-core GEMM, it runs once per matrix
+ * on the shared quantized activations. */
 qmm_status qmm_mul_mat_multi(qmm_type wt, int n, const void *const *W_packed, const int64_t *N,
                              int64_t K, const float *X, int64_t M, float *const *Y,
                              qmm_stream_t stream);
@@ -247,8 +250,8 @@ qmm_status qmm_mul_mat_ws(qmm_type wt, const void *W_packed, int64_t N, int64_t 
  * qmm_mul_mat_prepared: Y [M, N] from packed weights and a workspace filled
  *   by qmm_quantize_activations with the same wt, M and K (the contents are
  *   not checked). The workspace is read-only here, so several calls may
- *   share it; above 16 tokens, when the output has more 128 x 128 tiles
- *   than SMs, the call therefore takes the GEMM's stream-K partial area
+ *   share it; when the GEMM splits tiles (more 128 x 128 output tiles than
+ *   SMs, or fewer than half as many), the call therefore takes its partial area
  *   (about 20 MB) from the device's default memory pool,
  *   stream-ordered, and frees it after the call on the same stream.
  *   Errors as qmm_mul_mat_ws, plus QMM_ERR_NOMEM for that area. */
@@ -297,7 +300,8 @@ qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int64_t N, int6
  * divide K) and K / G <= 256 (QMM_ERR_UNSUPPORTED above); W_packed,
  * scales, zeros and A 16-byte aligned, C 2-byte aligned.
  * M > 16 with more 128 x 128 output tiles than SMs runs over a persistent
- * grid (stream-K); tiles split across CTAs are added up, in a fixed order,
+ * grid (stream-K), with fewer than half as many it splits K over the SMs;
+ * tiles split across CTAs are added up, in a fixed order,
  * through a partial area of about 20 MB that such a call allocates and
  * frees stream-ordered on `stream` (the device's default memory pool).
  * Errors: QMM_ERR_ARG for sizes (M, N >= 0, K > 0, G > 0, K % G == 0) or
