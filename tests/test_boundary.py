@@ -82,3 +82,20 @@ def test_validation_without_gpu(lib):
     assert g(3, 16, 16, 1, 255, None) == 1
     assert lib.qmm_status_string(4) == b"QMM_ERR_TIMEOUT"
     assert lib.qmm_status_string(99) == b"QMM_ERR_UNKNOWN"
+
+
+def test_type_ids_agree(built_lib):
+    """The qmm_type values in include/qmm.h, the binding's constants and the
+    oracle's type ids name the same formats."""
+    import block_quantized_matmul_q4_gb300 as q
+    import oracle
+    text = open(HEADER).read()
+    ids = {n: int(v) for n, v in re.findall(r"\b(QMM_TYPE_[A-Z0-9_]+)\s*=\s*(\d+)", text)}
+    assert ids == {"QMM_TYPE_Q4_0": 0, "QMM_TYPE_Q4_K": 1, "QMM_TYPE_Q8_0": 2, "QMM_TYPE_Q8_K": 3,
+                   "QMM_TYPE_W4A16": 4, "QMM_TYPE_Q6_K": 5}
+    for name, v in ids.items():
+        assert getattr(q, name) == v
+    for name in ("Q4_0", "Q4_K", "Q8_0", "Q8_K", "Q6_K"):
+        assert getattr(oracle, name) == ids["QMM_TYPE_" + name]
+        assert oracle.BLOCK_BYTES[getattr(oracle, name)] == ctypes.CDLL(built_lib).qmm_block_bytes(
+            ids["QMM_TYPE_" + name])
