@@ -610,3 +610,25 @@ def test_edge_magnitudes(orc, scale):
         assert np.all(np.abs(res["y32"] - res["y64"]) <= 1e-5 * res["den"] + 1e-37)
         if scale == 0.0:
             assert not res["y32"].any()
+
+
+def test_q6_K_exact_blocks_round_trip(orc):
+    # blocks built from exact values: d = 2^e, int8 scales with |s| = 127 in
+    # some group, a -32 in every group (the code of largest magnitude), so the
+    # scale rule must return exactly these d, s_j and codes -- for many
+    # random draws, sign patterns and exponents
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        e = int(rng.integers(-14, 0))
+        s = rng.integers(1, 128, 16) * rng.choice([-1, 1], 16)
+        s[int(rng.integers(0, 16))] = 127 * int(rng.choice([-1, 1]))
+        q = rng.integers(-31, 32, 256)
+        for j in range(16):
+            q[16 * j + int(rng.integers(0, 16))] = -32
+        x = (2.0 ** e * s[np.arange(256) // 16] * q).astype(np.float32)
+        raw = orc.quantize(orc.Q6_K, x)
+        blk = raw.view(DT_Q6_K)[0, 0]
+        assert float(h2f(blk["d"])) == 2.0 ** e, trial
+        assert blk["scales"].tolist() == s.tolist(), trial
+        w = orc.dequantize(orc.Q6_K, raw, 256)[0]
+        assert np.array_equal(w, x), trial
