@@ -112,8 +112,9 @@ def test_host_layout_helpers(tmp_path):
     src = tmp_path / "geom.cu"
     src.write_text(SRC)
     exe = tmp_path / "geom"
-    r = subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17", "-O1", "-I", CSRC, "-I", os.path.join(ROOT, "include"),
-                        "-o", str(exe), str(src)], capture_output=True, text=True, timeout=600)
+    cmd = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17", "-O1",
+           "-I", CSRC, "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0 and out.stdout.strip().endswith("OK"), out.stdout[-2000:]
