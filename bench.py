@@ -159,11 +159,20 @@ def run_graphs(big, small, n_big):
         small.replay()
 
 
-def timed(stream, fn):
-    """Run fn() between CUDA events on `stream`; returns seconds."""
+LEAD_SPIN_CYCLES = 2_000_000  # about 1 ms of SM clock: covers the host's enqueue of the replays
+
+
+def timed(stream, fn, lead_spin=False):
+    """Run fn() between CUDA events on `stream`; returns seconds. With
+    lead_spin, a spin kernel runs on `stream` just before the start event, so
+    that the work fn() enqueues is queued up by the time the start event is
+    reached."""
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    if lead_spin:
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(LEAD_SPIN_CYCLES)
     a.record(stream)
     with torch.cuda.stream(stream):
         fn()
@@ -214,34 +223,42 @@ def gpu_arm(args, rank, world):
     def gemv_only(i):
         q.qmm_mul_mat_prepared(wt, copies[i % COPIES], N, K, ws, ws_bytes, M, Y, stream)
 
-    # warm-up outside capture (module load, function attributes), then graphs
+    # warm-up outside capture (module load, function attributes), then graphs:
+    # the timed region replays g_big n_big times and g_small once, exactly
+    # args.steps steps
     for i in range(4):
         step(i)
     torch.cuda.synchronize()
     n0 = q.qmm_kernel_launch_count()
     g_big = capture(step, GRAPH_STEPS, stream)
     launches_per_step = (q.qmm_kernel_launch_count() - n0) // GRAPH_STEPS
-    rem = args.steps % GRAPH_STEPS
+    n_big, rem = divmod(args.steps, GRAPH_STEPS)
     g_small = capture(step, rem, stream) if rem else None
     wrem = args.warmup % GRAPH_STEPS
     g_wsmall = capture(step, wrem, stream) if wrem else None
     g_gemv = capture(gemv_only, GRAPH_STEPS, stream)
     torch.cuda.synchronize()
 
-    # warm-up steps (untimed)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)  # the sampler's first rows
+    # warm-up (untimed): args.warmup steps, then one replay of every graph the
+    # timed region uses (a graph's first launch uploads it), back to back
     with torch.cuda.stream(stream):
         run_graphs(g_big, g_wsmall, args.warmup // GRAPH_STEPS)
+        if n_big:
+            g_big.replay()
+        if g_small is not None:
+            g_small.replay()
     torch.cuda.synchronize()
 
-    # timed region: exactly K steps
-    clocks = ClockSampler(dev.index)
+    # timed region: exactly K steps. A spin kernel ahead of the start event
+    # keeps the GPU busy while the host enqueues the replays, so the events
+    # time the steps and not the host's launch latency.
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    t = timed(stream, lambda: run_graphs(g_big, g_small, args.steps // GRAPH_STEPS))
-    clk = clocks.stop()
+    t = timed(stream, lambda: run_graphs(g_big, g_small, n_big), lead_spin=True)
     torch.cuda.synchronize()
     bw, bxq, by, bx = step_bytes(q, N, K, M)
     per_step = bw + bxq + by + bx
@@ -250,9 +267,12 @@ def gpu_arm(args, rank, world):
     # dominant kernel. With M*K this small the activation quantizer runs inside
     # the GEMV (one kernel per step), so the step's event timing is the
     # kernel's. The GEMV on prepared activations is timed too, back to back
-    # over the rotating copies.
-    reps = max(1, min(2000, args.steps // GRAPH_STEPS))
-    t_prep = timed(stream, lambda: run_graphs(g_gemv, None, reps)) / (reps * GRAPH_STEPS)
+    # over the rotating copies: one warm replay, then at least 8 timed.
+    reps = max(8, min(2000, args.steps // GRAPH_STEPS))
+    with torch.cuda.stream(stream):
+        g_gemv.replay()
+    t_prep = timed(stream, lambda: run_graphs(g_gemv, None, reps), lead_spin=True) / (reps * GRAPH_STEPS)
+    clk = clocks.stop()
     peaks = load_peaks()
     if launches_per_step == 1:
         kname, t_kern, kbytes = "gemv_q4_K_kernel<1, fused>", t / args.steps, per_step

@@ -126,20 +126,21 @@ void prepare_pool(cudaStream_t s) {
     g_pool_ready[d] = true;
 }
 
-// More than 16 tokens run the fp16-operand tensor-core GEMM on fp16(d_a y)
-// activations (Q4_0: 32-blocks, permuted for its converter; Q4_K and Q6_K:
-// Q8_K codes in natural order); fewer the decode GEMVs: Q4_K from 2 tokens
+// More than 16 tokens run the fp16-operand tensor-core GEMM on fp16(2^e d_a y)
+// activations with a power of two 2^e per token (Q4_0: 32-blocks, permuted
+// for its converter; Q4_K and Q6_K: Q8_K codes in natural order); fewer the decode GEMVs: Q4_K from 2 tokens
 // on the mma.sync kernel and its activation images, otherwise the scalar
 // GEMV and the planar layout.
 bool use_gemm(qmm_type wt, int64_t M) {
     return M >= (wt == QMM_TYPE_Q4_K ? kGemmMinM : kGemmMinMScalar);
 }
 
-// Prefill workspaces: the quantized activations (read-only in the GEMM),
-// then the stream-K partial area that calls owning the workspace use.
+// Prefill workspaces: the quantized activations with their per-token scales
+// (read-only in the GEMM), then the stream-K partial area that calls owning
+// the workspace use.
 size_t prefill_act_bytes(qmm_type wt, int64_t M, int64_t K) {
     (void)wt;
-    return align_up(q4_0_prefill_bytes(M, K), 256);  // fp16 [M][K] for every weight type
+    return prefill_operand_bytes(M, K);  // the same layout for every weight type
 }
 
 size_t ws_bytes_for(qmm_type wt, int64_t M, int64_t K) {

@@ -9,16 +9,22 @@
 //     per 32 elements, so no integer sum spans more than one MMA K step;
 //     both operands are rounded once to fp16 instead), Y fp32.
 //   Q4_K prefill (page 1, "K-quant", "6-bit 参数"): Y = a w^T, w =
-//     fp16(q fp16(d s_j) - fp16(dmin m_j)) per sub-block of 32 (one fused
-//     multiply-add), a = fp16(d_a y) from the Q8_K codes y of X, Y fp32.
+//     fp16(d s_j q - dmin m_j) per sub-block of 32: the weight is formed in
+//     fp32 (d s_j q is exact, one rounding for the difference) and rounded
+//     once to fp16, so its error stays within 2^-11 |w| even where the two
+//     terms nearly cancel; a = fp16(2^e d_a y) from the Q8_K codes y of X,
+//     Y fp32.
 //   Q6_K prefill (page 1, "更低的比特: Q6_K 与 Q2_K 的取舍"): Y = a w^T,
-//     w = fp16(fp16(d s_j) q) with q = u - 32 per group of 16, a = fp16(d_a
-//     y) from the Q8_K codes y of X (d_a per 256), Y fp32. s_j q reaches
-//     4064, past fp16's exact integers, so the integer-valued form of the
-//     Q4_K GEMM does not carry over; each operand element is rounded instead
-//     (relative error <= 2^-10 for w, 2^-11 for a).
-// In all, the codes are exact in fp16 and the weight is rounded once or
-// twice (relative error <= 2^-10); the MMA accumulates in fp32 over all of K.
+//     w = fp16(d s_j q) with q = u - 32 per group of 16 (d s_j q has at most
+//     24 significant bits, so it is exact in fp32 and rounded once), a as
+//     for Q4_K.
+// In all, the codes are exact, every weight is its exact value rounded once
+// to fp16 (relative error <= 2^-11), and every activation is 2^e d_a y
+// rounded once to fp16, with a power of two 2^e per token that puts the
+// token's largest block scale 2^e d_a in [2^7, 2^8) -- so its largest |a| is
+// below 2^15 and its smaller ones stay in fp16's normal range for 28 more
+// octaves, whatever the magnitude of X -- and that the epilogue takes off
+// again (exact: a power of two). The MMA accumulates in fp32 over all of K.
 //
 // Tile = 128 weight rows (MMA M) x 128 tokens (MMA N). Up to one tile per SM
 // the grid has one CTA per tile; with more, one CTA per SM walks a
@@ -102,6 +108,7 @@ struct Args {
     // unit u = t * nsb + round; CTA c takes units [c U / G, (c+1) U / G)
     int64_t mblocks, units;
     float *part;  // split tiles: [CTA][slot 0: first tile, 1: last tile][128 cols][128 rows]
+    const float *tok_scale;  // 2^-e per token (padded to 16), or null (W4A16)
 };
 
 __device__ __forceinline__ uint32_t lop_or(uint32_t x, uint32_t mask) {
@@ -160,25 +167,84 @@ __device__ __forceinline__ void lut_scaled_word(uint32_t w, const uint32_t *tbl,
     p67 = hmul2_u(tbl[(t2 >> 8) & 0xFF], ss);
 }
 
-// The 4 Q6_K codes of one byte word u (bytes 0..63, stored u = q + 32) as two
-// fp16 pairs (bytes 0, 1) and (2, 3), times ds (fp16(d s_j) twice): each
-// byte becomes fp16(1024 + u) by placing 0x64 above it, 1024 + 32 comes
-// off exactly, and the product with ds is one rounding.
-__device__ __forceinline__ void q6k_pairs(uint32_t u, uint32_t ds, uint32_t &p01, uint32_t &p23) {
-    constexpr uint32_t k1056 = 0x64206420u;  // fp16 1024 + 32 twice
-    p01 = hmul2_u(hsub2_u(__byte_perm(u, 0x64646464u, 0x4140), k1056), ds);
-    p23 = hmul2_u(hsub2_u(__byte_perm(u, 0x64646464u, 0x4342), k1056), ds);
+// Pairs of fp32 values (Blackwell's f32x2 arithmetic: one instruction for
+// two lanes of work).
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2(float lo, float hi) { return pack2(__float_as_uint(lo), __float_as_uint(hi)); }
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// fp32 pair -> fp16 pair (first value in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t h2_of_f2(uint64_t v) {
+    uint32_t lo, hi, r;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
+    return r;
+}
+// (x & mask) | 2^23's bit pattern: a field of x at bit p (p + width <= 23)
+// becomes the float 2^23 + field 2^p, exactly.
+__device__ __forceinline__ uint32_t magic23(uint32_t x, uint32_t mask) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(mask), "r"(0x4B000000u));
+    return d;
+}
+constexpr float kTwo23 = 8388608.0f;
+
+// The 4 Q6_K codes of one byte word u (bytes 0..3, stored u = q + 32) as two
+// fp16 pairs (bytes 0, 1) and (2, 3) of d s_j q: byte b sits at bit p = 0,
+// 8, 16 of u or 8 of u >> 16, its float 2^23 + u 2^p less 2^23 + 32 2^p is
+// q 2^p exactly, and the product with (d s_j) 2^-p is exact (at most 24
+// significant bits); one rounding, to fp16. s01 = (ds, ds 2^-8), s23 = (ds
+// 2^-16, ds 2^-8).
+__device__ __forceinline__ void q6k_pairs(uint32_t u, uint64_t s01, uint64_t s23, uint32_t &p01, uint32_t &p23) {
+    const uint32_t v = u >> 16;
+    const uint64_t f01 = pack2(magic23(u, 0x3Fu), magic23(u, 0x3F00u));
+    const uint64_t f23 = pack2(magic23(u, 0x3F0000u), magic23(v, 0x3F00u));
+    const uint64_t b01 = f2(-(kTwo23 + 32.0f), -(kTwo23 + 8192.0f));
+    const uint64_t b23 = f2(-(kTwo23 + 2097152.0f), -(kTwo23 + 8192.0f));
+    p01 = h2_of_f2(mul_f2(add_f2(f01, b01), s01));
+    p23 = h2_of_f2(mul_f2(add_f2(f23, b23), s23));
 }
 
-// The 4 Q4_K codes q (0..15) of one byte word as two fp16 pairs (bytes 0, 1)
-// and (2, 3) of q fp16(d s_j) - fp16(dmin m_j): q is exact (1024 + q less
-// 1024) and the fused multiply-add rounds once. ds = fp16(d s_j) twice,
-// ndm = -fp16(dmin m_j) twice.
-__device__ __forceinline__ void q4k_pairs(uint32_t q, uint32_t ds, uint32_t ndm, uint32_t &p01,
-                                          uint32_t &p23) {
-    constexpr uint32_t k1024 = 0x64006400u;
-    p01 = hfma2_u(hsub2_u(__byte_perm(q, 0x64646464u, 0x4140), k1024), ds, ndm);
-    p23 = hfma2_u(hsub2_u(__byte_perm(q, 0x64646464u, 0x4342), k1024), ds, ndm);
+// The 8 Q4_K codes of one word of qs bytes: the low nibbles are elements
+// 0..3 of the low sub-block, the high nibbles elements 0..3 of the high one.
+// Each becomes q 2^p exactly (its float 2^23 + q 2^p less 2^23; the nibble at
+// bit p = 0, 8, 16 of w or 12 of w >> 12 for the low set, 4, 12 of w or 8,
+// 16 of w >> 12 for the high set), then one fused multiply-add with
+// (d s_j) 2^-p and -dmin m_j: the fp32 weight d s_j q - dmin m_j with one
+// rounding, then rounded once to fp16. Output: fp16 pairs (0, 1), (2, 3) of
+// each set. sl01 = (dsl, dsl 2^-8), sl23 = (dsl 2^-16, dsl 2^-12), sh01 =
+// (dsh 2^-4, dsh 2^-12), sh23 = (dsh 2^-8, dsh 2^-16); nml, nmh = -dmin m_j
+// twice.
+__device__ __forceinline__ void q4k_word(uint32_t w, uint64_t sl01, uint64_t sl23, uint64_t nml, uint64_t sh01,
+                                         uint64_t sh23, uint64_t nmh, uint32_t &l01, uint32_t &l23,
+                                         uint32_t &h01, uint32_t &h23) {
+    const uint32_t v = w >> 12;
+    const uint64_t bias = f2(-kTwo23, -kTwo23);
+    const uint64_t fl01 = pack2(magic23(w, 0xFu), magic23(w, 0xF00u));
+    const uint64_t fl23 = pack2(magic23(w, 0xF0000u), magic23(v, 0xF000u));
+    const uint64_t fh01 = pack2(magic23(w, 0xF0u), magic23(w, 0xF000u));
+    const uint64_t fh23 = pack2(magic23(v, 0xF00u), magic23(v, 0xF0000u));
+    l01 = h2_of_f2(fma_f2(add_f2(fl01, bias), sl01, nml));
+    l23 = h2_of_f2(fma_f2(add_f2(fl23, bias), sl23, nml));
+    h01 = h2_of_f2(fma_f2(add_f2(fh01, bias), sh01, nmh));
+    h23 = h2_of_f2(fma_f2(add_f2(fh23, bias), sh23, nmh));
 }
 
 // Columns m0 .. m0+15 of output row n (C is [M][N]: fp16 for W4A16, fp32 for
@@ -194,6 +260,19 @@ __device__ __forceinline__ void store_cols(const Args &a, int64_t m0, int64_t n,
             else
                 static_cast<float *>(a.C)[m * a.N + n] = v[j];
         }
+    }
+}
+
+// v[j] *= 2^-e of token j of the 16 at ts (the activation prescale taken
+// off: exact, a power of two). ts is 64-byte aligned and padded to 16 tokens.
+__device__ __forceinline__ void unscale16(const float *ts, float v[16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 t = __ldg(reinterpret_cast<const float4 *>(ts) + i);
+        v[4 * i] *= t.x;
+        v[4 * i + 1] *= t.y;
+        v[4 * i + 2] *= t.z;
+        v[4 * i + 3] *= t.w;
     }
 }
 
@@ -453,21 +532,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t f = k4_field(hdr.y, hdr.z, hdr.w, c);
                         const float dw = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
                         const float dmw = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
-                        uint32_t ds[2], dm[2];  // fp16(d s_j), -fp16(dmin m_j), twice; low then high sub-block
+                        // d s_j and dmin m_j of the low (h = 0) and high sub-block:
+                        // exact in fp32 (11-bit by 6-bit significands)
+                        float ds[2], dm[2];
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const uint32_t sv = (f >> (12 * h)) & 63u, mv = (f >> (12 * h + 6)) & 63u;
-                            const uint32_t hs = __half_as_ushort(__float2half_rn(__fmul_rn(dw, (float)sv)));
-                            const uint32_t hm = __half_as_ushort(__float2half_rn(__fmul_rn(dmw, (float)mv))) ^ 0x8000u;
-                            ds[h] = hs | (hs << 16);
-                            dm[h] = hm | (hm << 16);
+                            ds[h] = __fmul_rn(dw, (float)((f >> (12 * h)) & 63u));
+                            dm[h] = __fmul_rn(dmw, (float)((f >> (12 * h + 6)) & 63u));
                         }
+                        const uint64_t sl01 = f2(ds[0], ds[0] * 0x1p-8f), sl23 = f2(ds[0] * 0x1p-16f, ds[0] * 0x1p-12f);
+                        const uint64_t sh01 = f2(ds[1] * 0x1p-4f, ds[1] * 0x1p-12f);
+                        const uint64_t sh23 = f2(ds[1] * 0x1p-8f, ds[1] * 0x1p-16f);
+                        const uint64_t nml = f2(-dm[0], -dm[0]), nmh = f2(-dm[1], -dm[1]);
                         const uint32_t qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-                        for (int w = 0; w < 8; ++w) {
-                            q4k_pairs(qv[w] & 0x0F0F0F0Fu, ds[0], dm[0], lo[2 * w], lo[2 * w + 1]);
-                            q4k_pairs((qv[w] >> 4) & 0x0F0F0F0Fu, ds[1], dm[1], hi[2 * w], hi[2 * w + 1]);
-                        }
+                        for (int w = 0; w < 8; ++w)
+                            q4k_word(qv[w], sl01, sl23, nml, sh01, sh23, nmh, lo[2 * w], lo[2 * w + 1], hi[2 * w],
+                                     hi[2 * w + 1]);
                     } else if (F == kQ6K) {
                         // chunk c = elements 64c .. 64c+63 of super-block sb: the
                         // low nibbles of ql bytes 32c .. 32c+31 are its elements
@@ -483,12 +564,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint4 hw = *reinterpret_cast<const uint4 *>(row + 128 + 16 * c);
                         const uint32_t sc4 = *reinterpret_cast<const uint32_t *>(rec + kQ6ScOff + 16 * r + 4 * c);
                         const float dw = __half2float(*reinterpret_cast<const __half *>(rec + kQ6DOff + 2 * r));
-                        uint32_t ds[4];  // fp16(d s) twice: (tl 0, low), (tl 0, high), (tl 1, low), (tl 1, high)
+                        // (d s) 2^-p pairs, p as q6k_pairs takes them, for (tl 0, low),
+                        // (tl 0, high), (tl 1, low), (tl 1, high); d s is exact in fp32
+                        uint64_t s01[4], s23[4];
 #pragma unroll
                         for (int b = 0; b < 4; ++b) {
                             const float v = __fmul_rn(dw, (float)(int)(int8_t)(uint8_t)(sc4 >> (8 * b)));
-                            const uint32_t h = __half_as_ushort(__float2half_rn(v));
-                            ds[b] = h | (h << 16);
+                            s01[b] = f2(v, v * 0x1p-8f);
+                            s23[b] = f2(v * 0x1p-16f, v * 0x1p-8f);
                         }
                         const uint32_t qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
@@ -496,8 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int tl = w >> 2, ww = w & 3;
                             const uint32_t ul = q6k_u(qv[w], tl ? hw.z : hw.x, ww);
                             const uint32_t uh = q6k_u(qv[w] >> 4, tl ? hw.w : hw.y, ww);
-                            q6k_pairs(ul, ds[2 * tl], lo[2 * w], lo[2 * w + 1]);
-                            q6k_pairs(uh, ds[2 * tl + 1], hi[2 * w], hi[2 * w + 1]);
+                            q6k_pairs(ul, s01[2 * tl], s23[2 * tl], lo[2 * w], lo[2 * w + 1]);
+                            q6k_pairs(uh, s01[2 * tl + 1], s23[2 * tl + 1], hi[2 * w], hi[2 * w + 1]);
                         }
                     } else {
                         // chunk c = blocks 2c, 2c + 1 of the round. Byte l of a block
@@ -570,6 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float v[16];
                         tc::tmem_ld16(acc + (uint32_t)(c16 * 16), v);
                         tc::tmem_ld_wait();
+                        if (F != kW4A16) unscale16(a.tok_scale + m0 + c16 * 16, v);
                         if (row_ok) store_cols<F>(a, m0 + c16 * 16, n, v);
                     }
                 }
@@ -583,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float v[16];
                         tc::tmem_ld16(acc + (uint32_t)(c16 * 16), v);
                         tc::tmem_ld_wait();
+                        if (F != kW4A16) unscale16(a.tok_scale + m0 + c16 * 16, v);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) mine[(c16 * 16 + j) * kBM] = v[j];
                     }
@@ -604,31 +689,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// ------------------------------------------------------------------ Q4_0 prefill quantizer
-// X fp32 -> Q8_0 codes y and fp16 scale d per 32 (the arithmetic of the Q8_0
-// quantizer: amax / 127, codes rounded half away from zero), then
-// a = fp16(f32(d) * y) written with the elements of each block permuted to
+// ------------------------------------------------------------------ prefill activations
+// The fp16 activation operand a = fp16(2^e d_a y) [M][K], y the bit-exact Q8
+// codes and d_a their block scale (Q8_0: the fp16 scale widened; Q8_K: fp32),
+// with one power of two 2^e per token: e puts the token's largest block scale
+// 2^e d_a in [2^7, 2^8), so |a| < 127 2^8 < 65504 and the token's smaller
+// values keep fp16's full precision down to 2^-28 of its largest. 2^-e goes to
+// the per-token scale array (after the operand in the workspace, padded with
+// 1.0 to a multiple of 16 tokens) that the GEMM epilogue multiplies by.
+// One CTA of 256 threads per token: max |x| (or max d) over the token first,
+// then the blocks. The block scales are monotone in the block's max |x|, so
+// the token's largest d_a is the scale of the token's max |x|.
+constexpr int kActThreads = 256;
+
+__device__ __forceinline__ int prescale_exp(float dmax) {
+    const int ef = (int)((__float_as_uint(dmax) >> 23) & 0xFFu);
+    if (!(dmax > 0.0f) || ef == 255) return 0;  // zero token, or not finite
+    if (ef == 0) return 126;                    // subnormal scale
+    return min(126, max(-126, 134 - ef));       // 2^e dmax in [2^7, 2^8)
+}
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+__host__ __device__ inline int64_t pad16(int64_t M) { return (M + 15) / 16 * 16; }
+
+// Max of v >= +0 over the CTA; every thread gets it.
+__device__ __forceinline__ float cta_max_nonneg(float v, float *red) {
+    v = warp_max_nonneg(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kActThreads / 32; ++i) r = fmaxf(r, red[i]);
+    return r;
+}
+
+// max |x| over the token's K values (16-byte loads; K % 32 == 0).
+__device__ __forceinline__ float token_amax(const float *__restrict__ x, int64_t K, float *red) {
+    float a = 0.0f;
+    for (int64_t i = threadIdx.x; i < K / 4; i += kActThreads) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(x) + i);
+        a = fmaxf(fmaxf(a, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+    }
+    return cta_max_nonneg(a, red);
+}
+
+__device__ __forceinline__ void store_tok_scale(float *ts, int64_t M, int e) {
+    if (threadIdx.x == 0) ts[blockIdx.x] = pow2f(-e);
+    if (blockIdx.x == 0)
+        for (int64_t i = M + threadIdx.x; i < pad16(M); i += kActThreads) ts[i] = 1.0f;
+}
+
+// Q4_0: X fp32 -> Q8_0 codes y and fp16 scale d per 32 (the arithmetic of
+// the Q8_0 quantizer: amax / 127, codes rounded half away from zero), then
+// a = fp16(2^e f32(d) y) written with the elements of each block permuted to
 // the order the Q4_0 converter puts the weights in: element e (e' = e mod 16,
 // i = e' / 4, r = e' mod 4) goes to position 8 i + 4 (e >= 16) + 2 (r mod 2)
-// + r / 2. A warp takes 8 blocks per step, 4 lanes per block and 8
-// consecutive elements per lane (two 16-byte loads); the 4 elements
-// 4i .. 4i+3 of a lane land at positions 8 i + 4 (e >= 16) + (0, 2, 1, 3),
-// so each lane writes two 8-byte groups.
-__global__ void __launch_bounds__(256) quantize_q4_0_prefill_kernel(const float *__restrict__ X,
-                                                                    __half *__restrict__ out,
-                                                                    int64_t nblocks) {
+// + r / 2. 4 lanes per block, 8 consecutive elements per lane (two 16-byte
+// loads); the 4 elements 4i .. 4i+3 of a lane land at positions 8 i + 4 (e >=
+// 16) + (0, 2, 1, 3), so each lane writes two 8-byte groups.
+__global__ void __launch_bounds__(kActThreads) quantize_q4_0_prefill_kernel(const float *__restrict__ X,
+                                                                            __half *__restrict__ out,
+                                                                            float *__restrict__ ts,
+                                                                            int64_t M, int64_t K) {
     pdl_launch_dependents();
-    const int lane = threadIdx.x & 31, j = lane & 3;  // j: elements 8j .. 8j+7 of the block
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    __shared__ float red[kActThreads / 32];
+    const int64_t m = blockIdx.x, nb = K / QK4_0;
+    const float *x = X + m * K;
+    const float dmax = __half2float(__float2half_rn(__fdiv_rn(token_amax(x, K, red), 127.0f)));
+    const int ex = prescale_exp(dmax);
+    const float p2 = pow2f(ex);
+    store_tok_scale(ts, M, ex);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, j = lane & 3;  // j: elements 8j .. 8j+7
     // positions of this lane's two groups: elements 8j + 4g .. 8j + 4g + 3
     const int e0 = 8 * j, base0 = 8 * ((e0 & 15) >> 2) + ((e0 >> 4) << 2);
     const int e1 = e0 + 4, base1 = 8 * ((e1 & 15) >> 2) + ((e1 >> 4) << 2);
-    for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w * 8 < nblocks; w += nwarps) {
-        const int64_t b = w * 8 + (lane >> 2);
-        const bool live = b < nblocks;
+    for (int64_t g = warp; g * 8 < nb; g += kActThreads / 32) {
+        const int64_t b = g * 8 + (lane >> 2);
+        const bool live = b < nb;
         float4 v0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), v1 = v0;
         if (live) {
-            const float4 *src = reinterpret_cast<const float4 *>(X + b * QK4_0 + e0);
+            const float4 *src = reinterpret_cast<const float4 *>(x + b * QK4_0 + e0);
             v0 = src[0];
             v1 = src[1];
         }
@@ -640,49 +779,63 @@ __global__ void __launch_bounds__(256) quantize_q4_0_prefill_kernel(const float 
         ab = max(ab, __shfl_xor_sync(0xffffffffu, ab, 2));
         const float d = __fdiv_rn(__uint_as_float(ab), 127.0f);
         const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
-        const float df = __half2float(__float2half_rn(d));
-        auto val = [&](float x) { return __float2half_rn(df * (float)q8_code(x, id)); };
+        const float sd = __fmul_rn(__half2float(__float2half_rn(d)), p2);  // exact
+        auto val = [&](float xv) { return __float2half_rn(__fmul_rn(sd, (float)q8_code(xv, id))); };
         if (live) {
-            __half *dst = out + b * QK4_0;
+            __half *dst = out + (m * nb + b) * QK4_0;
             const __half2 p0 = __halves2half2(val(v0.x), val(v0.z)), p1 = __halves2half2(val(v0.y), val(v0.w));
-            const __half2 p2 = __halves2half2(val(v1.x), val(v1.z)), p3 = __halves2half2(val(v1.y), val(v1.w));
+            const __half2 q0 = __halves2half2(val(v1.x), val(v1.z)), q1 = __halves2half2(val(v1.y), val(v1.w));
             *reinterpret_cast<uint2 *>(dst + base0) = make_uint2(h2_bits(p0), h2_bits(p1));
-            *reinterpret_cast<uint2 *>(dst + base1) = make_uint2(h2_bits(p2), h2_bits(p3));
+            *reinterpret_cast<uint2 *>(dst + base1) = make_uint2(h2_bits(q0), h2_bits(q1));
         }
     }
 }
 
 // The same operand from canonical Q8_0 blocks [M][nb] x 34 B, for
-// qmm_mul_mat_q8.
-__global__ void __launch_bounds__(256) import_q8_0_prefill_kernel(const uint8_t *__restrict__ Xq,
-                                                                  __half *__restrict__ out,
-                                                                  int64_t nblocks) {
+// qmm_mul_mat_q8: the token's largest |d| first, then one warp per block.
+__global__ void __launch_bounds__(kActThreads) import_q8_0_prefill_kernel(const uint8_t *__restrict__ Xq,
+                                                                          __half *__restrict__ out,
+                                                                          float *__restrict__ ts,
+                                                                          int64_t M, int64_t K) {
     pdl_launch_dependents();
-    const int lane = threadIdx.x & 31;
+    __shared__ float red[kActThreads / 32];
+    const int64_t m = blockIdx.x, nb = K / QK4_0;
+    const uint8_t *row = Xq + m * nb * B_Q8_0;
+    float a = 0.0f;
+    for (int64_t b = threadIdx.x; b < nb; b += kActThreads)
+        a = fmaxf(a, fabsf(__half2float(*reinterpret_cast<const __half *>(row + b * B_Q8_0))));
+    const int ex = prescale_exp(cta_max_nonneg(a, red));
+    const float p2 = pow2f(ex);
+    store_tok_scale(ts, M, ex);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = lane, ep = e & 15, i = ep >> 2, r = ep & 3;
     const int pos = 8 * i + ((e >> 4) << 2) + 2 * (r & 1) + (r >> 1);
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += nwarps) {
-        const uint8_t *blk = Xq + b * B_Q8_0;
+    for (int64_t b = warp; b < nb; b += kActThreads / 32) {
+        const uint8_t *blk = row + b * B_Q8_0;
         const int q = (int8_t)blk[2 + lane];
-        const float d = __half2float(*reinterpret_cast<const __half *>(blk));
-        out[b * QK4_0 + pos] = __float2half_rn(d * (float)q);
+        const float sd = __fmul_rn(__half2float(*reinterpret_cast<const __half *>(blk)), p2);
+        out[(m * nb + b) * QK4_0 + pos] = __float2half_rn(__fmul_rn(sd, (float)q));
     }
 }
 
-// ------------------------------------------------------------------ Q6_K prefill activations
-// X fp32 -> Q8_K codes y and fp32 scale d per 256 (the Q8_K quantizer's
-// arithmetic: amax / 127, codes rounded half away from zero), then
-// a = fp16(d * y) in natural order [M][K]. One warp per super-block, 8
-// consecutive elements per lane (two 16-byte loads, one 16-byte store).
-__global__ void __launch_bounds__(256) quantize_q8_K_f16_kernel(const float *__restrict__ X,
-                                                                    __half *__restrict__ out,
-                                                                    int64_t nblocks) {
+// Q4_K and Q6_K: X fp32 -> Q8_K codes y and fp32 scale d per 256 (the Q8_K
+// quantizer's arithmetic: amax / 127, codes rounded half away from zero),
+// then a = fp16(2^e d y) in natural order [M][K]. One warp per super-block,
+// 8 consecutive elements per lane (two 16-byte loads, one 16-byte store).
+__global__ void __launch_bounds__(kActThreads) quantize_q8_K_f16_kernel(const float *__restrict__ X,
+                                                                        __half *__restrict__ out,
+                                                                        float *__restrict__ ts, int64_t M,
+                                                                        int64_t K) {
     pdl_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += nwarps) {
-        const float4 *src = reinterpret_cast<const float4 *>(X + b * QK_K + 8 * lane);
+    __shared__ float red[kActThreads / 32];
+    const int64_t m = blockIdx.x, nsb = K / QK_K;
+    const float *x = X + m * K;
+    const int ex = prescale_exp(__fdiv_rn(token_amax(x, K, red), 127.0f));
+    const float p2 = pow2f(ex);
+    store_tok_scale(ts, M, ex);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t b = warp; b < nsb; b += kActThreads / 32) {
+        const float4 *src = reinterpret_cast<const float4 *>(x + b * QK_K + 8 * lane);
         const float4 v0 = src[0], v1 = src[1];
         const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         float a = 0.0f;
@@ -690,27 +843,39 @@ __global__ void __launch_bounds__(256) quantize_q8_K_f16_kernel(const float *__r
         for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
         const float d = __fdiv_rn(warp_max_nonneg(a), 127.0f);
         const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+        const float sd = __fmul_rn(d, p2);  // exact
         uint32_t h[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const __half lo = __float2half_rn(__fmul_rn(d, (float)q8_code(v[2 * i], id)));
-            const __half hi = __float2half_rn(__fmul_rn(d, (float)q8_code(v[2 * i + 1], id)));
+            const __half lo = __float2half_rn(__fmul_rn(sd, (float)q8_code(v[2 * i], id)));
+            const __half hi = __float2half_rn(__fmul_rn(sd, (float)q8_code(v[2 * i + 1], id)));
             h[i] = h2_bits(__halves2half2(lo, hi));
         }
-        *reinterpret_cast<uint4 *>(out + b * QK_K + 8 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(out + (m * nsb + b) * QK_K + 8 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
     }
 }
 
 // The same operand from canonical Q8_K blocks [M][nsb] x 292 B, for
-// qmm_mul_mat_q8: one warp per block, 8 codes per lane.
-__global__ void __launch_bounds__(256) import_q8_K_f16_kernel(const uint8_t *__restrict__ Xq,
-                                                              __half *__restrict__ out, int64_t nblocks) {
+// qmm_mul_mat_q8: the token's largest |d| first, then one warp per block, 8
+// codes per lane.
+__global__ void __launch_bounds__(kActThreads) import_q8_K_f16_kernel(const uint8_t *__restrict__ Xq,
+                                                                      __half *__restrict__ out,
+                                                                      float *__restrict__ ts, int64_t M,
+                                                                      int64_t K) {
     pdl_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += nwarps) {
-        const uint8_t *blk = Xq + b * B_Q8_K;
-        const float d = *reinterpret_cast<const float *>(blk);
+    __shared__ float red[kActThreads / 32];
+    const int64_t m = blockIdx.x, nsb = K / QK_K;
+    const uint8_t *row = Xq + m * nsb * B_Q8_K;
+    float a = 0.0f;
+    for (int64_t b = threadIdx.x; b < nsb; b += kActThreads)
+        a = fmaxf(a, fabsf(*reinterpret_cast<const float *>(row + b * B_Q8_K)));
+    const int ex = prescale_exp(cta_max_nonneg(a, red));
+    const float p2 = pow2f(ex);
+    store_tok_scale(ts, M, ex);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t b = warp; b < nsb; b += kActThreads / 32) {
+        const uint8_t *blk = row + b * B_Q8_K;
+        const float sd = __fmul_rn(*reinterpret_cast<const float *>(blk), p2);
         // 292-byte blocks: 4-byte loads only
         const uint32_t cw[2] = {*reinterpret_cast<const uint32_t *>(blk + 4 + 8 * lane),
                                 *reinterpret_cast<const uint32_t *>(blk + 8 + 8 * lane)};
@@ -719,10 +884,10 @@ __global__ void __launch_bounds__(256) import_q8_K_f16_kernel(const uint8_t *__r
         for (int i = 0; i < 4; ++i) {
             const int q0 = (int)(int8_t)(uint8_t)(cw[i >> 1] >> (16 * (i & 1)));
             const int q1 = (int)(int8_t)(uint8_t)(cw[i >> 1] >> (16 * (i & 1) + 8));
-            h[i] = h2_bits(__halves2half2(__float2half_rn(__fmul_rn(d, (float)q0)),
-                                          __float2half_rn(__fmul_rn(d, (float)q1))));
+            h[i] = h2_bits(__halves2half2(__float2half_rn(__fmul_rn(sd, (float)q0)),
+                                          __float2half_rn(__fmul_rn(sd, (float)q1))));
         }
-        *reinterpret_cast<uint4 *>(out + b * QK_K + 8 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(out + (m * nsb + b) * QK_K + 8 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
     }
 }
 
@@ -756,15 +921,19 @@ cudaError_t launch_stream_k(Args a, const CUtensorMap &tmap_w, const CUtensorMap
 
 }  // namespace
 
+// The prefill workspace: the fp16 operand [M][K], then the per-token scales.
+static size_t operand_bytes(int64_t M, int64_t K) { return align_up((size_t)M * K * 2, 256); }
+static float *tok_scales(const void *ws, int64_t M, int64_t K) {
+    return reinterpret_cast<float *>(static_cast<uint8_t *>(const_cast<void *>(ws)) + operand_bytes(M, K));
+}
+size_t prefill_operand_bytes(int64_t M, int64_t K) {
+    return operand_bytes(M, K) + align_up((size_t)pad16(M) * sizeof(float), 256);
+}
+
 cudaError_t launch_import_q4_0_prefill(const void *Xq, void *ws, int64_t M, int64_t K,
                                        cudaStream_t s) {
-    const int64_t nblocks = M * (K / QK4_0);
-    int64_t grid = (nblocks + 7) / 8;
-    const int64_t cap = (int64_t)sm_count() * 16;
-    if (grid > cap) grid = cap;
-    if (grid < 1) grid = 1;
-    import_q8_0_prefill_kernel<<<(int)grid, 256, 0, s>>>(static_cast<const uint8_t *>(Xq),
-                                                         static_cast<__half *>(ws), nblocks);
+    import_q8_0_prefill_kernel<<<(unsigned)M, kActThreads, 0, s>>>(
+        static_cast<const uint8_t *>(Xq), static_cast<__half *>(ws), tok_scales(ws, M, K), M, K);
     count_launch();
     return cudaGetLastError();
 }
@@ -784,6 +953,7 @@ cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, 
     a.spg = (int)(G / kW4StepK);
     a.err = device_error_word();
     a.part = part;
+    a.tok_scale = nullptr;
     const int64_t nsteps = K / kW4StepK, ntiles16 = (N + kW4Tile - 1) / kW4Tile;
     CUtensorMap tmap_w, tmap_a;
     // packed weights as [16-row tile][step][1 KB], in 4-byte units
@@ -797,17 +967,10 @@ cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, 
     return launch_stream_k<kW4A16>(a, tmap_w, tmap_w, tmap_a, s);
 }
 
-// fp16 activations [M][K]
-size_t q4_0_prefill_bytes(int64_t M, int64_t K) { return align_up((size_t)M * K * 2, 256); }
-
 cudaError_t launch_quantize_q4_0_prefill(const float *X, void *ws, int64_t M, int64_t K,
                                          cudaStream_t s) {
-    const int64_t nblocks = M * (K / QK4_0);
-    int64_t grid = (nblocks + 63) / 64;  // 8 warps x 8 blocks
-    const int64_t cap = (int64_t)sm_count() * 16;
-    if (grid > cap) grid = cap;
-    if (grid < 1) grid = 1;
-    quantize_q4_0_prefill_kernel<<<(int)grid, 256, 0, s>>>(X, static_cast<__half *>(ws), nblocks);
+    quantize_q4_0_prefill_kernel<<<(unsigned)M, kActThreads, 0, s>>>(X, static_cast<__half *>(ws),
+                                                                    tok_scales(ws, M, K), M, K);
     count_launch();
     return cudaGetLastError();
 }
@@ -826,6 +989,7 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
     a.spg = 1;
     a.err = device_error_word();
     a.part = part;
+    a.tok_scale = tok_scales(ws, M, K);
     const int64_t nb = K / QK4_0, ntiles = tiles_of(N);
     const uint64_t tile_bytes = (uint64_t)nb * kQ4Tile * B_Q4_0;
     CUtensorMap tmap_w, tmap_d, tmap_a;
@@ -847,24 +1011,17 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
 }
 
 // ------------------------------------------------------------------ Q6_K prefill
-static int warp_grid(int64_t nblocks) {
-    int64_t grid = (nblocks + 7) / 8;  // 8 warps per CTA, one block each
-    const int64_t cap = (int64_t)sm_count() * 16;
-    if (grid > cap) grid = cap;
-    return (int)(grid < 1 ? 1 : grid);
-}
-
 cudaError_t launch_quantize_q8_K_f16(const float *X, void *ws, int64_t M, int64_t K, cudaStream_t s) {
-    const int64_t nblocks = M * (K / QK_K);
-    quantize_q8_K_f16_kernel<<<warp_grid(nblocks), 256, 0, s>>>(X, static_cast<__half *>(ws), nblocks);
+    quantize_q8_K_f16_kernel<<<(unsigned)M, kActThreads, 0, s>>>(X, static_cast<__half *>(ws),
+                                                                tok_scales(ws, M, K), M, K);
     count_launch();
     return cudaGetLastError();
 }
 
 cudaError_t launch_import_q8_K_f16(const void *Xq, void *ws, int64_t M, int64_t K, cudaStream_t s) {
-    const int64_t nblocks = M * (K / QK_K);
-    import_q8_K_f16_kernel<<<warp_grid(nblocks), 256, 0, s>>>(static_cast<const uint8_t *>(Xq),
-                                                               static_cast<__half *>(ws), nblocks);
+    import_q8_K_f16_kernel<<<(unsigned)M, kActThreads, 0, s>>>(static_cast<const uint8_t *>(Xq),
+                                                              static_cast<__half *>(ws), tok_scales(ws, M, K),
+                                                              M, K);
     count_launch();
     return cudaGetLastError();
 }
@@ -883,6 +1040,7 @@ cudaError_t launch_gemm_q4_K_f16(const void *Wp, int64_t N, int64_t K, const voi
     a.spg = 1;
     a.err = device_error_word();
     a.part = part;
+    a.tok_scale = tok_scales(ws, M, K);
     const int64_t nsb = K / QK_K;
     constexpr int kRec = kTileRows * B_Q4_K;  // 1152 B: one (tile, super-block)
     CUtensorMap tmap_w, tmap_a;
@@ -910,6 +1068,7 @@ cudaError_t launch_gemm_q6_K(const void *Wp, int64_t N, int64_t K, const void *w
     a.spg = 1;
     a.err = device_error_word();
     a.part = part;
+    a.tok_scale = tok_scales(ws, M, K);
     const int64_t nsb = K / QK_K;
     CUtensorMap tmap_w, tmap_a;
     // packed records as [8-row tile][super-block][1680 B], in 8-byte units

@@ -472,9 +472,12 @@ cudaError_t launch_gemv_mma_q4_K(MatSet ms, int64_t K, const float *X, const voi
 // kernel (M <= 16) and the tensor-core GEMM (M > 16).
 cudaError_t launch_w4a16_repack(bool inverse, const void *src, void *dst, int64_t N, int64_t K,
                                 cudaStream_t s);
-// Q4_K and Q6_K prefill: activations as fp16(d_a y) [M][K] (Q8_K codes y, d_a
-// per 256; q4_0_prefill_bytes), from fp32 X or from canonical Q8_K blocks,
-// then the fp16-operand GEMM.
+// Prefill workspace (every weight type): the activations as fp16(2^e d_a y)
+// [M][K] (Q8 codes y, block scale d_a, a power of two 2^e per token), then
+// 2^-e per token, fp32, padded with 1.0 to a multiple of 16 tokens.
+size_t prefill_operand_bytes(int64_t M, int64_t K);
+// Q4_K and Q6_K prefill: the operand from Q8_K codes in natural order, from
+// fp32 X or from canonical Q8_K blocks, then the fp16-operand GEMM.
 cudaError_t launch_quantize_q8_K_f16(const float *X, void *ws, int64_t M, int64_t K, cudaStream_t s);
 cudaError_t launch_import_q8_K_f16(const void *Xq, void *ws, int64_t M, int64_t K, cudaStream_t s);
 cudaError_t launch_gemm_q6_K(const void *Wp, int64_t N, int64_t K, const void *ws, float *part, int64_t M,
@@ -490,9 +493,8 @@ cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, 
                               float *part, cudaStream_t s);
 cudaError_t launch_w4a16_unpack_zeros(const uint32_t *zp, uint8_t *z, int64_t N, int64_t ng,
                                       cudaStream_t s);
-// Q4_0 prefill (M > 16): fp16(d_a y) activations (permuted per block) in a
-// workspace of q4_0_prefill_bytes, then the fp16-operand tensor-core GEMM.
-size_t q4_0_prefill_bytes(int64_t M, int64_t K);
+// Q4_0 prefill (M > 8): the operand from Q8_0 codes, each 32-block permuted
+// for the converter, then the fp16-operand tensor-core GEMM.
 cudaError_t launch_quantize_q4_0_prefill(const float *X, void *ws, int64_t M, int64_t K,
                                          cudaStream_t s);
 cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *ws, float *part,

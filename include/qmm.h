@@ -187,11 +187,17 @@ qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon
  * small (16-token groups of at most 8192 elements) the activation quantizer
  * runs inside the GEMV kernel (one launch per 16 tokens, no workspace), at
  * any M. Otherwise, above those counts (prefill), the tensor-core GEMM
- * multiplies fp16 operands with fp32 accumulation: the
- * weights decoded to fp16 (Q4_0 d (q - 8), Q4_K q fp16(d s_j) - fp16(dmin m_j),
- * Q6_K fp16(d s_j) q, each rounded once more to fp16) and the activations
- * as fp16(d_a y) from the same Q8 codes; every product is then within
- * 2^-10 of the factored form's. Otherwise the quantized activations go to
+ * multiplies fp16 operands with fp32 accumulation: each weight is its exact
+ * value rounded once to fp16 (Q4_0 d (q - 8); Q4_K d s_j q - dmin m_j,
+ * formed in fp32 first; Q6_K d s_j q) and each activation is 2^e d_a y
+ * rounded once to fp16, y the same Q8 codes and 2^e a power of two per
+ * token that puts the token's largest block scale 2^e d_a in [2^7, 2^8)
+ * (taken off again, exactly, before Y is written: any magnitude of X works,
+ * including values past fp16's 65504). Each product is then within
+ * 2^-10 (1 + 2^-11) of the factored form's, plus, only for weights below
+ * fp16's normal range (|w| < 2^-14), 2^-25 |a| from the weight's subnormal
+ * rounding; the prefill weights must satisfy |w| <= 65504 (any weight that
+ * came from fp16 storage does). Otherwise the quantized activations go to
  * a workspace that the library allocates stream-ordered (cudaMallocAsync)
  * and frees after the call, in the same stream.
  * W_packed comes from qmm_repack_weights.
@@ -268,15 +274,24 @@ qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, in
  * no allocator to draw from, or a latency-critical step that must never block
  * in cudaMalloc/cudaFree. This call allocates nothing: the quantized
  * activations go to a fixed 4 MiB device array inside libqmm (reserved on
- * every GPU that loads the library, until the process exits), then the same
- * decode GEMV as qmm_mul_mat runs on them. The caller still owns and passes
- * X, W_packed and Y (same layouts, alignment and errors as qmm_mul_mat).
- *   - Limit: qmm_workspace_bytes(wt, M, K) must be <= 4 MiB (about M*K <= 3.6
- *     million elements); larger requests return QMM_ERR_WORKSPACE and launch
- *     nothing.
+ * every GPU that loads the library, until the process exits), then a decode
+ * GEMV runs on them: the kernels qmm_mul_mat runs up to 16 tokens (8 for Q4_0
+ * and Q6_K). Above that it does not switch to the prefill GEMM (whose
+ * operands and stream-K area would not fit): it runs the GEMV in launches of
+ * up to 16 tokens, each of which reads the weights again. The caller still
+ * owns and passes X, W_packed and Y (same layouts, alignment and errors as
+ * qmm_mul_mat).
+ *   - Limit: the activations of the whole call must fit the 4 MiB. Q4_K from
+ *     2 tokens on stores them as the tensor-core GEMV's images (about 2.1
+ *     bytes per element of X: M*K up to about 1.9 million); Q4_0, Q6_K and
+ *     one Q4_K token as Q8 codes with their scales and sums (about 1.14 to
+ *     1.19 bytes per element: M*K up to about 3.5 million). Calls small
+ *     enough for the decode kernel's fused quantizer use no scratch at all.
+ *     Larger requests return QMM_ERR_WORKSPACE and launch nothing.
  *   - The first call on a device looks up the array's device address (once,
  *     with that device current); make that first call before any stream
- *     capture.
+ *     capture. The address is kept for the life of the process: after
+ *     cudaDeviceReset on that device, do not call this again.
  *   - All calls share the one array and it keeps the last call's contents;
  *     nothing in it needs to start at zero. Calls whose GPU work overlaps
  *     (different streams, or graphs replayed concurrently) race on it: order

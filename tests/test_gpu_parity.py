@@ -61,11 +61,13 @@ def edge_rows(K, seed):
 
 
 def check_close(y, ref, den, what):
+    """Relative bar with no absolute slack: where sum_k |w_k a_k| is 0 the
+    output must be exactly 0."""
     err = np.abs(y.astype(np.float64) - ref)
-    bad = err > TOL * den + 1e-30
+    bad = err > TOL * den
     assert np.all(np.isfinite(y)), f"{what}: non-finite output"
-    assert not bad.any(), (f"{what}: {bad.sum()} outputs off; worst normalised error "
-                           f"{np.max(err / np.maximum(den, 1e-30)):.3e}")
+    worst = np.max(np.where(den > 0, err / np.where(den > 0, den, 1.0), 0.0))
+    assert not bad.any(), f"{what}: {bad.sum()} outputs off; worst normalised error {worst:.3e}"
 
 
 # ------------------------------------------------------------------ quantizers

@@ -158,6 +158,53 @@ def activations(seed: int, M: int, K: int, hot_frac: float = 0.0, hot_scale: flo
     return x
 
 
+S_EDGE = 20  # first stream id of the edge-case rows
+
+
+def edge_activation_rows(seed: int, K: int, device="cpu") -> torch.Tensor:
+    """fp32 activation rows [14, K] with the magnitudes and shapes that stress
+    a quantized product: zeros, constants, N(0, 1) scaled by 1e-30, 1e-6,
+    1e-3, 1e4 and 3e5 (above fp16's largest value), all positive (as after a
+    SiLU) and all negative, a lone spike, a normal row with one element x 1e4,
+    a row whose first 32 elements are x 1e3 and the rest x 1e-3 (six decades
+    inside one token), and a +-0 pattern."""
+    n = lambda i, std=1.0: normal_flat(seed, S_EDGE + i, K, 0, device, std)
+    rows = [torch.zeros(K, device=device), torch.full((K,), 0.37, device=device),
+            torch.full((K,), -2.5, device=device),
+            n(0, 1e-30), n(1, 1e-6), n(2, 1e-3), n(3, 1e4), n(4, 3e5),
+            n(5).abs(), -n(6).abs()]
+    spike = torch.zeros(K, device=device)
+    spike[K // 3] = -5.0
+    rows.append(spike)
+    hot = n(7).clone()
+    hot[(2 * K) // 5] *= 1e4
+    rows.append(hot)
+    wide = n(8) * 1e-3
+    wide[:32] = n(9)[:32] * 1e3
+    rows.append(wide)
+    rows.append(torch.where(torch.arange(K, device=device) % 3 == 0, -0.0, 0.0))
+    return torch.stack(rows).to(torch.float32)
+
+
+def edge_weight_rows(seed: int, K: int, device="cpu") -> torch.Tensor:
+    """fp32 weight rows [10, K]: zeros, a negative constant, N(0, 0.02) scaled
+    by 1e-30, N(0, 1e-3), N(0, 1e2), N(0, 0.02) - 0.5 (every element
+    negative: a large min term), two rows whose every 32-element sub-block is
+    symmetric about zero (elements 16..31 the negatives of 0..15: the min term
+    and the code term nearly cancel), a lone spike and |N(0, 0.02)| + 0.01."""
+    n = lambda i, std=0.02: normal_flat(seed, S_EDGE + 10 + i, K, 0, device, std)
+    sym = n(3).view(-1, 2, 16)
+    sym = torch.stack([sym[:, 0], -sym[:, 0]], dim=1).reshape(K)
+    sym2 = n(4, 0.05).view(-1, 2, 16)
+    sym2 = torch.stack([sym2[:, 0], -sym2[:, 0]], dim=1).reshape(K) + 0.001
+    spike = torch.zeros(K, device=device)
+    spike[K // 2 + 1] = 0.3
+    rows = [torch.zeros(K, device=device), torch.full((K,), -0.013, device=device),
+            n(0) * 1e-30, n(1, 1e-3), n(2, 1e2), n(5) - 0.5, sym, sym2, spike,
+            n(6).abs() + 0.01]
+    return torch.stack(rows).to(torch.float32)
+
+
 @dataclass(frozen=True)
 class Linear:
     """One projection of a workload: weight [N, K], activations [M, K]."""
