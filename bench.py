@@ -396,19 +396,54 @@ def prefill_rate(q, dev, stream, L, M, seed, reps=6, graph_steps=4, wt=None):
             "gemm_us": round(t2 * 1e6, 2), "gemm_TOPS": round(ops / t2 / 1e12, 1)}
 
 
-def prefill_extras(q, dev, stream):
+PEAK_KINDS = (("mma_sync_s8_m16n8k32", 0, 4000), ("mma_sync_f16_m16n8k16", 1, 4000),
+              ("tcgen05_f16_128x128x16_smem_smem", 2, 20000), ("tcgen05_f16_128x128x16_tmem_smem", 3, 20000),
+              ("tcgen05_f16_128x256x16_smem_smem", 4, 10000), ("tcgen05_f16_128x256x16_tmem_smem", 5, 10000))
+
+
+def peaks_rate(q, dev, stream, reps=3):
+    """Tensor throughput microbenchmarks (qmm_debug_peak): TFLOP/s (TOPS for
+    s8) of back-to-back MMAs over the whole GPU, best of `reps` launches after
+    one warm launch, each timed with CUDA events on `stream`."""
+    out = {}
+    for name, kind, iters in PEAK_KINDS:
+        with torch.cuda.stream(stream):
+            q.qmm_debug_peak(kind, iters, stream)
+        best = None
+        for _ in range(reps):
+            ops = [0.0]
+
+            def run():
+                ops[0] = q.qmm_debug_peak(kind, iters, stream)
+            t = timed(stream, run, lead_spin=True)
+            best = t if best is None or t < best else best
+        out[name] = {"TFLOP/s": round(ops[0] / best / 1e12, 1), "us": round(best * 1e6, 1)}
+    q.qmm_check_device_error(stream)
+    out["note"] = ("qmm_debug_peak: nonzero operands, all SMs, best of 3 launches; mma.sync: 32 warps "
+                   "per SM x 8 independent accumulators; tcgen05: one CTA per SM, one thread "
+                   "issuing K = 64 rounds into one TMEM accumulator")
+    return out
+
+
+def prefill_extras(q, dev, stream, peaks_measured=None):
     peaks = load_peaks()
+    pm = peaks_measured or peaks_rate(q, dev, stream)
+    s8 = pm["mma_sync_s8_m16n8k32"]["TFLOP/s"]
+    tcf = pm["tcgen05_f16_128x128x16_tmem_smem"]["TFLOP/s"]
     out = {}
     for wt, tag in ((q.QMM_TYPE_Q4_K, "q4_K"), (q.QMM_TYPE_Q4_0, "q4_0"), (q.QMM_TYPE_Q6_K, "q6_K")):
         for L in wl.PREFILL_SHAPES:
             for M in wl.PREFILL_M:
                 r = prefill_rate(q, dev, stream, L, M, 31, wt=wt)
                 r["frac_of_fp16_peak"] = round(r["gemm_TOPS"] / peaks["bf16_tflops"], 4)
+                r["frac_of_tcgen05_f16_measured"] = round(r["gemm_TOPS"] / tcf, 4)
+                r["frac_of_int8_mma_sync_measured"] = round(r["gemm_TOPS"] / s8, 4)
                 out[f"{tag}_{L.name}_M{M}"] = r
                 torch.cuda.empty_cache()
     out["peak"] = {"value": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                   "note": "measured bf16 dense GEMM peak; kind::f16 with fp16 operands has "
-                           "the same nominal rate"}
+                   "note": "measured bf16 dense GEMM peak (cuBLAS); kind::f16 with fp16 operands "
+                           "has the same nominal rate"}
+    out["peaks_measured"] = pm
     return out
 
 
@@ -466,7 +501,8 @@ def w4a16_extras(q, dev, stream, reps=8, graph_steps=16):
 
 
 def gpu_extras(q, dev, stream, args):
-    out = {"prefill": prefill_extras(q, dev, stream)}
+    out = {"peaks": peaks_rate(q, dev, stream)}
+    out["prefill"] = prefill_extras(q, dev, stream, out["peaks"])
     out["w4a16_8192"] = w4a16_extras(q, dev, stream)
     torch.cuda.empty_cache()
     out["q6_K"] = q6_K_rate(q, dev, stream)
@@ -671,7 +707,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--case", choices=["decode", "prefill", "w4a16", "layer", "sweep", "q6_K", "small_m"],
+    ap.add_argument("--case", choices=["decode", "prefill", "w4a16", "layer", "sweep", "q6_K", "small_m",
+                                       "peaks"],
                     default="decode",
                     help="prefill / w4a16 / layer / sweep / q6_K: only that measurement (for "
                          "profiler captures)")
@@ -711,7 +748,7 @@ def main():
     if args.case != "decode":
         import block_quantized_matmul_q4_gb300 as q
         fn = {"prefill": prefill_extras, "w4a16": w4a16_extras, "layer": layer_rate, "q6_K": q6_K_rate,
-              "small_m": small_m_rate,
+              "small_m": small_m_rate, "peaks": peaks_rate,
               "sweep": lambda q, d, s: sweep_rate(q, d, s, args.m)}[args.case]
         print(json.dumps(fn(q, torch.device("cuda", torch.cuda.current_device()),
                             torch.cuda.Stream())), flush=True)
@@ -726,6 +763,21 @@ def main():
                 "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
                 "extras": res["extras"]}
+        pf = res["extras"].get("prefill") if res["extras"] else None
+        if pf:
+            # the metric's TOPS half: the Q4_K prefill GEMM, 11008 x 4096, M = 512,
+            # against the measured kind::f16 rate of the MMA form it issues
+            # (A in TMEM, B in shared memory), and the int8 mma.sync rate
+            r = pf["q4_K_up_11008x4096_M512"]
+            tcf = pf["peaks_measured"]["tcgen05_f16_128x128x16_tmem_smem"]["TFLOP/s"]
+            s8 = pf["peaks_measured"]["mma_sync_s8_m16n8k32"]["TFLOP/s"]
+            line["roofline_prefill"] = {
+                "bound": "tensor", "achieved": r["gemm_TOPS"], "peak": tcf, "unit": "TFLOP/s",
+                "frac": round(r["gemm_TOPS"] / tcf, 4), "kernel": "gemm_f16_kernel<Q4_K>",
+                "config": "Q4_K 11008x4096, M=512", "kernel_us": r["gemm_us"],
+                "peak_source": "measured here (qmm_debug_peak, tcgen05 kind::f16 128x128x16, A in TMEM)",
+                "frac_of_int8_mma_sync": round(r["gemm_TOPS"] / s8, 4),
+                "frac_of_bf16_cublas": r["frac_of_fp16_peak"]}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -56,6 +56,7 @@ _SIGS = {
     "qmm_w4a16_lut": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _vp]),
     "qmm_w4a16_unpack_zeros": (_i32, [_vp, _vp, _i64, _i64, _vp]),
     "qmm_debug_wait_timeout": (_i32, [_i64, _vp]),
+    "qmm_debug_peak": (_i32, [_i32, _i64, ctypes.POINTER(ctypes.c_double), _vp]),
     "qmm_status_string": (ctypes.c_char_p, [_i32]),
     "qmm_last_error": (ctypes.c_char_p, []),
     "qmm_check_device_error": (_i32, [_vp]),
@@ -213,6 +214,18 @@ def qmm_w4a16_unpack_zeros(zeros_packed, zeros, N: int, ngroups: int, stream=Non
     ([N, ceil(ngroups/8)]); see include/qmm.h."""
     _check("qmm_w4a16_unpack_zeros",
            _lib.qmm_w4a16_unpack_zeros(_ptr(zeros_packed), _ptr(zeros), N, ngroups, _stream(stream)))
+
+
+QMM_PEAK_MMA_S8, QMM_PEAK_MMA_F16, QMM_PEAK_TC_SS_128, QMM_PEAK_TC_TS_128, QMM_PEAK_TC_SS_256, \
+    QMM_PEAK_TC_TS_256 = range(6)
+
+
+def qmm_debug_peak(which: int, iters: int, stream=None) -> float:
+    """Launch tensor-core microbenchmark `which` on the stream; returns the
+    operations (2 per multiply-add) the launch performs."""
+    ops = ctypes.c_double(0.0)
+    _check("qmm_debug_peak", _lib.qmm_debug_peak(which, iters, ctypes.byref(ops), _stream(stream)))
+    return ops.value
 
 
 def qmm_debug_wait_timeout(limit_cycles: int, stream=None):

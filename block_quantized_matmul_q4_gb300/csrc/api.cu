@@ -554,6 +554,13 @@ qmm_status qmm_debug_wait_timeout(int64_t limit_cycles, qmm_stream_t stream) {
                        "debug kernel launch");
 }
 
+qmm_status qmm_debug_peak(int which, int64_t iters, double *ops, qmm_stream_t stream) {
+    QMM_CHECK_ARG(which >= QMM_PEAK_MMA_S8 && which <= QMM_PEAK_TC_TS_256, "unknown peak kind %d", which);
+    QMM_CHECK_ARG(iters >= 1 && iters <= 1000000, "iters must be in [1, 1e6] (got %lld)", (long long)iters);
+    QMM_CHECK_ARG(ops != nullptr, "null pointer argument");
+    return cuda_status(launch_debug_peak(which, iters, (cudaStream_t)stream, ops), "peak kernel launch");
+}
+
 const char *qmm_status_string(qmm_status s) {
     switch (s) {
     case QMM_OK: return "QMM_OK";

@@ -502,6 +502,9 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
 cudaError_t launch_debug_block_sums(qmm_type wt, const void *Wp, int64_t N, int64_t K,
                                     const void *Xq, int64_t M, int32_t *out, cudaStream_t s);
 cudaError_t launch_debug_wait_timeout(int64_t limit_cycles, cudaStream_t s);
+// Tensor-core throughput microbenchmark `which` (qmm_peak_kind); *ops = the
+// multiply-add operations (2 per MAC) the launch performs.
+cudaError_t launch_debug_peak(int which, int64_t iters, cudaStream_t s, double *ops);
 // Stream-K GEMMs (streamk.cu): CTAs for `tiles` tiles of `units` units (the
 // SM count above it, one per tile from half of it, else split K over up to
 // the SM count); bytes of the partial area; the fixup that adds the split

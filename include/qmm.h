@@ -380,6 +380,33 @@ qmm_status qmm_debug_wait_timeout(int64_t limit_cycles, qmm_stream_t stream);
 
 /* ---------------------------------------------------------------- status */
 
+/* Tensor-core throughput microbenchmarks: the peaks the prefill GEMMs are
+ * measured against (page 3, "性能判断: 带宽、解码和 Tensor Core 谁是瓶颈":
+ * judge a kernel against the unit it runs on). One launch on `stream` that
+ * runs `iters` rounds of back-to-back MMAs on nonzero operands over the
+ * whole GPU; *ops (host pointer) receives the operations it performs
+ * (2 per multiply-add), for the caller to divide by the launch's event time.
+ *   QMM_PEAK_MMA_S8     mma.sync m16n8k32 s8 x s8 -> s32 (the int8 tensor path
+ *                       of sm_103a: tcgen05 has no kind::i8 there), 32 warps
+ *                       per SM, 8 independent accumulators per warp
+ *   QMM_PEAK_MMA_F16    mma.sync m16n8k16 f16 x f16 -> f32, the same way
+ *   QMM_PEAK_TC_SS_128  tcgen05.mma kind::f16 M = 128, N = 128, K = 16, both
+ *                       operands in shared memory, one CTA per SM
+ *   QMM_PEAK_TC_TS_128  the same with A in TMEM (the prefill GEMMs' form)
+ *   QMM_PEAK_TC_SS_256, QMM_PEAK_TC_TS_256   the same with N = 256
+ * iters: 1 .. 10^6 (a round is 8 MMAs per warp for mma.sync, 4 (K = 64) for
+ * tcgen05); keep a launch well under a second. Errors: QMM_ERR_ARG for a bad
+ * kind or count, QMM_ERR_CUDA if the launch failed. */
+typedef enum {
+    QMM_PEAK_MMA_S8 = 0,
+    QMM_PEAK_MMA_F16 = 1,
+    QMM_PEAK_TC_SS_128 = 2,
+    QMM_PEAK_TC_TS_128 = 3,
+    QMM_PEAK_TC_SS_256 = 4,
+    QMM_PEAK_TC_TS_256 = 5
+} qmm_peak_kind;
+qmm_status qmm_debug_peak(int which, int64_t iters, double *ops, qmm_stream_t stream);
+
 /* Static string naming a status code. */
 const char *qmm_status_string(qmm_status s);
 
