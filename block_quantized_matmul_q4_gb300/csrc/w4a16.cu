@@ -24,10 +24,16 @@
 // takes a contiguous range of 16-row tiles, and a producer warp streams
 // them through a 5-stage shared-memory ring (one 16 KB bulk copy of 16
 // steps per stage, so 80 KB in flight per CTA; 64-byte rows, so the
-// consumers' 16-byte reads hit distinct banks), together with each tile's
-// scales and zeros (two slots) and, when small, all activations. Eight
-// consumer warps split each stage's K, then reduce per tile; every load in
-// their loop is from shared memory.
+// consumers' 16-byte reads hit distinct banks) from the kernel's first
+// instruction (programmatic dependent launch: the weights never depend on
+// the preceding kernel), together with each tile's scales and zeros, row by
+// row into one of two shared-memory slots whose rows are padded by 16 bytes
+// (the 8 rows a warp reads at once fall in distinct banks). Small
+// activations are staged in shared memory by the consumers once the
+// preceding kernel is done, in rows of 64 elements padded to 144 bytes (the
+// four 64-byte slices the lanes of a step read fall in distinct banks).
+// Eight consumer warps split each stage's K, then reduce per tile; every
+// operand of a step is loaded one step ahead.
 #include "tc.cuh"
 
 namespace qmm {
@@ -41,7 +47,6 @@ constexpr int kStepsPerStage = 16;  // 2048 elements per stage
 constexpr int kDStages = 5;
 constexpr int kDStageBytes = kStepsPerStage * kRowsPerTile * 64;  // 16 KB: [step][row][64 B]
 constexpr size_t kActStageMax = 16 * 1024;  // activations staged in shared memory up to this
-constexpr int kSzSlots = 2;                // tiles whose scales and zeros are staged at once
 
 __device__ __forceinline__ uint32_t lop_or(uint32_t x, uint32_t mask) {
     uint32_t d;  // (x & mask) | 0x64006400
@@ -117,48 +122,42 @@ struct DecodeArgs {
     int64_t M, N, K, G;
     int ng, spg;  // groups per row, 128-element steps per group
     unsigned *err;
-    uint32_t act_bytes;  // > 0: all of A staged in shared memory (M * K * 2 bytes);
-                         // 0: A is read from global memory (L2) in place
+    uint32_t act_bytes;  // kStagedA: A in shared memory, padded (actpad_bytes)
 };
+
+// Activations staged in shared memory: rows of 64 elements (128 B) padded to
+// 144 B, so the four 64-byte slices the lanes j = 0..3 of a step read sit in
+// distinct banks.
+constexpr uint32_t kActRow = 64, kActRowBytes = 144;
+__host__ __device__ inline uint32_t actpad_bytes(int64_t M, int64_t K) {
+    return (uint32_t)((M * K / kActRow) * kActRowBytes);
+}
+// Scales and zeros of a tile in shared memory, row by row with 16 bytes of
+// padding per row, so the 8 rows a warp reads at once sit in distinct banks
+// (rows of ng fp16 scales, then rows of ng zero bytes; ng % 16 == 0).
+__host__ __device__ inline uint32_t sz_stride_s(int ng) { return (uint32_t)ng * 2u + 16u; }
+__host__ __device__ inline uint32_t sz_stride_z(int ng) { return (uint32_t)ng + 16u; }
+__host__ __device__ inline uint32_t sz_slot_bytes(int ng, bool lut) {
+    return kRowsPerTile * (sz_stride_s(ng) + (lut ? 0u : sz_stride_z(ng)));
+}
+constexpr int kSzSlots = 2;
 
 // What one thread needs for one step besides the weights: its 32 activation
 // elements of token t/4 (and t/4 + 8 for the second N tile), the scales of
 // rows r0, r1 and their zeros as the fp16 constants of dequant_word.
-template <int NT, bool kLut>
+template <int NT>
 struct Operands {
     uint4 x[NT][4];
     float s0, s1;
     Zero2 z0, z1;
 };
 
-// xq[nt]: this thread's 32 activation elements of the step (shared or global
-// memory, generic addressing).
-template <int NT, bool kLut>
-__device__ __forceinline__ void load_ops(const DecodeArgs &a, const __half *const (&xq)[NT],
-                                         const __half *s_r0, const __half *s_r1,
-                                         const uint8_t *z_r0, const uint8_t *z_r1, int st,
-                                         Operands<NT, kLut> &P) {
-    const int g = a.spg == 1 ? st : st / a.spg;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) P.x[nt][q] = *reinterpret_cast<const uint4 *>(xq[nt] + 8 * q);
-    P.s0 = __half2float(s_r0[g * kRowsPerTile]);
-    P.s1 = __half2float(s_r1[g * kRowsPerTile]);
-    if (!kLut) {
-        P.z0 = make_zero2(z_r0[g * kRowsPerTile]);
-        P.z1 = make_zero2(z_r1[g * kRowsPerTile]);
-    }
-}
-
 // One 128-element step of rows r0, r1 against tokens t/4 (+8): 8 (or 16)
-// MMAs on exact q - z, scaled by s once in fp32. Two accumulator chains
-// (even and odd words) halve the dependent MMA latency.
+// MMAs on exact q - z (or LUT(q)) into two accumulator chains (even and odd
+// words, halving the dependent MMA latency), then scaled by s once in fp32.
 template <int NT, bool kLut>
-__device__ __forceinline__ void step_mma(const Operands<NT, kLut> &P, const uint32_t *tbl,
-                                         const uint8_t *wrow, int tok, int j, float (&tot)[NT][4]) {
-    const uint4 wv0 = *reinterpret_cast<const uint4 *>(wrow + tok * 64 + 16 * j);
-    const uint4 wv1 = *reinterpret_cast<const uint4 *>(wrow + (tok + 8) * 64 + 16 * j);
+__device__ __forceinline__ void step_mma(const Operands<NT> &P, const uint32_t *tbl, uint4 wv0, uint4 wv1,
+                                         float (&tot)[NT][4]) {
     const uint32_t w0[4] = {wv0.x, wv0.y, wv0.z, wv0.w};
     const uint32_t w1[4] = {wv1.x, wv1.y, wv1.z, wv1.w};
     float acc[2][NT][4];
@@ -199,9 +198,16 @@ __device__ __forceinline__ void step_mma(const Operands<NT, kLut> &P, const uint
     }
 }
 
-template <int NT, bool kLut>
-__global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
-    w4a16_decode_kernel(const DecodeArgs a) {
+// The decode kernel. kStagedA: all of A sits in shared memory (copied in by
+// the consumers into the padded layout), else it is read in place from
+// global memory (L2). kSzSmem: the producer copies each tile's scales and
+// zeros into one of two shared-memory slots (padded rows), else the
+// consumers read them from global memory. The producer streams the CTA's
+// tiles stage by stage from its first instruction on (the weights do not
+// depend on the preceding kernel, which may still be running: programmatic
+// dependent launch). Every operand of a step is loaded one step ahead.
+template <int NT, bool kLut, bool kStagedA, bool kSzSmem>
+__global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1) w4a16_decode_kernel(const DecodeArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ float red[kDecodeWarps][NT][4][32];
     __shared__ uint32_t pair_tbl[kLut ? 256 : 1];  // (LUT[i & 15], LUT[i >> 4]) as fp16 pairs
@@ -209,28 +215,20 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
     const int64_t ntiles = (a.N + kRowsPerTile - 1) / kRowsPerTile;
     const int64_t tb = (int64_t)blockIdx.x * ntiles / gridDim.x;
     const int64_t te = ((int64_t)blockIdx.x + 1) * ntiles / gridDim.x;
-    const int64_t nsteps = a.K / kStepK;
+    const int nsteps = (int)(a.K / kStepK);
     constexpr int sps = kStepsPerStage, S = kDStages;
-    const int64_t spt = (nsteps + sps - 1) / sps;  // stages per tile
-    // a tile's scales (16 rows x ng fp16) and zeros (16 x ng bytes), contiguous
-    // in global memory and in its shared-memory slot
-    const uint32_t s_bytes = (uint32_t)kRowsPerTile * (uint32_t)a.ng * 2u;
-    const uint32_t z_bytes = kLut ? 0u : (uint32_t)kRowsPerTile * (uint32_t)a.ng;
-    const uint32_t sz_slot = s_bytes + z_bytes;  // multiple of 32
+    const int spt = (nsteps + sps - 1) / sps;  // stages per tile
     constexpr uint32_t ring_bytes = (uint32_t)S * kDStageBytes;
+    const uint32_t ss = sz_stride_s(a.ng), zs = sz_stride_z(a.ng), slot_bytes = sz_slot_bytes(a.ng, kLut);
 
-    // shared memory: weight ring | activations | scale/zero slots | barriers
-    __half *x_sm = reinterpret_cast<__half *>(smem + ring_bytes);
-    uint8_t *sz_sm = smem + ring_bytes + a.act_bytes;
-    // the current tile's scales and zeros transposed to [group][16 rows], so
-    // that the 8 rows a warp reads at once sit in neighbouring banks
-    __half *s_tr = reinterpret_cast<__half *>(sz_sm + kSzSlots * sz_slot);
-    uint8_t *z_tr = reinterpret_cast<uint8_t *>(s_tr) + s_bytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(z_tr + z_bytes);
+    // shared memory: weight ring | activations (kStagedA) | scale/zero slots (kSzSmem) | barriers
+    const uint32_t act_sm = smem_u32(smem) + ring_bytes;
+    const uint32_t sz_sm = act_sm + (kStagedA ? a.act_bytes : 0u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + ring_bytes + (kStagedA ? a.act_bytes : 0u) +
+                                                  (kSzSmem ? kSzSlots * slot_bytes : 0u));
     uint64_t *empty = full + kDStages;
     uint64_t *szfull = empty + kDStages;
     uint64_t *szempty = szfull + kSzSlots;
-    uint64_t *actb = szempty + kSzSlots;
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
@@ -240,8 +238,8 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
             mbar_init(smem_u32(&szfull[i]), 1);
             mbar_init(smem_u32(&szempty[i]), kDecodeWarps);
         }
-        mbar_init(smem_u32(actb), 1);
         fence_barrier_init();
+        pdl_launch_dependents();  // the next kernel may start streaming its weights
     }
     if (kLut) {
         // the table is weight data, like the scales: ready before the launch
@@ -253,48 +251,38 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
 
     if (warp == kDecodeWarps) {
         // ------------------------------------------------------------ producer
-        // Per tile: its scales and zeros, then its weight stages; the ring
-        // holds five stages, so every CTA keeps 80 KB of weights in flight.
+        // Per tile: its scales and zeros (kSzSmem), then its weight stages;
+        // the ring holds five 16 KB stages, so every CTA keeps 80 KB of
+        // weights in flight.
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();  // every weight is read once
-            if (a.act_bytes) {
-                pdl_wait();  // the activations may come from the preceding kernel
-                mbar_arrive_expect_tx(smem_u32(actb), a.act_bytes);
-                bulk_g2s(smem_u32(x_sm), a.A, a.act_bytes, smem_u32(actb), policy_evict_last());
-            }
             int64_t it = 0;
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
             for (int64_t tile = tb; tile < te && ok; ++tile) {
-                const int64_t ti = tile - tb;
-                const int zs = (int)(ti % kSzSlots);
-                ok = mbar_wait(smem_u32(&szempty[zs]), (uint32_t)(((ti / kSzSlots) & 1) ^ 1), a.err);
-                if (!ok) break;
-                {
-                    // the tile's rows of scales and zeros: the 16-byte multiple by
-                    // bulk copy, a short tail (a partial last tile) by this thread
-                    // before its arrival publishes the slot
-                    const int64_t rows = a.N - tile * kRowsPerTile < kRowsPerTile
-                                             ? a.N - tile * kRowsPerTile : kRowsPerTile;
-                    const uint32_t sb = (uint32_t)rows * (uint32_t)a.ng * 2u;
-                    const uint32_t zb = kLut ? 0u : (uint32_t)rows * (uint32_t)a.ng;
-                    const uint32_t sb16 = sb & ~15u, zb16 = zb & ~15u;
-                    const uint8_t *ssrc = reinterpret_cast<const uint8_t *>(a.S + tile * kRowsPerTile * a.ng);
-                    const uint8_t *zsrc = kLut ? nullptr : a.Z + tile * kRowsPerTile * a.ng;
-                    uint8_t *dst = sz_sm + zs * sz_slot;
-                    for (uint32_t b = sb16; b < sb; ++b) dst[b] = ssrc[b];
-                    for (uint32_t b = zb16; b < zb; ++b) dst[s_bytes + b] = zsrc[b];
-                    const uint32_t bar = smem_u32(&szfull[zs]);
-                    mbar_arrive_expect_tx(bar, sb16 + zb16);
-                    if (sb16) bulk_g2s(smem_u32(dst), ssrc, sb16, bar, pol);
-                    if (zb16) bulk_g2s(smem_u32(dst + s_bytes), zsrc, zb16, bar, pol);
+                if (kSzSmem) {
+                    const int64_t ti = tile - tb;
+                    const int zsl = (int)(ti % kSzSlots);
+                    ok = mbar_wait(smem_u32(&szempty[zsl]), (uint32_t)(((ti / kSzSlots) & 1) ^ 1), a.err);
+                    if (!ok) break;
+                    const int rows = (int)(a.N - tile * kRowsPerTile < kRowsPerTile ? a.N - tile * kRowsPerTile
+                                                                                   : kRowsPerTile);
+                    const uint32_t sb = (uint32_t)a.ng * 2u, zb = (uint32_t)a.ng;
+                    const uint32_t bar = smem_u32(&szfull[zsl]);
+                    const uint32_t dst = sz_sm + (uint32_t)zsl * slot_bytes;
+                    mbar_arrive_expect_tx(bar, (uint32_t)rows * (sb + (kLut ? 0u : zb)));
+                    for (int r = 0; r < rows; ++r) {
+                        const int64_t n = tile * kRowsPerTile + r;
+                        bulk_g2s(dst + r * ss, a.S + n * a.ng, sb, bar, pol);
+                        if (!kLut) bulk_g2s(dst + kRowsPerTile * ss + r * zs, a.Z + n * a.ng, zb, bar, pol);
+                    }
                 }
-                for (int64_t sg = 0; sg < spt; ++sg, ++it) {
+                for (int sg = 0; sg < spt; ++sg, ++it) {
                     ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u, a.err);
                     if (!ok) break;
-                    const int64_t step0 = sg * sps;
-                    const int64_t nst = nsteps - step0 < sps ? nsteps - step0 : sps;
+                    const int step0 = sg * sps;
+                    const int nst = nsteps - step0 < sps ? nsteps - step0 : sps;
                     const uint32_t bar = smem_u32(&full[s]);
                     // steps past K are not copied (and never read)
                     mbar_arrive_expect_tx(bar, (uint32_t)nst * 1024u);
@@ -306,10 +294,11 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
             // drain: nothing may still be landing when the CTA exits
             for (int64_t k = it > S ? it - S : 0; k < it; ++k)
                 mbar_wait(smem_u32(&full[k % S]), (uint32_t)((k / S) & 1), a.err);
-            const int64_t nt_issued = te - tb;
-            for (int64_t k = nt_issued > kSzSlots ? nt_issued - kSzSlots : 0; k < nt_issued; ++k)
-                mbar_wait(smem_u32(&szfull[k % kSzSlots]), (uint32_t)((k / kSzSlots) & 1), a.err);
-            if (a.act_bytes) mbar_wait(smem_u32(actb), 0, a.err);
+            if (kSzSmem) {
+                const int64_t nt_issued = te - tb;
+                for (int64_t k = nt_issued > kSzSlots ? nt_issued - kSzSlots : 0; k < nt_issued; ++k)
+                    mbar_wait(smem_u32(&szfull[k % kSzSlots]), (uint32_t)((k / kSzSlots) & 1), a.err);
+            }
         }
         return;
     }
@@ -320,44 +309,48 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
     // warp can be left waiting for another.
     const int j = lane & 3, tok = lane >> 2;
     bool ok = true;
-    const __half *xs = a.A;
-    if (a.act_bytes) {
-        ok = mbar_wait(smem_u32(actb), 0, a.err);
-        xs = x_sm;
-    } else {
-        pdl_wait();  // the activations may come from the preceding kernel
+    pdl_wait();  // the activations may come from the preceding kernel
+    if (kStagedA) {
+        // A into the padded layout: 16 bytes per thread per pass
+        const uint32_t nchunks = (uint32_t)(a.M * a.K / 8);
+        for (uint32_t c = threadIdx.x; c < nchunks; c += kDecodeWarps * 32) {
+            const uint4 v = ldg_nc128(a.A + 8 * (size_t)c);
+            const uint32_t e = 8u * c;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(act_sm + (e / kActRow) * kActRowBytes +
+                                                                          (e % kActRow) * 2u),
+                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+        }
+        consumers_sync();
     }
     // tokens past M read a valid token's activations (they only feed outputs
     // that are never stored)
-    int mt[NT];
+    uint32_t xrow[NT];  // kStagedA: padded row of element tok_row * K + 32 j; else its element offset
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mt[nt] = nt * 8 + tok < a.M ? nt * 8 + tok : (int)a.M - 1;
+    for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t e0 = (uint32_t)((nt * 8 + tok < a.M ? nt * 8 + tok : a.M - 1) * a.K) + 32u * j;
+        xrow[nt] = kStagedA ? act_sm + (e0 / kActRow) * kActRowBytes + (e0 % kActRow) * 2u : e0;
+    }
     int64_t it = 0;
     int s = 0;
     uint32_t ph = 0;
     constexpr int kps = sps / kDecodeWarps;  // this warp's steps per stage
+    const int nk = warp < nsteps ? (nsteps - 1 - warp) / kDecodeWarps + 1 : 0;
     for (int64_t tile = tb; tile < te; ++tile) {
         const int64_t ti = tile - tb;
-        const int zs = (int)(ti % kSzSlots);
-        if (ok) ok = mbar_wait(smem_u32(&szfull[zs]), (uint32_t)((ti / kSzSlots) & 1), a.err);
+        const int zsl = (int)(ti % kSzSlots);
+        if (kSzSmem && ok) ok = mbar_wait(smem_u32(&szfull[zsl]), (uint32_t)((ti / kSzSlots) & 1), a.err);
         const int64_t r0 = tile * kRowsPerTile + tok, r1 = r0 + 8;
-        // Rows past N (zero weights) and tokens past M read valid addresses
-        // (clamped tokens, stale scale slots); they only feed outputs that are
-        // never stored, so no load needs a predicate.
-        {
-            const __half *s_all = reinterpret_cast<const __half *>(sz_sm + zs * sz_slot);
-            const uint8_t *z_all = sz_sm + zs * sz_slot + s_bytes;
-            for (int i = threadIdx.x; i < kRowsPerTile * a.ng; i += kDecodeWarps * 32) {
-                const int r = i / a.ng, g = i - r * a.ng;
-                s_tr[g * kRowsPerTile + r] = s_all[i];
-                if (!kLut) z_tr[g * kRowsPerTile + r] = z_all[i];
-            }
-            consumers_sync();
-            if (lane == 0) mbar_arrive(smem_u32(&szempty[zs]));  // slot free again
-        }
-        // scales / zeros of rows r0, r1 for group g at index g * 16 (stride 16)
-        const __half *s_r0 = s_tr + tok, *s_r1 = s_tr + tok + 8;
-        const uint8_t *z_r0 = z_tr + tok, *z_r1 = z_tr + tok + 8;
+        // Rows past N (zero weights) read row N - 1's scales and zeros (or a
+        // stale slot row); they only feed outputs that are never stored, so
+        // no load needs a predicate.
+        const int64_t rc0 = r0 < a.N ? r0 : a.N - 1, rc1 = r1 < a.N ? r1 : a.N - 1;
+        const __half *s_r0 = a.S + rc0 * a.ng, *s_r1 = a.S + rc1 * a.ng;
+        const uint8_t *z_r0 = kLut ? nullptr : a.Z + rc0 * a.ng;
+        const uint8_t *z_r1 = kLut ? nullptr : a.Z + rc1 * a.ng;
+        const uint32_t slot = sz_sm + (uint32_t)zsl * slot_bytes;
+        const uint32_t ss0 = slot + tok * ss, ss1 = ss0 + 8 * ss;
+        const uint32_t zs0 = slot + kRowsPerTile * ss + tok * zs, zs1 = zs0 + 8 * zs;
         float tot[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -366,32 +359,64 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1)
         // This warp's steps are warp + 8k, k = 0 .. nk-1, two per stage. While
         // it computes step k it has the operands of step k + 1 in flight (two
         // register sets, alternating).
-        const int nk = warp < nsteps ? (int)((nsteps - 1 - warp) / kDecodeWarps) + 1 : 0;
-        Operands<NT, kLut> P[2];
-        auto ops = [&](int k, Operands<NT, kLut> &Q) {
-            const int64_t st = warp + (int64_t)k * kDecodeWarps;
-            const __half *xq[NT];
+        Operands<NT> P[2];
+        auto ops = [&](int k, Operands<NT> &Q) {
+            const int st = warp + k * kDecodeWarps;
+            const int g = a.spg == 1 ? st : st / a.spg;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) xq[nt] = xs + (int64_t)mt[nt] * a.K + st * kStepK + 32 * j;
-            load_ops<NT, kLut>(a, xq, s_r0, s_r1, z_r0, z_r1, (int)st, Q);
+            for (int nt = 0; nt < NT; ++nt) {
+                if (kStagedA) {
+                    const uint32_t ad = xrow[nt] + (uint32_t)st * (2u * kActRowBytes);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) Q.x[nt][q] = lds128(ad + 16u * q);
+                } else {
+                    const uint32_t e = xrow[nt] + (uint32_t)st * kStepK;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) Q.x[nt][q] = ldg_nc128(a.A + e + 8 * q);
+                }
+            }
+            if (kSzSmem) {
+                uint32_t h0, h1;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h0) : "r"(ss0 + 2u * g));
+                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h1) : "r"(ss1 + 2u * g));
+                Q.s0 = __half2float(__ushort_as_half((unsigned short)h0));
+                Q.s1 = __half2float(__ushort_as_half((unsigned short)h1));
+                if (!kLut) {
+                    uint32_t z0, z1;
+                    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(z0) : "r"(zs0 + g));
+                    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(z1) : "r"(zs1 + g));
+                    Q.z0 = make_zero2(z0);
+                    Q.z1 = make_zero2(z1);
+                }
+            } else {
+                Q.s0 = __half2float(__ldg(s_r0 + g));
+                Q.s1 = __half2float(__ldg(s_r1 + g));
+                if (!kLut) {
+                    Q.z0 = make_zero2(__ldg(z_r0 + g));
+                    Q.z1 = make_zero2(__ldg(z_r1 + g));
+                }
+            }
         };
         if (nk > 0) ops(0, P[0]);
-        for (int64_t sg = 0; sg < spt; ++sg, ++it) {
+        for (int sg = 0; sg < spt; ++sg, ++it) {
             if (ok) ok = mbar_wait(smem_u32(&full[s]), ph, a.err);
-            const uint8_t *stage = smem + (size_t)s * kDStageBytes;
+            const uint32_t stage = smem_u32(smem) + (uint32_t)s * kDStageBytes + tok * 64u + 16u * j;
 #pragma unroll
             for (int h = 0; h < kps; ++h) {
-                const int k = (int)sg * kps + h;
+                const int k = sg * kps + h;
                 if (k < nk) {
                     if (k + 1 < nk) ops(k + 1, P[(h + 1) & 1]);
-                    step_mma<NT, kLut>(P[h & 1], pair_tbl, stage + (warp + h * kDecodeWarps) * 1024, tok, j,
-                                       tot);
+                    const uint32_t w = stage + (uint32_t)(warp + h * kDecodeWarps) * 1024u;
+                    step_mma<NT, kLut>(P[h & 1], pair_tbl, lds128(w), lds128(w + 512u), tot);
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
             if (++s == S) s = 0, ph ^= 1u;
         }
+        // this tile's scale/zero slot is free again
+        __syncwarp();
+        if (kSzSmem && lane == 0) mbar_arrive(smem_u32(&szempty[zsl]));
         // reduce the consumer warps' partial sums of this tile
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -474,12 +499,32 @@ cudaError_t launch_w4a16_repack(bool inverse, const void *src, void *dst, int64_
     return cudaGetLastError();
 }
 
-template <int NT, bool kLut>
+template <int NT, bool kLut, bool kStagedA, bool kSzSmem>
 cudaError_t launch_decode_nt(const DecodeArgs &a, int64_t grid, size_t smem, cudaStream_t s) {
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(w4a16_decode_kernel<NT, kLut>), (int)smem);
+    auto fn = w4a16_decode_kernel<NT, kLut, kStagedA, kSzSmem>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn), (int)smem);
     if (e != cudaSuccess) return e;
-    w4a16_decode_kernel<NT, kLut><<<(unsigned)grid, kDecodeThreads, smem, s>>>(a);
-    return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, a);
+}
+
+template <int NT, bool kLut>
+cudaError_t launch_decode_m(const DecodeArgs &a, bool staged, bool szsmem, int64_t grid, size_t smem,
+                            cudaStream_t s) {
+    if (staged)
+        return szsmem ? launch_decode_nt<NT, kLut, true, true>(a, grid, smem, s)
+                      : launch_decode_nt<NT, kLut, true, false>(a, grid, smem, s);
+    return szsmem ? launch_decode_nt<NT, kLut, false, true>(a, grid, smem, s)
+                  : launch_decode_nt<NT, kLut, false, false>(a, grid, smem, s);
 }
 
 cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z, const __half *lut,
@@ -500,21 +545,25 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
     a.spg = (int)(G / kStepK);
     a.err = device_error_word();
     const int64_t ntiles = (N + kRowsPerTile - 1) / kRowsPerTile;
-    // all of A in shared memory when it is small (one bulk copy per CTA)
-    const size_t act = (size_t)M * K * 2;
-    a.act_bytes = act <= kActStageMax ? (uint32_t)act : 0u;
-    const size_t sz = (size_t)(kSzSlots + 1) * kRowsPerTile * a.ng * 3;
-    const size_t bars = (2 * kDStages + 2 * kSzSlots + 1) * 8;
+    // all of A in shared memory when it is small (padded rows)
+    const bool staged = (size_t)M * K * 2 <= kActStageMax;
+    a.act_bytes = staged ? actpad_bytes(M, K) : 0u;
+    // the tile's scales and zeros in shared memory when every row is a
+    // multiple of 16 bytes and both slots fit beside the ring
+    const bool szsmem = a.ng % 16 == 0 && sz_slot_bytes(a.ng, lut != nullptr) <= 16384;
+    const size_t sz = szsmem ? (size_t)kSzSlots * sz_slot_bytes(a.ng, lut != nullptr) : 0;
+    const size_t bars = (2 * kDStages + 2 * kSzSlots) * 8;
     const int64_t grid = balanced_grid(ntiles, (M <= 8 ? 2 : 1) * (int64_t)sm_count());
     const size_t smem = (size_t)kDStages * kDStageBytes + a.act_bytes + sz + bars;
     cudaError_t e;
     if (M <= 8)
-        e = lut ? launch_decode_nt<1, true>(a, grid, smem, s) : launch_decode_nt<1, false>(a, grid, smem, s);
+        e = lut ? launch_decode_m<1, true>(a, staged, szsmem, grid, smem, s)
+                : launch_decode_m<1, false>(a, staged, szsmem, grid, smem, s);
     else
-        e = lut ? launch_decode_nt<2, true>(a, grid, smem, s) : launch_decode_nt<2, false>(a, grid, smem, s);
-    if (e != cudaSuccess) return e;
+        e = lut ? launch_decode_m<2, true>(a, staged, szsmem, grid, smem, s)
+                : launch_decode_m<2, false>(a, staged, szsmem, grid, smem, s);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 // Zero points packed 8 per word like the codes ([N][ceil(ng/8)] words,

@@ -30,6 +30,13 @@
  *   - The caller owns every buffer; the library never frees caller memory.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
  *     no call synchronizes the host except qmm_check_device_error.
+ *   - The mul_mat and W4A16 kernels launch with programmatic dependent launch:
+ *     they may start while the preceding kernel on the stream is finishing
+ *     and stream their weights (packed weights, W4A16 scales, zeros and code
+ *     table) at once; they read the activations and write the outputs only
+ *     after that kernel has completed. Weights are load-time data: the kernel
+ *     immediately preceding a call must not write them (a repack or weight
+ *     quantizer of this library never lets the next kernel start early).
  *   - Device buffers must be 16-byte aligned, except canonical Q4_0/Q8_0/Q6_K
  *     buffers (18/34/210-byte blocks), which need 2-byte alignment.
  *   - Errors: arguments are validated before anything is enqueued; on any
