@@ -397,7 +397,7 @@ qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, in
     QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(workspace, 16) && aligned(Y, 4),
                   "W_packed and workspace must be 16-byte aligned, Y 4-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
-    if (!use_gemm(wt, M) || !stream_k_splits(N, M, K))  // nothing to allocate
+    if (!use_gemm(wt, M) || !stream_k_splits(wt, N, M, K))  // nothing to allocate
         return prepared_impl(wt, W_packed, N, K, workspace, ws_bytes, M, Y, nullptr, s);
     if (ws_bytes < prefill_act_bytes(wt, M, K))  // before allocating anything
         return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes,
@@ -629,7 +629,7 @@ static qmm_status w4a16_impl(const char *fn, const void *W_packed, const uint16_
     if (M <= 16)
         return cuda_status(launch_w4a16_decode(W_packed, S, zeros, L, G, Ah, Ch, M, N, K, s),
                            "W4A16 kernel launch");
-    if (!stream_k_splits(N, M, K))  // one CTA per tile: no partial area
+    if (!stream_k_splits(QMM_TYPE_W4A16, N, M, K))  // one CTA per tile: no partial area
         return cuda_status(launch_w4a16_gemm(W_packed, S, zeros, L, G, Ah, Ch, M, N, K, nullptr, s),
                            "W4A16 kernel launch");
     return with_own_part(s, [&](float *part) {

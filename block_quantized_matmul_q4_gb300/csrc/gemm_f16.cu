@@ -26,15 +26,17 @@
 // octaves, whatever the magnitude of X -- and that the epilogue takes off
 // again (exact: a power of two). The MMA accumulates in fp32 over all of K.
 //
-// Tile = 128 weight rows (MMA M) x 128 tokens (MMA N). Up to one tile per SM
-// the grid has one CTA per tile; with more, one CTA per SM walks a
-// contiguous range of (tile, 256-element K round) units (stream-K): pieces
+// Tile = 128 weight rows (MMA M) x BN tokens (MMA N): BN = 256 above 128
+// tokens (every decoded weight then serves 256 tokens), else 128. Up to one
+// tile per SM the grid has one CTA per tile; with more, one CTA per SM walks
+// a contiguous range of (tile, 256-element K round) units (stream-K): pieces
 // of tiles that span two or more CTAs go to partial slots and a fixup
-// kernel adds them (streamk.cu). Two TMEM accumulators let the MMAs of the
-// next piece start while the epilogue drains the last one. 15 warps:
-//   warp 0      producer: per 256 elements of K one weight stage (TMA copies
-//               of the packed tiles of the CTA's 128 rows) and one activation
-//               stage of four 2-D TMA tiles (128B swizzle, 64 KB);
+// kernel adds them (streamk.cu). With BN = 128 two TMEM accumulators let the
+// MMAs of the next piece start while the epilogue drains the last one.
+// 16 warps:
+//   warp 0      activation producer: 16 KB stages, 2-D TMA tiles of BN
+//               tokens by 64 (BN = 128, 128B swizzle) or 32 (BN = 256, 64B
+//               swizzle) elements of K;
 //   warp 1      MMA issuer (one thread) and TMEM owner;
 //   warp 2      MMA waiter: the issuer's barrier waits, handed over per pair
 //               of K chunks through a named barrier (a shared-memory access
@@ -43,9 +45,14 @@
 //               (its TMEM lane), fp16 weights built in registers and stored
 //               into a TMEM operand ring with tcgen05.st;
 //   warps 11..14 epilogue: one tcgen05.ld pass over the accumulator per
-//               piece.
+//               piece;
+//   warp 15     weight producer: per 256 elements of K one weight stage (TMA
+//               copies of the packed tiles of the CTA's 128 rows), as soon as
+//               the converters free one.
 // All mbarrier waits are bounded; on a timeout the CTA drains its copies and
 // MMAs, frees its TMEM and returns with the device error word set.
+#include <cstring>
+
 #include "tc.cuh"
 
 namespace qmm {
@@ -53,24 +60,52 @@ namespace {
 
 enum Format { kW4A16 = 0, kQ40 = 1, kQ6K = 2, kQ4K = 3 };
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;  // rows, tokens, K per chunk
-constexpr int kSB = 256;                       // K per pipeline round
-constexpr int kChunks = kSB / kBK;             // 4
-static_assert(kSB == kSkRound && kBM == kSkTile && kBN == kSkTile, "stream-K units");
-constexpr int kGroups = 2;                     // A handed over in pairs of chunks
-constexpr int kWStages = 3, kActStages = 2;
-constexpr int kWBytesMax = 16 * kQ6Rec;         // largest weight stage: Q6_K, 16 records of 8 rows
-constexpr int kChunkBytes = kBN * kBK * 2;     // 16 KB
-constexpr int kActBytes = kChunks * kChunkBytes;  // 64 KB
+constexpr int kBM = 128, kBK = 64;  // rows, K per chunk; the tile's token count BN is 128 or 256
+constexpr int kSB = 256;            // K per pipeline round
+constexpr int kChunks = kSB / kBK;  // 4
+static_assert(kSB == kSkRound && kBM == kSkTile, "stream-K units");
+constexpr int kGroups = 2;          // A handed over in pairs of chunks
+constexpr int kARounds = 2;         // the A operand ring holds two rounds: converters run a round ahead
+constexpr int kWStagesMax = 4;          // weight stages: 4 where shared memory allows, else 3
+constexpr int kWBytesMax = 16 * kQ6Rec;  // largest weight stage: Q6_K, 16 records of 8 rows
 constexpr int kConvWarps = 8, kEpiWarps = 4;
-constexpr int kThreads = (3 + kConvWarps + kEpiWarps) * 32;
+constexpr int kEpiWarp0 = 3 + kConvWarps, kWProdWarp = kEpiWarp0 + kEpiWarps;
+constexpr int kThreads = (kWProdWarp + 1) * 32;
+constexpr int kActRing = 128 * 1024;  // activation stages: 8 x 16 KB
 constexpr int kOffAct = 0;
-constexpr int kOffW = kOffAct + kActStages * kActBytes;
-constexpr int kNumBars = 2 * (kWStages + kActStages + kGroups) + 5;  // + acc_full[2], acc_empty[2], done
+constexpr int kOffW = kOffAct + kActRing;
+constexpr int kActStagesMax = 8;
+constexpr int kNumBars = 2 * (kWStagesMax + kActStagesMax + kARounds * kGroups) + 5;  // + acc_full[2], acc_empty[2], done
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColAcc = 0, kColARing = 2 * kBN;  // two accumulators (stream-K pieces), A ring
+// Epilogue output staging: 16 tokens x 128 rows (the C tile's 2-D TMA box),
+// fp32 or fp16, double-buffered.
+constexpr int kStageCols = 16;
+constexpr int kStageBytes = kStageCols * kBM * 4;
 constexpr uint32_t kARingCols = kBK / 2;
-static_assert(kColARing + kChunks * kARingCols <= kTmemCols, "TMEM budget");
+
+// Tile width BN (tokens): 128 with two TMEM accumulators, so the next
+// piece's MMAs run while the epilogue drains the last one; or 256 with one
+// (256 columns), so that every weight the converters decode serves twice as
+// many tokens. Either way the accumulators take 256 columns and the A
+// operand ring (two rounds of four 32-column chunks) the other 256. An
+// activation stage is 16 KB either way: BN tokens x kActK elements of K (64
+// with the 128-byte swizzle, or 32 with the 64-byte one), so that the ring
+// always has eight stages and a stage is freed as soon as its own MMAs are
+// done.
+template <int BN>
+struct Tile {
+    static_assert(BN == 128 || BN == 256, "tile width");
+    static constexpr int kAccs = BN == 128 ? 2 : 1;
+    static constexpr int kActK = BN == 128 ? 64 : 32;
+    static constexpr int kSlices = kBK / kActK;            // activation stages per 64-element chunk
+    static constexpr int kActBytes = BN * kActK * 2;       // one activation stage
+    static constexpr int kActStages = kActRing / kActBytes;
+    static constexpr uint32_t kSwz = kActK == 64 ? 2 : 4;  // descriptor layout: 128- or 64-byte swizzle
+    static constexpr uint32_t kSbo = 8 * kActK * 2;        // bytes per 8 rows
+    static constexpr uint32_t kColARing = kAccs * BN;
+    static_assert(kColARing + kARounds * kChunks * kARingCols <= kTmemCols, "TMEM budget");
+    static_assert(kActStages <= kActStagesMax, "barriers");
+};
 
 // W4A16 packed tiles: 16 rows, steps of 128 elements (1 KB each).
 constexpr int kW4StepK = 128, kW4Tile = 16;
@@ -88,10 +123,15 @@ struct FmtInfo {
     static_assert(kWBytes <= kWBytesMax, "weight stage");
     // Shared memory: activation stages | weight stages (this format's size:
     // the unused rest of the SM's 228 KB stays L1, where the W4A16
-    // converters' scale and zero reads hit) | code table | barriers.
+    // converters' scale and zero reads hit) | W4A16 code table (256 fp16
+    // pairs) or, for the other formats, the epilogue's token scales (up to
+    // 256 floats) | the epilogue's two output staging blocks | barriers.
     static constexpr int kWStage = (kWBytes + 127) / 128 * 128;
-    static constexpr int kOffLut = kOffW + kWStages * kWStage;  // W4A16 code table: 256 fp16 pairs
-    static constexpr int kOffBar = kOffLut + 1024;
+    static constexpr int kFixed = kOffW + 1024 + 2 * kStageBytes + kNumBars * 8 + 16 + 1024;
+    static constexpr int kWStages = kFixed + kWStagesMax * kWStage <= 227 * 1024 ? kWStagesMax : 3;
+    static constexpr int kOffLut = kOffW + kWStages * kWStage;
+    static constexpr int kOffStage = kOffLut + 1024;
+    static constexpr int kOffBar = kOffStage + 2 * kStageBytes;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
@@ -107,8 +147,9 @@ struct Args {
     // stream-K: tile t = (row block t / mblocks, token block t % mblocks);
     // unit u = t * nsb + round; CTA c takes units [c U / G, (c+1) U / G)
     int64_t mblocks, units;
-    float *part;  // split tiles: [CTA][slot 0: first tile, 1: last tile][128 cols][128 rows]
+    float *part;  // split tiles: [CTA][slot 0: first tile, 1: last tile][BN cols][128 rows]
     const float *tok_scale;  // 2^-e per token (padded to 16), or null (W4A16)
+    int c_tma;               // whole tiles go to C through tmap_c (rows of C 16-byte aligned), else plain stores
 };
 
 __device__ __forceinline__ uint32_t lop_or(uint32_t x, uint32_t mask) {
@@ -133,6 +174,8 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
 }
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ void handoff_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+// the four epilogue warps
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 // fp16 scale * (q - zero) for the 8 codes of one word, as four pairs of
 // (low 16 bits, high 16 bits) fields: fields at bits 0-3 | 16-19, 8-11 |
@@ -263,12 +306,12 @@ __device__ __forceinline__ void store_cols(const Args &a, int64_t m0, int64_t n,
     }
 }
 
-// v[j] *= 2^-e of token j of the 16 at ts (the activation prescale taken
-// off: exact, a power of two). ts is 64-byte aligned and padded to 16 tokens.
-__device__ __forceinline__ void unscale16(const float *ts, float v[16]) {
+// v[j] *= 2^-e of token j of the 16 at ts, in shared memory (the activation
+// prescale taken off: exact, a power of two). ts is 16-byte aligned.
+__device__ __forceinline__ void scale16_s(const float *ts, float v[16]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float4 t = __ldg(reinterpret_cast<const float4 *>(ts) + i);
+        const float4 t = reinterpret_cast<const float4 *>(ts)[i];
         v[4 * i] *= t.x;
         v[4 * i + 1] *= t.y;
         v[4 * i + 2] *= t.z;
@@ -276,12 +319,17 @@ __device__ __forceinline__ void unscale16(const float *ts, float v[16]) {
     }
 }
 
-template <int F>
+template <int F, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_kernel(const Args a, const __grid_constant__ CUtensorMap tmap_w,
                     const __grid_constant__ CUtensorMap tmap_d,
-                    const __grid_constant__ CUtensorMap tmap_a) {
-    constexpr int kWBytes = FmtInfo<F>::kWBytes;
+                    const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_c) {
+    constexpr int kWBytes = FmtInfo<F>::kWBytes, kWStages = FmtInfo<F>::kWStages;
+    using T = Tile<BN>;
+    constexpr int kActStages = T::kActStages, kActBytes = T::kActBytes, kAccs = T::kAccs;
+    constexpr int kSlices = T::kSlices, kActK = T::kActK;
+    constexpr uint32_t kColARing = T::kColARing;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -295,8 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + FmtInfo<F>::kOffBar);
     uint64_t *w_full = bar, *w_empty = w_full + kWStages;
     uint64_t *act_full = w_empty + kWStages, *act_empty = act_full + kActStages;
-    uint64_t *a_full = act_empty + kActStages, *a_empty = a_full + kGroups;
-    uint64_t *acc_full = a_empty + kGroups, *acc_empty = acc_full + 2, *done = acc_empty + 2;
+    // A ring slot group (round parity r, group g) = r * kGroups + g
+    uint64_t *a_full = act_empty + kActStages, *a_empty = a_full + kARounds * kGroups;
+    uint64_t *acc_full = a_empty + kARounds * kGroups, *acc_empty = acc_full + kAccs, *done = acc_empty + kAccs;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
 
     if (threadIdx.x == 0) {
@@ -308,11 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&act_full[i]), 1);
             mbar_init(smem_u32(&act_empty[i]), 1);
         }
-        for (int i = 0; i < kGroups; ++i) {
+        for (int i = 0; i < kARounds * kGroups; ++i) {
             mbar_init(smem_u32(&a_full[i]), kConvWarps);  // both sets, one chunk each
             mbar_init(smem_u32(&a_empty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kAccs; ++i) {
             mbar_init(smem_u32(&acc_full[i]), 1);
             mbar_init(smem_u32(&acc_empty[i]), kEpiWarps);
         }
@@ -334,21 +383,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ activation producer
         if (lane == 0) {
-            tc::prefetch_tensormap(&tmap_w);
-            if (F == kQ40) tc::prefetch_tensormap(&tmap_d);
             tc::prefetch_tensormap(&tmap_a);
-            const uint64_t pol = policy_evict_last();  // weights and A are reused by other CTAs
+            const uint64_t pol = policy_evict_last();  // A is reused by the other row blocks' CTAs
             pdl_wait();  // the activations may come from the preceding kernel
-            int64_t issued_w = 0, issued_a = 0;
+            int64_t issued_a = 0;
             bool ok = true;
             for (int64_t i = 0; i < u1 - u0 && ok; ++i) {
                 const int64_t tile = (u0 + i) / nsb, sb = u0 + i - tile * nsb;
-                const int64_t n0 = (tile / a.mblocks) * kBM, m0 = (tile % a.mblocks) * kBN;
+                const int64_t m0 = (tile % a.mblocks) * BN;
+                // the round's activations: one stage per kActK elements of K
+                // (stage sequence number (4 i + c) kSlices + slice); K past the
+                // end and tokens past M read as zeros
+                for (int q = 0; q < kChunks * kSlices && ok; ++q, ++issued_a) {
+                    const int st = (int)(issued_a % kActStages);
+                    ok = mbar_wait(smem_u32(&act_empty[st]), (uint32_t)(((issued_a / kActStages) & 1) ^ 1), a.err);
+                    if (!ok) break;
+                    const uint32_t abar = smem_u32(&act_full[st]);
+                    mbar_arrive_expect_tx(abar, kActBytes);
+                    tc::tma_load_2d(smem_u32(smem + kOffAct + st * kActBytes), &tmap_a,
+                                    (int32_t)(sb * kSB + q * kActK), (int32_t)m0, abar, pol);
+                }
+            }
+            for (int64_t k = issued_a > kActStages ? issued_a - kActStages : 0; k < issued_a; ++k)
+                mbar_wait(smem_u32(&act_full[k % kActStages]), (uint32_t)((k / kActStages) & 1), a.err);
+        }
+        __syncwarp();  // lanes 1..31 wait here for the producer lane
+    } else if (warp == kWProdWarp) {
+        // ------------------------------------------------------------ weight producer
+        // A warp of its own, so that weight stages go out as soon as the
+        // converters free them, never queued behind activation chunks.
+        if (lane == 0) {
+            tc::prefetch_tensormap(&tmap_w);
+            if (F == kQ40) tc::prefetch_tensormap(&tmap_d);
+            const uint64_t pol = policy_evict_last();  // the other token blocks' CTAs read the same rows
+            pdl_wait();
+            int64_t issued_w = 0;
+            for (int64_t i = 0; i < u1 - u0; ++i) {
+                const int64_t tile = (u0 + i) / nsb, sb = u0 + i - tile * nsb;
+                const int64_t n0 = (tile / a.mblocks) * kBM;
                 const int ws = (int)(i % kWStages);
-                ok = mbar_wait(smem_u32(&w_empty[ws]), (uint32_t)(((i / kWStages) & 1) ^ 1), a.err);
-                if (!ok) break;
+                if (!mbar_wait(smem_u32(&w_empty[ws]), (uint32_t)(((i / kWStages) & 1) ^ 1), a.err)) break;
                 // rows past the last tile and K past the end read as zeros
                 const uint32_t wbar = smem_u32(&w_full[ws]);
                 uint8_t *wdst = smem + kOffW + ws * FmtInfo<F>::kWStage;
@@ -370,39 +446,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (int32_t)(n0 / kQ4Tile), wbar, pol);
                 }
                 ++issued_w;
-                const int st = (int)(i % kActStages);
-                ok = mbar_wait(smem_u32(&act_empty[st]), (uint32_t)(((i / kActStages) & 1) ^ 1), a.err);
-                if (!ok) break;
-                const uint32_t abar = smem_u32(&act_full[st]);
-                mbar_arrive_expect_tx(abar, kActBytes);
-                for (int c = 0; c < kChunks; ++c)
-                    tc::tma_load_2d(smem_u32(smem + kOffAct + st * kActBytes + c * kChunkBytes), &tmap_a,
-                                    (int32_t)(sb * kSB + c * kBK), (int32_t)m0, abar, pol);
-                ++issued_a;
             }
             for (int64_t k = issued_w > kWStages ? issued_w - kWStages : 0; k < issued_w; ++k)
                 mbar_wait(smem_u32(&w_full[k % kWStages]), (uint32_t)((k / kWStages) & 1), a.err);
-            for (int64_t k = issued_a > kActStages ? issued_a - kActStages : 0; k < issued_a; ++k)
-                mbar_wait(smem_u32(&act_full[k % kActStages]), (uint32_t)((k / kActStages) & 1), a.err);
         }
-        __syncwarp();  // lanes 1..31 wait here for the producer lane
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Meets the waiter at the named barrier the same number of times
         // whatever happens; after a timeout the MMAs run on stale operands and
         // the error word reports it.
-        constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
-        const uint64_t bdesc0 = tc::smem_desc(smem_u32(smem + kOffAct), 1024, 2);
+        constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, BN);
+        const uint64_t bdesc0 = tc::smem_desc(smem_u32(smem + kOffAct), T::kSbo, T::kSwz);
         int64_t i = 0;  // units done: the pipeline position
-        int pc = 0;     // pieces done: accumulator pc & 1
+        int pc = 0;     // pieces done: accumulator pc % kAccs
         for (int64_t u = u0; u < u1; ++pc) {
             const int64_t tile = u / nsb;
             const int sb_begin = (int)(u - tile * nsb);
             const int sb_end = (int)(nsb < sb_begin + (u1 - u) ? nsb : sb_begin + (u1 - u));
             u += sb_end - sb_begin;
-            const uint32_t dacc = tmem + kColAcc + (uint32_t)((pc & 1) * kBN);
+            const uint32_t dacc = tmem + (uint32_t)((pc % kAccs) * BN);
             for (int sb = sb_begin; sb < sb_end; ++sb, ++i) {
-                const int st = (int)(i % kActStages);
 #pragma unroll 1
                 for (int g = 0; g < kGroups; ++g) {
                     handoff_sync();
@@ -411,21 +475,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int h = 0; h < kChunks / kGroups; ++h) {
                             const int c = g * (kChunks / kGroups) + h;
-                            const uint32_t acol = tmem + kColARing + (uint32_t)c * kARingCols;
-                            // K step of 16 fp16 = 32 bytes = 2 in the descriptor's address field
-                            const uint64_t bdesc = bdesc0 + (uint64_t)((st * kActBytes + c * kChunkBytes) >> 4);
+                            const uint32_t acol =
+                                tmem + kColARing + (uint32_t)((int)(i & 1) * kChunks + c) * kARingCols;
 #pragma unroll
-                            for (int kk = 0; kk < kBK / 16; ++kk)
-                                tc::mma_f16_ta(dacc, acol + 8 * kk, bdesc + 2 * kk, idesc,
-                                               ((sb - sb_begin) | c | kk) != 0);
+                            for (int sl = 0; sl < kSlices; ++sl) {
+                                const int st = (int)(((i * kChunks + c) * kSlices + sl) % kActStages);
+                                const uint64_t bdesc = bdesc0 + (uint64_t)((st * kActBytes) >> 4);
+                                // K step of 16 fp16 = 32 bytes = 2 in the descriptor's address field
+#pragma unroll
+                                for (int kq = 0; kq < kActK / 16; ++kq) {
+                                    const int kk = sl * (kActK / 16) + kq;
+                                    tc::mma_f16_ta(dacc, acol + 8 * kk, bdesc + 2 * kq, idesc,
+                                                   ((sb - sb_begin) | c | kk) != 0);
+                                }
+                                tc::commit(smem_u32(&act_empty[st]));  // the stage is free once these are done
+                            }
                         }
-                        tc::commit(smem_u32(&a_empty[g]));
-                        if (g == kGroups - 1) tc::commit(smem_u32(&act_empty[st]));
+                        tc::commit(smem_u32(&a_empty[(int)(i & 1) * kGroups + g]));
                     }
                     __syncwarp();
                 }
             }
-            if (lane == 0) tc::commit(smem_u32(&acc_full[pc & 1]));
+            if (lane == 0) tc::commit(smem_u32(&acc_full[pc % kAccs]));
             __syncwarp();
         }
         if (lane == 0) {
@@ -446,15 +517,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sb_end = (int)(nsb < sb_begin + (u1 - u) ? nsb : sb_begin + (u1 - u));
             u += sb_end - sb_begin;
             if (lane == 0 && ok)
-                ok = mbar_wait(smem_u32(&acc_empty[pc & 1]), (uint32_t)(((pc >> 1) & 1) ^ 1), a.err);
+                ok = mbar_wait(smem_u32(&acc_empty[pc % kAccs]), (uint32_t)(((pc / kAccs) & 1) ^ 1), a.err);
             for (int sb = sb_begin; sb < sb_end; ++sb, ++i) {
-                const int st = (int)(i % kActStages);
-                const uint32_t par = (uint32_t)(i & 1);
-                if (lane == 0 && ok)
-                    ok = mbar_wait(smem_u32(&act_full[st]), (uint32_t)((i / kActStages) & 1), a.err);
+                const uint32_t par = (uint32_t)((i >> 1) & 1);  // slot group used every other round
+                const int rg = (int)(i & 1) * kGroups;
 #pragma unroll 1
                 for (int g = 0; g < kGroups; ++g) {
-                    if (lane == 0 && ok) ok = mbar_wait(smem_u32(&a_full[g]), par, a.err);
+                    // the group's two activation chunks, then its A operands
+                    for (int h = 0; h < (kChunks / kGroups) * kSlices && ok; ++h) {
+                        const int64_t ci = (i * kChunks + g * (kChunks / kGroups)) * kSlices + h;
+                        if (lane == 0)
+                            ok = mbar_wait(smem_u32(&act_full[ci % kActStages]), (uint32_t)((ci / kActStages) & 1),
+                                           a.err);
+                    }
+                    if (lane == 0 && ok) ok = mbar_wait(smem_u32(&a_full[rg + g]), par, a.err);
                     __syncwarp();
                     handoff_sync();
                 }
@@ -477,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t nc = n < a.N ? n : a.N - 1;  // rows past N: zero codes, clamped scales
             for (int64_t sb = sb_begin; sb < sb_end && ok; ++sb, ++pos) {
                 const int ws = (int)(pos % kWStages);
-                const uint32_t par = (uint32_t)(pos & 1);
+                const uint32_t par = (uint32_t)((pos >> 1) & 1);  // A ring slot group used every other round
+                const int rg = (int)(pos & 1) * kGroups;
                 ok = mbar_wait_warp(smem_u32(&w_full[ws]), (uint32_t)((pos / kWStages) & 1), a.err);
                 if (!ok) break;
                 const uint8_t *wst = smem + kOffW + ws * FmtInfo<F>::kWStage;
@@ -606,16 +683,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             out[4 * i + 3]);
                         }
                     }
-                    ok = mbar_wait_warp(smem_u32(&a_empty[g]), par ^ 1, a.err);
+                    ok = mbar_wait_warp(smem_u32(&a_empty[rg + g]), par ^ 1, a.err);
                     if (!ok) break;
                     tc::fence_after_sync();
-                    const uint32_t acol = tmem + lane_addr + kColARing + (uint32_t)c * kARingCols;
+                    const uint32_t acol =
+                        tmem + lane_addr + kColARing + (uint32_t)((int)(pos & 1) * kChunks + c) * kARingCols;
                     tc::tmem_st16(acol, lo);
                     tc::tmem_st16(acol + 16, hi);
                     tc::tmem_st_wait();
                     tc::fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&a_full[g]));
+                    if (lane == 0) mbar_arrive(smem_u32(&a_full[rg + g]));
                 }
                 __syncwarp();
                 if (lane == 0 && ok) mbar_arrive(smem_u32(&w_empty[ws]));
@@ -623,62 +701,108 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // Per piece: a whole tile goes to C, a part of one to this CTA's
-        // partial slot for the fixup kernel; then the accumulator is free for
-        // the piece after next. After a timed-out wait the loop still walks
-        // the pieces, without waits or stores.
+        // Per piece: the piece's token scales (2^-e per token) go to shared
+        // memory while its MMAs run; then the accumulator is read back 32
+        // columns per TMEM wait, and the accumulator is free for the piece
+        // kAccs later. A whole tile goes to C 16 columns at a time through a
+        // staging block in shared memory [16 tokens][128 rows] and a 2-D TMA
+        // store (which leaves out rows past N and tokens past M): one thread
+        // (the first epilogue lane) issues the stores, and a staging block is
+        // rewritten once the store issued from it two blocks back has read it.
+        // Where C's rows are not 16-byte aligned, whole tiles go to C by
+        // plain stores. A part of a split tile goes to this CTA's partial
+        // slot by plain stores (contiguous). After a timed-out wait the loop
+        // still walks the pieces and blocks (and meets the other epilogue
+        // warps at every barrier), without waits, TMEM loads or stores.
         const int quarter = warp & 3;  // TMEM lanes 32 * (warp % 4) ..
         const int nl = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const bool issuer = warp == kEpiWarp0 && lane == 0;
+        float *ts_s = reinterpret_cast<float *>(smem + FmtInfo<F>::kOffLut);
+        uint8_t *stage = smem + FmtInfo<F>::kOffStage;
+        if (F != kW4A16) pdl_wait();  // the token scales come from the preceding kernel
         bool ok = true;
         int pc = 0;
+        uint32_t blk = 0;  // staging blocks used so far: block blk is in buffer blk & 1
         for (int64_t u = u0; u < u1; ++pc) {
             const int64_t tile = u / nsb;
             const int sb_begin = (int)(u - tile * nsb);
             const int sb_end = (int)(nsb < sb_begin + (u1 - u) ? nsb : sb_begin + (u1 - u));
             u += sb_end - sb_begin;
-            const int64_t n = (tile / a.mblocks) * kBM + nl, m0 = (tile % a.mblocks) * kBN;
-            const uint32_t acc = tmem + lane_addr + kColAcc + (uint32_t)((pc & 1) * kBN);
-            if (ok) ok = mbar_wait_warp(smem_u32(&acc_full[pc & 1]), (uint32_t)((pc >> 1) & 1), a.err);
+            const int64_t n0 = (tile / a.mblocks) * kBM, m0 = (tile % a.mblocks) * BN;
+            const int64_t n = n0 + nl;
+            const uint32_t acc = tmem + lane_addr + (uint32_t)((pc % kAccs) * BN);
+            // column groups holding tokens < M (warp-uniform): the rest is
+            // padding; m0 + 16 ncg <= M rounded up to 16, the scales' length
+            const int ncg = (int)((a.M - m0 < BN ? a.M - m0 + 15 : BN) / 16);
+            if (F != kW4A16) {
+                epi_sync();  // every epilogue warp is done with the last piece's scales
+                for (int j = (warp - kEpiWarp0) * 32 + lane; j < ncg * 16; j += kEpiWarps * 32)
+                    ts_s[j] = a.tok_scale[m0 + j];
+                epi_sync();
+            }
+            if (ok) ok = mbar_wait_warp(smem_u32(&acc_full[pc % kAccs]), (uint32_t)((pc / kAccs) & 1), a.err);
             if (ok) tc::fence_after_sync();
-            // TMEM loads are warp-collective: every lane takes them (ok is
-            // warp-uniform); only the stores depend on the row
-            const bool row_ok = n < a.N;
-            // column groups holding tokens < M (warp-uniform): the rest is padding
-            const int ncg = (int)((a.M - m0 < kBN ? a.M - m0 + 15 : kBN) / 16);
-            if (sb_begin == 0 && sb_end == nsb) {
-                if (ok) {
+            const bool whole = sb_begin == 0 && sb_end == nsb;
+            const bool staged = whole && a.c_tma;
+            // this CTA's partial slot for a part of a split tile: column j at j * kBM
+            float *slot = whole ? nullptr : a.part + sk_slot(blockIdx.x, tile, a.units, gridDim.x, nsb, BN);
 #pragma unroll 1
-                    for (int c16 = 0; c16 < ncg; ++c16) {
-                        float v[16];
-                        tc::tmem_ld16(acc + (uint32_t)(c16 * 16), v);
-                        tc::tmem_ld_wait();
-                        if (F != kW4A16) unscale16(a.tok_scale + m0 + c16 * 16, v);
-                        if (row_ok) store_cols<F>(a, m0 + c16 * 16, n, v);
-                    }
+            for (int c32 = 0; c32 < ncg; c32 += 2) {
+                // columns 16 c32 .. 16 c32 + 31 (below BN even where the
+                // second half is past the last group); TMEM loads are
+                // warp-collective and ok is warp-uniform
+                float v[2][16];
+                if (ok) {
+                    tc::tmem_ld16(acc + (uint32_t)(c32 * 16), v[0]);
+                    tc::tmem_ld16(acc + (uint32_t)(c32 * 16 + 16), v[1]);
+                    tc::tmem_ld_wait();
                 }
-            } else {
-                // a part of a split tile: to this CTA's slot (column-major:
-                // column j of this row at j * kBM) for the fixup kernel
-                float *mine = a.part + sk_slot(blockIdx.x, tile, a.units, gridDim.x, nsb) + nl;
-                if (ok) {
-#pragma unroll 1
-                    for (int c16 = 0; c16 < ncg; ++c16) {
-                        float v[16];
-                        tc::tmem_ld16(acc + (uint32_t)(c16 * 16), v);
-                        tc::tmem_ld_wait();
-                        if (F != kW4A16) unscale16(a.tok_scale + m0 + c16 * 16, v);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) mine[(c16 * 16 + j) * kBM] = v[j];
+                for (int h = 0; h < 2; ++h) {
+                    const int c16 = c32 + h;
+                    if (c16 >= ncg) break;
+                    if (F != kW4A16 && ok) scale16_s(ts_s + c16 * 16, v[h]);
+                    if (!staged) {
+                        if (ok && whole && n < a.N) {
+                            store_cols<F>(a, m0 + c16 * 16, n, v[h]);
+                        } else if (ok && !whole) {
+                            float *mine = slot + c16 * 16 * kBM + nl;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) mine[j * kBM] = v[h][j];
+                        }
+                        continue;
                     }
+                    uint8_t *sb = stage + (blk & 1) * kStageBytes;
+                    if (issuer) tc::bulk_wait_read<1>();  // the copy from this buffer two blocks back
+                    epi_sync();
+                    if (ok) {
+                        if (F == kW4A16) {
+                            __half *st = reinterpret_cast<__half *>(sb) + nl;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) st[j * kBM] = __float2half_rn(v[h][j]);
+                        } else {
+                            float *st = reinterpret_cast<float *>(sb) + nl;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) st[j * kBM] = v[h][j];
+                        }
+                    }
+                    tc::fence_proxy_async();
+                    epi_sync();
+                    if (issuer && ok) {
+                        tc::tma_store_2d(&tmap_c, (int32_t)n0, (int32_t)(m0 + c16 * 16), smem_u32(sb));
+                        tc::bulk_commit();
+                    }
+                    ++blk;
                 }
             }
             if (ok) {
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[pc & 1]));
+                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[pc % kAccs]));
             }
         }
+        if (issuer) tc::bulk_wait_all();  // the copies' writes done before the CTA ends
     }
 
     tc::fence_before_sync();
@@ -893,13 +1017,29 @@ __global__ void __launch_bounds__(kActThreads) import_q8_K_f16_kernel(const uint
 
 // The GEMM (programmatic dependent launch): one CTA per tile, or with more
 // tiles than SMs a persistent stream-K grid and the fixup of its split tiles.
-template <int F>
-cudaError_t launch_stream_k(Args a, const CUtensorMap &tmap_w, const CUtensorMap &tmap_d,
-                            const CUtensorMap &tmap_a, cudaStream_t s) {
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_f16_kernel<F>), FmtInfo<F>::kSmemBytes);
+// act: the fp16 activations [M][K], read through a swizzled 2-D tensor
+// map whose box is one stage (BN tokens x kActK elements). C is written through
+// a 2-D tensor map (box 128 rows x 16 tokens) where its base and rows are
+// 16-byte aligned, else by plain stores.
+template <int F, int BN>
+cudaError_t launch_stream_k_bn(Args a, const CUtensorMap &tmap_w, const CUtensorMap &tmap_d, const void *act,
+                               cudaStream_t s) {
+    auto fn = gemm_f16_kernel<F, BN>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn), FmtInfo<F>::kSmemBytes);
     if (e != cudaSuccess) return e;
+    CUtensorMap tmap_a;
+    if (!tc::make_tmap_2d(&tmap_a, act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.M, (uint64_t)a.K, BN,
+                          Tile<BN>::kActK,
+                          Tile<BN>::kActK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    CUtensorMap tmap_c;
+    const uint32_t celem = F == kW4A16 ? 2 : 4;
+    a.c_tma = ((uintptr_t)a.C % 16) == 0 && ((uint64_t)a.N * celem) % 16 == 0 &&
+              tc::make_tmap_2d(&tmap_c, a.C, F == kW4A16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                               celem, (uint64_t)a.M, (uint64_t)a.N, kStageCols, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!a.c_tma) memset(&tmap_c, 0, sizeof tmap_c);
     const int64_t nsb = (a.K + kSB - 1) / kSB;
-    a.mblocks = (a.M + kBN - 1) / kBN;
+    a.mblocks = (a.M + BN - 1) / BN;
     const int64_t tiles = ((a.N + kBM - 1) / kBM) * a.mblocks;
     a.units = tiles * nsb;
     const int64_t G = stream_k_grid(tiles, a.units);
@@ -913,10 +1053,19 @@ cudaError_t launch_stream_k(Args a, const CUtensorMap &tmap_w, const CUtensorMap
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemm_f16_kernel<F>, a, tmap_w, tmap_d, tmap_a);
+    e = cudaLaunchKernelEx(&cfg, fn, a, tmap_w, tmap_d, tmap_a, tmap_c);
     count_launch();
     if (e != cudaSuccess || G == tiles) return e;
-    return launch_stream_k_fixup(a.part, a.C, F == kW4A16, a.N, a.M, a.mblocks, nsb, a.units, G, s);
+    return launch_stream_k_fixup(a.part, a.C, F == kW4A16, BN, a.N, a.M, a.mblocks, nsb, a.units, G, s);
+}
+
+template <int F>
+cudaError_t launch_stream_k(const Args &a, const CUtensorMap &tmap_w, const CUtensorMap &tmap_d, const void *act,
+                            cudaStream_t s) {
+    constexpr int wt = F == kW4A16 ? QMM_TYPE_W4A16 : F == kQ40 ? QMM_TYPE_Q4_0 : F == kQ6K ? QMM_TYPE_Q6_K
+                                                                                       : QMM_TYPE_Q4_K;
+    return gemm_tile_cols(wt, a.M) == 256 ? launch_stream_k_bn<F, 256>(a, tmap_w, tmap_d, act, s)
+                                      : launch_stream_k_bn<F, 128>(a, tmap_w, tmap_d, act, s);
 }
 
 }  // namespace
@@ -955,16 +1104,14 @@ cudaError_t launch_w4a16_gemm(const void *W, const __half *S, const uint8_t *Z, 
     a.part = part;
     a.tok_scale = nullptr;
     const int64_t nsteps = K / kW4StepK, ntiles16 = (N + kW4Tile - 1) / kW4Tile;
-    CUtensorMap tmap_w, tmap_a;
+    CUtensorMap tmap_w;
     // packed weights as [16-row tile][step][1 KB], in 4-byte units
     const uint64_t wdims[3] = {256, (uint64_t)nsteps, (uint64_t)ntiles16};
     const uint64_t wstrides[2] = {1024, (uint64_t)nsteps * 1024};
     const uint32_t wbox[3] = {256, kSB / kW4StepK, kBM / kW4Tile};
-    if (!tc::make_tmap_3d(&tmap_w, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, wdims, wstrides, wbox) ||
-        !tc::make_tmap_2d(&tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M, (uint64_t)K,
-                          kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!tc::make_tmap_3d(&tmap_w, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, wdims, wstrides, wbox))
         return cudaErrorInvalidValue;
-    return launch_stream_k<kW4A16>(a, tmap_w, tmap_w, tmap_a, s);
+    return launch_stream_k<kW4A16>(a, tmap_w, tmap_w, A, s);
 }
 
 cudaError_t launch_quantize_q4_0_prefill(const float *X, void *ws, int64_t M, int64_t K,
@@ -992,7 +1139,7 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
     a.tok_scale = tok_scales(ws, M, K);
     const int64_t nb = K / QK4_0, ntiles = tiles_of(N);
     const uint64_t tile_bytes = (uint64_t)nb * kQ4Tile * B_Q4_0;
-    CUtensorMap tmap_w, tmap_d, tmap_a;
+    CUtensorMap tmap_w, tmap_d;
     // nibble planes as [tile][row][block][4 words], read as [tile][block][row][16 B]
     const uint64_t ndims[4] = {4, (uint64_t)kQ4Tile, (uint64_t)nb, (uint64_t)ntiles};
     const uint64_t nstrides[3] = {(uint64_t)nb * 16, 16, tile_bytes};
@@ -1003,11 +1150,9 @@ cudaError_t launch_gemm_q4_0(const void *Wp, int64_t N, int64_t K, const void *w
     const uint32_t dbox[3] = {(uint32_t)kQ4Tile, kQ4Blocks, kBM / kQ4Tile};
     const uint8_t *dplane = static_cast<const uint8_t *>(Wp) + (size_t)nb * kQ4Tile * 16;
     if (!tc::make_tmap_4d(&tmap_w, Wp, CU_TENSOR_MAP_DATA_TYPE_UINT32, ndims, nstrides, nbox) ||
-        !tc::make_tmap_3d(&tmap_d, dplane, CU_TENSOR_MAP_DATA_TYPE_UINT16, ddims, dstrides, dbox) ||
-        !tc::make_tmap_2d(&tmap_a, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M, (uint64_t)K,
-                          kBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+        !tc::make_tmap_3d(&tmap_d, dplane, CU_TENSOR_MAP_DATA_TYPE_UINT16, ddims, dstrides, dbox))
         return cudaErrorInvalidValue;
-    return launch_stream_k<kQ40>(a, tmap_w, tmap_d, tmap_a, s);
+    return launch_stream_k<kQ40>(a, tmap_w, tmap_d, ws, s);
 }
 
 // ------------------------------------------------------------------ Q6_K prefill
@@ -1043,15 +1188,13 @@ cudaError_t launch_gemm_q4_K_f16(const void *Wp, int64_t N, int64_t K, const voi
     a.tok_scale = tok_scales(ws, M, K);
     const int64_t nsb = K / QK_K;
     constexpr int kRec = kTileRows * B_Q4_K;  // 1152 B: one (tile, super-block)
-    CUtensorMap tmap_w, tmap_a;
+    CUtensorMap tmap_w;
     const uint64_t wdims[3] = {kRec / 8, (uint64_t)nsb, (uint64_t)tiles_of(N)};
     const uint64_t wstrides[2] = {(uint64_t)kRec, (uint64_t)nsb * kRec};
     const uint32_t wbox[3] = {kRec / 8, 1, kBM / kTileRows};
-    if (!tc::make_tmap_3d(&tmap_w, Wp, CU_TENSOR_MAP_DATA_TYPE_UINT64, wdims, wstrides, wbox) ||
-        !tc::make_tmap_2d(&tmap_a, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M, (uint64_t)K, kBN, kBK,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!tc::make_tmap_3d(&tmap_w, Wp, CU_TENSOR_MAP_DATA_TYPE_UINT64, wdims, wstrides, wbox))
         return cudaErrorInvalidValue;
-    return launch_stream_k<kQ4K>(a, tmap_w, tmap_w, tmap_a, s);
+    return launch_stream_k<kQ4K>(a, tmap_w, tmap_w, ws, s);
 }
 
 cudaError_t launch_gemm_q6_K(const void *Wp, int64_t N, int64_t K, const void *ws, float *part, int64_t M,
@@ -1070,16 +1213,14 @@ cudaError_t launch_gemm_q6_K(const void *Wp, int64_t N, int64_t K, const void *w
     a.part = part;
     a.tok_scale = tok_scales(ws, M, K);
     const int64_t nsb = K / QK_K;
-    CUtensorMap tmap_w, tmap_a;
+    CUtensorMap tmap_w;
     // packed records as [8-row tile][super-block][1680 B], in 8-byte units
     const uint64_t wdims[3] = {kQ6Rec / 8, (uint64_t)nsb, (uint64_t)tiles_of(N)};
     const uint64_t wstrides[2] = {(uint64_t)kQ6Rec, (uint64_t)nsb * kQ6Rec};
     const uint32_t wbox[3] = {kQ6Rec / 8, 1, kBM / kTileRows};
-    if (!tc::make_tmap_3d(&tmap_w, Wp, CU_TENSOR_MAP_DATA_TYPE_UINT64, wdims, wstrides, wbox) ||
-        !tc::make_tmap_2d(&tmap_a, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)M, (uint64_t)K, kBN, kBK,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!tc::make_tmap_3d(&tmap_w, Wp, CU_TENSOR_MAP_DATA_TYPE_UINT64, wdims, wstrides, wbox))
         return cudaErrorInvalidValue;
-    return launch_stream_k<kQ6K>(a, tmap_w, tmap_w, tmap_a, s);
+    return launch_stream_k<kQ6K>(a, tmap_w, tmap_w, ws, s);
 }
 
 }  // namespace qmm

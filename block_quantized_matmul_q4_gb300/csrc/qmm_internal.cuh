@@ -327,19 +327,26 @@ __device__ __forceinline__ int clampi(int v, int lo, int hi) { return min(max(v,
 // SM count and a tile may span several CTAs: each CTA that holds only part of
 // it writes that piece to its partial slot (slot 0 when the tile is the
 // CTA's first, 1 when its last), and the fixup kernel (streamk.cu) adds the
-// pieces in CTA order and writes the tile.
-constexpr int kSkTile = 128;   // tile rows = tile columns
+// pieces in CTA order and writes the tile. A tile is 128 weight rows by
+// gemm_tile_cols(wt, M) tokens: 256 above 128 tokens (every decoded weight
+// then serves 256 tokens), else 128; Q4_0, whose weights decode in a few fp16
+// instructions, measured faster at 128 whatever M.
+constexpr int kSkTile = 128;   // tile rows
 constexpr int kSkRound = 256;  // K elements per unit
+constexpr int kSkColsMax = 256;
+__host__ __device__ inline int gemm_tile_cols(int wt, int64_t M) {
+    return wt != QMM_TYPE_Q4_0 && M > 128 ? 256 : 128;
+}
 
 // The CTA whose range holds unit u.
 __host__ __device__ __forceinline__ int64_t sk_cta_of(int64_t u, int64_t U, int64_t G) {
     return ((u + 1) * G - 1) / U;
 }
 // Float offset of CTA c's slot for `tile` in the partial area
-// [G][2][128 cols][128 rows] (a column's 128 rows contiguous).
+// [G][2][cols][128 rows] (a column's 128 rows contiguous), cols the tile's.
 __host__ __device__ __forceinline__ int64_t sk_slot(int64_t c, int64_t tile, int64_t U, int64_t G,
-                                                    int64_t nsb) {
-    return (c * 2 + ((c * U / G) / nsb == tile ? 0 : 1)) * (int64_t)(kSkTile * kSkTile);
+                                                    int64_t nsb, int cols) {
+    return (c * 2 + ((c * U / G) / nsb == tile ? 0 : 1)) * (int64_t)(kSkTile * cols);
 }
 
 // ------------------------------------------------------------------ activation quantization
@@ -507,15 +514,16 @@ cudaError_t launch_debug_wait_timeout(int64_t limit_cycles, cudaStream_t s);
 cudaError_t launch_debug_peak(int which, int64_t iters, cudaStream_t s, double *ops);
 // Stream-K GEMMs (streamk.cu): CTAs for `tiles` tiles of `units` units (the
 // SM count above it, one per tile from half of it, else split K over up to
-// the SM count); bytes of the partial area; the fixup that adds the split
-// tiles' pieces into C (fp32, or fp16 when half_out), launched only when
-// G != tiles.
+// the SM count); bytes of the partial area (enough for either tile width);
+// the fixup that adds the split tiles' pieces into C (fp32, or fp16 when
+// half_out), launched only when G != tiles.
 int64_t stream_k_grid(int64_t tiles, int64_t units);
 size_t stream_k_part_bytes();
-// Whether an N x M output of depth K (128 x 128 tiles, 256-element units)
-// runs split tiles, i.e. needs the partial area.
-bool stream_k_splits(int64_t N, int64_t M, int64_t K);
-cudaError_t launch_stream_k_fixup(const float *part, void *C, bool half_out, int64_t N, int64_t M,
+// Whether an N x M output of depth K (128 x gemm_tile_cols(wt, M) tiles,
+// 256-element units) of weight type wt runs split tiles, i.e. needs the
+// partial area.
+bool stream_k_splits(int wt, int64_t N, int64_t M, int64_t K);
+cudaError_t launch_stream_k_fixup(const float *part, void *C, bool half_out, int cols, int64_t N, int64_t M,
                                   int64_t mblocks, int64_t nsb, int64_t units, int64_t G,
                                   cudaStream_t s);
 }  // namespace qmm

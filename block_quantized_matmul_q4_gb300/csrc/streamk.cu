@@ -4,14 +4,14 @@
 // contiguous ranges (CTA c: [c U / G, (c+1) U / G)); a CTA that holds all of
 // a tile's units writes it, otherwise its piece went to its partial slot
 // (slot 0 when the tile is the CTA's first, 1 when its last), fp32
-// [G][2][128 cols][128 rows]. Here every split tile gets the sum of its
+// [G][2][TN cols][128 rows]. Here every split tile gets the sum of its
 // pieces, added in CTA order (the same order every run), written to C.
 #include "qmm_internal.cuh"
 
 namespace qmm {
 namespace {
 
-constexpr int kTM = kSkTile, kTN = kSkTile;  // tile rows (weights) and columns (tokens)
+constexpr int kTM = kSkTile;  // tile rows (weights); TN, the columns (tokens), is a template parameter
 constexpr int64_t kMaxGrid = 1024;           // CTAs of a persistent grid at most
 constexpr int kFixupThreads = 512;
 
@@ -27,17 +27,28 @@ __device__ __forceinline__ float out_cast<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __half out_cast<__half>(float v) { return __float2half_rn(v); }
 
+// Rows n .. n+3 of one column of C in a single store (C's rows 16-byte
+// aligned for fp32, 8-byte for fp16, n a multiple of 4).
+__device__ __forceinline__ void store4(float *y, float4 v) { *reinterpret_cast<float4 *>(y) = v; }
+__device__ __forceinline__ void store4(__half *y, float4 v) {
+    const __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+    *reinterpret_cast<uint2 *>(y) = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
+                                               *reinterpret_cast<const uint32_t *>(&hi));
+}
+
 // The pieces of one split tile, added in CTA order and stored. Each thread
 // takes 4 consecutive rows of a column (one 16-byte load per piece) and keeps
 // 4 columns in flight; a warp covers 128 rows of one column = 512 contiguous
-// bytes of every slot. kFull: all 128 columns hold tokens (the bound is a
+// bytes of every slot. kFull: all TN columns hold tokens (the bound is a
 // constant); otherwise the first nq quads only (the columns the GEMM
-// epilogue wrote, tokens < M rounded up to 16).
-template <bool kFull, class T>
+// epilogue wrote, tokens < M rounded up to 16). vec: C's rows are aligned
+// for one 4-row store (N a multiple of 4, C aligned).
+template <int TN, bool kFull, class T>
 __device__ __forceinline__ void fixup_tile(const float *__restrict__ part, T *__restrict__ C, int64_t N,
                                            int64_t M, int64_t tile, int64_t n0, int64_t m0, int nq,
-                                           int64_t ca, int64_t cb, int64_t nsb, int64_t units, int64_t G) {
-    constexpr int kQuads = kTM * kTN / 4;
+                                           int64_t ca, int64_t cb, int64_t nsb, int64_t units, int64_t G,
+                                           bool vec) {
+    constexpr int kQuads = kTM * TN / 4;
     const int nquads = kFull ? kQuads : nq;
     for (int e0 = threadIdx.x; e0 < nquads; e0 += 4 * kFixupThreads) {
         float4 v[4];
@@ -46,13 +57,13 @@ __device__ __forceinline__ void fixup_tile(const float *__restrict__ part, T *__
         for (int h = 0; h < 4; ++h) {
             const int e = e0 + h * kFixupThreads;  // kQuads is a multiple of 4 * kFixupThreads
             rr[h] = (e % (kTM / 4)) * 4;
-            cc[h] = (kFull || e < nquads) ? e / (kTM / 4) : kTN;  // kTN: not written, skipped
+            cc[h] = (kFull || e < nquads) ? e / (kTM / 4) : TN;  // TN: not written, skipped
         }
         for (int64_t k = ca; k <= cb; ++k) {
-            const float *slot = part + sk_slot(k, tile, units, G, nsb);
+            const float *slot = part + sk_slot(k, tile, units, G, nsb, TN);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                if (!kFull && cc[h] >= kTN) continue;
+                if (!kFull && cc[h] >= TN) continue;
                 const float4 p = __ldcg(reinterpret_cast<const float4 *>(slot + cc[h] * kTM + rr[h]));
                 if (k == ca) {
                     v[h] = p;
@@ -67,8 +78,12 @@ __device__ __forceinline__ void fixup_tile(const float *__restrict__ part, T *__
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             const int64_t m = m0 + cc[h], n = n0 + rr[h];
-            if ((kFull || cc[h] < kTN) && m < M) {
+            if ((kFull || cc[h] < TN) && m < M) {
                 T *y = C + m * N + n;
+                if (vec && n + 3 < N) {
+                    store4(y, v[h]);
+                    continue;
+                }
                 if (n < N) y[0] = out_cast<T>(v[h].x);
                 if (n + 1 < N) y[1] = out_cast<T>(v[h].y);
                 if (n + 2 < N) y[2] = out_cast<T>(v[h].z);
@@ -79,25 +94,25 @@ __device__ __forceinline__ void fixup_tile(const float *__restrict__ part, T *__
 }
 
 // One CTA per tile (whole tiles return at once).
-template <class T>
+template <int TN, class T>
 __global__ void __launch_bounds__(kFixupThreads) stream_k_fixup_kernel(const float *__restrict__ part,
                                                                        T *__restrict__ C, int64_t N,
                                                                        int64_t M, int64_t mblocks,
                                                                        int64_t nsb, int64_t units,
-                                                                       int64_t G) {
+                                                                       int64_t G, bool vec) {
     pdl_wait();  // the GEMM's pieces
     const int64_t tile = blockIdx.x;
     const int64_t ca = sk_cta_of(tile * nsb, units, G), cb = sk_cta_of(tile * nsb + nsb - 1, units, G);
     if (ca == cb) return;  // written whole by its CTA
-    const int64_t n0 = (tile / mblocks) * kTM, m0 = (tile % mblocks) * kTN;
-    const int64_t mv = M - m0 < kTN ? M - m0 : kTN;  // columns holding tokens
-    if (mv == kTN)
-        fixup_tile<true>(part, C, N, M, tile, n0, m0, 0, ca, cb, nsb, units, G);
+    const int64_t n0 = (tile / mblocks) * kTM, m0 = (tile % mblocks) * TN;
+    const int64_t mv = M - m0 < TN ? M - m0 : TN;  // columns holding tokens
+    if (mv == TN)
+        fixup_tile<TN, true>(part, C, N, M, tile, n0, m0, 0, ca, cb, nsb, units, G, vec);
     else
-        fixup_tile<false>(part, C, N, M, tile, n0, m0, (int)((mv + 15) / 16 * 16) * (kTM / 4), ca, cb, nsb,
-                          units, G);
+        fixup_tile<TN, false>(part, C, N, M, tile, n0, m0, (int)((mv + 15) / 16 * 16) * (kTM / 4), ca, cb, nsb,
+                              units, G, vec);
 }
-static_assert((kTM * kTN / 4) % (4 * kFixupThreads) == 0, "fixup tiling");
+static_assert((kTM * 128 / 4) % (4 * kFixupThreads) == 0, "fixup tiling");
 
 }  // namespace
 
@@ -113,18 +128,19 @@ int64_t stream_k_grid(int64_t tiles, int64_t units) {
     return units < g ? (units < 1 ? 1 : units) : g;
 }
 
-bool stream_k_splits(int64_t N, int64_t M, int64_t K) {
-    const int64_t tiles = ((N + kTM - 1) / kTM) * ((M + kTN - 1) / kTN);
+bool stream_k_splits(int wt, int64_t N, int64_t M, int64_t K) {
+    const int64_t tn = gemm_tile_cols(wt, M);
+    const int64_t tiles = ((N + kTM - 1) / kTM) * ((M + tn - 1) / tn);
     const int64_t units = tiles * ((K + kSkRound - 1) / kSkRound);
     return stream_k_grid(tiles, units) != tiles;
 }
 
-// Two 128 x 128 fp32 slots per CTA of the largest grid.
-size_t stream_k_part_bytes() { return align_up((size_t)2 * max_grid() * kTM * kTN * 4, 256); }
+// Two fp32 slots of the widest tile per CTA of the largest grid.
+size_t stream_k_part_bytes() { return align_up((size_t)2 * max_grid() * kTM * kSkColsMax * 4, 256); }
 
-cudaError_t launch_stream_k_fixup(const float *part, void *C, bool half_out, int64_t N, int64_t M,
-                                  int64_t mblocks, int64_t nsb, int64_t units, int64_t G,
-                                  cudaStream_t s) {
+template <int TN>
+cudaError_t launch_fixup_tn(const float *part, void *C, bool half_out, int64_t N, int64_t M, int64_t mblocks,
+                            int64_t nsb, int64_t units, int64_t G, cudaStream_t s) {
     const int64_t nblocks = (N + kTM - 1) / kTM;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nblocks * mblocks));
@@ -135,13 +151,18 @@ cudaError_t launch_stream_k_fixup(const float *part, void *C, bool half_out, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e;
     if (half_out)
-        e = cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<__half>, part, static_cast<__half *>(C), N, M,
-                               mblocks, nsb, units, G);
-    else
-        e = cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<float>, part, static_cast<float *>(C), N, M,
-                               mblocks, nsb, units, G);
+        return cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<TN, __half>, part, static_cast<__half *>(C), N, M,
+                                  mblocks, nsb, units, G, N % 4 == 0 && (uintptr_t)C % 8 == 0);
+    return cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<TN, float>, part, static_cast<float *>(C), N, M, mblocks,
+                              nsb, units, G, N % 4 == 0 && (uintptr_t)C % 16 == 0);
+}
+
+cudaError_t launch_stream_k_fixup(const float *part, void *C, bool half_out, int cols, int64_t N, int64_t M,
+                                  int64_t mblocks, int64_t nsb, int64_t units, int64_t G,
+                                  cudaStream_t s) {
+    cudaError_t e = cols == 256 ? launch_fixup_tn<256>(part, C, half_out, N, M, mblocks, nsb, units, G, s)
+                                : launch_fixup_tn<128>(part, C, half_out, N, M, mblocks, nsb, units, G, s);
     count_launch();
     return e;
 }

@@ -74,8 +74,9 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t m, uint32_t n) {
 }
 
 // Shared-memory matrix descriptor for a K-major tile. swizzle: 2 = 128B,
-// 6 = 32B. sbo = byte stride between 8-row groups. The tile base must be
-// aligned to the swizzle atom (1024 B for 128B, 256 B for 32B).
+// 4 = 64B, 6 = 32B. sbo = byte stride between 8-row groups. The tile base
+// must be aligned to the swizzle atom (1024 B for 128B, 512 B for 64B, 256 B
+// for 32B).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo, uint32_t swizzle) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFF) >> 4);  // start address
@@ -157,6 +158,25 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         "l"(policy)
         : "memory");
 }
+// A shared -> global 2-D tile store through a tensor map (elements outside
+// the tensor are not written), tracked in the bulk groups of the issuing
+// thread. The shared source must be made visible to the async proxy
+// (fence_proxy_async) by the threads that wrote it first.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int32_t c0, int32_t c1, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most N of this thread's bulk groups still reading their shared source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// All of this thread's bulk groups complete (their writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -36,7 +36,7 @@ int main() {
             const int64_t u0 = c * U / G, u1 = (c + 1) * U / G;
             if (u1 <= u0) continue;
             const int64_t t0 = u0 / nsb, t1 = (u1 - 1) / nsb;
-            const int64_t s0 = sk_slot(c, t0, U, G, nsb), s1 = sk_slot(c, t1, U, G, nsb);
+            const int64_t s0 = sk_slot(c, t0, U, G, nsb, 128), s1 = sk_slot(c, t1, U, G, nsb, 128);
             CHECK(s0 == c * 2 * 16384);
             CHECK(t0 == t1 || s1 == (c * 2 + 1) * 16384);
             CHECK(used.insert(s0).second);
