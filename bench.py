@@ -507,6 +507,7 @@ def gpu_extras(q, dev, stream, args):
     torch.cuda.empty_cache()
     out["q6_K"] = q6_K_rate(q, dev, stream)
     out["q4_K_4096_M_sweep"] = sweep_rate(q, dev, stream)
+    out["q4_0_q6_K_4096_M_sweep"] = small_m_rate(q, dev, stream)
     # Q4_0 x Q8_0 GEMV, 256 x 1024, M = 1 (L2-resident correctness case)
     Ls = wl.GEMV_Q4_0_SMALL
     t, b = gemv_rate(q, dev, stream, q.QMM_TYPE_Q4_0, Ls.N, Ls.K, 1, 0, Ls, copies=1)
@@ -542,9 +543,11 @@ def q6_K_rate(q, dev, stream):
 
 
 def small_m_rate(q, dev, stream):
-    """Q4_0 and Q6_K at 4096 x 4096, M in {2, 4, 8, 16}: qmm_mul_mat_ws (the
-    path mul_mat takes) against qmm_mul_mat_static (always the 16-token
-    scalar GEMV); us per call, weights rotating over 32 copies."""
+    """Q4_0 and Q6_K at 4096 x 4096, M in {1, 2, 4, 8, 12, 16} through
+    qmm_mul_mat_ws: M = 1 runs the scalar GEMV, M >= 2 the tensor-core one
+    (with its activation image written by a quantizer launch ahead of it);
+    us per call, weights rotating over 32 copies (302 MB, above L2), GB/s of
+    the weight bytes."""
     out = {}
     L = wl.GEMV_Q4_K_4096
     for wt, tag in ((q.QMM_TYPE_Q4_0, "q4_0"), (q.QMM_TYPE_Q6_K, "q6_K")):
@@ -555,25 +558,21 @@ def small_m_rate(q, dev, stream):
         Wp = q.empty_packed(wt, L.N, L.K)
         q.qmm_repack_weights(wt, Wq, Wp, L.N, L.K)
         del w, Wq
+        wbytes = Wp.numel()
         cps = [Wp] + [Wp.clone() for _ in range(31)]
-        for M in (2, 4, 8, 16):
+        for M in (1, 2, 4, 8, 12, 16):
             X = wl.activations(0, M, L.K, device=dev)
             Y = torch.empty(M, L.N, device=dev)
-            ws_bytes = q.qmm_workspace_bytes(wt, M, L.K)
+            ws_bytes = max(q.qmm_workspace_bytes(wt, M, L.K), 16)
             ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-            res = {}
-            for name, fn in (("mul_mat", lambda i: q.qmm_mul_mat_ws(wt, cps[i % 32], L.N, L.K, X, M, Y, ws,
-                                                                    ws_bytes, stream)),
-                             ("gemv", lambda i: q.qmm_mul_mat_static(wt, cps[i % 32], L.N, L.K, X, M, Y,
-                                                                     stream))):
-                for i in range(3):
-                    fn(i)
-                g = capture(fn, GRAPH_STEPS, stream)
-                with torch.cuda.stream(stream):
-                    g.replay()
-                t = timed(stream, lambda: run_graphs(g, None, 20)) / (20 * GRAPH_STEPS)
-                res[name + "_us"] = round(t * 1e6, 3)
-            out[f"{tag}_m{M}"] = res
+            fn = lambda i: q.qmm_mul_mat_ws(wt, cps[i % 32], L.N, L.K, X, M, Y, ws, ws_bytes, stream)
+            for i in range(3):
+                fn(i)
+            g = capture(fn, GRAPH_STEPS, stream)
+            with torch.cuda.stream(stream):
+                g.replay()
+            t = timed(stream, lambda: run_graphs(g, None, 20)) / (20 * GRAPH_STEPS)
+            out[f"{tag}_m{M}"] = {"us": round(t * 1e6, 3), "GB/s": round(wbytes / t / 1e9, 1)}
         del cps, Wp
         torch.cuda.empty_cache()
     return out

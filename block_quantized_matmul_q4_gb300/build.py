@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libqmm.so")
 
 SOURCES = ["api.cu", "quantize.cu", "repack.cu", "gemv.cu", "debug.cu", "static_scratch.cu", "tmap.cu",
-           "w4a16.cu", "gemm_f16.cu", "gemv_mma.cu", "streamk.cu", "peaks.cu"]
+           "w4a16.cu", "gemm_f16.cu", "gemv_mma.cu", "gemv_mma6.cu", "streamk.cu", "peaks.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
                  "-I", CSRC, "--expt-relaxed-constexpr"]

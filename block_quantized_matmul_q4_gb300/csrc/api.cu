@@ -132,7 +132,8 @@ void prepare_pool(cudaStream_t s) {
 // on the mma.sync kernel and its activation images, otherwise the scalar
 // GEMV and the planar layout.
 bool use_gemm(qmm_type wt, int64_t M) {
-    return M >= (wt == QMM_TYPE_Q4_K ? kGemmMinM : kGemmMinMScalar);
+    (void)wt;
+    return M >= kGemmMinM;
 }
 
 // Prefill workspaces: the quantized activations with their per-token scales
@@ -144,7 +145,7 @@ size_t prefill_act_bytes(qmm_type wt, int64_t M, int64_t K) {
 }
 
 size_t ws_bytes_for(qmm_type wt, int64_t M, int64_t K) {
-    if (!use_gemm(wt, M) && gemv_use_mma(wt, M, K)) return gemv_mma_image_bytes(M, K);
+    if (!use_gemm(wt, M) && gemv_use_mma(wt, M, K)) return mma_image_bytes(wt, M, K);
     if (!use_gemm(wt, M)) return planar_bytes(M, K, elems(wt), nullptr, nullptr);
     return prefill_act_bytes(wt, M, K) + stream_k_part_bytes();
 }
@@ -174,7 +175,7 @@ qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K,
         const size_t need = ws_bytes_for(wt, M, K);
         if (ws_bytes < need)
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
-        return cuda_status(launch_quantize_mma_image(X, ws, M, K, s), "activation quantizer launch");
+        return cuda_status(launch_mma_image(wt, false, X, ws, M, K, s), "activation quantizer launch");
     }
     Planar p;
     qmm_status st = carve(wt, M, K, ws, ws_bytes, &p);
@@ -201,7 +202,7 @@ qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, cons
         const size_t need = ws_bytes_for(wt, M, K);
         if (ws_bytes < need)
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
-        return cuda_status(launch_gemv_mma_q4_K(single_mat(Wp, N, Y), K, nullptr, ws, M, /*pdl=*/true, s),
+        return cuda_status(launch_gemv_mma(wt, single_mat(Wp, N, Y), K, ws, M, /*pdl=*/true, s),
                            "mul_mat kernel launch");
     }
     Planar p;
@@ -456,7 +457,7 @@ qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t 
             e = launch_import_q8_K_f16(Xq, ws, M, K, s);
         }
     } else if (gemv_use_mma(wt, M, K)) {
-        e = launch_import_mma_image(Xq, ws, M, K, s);
+        e = launch_mma_image(wt, true, Xq, ws, M, K, s);
     } else {
         Planar p;
         planar_bytes(M, K, elems(wt), &p, (uint8_t *)ws);
@@ -507,7 +508,7 @@ qmm_status qmm_mul_mat_multi(qmm_type wt, int n, const void *const *W_packed, co
             for (int i = 0; i < ms.n && st == QMM_OK; ++i)
                 st = prepared_impl(wt, ms.W[i], ms.N[i], K, ws, need, M, ms.Y[i], ws_part(wt, M, K, ws), s);
         } else if (gemv_use_mma(wt, M, K)) {
-            st = cuda_status(launch_gemv_mma_q4_K(ms, K, nullptr, ws, M, /*pdl=*/true, s),
+            st = cuda_status(launch_gemv_mma(wt, ms, K, ws, M, /*pdl=*/true, s),
                              "mul_mat kernel launch");
         } else {
             Planar p;

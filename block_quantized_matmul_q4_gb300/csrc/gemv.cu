@@ -711,11 +711,14 @@ uint32_t act_layout(qmm_type wt, int64_t mt, int64_t K, uint32_t *bs_off, uint32
 }  // namespace
 
 bool gemv_use_mma(qmm_type wt, int64_t M, int64_t K) {
-    return wt == QMM_TYPE_Q4_K && M >= kMmaMinM && gemv_mma_max_tokens(K) >= 1;
+    if (M < kMmaMinM) return false;
+    if (wt == QMM_TYPE_Q4_K) return gemv_mma_max_tokens(K) >= 1;
+    return (wt == QMM_TYPE_Q6_K || wt == QMM_TYPE_Q4_0) && gemv_mma6_max_tokens(wt, K) >= 1;
 }
 
 bool gemv_can_fuse(qmm_type wt, int64_t M, int64_t K) {
-    if (gemv_use_mma(wt, M, K)) return M * K <= kMmaFuseElems;
+    // only the Q4_K tensor-core GEMV has its quantizer inside
+    if (gemv_use_mma(wt, M, K)) return wt == QMM_TYPE_Q4_K && M * K <= kMmaFuseElems;
     const int64_t mt = min64(M, kMaxMT);
     return act_layout(wt, mt, K, nullptr, nullptr) <= (uint32_t)kActMax && mt * K <= kFuseMaxElems;
 }

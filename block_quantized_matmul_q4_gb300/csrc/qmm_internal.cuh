@@ -97,13 +97,11 @@ __host__ __device__ __forceinline__ int mat_of(const MatSet &s, int64_t unit) {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Tokens per call from which mul_mat runs the tensor-core GEMM: Q4_K keeps
-// its tensor-core GEMV up to 16 tokens; Q4_0 and Q6_K, whose decode GEMV is
-// scalar, switch where that GEMV moves to its 16-token form (4096 x 4096,
-// measured: the split-K GEMM takes 20-22 us from 4 to 16 tokens, the scalar
-// GEMV 9-11 us at 4, 18-24 at 8, 30-42 at 16).
+// Tokens per call from which mul_mat runs the tensor-core GEMM; below, every
+// format has a tensor-core GEMV from 2 tokens on (4096 x 4096, measured: the
+// Q4_0 / Q6_K GEMVs take 10.8 / 11.0 us at 12 tokens and 11.7 / 12.2 at 16,
+// the split-K GEMM 18.9 / 21.6 and 16.8 / 18.2).
 constexpr int64_t kGemmMinM = 17;
-constexpr int64_t kGemmMinMScalar = 9;
 
 // Workspace carve-up for M rows of K activations with block size qk.
 __host__ __device__ inline size_t planar_bytes(int64_t M, int64_t K, int qk, Planar *p,
@@ -475,6 +473,23 @@ cudaError_t launch_quantize_mma_image(const float *X, void *img, int64_t M, int6
                                       cudaStream_t s);
 cudaError_t launch_gemv_mma_q4_K(MatSet ms, int64_t K, const float *X, const void *img, int64_t M,
                                  bool pdl, cudaStream_t s);
+// Tensor-core decode GEMV for Q6_K and Q4_0 (gemv_mma6.cu), from kMmaMinM
+// tokens on where K is a multiple of 256 and one token's activations fit its
+// shared memory; its activations are always an image written ahead of it.
+int gemv_mma6_max_tokens(qmm_type wt, int64_t K);
+size_t gemv_mma6_image_bytes(qmm_type wt, int64_t M, int64_t K);
+cudaError_t launch_image6(qmm_type wt, bool import, const void *src, void *img, int64_t M, int64_t K,
+                          cudaStream_t s);
+cudaError_t launch_gemv_mma6(qmm_type wt, MatSet ms, int64_t K, const void *img, int64_t M, bool pdl,
+                             cudaStream_t s);
+// The tensor-core decode path of any format (gemv_use_mma): the image bytes
+// for M tokens; the image from fp32 X (import = false) or from canonical Q8
+// blocks (import = true); the GEMV over the image.
+size_t mma_image_bytes(qmm_type wt, int64_t M, int64_t K);
+cudaError_t launch_mma_image(qmm_type wt, bool import, const void *src, void *img, int64_t M, int64_t K,
+                             cudaStream_t s);
+cudaError_t launch_gemv_mma(qmm_type wt, MatSet ms, int64_t K, const void *img, int64_t M, bool pdl,
+                            cudaStream_t s);
 // W4A16: nibble interleave of the packed layout (or its inverse), the decode
 // kernel (M <= 16) and the tensor-core GEMM (M > 16).
 cudaError_t launch_w4a16_repack(bool inverse, const void *src, void *dst, int64_t N, int64_t K,

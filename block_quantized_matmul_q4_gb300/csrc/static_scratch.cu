@@ -72,7 +72,7 @@ extern "C" qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int6
         return set_error(QMM_OK, "");
     }
     const bool mma = gemv_use_mma(wt, M, K);
-    const size_t need = mma ? gemv_mma_image_bytes(M, K) : planar_bytes(M, K, qk, nullptr, nullptr);
+    const size_t need = mma ? mma_image_bytes(wt, M, K) : planar_bytes(M, K, qk, nullptr, nullptr);
     if (need > kStaticScratchBytes)
         return set_error(QMM_ERR_WORKSPACE,
                          "qmm_mul_mat_static: M=%lld x K=%lld needs %zu bytes of scratch, more than "
@@ -84,8 +84,8 @@ extern "C" qmm_status qmm_mul_mat_static(qmm_type wt, const void *W_packed, int6
     // Nothing in the scratch has to start at zero: the quantizer writes every
     // byte the GEMV reads.
     if (mma) {
-        cudaError_t e = launch_quantize_mma_image(X, scratch, M, K, s);
-        if (e == cudaSuccess) e = launch_gemv_mma_q4_K(single_mat(W_packed, N, Y), K, nullptr, scratch, M, true, s);
+        cudaError_t e = launch_mma_image(wt, false, X, scratch, M, K, s);
+        if (e == cudaSuccess) e = launch_gemv_mma(wt, single_mat(W_packed, N, Y), K, scratch, M, true, s);
         if (e != cudaSuccess)
             return set_error(QMM_ERR_CUDA, "mul_mat launch: %s", cudaGetErrorString(e));
         return set_error(QMM_OK, "");

@@ -189,11 +189,12 @@ qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon
  *   Q4_0: sum_b fp16(d_w) fp16(d_a) sum_{i<32} (q_i - 8) y_i
  *   Q4_K: sum_sb d_a (d * sum_j s_j sum_i q_i y_i - dmin * sum_j m_j sum_i y_i)
  *   Q6_K: sum_sb d_a d sum_j s_j sum_i q_i y_i  (16 groups j of 16, no min)
- * Decode (Q4_K up to 16 tokens, Q4_0 and Q6_K up to 8): the GEMV kernels
- * take integer block sums with fp32 accumulation across blocks. When M*K is
- * small (16-token groups of at most 8192 elements) the activation quantizer
- * runs inside the GEMV kernel (one launch per 16 tokens, no workspace), at
- * any M. Otherwise, above those counts (prefill), the tensor-core GEMM
+ * Decode (up to 16 tokens): the GEMV kernels take integer block sums with
+ * fp32 accumulation across blocks (dp4a for one token; from 2 tokens
+ * mma.sync on integer-valued fp16 operands, each block's integer sum exact).
+ * When M*K is small (Q4_0, Q6_K: one token of at most 8192 elements; Q4_K:
+ * 16-token groups of at most 8192 elements) the activation quantizer runs
+ * inside the GEMV kernel (no workspace), at any M. Otherwise, above those counts (prefill), the tensor-core GEMM
  * multiplies fp16 operands with fp32 accumulation: each weight is its exact
  * value rounded once to fp16 (Q4_0 d (q - 8); Q4_K d s_j q - dmin m_j,
  * formed in fp32 first; Q6_K d s_j q) and each activation is 2^e d_a y
@@ -282,18 +283,18 @@ qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, in
  * in cudaMalloc/cudaFree. This call allocates nothing: the quantized
  * activations go to a fixed 4 MiB device array inside libqmm (reserved on
  * every GPU that loads the library, until the process exits), then a decode
- * GEMV runs on them: the kernels qmm_mul_mat runs up to 16 tokens (8 for Q4_0
- * and Q6_K). Above that it does not switch to the prefill GEMM (whose
+ * GEMV runs on them: the kernels qmm_mul_mat runs up to 16 tokens. Above
+ * that it does not switch to the prefill GEMM (whose
  * operands and stream-K area would not fit): it runs the GEMV in launches of
  * up to 16 tokens, each of which reads the weights again. The caller still
  * owns and passes X, W_packed and Y (same layouts, alignment and errors as
  * qmm_mul_mat).
- *   - Limit: the activations of the whole call must fit the 4 MiB. Q4_K from
- *     2 tokens on stores them as the tensor-core GEMV's images (about 2.1
- *     bytes per element of X: M*K up to about 1.9 million); Q4_0, Q6_K and
- *     one Q4_K token as Q8 codes with their scales and sums (about 1.14 to
- *     1.19 bytes per element: M*K up to about 3.5 million). Calls small
- *     enough for the decode kernel's fused quantizer use no scratch at all.
+ *   - Limit: the activations of the whole call must fit the 4 MiB. From 2
+ *     tokens on they are the tensor-core GEMV's images (about 2.0 to 2.2
+ *     bytes per element of X: M*K up to about 1.9 million); one token is
+ *     stored as Q8 codes with their scales and sums (about 1.14 to 1.19
+ *     bytes per element: K up to about 3.5 million). Calls small enough for
+ *     the decode kernel's fused quantizer use no scratch at all.
  *     Larger requests return QMM_ERR_WORKSPACE and launch nothing.
  *   - The first call on a device looks up the array's device address (once,
  *     with that device current); make that first call before any stream

@@ -1,7 +1,7 @@
-"""GPU parity of the prefill path (more than 16 tokens for Q4_K, 8 for Q4_0
-and Q6_K): the prefill quantizers and the tcgen05 GEMMs, whose operands are
-the weights rounded once to fp16 and the activations 2^e d_a y rounded once
-to fp16 (a power of two 2^e per token, taken off in the epilogue), through
+"""GPU parity of the prefill path (more than 16 tokens): the prefill
+quantizers and the tcgen05 GEMMs, whose operands are the weights rounded once
+to fp16 and the activations 2^e d_a y rounded once to fp16 (a power of two
+2^e per token, taken off in the epilogue), through
 the C ABI, against the oracle.
 Bar: |Y_gpu - Y_fp64| <= 1e-3 * sum_k |w_k a_k| per element, no absolute
 slack (an output whose sum is 0 must be exactly 0)."""
