@@ -9,13 +9,15 @@
 //   y   += d_a (d isum).
 // One m16n8k16 step is one group: A holds q (|q| <= 32, exact in fp16), B the
 // Q8_K codes (exact), so the step's fp32 result is S_j exactly (|S_j| <=
-// 16 * 32 * 127 < 2^24); it is converted to an integer and s_j S_j is added
-// in int32, as the scalar kernels do.
+// 16 * 32 * 127 < 2^24), and so is s_j S_j (< 2^23 in magnitude); isum is
+// their fp32 sum, exact while it stays below 2^24 in magnitude, which only
+// a super-block with most of its products near their bounds reaches. (No
+// float-to-integer conversions: they run on the narrow conversion pipe.)
 //
 // Q4_0 x Q8_0 (page 1, "最基础的两块"): per block of 32 and (row, token)
 //   isum = sum_k (q_k - 8) y_k,   y += d_a (d isum).
 // Two steps are one block: A holds q - 8 (exact), B the codes; the block sum
-// (|isum| <= 32 * 8 * 127) is exact in fp32 and converted to an integer.
+// (|isum| <= 32 * 8 * 127) is exact in fp32.
 //
 // Against the scalar dp4a GEMVs, one set of weight conversions serves all the
 // tokens of a launch, so the cost per weight hardly grows with M.
@@ -130,6 +132,13 @@ __device__ __forceinline__ void q40_pairs(uint32_t w, uint32_t &l02, uint32_t &l
     l13 = h2sub(lop_mask_or(v, 0x000F000Fu), kH1032);
     h02 = h2fma(lop_mask_or(w, 0x00F000F0u), kH16th, kHNeg72);
     h13 = h2fma(lop_mask_or(v, 0x00F000F0u), kH16th, kHNeg72);
+}
+
+// The signed byte k of x as a float, exactly, without a conversion
+// instruction: 2^23 + (byte + 128) less 2^23 + 128.
+__device__ __forceinline__ float sbyte_f(uint32_t x, int k) {
+    const uint32_t b = ((x >> (8 * k)) & 0xFFu) ^ 0x80u;
+    return __int_as_float(0x4B000000 | (int)b) - 8388736.0f;
 }
 
 __device__ __forceinline__ void wait_or_skip6(uint32_t bar, uint32_t parity, unsigned *err, volatile int *abort_flag) {
@@ -271,11 +280,11 @@ __global__ void __launch_bounds__(kThreads6, NT == 1 ? 2 : 1) gemv_mma6_kernel(c
                 const float dA = __half2float(*reinterpret_cast<const __half *>(recA + kQ6DOff + 2 * g));
                 const float dB = __half2float(*reinterpret_cast<const __half *>(recB + kQ6DOff + 2 * g));
                 __syncwarp();
-                int isum[NT][4];
+                float isum[NT][4];
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) isum[n][e] = 0;
+                    for (int e = 0; e < 4; ++e) isum[n][e] = 0.0f;
 #pragma unroll
                 for (int tq = 0; tq < 8; ++tq) {
                     const uint32_t qa = *reinterpret_cast<const uint32_t *>(rowA + 16 * tq + 4 * t);
@@ -290,8 +299,7 @@ __global__ void __launch_bounds__(kThreads6, NT == 1 ? 2 : 1) gemv_mma6_kernel(c
                         uint32_t a02, a13, b02, b13;
                         q6_pair(h ? qa >> 4 : qa, h ? ha.y : ha.x, t, a02, a13);
                         q6_pair(h ? qb >> 4 : qb, h ? hb.y : hb.x, t, b02, b13);
-                        const int sA = (int)(int8_t)(uint8_t)(sa >> (8 * (q & 3)));
-                        const int sB = (int)(int8_t)(uint8_t)(sbv >> (8 * (q & 3)));
+                        const float sA = sbyte_f(sa, q & 3), sB = sbyte_f(sbv, q & 3);
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {
                             uint2 y = make_uint2(0u, 0u);
@@ -299,10 +307,10 @@ __global__ void __launch_bounds__(kThreads6, NT == 1 ? 2 : 1) gemv_mma6_kernel(c
                             float c[4];
                             mma16816(c, a02, b02, a13, b13, y.x, y.y, true);
                             // C: e = 0, 1 row g (tile A), tokens 2t, 2t + 1; e = 2, 3 row g + 8
-                            isum[n][0] += sA * (int)c[0];
-                            isum[n][1] += sA * (int)c[1];
-                            isum[n][2] += sB * (int)c[2];
-                            isum[n][3] += sB * (int)c[3];
+                            isum[n][0] = fmaf(sA, c[0], isum[n][0]);
+                            isum[n][1] = fmaf(sA, c[1], isum[n][1]);
+                            isum[n][2] = fmaf(sB, c[2], isum[n][2]);
+                            isum[n][3] = fmaf(sB, c[3], isum[n][3]);
                         }
                     }
                 }
@@ -311,10 +319,10 @@ __global__ void __launch_bounds__(kThreads6, NT == 1 ? 2 : 1) gemv_mma6_kernel(c
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
                     const float2 da = *reinterpret_cast<const float2 *>(dsl + j * nt + n * 8 + 2 * t);
-                    acc[n][0] += da.x * (dA * (float)isum[n][0]);
-                    acc[n][1] += da.y * (dA * (float)isum[n][1]);
-                    acc[n][2] += da.x * (dB * (float)isum[n][2]);
-                    acc[n][3] += da.y * (dB * (float)isum[n][3]);
+                    acc[n][0] += da.x * (dA * isum[n][0]);
+                    acc[n][1] += da.y * (dA * isum[n][1]);
+                    acc[n][2] += da.x * (dB * isum[n][2]);
+                    acc[n][3] += da.y * (dB * isum[n][3]);
                 }
             } else {
                 const uint8_t *nibA = st + g * kRow40 + warp * 8 * 16 + 4 * t;
@@ -348,10 +356,10 @@ __global__ void __launch_bounds__(kThreads6, NT == 1 ? 2 : 1) gemv_mma6_kernel(c
                         mma16816(c, al02, bl02, al13, bl13, y0.x, y0.y, true);
                         mma16816(c, ah02, bh02, ah13, bh13, y1.x, y1.y, false);
                         const float2 da = *reinterpret_cast<const float2 *>(dsl + (j * 8 + b) * nt + n * 8 + 2 * t);
-                        acc[n][0] += da.x * (dA[b] * (float)(int)c[0]);
-                        acc[n][1] += da.y * (dA[b] * (float)(int)c[1]);
-                        acc[n][2] += da.x * (dB[b] * (float)(int)c[2]);
-                        acc[n][3] += da.y * (dB[b] * (float)(int)c[3]);
+                        acc[n][0] += da.x * (dA[b] * c[0]);
+                        acc[n][1] += da.y * (dA[b] * c[1]);
+                        acc[n][2] += da.x * (dB[b] * c[2]);
+                        acc[n][3] += da.y * (dB[b] * c[3]);
                     }
                 }
             }
@@ -454,54 +462,62 @@ __device__ __forceinline__ void put_unit(uint8_t *img, int64_t nu, int mc, int m
     }
 }
 
-// The image of each launch of `per` tokens (the last one holds the rest), from
-// fp32 X: Q8_K per super-block (Q6_K) or Q8_0 per 32 (Q4_0), the codes and
+// Q6_K's image of each launch of `per` tokens (the last one holds the
+// rest) from fp32 X, one warp per (token, super-block): the Q8_K codes and
 // scales of the planar quantizer bit for bit.
-template <int F>
-__global__ void __launch_bounds__(256) quantize_image6_kernel(const float *X, uint8_t *img, int64_t M, int64_t nu,
-                                                              int per) {
+__global__ void __launch_bounds__(256) quantize_image6k_kernel(const float *X, uint8_t *img, int64_t M, int64_t nu,
+                                                               int per) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (threadIdx.x == 0) pdl_launch_dependents();
     if (gw >= M * nu) return;
     pdl_wait();
-    const int64_t m = gw / nu, u = gw % nu, K = nu * 256;
+    const int64_t m = gw / nu, u = gw % nu;
     const int64_t launch = m / per;
     const int ml = (int)(m - launch * per);
     const int mc = (int)(M - launch * per < per ? M - launch * per : per);
-    uint8_t *base = img + (size_t)launch * kWarps6 * layout6(F, nu, per).warp_bytes;
-    const float *x = X + m * K + u * 256;
-    int q[8];
+    uint8_t *base = img + (size_t)launch * kWarps6 * layout6(kF6K, nu, per).warp_bytes;
+    const float4 *x = reinterpret_cast<const float4 *>(X + m * nu * 256 + u * 256 + 8 * lane);
+    const float4 v0 = __ldg(x), v1 = __ldg(x + 1);
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t lo, hi;
+    int bsum, q[8];
     float d;
-    if (F == kF6K) {
-        const float4 v0 = __ldg(reinterpret_cast<const float4 *>(x + 8 * lane));
-        const float4 v1 = __ldg(reinterpret_cast<const float4 *>(x + 8 * lane) + 1);
-        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        uint32_t lo, hi;
-        int bsum;
-        q8_K_warp(v, lo, hi, d, bsum);
+    q8_K_warp(v, lo, hi, d, bsum);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) q[k] = (int)(int8_t)(uint8_t)((k < 4 ? lo : hi) >> (8 * (k & 3)));
-    } else {
-        // eight Q8_0 blocks, one per pass, one element per lane; lane l keeps
-        // elements 8l .. 8l+7 (block l / 4) for the image
-        float dl = 0.0f;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            int c, sum;
-            __half dh;
-            q8_0_warp(x[32 * b + lane], c, dh, sum);
-            // element 32 b + lane belongs to lane 4 b + lane / 8, slot lane % 8
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int v = __shfl_sync(0xffffffffu, c, ((lane & 3) << 3) + k);
-                if ((lane >> 2) == b) q[k] = v;
-            }
-            if ((lane >> 2) == b) dl = __half2float(dh);
-        }
-        d = dl;
-    }
-    put_unit<F>(base, nu, mc, ml, u, lane, q, &d);
+    for (int k = 0; k < 8; ++k) q[k] = (int)(int8_t)(uint8_t)((k < 4 ? lo : hi) >> (8 * (k & 3)));
+    put_unit<kF6K>(base, nu, mc, ml, u, lane, q, &d);
+}
+
+// Q4_0's image from fp32 X with one warp per (token, block of 32): one
+// Q8_0 pass per warp (element = lane), so the quantizer's critical path is
+// one block long.
+__global__ void __launch_bounds__(256) quantize_image40_kernel(const float *X, uint8_t *img, int64_t M, int64_t nu,
+                                                               int per) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nb = nu * 8;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    if (gw >= M * nb) return;
+    pdl_wait();
+    const int64_t m = gw / nb, blk = gw % nb, u = blk / 8;
+    const int b = (int)(blk % 8);
+    const int64_t launch = m / per;
+    const int ml = (int)(m - launch * per);
+    const int mc = (int)(M - launch * per < per ? M - launch * per : per);
+    const Layout6 L = layout6(kF40, nu, mc);
+    uint8_t *area = img + (size_t)launch * kWarps6 * layout6(kF40, nu, per).warp_bytes +
+                    (size_t)(u % kWarps6) * L.warp_bytes;
+    const int64_t j = u / kWarps6;
+    int c, sum;
+    __half dh;
+    q8_0_warp(X[m * nu * 256 + blk * 32 + lane], c, dh, sum);
+    const int step = 2 * b + (lane >> 4);
+    *reinterpret_cast<__half *>(area + ((j * kSteps6 + step) * mc + ml) * kSlot6 + slot_elem(lane & 15)) =
+        __int2half_rn(c);
+    float *dsl = reinterpret_cast<float *>(area + L.d_off) + (j * 8 + b) * L.nt;
+    if (lane == 0) dsl[ml] = __half2float(dh);
+    if (ml == 0 && lane >= mc && lane < L.nt) dsl[lane] = 0.0f;  // padding tokens
 }
 
 // The same image from canonical blocks (qmm_mul_mat_q8): Q8_K [M][nu] x 292 B
@@ -599,7 +615,9 @@ cudaError_t launch_image6(qmm_type wt, bool import, const void *src, void *img, 
     if (per == 0) return cudaErrorInvalidValue;
     const int64_t nu = K / 256;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((M * nu + 7) / 8));
+    // one warp per (token, unit), or per (token, block) for Q4_0 from fp32
+    const bool per_block = !import && wt == QMM_TYPE_Q4_0;
+    cfg.gridDim = dim3((unsigned)((M * nu * (per_block ? 8 : 1) + 7) / 8));
     cfg.blockDim = dim3(256);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -615,8 +633,8 @@ cudaError_t launch_image6(qmm_type wt, bool import, const void *src, void *img, 
                 : cudaLaunchKernelEx(&cfg, import_image6_kernel<kF40>, static_cast<const uint8_t *>(src), out, M, nu, per);
     else
         e = wt == QMM_TYPE_Q6_K
-                ? cudaLaunchKernelEx(&cfg, quantize_image6_kernel<kF6K>, static_cast<const float *>(src), out, M, nu, per)
-                : cudaLaunchKernelEx(&cfg, quantize_image6_kernel<kF40>, static_cast<const float *>(src), out, M, nu, per);
+                ? cudaLaunchKernelEx(&cfg, quantize_image6k_kernel, static_cast<const float *>(src), out, M, nu, per)
+                : cudaLaunchKernelEx(&cfg, quantize_image40_kernel, static_cast<const float *>(src), out, M, nu, per);
     count_launch();
     return e;
 }
