@@ -70,9 +70,10 @@ def test_prefill_full_size_sampled(q, orc, shape, M):
     q.qmm_quantize_weights(q.QMM_TYPE_Q4_K, w, Wq, L.N, L.K)
     Wp = q.empty_packed(q.QMM_TYPE_Q4_K, L.N, L.K)
     q.qmm_repack_weights(q.QMM_TYPE_Q4_K, Wq, Wp, L.N, L.K)
-    Y = torch.empty(M, L.N, device="cuda")
+    Y = torch.full((M, L.N), float("nan"), device="cuda")
     q.qmm_mul_mat(q.QMM_TYPE_Q4_K, Wp, L.N, L.K, x, M, Y)
     q.qmm_check_device_error()
+    assert bool(torch.isfinite(Y).all()), "non-finite (or unwritten) outputs"
     rows = np.unique(np.r_[0:3, 127:130, L.N - 3:L.N, np.linspace(0, L.N - 1, 24).astype(np.int64)])
     w_rows = w[torch.as_tensor(rows, device="cuda")].cpu().numpy()
     Wc_rows = orc.quantize(q.QMM_TYPE_Q4_K, w_rows)
@@ -106,19 +107,21 @@ def test_prefill_q4_0_small(q, orc, N, K, M):
 
 
 @pytest.mark.parametrize("shape", wl.PREFILL_SHAPES, ids=lambda L: L.name)
-def test_prefill_q4_0_full_size_sampled(q, orc, shape):
-    """Q4_0 prefill at full size, M = 512: weights quantized on the GPU,
-    sampled rows checked against the oracle."""
-    L, M, wt = shape, 512, q.QMM_TYPE_Q4_0
+@pytest.mark.parametrize("M", wl.PREFILL_M)
+def test_prefill_q4_0_full_size_sampled(q, orc, shape, M):
+    """Q4_0 prefill at full size (M in {512, 2048}): weights quantized on the
+    GPU, every output finite, sampled rows checked against the oracle."""
+    L, wt = shape, q.QMM_TYPE_Q4_0
     w = wl.weights(33, L.N, L.K, L.wstd, device="cuda")
     x = wl.activations(33, M, L.K, device="cuda")
     Wq = q.empty_blocks(wt, L.N, L.K)
     q.qmm_quantize_weights(wt, w, Wq, L.N, L.K)
     Wp = q.empty_packed(wt, L.N, L.K)
     q.qmm_repack_weights(wt, Wq, Wp, L.N, L.K)
-    Y = torch.empty(M, L.N, device="cuda")
+    Y = torch.full((M, L.N), float("nan"), device="cuda")
     q.qmm_mul_mat(wt, Wp, L.N, L.K, x, M, Y)
     q.qmm_check_device_error()
+    assert bool(torch.isfinite(Y).all()), "non-finite (or unwritten) outputs"
     rows = np.unique(np.r_[0:3, 127:130, L.N - 3:L.N, np.linspace(0, L.N - 1, 24).astype(np.int64)])
     Wc_rows = Wq.view(L.N, -1)[torch.as_tensor(rows, device="cuda")].cpu().numpy()
     ref = orc.mul_mat(wt, Wc_rows, len(rows), L.K, x.cpu().numpy(), nthreads=orc.default_threads())
