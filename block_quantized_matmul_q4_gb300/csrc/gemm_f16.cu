@@ -904,7 +904,7 @@ __global__ void __launch_bounds__(kActThreads) quantize_q4_0_prefill_kernel(cons
         const float d = __fdiv_rn(__uint_as_float(ab), 127.0f);
         const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
         const float sd = __fmul_rn(__half2float(__float2half_rn(d)), p2);  // exact
-        auto val = [&](float xv) { return __float2half_rn(__fmul_rn(sd, (float)q8_code(xv, id))); };
+        auto val = [&](float xv) { return __float2half_rn(__fmul_rn(sd, int_as_exact_float(q8_code(xv, id)))); };
         if (live) {
             __half *dst = out + (m * nb + b) * QK4_0;
             const __half2 p0 = __halves2half2(val(v0.x), val(v0.z)), p1 = __halves2half2(val(v0.y), val(v0.w));
@@ -971,9 +971,8 @@ __global__ void __launch_bounds__(kActThreads) quantize_q8_K_f16_kernel(const fl
         uint32_t h[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const __half lo = __float2half_rn(__fmul_rn(sd, (float)q8_code(v[2 * i], id)));
-            const __half hi = __float2half_rn(__fmul_rn(sd, (float)q8_code(v[2 * i + 1], id)));
-            h[i] = h2_bits(__halves2half2(lo, hi));
+            h[i] = h2_bits(__floats2half2_rn(__fmul_rn(sd, int_as_exact_float(q8_code(v[2 * i], id))),
+                                             __fmul_rn(sd, int_as_exact_float(q8_code(v[2 * i + 1], id)))));
         }
         *reinterpret_cast<uint4 *>(out + (m * nsb + b) * QK_K + 8 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
     }

@@ -563,28 +563,43 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q4_0_kernel(const GemvArgs a
     if (kMode == kFused) {
         pdl_wait();
         uint8_t *aw = smem + kRingBytes;
-        // blocks b = warp + 8 j of all the tokens' rows (b * QK4_0 is the
-        // element offset): up to kQBatch per warp, loads issued first
-        constexpr int kQBatch = 8;
+        // groups of eight blocks, four lanes per block (b * QK4_0 is the
+        // element offset over all the tokens' rows): group g0 + 8 j of warp
+        // g0, up to kQBatch per warp with their loads issued first; lanes
+        // past the last block take zeros and store nothing
+        constexpr int kQBatch = 2;
         const int nq = (int)(mc * nb);
-        for (int b0 = warp; b0 < nq; b0 += kQBatch * kConsumerWarps) {
-            float xv[kQBatch];
+        const int bl = lane >> 2, part = lane & 3;
+        for (int g0 = warp * 8; g0 < nq; g0 += kQBatch * kConsumerWarps * 8) {
+            float4 v[kQBatch][2];
 #pragma unroll
             for (int j = 0; j < kQBatch; ++j) {
-                const int b = b0 + j * kConsumerWarps;
-                if (b < nq) xv[j] = __ldg(a.X + a.m0 * K + (int64_t)b * QK4_0 + lane);
+                const int b = g0 + j * kConsumerWarps * 8 + bl;
+                v[j][0] = v[j][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (b < nq) {
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(a.X + a.m0 * K + (int64_t)b * QK4_0 + 8 * part);
+                    v[j][0] = __ldg(src);
+                    v[j][1] = __ldg(src + 1);
+                }
             }
 #pragma unroll
             for (int j = 0; j < kQBatch; ++j) {
-                const int b = b0 + j * kConsumerWarps;
-                if (b < nq) {
-                    int q, sum;
+                const int gb = g0 + j * kConsumerWarps * 8;
+                if (gb < nq) {  // warp-uniform: the shuffles need every lane
+                    const int b = gb + bl;
+                    const float x[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w,
+                                        v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
+                    uint32_t lo, hi;
+                    int sum;
                     __half dh;
-                    q8_0_warp(xv[j], q, dh, sum);
-                    aw[(int64_t)b * QK4_0 + lane] = (uint8_t)(int8_t)q;
-                    if (lane == 0) {
-                        reinterpret_cast<int16_t *>(aw + a.act_bs)[b] = (int16_t)sum;
-                        reinterpret_cast<float *>(aw + a.act_d)[b] = __half2float(dh);
+                    q8_0_quad(x, lo, hi, dh, sum);
+                    if (b < nq) {
+                        *reinterpret_cast<uint2 *>(aw + (int64_t)b * QK4_0 + 8 * part) = make_uint2(lo, hi);
+                        if (part == 0) {
+                            reinterpret_cast<int16_t *>(aw + a.act_bs)[b] = (int16_t)sum;
+                            reinterpret_cast<float *>(aw + a.act_d)[b] = __half2float(dh);
+                        }
                     }
                 }
             }

@@ -139,8 +139,8 @@ __device__ __forceinline__ void put_sb(uint8_t *codes, uint8_t *sums, float *dsl
 
 // Q8_K quantization of 8 values per lane (page 1, "第一步: 激活得先变成
 // Q8_K"): d = amax / 127, codes round-half-away(x / d) clamped to +-127 --
-// the arithmetic of q8_K_warp, keeping the codes as floats so that they pack
-// straight into fp16 pairs (exact: integers of magnitude <= 127).
+// the arithmetic of q8_K_warp -- packed into fp16 pairs (exact: integers of
+// magnitude <= 127) and the 16-code sums as fp32, all without conversions.
 __device__ __forceinline__ void quant_sb(const float v[8], uint32_t h[4], float &bsum, float &d) {
     float a = 0.0f;
 #pragma unroll
@@ -148,17 +148,22 @@ __device__ __forceinline__ void quant_sb(const float v[8], uint32_t h[4], float 
     const float amax = warp_max_nonneg(a);
     d = __fdiv_rn(amax, 127.0f);
     const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
-    float q[8], s = 0.0f;
+    int q[8], s = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        q[i] = fminf(fmaxf(round_half_away(__fmul_rn(v[i], id)), -127.0f), 127.0f);
-        s = __fadd_rn(s, q[i]);  // exact: integers below 2^11
+        q[i] = q8_code(v[i], id);
+        s += q[i];
     }
-    bsum = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));
-    h[0] = half2_bits(q[0], q[2]);
-    h[1] = half2_bits(q[1], q[3]);
-    h[2] = half2_bits(q[4], q[6]);
-    h[3] = half2_bits(q[5], q[7]);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    bsum = int_as_exact_float(s);
+    // fp16 pairs of the codes: (1152 + q) as bits, then 1152 taken off (exact)
+    auto pair = [&](int x, int y) {
+        return hsub2_u(biased_half_bits(x) | (biased_half_bits(y) << 16), 0x64806480u);
+    };
+    h[0] = pair(q[0], q[2]);
+    h[1] = pair(q[1], q[3]);
+    h[2] = pair(q[4], q[6]);
+    h[3] = pair(q[5], q[7]);
 }
 
 // Scale operands of one row for lane column t: field f = s_2t | m_2t << 6 |

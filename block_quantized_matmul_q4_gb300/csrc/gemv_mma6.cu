@@ -435,6 +435,11 @@ __device__ __forceinline__ void image_pos(int e, int &step, int &i) {
     }
 }
 
+// A Q8 code (|q| <= 127) as fp16 without a conversion instruction.
+__device__ __forceinline__ __half code_half(int q) {
+    return __hsub(__ushort_as_half((unsigned short)biased_half_bits(q)), __ushort_as_half((unsigned short)0x6480));
+}
+
 // One warp per (token, unit): the unit's 256 codes (8 per lane, elements 8l
 // .. 8l+7) and scales into the launch's image.
 template <int F>
@@ -448,7 +453,7 @@ __device__ __forceinline__ void put_unit(uint8_t *img, int64_t nu, int mc, int m
         int step, i;
         image_pos<F>(8 * lane + k, step, i);
         *reinterpret_cast<__half *>(area + ((j * kSteps6 + step) * mc + ml) * kSlot6 + slot_elem(i)) =
-            __int2half_rn(q[k]);
+            code_half(q[k]);
     }
     float *dsl = reinterpret_cast<float *>(area + L.d_off);
     if (F == kF6K) {
@@ -514,7 +519,7 @@ __global__ void __launch_bounds__(256) quantize_image40_kernel(const float *X, u
     q8_0_warp(X[m * nu * 256 + blk * 32 + lane], c, dh, sum);
     const int step = 2 * b + (lane >> 4);
     *reinterpret_cast<__half *>(area + ((j * kSteps6 + step) * mc + ml) * kSlot6 + slot_elem(lane & 15)) =
-        __int2half_rn(c);
+        code_half(c);
     float *dsl = reinterpret_cast<float *>(area + L.d_off) + (j * 8 + b) * L.nt;
     if (lane == 0) dsl[ml] = __half2float(dh);
     if (ml == 0 && lane >= mc && lane < L.nt) dsl[lane] = 0.0f;  // padding tokens

@@ -318,6 +318,36 @@ __device__ __forceinline__ float round_half_away(float v) {
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return min(max(v, lo), hi); }
 
+// floor(a + 0.5) for 0 <= a < 2^22 without a float-to-integer conversion
+// (those run on the narrow conversion pipe): a + 0.5 rounded to nearest, then
+// 2^23 added with rounding toward zero leaves the integer part in the low
+// mantissa bits. The same value as round_half_away's floor for such a.
+__device__ __forceinline__ int floor_half_up(float a) {
+    return __float_as_int(__fadd_rz(__fadd_rn(a, 0.5f), 8388608.0f)) - 0x4B000000;
+}
+
+// n with the sign of p (the sign bit as a mask; n = 0 gives 0 for p = -0).
+__device__ __forceinline__ int with_sign_of(int n, float p) {
+    const int s = __float_as_int(p) >> 31;
+    return (n ^ s) - s;
+}
+
+// (int)round_half_away(p) for |p| < 2^22.
+__device__ __forceinline__ int round_half_away_int(float p) {
+    return with_sign_of(floor_half_up(fabsf(p)), p);
+}
+
+// An integer |v| < 2^22 as fp32 without a conversion: 1.5 * 2^23 + v has v
+// in its low mantissa bits; subtracting 1.5 * 2^23 is exact.
+__device__ __forceinline__ float int_as_exact_float(int v) {
+    return __int_as_float(0x4B400000 + v) - 12582912.0f;
+}
+
+// An integer |v| < 2^10 as fp16 bits without a conversion: 1152 + v lies in
+// [1024, 2048), where fp16 holds every integer, so its bits are 0x6480 + v.
+// Subtracting 1152 (0x6480) in fp16 afterwards is exact.
+__device__ __forceinline__ uint32_t biased_half_bits(int v) { return (uint32_t)(0x6480 + v); }
+
 // ------------------------------------------------------------------ stream-K
 // The tensor-core GEMMs run a grid of G CTAs over units u = tile * nsb +
 // k-round (U units), CTA c taking [c U / G, (c+1) U / G). With at most as
@@ -358,8 +388,11 @@ __device__ __forceinline__ float warp_max_nonneg(float v) {
     return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
 
+// clamp(round_half_away(x id), -127, 127); min(|p|, 255) keeps floor_half_up
+// in range. Equal to the conversion form for every non-NaN p.
 __device__ __forceinline__ int q8_code(float x, float id) {
-    return clampi((int)round_half_away(__fmul_rn(x, id)), -127, 127);
+    const float p = __fmul_rn(x, id);
+    return with_sign_of(min(floor_half_up(fminf(fabsf(p), 255.0f)), 127), p);
 }
 
 // Q8_0 block held one element per lane: code, scale (fp32 value of the fp16
@@ -371,6 +404,32 @@ __device__ __forceinline__ void q8_0_warp(float x, int &q, __half &dh, int &sum)
     q = q8_code(x, id);
     dh = __float2half_rn(d);
     sum = __reduce_add_sync(0xffffffffu, q);
+}
+
+// Q8_0 block held 8 elements per lane by four consecutive lanes (lane l:
+// elements 8 (l % 4) .. 8 (l % 4) + 7 of the warp's block l / 4), so a warp
+// quantizes eight blocks at once: the arithmetic of q8_0_warp, the codes
+// packed little-endian in (lo, hi), the block's code sum on all four lanes.
+__device__ __forceinline__ void q8_0_quad(const float v[8], uint32_t &lo, uint32_t &hi, __half &dh,
+                                          int &sum) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    const float amax = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+    int q[8], s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        q[i] = q8_code(v[i], id);
+        s += q[i];
+    }
+    lo = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
+    hi = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    sum = s + __shfl_xor_sync(0xffffffffu, s, 2);
+    dh = __float2half_rn(d);
 }
 
 // Q8_K super-block held 8 elements per lane (lane l: elements 8l .. 8l+7):
@@ -389,7 +448,7 @@ __device__ __forceinline__ void q8_K_warp(const float v[8], uint32_t &lo, uint32
     int q[8], s = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        q[i] = (int)round_half_away(__fmul_rn(v[i], id));
+        q[i] = round_half_away_int(__fmul_rn(v[i], id));
         s += q[i];
     }
     // low bytes of q[0..3] and q[4..7], little-endian
