@@ -200,7 +200,9 @@ __device__ __forceinline__ float q4k_dot(const uint4 &hdr, const uint4 &q, const
     s1b = dp4a_us(q.w & 0xF0F0F0F0u, y1.w, s1b);
     const int isum = sc0 * (s0 + s0b) + sc1 * ((s1 + s1b) >> 4);
     const int msum = mn0 * (int)(int16_t)(bw & 0xFFFF) + mn1 * (bw >> 16);
-    return da * (dw * (float)isum - dmw * (float)msum);
+    // |isum| <= 2 * 63 * 16 * 15 * 127 and msum <= 2 * 63 * 2032: exact
+    // conversions without the conversion pipe
+    return da * (dw * int_as_exact_float(isum) - dmw * int_as_exact_float(msum));
 }
 
 // The Q8_K quantizer fused into the GEMV prologue (K-quant weights): the
@@ -728,6 +730,10 @@ uint32_t act_layout(qmm_type wt, int64_t mt, int64_t K, uint32_t *bs_off, uint32
 bool gemv_use_mma(qmm_type wt, int64_t M, int64_t K) {
     if (M < kMmaMinM) return false;
     if (wt == QMM_TYPE_Q4_K) return gemv_mma_max_tokens(K) >= 1;
+    // Q6_K at two tokens small enough for the fused quantizer: the one-kernel
+    // dp4a GEMV beats the quantizer kernel plus the tensor-core GEMV (4096^2:
+    // 5.5 against 7.4 us); from three tokens the tensor cores win
+    if (wt == QMM_TYPE_Q6_K && M == 2 && M * K <= kFuseMaxElems) return false;
     return (wt == QMM_TYPE_Q6_K || wt == QMM_TYPE_Q4_0) && gemv_mma6_max_tokens(wt, K) >= 1;
 }
 

@@ -101,9 +101,9 @@ size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K);
 
 /* Bytes of the workspace qmm_mul_mat_ws needs for M activation rows of
  * length K against weights of type wt (Q4_0, Q4_K or Q6_K); 0 if invalid.
- * When the call runs the tensor-core GEMM (Q4_K above 16 tokens, Q4_0 and
- * Q6_K above 8) it ends with a partial area of about 20 MB: with more 128 x
- * 128 output tiles than SMs the GEMM gives each SM an equal share of the
+ * When the call runs the tensor-core GEMM (above 16 tokens, every weight
+ * type) it ends with a partial area of about 20 MB: with more output tiles
+ * than SMs the GEMM gives each SM an equal share of the
  * (tile, K-step) work (stream-K), with fewer than half as many it splits K
  * over the SMs, and the parts of tiles that several CTAs computed meet
  * there before a second kernel adds them. */

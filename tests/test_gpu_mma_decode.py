@@ -65,12 +65,13 @@ def test_mma_decode_shapes(q, orc, wt, N, K, M):
     check(y[:M * N].reshape(M, N), ref["y64"], ref["den"], f"wt={wt} N={N} K={K} M={M}")
 
 
-@pytest.mark.parametrize("wt", [Q6_K, Q4_0])
-@pytest.mark.parametrize("M", [2, 5, 8])
+@pytest.mark.parametrize("wt,M", [(Q6_K, 3), (Q6_K, 5), (Q6_K, 8), (Q4_0, 2), (Q4_0, 5), (Q4_0, 8)])
 def test_mma_decode_block_arithmetic_exact(q, orc, wt, M):
     """Each token's activations nonzero in one block only (Q4_0: block m % 8
     of 8; Q6_K: the one super-block of K = 256): the output is the factored
-    form of that block's integer sum, bit for bit."""
+    form of that block's integer sum, bit for bit. (Q6_K at two tokens and a
+    K this small takes the dp4a GEMV with its fused quantizer, whose lanes
+    add partial products, so its first tensor-core case is three tokens.)"""
     N, K = 40, 256
     w = wl.weights(51, N, K, 0.02, row_offset_std=0.0 if wt == Q4_0 else 0.005).numpy()
     x = wl.activations(51, M, K).numpy()
