@@ -3,8 +3,8 @@ memory (a serving loop with a frozen allocator, a runtime that gives the
 library no allocator, a step that must never block in cudaMalloc). It keeps
 its activation scratch in a fixed array inside libqmm. Through the C ABI,
 several calls in a row share that array, each in a different layout than the
-one before (the tensor-core GEMV's activation images, the Q8_K and Q8_0
-planar codes, a call split into two launches); each result is checked
+one before (the tensor-core GEMVs' activation images, the Q8_K and Q8_0
+planar codes of the one-token GEMV, a call split into two launches); each result is checked
 against the oracle's fp64 result and against qmm_mul_mat's (the existing
 entry point), within the same 1e-3 * sum|w a| bound the other GPU tests use,
 and bit for bit against qmm_mul_mat_ws where that call runs the same
@@ -53,9 +53,11 @@ def test_static_scratch_matches_oracle_and_mul_mat(q, orc):
     Q4_0, Q4_K, Q6_K = q.QMM_TYPE_Q4_0, q.QMM_TYPE_Q4_K, q.QMM_TYPE_Q6_K
     # (type, N, K, M, seed, same kernels as qmm_mul_mat_ws): in call order
     cases = [(Q4_K, 72, 4096, 16, 21, True),    # activation images, one launch
-             (Q4_0, 40, 4096, 3, 22, True),     # Q8_0 planar (above the fused limit)
+             (Q4_0, 40, 4096, 3, 22, True),     # Q4_0 tensor-core image
              (Q4_K, 72, 4096, 20, 23, False),   # images, two launches (16 + 4); mul_mat: GEMM
-             (Q6_K, 40, 2048, 5, 24, True),     # Q8_K planar
+             (Q6_K, 40, 2048, 5, 24, True),     # Q6_K tensor-core image
+             (Q6_K, 40, 16384, 1, 25, True),    # Q8_K planar (one token above the fused limit)
+             (Q4_0, 24, 16384, 1, 26, True),    # Q8_0 planar
              (Q4_K, 72, 4096, 16, 21, True)]    # the first call again, after the others
     outs = []
     for wt, N, K, M, seed, same in cases:
