@@ -128,12 +128,19 @@ void prepare_pool(cudaStream_t s) {
 
 // More than 16 tokens run the fp16-operand tensor-core GEMM on fp16(2^e d_a y)
 // activations with a power of two 2^e per token (Q4_0: 32-blocks, permuted
-// for its converter; Q4_K and Q6_K: Q8_K codes in natural order); fewer the decode GEMVs: Q4_K from 2 tokens
-// on the mma.sync kernel and its activation images, otherwise the scalar
-// GEMV and the planar layout.
-bool use_gemm(qmm_type wt, int64_t M) {
-    (void)wt;
-    return M >= kGemmMinM;
+// for its converter; Q4_K and Q6_K: Q8_K codes in natural order); fewer the
+// decode GEMVs: from 2 tokens the mma.sync kernels and their activation
+// images, otherwise the scalar GEMV and the planar layout. A decode batch
+// whose activation image does not fit one CTA's shared memory (large K) takes
+// several tensor-core GEMV launches, each reading all the weights again; from
+// three such launches (two for Q4_0 and Q6_K) the GEMM, which reads them
+// once, is faster (Q4_K 8192 x 28672, 16 tokens: 255 -> 81 us; Q6_K 8192^2,
+// 12 tokens: 44 -> 32 us; at two Q4_K launches the GEMV is as fast or faster).
+bool use_gemm(qmm_type wt, int64_t M, int64_t K) {
+    if (M >= kGemmMinM) return true;
+    const int per = wt == QMM_TYPE_Q4_K ? gemv_mma_max_tokens(K) : gemv_mma6_max_tokens(wt, K);
+    if (!gemv_use_mma(wt, M, K) || M <= per) return false;
+    return (M + per - 1) / per >= (wt == QMM_TYPE_Q4_K ? 3 : 2);
 }
 
 // Prefill workspaces: the quantized activations with their per-token scales
@@ -145,8 +152,8 @@ size_t prefill_act_bytes(qmm_type wt, int64_t M, int64_t K) {
 }
 
 size_t ws_bytes_for(qmm_type wt, int64_t M, int64_t K) {
-    if (!use_gemm(wt, M) && gemv_use_mma(wt, M, K)) return mma_image_bytes(wt, M, K);
-    if (!use_gemm(wt, M)) return planar_bytes(M, K, elems(wt), nullptr, nullptr);
+    if (!use_gemm(wt, M, K) && gemv_use_mma(wt, M, K)) return mma_image_bytes(wt, M, K);
+    if (!use_gemm(wt, M, K)) return planar_bytes(M, K, elems(wt), nullptr, nullptr);
     return prefill_act_bytes(wt, M, K) + stream_k_part_bytes();
 }
 
@@ -163,7 +170,7 @@ qmm_status carve(qmm_type wt, int64_t M, int64_t K, const void *ws, size_t ws_by
 
 qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K, void *ws,
                               size_t ws_bytes, cudaStream_t s) {
-    if (use_gemm(wt, M)) {
+    if (use_gemm(wt, M, K)) {
         const size_t need = ws_bytes_for(wt, M, K);
         if (ws_bytes < need)
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
@@ -188,7 +195,7 @@ qmm_status quantize_acts_impl(qmm_type wt, const float *X, int64_t M, int64_t K,
 // no other work uses until this call's work on `s` is done.
 qmm_status prepared_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, const void *ws,
                          size_t ws_bytes, int64_t M, float *Y, float *part, cudaStream_t s) {
-    if (use_gemm(wt, M)) {
+    if (use_gemm(wt, M, K)) {
         const size_t need = prefill_act_bytes(wt, M, K);
         if (ws_bytes < need)
             return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
@@ -223,7 +230,7 @@ qmm_status mul_mat_impl(qmm_type wt, const void *Wp, int64_t N, int64_t K, const
     }
     qmm_status st = quantize_acts_impl(wt, X, M, K, ws, ws_bytes, s);
     if (st != QMM_OK) return st;
-    return prepared_impl(wt, Wp, N, K, ws, ws_bytes, M, Y, use_gemm(wt, M) ? ws_part(wt, M, K, ws) : nullptr,
+    return prepared_impl(wt, Wp, N, K, ws, ws_bytes, M, Y, use_gemm(wt, M, K) ? ws_part(wt, M, K, ws) : nullptr,
                          s);
 }
 
@@ -398,7 +405,7 @@ qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, in
     QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(workspace, 16) && aligned(Y, 4),
                   "W_packed and workspace must be 16-byte aligned, Y 4-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
-    if (!use_gemm(wt, M) || !stream_k_splits(wt, N, M, K))  // nothing to allocate
+    if (!use_gemm(wt, M, K) || !stream_k_splits(wt, N, M, K))  // nothing to allocate
         return prepared_impl(wt, W_packed, N, K, workspace, ws_bytes, M, Y, nullptr, s);
     if (ws_bytes < prefill_act_bytes(wt, M, K))  // before allocating anything
         return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes,
@@ -450,7 +457,7 @@ qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t 
         return set_error(QMM_ERR_NOMEM, "cudaMallocAsync(%zu): %s", need, cudaGetErrorString(e));
     }
     // the caller's blocks, rewritten into the layout the kernel for (wt, M, K) reads
-    if (use_gemm(wt, M)) {
+    if (use_gemm(wt, M, K)) {
         if (wt == QMM_TYPE_Q4_0) {
             e = launch_import_q4_0_prefill(Xq, ws, M, K, s);
         } else {
@@ -465,7 +472,7 @@ qmm_status qmm_mul_mat_q8(qmm_type wt, const void *W_packed, int64_t N, int64_t 
     }
     st = cuda_status(e, "activation import launch");
     if (st == QMM_OK)
-        st = prepared_impl(wt, W_packed, N, K, ws, need, M, Y, use_gemm(wt, M) ? ws_part(wt, M, K, ws) : nullptr, s);
+        st = prepared_impl(wt, W_packed, N, K, ws, need, M, Y, use_gemm(wt, M, K) ? ws_part(wt, M, K, ws) : nullptr, s);
     cudaError_t ef = cudaFreeAsync(ws, s);
     if (st == QMM_OK && ef != cudaSuccess) return cuda_status(ef, "cudaFreeAsync");
     return st;
@@ -488,7 +495,7 @@ qmm_status qmm_mul_mat_multi(qmm_type wt, int n, const void *const *W_packed, co
     }
     if (M == 0 || ms.n == 0) return ok();
     cudaStream_t s = (cudaStream_t)stream;
-    if (!use_gemm(wt, M) && gemv_can_fuse(wt, M, K)) {  // one kernel, no workspace
+    if (!use_gemm(wt, M, K) && gemv_can_fuse(wt, M, K)) {  // one kernel, no workspace
         Planar none{nullptr, nullptr, nullptr};
         return cuda_status(launch_gemv(wt, ms, K, none, X, M, /*pdl=*/true, s), "mul_mat kernel launch");
     }
@@ -504,7 +511,7 @@ qmm_status qmm_mul_mat_multi(qmm_type wt, int n, const void *const *W_packed, co
     // stream-K partial area in turn, in stream order
     qmm_status st = quantize_acts_impl(wt, X, M, K, ws, need, s);
     if (st == QMM_OK) {
-        if (use_gemm(wt, M)) {
+        if (use_gemm(wt, M, K)) {
             for (int i = 0; i < ms.n && st == QMM_OK; ++i)
                 st = prepared_impl(wt, ms.W[i], ms.N[i], K, ws, need, M, ms.Y[i], ws_part(wt, M, K, ws), s);
         } else if (gemv_use_mma(wt, M, K)) {

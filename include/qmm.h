@@ -101,8 +101,9 @@ size_t qmm_packed_bytes(qmm_type wt, int64_t N, int64_t K);
 
 /* Bytes of the workspace qmm_mul_mat_ws needs for M activation rows of
  * length K against weights of type wt (Q4_0, Q4_K or Q6_K); 0 if invalid.
- * When the call runs the tensor-core GEMM (above 16 tokens, every weight
- * type) it ends with a partial area of about 20 MB: with more output tiles
+ * When the call runs the tensor-core GEMM (above 16 tokens, or a decode
+ * batch with a K too large for the tensor-core GEMV's single launch, see
+ * qmm_mul_mat) it ends with a partial area of about 20 MB: with more output tiles
  * than SMs the GEMM gives each SM an equal share of the
  * (tile, K-step) work (stream-K), with fewer than half as many it splits K
  * over the SMs, and the parts of tiles that several CTAs computed meet
@@ -190,11 +191,16 @@ qmm_status qmm_unrepack_weights(qmm_type wt, const void *W_packed, void *W_canon
  *   Q4_K: sum_sb d_a (d * sum_j s_j sum_i q_i y_i - dmin * sum_j m_j sum_i y_i)
  *   Q6_K: sum_sb d_a d sum_j s_j sum_i q_i y_i  (16 groups j of 16, no min)
  * Decode (up to 16 tokens): the GEMV kernels take integer block sums with
- * fp32 accumulation across blocks (dp4a for one token; from 2 tokens
- * mma.sync on integer-valued fp16 operands, each block's integer sum exact).
- * When M*K is small (Q4_0, Q6_K: one token of at most 8192 elements; Q4_K:
+ * fp32 accumulation across blocks (dp4a for one token, and for two Q6_K
+ * tokens of at most 8192 elements in all; otherwise from 2 tokens mma.sync
+ * on integer-valued fp16 operands, each block's integer sum exact). When
+ * M*K is small (Q4_0, Q6_K: at most 8192 elements on the dp4a GEMV; Q4_K:
  * 16-token groups of at most 8192 elements) the activation quantizer runs
- * inside the GEMV kernel (no workspace), at any M. Otherwise, above those counts (prefill), the tensor-core GEMM
+ * inside the GEMV kernel (no workspace). The tensor-core GEMV holds all of
+ * a launch's activations in shared memory, so a large K caps its tokens
+ * per launch; a decode batch that would take three or more launches (two
+ * for Q4_0 and Q6_K), each reading the weights again, runs the GEMM below.
+ * Above 16 tokens (prefill), and for those batches, the tensor-core GEMM
  * multiplies fp16 operands with fp32 accumulation: each weight is its exact
  * value rounded once to fp16 (Q4_0 d (q - 8); Q4_K d s_j q - dmin m_j,
  * formed in fp32 first; Q6_K d s_j q) and each activation is 2^e d_a y
@@ -283,8 +289,8 @@ qmm_status qmm_mul_mat_prepared(qmm_type wt, const void *W_packed, int64_t N, in
  * in cudaMalloc/cudaFree. This call allocates nothing: the quantized
  * activations go to a fixed 4 MiB device array inside libqmm (reserved on
  * every GPU that loads the library, until the process exits), then a decode
- * GEMV runs on them: the kernels qmm_mul_mat runs up to 16 tokens. Above
- * that it does not switch to the prefill GEMM (whose
+ * GEMV runs on them (the one qmm_mul_mat runs for up to 16 tokens of a
+ * small K). It never switches to the prefill GEMM (whose
  * operands and stream-K area would not fit): it runs the GEMV in launches of
  * up to 16 tokens, each of which reads the weights again. The caller still
  * owns and passes X, W_packed and Y (same layouts, alignment and errors as
