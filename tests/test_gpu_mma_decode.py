@@ -14,7 +14,7 @@ import workloads as wl
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-3
-Q4_0, Q6_K = 0, 5
+Q4_0, Q4_K, Q6_K = 0, 1, 5
 
 
 @pytest.fixture(scope="module")
@@ -127,3 +127,30 @@ def test_mma_decode_prepared_and_q8(q, orc, wt, N, K, M):
     check(Y1.cpu().numpy(), ref["y64"], ref["den"], f"prepared wt={wt}")
     assert torch.equal(Y1, Y2)
     assert torch.equal(Y1, Y3), "image from canonical Q8 blocks differs"
+
+
+@pytest.mark.parametrize("wt,K,M", [(Q4_K, 28672, 9), (Q4_K, 28672, 16), (Q6_K, 8192, 12), (Q4_0, 8192, 16)])
+def test_large_k_decode_batch(q, orc, wt, K, M):
+    """A decode batch whose K is too large for the tensor-core GEMV to hold
+    it in one or two launches (Q4_K: fewer than three) takes the GEMM; the
+    output is checked against the oracle like any other, through every entry
+    point that dispatches on it (mul_mat, the workspace call, prepared)."""
+    N = 40
+    w = wl.weights(53, N, K, 0.02, row_offset_std=0.0 if wt == Q4_0 else 0.005).numpy()
+    x = wl.activations(53, M, K).numpy()
+    Wc, Wp = packed(q, orc, wt, w, N, K)
+    ref = orc.mul_mat(wt, Wc, N, K, x, nthreads=orc.default_threads())
+    X = dev(x)
+    Y1 = torch.full((M, N), float("nan"), device="cuda")
+    q.qmm_mul_mat(wt, Wp, N, K, X, M, Y1)
+    ws_bytes = q.qmm_workspace_bytes(wt, M, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    Y2 = torch.full((M, N), float("nan"), device="cuda")
+    q.qmm_mul_mat_ws(wt, Wp, N, K, X, M, Y2, ws, ws_bytes)
+    Y3 = torch.full((M, N), float("nan"), device="cuda")
+    q.qmm_quantize_activations(wt, X, M, K, ws, ws_bytes)
+    q.qmm_mul_mat_prepared(wt, Wp, N, K, ws, ws_bytes, M, Y3)
+    q.qmm_check_device_error()
+    for Y, what in ((Y1, "mul_mat"), (Y2, "mul_mat_ws"), (Y3, "prepared")):
+        check(Y.cpu().numpy(), ref["y64"], ref["den"], f"{what} wt={wt} K={K} M={M}")
+    assert torch.equal(Y1, Y2)
