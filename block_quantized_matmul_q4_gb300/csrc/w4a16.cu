@@ -440,6 +440,283 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 1 ? 2 : 1) w4a16_decode_
     }
 }
 
+// K-major decode, for 9..16 tokens whose activations are too large for the
+// staged layout (M K > 8192 elements; 16 tokens of K = 8192 are 256 KB). The kernel above would
+// fetch every step's activation fragments from L2 once per tile, with the
+// load latency on each step's critical path. Here a CTA takes up to
+// kKmTiles of its tiles at a time, 16-step chunk of K by chunk: the
+// producer bulk-copies the chunk of A ([M][2048] fp16, one copy per token
+// into a row skewed by 16 bytes so that the eight tokens a step reads fall
+// in different banks) into one of two shared-memory slots once, and all of
+// those tiles' weight stages of that chunk read it. Each tile keeps its
+// own partial sums (statically indexed), reduced across the consumer warps
+// at the end. Scales and zeros are read from global memory for each (tile,
+// chunk), ahead of the chunk's MMAs -- from shared memory where every row of
+// them is a multiple of 16 bytes (kSzSmem: the producer copies the scales and
+// zeros of a group's tiles into one slot each, as the kernel above does per
+// tile), else from global memory.
+constexpr int kKmTiles = 4;
+constexpr int kKmASlots = 2;
+constexpr int kKmStages = 4;  // weight stages (the A slots take the room of the fifth)
+constexpr uint32_t kKmTokBytes = kStepsPerStage * kStepK * 2 + 16;  // one token's chunk, skewed
+__host__ __device__ inline uint32_t km_slot_bytes(int64_t M) {
+    return (uint32_t)(((uint64_t)M * kKmTokBytes + 127) & ~127ull);
+}
+
+template <bool kLut, bool kSzSmem>
+__global__ void __launch_bounds__(kDecodeThreads, 1) w4a16_decode_kmajor_kernel(const DecodeArgs a) {
+    constexpr int NT = 2;  // 9..16 tokens
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ float red[kDecodeWarps][NT][4][32];
+    __shared__ uint32_t pair_tbl[kLut ? 256 : 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ntiles = (a.N + kRowsPerTile - 1) / kRowsPerTile;
+    const int64_t tb = (int64_t)blockIdx.x * ntiles / gridDim.x;
+    const int64_t te = ((int64_t)blockIdx.x + 1) * ntiles / gridDim.x;
+    const int nsteps = (int)(a.K / kStepK);
+    constexpr int sps = kStepsPerStage, S = kKmStages;
+    const int spt = (nsteps + sps - 1) / sps;  // chunks of K
+    constexpr uint32_t ring_bytes = (uint32_t)S * kDStageBytes;
+    const uint32_t slot_bytes = km_slot_bytes(a.M);
+    const uint32_t a_sm = smem_u32(smem) + ring_bytes;
+    const uint32_t ss = sz_stride_s(a.ng), zs = sz_stride_z(a.ng), sz_bytes = sz_slot_bytes(a.ng, kLut);
+    const uint32_t sz_sm = a_sm + kKmASlots * slot_bytes;  // kKmTiles scale/zero slots (kSzSmem)
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + ring_bytes + kKmASlots * slot_bytes +
+                                                  (kSzSmem ? kKmTiles * sz_bytes : 0u));
+    uint64_t *empty = full + S;
+    uint64_t *afull = empty + S;
+    uint64_t *aempty = afull + kKmASlots;
+    uint64_t *szfull = aempty + kKmASlots;
+    uint64_t *szempty = szfull + kKmTiles;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), kDecodeWarps);
+        }
+        for (int i = 0; i < kKmASlots; ++i) {
+            mbar_init(smem_u32(&afull[i]), 1);
+            mbar_init(smem_u32(&aempty[i]), kDecodeWarps);
+        }
+        for (int i = 0; i < kKmTiles; ++i) {
+            mbar_init(smem_u32(&szfull[i]), 1);
+            mbar_init(smem_u32(&szempty[i]), kDecodeWarps);
+        }
+        fence_barrier_init();
+        pdl_launch_dependents();  // the next kernel may start streaming its weights
+    }
+    if (kLut) {
+        for (int i = threadIdx.x; i < 256; i += kDecodeThreads)
+            pair_tbl[i] = (uint32_t)__half_as_ushort(a.lut[i & 15]) |
+                          ((uint32_t)__half_as_ushort(a.lut[i >> 4]) << 16);
+    }
+    __syncthreads();
+
+    if (warp == kDecodeWarps) {
+        // ------------------------------------------------------------ producer
+        // Per group of tiles and chunk: the A chunk (after the first chunk's
+        // weights, so that those stream before the wait for the preceding
+        // kernel), then one weight stage per tile of the group.
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first(), pol_a = policy_evict_last();
+            int64_t it = 0, ai = 0;
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true, released = false;
+            auto a_chunk = [&](int sg) {
+                if (!released) {
+                    pdl_wait();  // A may be written by the preceding kernel
+                    released = true;
+                }
+                const int as = (int)(ai % kKmASlots);
+                ok = mbar_wait(smem_u32(&aempty[as]), (uint32_t)(((ai / kKmASlots) & 1) ^ 1), a.err);
+                if (!ok) return;
+                const int nst = nsteps - sg * sps < sps ? nsteps - sg * sps : sps;
+                const uint32_t bar = smem_u32(&afull[as]);
+                mbar_arrive_expect_tx(bar, (uint32_t)a.M * (uint32_t)nst * (kStepK * 2));
+                for (int64_t m = 0; m < a.M; ++m)
+                    bulk_g2s(a_sm + (uint32_t)as * slot_bytes + (uint32_t)m * kKmTokBytes,
+                             a.A + m * a.K + (int64_t)sg * sps * kStepK, (uint32_t)nst * (kStepK * 2), bar, pol_a);
+                ++ai;
+            };
+            int64_t gi = 0;  // groups issued
+            for (int64_t g0 = tb; g0 < te && ok; g0 += kKmTiles, ++gi) {
+                const int64_t g1 = te - g0 < kKmTiles ? te : g0 + kKmTiles;
+                // the group's scales and zeros, one slot per tile (weight data:
+                // ready before the launch, like the weights)
+                for (int64_t tile = g0; kSzSmem && tile < g1 && ok; ++tile) {
+                    const int ti = (int)(tile - g0);
+                    ok = mbar_wait(smem_u32(&szempty[ti]), (uint32_t)((gi & 1) ^ 1), a.err);
+                    if (!ok) break;
+                    const int rows = (int)(a.N - tile * kRowsPerTile < kRowsPerTile ? a.N - tile * kRowsPerTile
+                                                                                   : kRowsPerTile);
+                    const uint32_t sb = (uint32_t)a.ng * 2u, zb = (uint32_t)a.ng;
+                    const uint32_t bar = smem_u32(&szfull[ti]);
+                    const uint32_t dst = sz_sm + (uint32_t)ti * sz_bytes;
+                    mbar_arrive_expect_tx(bar, (uint32_t)rows * (sb + (kLut ? 0u : zb)));
+                    for (int r = 0; r < rows; ++r) {
+                        const int64_t n = tile * kRowsPerTile + r;
+                        bulk_g2s(dst + r * ss, a.S + n * a.ng, sb, bar, pol);
+                        if (!kLut) bulk_g2s(dst + kRowsPerTile * ss + r * zs, a.Z + n * a.ng, zb, bar, pol);
+                    }
+                }
+                for (int sg = 0; sg < spt && ok; ++sg) {
+                    if (released) a_chunk(sg);
+                    const int nst = nsteps - sg * sps < sps ? nsteps - sg * sps : sps;
+                    for (int64_t tile = g0; tile < g1 && ok; ++tile, ++it) {
+                        ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u, a.err);
+                        if (!ok) break;
+                        const uint32_t bar = smem_u32(&full[s]);
+                        mbar_arrive_expect_tx(bar, (uint32_t)nst * 1024u);
+                        bulk_g2s(smem_u32(smem + (size_t)s * kDStageBytes), a.W + (tile * nsteps + sg * sps) * 1024,
+                                 (uint32_t)nst * 1024u, bar, pol);
+                        if (++s == S) s = 0, ph ^= 1u;
+                    }
+                    if (!released && ok) a_chunk(sg);  // the very first chunk
+                }
+            }
+            // drain: nothing may still be landing when the CTA exits
+            for (int64_t k = it > S ? it - S : 0; k < it; ++k)
+                mbar_wait(smem_u32(&full[k % S]), (uint32_t)((k / S) & 1), a.err);
+            for (int64_t k = ai > kKmASlots ? ai - kKmASlots : 0; k < ai; ++k)
+                mbar_wait(smem_u32(&afull[k % kKmASlots]), (uint32_t)((k / kKmASlots) & 1), a.err);
+            if (kSzSmem && gi > 0) {  // the last group's slots
+                const int64_t glast = tb + (gi - 1) * kKmTiles;
+                const int nlast = (int)(te - glast < kKmTiles ? te - glast : kKmTiles);
+                for (int ti = 0; ti < nlast; ++ti)
+                    mbar_wait(smem_u32(&szfull[ti]), (uint32_t)((gi - 1) & 1), a.err);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // A timed-out wait leaves `ok` false: the warp stops waiting but keeps its
+    // place in the barriers (results are garbage, the error word says so).
+    const int j = lane & 3, tok = lane >> 2;
+    bool ok = true;
+    pdl_wait();  // C is written below
+    uint32_t xoff[NT];  // this lane's token row inside an A slot, at its 32 elements of a step
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        // tokens past M read a valid token's activations (their outputs are never stored)
+        const int64_t m = nt * 8 + tok < a.M ? nt * 8 + tok : a.M - 1;
+        xoff[nt] = (uint32_t)m * kKmTokBytes + 64u * j;
+    }
+    constexpr int kps = sps / kDecodeWarps;  // this warp's steps per chunk
+    int64_t ai = 0, gi = 0;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int64_t g0 = tb; g0 < te; g0 += kKmTiles, ++gi) {
+        const int ng_tiles = (int)(te - g0 < kKmTiles ? te - g0 : kKmTiles);
+        if (kSzSmem) {
+#pragma unroll
+            for (int ti = 0; ti < kKmTiles; ++ti)
+                if (ti < ng_tiles && ok) ok = mbar_wait(smem_u32(&szfull[ti]), (uint32_t)(gi & 1), a.err);
+        }
+        float tot[kKmTiles][NT][4];
+#pragma unroll
+        for (int ti = 0; ti < kKmTiles; ++ti)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tot[ti][nt][i] = 0.0f;
+        for (int sg = 0; sg < spt; ++sg, ++ai) {
+            const int as = (int)(ai % kKmASlots);
+            if (ok) ok = mbar_wait(smem_u32(&afull[as]), (uint32_t)((ai / kKmASlots) & 1), a.err);
+            const uint32_t aslot = a_sm + (uint32_t)as * slot_bytes;
+#pragma unroll
+            for (int ti = 0; ti < kKmTiles; ++ti) {
+                if (ti < ng_tiles) {
+                    const int64_t tile = g0 + ti;
+                    const int64_t r0 = tile * kRowsPerTile + tok, r1 = r0 + 8;
+                    const int64_t rc0 = r0 < a.N ? r0 : a.N - 1, rc1 = r1 < a.N ? r1 : a.N - 1;
+                    // this warp's steps of the chunk: their activations, scales, zeros
+                    if (ok) ok = mbar_wait(smem_u32(&full[s]), ph, a.err);
+                    const uint32_t stage = smem_u32(smem) + (uint32_t)s * kDStageBytes + tok * 64u + 16u * j;
+                    // this warp's steps of the chunk, each with its activations,
+                    // scales and zeros loaded just before its MMAs
+#pragma unroll
+                    for (int h = 0; h < kps; ++h) {
+                        const int sl = warp + h * kDecodeWarps, st = sg * sps + sl;
+                        if (st < nsteps) {
+                            const int g = a.spg == 1 ? st : st / a.spg;
+                            Operands<NT> P;
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    P.x[nt][q] = lds128(aslot + xoff[nt] + (uint32_t)sl * (kStepK * 2) + 16u * q);
+                            if (kSzSmem) {
+                                const uint32_t ss0 = sz_sm + (uint32_t)ti * sz_bytes + tok * ss, ss1 = ss0 + 8 * ss;
+                                const uint32_t zs0 = sz_sm + (uint32_t)ti * sz_bytes + kRowsPerTile * ss + tok * zs;
+                                uint32_t h0, h1;
+                                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h0) : "r"(ss0 + 2u * g));
+                                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h1) : "r"(ss1 + 2u * g));
+                                P.s0 = __half2float(__ushort_as_half((unsigned short)h0));
+                                P.s1 = __half2float(__ushort_as_half((unsigned short)h1));
+                                if (!kLut) {
+                                    uint32_t z0, z1;
+                                    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(z0) : "r"(zs0 + g));
+                                    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(z1) : "r"(zs0 + 8 * zs + g));
+                                    P.z0 = make_zero2(z0);
+                                    P.z1 = make_zero2(z1);
+                                }
+                            } else {
+                                P.s0 = __half2float(__ldg(a.S + rc0 * a.ng + g));
+                                P.s1 = __half2float(__ldg(a.S + rc1 * a.ng + g));
+                                if (!kLut) {
+                                    P.z0 = make_zero2(__ldg(a.Z + rc0 * a.ng + g));
+                                    P.z1 = make_zero2(__ldg(a.Z + rc1 * a.ng + g));
+                                }
+                            }
+                            const uint32_t w = stage + (uint32_t)sl * 1024u;
+                            step_mma<NT, kLut>(P, pair_tbl, lds128(w), lds128(w + 512u), tot[ti]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+                    if (++s == S) s = 0, ph ^= 1u;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&aempty[as]));  // the chunk's activations are read
+        }
+        // reduce the consumer warps' partial sums, tile by tile
+#pragma unroll
+        for (int ti = 0; ti < kKmTiles; ++ti) {
+            if (ti < ng_tiles) {
+                const int64_t tile = g0 + ti;
+                const int64_t r0 = tile * kRowsPerTile + tok, r1 = r0 + 8;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) red[warp][nt][i][lane] = tot[ti][nt][i];
+                consumers_sync();
+                if (warp < NT) {
+                    const int nt = warp;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float sum = 0.0f;
+#pragma unroll
+                        for (int w = 0; w < kDecodeWarps; ++w) sum += red[w][nt][i][lane];
+                        // c0, c1: row t/4, tokens 2j, 2j+1; c2, c3: row t/4 + 8
+                        const int64_t n = (i < 2) ? r0 : r1;
+                        const int64_t m = nt * 8 + 2 * j + (i & 1);
+                        if (n < a.N && m < a.M) a.C[m * a.N + n] = __float2half_rn(sum);
+                    }
+                }
+                consumers_sync();
+            }
+        }
+        if (kSzSmem) {  // the group's scale/zero slots are free again
+            __syncwarp();
+#pragma unroll
+            for (int ti = 0; ti < kKmTiles; ++ti)
+                if (ti < ng_tiles && lane == 0) mbar_arrive(smem_u32(&szempty[ti]));
+        }
+    }
+}
+
 // ------------------------------------------------------------------ repack
 // Nibble slot p of a packed word holds element kPackOrder[p] of the word.
 __device__ __forceinline__ uint32_t pack_word(uint32_t c) {
@@ -527,6 +804,24 @@ cudaError_t launch_decode_m(const DecodeArgs &a, bool staged, bool szsmem, int64
                   : launch_decode_nt<NT, kLut, false, false>(a, grid, smem, s);
 }
 
+template <bool kLut, bool kSzSmem>
+cudaError_t launch_decode_kmajor(const DecodeArgs &a, int64_t grid, size_t smem, cudaStream_t s) {
+    auto fn = w4a16_decode_kmajor_kernel<kLut, kSzSmem>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn), (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, a);
+}
+
 cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z, const __half *lut,
                                 int64_t G, const __half *A, __half *C, int64_t M, int64_t N, int64_t K,
                                 cudaStream_t s) {
@@ -545,8 +840,25 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
     a.spg = (int)(G / kStepK);
     a.err = device_error_word();
     const int64_t ntiles = (N + kRowsPerTile - 1) / kRowsPerTile;
-    // all of A in shared memory when it is small (padded rows)
+    // all of A in shared memory when it is small (padded rows); else, from
+    // 9 tokens, the K-major kernel with A chunks in shared memory (8192^2, 16
+    // tokens: 25.4 -> 19.6 us; with 8 or fewer, whose activation fragments are
+    // fewer, reading them from L2 stays faster: 14.9 against 17.4 us at 8)
     const bool staged = (size_t)M * K * 2 <= kActStageMax;
+    if (!staged && M > 8) {
+        a.act_bytes = 0;
+        const bool szk = a.ng % 16 == 0 && sz_slot_bytes(a.ng, lut != nullptr) <= 8192;
+        const size_t smem = (size_t)kKmStages * kDStageBytes + kKmASlots * (size_t)km_slot_bytes(M) +
+                            (szk ? (size_t)kKmTiles * sz_slot_bytes(a.ng, lut != nullptr) : 0) +
+                            (2 * kKmStages + 2 * kKmASlots + 2 * kKmTiles) * 8;
+        const int64_t grid = balanced_grid(ntiles, (int64_t)sm_count());
+        const cudaError_t e = lut ? (szk ? launch_decode_kmajor<true, true>(a, grid, smem, s)
+                                         : launch_decode_kmajor<true, false>(a, grid, smem, s))
+                                  : (szk ? launch_decode_kmajor<false, true>(a, grid, smem, s)
+                                         : launch_decode_kmajor<false, false>(a, grid, smem, s));
+        count_launch();
+        return e;
+    }
     a.act_bytes = staged ? actpad_bytes(M, K) : 0u;
     // the tile's scales and zeros in shared memory when every row is a
     // multiple of 16 bytes and both slots fit beside the ring
@@ -559,9 +871,9 @@ cudaError_t launch_w4a16_decode(const void *W, const __half *S, const uint8_t *Z
     if (M <= 8)
         e = lut ? launch_decode_m<1, true>(a, staged, szsmem, grid, smem, s)
                 : launch_decode_m<1, false>(a, staged, szsmem, grid, smem, s);
-    else
-        e = lut ? launch_decode_m<2, true>(a, staged, szsmem, grid, smem, s)
-                : launch_decode_m<2, false>(a, staged, szsmem, grid, smem, s);
+    else  // 9..16 tokens reach here only with the staged layout
+        e = lut ? launch_decode_m<2, true>(a, true, szsmem, grid, smem, s)
+                : launch_decode_m<2, false>(a, true, szsmem, grid, smem, s);
     count_launch();
     return e;
 }

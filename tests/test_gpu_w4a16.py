@@ -81,7 +81,10 @@ def test_repack_round_trip(q):
                                      (100, 384, 128, 130), (200, 640, 128, 33), (48, 1024, 256, 200),
                                      (136, 1152, 384, 257),
                                      (128, 8192, 128, 40),    # one tile over 32 CTAs (stream-K pieces)
-                                     (1000, 4096, 128, 300)])  # CTA ranges straddling tiles
+                                     (1000, 4096, 128, 300),  # CTA ranges straddling tiles
+                                     (40, 2304, 128, 9),      # K-major decode: a partial K chunk, a partial tile
+                                     (10000, 1024, 128, 16),  # K-major decode: more tiles per CTA than one group
+                                     (64, 4096, 128, 4)])     # decode with A read in place (too large to stage)
 def test_w4a16_small(q, orc, N, K, G, M):
     qc, s16, z, A16 = wl.w4a16_inputs(40, N, K, G, M)
     qweight = orc.w4a16_pack(qc.numpy())
@@ -203,7 +206,7 @@ def run_lut(q, Wp, s16, lut16, G, A16, M, N, K):
 
 @pytest.mark.parametrize("N,K,G,M", [(64, 256, 128, 1), (100, 512, 128, 5), (48, 1024, 256, 16),
                                      (33, 384, 128, 9), (40, 512, 128, 17), (200, 640, 128, 33),
-                                     (136, 1152, 384, 257), (1000, 4096, 128, 300)])
+                                     (136, 1152, 384, 257), (1000, 4096, 128, 300), (40, 2304, 128, 9)])
 def test_w4a16_lut_small(q, orc, N, K, G, M):
     """W-hat = s LUT(q) with the NF4-like table: decode (M <= 16) and the
     tensor-core GEMM (M > 16, stream-K when tiles outnumber SMs)."""
