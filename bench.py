@@ -447,7 +447,7 @@ def prefill_extras(q, dev, stream, peaks_measured=None):
     return out
 
 
-def w4a16_extras(q, dev, stream, reps=8, graph_steps=16):
+def w4a16_extras(q, dev, stream, reps=8, graph_steps=16, ms=None):
     """W4A16 on the 8192 x 8192, G = 128 layer at M in {1, 16, 256}: us per
     call, GB/s of algorithmic bytes (codes + scales + zeros + A + C) and
     TOPS (2 M N K). Rotating weight copies larger than L2 at M <= 16."""
@@ -469,7 +469,7 @@ def w4a16_extras(q, dev, stream, reps=8, graph_steps=16):
     sets = [(Wp, s16, z)] + [(Wp.clone(), s16.clone(), z.clone()) for _ in range(ncopies - 1)]
     wbytes = Wp.numel() + s16.numel() * 2 + z.numel()
     out = {}
-    for M in wl.W4A16_M:
+    for M in (ms or wl.W4A16_M):
         A = wl.normal_rows(9, wl.S_A, M, K, device=dev).to(torch.float16)
         C = torch.empty(M, N, dtype=torch.float16, device=dev)
         nset = ncopies if M <= 16 else 1
@@ -712,7 +712,7 @@ def main():
                     help="prefill / w4a16 / layer / sweep / q6_K: only that measurement (for "
                          "profiler captures)")
     ap.add_argument("--m", type=int, action="append",
-                    help="with --case sweep: only these token counts")
+                    help="with --case sweep or w4a16: only these token counts")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -746,7 +746,8 @@ def main():
         torch.cuda.set_device(0)
     if args.case != "decode":
         import block_quantized_matmul_q4_gb300 as q
-        fn = {"prefill": prefill_extras, "w4a16": w4a16_extras, "layer": layer_rate, "q6_K": q6_K_rate,
+        fn = {"prefill": prefill_extras, "w4a16": lambda q, d, s: w4a16_extras(q, d, s, ms=args.m),
+              "layer": layer_rate, "q6_K": q6_K_rate,
               "small_m": small_m_rate, "peaks": peaks_rate,
               "sweep": lambda q, d, s: sweep_rate(q, d, s, args.m)}[args.case]
         print(json.dumps(fn(q, torch.device("cuda", torch.cuda.current_device()),

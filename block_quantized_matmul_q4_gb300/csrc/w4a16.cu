@@ -99,9 +99,11 @@ __device__ __forceinline__ void lut_word(uint32_t w, const uint32_t *tbl, uint32
     p67 = tbl[(t2 >> 8) & 0xFF];
 }
 
+// A register-only operation: not volatile, so the compiler may interleave
+// independent MMAs with the loads and conversions around them.
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
         "{%8, %9}, {%0, %1, %2, %3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
