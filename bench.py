@@ -287,28 +287,32 @@ def gpu_arm(args, rank, world):
                 "launches_per_step": launches_per_step,
                 "prepared_gemv_us": round(t_prep * 1e6, 3)}
 
-    # end to end through the public API: pinned host X -> device, qmm_mul_mat
-    # (the user call, which quantizes, allocates its workspace stream-ordered
-    # and runs the GEMV), result -> pinned host
+    # end to end through the public C-ABI call with host buffers: per step one
+    # qmm_mul_mat_host call, which copies the pinned host X to the device,
+    # quantizes it and runs the GEMV, and copies Y back to pinned host memory,
+    # all in stream order; eager launches from Python, no graph
     e2e_steps = max(3, min(args.steps, 3000))
     Xh = X.cpu().pin_memory()
     Yh = torch.empty(M, N).pin_memory()
-    Xd = torch.empty_like(X)
+    hbytes = q.qmm_host_call_bytes(wt, M, N, K)
+    hbuf = torch.empty(hbytes, dtype=torch.uint8, device=X.device)
+    sptr = stream.cuda_stream
+    wptrs = [c.data_ptr() for c in copies]
+    xp, yp, bp = Xh.data_ptr(), Yh.data_ptr(), hbuf.data_ptr()
+    call = q._lib.qmm_mul_mat_host
 
     def e2e_loop():
         for i in range(e2e_steps):
-            Xd.copy_(Xh, non_blocking=True)
-            q.qmm_mul_mat(wt, copies[i % COPIES], N, K, Xd, M, Y, stream)
-            Yh.copy_(Y, non_blocking=True)
+            st = call(wt, wptrs[i % COPIES], N, K, xp, M, yp, bp, hbytes, sptr)
+            if st:
+                q._check("qmm_mul_mat_host", st)
 
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            Xd.copy_(Xh, non_blocking=True)
-            q.qmm_mul_mat(wt, copies[i], N, K, Xd, M, Y, stream)
+    for i in range(3):
+        call(wt, wptrs[i], N, K, xp, M, yp, bp, hbytes, sptr)
     t_e2e = timed(stream, e2e_loop)
     e2e = {"value": round(per_step * e2e_steps * world / t_e2e / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": Xh.numel() * 4, "d2h_bytes_per_step": Yh.numel() * 4,
-           "steps": e2e_steps, "path": "qmm_mul_mat, eager launches"}
+           "steps": e2e_steps, "path": "qmm_mul_mat_host (C ABI, one call per step: pinned host X copied in, Y stored by the kernel into pinned host memory), eager"}
     q.qmm_check_device_error(stream)
 
     extras = {}

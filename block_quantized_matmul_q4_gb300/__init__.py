@@ -45,6 +45,8 @@ _SIGS = {
     "qmm_unrepack_weights": (_i32, [_i32, _vp, _vp, _i64, _i64, _vp]),
     "qmm_mul_mat": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_mul_mat_ws": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "qmm_host_call_bytes": (_sz, [_i32, _i64, _i64, _i64]),
+    "qmm_mul_mat_host": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _sz, _vp]),
     "qmm_mul_mat_q8": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_mul_mat_multi": (_i32, [_i32, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_i64), _i64, _vp,
                                  _i64, ctypes.POINTER(_vp), _vp]),
@@ -164,6 +166,27 @@ def qmm_mul_mat_ws(wt: int, W_packed, N: int, K: int, X, M: int, Y, workspace, w
     _check("qmm_mul_mat_ws",
            _lib.qmm_mul_mat_ws(wt, _ptr(W_packed), N, K, _ptr(X), M, _ptr(Y), _ptr(workspace),
                                ws_bytes, _stream(stream)))
+
+
+def _host_ptr(t):
+    if isinstance(t, int):
+        return t
+    if t.is_cuda:
+        raise ValueError("qmm_mul_mat_host takes host tensors for X and Y")
+    if not t.is_contiguous():
+        raise ValueError("libqmm takes contiguous tensors")
+    return t.data_ptr()
+
+
+def qmm_host_call_bytes(wt: int, M: int, N: int, K: int) -> int:
+    return int(_lib.qmm_host_call_bytes(wt, M, N, K))
+
+
+def qmm_mul_mat_host(wt: int, W_packed, N: int, K: int, X_host, M: int, Y_host, device_buf,
+                     buf_bytes: int, stream=None):
+    _check("qmm_mul_mat_host",
+           _lib.qmm_mul_mat_host(wt, _ptr(W_packed), N, K, _host_ptr(X_host), M, _host_ptr(Y_host),
+                                 _ptr(device_buf), buf_bytes, _stream(stream)))
 
 
 def qmm_quantize_activations(wt: int, X, M: int, K: int, workspace, ws_bytes: int, stream=None):

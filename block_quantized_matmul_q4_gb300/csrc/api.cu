@@ -352,9 +352,12 @@ static qmm_status repack_common(qmm_type wt, const void *src, void *dst, int64_t
     const void *packed = inverse ? src : dst;
     QMM_CHECK_ARG(aligned(packed, 16), "packed weights must be 16-byte aligned");
     QMM_CHECK_ARG(aligned(canon, wt == QMM_TYPE_Q4_K ? 16 : 2), "canonical weights misaligned");
+    // canonical blocks span N rows, packed ones are padded to whole tiles
     const uintptr_t a = (uintptr_t)src, b = (uintptr_t)dst;
     const size_t pb = qmm_packed_bytes(wt, N, K);
-    QMM_CHECK_ARG(a + pb <= b || b + pb <= a, "source and destination overlap");
+    const size_t cb = (size_t)N * (size_t)(K / qmm_block_elems(wt)) * qmm_block_bytes(wt);
+    const size_t sb = inverse ? pb : cb, db = inverse ? cb : pb;
+    QMM_CHECK_ARG(a + sb <= b || b + db <= a, "source and destination overlap");
     return cuda_status(launch_repack(wt, inverse, src, dst, N, K, (cudaStream_t)stream),
                        "repack launch");
 }
@@ -380,6 +383,54 @@ qmm_status qmm_mul_mat_ws(qmm_type wt, const void *W_packed, int64_t N, int64_t 
     if (ws_bytes < need)
         return set_error(QMM_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, need);
     return mul_mat_impl(wt, W_packed, N, K, X, M, Y, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+// Device buffer of qmm_mul_mat_host: X, then Y, then the workspace.
+static size_t host_x_bytes(int64_t M, int64_t K) { return (size_t)align_up((uint64_t)M * K * 4, 16); }
+static size_t host_y_bytes(int64_t M, int64_t N) { return (size_t)align_up((uint64_t)M * N * 4, 16); }
+
+size_t qmm_host_call_bytes(qmm_type wt, int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || (M > 0 && qmm_workspace_bytes(wt, M, K) == 0)) return 0;
+    if (M == 0 || N == 0) return 16;
+    return host_x_bytes(M, K) + host_y_bytes(M, N) + qmm_workspace_bytes(wt, M, K);
+}
+
+qmm_status qmm_mul_mat_host(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X_host,
+                            int64_t M, float *Y_host, void *device_buf, size_t buf_bytes,
+                            qmm_stream_t stream) {
+    qmm_status st = check_weight_args(wt, N, K);
+    if (st != QMM_OK) return st;
+    QMM_CHECK_ARG(M >= 0, "M must be >= 0 (got %lld)", (long long)M);
+    if (M == 0 || N == 0) return ok();
+    QMM_CHECK_ARG(W_packed && X_host && Y_host && device_buf, "null pointer argument");
+    QMM_CHECK_ARG(aligned(W_packed, 16) && aligned(device_buf, 16),
+                  "W_packed and device_buf must be 16-byte aligned");
+    const size_t need = qmm_host_call_bytes(wt, M, N, K);
+    if (buf_bytes < need)
+        return set_error(QMM_ERR_WORKSPACE, "device buffer of %zu bytes < %zu needed", buf_bytes, need);
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t *base = static_cast<uint8_t *>(device_buf);
+    float *Xd = reinterpret_cast<float *>(base);
+    float *Yd = reinterpret_cast<float *>(base + host_x_bytes(M, K));
+    void *ws = base + host_x_bytes(M, K) + host_y_bytes(M, N);
+    const size_t ws_bytes = buf_bytes - host_x_bytes(M, K) - host_y_bytes(M, N);
+    // X goes in by one asynchronous copy (the kernels read it many times,
+    // from L2); Y, written once, goes straight to the caller's memory when
+    // that is page-locked and mapped into the device's address space (what
+    // cudaHostAlloc and cudaHostRegister give on this system), which saves
+    // the copy call back -- else by a copy from device_buf.
+    cudaPointerAttributes ay = {};
+    const bool y_mapped = cudaPointerGetAttributes(&ay, Y_host) == cudaSuccess && ay.type == cudaMemoryTypeHost &&
+                          ay.devicePointer && aligned(ay.devicePointer, 4);
+    cudaGetLastError();  // a failed query is not an error of this call
+    cudaError_t e = cudaMemcpyAsync(Xd, X_host, (size_t)M * K * 4, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e, "X host-to-device copy");
+    if (y_mapped) return mul_mat_impl(wt, W_packed, N, K, Xd, M, static_cast<float *>(ay.devicePointer), ws, ws_bytes, s);
+    st = mul_mat_impl(wt, W_packed, N, K, Xd, M, Yd, ws, ws_bytes, s);
+    if (st != QMM_OK) return st;
+    e = cudaMemcpyAsync(Y_host, Yd, (size_t)M * N * 4, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_status(e, "Y device-to-host copy");
+    return ok();
 }
 
 qmm_status qmm_quantize_activations(qmm_type wt, const float *X, int64_t M, int64_t K,

@@ -256,6 +256,32 @@ qmm_status qmm_mul_mat_ws(qmm_type wt, const void *W_packed, int64_t N, int64_t 
                           int64_t M, float *Y, void *workspace, size_t ws_bytes,
                           qmm_stream_t stream);
 
+/* qmm_mul_mat on HOST activations and outputs, for a caller whose X starts
+ * and whose Y ends in host memory (the same y = W x over block formats,
+ * page 1, "通用实现"): in stream order, X_host [M, K] fp32 is copied to the
+ * device, the product runs exactly as qmm_mul_mat_ws (same kernels, same
+ * bits), and Y [M, N] fp32 is copied back to Y_host; one call, so the host
+ * pays one library call per product instead of three.
+ *   device_buf: caller-owned device memory of at least
+ *     qmm_host_call_bytes(wt, M, N, K) bytes, 16-byte aligned; it holds X,
+ *     Y and the workspace, and is in use until the call's work on `stream`
+ *     has finished.
+ *   X_host, Y_host: host memory. X is copied into device_buf by
+ *     cudaMemcpyAsync (the kernels read it many times). Y, written once, is
+ *     stored by the kernels straight into Y_host when that is page-locked
+ *     memory mapped into the device's address space (cudaHostAlloc,
+ *     cudaHostRegister), saving the copy back; else it is copied from
+ *     device_buf. Page-locked memory lets the copies run asynchronously;
+ *     with pageable memory the runtime stages them and the call may block.
+ *     Y_host holds the result only once the stream has reached the end of
+ *     the call.
+ * Errors: those of qmm_mul_mat_ws; QMM_ERR_WORKSPACE when buf_bytes is too
+ * small; QMM_ERR_CUDA when a copy cannot be enqueued. */
+size_t qmm_host_call_bytes(qmm_type wt, int64_t M, int64_t N, int64_t K);
+qmm_status qmm_mul_mat_host(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X_host,
+                            int64_t M, float *Y_host, void *device_buf, size_t buf_bytes,
+                            qmm_stream_t stream);
+
 /* The two halves of qmm_mul_mat_ws, for callers that reuse one quantized
  * activation across several weight matrices (page 1, "为什么每个任务都要重新
  * 量化激活": a mul_mat quantizes its activations once; projections sharing an

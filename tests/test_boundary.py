@@ -99,3 +99,29 @@ def test_type_ids_agree(built_lib):
         assert getattr(oracle, name) == ids["QMM_TYPE_" + name]
         assert oracle.BLOCK_BYTES[getattr(oracle, name)] == ctypes.CDLL(built_lib).qmm_block_bytes(
             ids["QMM_TYPE_" + name])
+
+
+def test_host_call_bytes(lib):
+    """qmm_mul_mat_host's device buffer: X, then Y (each rounded up to 16
+    bytes), then the workspace of qmm_mul_mat_ws; 0 for invalid shapes."""
+    f = lib.qmm_host_call_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+    r16 = lambda n: (n + 15) // 16 * 16
+    for wt, M, N, K in [(1, 1, 4096, 4096), (0, 3, 40, 4096), (5, 20, 11008, 4096), (1, 1, 5, 256)]:
+        assert f(wt, M, N, K) == r16(M * K * 4) + r16(M * N * 4) + lib.qmm_workspace_bytes(wt, M, K)
+    assert f(1, 1, 10, 100) == 0  # K not a multiple of 256
+    assert f(3, 1, 10, 256) == 0  # not a weight type
+
+
+def test_repack_overlap_rejected(lib):
+    """qmm_repack_weights refuses overlapping canonical and packed buffers
+    before it launches anything. (Buffers that only the packed side's tile
+    padding would make overlap are accepted: the Q6_K N = 300 case of
+    test_gpu_parity.test_mul_mat_host_buffers allocates such a pair.)"""
+    f = lib.qmm_repack_weights
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+    src = 1 << 20
+    assert f(5, src, src + 16, 300, 2048, None) == 1  # QMM_ERR_ARG
+    assert "overlap" in lib.qmm_last_error().decode()
