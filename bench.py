@@ -288,9 +288,9 @@ def gpu_arm(args, rank, world):
                 "prepared_gemv_us": round(t_prep * 1e6, 3)}
 
     # end to end through the public C-ABI call with host buffers: per step one
-    # qmm_mul_mat_host call, which copies the pinned host X to the device,
-    # quantizes it and runs the GEMV, and copies Y back to pinned host memory,
-    # all in stream order; eager launches from Python, no graph
+    # qmm_mul_mat_host call (pinned, mapped buffers): a kernel pulls X from
+    # host memory into device memory, the GEMV quantizes it and stores Y into
+    # pinned host memory, all in stream order; eager launches, no graph
     e2e_steps = max(3, min(args.steps, 3000))
     Xh = X.cpu().pin_memory()
     Yh = torch.empty(M, N).pin_memory()
@@ -303,16 +303,16 @@ def gpu_arm(args, rank, world):
 
     def e2e_loop():
         for i in range(e2e_steps):
-            st = call(wt, wptrs[i % COPIES], N, K, xp, M, yp, bp, hbytes, sptr)
+            st = call(wt, wptrs[i % COPIES], N, K, xp, M, yp, bp, hbytes, q.QMM_HOST_MAPPED, sptr)
             if st:
                 q._check("qmm_mul_mat_host", st)
 
     for i in range(3):
-        call(wt, wptrs[i], N, K, xp, M, yp, bp, hbytes, sptr)
+        call(wt, wptrs[i], N, K, xp, M, yp, bp, hbytes, q.QMM_HOST_MAPPED, sptr)
     t_e2e = timed(stream, e2e_loop)
     e2e = {"value": round(per_step * e2e_steps * world / t_e2e / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": Xh.numel() * 4, "d2h_bytes_per_step": Yh.numel() * 4,
-           "steps": e2e_steps, "path": "qmm_mul_mat_host (C ABI, one call per step: pinned host X copied in, Y stored by the kernel into pinned host memory), eager"}
+           "steps": e2e_steps, "path": "qmm_mul_mat_host with QMM_HOST_MAPPED (C ABI, one call per step: a kernel pulls the pinned host X into device memory, the GEMV stores Y into pinned host memory), eager"}
     q.qmm_check_device_error(stream)
 
     extras = {}

@@ -46,7 +46,7 @@ _SIGS = {
     "qmm_mul_mat": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_mul_mat_ws": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _sz, _vp]),
     "qmm_host_call_bytes": (_sz, [_i32, _i64, _i64, _i64]),
-    "qmm_mul_mat_host": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "qmm_mul_mat_host": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _sz, ctypes.c_uint, _vp]),
     "qmm_mul_mat_q8": (_i32, [_i32, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "qmm_mul_mat_multi": (_i32, [_i32, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_i64), _i64, _vp,
                                  _i64, ctypes.POINTER(_vp), _vp]),
@@ -182,11 +182,14 @@ def qmm_host_call_bytes(wt: int, M: int, N: int, K: int) -> int:
     return int(_lib.qmm_host_call_bytes(wt, M, N, K))
 
 
+QMM_HOST_MAPPED = 1
+
+
 def qmm_mul_mat_host(wt: int, W_packed, N: int, K: int, X_host, M: int, Y_host, device_buf,
-                     buf_bytes: int, stream=None):
+                     buf_bytes: int, stream=None, flags: int = 0):
     _check("qmm_mul_mat_host",
            _lib.qmm_mul_mat_host(wt, _ptr(W_packed), N, K, _host_ptr(X_host), M, _host_ptr(Y_host),
-                                 _ptr(device_buf), buf_bytes, _stream(stream)))
+                                 _ptr(device_buf), buf_bytes, flags, _stream(stream)))
 
 
 def qmm_quantize_activations(wt: int, X, M: int, K: int, workspace, ws_bytes: int, stream=None):

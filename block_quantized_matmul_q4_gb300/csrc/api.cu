@@ -385,6 +385,34 @@ qmm_status qmm_mul_mat_ws(qmm_type wt, const void *W_packed, int64_t N, int64_t 
     return mul_mat_impl(wt, W_packed, N, K, X, M, Y, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
+// X of qmm_mul_mat_host from mapped host memory into device_buf: one pass,
+// 16 bytes per thread (X_host and the buffer are 16-byte aligned, M K is a
+// multiple of 32). It follows the previous kernel in the stream, which may
+// still read the buffer, and lets the GEMV after it launch early.
+__global__ void __launch_bounds__(256) pull_x_kernel(const float4 *__restrict__ src, float4 *__restrict__ dst,
+                                                     int64_t n4) {
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    pdl_wait();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+// Whether a host pointer from cudaHostAlloc / cudaHostRegister is usable on
+// the current device as it is (cached per device).
+static bool host_pointers_usable() {
+    static int cached[64] = {};  // 0 unknown, 1 yes, 2 no
+    const int d = current_device();
+    if (d < 0 || d >= 64) return false;
+    if (!cached[d]) {
+        int uva = 0, reg = 0;
+        cudaDeviceGetAttribute(&uva, cudaDevAttrUnifiedAddressing, d);
+        cudaDeviceGetAttribute(&reg, cudaDevAttrCanUseHostPointerForRegisteredMem, d);
+        cudaGetLastError();
+        cached[d] = uva && reg ? 1 : 2;
+    }
+    return cached[d] == 1;
+}
+
 // Device buffer of qmm_mul_mat_host: X, then Y, then the workspace.
 static size_t host_x_bytes(int64_t M, int64_t K) { return (size_t)align_up((uint64_t)M * K * 4, 16); }
 static size_t host_y_bytes(int64_t M, int64_t N) { return (size_t)align_up((uint64_t)M * N * 4, 16); }
@@ -396,7 +424,7 @@ size_t qmm_host_call_bytes(qmm_type wt, int64_t M, int64_t N, int64_t K) {
 }
 
 qmm_status qmm_mul_mat_host(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X_host,
-                            int64_t M, float *Y_host, void *device_buf, size_t buf_bytes,
+                            int64_t M, float *Y_host, void *device_buf, size_t buf_bytes, unsigned flags,
                             qmm_stream_t stream) {
     qmm_status st = check_weight_args(wt, N, K);
     if (st != QMM_OK) return st;
@@ -414,6 +442,28 @@ qmm_status qmm_mul_mat_host(qmm_type wt, const void *W_packed, int64_t N, int64_
     float *Yd = reinterpret_cast<float *>(base + host_x_bytes(M, K));
     void *ws = base + host_x_bytes(M, K) + host_y_bytes(M, N);
     const size_t ws_bytes = buf_bytes - host_x_bytes(M, K) - host_y_bytes(M, N);
+    QMM_CHECK_ARG((flags & ~QMM_HOST_MAPPED) == 0, "unknown flags 0x%x", flags);
+    if (flags & QMM_HOST_MAPPED) {
+        if (!host_pointers_usable())
+            return set_error(QMM_ERR_UNSUPPORTED, "this device cannot use host pointers directly");
+        QMM_CHECK_ARG(aligned(X_host, 16) && aligned(Y_host, 4), "X_host must be 16-byte aligned, Y_host 4-byte");
+        const int64_t n4 = M * K / 4;
+        cudaLaunchConfig_t cfg = {};
+        const int64_t blocks = (n4 + 255) / 256;
+        cfg.gridDim = dim3((unsigned)(blocks < 64 ? blocks : 64));
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, pull_x_kernel, reinterpret_cast<const float4 *>(X_host),
+                                           reinterpret_cast<float4 *>(Xd), n4);
+        count_launch();
+        if (e != cudaSuccess) return cuda_status(e, "X pull launch");
+        return mul_mat_impl(wt, W_packed, N, K, Xd, M, Y_host, ws, ws_bytes, s);
+    }
     // X goes in by one asynchronous copy (the kernels read it many times,
     // from L2); Y, written once, goes straight to the caller's memory when
     // that is page-locked and mapped into the device's address space (what

@@ -276,10 +276,20 @@ qmm_status qmm_mul_mat_ws(qmm_type wt, const void *W_packed, int64_t N, int64_t 
  *     Y_host holds the result only once the stream has reached the end of
  *     the call.
  * Errors: those of qmm_mul_mat_ws; QMM_ERR_WORKSPACE when buf_bytes is too
- * small; QMM_ERR_CUDA when a copy cannot be enqueued. */
+ * small; QMM_ERR_CUDA when a copy cannot be enqueued.
+
+ *   flags: 0, or QMM_HOST_MAPPED: the caller states that X_host and Y_host
+ *     are page-locked memory the device can address by the same pointers
+ *     (cudaHostAlloc under unified addressing, or cudaHostRegister where
+ *     the device attribute cudaDevAttrCanUseHostPointerForRegisteredMem is
+ *     1; QMM_ERR_UNSUPPORTED if the device has neither). Then no copy call
+ *     and no pointer query is made: a small kernel pulls X into device_buf
+ *     and the kernels store Y into Y_host. Passing the flag for any other
+ *     memory is undefined behaviour. */
+#define QMM_HOST_MAPPED 1u
 size_t qmm_host_call_bytes(qmm_type wt, int64_t M, int64_t N, int64_t K);
 qmm_status qmm_mul_mat_host(qmm_type wt, const void *W_packed, int64_t N, int64_t K, const float *X_host,
-                            int64_t M, float *Y_host, void *device_buf, size_t buf_bytes,
+                            int64_t M, float *Y_host, void *device_buf, size_t buf_bytes, unsigned flags,
                             qmm_stream_t stream);
 
 /* The two halves of qmm_mul_mat_ws, for callers that reuse one quantized

@@ -125,3 +125,15 @@ def test_repack_overlap_rejected(lib):
     src = 1 << 20
     assert f(5, src, src + 16, 300, 2048, None) == 1  # QMM_ERR_ARG
     assert "overlap" in lib.qmm_last_error().decode()
+
+
+def test_host_call_rejects_unknown_flags(lib):
+    """qmm_mul_mat_host checks its flags (only QMM_HOST_MAPPED = 1 exists)
+    before any CUDA call."""
+    f = lib.qmm_mul_mat_host
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint, ctypes.c_void_p]
+    p = 1 << 20
+    assert f(1, p, 8, 256, p, 1, p, p, 1 << 30, 2, None) == 1
+    assert "flags" in lib.qmm_last_error().decode()

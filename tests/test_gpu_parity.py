@@ -420,10 +420,11 @@ def test_prepared_shared_workspace_two_streams(q, orc, wt):
 
 
 @pytest.mark.parametrize("wt,N,K,M", [(1, 4096, 4096, 1), (0, 40, 4096, 3), (5, 300, 2048, 20)])
-@pytest.mark.parametrize("pinned", [True, False])
-def test_mul_mat_host_buffers(q, wt, N, K, M, pinned):
-    """qmm_mul_mat_host (X from and Y to host memory, one call) gives the
-    bits of qmm_mul_mat on device copies of the same X."""
+@pytest.mark.parametrize("pinned,flags", [(True, 0), (True, 1), (False, 0)])
+def test_mul_mat_host_buffers(q, wt, N, K, M, pinned, flags):
+    """qmm_mul_mat_host (X from and Y to host memory, one call; with
+    QMM_HOST_MAPPED the kernels pull X and store Y through the mapped pinned
+    buffers) gives the bits of qmm_mul_mat on device copies of the same X."""
     w = wl.weights(60, N, K, 0.02, row_offset_std=0.0 if wt == 0 else 0.005, device="cuda")
     Wq = torch.empty(N * (K // (32 if wt == 0 else 256)) * q.qmm_block_bytes(wt), dtype=torch.uint8, device="cuda")
     q.qmm_quantize_weights(wt, w, Wq, N, K)
@@ -436,12 +437,12 @@ def test_mul_mat_host_buffers(q, wt, N, K, M, pinned):
     nbytes = q.qmm_host_call_bytes(wt, M, N, K)
     buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-    q.qmm_mul_mat_host(wt, Wp, N, K, Xh, M, Yh, buf, nbytes, stream)
+    q.qmm_mul_mat_host(wt, Wp, N, K, Xh, M, Yh, buf, nbytes, stream, flags)
     stream.synchronize()
     q.qmm_check_device_error()
     Yd = torch.empty(M, N, device="cuda")
     q.qmm_mul_mat(wt, Wp, N, K, x.cuda(), M, Yd)
     assert torch.equal(Yh, Yd.cpu())
     with pytest.raises(q.QmmError) as e:
-        q.qmm_mul_mat_host(wt, Wp, N, K, Xh, M, Yh, buf, nbytes - 16, stream)
+        q.qmm_mul_mat_host(wt, Wp, N, K, Xh, M, Yh, buf, nbytes - 16, stream, flags)
     assert e.value.status == 6
