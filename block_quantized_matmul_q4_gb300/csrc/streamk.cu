@@ -36,7 +36,8 @@ __device__ __forceinline__ void store4(__half *y, float4 v) {
                                                *reinterpret_cast<const uint32_t *>(&hi));
 }
 
-// The pieces of one split tile, added in CTA order and stored. Each thread
+// The pieces of one split tile, added in CTA order and stored (stream-K
+// grids). Each thread
 // takes 4 consecutive rows of a column (one 16-byte load per piece) and keeps
 // 4 columns in flight; a warp covers 128 rows of one column = 512 contiguous
 // bytes of every slot. kFull: all TN columns hold tokens (the bound is a
@@ -93,7 +94,8 @@ __device__ __forceinline__ void fixup_tile(const float *__restrict__ part, T *__
     }
 }
 
-// One CTA per tile (whole tiles return at once).
+// Stream-K grids (more tiles than SMs, a tile in two or three pieces): one
+// CTA per tile (whole tiles return at once).
 template <int TN, class T>
 __global__ void __launch_bounds__(kFixupThreads) stream_k_fixup_kernel(const float *__restrict__ part,
                                                                        T *__restrict__ C, int64_t N,
@@ -113,6 +115,91 @@ __global__ void __launch_bounds__(kFixupThreads) stream_k_fixup_kernel(const flo
                               units, G, vec);
 }
 static_assert((kTM * 128 / 4) % (4 * kFixupThreads) == 0, "fixup tiling");
+
+// Split-K grids (fewer tiles than half the SMs, each tile in many pieces):
+// the pieces of one tile added in CTA order and stored by `splits` CTAs per
+// tile, each over TN / splits of its columns (so that the few tiles still
+// spread over all the SMs). Each thread takes 4
+// consecutive rows of a column (a 16-byte load per piece), kQ of them, and
+// issues the loads of up to kBatch pieces before adding them, in CTA order
+// (the same order every run). A warp covers 128 rows of one column = 512
+// contiguous bytes of every slot. Columns past the last token (rounded up to
+// 16, the columns the GEMM epilogue wrote) are skipped. vec: C's rows are
+// aligned for one 4-row store (N a multiple of 4, C aligned).
+constexpr int kFixupQ = 2;      // quads per thread
+constexpr int kFixupBatch = 4;  // pieces loaded at once
+template <int TN, class T>
+__global__ void __launch_bounds__(kFixupThreads, 2) split_k_fixup_kernel(const float *__restrict__ part,
+                                                                       T *__restrict__ C, int64_t N,
+                                                                       int64_t M, int64_t mblocks,
+                                                                       int64_t nsb, int64_t units,
+                                                                       int64_t G, int splits, bool vec) {
+    pdl_wait();  // the GEMM's pieces
+    const int64_t tile = blockIdx.x / splits;
+    const int split = (int)(blockIdx.x % splits);
+    const int64_t ca = sk_cta_of(tile * nsb, units, G), cb = sk_cta_of(tile * nsb + nsb - 1, units, G);
+    if (ca == cb) return;  // written whole by its CTA
+    const int64_t n0 = (tile / mblocks) * kTM, m0 = (tile % mblocks) * TN;
+    const int64_t mv = M - m0 < TN ? M - m0 : TN;  // columns holding tokens
+    const int cols = TN / splits, c0 = split * cols;
+    const int cend = (int)((mv + 15) / 16 * 16) < c0 + cols ? (int)((mv + 15) / 16 * 16) : c0 + cols;
+    const int nquads = (cend - c0) * (kTM / 4);
+    for (int e0 = threadIdx.x; e0 < nquads; e0 += kFixupQ * kFixupThreads) {
+        float4 v[kFixupQ];
+        int rr[kFixupQ], cc[kFixupQ];
+        bool live[kFixupQ];
+#pragma unroll
+        for (int h = 0; h < kFixupQ; ++h) {
+            const int e = e0 + h * kFixupThreads;
+            live[h] = e < nquads;
+            rr[h] = (e % (kTM / 4)) * 4;
+            cc[h] = c0 + e / (kTM / 4);
+            v[h] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+        for (int64_t k0 = ca; k0 <= cb; k0 += kFixupBatch) {
+            float4 p[kFixupBatch][kFixupQ];
+#pragma unroll
+            for (int b = 0; b < kFixupBatch; ++b) {
+                if (k0 + b > cb) break;
+                const float *slot = part + sk_slot(k0 + b, tile, units, G, nsb, TN);
+#pragma unroll
+                for (int h = 0; h < kFixupQ; ++h)
+                    if (live[h]) p[b][h] = __ldcg(reinterpret_cast<const float4 *>(slot + cc[h] * kTM + rr[h]));
+            }
+#pragma unroll
+            for (int b = 0; b < kFixupBatch; ++b) {
+                if (k0 + b > cb) break;
+#pragma unroll
+                for (int h = 0; h < kFixupQ; ++h) {
+                    if (!live[h]) continue;
+                    if (k0 + b == ca) {
+                        v[h] = p[b][h];
+                    } else {
+                        v[h].x += p[b][h].x;
+                        v[h].y += p[b][h].y;
+                        v[h].z += p[b][h].z;
+                        v[h].w += p[b][h].w;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < kFixupQ; ++h) {
+            const int64_t m = m0 + cc[h], n = n0 + rr[h];
+            if (live[h] && m < M) {
+                T *y = C + m * N + n;
+                if (vec && n + 3 < N) {
+                    store4(y, v[h]);
+                    continue;
+                }
+                if (n < N) y[0] = out_cast<T>(v[h].x);
+                if (n + 1 < N) y[1] = out_cast<T>(v[h].y);
+                if (n + 2 < N) y[2] = out_cast<T>(v[h].z);
+                if (n + 3 < N) y[3] = out_cast<T>(v[h].w);
+            }
+        }
+    }
+}
 
 }  // namespace
 
@@ -141,9 +228,14 @@ size_t stream_k_part_bytes() { return align_up((size_t)2 * max_grid() * kTM * kS
 template <int TN>
 cudaError_t launch_fixup_tn(const float *part, void *C, bool half_out, int64_t N, int64_t M, int64_t mblocks,
                             int64_t nsb, int64_t units, int64_t G, cudaStream_t s) {
-    const int64_t nblocks = (N + kTM - 1) / kTM;
+    const int64_t nblocks = (N + kTM - 1) / kTM, tiles = nblocks * mblocks;
+    // CTAs per tile: enough for about two per SM over all tiles, a power of
+    // two up to one per 32 columns
+    const bool split_k = tiles < G;  // else stream-K: one CTA per tile
+    int splits = 1;
+    while (split_k && splits < TN / 32 && tiles * splits < 2 * (int64_t)sm_count()) splits *= 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(nblocks * mblocks));
+    cfg.gridDim = dim3((unsigned)(tiles * splits));
     cfg.blockDim = dim3(kFixupThreads);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -151,11 +243,16 @@ cudaError_t launch_fixup_tn(const float *part, void *C, bool half_out, int64_t N
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (half_out)
-        return cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<TN, __half>, part, static_cast<__half *>(C), N, M,
-                                  mblocks, nsb, units, G, N % 4 == 0 && (uintptr_t)C % 8 == 0);
-    return cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<TN, float>, part, static_cast<float *>(C), N, M, mblocks,
-                              nsb, units, G, N % 4 == 0 && (uintptr_t)C % 16 == 0);
+    const bool vh = N % 4 == 0 && (uintptr_t)C % 8 == 0, vf = N % 4 == 0 && (uintptr_t)C % 16 == 0;
+    if (!split_k)
+        return half_out ? cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<TN, __half>, part, static_cast<__half *>(C),
+                                             N, M, mblocks, nsb, units, G, vh)
+                        : cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<TN, float>, part, static_cast<float *>(C),
+                                             N, M, mblocks, nsb, units, G, vf);
+    return half_out ? cudaLaunchKernelEx(&cfg, split_k_fixup_kernel<TN, __half>, part, static_cast<__half *>(C), N,
+                                         M, mblocks, nsb, units, G, splits, vh)
+                    : cudaLaunchKernelEx(&cfg, split_k_fixup_kernel<TN, float>, part, static_cast<float *>(C), N, M,
+                                         mblocks, nsb, units, G, splits, vf);
 }
 
 cudaError_t launch_stream_k_fixup(const float *part, void *C, bool half_out, int cols, int64_t N, int64_t M,
