@@ -36,100 +36,22 @@ __device__ __forceinline__ void store4(__half *y, float4 v) {
                                                *reinterpret_cast<const uint32_t *>(&hi));
 }
 
-// The pieces of one split tile, added in CTA order and stored (stream-K
-// grids). Each thread
-// takes 4 consecutive rows of a column (one 16-byte load per piece) and keeps
-// 4 columns in flight; a warp covers 128 rows of one column = 512 contiguous
-// bytes of every slot. kFull: all TN columns hold tokens (the bound is a
-// constant); otherwise the first nq quads only (the columns the GEMM
-// epilogue wrote, tokens < M rounded up to 16). vec: C's rows are aligned
-// for one 4-row store (N a multiple of 4, C aligned).
-template <int TN, bool kFull, class T>
-__device__ __forceinline__ void fixup_tile(const float *__restrict__ part, T *__restrict__ C, int64_t N,
-                                           int64_t M, int64_t tile, int64_t n0, int64_t m0, int nq,
-                                           int64_t ca, int64_t cb, int64_t nsb, int64_t units, int64_t G,
-                                           bool vec) {
-    constexpr int kQuads = kTM * TN / 4;
-    const int nquads = kFull ? kQuads : nq;
-    for (int e0 = threadIdx.x; e0 < nquads; e0 += 4 * kFixupThreads) {
-        float4 v[4];
-        int rr[4], cc[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const int e = e0 + h * kFixupThreads;  // kQuads is a multiple of 4 * kFixupThreads
-            rr[h] = (e % (kTM / 4)) * 4;
-            cc[h] = (kFull || e < nquads) ? e / (kTM / 4) : TN;  // TN: not written, skipped
-        }
-        for (int64_t k = ca; k <= cb; ++k) {
-            const float *slot = part + sk_slot(k, tile, units, G, nsb, TN);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                if (!kFull && cc[h] >= TN) continue;
-                const float4 p = __ldcg(reinterpret_cast<const float4 *>(slot + cc[h] * kTM + rr[h]));
-                if (k == ca) {
-                    v[h] = p;
-                } else {
-                    v[h].x += p.x;
-                    v[h].y += p.y;
-                    v[h].z += p.z;
-                    v[h].w += p.w;
-                }
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const int64_t m = m0 + cc[h], n = n0 + rr[h];
-            if ((kFull || cc[h] < TN) && m < M) {
-                T *y = C + m * N + n;
-                if (vec && n + 3 < N) {
-                    store4(y, v[h]);
-                    continue;
-                }
-                if (n < N) y[0] = out_cast<T>(v[h].x);
-                if (n + 1 < N) y[1] = out_cast<T>(v[h].y);
-                if (n + 2 < N) y[2] = out_cast<T>(v[h].z);
-                if (n + 3 < N) y[3] = out_cast<T>(v[h].w);
-            }
-        }
-    }
-}
-
-// Stream-K grids (more tiles than SMs, a tile in two or three pieces): one
-// CTA per tile (whole tiles return at once).
-template <int TN, class T>
-__global__ void __launch_bounds__(kFixupThreads) stream_k_fixup_kernel(const float *__restrict__ part,
-                                                                       T *__restrict__ C, int64_t N,
-                                                                       int64_t M, int64_t mblocks,
-                                                                       int64_t nsb, int64_t units,
-                                                                       int64_t G, bool vec) {
-    pdl_wait();  // the GEMM's pieces
-    const int64_t tile = blockIdx.x;
-    const int64_t ca = sk_cta_of(tile * nsb, units, G), cb = sk_cta_of(tile * nsb + nsb - 1, units, G);
-    if (ca == cb) return;  // written whole by its CTA
-    const int64_t n0 = (tile / mblocks) * kTM, m0 = (tile % mblocks) * TN;
-    const int64_t mv = M - m0 < TN ? M - m0 : TN;  // columns holding tokens
-    if (mv == TN)
-        fixup_tile<TN, true>(part, C, N, M, tile, n0, m0, 0, ca, cb, nsb, units, G, vec);
-    else
-        fixup_tile<TN, false>(part, C, N, M, tile, n0, m0, (int)((mv + 15) / 16 * 16) * (kTM / 4), ca, cb, nsb,
-                              units, G, vec);
-}
-static_assert((kTM * 128 / 4) % (4 * kFixupThreads) == 0, "fixup tiling");
-
-// Split-K grids (fewer tiles than half the SMs, each tile in many pieces):
-// the pieces of one tile added in CTA order and stored by `splits` CTAs per
-// tile, each over TN / splits of its columns (so that the few tiles still
-// spread over all the SMs). Each thread takes 4
+// The pieces of one split tile added in CTA order and stored, by `splits`
+// CTAs per tile, each over TN / splits of its columns: for split-K grids
+// (fewer tiles than half the SMs, each tile in many pieces) enough CTAs for
+// about two per SM, so that the few tiles still spread over all the SMs; for
+// stream-K grids (a tile in two or three pieces) one CTA per tile. Each thread takes 4
 // consecutive rows of a column (a 16-byte load per piece), kQ of them, and
 // issues the loads of up to kBatch pieces before adding them, in CTA order
 // (the same order every run). A warp covers 128 rows of one column = 512
 // contiguous bytes of every slot. Columns past the last token (rounded up to
 // 16, the columns the GEMM epilogue wrote) are skipped. vec: C's rows are
 // aligned for one 4-row store (N a multiple of 4, C aligned).
-constexpr int kFixupQ = 2;      // quads per thread
-constexpr int kFixupBatch = 4;  // pieces loaded at once
-template <int TN, class T>
-__global__ void __launch_bounds__(kFixupThreads, 2) split_k_fixup_kernel(const float *__restrict__ part,
+// kFixupQ quads per thread, kFixupBatch pieces loaded at once: 2 x 4 for
+// split-K (many pieces, two CTAs per SM), 4 x 2 for stream-K (two or three
+// pieces, one CTA per tile: eight loads in flight per thread).
+template <int TN, class T, int kFixupQ, int kFixupBatch>
+__global__ void __launch_bounds__(kFixupThreads, kFixupQ == 2 ? 2 : 1) fixup_kernel(const float *__restrict__ part,
                                                                        T *__restrict__ C, int64_t N,
                                                                        int64_t M, int64_t mblocks,
                                                                        int64_t nsb, int64_t units,
@@ -231,7 +153,7 @@ cudaError_t launch_fixup_tn(const float *part, void *C, bool half_out, int64_t N
     const int64_t nblocks = (N + kTM - 1) / kTM, tiles = nblocks * mblocks;
     // CTAs per tile: enough for about two per SM over all tiles, a power of
     // two up to one per 32 columns
-    const bool split_k = tiles < G;  // else stream-K: one CTA per tile
+    const bool split_k = tiles < G;  // else stream-K: one CTA per tile, four quads per thread
     int splits = 1;
     while (split_k && splits < TN / 32 && tiles * splits < 2 * (int64_t)sm_count()) splits *= 2;
     cudaLaunchConfig_t cfg = {};
@@ -245,14 +167,14 @@ cudaError_t launch_fixup_tn(const float *part, void *C, bool half_out, int64_t N
     cfg.numAttrs = 1;
     const bool vh = N % 4 == 0 && (uintptr_t)C % 8 == 0, vf = N % 4 == 0 && (uintptr_t)C % 16 == 0;
     if (!split_k)
-        return half_out ? cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<TN, __half>, part, static_cast<__half *>(C),
-                                             N, M, mblocks, nsb, units, G, vh)
-                        : cudaLaunchKernelEx(&cfg, stream_k_fixup_kernel<TN, float>, part, static_cast<float *>(C),
-                                             N, M, mblocks, nsb, units, G, vf);
-    return half_out ? cudaLaunchKernelEx(&cfg, split_k_fixup_kernel<TN, __half>, part, static_cast<__half *>(C), N,
-                                         M, mblocks, nsb, units, G, splits, vh)
-                    : cudaLaunchKernelEx(&cfg, split_k_fixup_kernel<TN, float>, part, static_cast<float *>(C), N, M,
-                                         mblocks, nsb, units, G, splits, vf);
+        return half_out ? cudaLaunchKernelEx(&cfg, fixup_kernel<TN, __half, 4, 2>, part,
+                                             static_cast<__half *>(C), N, M, mblocks, nsb, units, G, 1, vh)
+                        : cudaLaunchKernelEx(&cfg, fixup_kernel<TN, float, 4, 2>, part,
+                                             static_cast<float *>(C), N, M, mblocks, nsb, units, G, 1, vf);
+    return half_out ? cudaLaunchKernelEx(&cfg, fixup_kernel<TN, __half, 2, 4>, part, static_cast<__half *>(C),
+                                         N, M, mblocks, nsb, units, G, splits, vh)
+                    : cudaLaunchKernelEx(&cfg, fixup_kernel<TN, float, 2, 4>, part, static_cast<float *>(C), N,
+                                         M, mblocks, nsb, units, G, splits, vf);
 }
 
 cudaError_t launch_stream_k_fixup(const float *part, void *C, bool half_out, int cols, int64_t N, int64_t M,
