@@ -116,6 +116,35 @@ def test_w4a16_full_size_sampled(q, orc, M):
     check(c[:, rows], ref["c64"], ref["den"], f"8192x8192 M={M}")
 
 
+@pytest.mark.parametrize("N,K,G,M", [(48, 1024, 128, 1), (100, 512, 128, 5), (40, 2304, 128, 9),
+                                     (64, 4096, 128, 4), (64, 256, 128, 40), (1000, 4096, 128, 300)])
+def test_w4a16_degenerate_weights(q, orc, N, K, G, M):
+    """The method's degenerate weights on every path (decode with staged and
+    in-place activations, K-major decode, GEMM, stream-K GEMM): q = z
+    everywhere (w = 0, so C must be exactly 0: no residue of the zero-point
+    arithmetic), then one nonzero weight per row at a row-dependent position
+    (C[m, n] = s d A[m, k_n]: a misplaced code, scale, zero or activation
+    element lands in the wrong output or multiplies the wrong A)."""
+    _, s16, z, A16 = wl.w4a16_inputs(46, N, K, G, M)
+    zk = z.repeat_interleave(G, dim=1).numpy()  # [N, K]: every code equal to its group's zero
+    s_d, z_d, A_d = s16.cuda(), z.cuda(), A16.cuda()
+    Wz = packed_from_canon(q, torch.from_numpy(orc.w4a16_pack(zk).view(np.int32)).cuda(), N, K)
+    c = run(q, Wz, s_d, z_d, G, A_d, M, N, K)
+    assert np.all(c == 0), f"w = 0 gave {np.count_nonzero(c)} nonzero outputs"
+    n = np.arange(N)
+    k = (n * 7919 + 13) % K
+    one = zk.copy()
+    one[n, k] = (zk[n, k] + 1 + n % 15) % 16  # q - z != 0 (mod 16), varied per row
+    qweight = orc.w4a16_pack(one)
+    Wp = packed_from_canon(q, torch.from_numpy(qweight.view(np.int32)).cuda(), N, K)
+    c = run(q, Wp, s_d, z_d, G, A_d, M, N, K)
+    ref = orc.w4a16_matmul(qweight, s16.view(torch.int16).numpy().view(np.uint16), z.numpy(), G,
+                           A16.view(torch.int16).numpy().view(np.uint16),
+                           nthreads=orc.default_threads())
+    assert np.all(ref["den"] > 0)
+    check(c, ref["c64"], ref["den"], f"one-hot N={N} K={K} G={G} M={M}")
+
+
 def test_w4a16_errors(q):
     N, K, G, M = 16, 256, 128, 2
     Wp = torch.zeros(N * K // 2, dtype=torch.uint8, device="cuda")
