@@ -61,6 +61,11 @@ __global__ void __launch_bounds__(kFixupThreads, kFixupQ == 2 ? 2 : 1) fixup_ker
     const int split = (int)(blockIdx.x % splits);
     const int64_t ca = sk_cta_of(tile * nsb, units, G), cb = sk_cta_of(tile * nsb + nsb - 1, units, G);
     if (ca == cb) return;  // written whole by its CTA
+    // Slots of the pieces, without a division per piece: every CTA after ca
+    // starts inside the tile (its first tile: slot 0); ca's piece is in slot 0
+    // only when ca's range starts at the tile, else in slot 1 (its last tile).
+    const int64_t sbytes = (int64_t)kTM * TN;
+    const int64_t slot_ca = (ca * 2 + (ca * units / G < tile * nsb ? 1 : 0)) * sbytes;
     const int64_t n0 = (tile / mblocks) * kTM, m0 = (tile % mblocks) * TN;
     const int64_t mv = M - m0 < TN ? M - m0 : TN;  // columns holding tokens
     const int cols = TN / splits, c0 = split * cols;
@@ -83,7 +88,7 @@ __global__ void __launch_bounds__(kFixupThreads, kFixupQ == 2 ? 2 : 1) fixup_ker
 #pragma unroll
             for (int b = 0; b < kFixupBatch; ++b) {
                 if (k0 + b > cb) break;
-                const float *slot = part + sk_slot(k0 + b, tile, units, G, nsb, TN);
+                const float *slot = part + (k0 + b == ca ? slot_ca : (k0 + b) * 2 * sbytes);
 #pragma unroll
                 for (int h = 0; h < kFixupQ; ++h)
                     if (live[h]) p[b][h] = __ldcg(reinterpret_cast<const float4 *>(slot + cc[h] * kTM + rr[h]));
