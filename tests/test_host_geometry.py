@@ -42,6 +42,14 @@ int main() {
             CHECK(used.insert(s0).second);
             if (t1 != t0) CHECK(used.insert(s1).second);
         }
+        // the fixup's shortcut: of a split tile's pieces only the first CTA's
+        // can sit in slot 1 (the tile is that CTA's last), and only when the
+        // CTA's range starts before the tile; every later CTA starts inside it
+        for (int64_t t = 0; t < U / nsb; ++t) {
+            const int64_t ca = sk_cta_of(t * nsb, U, G), cb = sk_cta_of(t * nsb + nsb - 1, U, G);
+            for (int64_t c = ca; c <= cb && ca != cb; ++c)
+                CHECK(sk_slot(c, t, U, G, nsb, 128) == (c * 2 + (c == ca && ca * U / G < t * nsb ? 1 : 0)) * 16384);
+        }
     }
     // Q6_K lanes: (t, hi, i) covers the 256 elements once; the high-bit
     // positions of a lane word are 16 distinct bit pairs
